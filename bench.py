@@ -1,0 +1,343 @@
+#!/usr/bin/env python3
+"""Benchmark of the KDA forward (chunked WY prefill) and the KDA decode step on GB300.
+
+One step = one chunked forward over the prefill workload (B8 H32 T4096 K=V=128,
+chunk 64, bf16 I/O, fp32 state) through the C ABI: gate, intra-chunk WY,
+inter-chunk carry and output.  After the timed prefill steps the decode
+workload (B256 H32 K=V=128, fp32 state 512 MiB updated in place) is timed for
+64 consecutive single-token steps and reported in the same JSON line under
+"decode".
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+Under torchrun (N > 1) every rank runs the whole workload on its own GPU (weak
+scaling, no data-path collective); rank 0 prints one JSON line.
+
+--impl reference times the f64 CPU oracle (the token-by-token recurrence) on the
+host cores, on a bounded sample of the same workload per step.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "KDA fwd tokens/s & TFLOP/s (% bf16 peak); decode state GB/s (% HBM)"
+WORKLOAD = "prefill_bf16"
+# Algorithmic work per token-head of the chunked forward (C = 64, K = V = 128):
+#   FLOPs 6KV + 3CK + 2CV + C^2/3 (triangular counts) and the essential HBM bytes:
+#   q, k, v, z read and o written in bf16 (5 x 256 B) plus beta (2 B).
+def flops_per_token_head(C, K, V):
+    return 6 * K * V + 3 * C * K + 2 * C * V + C * C / 3.0
+
+
+def bytes_per_token_head(K, V, io_bytes=2):
+    return io_bytes * (3 * K + V) + io_bytes * V + io_bytes
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as fh:
+            d = json.load(fh)
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained"), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"], stdout=self.fh,
+                stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        rows = []
+        with open(self.path) as fh:
+            for ln in fh:
+                parts = [p.strip() for p in ln.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = sorted(float(r[1]) for r in rows if r[1].replace(".", "").isdigit())
+        mx = max(float(r[2]) for r in rows if r[2].replace(".", "").isdigit())
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i] == "Active"})
+        return {"sm_mhz": sm[len(sm) // 2] if sm else None, "sm_max_mhz": mx,
+                "reasons": reasons, "samples": len(rows)}
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def timed(fn, steps, stream, events=True):
+    import torch
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    start.record(stream)
+    for _ in range(steps):
+        fn()
+    end.record(stream)
+    torch.cuda.synchronize()
+    return start.elapsed_time(end) / 1e3
+
+
+def oracle_sample(inp, n_pairs, threads, T=None):
+    """Run the f64 oracle on n_pairs (b, h) sequences of the workload; returns (seconds, tokens)."""
+    import oracle
+    T = T or inp.T
+    pairs = [(i % inp.B, (i * 7) % inp.H) for i in range(n_pairs)]
+    bs = [p[0] for p in pairs]
+    hs = [p[1] for p in pairs]
+    g = lambda t: t[bs, hs, :T].unsqueeze(0)
+    h0 = None if inp.h0 is None else inp.h0[bs, hs].unsqueeze(0)
+    args = (g(inp.q), g(inp.k), g(inp.v), g(inp.z), inp.beta[bs, hs, :T].unsqueeze(0),
+            inp.A_log[hs], inp.dt_bias[hs])
+    args = tuple(oracle.f64(a) for a in args)
+    t0 = time.perf_counter()
+    oracle.forward(*args, inp.scale, h0, threads=threads)
+    dt = time.perf_counter() - t0
+    # tokens of the workload's unit: one token-head sequence of T tokens is T / H "tokens"
+    return dt, n_pairs * T / inp.H
+
+
+def cpu_baseline(inp, budget_s=12.0):
+    """Oracle as it stands, on the host cores, on a bounded sample; tokens/s (B*T tokens)."""
+    threads = os.cpu_count() or 1
+    # calibrate: one thread, one (b, h) sequence of 256 tokens
+    dt, _ = oracle_sample(inp, 1, 1, T=256)
+    sec_per_token = dt / 256
+    T = inp.T
+    rounds = max(1, int(budget_s / max(sec_per_token * T, 1e-9)))
+    n = threads * rounds
+    dt, tokens = oracle_sample(inp, n, threads, T=T)
+    return {"value": tokens / dt, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+            "sample": f"{n} (b,h) sequences x T={T} of the {WORKLOAD} workload "
+                      f"({n * T} token-heads, {dt:.1f} s); tokens = token-heads / H"}
+
+
+def run_reference(args):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    from gated_delta_rule_26_gb300 import inputs
+    inp = inputs.workload(WORKLOAD)
+    threads = os.cpu_count() or 1
+    # one step = a bounded sample: `threads` (b, h) sequences of 1024 tokens
+    T = 1024
+    for _ in range(args.warmup):
+        oracle_sample(inp, threads, threads, T=T)
+    tot_s, tot_tok = 0.0, 0.0
+    for _ in range(args.steps):
+        dt, tok = oracle_sample(inp, threads, threads, T=T)
+        tot_s += dt
+        tot_tok += tok
+    value = tot_tok / tot_s
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * tot_s / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": f"{WORKLOAD} B8 H32 T4096 K=V=128 chunk 64 (sampled)"},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads,
+                             "kind": "oracle",
+                             "sample": f"per step {threads} (b,h) sequences x T={T}"},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--decode-steps", type=int, default=64)
+    args = ap.parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+
+    import torch
+    ws, rank, local = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    from gated_delta_rule_26_gb300 import build as kbuild
+    kbuild.build()
+    from gated_delta_rule_26_gb300 import inputs, kda
+
+    def barrier():
+        if ws > 1:
+            torch.distributed.barrier()
+
+    peaks = load_peaks()
+    inp_cpu = inputs.workload(WORKLOAD)
+    B, H, T, K, V, C = inp_cpu.B, inp_cpu.H, inp_cpu.T, inp_cpu.K, inp_cpu.V, inp_cpu.chunk
+    d = inp_cpu.to("cuda")
+    stream = torch.cuda.current_stream()
+    out = torch.empty(B, H, T, V, device="cuda", dtype=torch.bfloat16)
+    hT = torch.empty(B, H, K, V, device="cuda", dtype=torch.float32)
+
+    def step():
+        kda.chunk_forward(d.q, d.k, d.v, d.z, d.beta, d.A_log, d.dt_bias, inp_cpu.scale, d.h0, C,
+                          out=out, hT=hT)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(torch.cuda.current_device())
+    sampler.start()
+    time.sleep(0.3)
+    barrier()
+    n0 = kda.launch_count()
+    secs = timed(step, args.steps, stream)
+    launches = kda.launch_count() - n0
+    clocks = sampler.stop()
+    barrier()
+    if ws > 1:
+        t = torch.tensor([secs], device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        secs = float(t.item())
+    per_step = secs / args.steps
+    tokens = B * T
+    token_heads = B * H * T
+    value = ws * tokens / per_step
+    flops = token_heads * flops_per_token_head(C, K, V)
+    alg_bytes = token_heads * bytes_per_token_head(K, V) + B * H * K * V * 4 * (
+        2 if inp_cpu.h0 is not None else 1)
+    kernels_per_step = launches / args.steps
+    # Dominant kernel: the chunked forward launches `kernels_per_step` kernels per step; with one
+    # kernel the step time is that kernel's time.
+    achieved_gbs = alg_bytes / per_step / 1e9
+    roofline = {"bound": "hbm", "achieved": achieved_gbs, "peak": peaks["hbm_gbs"],
+                "unit": "GB/s", "frac": achieved_gbs / peaks["hbm_gbs"], "traffic": None,
+                "kernel": "kda chunked forward", "kernels_per_step": kernels_per_step,
+                "peak_source": peaks["source"]}
+    tflops = flops / per_step / 1e12
+
+    # ---- end to end through the public API: pinned host inputs -> device -> forward -> host
+    host = {n: getattr(inp_cpu, n).pin_memory() for n in ("q", "k", "v", "z", "beta", "A_log",
+                                                         "dt_bias")}
+    dev = {n: torch.empty_like(t, device="cuda") for n, t in host.items()}
+    out_h = torch.empty(B, H, T, V, dtype=torch.bfloat16).pin_memory()
+    hT_h = torch.empty(B, H, K, V, dtype=torch.float32).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = out_h.numel() * out_h.element_size() + hT_h.numel() * hT_h.element_size()
+
+    def e2e_step():
+        for n, t in host.items():
+            dev[n].copy_(t, non_blocking=True)
+        kda.chunk_forward(dev["q"], dev["k"], dev["v"], dev["z"], dev["beta"], dev["A_log"],
+                          dev["dt_bias"], inp_cpu.scale, None, C, out=out, hT=hT)
+        out_h.copy_(out, non_blocking=True)
+        hT_h.copy_(hT, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    e2e_steps = max(3, min(args.steps, 10))
+    barrier()
+    e2e_secs = timed(e2e_step, e2e_steps, stream)
+    if ws > 1:
+        t = torch.tensor([e2e_secs], device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_secs = float(t.item())
+    e2e = {"value": ws * tokens / (e2e_secs / e2e_steps), "unit": "tokens/s",
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+    del host, dev, out_h, hT_h
+
+    # ---- decode: 64 consecutive in-place steps on the 512 MiB fp32 state
+    dec = inputs.decode(steps=args.decode_steps)
+    dq, dk, dv, dz, db = (t.cuda() for t in (dec.q, dec.k, dec.v, dec.z, dec.beta))
+    dA, ddt = dec.A_log.cuda(), dec.dt_bias.cuda()
+    state = dec.state.cuda()
+    dout = torch.empty(dec.B, dec.H, 1, dec.V, device="cuda", dtype=torch.bfloat16)
+    it = [0]
+
+    def dstep():
+        s = it[0] % dec.steps
+        kda.recurrent_step(dq[s], dk[s], dv[s], dz[s], db[s], dA, ddt, state, dec.scale, out=dout)
+        it[0] += 1
+
+    for _ in range(3):
+        dstep()
+    barrier()
+    dsecs = timed(dstep, dec.steps, stream)
+    dper = dsecs / dec.steps
+    dbytes = 2 * dec.B * dec.H * dec.K * dec.V * 4 + dec.B * dec.H * (3 * dec.K + 2 * dec.V + 1) * 2
+    decode = {"value": ws * dec.B / dper, "unit": "tokens/s", "us_per_step": dper * 1e6,
+              "state_GBps": dbytes / dper / 1e9,
+              "roofline": {"bound": "hbm", "achieved": dbytes / dper / 1e9,
+                           "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                           "frac": dbytes / dper / 1e9 / peaks["hbm_gbs"], "traffic": None},
+              "config": {"workload": "decode_bf16 B256 H32 K=V=128, 64 consecutive steps",
+                         "bytes_per_step": dbytes}}
+
+    line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws,
+            "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": per_step * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": f"{WORKLOAD} B{B} H{H} T{T} K={K} V={V} chunk {C}",
+                       "B": B, "H": H, "T": T, "K": K, "V": V, "chunk": C,
+                       "state": "fp32", "h0": "zero",
+                       "l2": "inputs larger than L2 (%.2f GB per step)" % (alg_bytes / 1e9),
+                       "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU"},
+            "tflops": tflops, "tflops_frac_bf16_burst": tflops / peaks["bf16_tflops"],
+            "tflops_convention": "algorithmic (triangular) FLOPs 6KV+3CK+2CV+C^2/3 per token-head",
+            "roofline": roofline, "e2e": e2e, "clocks": clocks, "gpu_launches": launches,
+            "decode": decode}
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(inp_cpu)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

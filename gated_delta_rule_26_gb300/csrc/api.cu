@@ -1,0 +1,120 @@
+// api.cu -- the extern "C" entry points of libkda: argument validation on the
+// host, path selection, launch.  No exception crosses this boundary and
+// nothing is launched when an argument is rejected.
+#include <stdint.h>
+
+#include <atomic>
+
+#include "common.cuh"
+
+namespace kda {
+cudaError_t launch_chunk_tc(const ChunkArgs& a, cudaStream_t s, bool* taken);
+}
+
+namespace kda {
+static std::atomic<unsigned long long> g_launches{0};
+void count_launches(int n) { g_launches.fetch_add((unsigned long long)n, std::memory_order_relaxed); }
+}  // namespace kda
+
+namespace {
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool dim_ok(int x) { return x >= 8 && x <= 128 && (x % 8) == 0; }
+
+int check_dims(const kda_dims* d, bool need_v) {
+    if (!d) return KDA_ERR_INVALID_ARG;
+    if (d->B < 1 || d->H < 1 || d->T < 0 || d->K < 1 || (need_v && d->V < 1))
+        return KDA_ERR_INVALID_ARG;
+    if (!dim_ok(d->K) || (need_v && !dim_ok(d->V))) return KDA_ERR_UNSUPPORTED;
+    if ((long long)d->B * d->H > 0x7fffffffLL) return KDA_ERR_UNSUPPORTED;
+    return KDA_OK;
+}
+
+bool dtype_ok(int dt) { return dt == KDA_F32 || dt == KDA_BF16; }
+
+int check_ptrs(std::initializer_list<const void*> required,
+               std::initializer_list<const void*> optional) {
+    for (const void* p : required)
+        if (!p) return KDA_ERR_INVALID_ARG;
+    for (const void* p : required)
+        if (!aligned16(p)) return KDA_ERR_MISALIGNED;
+    for (const void* p : optional)
+        if (p && !aligned16(p)) return KDA_ERR_MISALIGNED;
+    return KDA_OK;
+}
+
+int from_cuda(cudaError_t e) { return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA; }
+
+}  // namespace
+
+extern "C" {
+
+unsigned long long kda_launch_count(void) { return kda::g_launches.load(std::memory_order_relaxed); }
+
+const char* kda_status_string(int status) {
+    switch (status) {
+        case KDA_OK: return "ok";
+        case KDA_ERR_INVALID_ARG: return "invalid argument";
+        case KDA_ERR_UNSUPPORTED: return "unsupported size or chunk";
+        case KDA_ERR_MISALIGNED: return "pointer not 16-byte aligned";
+        case KDA_ERR_CUDA: return "CUDA error";
+        case KDA_ERR_NO_MEMORY: return "out of device memory";
+        default: return "unknown status";
+    }
+}
+
+int kda_gate(const kda_dims* dims, kda_dtype z_dtype, const void* z, const float* A_log,
+             const float* dt_bias, int chunk, float* g_out, kda_stream_t stream) {
+    int st = check_dims(dims, false);
+    if (st) return st;
+    if (!dtype_ok(z_dtype)) return KDA_ERR_INVALID_ARG;
+    if (chunk != 0 && chunk != 16 && chunk != 32 && chunk != 64) return KDA_ERR_UNSUPPORTED;
+    const int span = chunk > 0 ? chunk : 64;
+    if ((dims->T + span - 1) / span > 65535) return KDA_ERR_UNSUPPORTED;
+    if (dims->T == 0) return KDA_OK;
+    st = check_ptrs({z, A_log, dt_bias, g_out}, {});
+    if (st) return st;
+    return from_cuda(kda::launch_gate(dims->B, dims->H, dims->T, dims->K, z_dtype, z, A_log,
+                                      dt_bias, chunk, g_out, (cudaStream_t)stream));
+}
+
+int kda_chunk_forward(const kda_dims* dims, kda_dtype io_dtype, const void* q, const void* k,
+                      const void* v, const void* z, const void* beta, const float* A_log,
+                      const float* dt_bias, float scale, const float* h0, int chunk, void* out,
+                      float* hT, kda_stream_t stream) {
+    int st = check_dims(dims, true);
+    if (st) return st;
+    if (!dtype_ok(io_dtype)) return KDA_ERR_INVALID_ARG;
+    if (chunk != 16 && chunk != 32 && chunk != 64) return KDA_ERR_UNSUPPORTED;
+    if (dims->T > 0) {
+        st = check_ptrs({q, k, v, z, beta, A_log, dt_bias, out}, {h0, hT});
+    } else {
+        st = check_ptrs({}, {h0, hT});
+    }
+    if (st) return st;
+    if (dims->T == 0 && !hT) return KDA_OK;
+    kda::ChunkArgs a{dims->B, dims->H, dims->T, dims->K, dims->V, chunk, io_dtype, q, k, v, z,
+                     beta, A_log, dt_bias, h0, scale, out, hT};
+    bool taken = false;
+    cudaError_t e = kda::launch_chunk_tc(a, (cudaStream_t)stream, &taken);
+    if (taken) return e == cudaErrorMemoryAllocation ? KDA_ERR_NO_MEMORY : from_cuda(e);
+    return from_cuda(kda::launch_chunk_simt(a, (cudaStream_t)stream));
+}
+
+int kda_recurrent_step(const kda_dims* dims, kda_dtype io_dtype, const void* q, const void* k,
+                       const void* v, const void* z, const void* beta, const float* A_log,
+                       const float* dt_bias, float scale, float* state, void* out,
+                       kda_stream_t stream) {
+    int st = check_dims(dims, true);
+    if (st) return st;
+    if (!dtype_ok(io_dtype)) return KDA_ERR_INVALID_ARG;
+    if (dims->T != 1) return KDA_ERR_INVALID_ARG;
+    st = check_ptrs({q, k, v, z, beta, A_log, dt_bias, state, out}, {});
+    if (st) return st;
+    kda::StepArgs a{dims->B, dims->H, dims->K, dims->V, io_dtype, q, k, v, z, beta,
+                    A_log, dt_bias, scale, state, out};
+    return from_cuda(kda::launch_decode(a, (cudaStream_t)stream));
+}
+
+}  // extern "C"

@@ -1,0 +1,60 @@
+// common.cuh -- small device helpers shared by the libkda kernels.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "kda.h"
+
+namespace kda {
+
+// I/O element loads and stores for the two supported dtypes.
+__device__ __forceinline__ float ld_io(const float* p) { return *p; }
+__device__ __forceinline__ float ld_io(const __nv_bfloat16* p) { return __bfloat162float(*p); }
+__device__ __forceinline__ void st_io(float* p, float x) { *p = x; }
+__device__ __forceinline__ void st_io(__nv_bfloat16* p, float x) { *p = __float2bfloat16_rn(x); }
+
+// softplus(x) = log(1 + e^x) = max(x, 0) + log1p(e^{-|x|}); neither term overflows.
+__device__ __forceinline__ float softplus_f32(float x) {
+    return fmaxf(x, 0.0f) + log1pf(expf(-fabsf(x)));
+}
+
+// The KDA decay gate, log domain: g = -exp(A_log) * softplus(z + dt_bias) <= 0
+// (kdafix-2026-10-02, "Fix 1": softplus first, then the -exp(A_log) multiplier).
+__device__ __forceinline__ float kda_log_decay(float z, float dt_bias, float exp_A) {
+    return -(exp_A * softplus_f32(z + dt_bias));
+}
+
+// Launch-side argument bundle used by the internal launchers.
+struct ChunkArgs {
+    int B, H, T, K, V, chunk;
+    kda_dtype io;
+    const void *q, *k, *v, *z, *beta;
+    const float *A_log, *dt_bias, *h0;
+    float scale;
+    void* out;
+    float* hT;
+};
+
+struct StepArgs {
+    int B, H, K, V;
+    kda_dtype io;
+    const void *q, *k, *v, *z, *beta;
+    const float *A_log, *dt_bias;
+    float scale;
+    float* state;
+    void* out;
+};
+
+// Count `n` kernel launches (read through kda_launch_count()).
+void count_launches(int n);
+
+// Internal launchers (one per kernel family); each returns a cudaError_t from the launch.
+cudaError_t launch_gate(int B, int H, int T, int K, kda_dtype zdt, const void* z,
+                        const float* A_log, const float* dt_bias, int chunk, float* g,
+                        cudaStream_t s);
+cudaError_t launch_decode(const StepArgs& a, cudaStream_t s);
+cudaError_t launch_chunk_simt(const ChunkArgs& a, cudaStream_t s);
+
+}  // namespace kda

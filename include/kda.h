@@ -1,0 +1,116 @@
+/*
+ * kda.h -- C ABI of libkda, the GB300 (sm_103a) Kimi Delta Attention forward.
+ *
+ * The method (kdafix-2026-10-02, "Fix 1 -- decay form" and "Fix 2 -- read
+ * scale"): per (batch b, head h) a state S of shape K x V; per token t and key
+ * channel c the log decay
+ *
+ *     g[t,c] = -exp(A_log[h]) * softplus(z[t,c] + dt_bias[h,c]),   alpha = exp(g),
+ *
+ * and the step
+ *
+ *     S <- diag(alpha_t) S;   u = v_t - S^T k_t;   S <- S + beta_t k_t u^T;
+ *     o_t = S^T (scale * q_t).
+ *
+ * The scale (default K**-0.5) is folded into q: it enters the read only and
+ * never the state.  kda_chunk_forward computes the same function chunk-parallel
+ * in WY form; its inter-chunk carry uses exp(G_last - G) with G the in-chunk
+ * cumulative log decay (kda-adjoint-2026-10-01, section 2).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - All tensor pointers are DEVICE pointers to contiguous, head-major arrays:
+ *       q, k, z   : (B, H, T, K)        v, out : (B, H, T, V)
+ *       beta      : (B, H, T)           A_log  : (H)          dt_bias : (H, K)
+ *       h0, hT, state : (B, H, K, V)    float32 always
+ *   q, k, v, z, beta and out have the I/O dtype (KDA_F32 or KDA_BF16);
+ *   A_log, dt_bias and the state are float32.
+ * - Every pointer must be 16-byte aligned, else KDA_ERR_MISALIGNED.
+ * - The caller owns every buffer.  The library keeps no state between calls
+ *   except the CUDA resources the runtime itself caches; it is re-entrant.
+ *   Scratch memory, where a path needs it, is taken with cudaMallocAsync on the
+ *   caller's stream and released on the same stream before the call returns.
+ * - Work is enqueued on `stream` (NULL = the legacy default stream); calls
+ *   return as soon as it is enqueued.  Argument errors are detected on the host
+ *   before anything is launched; a launch error is reported as KDA_ERR_CUDA;
+ *   errors during execution surface at the caller's next synchronisation.
+ *   No C++ exception crosses this boundary.
+ * - Supported sizes: B, H >= 1; T >= 0 (T = 0 is a no-op apart from hT = h0);
+ *   K and V multiples of 8 in [8, 128]; chunk in {16, 32, 64}.  Anything else
+ *   returns KDA_ERR_UNSUPPORTED.  T need not be a multiple of chunk.
+ */
+#ifndef KDA_H_
+#define KDA_H_
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st;
+typedef struct CUstream_st* kda_stream_t; /* the same type as cudaStream_t */
+
+typedef enum { KDA_F32 = 0, KDA_BF16 = 1 } kda_dtype;
+
+typedef struct {
+    int B, H, T, K, V;
+} kda_dims;
+
+enum {
+    KDA_OK = 0,
+    KDA_ERR_INVALID_ARG = -1, /* null pointer, negative size, bad enum */
+    KDA_ERR_UNSUPPORTED = -2, /* size or chunk outside the supported set */
+    KDA_ERR_MISALIGNED = -3,  /* a pointer not 16-byte aligned */
+    KDA_ERR_CUDA = -4,        /* a CUDA runtime call or launch failed */
+    KDA_ERR_NO_MEMORY = -5    /* scratch allocation failed */
+};
+
+/*
+ * kda_gate -- the decay gate alone (kdafix-2026-10-02, "Fix 1").
+ *   g_out[b,h,t,c] = -exp(A_log[h]) * softplus(z[b,h,t,c] + dt_bias[h,c])   (chunk == 0)
+ *   or its inclusive cumulative sum over the tokens of each chunk of `chunk`
+ *   tokens (chunk in {16, 32, 64}): G[t] = sum of g over the chunk's tokens up to t.
+ * z has dtype z_dtype, shape (B, H, T, K); g_out is float32 (B, H, T, K).
+ * dims->V is ignored.
+ */
+int kda_gate(const kda_dims* dims, kda_dtype z_dtype, const void* z, const float* A_log,
+             const float* dt_bias, int chunk, float* g_out, kda_stream_t stream);
+
+/*
+ * kda_chunk_forward -- the KDA forward over T tokens, chunk-parallel WY form.
+ *   scale : the read scale folded into q (pass K**-0.5 for the default).
+ *   h0    : initial state (B,H,K,V) float32, or NULL for zero.
+ *   out   : (B,H,T,V) in io_dtype.
+ *   hT    : final state (B,H,K,V) float32, or NULL if not wanted.
+ * h0 and hT may be the same buffer (the state is then advanced in place).
+ */
+int kda_chunk_forward(const kda_dims* dims, kda_dtype io_dtype, const void* q, const void* k,
+                      const void* v, const void* z, const void* beta, const float* A_log,
+                      const float* dt_bias, float scale, const float* h0, int chunk, void* out,
+                      float* hT, kda_stream_t stream);
+
+/*
+ * kda_recurrent_step -- one decode token per (b, h): the step above applied
+ * once, in place on `state` (B,H,K,V) float32.  dims->T must be 1; q, k, z are
+ * (B,H,1,K), v and out (B,H,1,V), beta (B,H,1), all in io_dtype.
+ * (kdafix-2026-10-02, "Fix 2": the decode read uses the same folded scale.)
+ */
+int kda_recurrent_step(const kda_dims* dims, kda_dtype io_dtype, const void* q, const void* k,
+                       const void* v, const void* z, const void* beta, const float* A_log,
+                       const float* dt_bias, float scale, float* state, void* out,
+                       kda_stream_t stream);
+
+/* A static, human-readable name for a status code. */
+const char* kda_status_string(int status);
+
+/*
+ * Diagnostic: the number of CUDA kernels this library has launched in this
+ * process so far (all devices, all threads; a relaxed atomic counter).
+ * Benchmarks read it before and after a timed region to count launches.
+ */
+unsigned long long kda_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KDA_H_ */

@@ -1,0 +1,257 @@
+"""GPU parity: libkda (through its C ABI) against the f64 oracle on the same seeded inputs.
+
+Bars (stated once, used everywhere below):
+* fp32 I/O: max|x - y| / max|y| <= 1e-4, per tensor (o and hT separately);
+* bf16 I/O: ||x - y||_2 / ||y||_2 <= 2e-2 and max|x - y| <= 5e-2, per tensor;
+* the gate alone (fp32 output): max|x - y| / max|y| <= 1e-5.
+Small cases run whole; the full-size workloads run whole on the GPU and are
+compared on sampled (b, h) sequences that the oracle recomputes token by token.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gated_delta_rule_26_gb300 import inputs
+
+pytestmark = pytest.mark.gpu
+
+FP32_BAR = 1e-4
+BF16_REL, BF16_ABS = 2e-2, 5e-2
+
+
+def check(name, got, ref, dtype):
+    got = got.detach().double().cpu().numpy() if hasattr(got, "detach") else np.asarray(got)
+    ref = np.asarray(ref, dtype=np.float64)
+    assert got.shape == ref.shape, (name, got.shape, ref.shape)
+    assert np.all(np.isfinite(got)), name
+    diff = np.abs(got - ref)
+    if dtype == "f32":
+        err = diff.max() / max(np.abs(ref).max(), 1e-30)
+        assert err <= FP32_BAR, f"{name}: max rel {err:.3e} > {FP32_BAR}"
+    else:
+        rel = np.linalg.norm(got - ref) / max(np.linalg.norm(ref), 1e-30)
+        assert rel <= BF16_REL, f"{name}: normwise rel {rel:.3e} > {BF16_REL}"
+        assert diff.max() <= BF16_ABS, f"{name}: max abs {diff.max():.3e} > {BF16_ABS}"
+
+
+def run_and_compare(kda, inp, chunk=None, with_h0=True, want_hT=True, threads=4):
+    d = inp.to("cuda")
+    h0 = d.h0 if with_h0 else None
+    o, hT = kda.chunk_forward(d.q, d.k, d.v, d.z, d.beta, d.A_log, d.dt_bias, inp.scale, h0,
+                              chunk or inp.chunk, output_final_state=want_hT)
+    torch.cuda.synchronize()
+    o_ref, h_ref = oracle.forward(inp.q, inp.k, inp.v, inp.z, inp.beta, inp.A_log, inp.dt_bias,
+                                  inp.scale, inp.h0 if with_h0 else None, threads=threads)
+    check("o", o, o_ref, inp.dtype)
+    if want_hT:
+        check("hT", hT, h_ref, inp.dtype)
+    return o, hT
+
+
+# ---------------------------------------------------------------- gate
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("chunk", [0, 16, 64])
+def test_gate_matches_oracle(kda, dtype, chunk):
+    inp = inputs.make(2, 3, 100, 64, 8, dtype=dtype, seed=7, dt_std=0.5)
+    d = inp.to("cuda")
+    g = kda.gate(d.z, d.A_log, d.dt_bias, chunk=chunk)
+    torch.cuda.synchronize()
+    ref = oracle.gate(inp.z, inp.A_log, inp.dt_bias)
+    if chunk:
+        T = ref.shape[2]
+        ref = np.concatenate([np.cumsum(ref[:, :, s:s + chunk], axis=2)
+                              for s in range(0, T, chunk)], axis=2)
+    got = g.double().cpu().numpy()
+    assert np.all(got <= 0)
+    err = np.abs(got - ref).max() / np.abs(ref).max()
+    assert err <= 1e-5, err
+
+
+# ---------------------------------------------------------------- fp32 workloads
+@pytest.mark.parametrize("A_log_value", [-3.0, 0.0, 2.0])
+def test_small_fp32_per_A_log(kda, A_log_value):
+    """B1 H2 T32 K=V=8, two chunks of 16, both heads at one A_log value, h0 ~ N(0, 0.1^2)."""
+    run_and_compare(kda, inputs.workload("small_fp32", A_log_value=A_log_value))
+
+
+def test_small_fp32_z_sweep(kda):
+    """The same shape with z swept linearly over [-6, 6] across (t, c), per A_log value."""
+    for a in (-3.0, 0.0, 2.0):
+        run_and_compare(kda, inputs.workload("small_fp32", A_log_value=a, z_sweep=(-6.0, 6.0)))
+
+
+def test_multi_chunk_fp32(kda):
+    """B2 H8 T256 K=V=64, sixteen chunks of 16: the multi-chunk carry."""
+    run_and_compare(kda, inputs.workload("multi_chunk_fp32"))
+
+
+@pytest.mark.parametrize("B,H,T,K,V,chunk,dtype", [
+    (1, 2, 37, 16, 24, 16, "f32"),     # ragged tail, K != V
+    (2, 3, 100, 64, 32, 32, "f32"),    # ragged, several chunks
+    (1, 2, 130, 128, 128, 64, "f32"),  # full width, ragged
+    (1, 1, 1, 8, 8, 16, "f32"),        # one token
+    (1, 2, 70, 128, 64, 64, "bf16"),   # bf16 through the general path
+    (2, 2, 200, 128, 128, 64, "bf16"), # the tensor-core shape, several chunks, ragged
+    (1, 3, 64, 128, 128, 64, "bf16"),  # exactly one chunk
+    (2, 2, 192, 128, 128, 16, "bf16"), # chunk 16 at full width
+])
+def test_shapes_and_ragged_tails(kda, B, H, T, K, V, chunk, dtype):
+    inp = inputs.make(B, H, T, K, V, chunk=chunk, dtype=dtype, seed=B * 1000 + T, dt_std=0.1,
+                      h0_std=0.1)
+    run_and_compare(kda, inp)
+
+
+def test_zero_initial_state_and_no_final_state(kda):
+    inp = inputs.make(1, 2, 48, 32, 32, chunk=16, dtype="f32", seed=3, h0_std=0.1)
+    run_and_compare(kda, inp, with_h0=False, want_hT=True)
+    run_and_compare(kda, inp, with_h0=True, want_hT=False)
+
+
+def test_empty_sequence_copies_state(kda):
+    inp = inputs.make(1, 2, 0, 32, 16, chunk=16, dtype="f32", seed=4, h0_std=0.1)
+    d = inp.to("cuda")
+    _, hT = kda.chunk_forward(d.q, d.k, d.v, d.z, d.beta, d.A_log, d.dt_bias, inp.scale, d.h0, 16)
+    torch.cuda.synchronize()
+    assert torch.equal(hT.cpu(), inp.h0)
+
+
+def test_resume_equals_whole(kda):
+    inp = inputs.make(2, 2, 160, 128, 128, chunk=64, dtype="bf16", seed=9, h0_std=0.1)
+    d = inp.to("cuda")
+    o, h = kda.chunk_forward(d.q, d.k, d.v, d.z, d.beta, d.A_log, d.dt_bias, inp.scale, d.h0, 64)
+    sl = lambda t, a, b: t[:, :, a:b].contiguous()
+    o1, h1 = kda.chunk_forward(sl(d.q, 0, 64), sl(d.k, 0, 64), sl(d.v, 0, 64), sl(d.z, 0, 64),
+                               sl(d.beta, 0, 64), d.A_log, d.dt_bias, inp.scale, d.h0, 64)
+    o2, h2 = kda.chunk_forward(sl(d.q, 64, 160), sl(d.k, 64, 160), sl(d.v, 64, 160),
+                               sl(d.z, 64, 160), sl(d.beta, 64, 160), d.A_log, d.dt_bias,
+                               inp.scale, h1, 64)
+    torch.cuda.synchronize()
+    # same chunk boundaries => same arithmetic: bit-identical
+    assert torch.equal(torch.cat([o1, o2], dim=2), o)
+    assert torch.equal(h2, h)
+
+
+def test_run_twice_is_bitwise_identical(kda):
+    inp = inputs.make(2, 4, 300, 128, 128, chunk=64, dtype="bf16", seed=5, h0_std=0.1)
+    d = inp.to("cuda")
+    a = kda.chunk_forward(d.q, d.k, d.v, d.z, d.beta, d.A_log, d.dt_bias, inp.scale, d.h0, 64)
+    b = kda.chunk_forward(d.q, d.k, d.v, d.z, d.beta, d.A_log, d.dt_bias, inp.scale, d.h0, 64)
+    torch.cuda.synchronize()
+    assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+
+
+def test_scale_enters_only_the_read_on_gpu(kda):
+    inp = inputs.make(1, 2, 96, 64, 64, chunk=32, dtype="f32", seed=6, h0_std=0.1)
+    d = inp.to("cuda")
+    o1, h1 = kda.chunk_forward(d.q, d.k, d.v, d.z, d.beta, d.A_log, d.dt_bias, 1.0, d.h0, 32)
+    o8, h8 = kda.chunk_forward(d.q, d.k, d.v, d.z, d.beta, d.A_log, d.dt_bias, 0.125, d.h0, 32)
+    torch.cuda.synchronize()
+    assert torch.equal(h1, h8)
+    torch.testing.assert_close(o8, 0.125 * o1, rtol=1e-6, atol=1e-7)
+
+
+# ---------------------------------------------------------------- full-size workloads, sampled
+def _sample_pairs(inp, pairs):
+    """Gather (b, h) sequences into a (1, n, T, *) problem the oracle can run."""
+    bs = [p[0] for p in pairs]
+    hs = [p[1] for p in pairs]
+    g = lambda t: t[bs, hs].unsqueeze(0)
+    h0 = None if inp.h0 is None else g(inp.h0)
+    return (g(inp.q), g(inp.k), g(inp.v), g(inp.z), g(inp.beta), inp.A_log[hs],
+            inp.dt_bias[hs], h0)
+
+
+@pytest.mark.parametrize("name,pairs", [
+    ("prefill_bf16", [(0, 0), (3, 17), (7, 31)]),
+    ("long_bf16", [(0, 5), (0, 30)]),
+])
+def test_full_size_sampled(kda, name, pairs):
+    inp = inputs.workload(name)
+    d = inp.to("cuda")
+    o, hT = kda.chunk_forward(d.q, d.k, d.v, d.z, d.beta, d.A_log, d.dt_bias, inp.scale, d.h0,
+                              inp.chunk)
+    torch.cuda.synchronize()
+    q, k, v, z, beta, A, dt, h0 = _sample_pairs(inp, pairs)
+    o_ref, h_ref = oracle.forward(q, k, v, z, beta, A, dt, inp.scale, h0, threads=len(pairs))
+    bs = [p[0] for p in pairs]
+    hs = [p[1] for p in pairs]
+    check(f"{name} o", o[bs, hs].unsqueeze(0), o_ref, "bf16")
+    check(f"{name} hT", hT[bs, hs].unsqueeze(0), h_ref, "bf16")
+    assert torch.isfinite(o).all() and torch.isfinite(hT).all()
+
+
+# ---------------------------------------------------------------- decode
+def _decode_run(kda, dec, state_dev):
+    outs = []
+    for s in range(dec.steps):
+        o = kda.recurrent_step(dec.q[s], dec.k[s], dec.v[s], dec.z[s], dec.beta[s], dec.A_log,
+                               dec.dt_bias, state_dev, dec.scale)
+        outs.append(o)
+    torch.cuda.synchronize()
+    return torch.stack(outs)  # (steps, B, H, 1, V)
+
+
+def _decode_oracle(dec, pairs):
+    bs = [p[0] for p in pairs]
+    hs = [p[1] for p in pairs]
+    seq = lambda t: t[:, bs, hs, 0].permute(1, 0, 2).unsqueeze(0)  # (1, n, steps, K)
+    beta = dec.beta[:, bs, hs, 0].permute(1, 0).unsqueeze(0)
+    return oracle.forward(seq(dec.q), seq(dec.k), seq(dec.v), seq(dec.z), beta, dec.A_log[hs],
+                          dec.dt_bias[hs], dec.scale, dec.state[bs, hs].unsqueeze(0), threads=4)
+
+
+def test_decode_full_size_sampled(kda):
+    """B256 H32 K=V=128, 64 consecutive in-place steps on the whole state; sampled pairs checked
+    against the oracle's token-by-token run (every step's o and the final state)."""
+    dec = inputs.decode()
+    dev = lambda t: t.cuda()
+    d = inputs.DecodeInputs(dec.B, dec.H, dec.K, dec.V, dec.steps, dec.dtype, dev(dec.q),
+                            dev(dec.k), dev(dec.v), dev(dec.z), dev(dec.beta), dev(dec.A_log),
+                            dev(dec.dt_bias), dev(dec.state), dec.scale)
+    state = d.state.clone()
+    outs = _decode_run(kda, d, state)
+    pairs = [(0, 0), (17, 3), (128, 16), (255, 31), (64, 9), (200, 27)]
+    o_ref, h_ref = _decode_oracle(dec, pairs)
+    bs = [p[0] for p in pairs]
+    hs = [p[1] for p in pairs]
+    got_o = outs[:, bs, hs, 0].permute(1, 0, 2).unsqueeze(0)
+    check("decode o", got_o, o_ref, "bf16")
+    check("decode state", state[bs, hs].unsqueeze(0), h_ref, "bf16")
+
+
+@pytest.mark.parametrize("K,V", [(8, 8), (64, 32), (128, 128), (24, 40)])
+def test_decode_fp32_small(kda, K, V):
+    dec = inputs.decode(B=3, H=2, K=K, V=V, steps=20, dtype="f32", seed=K * 7 + V)
+    dev = lambda t: t.cuda()
+    d = inputs.DecodeInputs(dec.B, dec.H, K, V, dec.steps, "f32", dev(dec.q), dev(dec.k),
+                            dev(dec.v), dev(dec.z), dev(dec.beta), dev(dec.A_log),
+                            dev(dec.dt_bias), dev(dec.state), dec.scale)
+    state = d.state.clone()
+    outs = _decode_run(kda, d, state)
+    pairs = [(b, h) for b in range(3) for h in range(2)]
+    o_ref, h_ref = _decode_oracle(dec, pairs)
+    got_o = outs[:, [p[0] for p in pairs], [p[1] for p in pairs], 0].permute(1, 0, 2).unsqueeze(0)
+    check("decode o", got_o, o_ref, "f32")
+    check("decode state", state[[p[0] for p in pairs], [p[1] for p in pairs]].unsqueeze(0), h_ref,
+          "f32")
+
+
+def test_decode_matches_chunk_forward(kda):
+    """64 decode steps and one chunked forward over the same 64 tokens agree (two GPU paths)."""
+    inp = inputs.make(2, 4, 64, 128, 128, chunk=64, dtype="f32", seed=12, h0_std=0.1)
+    d = inp.to("cuda")
+    o_c, h_c = kda.chunk_forward(d.q, d.k, d.v, d.z, d.beta, d.A_log, d.dt_bias, inp.scale, d.h0,
+                                 64)
+    state = d.h0.clone()
+    outs = []
+    for t in range(64):
+        sl = lambda x: x[:, :, t:t + 1].contiguous()
+        outs.append(kda.recurrent_step(sl(d.q), sl(d.k), sl(d.v), sl(d.z), sl(d.beta), d.A_log,
+                                       d.dt_bias, state, inp.scale))
+    torch.cuda.synchronize()
+    o_r = torch.cat(outs, dim=2)
+    assert (o_r - o_c).abs().max() / o_c.abs().max() < 1e-4
+    assert (state - h_c).abs().max() / h_c.abs().max() < 1e-4
