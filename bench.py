@@ -187,6 +187,41 @@ def run_reference(args):
     return 0
 
 
+def run_decode(args, kda, inputs, peaks, ws, barrier):
+    """Time `decode_steps` consecutive in-place decode steps on the fp32 state."""
+    import torch
+    stream = torch.cuda.current_stream()
+    dec = inputs.decode(steps=args.decode_steps, B=args.decode_batch)
+
+    dq, dk, dv, dz, db = (t.cuda() for t in (dec.q, dec.k, dec.v, dec.z, dec.beta))
+    dA, ddt = dec.A_log.cuda(), dec.dt_bias.cuda()
+    state = dec.state.cuda()
+    dout = torch.empty(dec.B, dec.H, 1, dec.V, device="cuda", dtype=torch.bfloat16)
+    it = [0]
+
+    def dstep():
+        s = it[0] % dec.steps
+        kda.recurrent_step(dq[s], dk[s], dv[s], dz[s], db[s], dA, ddt, state, dec.scale, out=dout)
+        it[0] += 1
+
+    for _ in range(3):
+        dstep()
+    barrier()
+    dsecs = timed(dstep, dec.steps, stream)
+    dper = dsecs / dec.steps
+    dbytes = 2 * dec.B * dec.H * dec.K * dec.V * 4 + dec.B * dec.H * (3 * dec.K + 2 * dec.V + 1) * 2
+    decode = {"value": ws * dec.B / dper, "unit": "tokens/s", "us_per_step": dper * 1e6,
+              "state_GBps": dbytes / dper / 1e9,
+              "roofline": {"bound": "hbm", "achieved": dbytes / dper / 1e9,
+                           "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                           "frac": dbytes / dper / 1e9 / peaks["hbm_gbs"], "traffic": None},
+              "config": {"workload": f"decode_bf16 B{dec.B} H{dec.H} K={dec.K} V={dec.V}, "
+                                     f"{dec.steps} consecutive steps",
+                         "bytes_per_step": dbytes}}
+
+    return decode
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -195,6 +230,10 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--decode-steps", type=int, default=64)
+    ap.add_argument("--decode-batch", type=int, default=None,
+                    help="decode batch B (default: the decode workload's 256)")
+    ap.add_argument("--only", default="all", choices=["all", "prefill", "decode"],
+                    help="time only one of the two workloads (for profiler captures)")
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)
@@ -216,6 +255,11 @@ def main():
             torch.distributed.barrier()
 
     peaks = load_peaks()
+    if args.only == "decode":
+        decode = run_decode(args, kda, inputs, peaks, ws, barrier)
+        if rank == 0:
+            print(json.dumps({"metric": "decode only", "decode": decode}), flush=True)
+        return 0
     inp_cpu = inputs.workload(WORKLOAD)
     B, H, T, K, V, C = inp_cpu.B, inp_cpu.H, inp_cpu.T, inp_cpu.K, inp_cpu.V, inp_cpu.chunk
     d = inp_cpu.to("cuda")
@@ -290,33 +334,7 @@ def main():
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
     del host, dev, out_h, hT_h
 
-    # ---- decode: 64 consecutive in-place steps on the 512 MiB fp32 state
-    dec = inputs.decode(steps=args.decode_steps)
-    dq, dk, dv, dz, db = (t.cuda() for t in (dec.q, dec.k, dec.v, dec.z, dec.beta))
-    dA, ddt = dec.A_log.cuda(), dec.dt_bias.cuda()
-    state = dec.state.cuda()
-    dout = torch.empty(dec.B, dec.H, 1, dec.V, device="cuda", dtype=torch.bfloat16)
-    it = [0]
-
-    def dstep():
-        s = it[0] % dec.steps
-        kda.recurrent_step(dq[s], dk[s], dv[s], dz[s], db[s], dA, ddt, state, dec.scale, out=dout)
-        it[0] += 1
-
-    for _ in range(3):
-        dstep()
-    barrier()
-    dsecs = timed(dstep, dec.steps, stream)
-    dper = dsecs / dec.steps
-    dbytes = 2 * dec.B * dec.H * dec.K * dec.V * 4 + dec.B * dec.H * (3 * dec.K + 2 * dec.V + 1) * 2
-    decode = {"value": ws * dec.B / dper, "unit": "tokens/s", "us_per_step": dper * 1e6,
-              "state_GBps": dbytes / dper / 1e9,
-              "roofline": {"bound": "hbm", "achieved": dbytes / dper / 1e9,
-                           "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                           "frac": dbytes / dper / 1e9 / peaks["hbm_gbs"], "traffic": None},
-              "config": {"workload": "decode_bf16 B256 H32 K=V=128, 64 consecutive steps",
-                         "bytes_per_step": dbytes}}
-
+    decode = None if args.only == "prefill" else run_decode(args, kda, inputs, peaks, ws, barrier)
     line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws,
             "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": per_step * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",

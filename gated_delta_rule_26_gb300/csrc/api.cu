@@ -33,16 +33,29 @@ int check_dims(const kda_dims* d, bool need_v) {
 
 bool dtype_ok(int dt) { return dt == KDA_F32 || dt == KDA_BF16; }
 
+bool aligned_to(const void* p, unsigned bytes) {
+    return (reinterpret_cast<uintptr_t>(p) & (uintptr_t)(bytes - 1)) == 0;
+}
+
+// `required` must be non-null and 16-byte aligned; `optional` may be null, else 16-byte
+// aligned; `elementwise` must be non-null and aligned to `elem_bytes` (read per element).
 int check_ptrs(std::initializer_list<const void*> required,
-               std::initializer_list<const void*> optional) {
+               std::initializer_list<const void*> optional,
+               std::initializer_list<const void*> elementwise = {}, unsigned elem_bytes = 4) {
     for (const void* p : required)
+        if (!p) return KDA_ERR_INVALID_ARG;
+    for (const void* p : elementwise)
         if (!p) return KDA_ERR_INVALID_ARG;
     for (const void* p : required)
         if (!aligned16(p)) return KDA_ERR_MISALIGNED;
     for (const void* p : optional)
         if (p && !aligned16(p)) return KDA_ERR_MISALIGNED;
+    for (const void* p : elementwise)
+        if (!aligned_to(p, elem_bytes)) return KDA_ERR_MISALIGNED;
     return KDA_OK;
 }
+
+unsigned io_bytes(kda_dtype dt) { return dt == KDA_BF16 ? 2u : 4u; }
 
 int from_cuda(cudaError_t e) { return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA; }
 
@@ -73,7 +86,8 @@ int kda_gate(const kda_dims* dims, kda_dtype z_dtype, const void* z, const float
     const int span = chunk > 0 ? chunk : 64;
     if ((dims->T + span - 1) / span > 65535) return KDA_ERR_UNSUPPORTED;
     if (dims->T == 0) return KDA_OK;
-    st = check_ptrs({z, A_log, dt_bias, g_out}, {});
+    st = check_ptrs({g_out}, {}, {z}, io_bytes(z_dtype));
+    if (!st) st = check_ptrs({}, {}, {A_log, dt_bias}, 4);
     if (st) return st;
     return from_cuda(kda::launch_gate(dims->B, dims->H, dims->T, dims->K, z_dtype, z, A_log,
                                       dt_bias, chunk, g_out, (cudaStream_t)stream));
@@ -88,7 +102,8 @@ int kda_chunk_forward(const kda_dims* dims, kda_dtype io_dtype, const void* q, c
     if (!dtype_ok(io_dtype)) return KDA_ERR_INVALID_ARG;
     if (chunk != 16 && chunk != 32 && chunk != 64) return KDA_ERR_UNSUPPORTED;
     if (dims->T > 0) {
-        st = check_ptrs({q, k, v, z, beta, A_log, dt_bias, out}, {h0, hT});
+        st = check_ptrs({q, k, v, z, out}, {h0, hT}, {beta}, io_bytes(io_dtype));
+        if (!st) st = check_ptrs({}, {}, {A_log, dt_bias}, 4);
     } else {
         st = check_ptrs({}, {h0, hT});
     }
@@ -110,7 +125,8 @@ int kda_recurrent_step(const kda_dims* dims, kda_dtype io_dtype, const void* q, 
     if (st) return st;
     if (!dtype_ok(io_dtype)) return KDA_ERR_INVALID_ARG;
     if (dims->T != 1) return KDA_ERR_INVALID_ARG;
-    st = check_ptrs({q, k, v, z, beta, A_log, dt_bias, state, out}, {});
+    st = check_ptrs({state}, {}, {q, k, v, z, beta, out}, io_bytes(io_dtype));
+    if (!st) st = check_ptrs({}, {}, {A_log, dt_bias}, 4);
     if (st) return st;
     kda::StepArgs a{dims->B, dims->H, dims->K, dims->V, io_dtype, q, k, v, z, beta,
                     A_log, dt_bias, scale, state, out};

@@ -25,7 +25,11 @@
  *       h0, hT, state : (B, H, K, V)    float32 always
  *   q, k, v, z, beta and out have the I/O dtype (KDA_F32 or KDA_BF16);
  *   A_log, dt_bias and the state are float32.
- * - Every pointer must be 16-byte aligned, else KDA_ERR_MISALIGNED.
+ * - Alignment (else KDA_ERR_MISALIGNED): q, k, v, z, out, h0, hT and state
+ *   must be 16-byte aligned for kda_chunk_forward (tiles are moved in 16-byte
+ *   units); kda_recurrent_step needs 16 bytes only for `state`; beta, A_log,
+ *   dt_bias (and, for kda_recurrent_step and kda_gate, the per-token vectors)
+ *   need only their element alignment.
  * - The caller owns every buffer.  The library keeps no state between calls
  *   except the CUDA resources the runtime itself caches; it is re-entrant.
  *   Scratch memory, where a path needs it, is taken with cudaMallocAsync on the

@@ -88,7 +88,9 @@ def test_recurrent_step_requires_one_token(lib):
     assert lib.kda_recurrent_step(ctypes.byref(Dims(2, 2, 2, 64, 64)), 1, p, p, p, p, p, p, p,
                                   0.1, p, p, None) == -1
     assert lib.kda_recurrent_step(ctypes.byref(Dims(2, 2, 1, 64, 64)), 1, p, p, p, p, p, p, p,
-                                  0.1, vp((1 << 20) + 8), p, None) == -3
+                                  0.1, vp((1 << 20) + 8), p, None) == -3   # state
+    assert lib.kda_recurrent_step(ctypes.byref(Dims(2, 2, 1, 64, 64)), 1, vp((1 << 20) + 1), p,
+                                  p, p, p, p, p, 0.1, p, p, None) == -3   # odd bf16 address
 
 
 def test_gate_rejects_bad_chunk(lib):
