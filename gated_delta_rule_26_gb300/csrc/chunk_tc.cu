@@ -1,13 +1,785 @@
-// chunk_tc.cu -- tensor-core (tcgen05) path of the chunked forward.
+// chunk_tc.cu -- the KDA chunked forward on the 5th-generation tensor cores
+// (tcgen05 + TMEM + TMA), for bf16 I/O with K = V = 128 and chunk C = 64.
+//
+// One CTA (8 warps) owns one (b, h) sequence and walks its chunks in order.
+// The fp32 state S (K x V) lives in TMEM for the whole sequence; per chunk:
+//
+//   P1  TMA: q, k, v, z tiles (64 x 128 bf16 each) into shared memory.
+//   P2  gate g = -exp(A_log) softplus(z + dt_bias) and the in-chunk cumulative
+//       log decay G (kdafix-2026-10-02 "Fix 1"; kda-adjoint-2026-10-01 sec. 2).
+//   P3  decay-folded scores  A[t,i] = beta_t sum_c k_tc k_ic e^{G_tc - G_ic}  (i < t)
+//       and M[t,i] = sum_c q_tc k_ic e^{G_tc - G_ic}  (i <= t) on the tensor cores.
+//       e^{G_t - G_i} cannot be split as e^{G_t} e^{-G_i} (e^{-G_i} overflows
+//       fp32 within a chunk when the decay is strong), so pairs are grouped by
+//       the level of the binary tree over the 64 tokens at which t and i part:
+//       at a level with half-width h, t in the upper half and i in the lower
+//       half of the same 2h-block share the reference r = last token of the
+//       lower half, e^{G_t - G_i} = e^{G_t - G_r} e^{G_r - G_i}, both factors
+//       <= 1.  Four levels (h = 32, 16, 8, 4) are four GEMMs of scaled operands
+//       (M = 128: k rows then q rows; N = 64; K = 128); pairs inside a 4-token
+//       block take the exact pairwise exponential on CUDA cores.
+//   P4  T = (I + A)^{-1} by blocked forward substitution (16 x 16 diagonal
+//       blocks, then the off-diagonal blocks), fp32 on CUDA cores.
+//   P5  W^T = (diag(beta) K Gamma)^T T^T and U^T = (diag(beta) V)^T T^T  (tcgen05),
+//       then Q'^T = (Q Gamma)^T - W^T M^T and U'^T = U^T M^T  (tcgen05), so that
+//       o = scale (Q' S + U') and Delta = U - W S both come from ONE product with S.
+//   C1  D = [W ; Q'] S     (M = 128, N = 128, K = 128; S as bf16 operand).
+//   C2  Delta = U - D[0:64]; o = scale (D[64:128] + U')  -> bf16 to HBM.
+//       Meanwhile the fp32 state in TMEM is scaled by Gamma_last (row c by
+//       e^{G_last,c}).
+//   C3  S += (K * e^{G_last - G})^T Delta   accumulated in TMEM in fp32
+//       (the carry with a single exponential of the log-space difference,
+//       kda-adjoint-2026-10-01 sections 2 and 5b), then S -> bf16 operand.
+//
+// Operand layouts are the tcgen05 canonical 128-byte-swizzled layouts, either
+// K-major (rows of 128 B along the contraction) or MN-major (rows of 128 B
+// along M/N); both are written directly by the threads that produce them.
+// Every mbarrier wait is bounded; on a timeout the CTA records it in
+// g_kda_tc_timeout, releases its TMEM and exits.
+#include <cuda.h>
+
 #include "common.cuh"
+#include "tc_ptx.cuh"
 
 namespace kda {
 
+__device__ int g_kda_tc_timeout;
+
+namespace {
+
+constexpr int C = 64, KD = 128, VD = 128, NT = 256;
+constexpr float LOG2E = 1.4426950408889634f;
+
+// ---- shared memory map (bytes from a 1024-byte aligned base)
+constexpr uint32_t OFF_LVL = 0;                 // 64 KB multi-use region (see LV_*)
+constexpr uint32_t OFF_G = 65536;               // 32 KB fp32 G[t][c]
+constexpr uint32_t OFF_Q = OFF_G + 32768;       // 16 KB bf16 q tile, row-major [t][c]
+constexpr uint32_t OFF_K = OFF_Q + 16384;       // 16 KB bf16 k tile
+constexpr uint32_t OFF_V = OFF_K + 16384;       // 16 KB bf16 v tile, later T fp32 [t][i]
+constexpr uint32_t OFF_A1 = OFF_V + 16384;      // 32 KB [W^T | Q'^T], MN-major (2 atoms)
+constexpr uint32_t OFF_S = OFF_A1 + 32768;      // 32 KB S bf16, MN-major [c][v] (2 atoms)
+constexpr uint32_t OFF_MISC = OFF_S + 32768;
+// multi-use region, in order of use within a chunk
+constexpr uint32_t LV_Z = 0;        // z tile (16 KB)                    P1-P2
+constexpr uint32_t LV_L0 = 0;       // level operand buffer 0 (32 KB)    P3
+constexpr uint32_t LV_L1 = 32768;   // level operand buffer 1 (32 KB)    P3
+constexpr uint32_t LV_AF = 0;       // A fp32 [t][i] (16 KB)             P3-P4
+constexpr uint32_t LV_MB = 16384;   // M bf16 K-major [t][i] (8 KB)      P3-P5
+constexpr uint32_t LV_TB = 24576;   // T bf16 K-major [t][i] (8 KB)      P4-P5
+constexpr uint32_t LV_BKG = 32768;  // beta K Gamma, MN-major [t][c]     P3-P5
+constexpr uint32_t LV_BV = 49152;   // beta V, MN-major [t][v]           P3-P5
+constexpr uint32_t LV_UT = 0;       // U^T K-major [v][i] (16 KB)        P5-C2
+constexpr uint32_t LV_UPT = 32768;  // U'^T plain [v][t] (16 KB)         P5-C2
+constexpr uint32_t LV_KT = 49152;   // K~ MN-major [t][c] (16 KB)        P5-C3
+constexpr uint32_t LV_DELTA = 16384;// Delta MN-major [t][v] (16 KB)     C2-C3
+
+struct Misc {
+    uint64_t bar_tma, bar_mma;
+    uint32_t tmem_base;
+    int pad;
+    float beta[C];
+    float gamma_last[KD];
+    float dt[KD];
+    float diag[16][16];
+};
+constexpr uint32_t SMEM_BYTES = OFF_MISC + sizeof(Misc) + 1024;
+
+// ---- TMEM columns (512 allocated)
+constexpr uint32_t TM_S = 0;      // fp32 state, lanes = key channel c, cols = v   (128)
+constexpr uint32_t TM_LVL = 128;  // four level score tiles                        (4 x 64)
+constexpr uint32_t TM_QP = 128;   // W^T M^T                                       (64)
+constexpr uint32_t TM_UP = 192;   // U^T M^T                                       (64)
+constexpr uint32_t TM_D1 = 256;   // [W ; Q'] S                                    (128)
+constexpr uint32_t TM_W = 384;    // W^T                                           (64)
+constexpr uint32_t TM_U = 448;    // U^T                                           (64)
+
+constexpr uint32_t IDESC_LVL = tc::idesc_bf16(128, 64, 0, 0);
+constexpr uint32_t IDESC_WU = tc::idesc_bf16(128, 64, 1, 0);
+constexpr uint32_t IDESC_QU = tc::idesc_bf16(128, 64, 0, 0);
+constexpr uint32_t IDESC_SQ = tc::idesc_bf16(128, 128, 1, 1);
+
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+__device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+__device__ __forceinline__ void unpack8(uint4 r, float (&f)[8]) {
+    f[0] = bf_lo(r.x); f[1] = bf_hi(r.x); f[2] = bf_lo(r.y); f[3] = bf_hi(r.y);
+    f[4] = bf_lo(r.z); f[5] = bf_hi(r.z); f[6] = bf_lo(r.w); f[7] = bf_hi(r.w);
+}
+__device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
+    return make_uint4(tc::pack_bf16x2(f[0], f[1]), tc::pack_bf16x2(f[2], f[3]),
+                      tc::pack_bf16x2(f[4], f[5]), tc::pack_bf16x2(f[6], f[7]));
+}
+__device__ __forceinline__ float bf16_at(const uint8_t* p) {
+    return __uint_as_float(((uint32_t) * reinterpret_cast<const uint16_t*>(p)) << 16);
+}
+
+// K-major tile with `rows` rows: byte offset of element (row, k); k atoms of 64.
+__device__ __forceinline__ uint32_t kmaj_off(int row, int k, int rows) {
+    return (uint32_t)((k >> 6) * (rows * 128)) + tc::sw128_offset(row, (k & 63) >> 3) + (k & 7) * 2;
+}
+// MN-major tile: element (krow, mn), MN atoms of 64 elements `atom` bytes apart.
+__device__ __forceinline__ uint32_t mnmaj_off(int krow, int mn, uint32_t atom) {
+    return (uint32_t)(mn >> 6) * atom + tc::sw128_offset(krow, (mn & 63) >> 3) + (mn & 7) * 2;
+}
+__device__ __forceinline__ uint64_t desc_k(uint32_t saddr, int rows, int ks) {
+    const int k0 = ks * 16;
+    return tc::smem_desc(saddr + (k0 >> 6) * (rows * 128) + (k0 & 63) * 2, 16, 1024);
+}
+__device__ __forceinline__ uint64_t desc_mn(uint32_t saddr, uint32_t atom, int ks) {
+    return tc::smem_desc(saddr + ks * 2048, atom, 1024);
+}
+__device__ __forceinline__ uint32_t taddr(uint32_t base, int warp, uint32_t col) {
+    return base + ((uint32_t)((warp & 3) * 32) << 16) + col;
+}
+
+// Build two levels' operands: rows 0..63 hold k_t scaled to the level's reference,
+// rows 64..127 hold q_t scaled (upper-half tokens only).
+__device__ __forceinline__ void build_levels(uint8_t* sm, int li0, int tid) {
+    const float* G = reinterpret_cast<const float*>(sm + OFF_G);
+    const int c8 = tid & 15;
+#pragma unroll 1
+    for (int r = 0; r < 4; ++r) {
+        const int t = (tid >> 4) + 16 * r;
+        float kf[8], qf[8], g8[8];
+        unpack8(*reinterpret_cast<const uint4*>(sm + OFF_K + t * 256 + c8 * 16), kf);
+        unpack8(*reinterpret_cast<const uint4*>(sm + OFF_Q + t * 256 + c8 * 16), qf);
+        const float4 ga = *reinterpret_cast<const float4*>(G + t * KD + c8 * 8);
+        const float4 gb = *reinterpret_cast<const float4*>(G + t * KD + c8 * 8 + 4);
+        g8[0] = ga.x; g8[1] = ga.y; g8[2] = ga.z; g8[3] = ga.w;
+        g8[4] = gb.x; g8[5] = gb.y; g8[6] = gb.z; g8[7] = gb.w;
+#pragma unroll
+        for (int l = 0; l < 2; ++l) {
+            const int li = li0 + l;
+            const int h = 32 >> li;
+            const int ref = (t & ~(2 * h - 1)) + h - 1;
+            const bool upper = (t & h) != 0;
+            const float4 ra = *reinterpret_cast<const float4*>(G + ref * KD + c8 * 8);
+            const float4 rb = *reinterpret_cast<const float4*>(G + ref * KD + c8 * 8 + 4);
+            const float r8[8] = {ra.x, ra.y, ra.z, ra.w, rb.x, rb.y, rb.z, rb.w};
+            float f[8], kv[8], qv[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                f[j] = ex2((upper ? g8[j] - r8[j] : r8[j] - g8[j]) * LOG2E);
+                kv[j] = kf[j] * f[j];
+                qv[j] = qf[j] * f[j];
+            }
+            uint8_t* L = sm + OFF_LVL + (l ? LV_L1 : LV_L0);
+            *reinterpret_cast<uint4*>(L + kmaj_off(t, c8 * 8, 128)) = pack8(kv);
+            if (upper) *reinterpret_cast<uint4*>(L + kmaj_off(64 + t, c8 * 8, 128)) = pack8(qv);
+        }
+    }
+}
+
+}  // namespace
+
+__global__ void __launch_bounds__(NT, 1)
+    kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
+                        const __grid_constant__ CUtensorMap tm_k,
+                        const __grid_constant__ CUtensorMap tm_v,
+                        const __grid_constant__ CUtensorMap tm_z, int H, int T,
+                        const __nv_bfloat16* __restrict__ beta, const float* __restrict__ A_log,
+                        const float* __restrict__ dt_bias, float scale,
+                        const float* __restrict__ h0, __nv_bfloat16* __restrict__ out,
+                        float* __restrict__ hT) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+    const uint32_t sb = tc::smem_u32(sm);
+    Misc& ms = *reinterpret_cast<Misc*>(sm + OFF_MISC);
+    float* G = reinterpret_cast<float*>(sm + OFF_G);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const size_t bh = blockIdx.x;
+    const int h = (int)(bh % H);
+    const float exp_A = expf(A_log[h]);
+
+    for (int i = tid; i < (int)(OFF_MISC / 16); i += NT)
+        reinterpret_cast<uint4*>(sm)[i] = make_uint4(0u, 0u, 0u, 0u);
+    if (tid < KD) ms.dt[tid] = dt_bias[(size_t)h * KD + tid];
+    if (tid == 0) {
+        tc::mbar_init(&ms.bar_tma, 1);
+        tc::mbar_init(&ms.bar_mma, 1);
+        tc::fence_barrier_init();
+        tc::tma_prefetch_desc(&tm_q);
+        tc::tma_prefetch_desc(&tm_k);
+        tc::tma_prefetch_desc(&tm_v);
+        tc::tma_prefetch_desc(&tm_z);
+    }
+    if (warp == 0) {
+        tc::tmem_alloc(&ms.tmem_base, 512);
+        tc::tmem_relinquish();
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = ms.tmem_base;
+
+    // Initial state: fp32 into TMEM (lane c), bf16 copy as the MN-major operand [c][v].
+    if (tid < KD) {
+        const int c = tid;
+#pragma unroll 1
+        for (int v0 = 0; v0 < VD; v0 += 16) {
+            float f[16];
+#pragma unroll
+            for (int j = 0; j < 16; j += 4) {
+                float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (h0) x = *reinterpret_cast<const float4*>(h0 + (bh * KD + c) * VD + v0 + j);
+                f[j] = x.x; f[j + 1] = x.y; f[j + 2] = x.z; f[j + 3] = x.w;
+            }
+            uint32_t r[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) r[j] = __float_as_uint(f[j]);
+            tc::tmem_st16(taddr(tmem, warp, TM_S + v0), r);
+            float lo[8], hi[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) { lo[j] = f[j]; hi[j] = f[8 + j]; }
+            *reinterpret_cast<uint4*>(sm + OFF_S + mnmaj_off(c, v0, 16384)) = pack8(lo);
+            *reinterpret_cast<uint4*>(sm + OFF_S + mnmaj_off(c, v0 + 8, 16384)) = pack8(hi);
+        }
+        tc::tmem_st_wait();
+    }
+    tc::fence_proxy_async_smem();
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+
+    uint32_t tma_phase = 0, mma_phase = 0;
+    bool failed = false;
+    const int nchunks = (T + C - 1) / C;
+
+#define KDA_WAIT_MMA()                                                   \
+    do {                                                                 \
+        const bool ok_ = tc::mbar_wait(&ms.bar_mma, mma_phase);          \
+        mma_phase ^= 1u;                                                 \
+        if (__syncthreads_or(!ok_)) failed = true;                       \
+        tc::fence_after_sync();                                          \
+    } while (0)
+#define KDA_SYNC_FOR_MMA()                                               \
+    do {                                                                 \
+        tc::fence_proxy_async_smem();                                    \
+        tc::fence_before_sync();                                         \
+        __syncthreads();                                                 \
+        tc::fence_after_sync();                                          \
+    } while (0)
+
+    for (int n = 0; n < nchunks && !failed; ++n) {
+        const int t0 = n * C, cn = min(C, T - t0);
+        // ---------------------------------------------------------------- P1
+        if (tid == 0) {
+            tc::mbar_arrive_expect_tx(&ms.bar_tma, 4u * 16384u);
+            tc::tma_load_3d(sm + OFF_Q, &tm_q, 0, t0, (int)bh, &ms.bar_tma);
+            tc::tma_load_3d(sm + OFF_K, &tm_k, 0, t0, (int)bh, &ms.bar_tma);
+            tc::tma_load_3d(sm + OFF_V, &tm_v, 0, t0, (int)bh, &ms.bar_tma);
+            tc::tma_load_3d(sm + OFF_LVL + LV_Z, &tm_z, 0, t0, (int)bh, &ms.bar_tma);
+        }
+        if (tid < C)
+            ms.beta[tid] = tid < cn ? __bfloat162float(beta[bh * T + t0 + tid]) : 0.f;
+        {
+            const bool ok = tc::mbar_wait(&ms.bar_tma, tma_phase);
+            tma_phase ^= 1u;
+            if (__syncthreads_or(!ok)) { failed = true; break; }
+        }
+        // ---------------------------------------------------------------- P2
+        {
+            const int c = tid & 127, half = tid >> 7;
+            const float dt = ms.dt[c];
+            const uint8_t* zt = sm + OFF_LVL + LV_Z;
+            float acc = 0.f;
+#pragma unroll 4
+            for (int t = half * 32; t < half * 32 + 32; ++t) {
+                const float x = bf16_at(zt + t * 256 + c * 2) + dt;
+                const float sp = fmaxf(x, 0.f) + __logf(1.f + __expf(-fabsf(x)));
+                acc += (t < cn) ? -(exp_A * sp) : 0.f;
+                G[t * KD + c] = acc;
+            }
+        }
+        __syncthreads();
+        if (tid >= 128) {
+            const int c = tid - 128;
+            const float base = G[31 * KD + c];
+#pragma unroll 4
+            for (int t = 32; t < 64; ++t) G[t * KD + c] += base;
+        }
+        __syncthreads();
+        // ---------------------------------------------------------------- P3: levels 32, 16
+        build_levels(sm, 0, tid);
+        KDA_SYNC_FOR_MMA();
+        if (tid == 0) {
+#pragma unroll
+            for (int l = 0; l < 2; ++l) {
+                const uint32_t L = sb + OFF_LVL + (l ? LV_L1 : LV_L0);
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks)
+                    tc::mma_bf16(tmem + TM_LVL + 64 * l, desc_k(L, 128, ks), desc_k(L, 128, ks),
+                                 IDESC_LVL, ks > 0);
+            }
+            tc::mma_commit(&ms.bar_mma);
+        }
+        // pairs inside 4-token blocks: exact pairwise decay, CUDA cores
+        {
+            const int b4 = tid >> 4, c8 = tid & 15;
+            float kk[4][8], qq[4][8], gg[4][8];
+#pragma unroll
+            for (int a = 0; a < 4; ++a) {
+                const int t = 4 * b4 + a;
+                unpack8(*reinterpret_cast<const uint4*>(sm + OFF_K + t * 256 + c8 * 16), kk[a]);
+                unpack8(*reinterpret_cast<const uint4*>(sm + OFF_Q + t * 256 + c8 * 16), qq[a]);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) gg[a][j] = G[t * KD + c8 * 8 + j];
+            }
+            float v[16];
+#pragma unroll
+            for (int a = 0; a < 4; ++a) {  // M diagonal
+                float s = 0.f;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) s = fmaf(qq[a][j], kk[a][j], s);
+                v[6 + a] = s;
+            }
+#pragma unroll
+            for (int a = 1; a < 4; ++a)
+#pragma unroll
+                for (int b = 0; b < a; ++b) {
+                    float sa = 0.f, sq = 0.f;
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const float kd = kk[b][j] * ex2((gg[a][j] - gg[b][j]) * LOG2E);
+                        sa = fmaf(kk[a][j], kd, sa);
+                        sq = fmaf(qq[a][j], kd, sq);
+                    }
+                    const int idx = a * (a - 1) / 2 + b;
+                    v[idx] = sa;
+                    v[10 + idx] = sq;
+                }
+            // reduce-scatter across the 16 lanes that share this 4-token block
+#pragma unroll
+            for (int off = 8, w = 8; off >= 1; off >>= 1, w >>= 1) {
+                const bool hi = (lane & off) != 0;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    if (j < w) {
+                        const float send = hi ? v[j] : v[j + w];
+                        const float keep = hi ? v[j + w] : v[j];
+                        v[j] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+                    }
+                }
+            }
+            ms.diag[b4][c8] = v[0];
+        }
+        KDA_WAIT_MMA();
+        if (failed) break;
+        // ---------------------------------------------------------------- P3: levels 8, 4
+        build_levels(sm, 2, tid);
+        KDA_SYNC_FOR_MMA();
+        if (tid == 0) {
+#pragma unroll
+            for (int l = 0; l < 2; ++l) {
+                const uint32_t L = sb + OFF_LVL + (l ? LV_L1 : LV_L0);
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks)
+                    tc::mma_bf16(tmem + TM_LVL + 128 + 64 * l, desc_k(L, 128, ks),
+                                 desc_k(L, 128, ks), IDESC_LVL, ks > 0);
+            }
+            tc::mma_commit(&ms.bar_mma);
+        }
+        KDA_WAIT_MMA();
+        if (failed) break;
+        // ---------------------------------------------------------------- P3 epilogue
+        if (warp < 4) {
+            // TMEM lane r: rows 0..63 are A rows (k side), rows 64..127 are M rows (q side)
+            const int r = tid, t = r & 63;
+            const bool is_m = r >= 64;
+            const float bt = ms.beta[t];
+            float* Af = reinterpret_cast<float*>(sm + OFF_LVL + LV_AF);
+#pragma unroll 1
+            for (int i0 = 0; i0 < 64; i0 += 16) {
+                uint32_t d0[16], d1[16], d2[16], d3[16];
+                tc::tmem_ld16(taddr(tmem, warp, TM_LVL + i0), d0);
+                tc::tmem_ld16(taddr(tmem, warp, TM_LVL + 64 + i0), d1);
+                tc::tmem_ld16(taddr(tmem, warp, TM_LVL + 128 + i0), d2);
+                tc::tmem_ld16(taddr(tmem, warp, TM_LVL + 192 + i0), d3);
+                tc::tmem_ld_wait();
+                float o16[16];
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const int i = i0 + j;
+                    const int x = t ^ i;
+                    float val = __uint_as_float(x >= 32 ? d0[j] : x >= 16 ? d1[j] : x >= 8 ? d2[j] : d3[j]);
+                    if (x < 4) {
+                        const int tl = t & 3, il = i & 3;
+                        const int idx = (tl == il) ? 6 + tl
+                                                   : (is_m ? 10 : 0) + tl * (tl - 1) / 2 + il;
+                        val = ms.diag[t >> 2][tl >= il ? idx : 0];
+                    }
+                    const bool valid = is_m ? (i <= t) : (i < t);
+                    o16[j] = valid ? (is_m ? val : bt * val) : 0.f;
+                }
+                if (!is_m) {
+#pragma unroll
+                    for (int j = 0; j < 16; j += 4)
+                        *reinterpret_cast<float4*>(Af + t * 64 + i0 + j) =
+                            make_float4(o16[j], o16[j + 1], o16[j + 2], o16[j + 3]);
+                } else {
+                    float lo[8], hi[8];
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) { lo[j] = o16[j]; hi[j] = o16[8 + j]; }
+                    *reinterpret_cast<uint4*>(sm + OFF_LVL + LV_MB + kmaj_off(t, i0, 64)) = pack8(lo);
+                    *reinterpret_cast<uint4*>(sm + OFF_LVL + LV_MB + kmaj_off(t, i0 + 8, 64)) = pack8(hi);
+                }
+            }
+        } else {
+            // beta K Gamma and beta V as MN-major [t][.] operands
+            const int tt = tid - 128;
+#pragma unroll 1
+            for (int it = 0; it < 8; ++it) {
+                const int item = tt + 128 * it, t = item >> 4, c8 = item & 15;
+                const float bt = ms.beta[t];
+                float kf[8], vf[8], o[8];
+                unpack8(*reinterpret_cast<const uint4*>(sm + OFF_K + t * 256 + c8 * 16), kf);
+                unpack8(*reinterpret_cast<const uint4*>(sm + OFF_V + t * 256 + c8 * 16), vf);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) o[j] = bt * kf[j] * ex2(G[t * KD + c8 * 8 + j] * LOG2E);
+                *reinterpret_cast<uint4*>(sm + OFF_LVL + LV_BKG + mnmaj_off(t, c8 * 8, 8192)) = pack8(o);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) o[j] = bt * vf[j];
+                *reinterpret_cast<uint4*>(sm + OFF_LVL + LV_BV + mnmaj_off(t, c8 * 8, 8192)) = pack8(o);
+            }
+        }
+        tc::fence_before_sync();
+        __syncthreads();
+        // ---------------------------------------------------------------- P4: T = (I + A)^{-1}
+        {
+            const float* Af = reinterpret_cast<const float*>(sm + OFF_LVL + LV_AF);
+            float* Tf = reinterpret_cast<float*>(sm + OFF_V);  // v tile is consumed
+            // zero the strictly upper blocks
+            for (int e = tid; e < 64 * 64; e += NT) {
+                const int t = e >> 6, i = e & 63;
+                if ((i >> 4) > (t >> 4)) Tf[e] = 0.f;
+            }
+            if (tid < 64) {
+                const int R = tid >> 4, j = tid & 15;
+                float x[16];
+#pragma unroll
+                for (int t = 0; t < 16; ++t) x[t] = (t == j) ? 1.f : 0.f;
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+#pragma unroll
+                    for (int t = i + 1; t < 16; ++t)
+                        x[t] = fmaf(-Af[(16 * R + t) * 64 + 16 * R + i], x[i], x[t]);
+#pragma unroll
+                for (int t = 0; t < 16; ++t) Tf[(16 * R + t) * 64 + 16 * R + j] = x[t];
+            }
+            __syncthreads();
+            const int r = tid >> 4, cc = tid & 15;
+#pragma unroll 1
+            for (int d = 1; d < 4; ++d) {
+                // X_RC = sum_{j=C}^{R-1} A_Rj T_jC, stored in the (R, C) block
+                for (int m = 0; m < 4 - d; ++m) {
+                    const int R = d + m, Cb = m;
+                    float s = 0.f;
+                    for (int jb = Cb; jb < R; ++jb)
+#pragma unroll
+                        for (int l = 0; l < 16; ++l)
+                            s = fmaf(Af[(16 * R + r) * 64 + 16 * jb + l],
+                                     Tf[(16 * jb + l) * 64 + 16 * Cb + cc], s);
+                    Tf[(16 * R + r) * 64 + 16 * Cb + cc] = s;
+                }
+                __syncthreads();
+                float y[3];
+                for (int m = 0; m < 4 - d; ++m) {
+                    const int R = d + m, Cb = m;
+                    float s = 0.f;
+#pragma unroll
+                    for (int l = 0; l < 16; ++l)
+                        s = fmaf(Tf[(16 * R + r) * 64 + 16 * R + l],
+                                 Tf[(16 * R + l) * 64 + 16 * Cb + cc], s);
+                    y[m] = -s;
+                }
+                __syncthreads();
+                for (int m = 0; m < 4 - d; ++m)
+                    Tf[(16 * (d + m) + r) * 64 + 16 * m + cc] = y[m];
+                __syncthreads();
+            }
+            // T -> bf16 K-major [t][i]
+            for (int it = tid; it < 64 * 8; it += NT) {
+                const int t = it >> 3, i8 = it & 7;
+                float f[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) f[j] = Tf[t * 64 + i8 * 8 + j];
+                *reinterpret_cast<uint4*>(sm + OFF_LVL + LV_TB + kmaj_off(t, i8 * 8, 64)) = pack8(f);
+            }
+        }
+        KDA_SYNC_FOR_MMA();
+        // ---------------------------------------------------------------- P5: W^T, U^T
+        if (tid == 0) {
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks) {
+                const uint64_t b = desc_k(sb + OFF_LVL + LV_TB, 64, ks);
+                tc::mma_bf16(tmem + TM_W, desc_mn(sb + OFF_LVL + LV_BKG, 8192, ks), b, IDESC_WU, ks > 0);
+                tc::mma_bf16(tmem + TM_U, desc_mn(sb + OFF_LVL + LV_BV, 8192, ks), b, IDESC_WU, ks > 0);
+            }
+            tc::mma_commit(&ms.bar_mma);
+        }
+        KDA_WAIT_MMA();
+        if (failed) break;
+        {
+            // lanes of warps 0-3: W^T row c -> [W^T | .] operand; warps 4-7: U^T row v
+            const int row = tid & 127;
+            const uint32_t col = warp < 4 ? TM_W : TM_U;
+#pragma unroll 1
+            for (int t0c = 0; t0c < 64; t0c += 16) {
+                uint32_t d[16];
+                tc::tmem_ld16(taddr(tmem, warp, col + t0c), d);
+                tc::tmem_ld_wait();
+                float lo[8], hi[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) { lo[j] = __uint_as_float(d[j]); hi[j] = __uint_as_float(d[8 + j]); }
+                if (warp < 4) {
+                    *reinterpret_cast<uint4*>(sm + OFF_A1 + mnmaj_off(row, t0c, 16384)) = pack8(lo);
+                    *reinterpret_cast<uint4*>(sm + OFF_A1 + mnmaj_off(row, t0c + 8, 16384)) = pack8(hi);
+                } else {
+                    *reinterpret_cast<uint4*>(sm + OFF_LVL + LV_UT + kmaj_off(row, t0c, 128)) = pack8(lo);
+                    *reinterpret_cast<uint4*>(sm + OFF_LVL + LV_UT + kmaj_off(row, t0c + 8, 128)) = pack8(hi);
+                }
+            }
+        }
+        KDA_SYNC_FOR_MMA();
+        // ---------------------------------------------------------------- P5: W^T M^T, U^T M^T
+        if (tid == 0) {
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks) {
+                const uint64_t b = desc_k(sb + OFF_LVL + LV_MB, 64, ks);
+                tc::mma_bf16(tmem + TM_QP, desc_k(sb + OFF_A1, 128, ks), b, IDESC_QU, ks > 0);
+                tc::mma_bf16(tmem + TM_UP, desc_k(sb + OFF_LVL + LV_UT, 128, ks), b, IDESC_QU, ks > 0);
+            }
+            tc::mma_commit(&ms.bar_mma);
+        }
+        KDA_WAIT_MMA();
+        if (failed) break;
+        if (warp < 4) {
+            // Q'^T[c][t] = q[t][c] Gamma[t][c] - (W^T M^T)[c][t]
+            const int c = tid;
+            const uint8_t* qt = sm + OFF_Q + c * 2;
+#pragma unroll 1
+            for (int t0c = 0; t0c < 64; t0c += 16) {
+                uint32_t d[16];
+                tc::tmem_ld16(taddr(tmem, warp, TM_QP + t0c), d);
+                tc::tmem_ld_wait();
+                float f[16];
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const int t = t0c + j;
+                    f[j] = bf16_at(qt + t * 256) * ex2(G[t * KD + c] * LOG2E) - __uint_as_float(d[j]);
+                }
+                float lo[8], hi[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) { lo[j] = f[j]; hi[j] = f[8 + j]; }
+                *reinterpret_cast<uint4*>(sm + OFF_A1 + mnmaj_off(c, 64 + t0c, 16384)) = pack8(lo);
+                *reinterpret_cast<uint4*>(sm + OFF_A1 + mnmaj_off(c, 64 + t0c + 8, 16384)) = pack8(hi);
+            }
+            ms.gamma_last[c] = ex2(G[63 * KD + c] * LOG2E);
+        } else {
+            // U'^T[v][t] (plain rows of 64 bf16)
+            const int v = tid - 128;
+#pragma unroll 1
+            for (int t0c = 0; t0c < 64; t0c += 16) {
+                uint32_t d[16];
+                tc::tmem_ld16(taddr(tmem, warp, TM_UP + t0c), d);
+                tc::tmem_ld_wait();
+                float lo[8], hi[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) { lo[j] = __uint_as_float(d[j]); hi[j] = __uint_as_float(d[8 + j]); }
+                *reinterpret_cast<uint4*>(sm + OFF_LVL + LV_UPT + v * 128 + t0c * 2) = pack8(lo);
+                *reinterpret_cast<uint4*>(sm + OFF_LVL + LV_UPT + v * 128 + t0c * 2 + 16) = pack8(hi);
+            }
+        }
+        // K~ = K * e^{G_last - G}, MN-major [t][c]
+        for (int it = 0; it < 4; ++it) {
+            const int item = tid + NT * it, t = item >> 4, c8 = item & 15;
+            float kf[8], o[8];
+            unpack8(*reinterpret_cast<const uint4*>(sm + OFF_K + t * 256 + c8 * 16), kf);
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                o[j] = kf[j] * ex2((G[63 * KD + c8 * 8 + j] - G[t * KD + c8 * 8 + j]) * LOG2E);
+            *reinterpret_cast<uint4*>(sm + OFF_LVL + LV_KT + mnmaj_off(t, c8 * 8, 8192)) = pack8(o);
+        }
+        KDA_SYNC_FOR_MMA();
+        // ---------------------------------------------------------------- C1: [W ; Q'] S
+        if (tid == 0) {
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks)
+                tc::mma_bf16(tmem + TM_D1, desc_mn(sb + OFF_A1, 16384, ks),
+                             desc_mn(sb + OFF_S, 16384, ks), IDESC_SQ, ks > 0);
+            tc::mma_commit(&ms.bar_mma);
+        }
+        KDA_WAIT_MMA();
+        if (failed) break;
+        // ---------------------------------------------------------------- C2
+        if (warp < 2) {
+            // Delta[t][v] = U[t][v] - (W S)[t][v]   -> MN-major [t][v] operand
+            const int t = tid;
+#pragma unroll 1
+            for (int v0 = 0; v0 < VD; v0 += 16) {
+                uint32_t d[16];
+                tc::tmem_ld16(taddr(tmem, warp, TM_D1 + v0), d);
+                tc::tmem_ld_wait();
+                float lo[8], hi[8];
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const float u = bf16_at(sm + OFF_LVL + LV_UT + kmaj_off(v0 + j, t, 128));
+                    const float x = u - __uint_as_float(d[j]);
+                    if (j < 8) lo[j] = x; else hi[j - 8] = x;
+                }
+                *reinterpret_cast<uint4*>(sm + OFF_LVL + LV_DELTA + mnmaj_off(t, v0, 8192)) = pack8(lo);
+                *reinterpret_cast<uint4*>(sm + OFF_LVL + LV_DELTA + mnmaj_off(t, v0 + 8, 8192)) = pack8(hi);
+            }
+        } else if (warp < 4) {
+            // o[t][v] = scale ((Q' S)[t][v] + U'[t][v])
+            const int t = tid - 64;
+            __nv_bfloat16* orow = out + (bh * T + t0 + t) * VD;
+#pragma unroll 1
+            for (int v0 = 0; v0 < VD; v0 += 16) {
+                uint32_t d[16];
+                tc::tmem_ld16(taddr(tmem, warp, TM_D1 + v0), d);
+                tc::tmem_ld_wait();
+                float lo[8], hi[8];
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const float up = bf16_at(sm + OFF_LVL + LV_UPT + (v0 + j) * 128 + t * 2);
+                    const float x = scale * (__uint_as_float(d[j]) + up);
+                    if (j < 8) lo[j] = x; else hi[j - 8] = x;
+                }
+                if (t < cn) {
+                    *reinterpret_cast<uint4*>(orow + v0) = pack8(lo);
+                    *reinterpret_cast<uint4*>(orow + v0 + 8) = pack8(hi);
+                }
+            }
+        } else {
+            // S <- diag(Gamma_last) S in TMEM (lane c)
+            const int c = tid - 128;
+            const float gl = ms.gamma_last[c];
+#pragma unroll 1
+            for (int v0 = 0; v0 < VD; v0 += 16) {
+                uint32_t d[16];
+                tc::tmem_ld16(taddr(tmem, warp, TM_S + v0), d);
+                tc::tmem_ld_wait();
+#pragma unroll
+                for (int j = 0; j < 16; ++j) d[j] = __float_as_uint(__uint_as_float(d[j]) * gl);
+                tc::tmem_st16(taddr(tmem, warp, TM_S + v0), d);
+            }
+            tc::tmem_st_wait();
+        }
+        KDA_SYNC_FOR_MMA();
+        // ---------------------------------------------------------------- C3: S += K~^T Delta
+        if (tid == 0) {
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks)
+                tc::mma_bf16(tmem + TM_S, desc_mn(sb + OFF_LVL + LV_KT, 8192, ks),
+                             desc_mn(sb + OFF_LVL + LV_DELTA, 8192, ks), IDESC_SQ, 1u);
+            tc::mma_commit(&ms.bar_mma);
+        }
+        KDA_WAIT_MMA();
+        if (failed) break;
+        if (warp < 4) {
+            const int c = tid;
+#pragma unroll 1
+            for (int v0 = 0; v0 < VD; v0 += 16) {
+                uint32_t d[16];
+                tc::tmem_ld16(taddr(tmem, warp, TM_S + v0), d);
+                tc::tmem_ld_wait();
+                float lo[8], hi[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) { lo[j] = __uint_as_float(d[j]); hi[j] = __uint_as_float(d[8 + j]); }
+                *reinterpret_cast<uint4*>(sm + OFF_S + mnmaj_off(c, v0, 16384)) = pack8(lo);
+                *reinterpret_cast<uint4*>(sm + OFF_S + mnmaj_off(c, v0 + 8, 16384)) = pack8(hi);
+            }
+        }
+        KDA_SYNC_FOR_MMA();
+    }
+#undef KDA_WAIT_MMA
+#undef KDA_SYNC_FOR_MMA
+
+    if (!failed && hT && tid < KD) {
+        const int c = tid;
+#pragma unroll 1
+        for (int v0 = 0; v0 < VD; v0 += 16) {
+            uint32_t d[16];
+            tc::tmem_ld16(taddr(tmem, warp, TM_S + v0), d);
+            tc::tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < 16; j += 4)
+                *reinterpret_cast<float4*>(hT + (bh * KD + c) * VD + v0 + j) =
+                    make_float4(__uint_as_float(d[j]), __uint_as_float(d[j + 1]),
+                                __uint_as_float(d[j + 2]), __uint_as_float(d[j + 3]));
+        }
+    }
+    if (failed && tid == 0) {
+        atomicExch(&g_kda_tc_timeout, 1);
+        // give any tensor-core work still in flight a bounded chance to finish
+        tc::mbar_wait(&ms.bar_mma, mma_phase, 200000000ull);
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 0) tc::tmem_dealloc(tmem, 512);
+}
+
+namespace {
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    // The driver entry point is looked up once through the runtime (no -lcuda link).
+    static EncodeTiledFn fn = []() -> EncodeTiledFn {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return nullptr;
+        return reinterpret_cast<EncodeTiledFn>(p);
+    }();
+    return fn;
+}
+
+// 3-D view (channel, token, b*h) of a (B, H, T, 128) bf16 tensor; 64 x 128 tiles, no swizzle.
+bool make_tile_map(CUtensorMap* map, const void* base, int T, int BH) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return false;
+    cuuint64_t dims[3] = {128, (cuuint64_t)T, (cuuint64_t)BH};
+    cuuint64_t strides[2] = {128 * 2, (cuuint64_t)T * 128 * 2};
+    cuuint32_t box[3] = {128, 64, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
+               box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
 cudaError_t launch_chunk_tc(const ChunkArgs& a, cudaStream_t s, bool* taken) {
-    (void)a;
-    (void)s;
     *taken = false;
-    return cudaSuccess;
+    if (a.io != KDA_BF16 || a.K != 128 || a.V != 128 || a.chunk != 64 || a.T <= 0) return cudaSuccess;
+    *taken = true;
+    const int BH = a.B * a.H;
+    CUtensorMap mq, mk, mv, mz;
+    if (!make_tile_map(&mq, a.q, a.T, BH) || !make_tile_map(&mk, a.k, a.T, BH) ||
+        !make_tile_map(&mv, a.v, a.T, BH) || !make_tile_map(&mz, a.z, a.T, BH))
+        return cudaErrorInvalidValue;
+    cudaError_t err = cudaFuncSetAttribute(kda_chunk_tc_kernel,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           (int)SMEM_BYTES);
+    if (err != cudaSuccess) return err;
+    kda_chunk_tc_kernel<<<BH, NT, SMEM_BYTES, s>>>(
+        mq, mk, mv, mz, a.H, a.T, (const __nv_bfloat16*)a.beta, a.A_log, a.dt_bias, a.scale, a.h0,
+        (__nv_bfloat16*)a.out, a.hT);
+    count_launches(1);
+    return cudaGetLastError();
 }
 
 }  // namespace kda
