@@ -234,6 +234,9 @@ def main():
                     help="decode batch B (default: the decode workload's 256)")
     ap.add_argument("--only", default="all", choices=["all", "prefill", "decode"],
                     help="time only one of the two workloads (for profiler captures)")
+    ap.add_argument("--prefill-T", type=int, default=None,
+                    help="sequence length of the prefill workload (default 4096; smaller for "
+                         "profiler captures)")
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)
@@ -260,7 +263,7 @@ def main():
         if rank == 0:
             print(json.dumps({"metric": "decode only", "decode": decode}), flush=True)
         return 0
-    inp_cpu = inputs.workload(WORKLOAD)
+    inp_cpu = inputs.workload(WORKLOAD, **({"T": args.prefill_T} if args.prefill_T else {}))
     B, H, T, K, V, C = inp_cpu.B, inp_cpu.H, inp_cpu.T, inp_cpu.K, inp_cpu.V, inp_cpu.chunk
     d = inp_cpu.to("cuda")
     stream = torch.cuda.current_stream()
@@ -304,6 +307,13 @@ def main():
                 "peak_source": peaks["source"]}
     tflops = flops / per_step / 1e12
 
+    if args.only == "prefill":
+        line = {"metric": METRIC, "value": value, "unit": "tokens/s", "ms_per_step": per_step * 1e3,
+                "config": {"workload": f"{WORKLOAD} B{B} H{H} T{T}"}, "roofline": roofline,
+                "gpu_launches": launches}
+        if rank == 0:
+            print(json.dumps(line), flush=True)
+        return 0
     # ---- end to end through the public API: pinned host inputs -> device -> forward -> host
     host = {n: getattr(inp_cpu, n).pin_memory() for n in ("q", "k", "v", "z", "beta", "A_log",
                                                          "dt_bias")}

@@ -10,12 +10,15 @@
 // over S, so S is read once and written once: 2 * K * V * 4 bytes per (b, h),
 // the HBM floor of this step.
 //
-// Layout: one CTA of 256 threads (8 warps) per (b, h).  Lane l owns the four
-// value columns [4l, 4l + 4) (one float4; a warp covers a whole 512-byte row,
-// fully coalesced), warp w owns the key rows [w * R, (w + 1) * R) with
-// R = ceil(K / 8) <= 16, so a thread keeps at most 16 float4 of S in registers
-// between the read and the write.  The per-column partial sums of the eight
-// warps are combined through shared memory; k . q is a warp-shuffle reduction.
+// Layout: the value columns of S are independent, so each (b, h) is split into
+// two CTAs of 256 threads (8 warps), one per half of the V columns.  Lane l owns
+// the two columns [2l, 2l + 2) of its half (one float2; a warp covers 256
+// contiguous bytes of a row, fully coalesced), warp w owns the key rows
+// [w * R, (w + 1) * R) with R = ceil(K / 8) <= 16, so a thread keeps at most 16
+// float2 of S in registers between the read and the write.  The small register
+// footprint lets four CTAs share an SM, so one CTA's reads overlap another's
+// writes.  The per-column partial sums of the eight warps are combined through
+// shared memory; k . q is a warp-shuffle reduction.
 // State loads and stores use the streaming cache hints (the state is larger
 // than L2 and touched once per step).
 #include "common.cuh"
@@ -27,44 +30,41 @@ constexpr int kDecodeThreads = 256;
 constexpr int kDecodeWarps = kDecodeThreads / 32;
 constexpr int kMaxRowsPerWarp = 16;  // K <= 128
 
-__device__ __forceinline__ float4 f4_scale(float4 a, float s) {
-    return make_float4(a.x * s, a.y * s, a.z * s, a.w * s);
+__device__ __forceinline__ float2 f2_scale(float2 a, float s) { return make_float2(a.x * s, a.y * s); }
+__device__ __forceinline__ float2 f2_fma(float2 a, float s, float2 c) {
+    return make_float2(fmaf(a.x, s, c.x), fmaf(a.y, s, c.y));
 }
-__device__ __forceinline__ float4 f4_fma(float4 a, float s, float4 c) {
-    return make_float4(fmaf(a.x, s, c.x), fmaf(a.y, s, c.y), fmaf(a.z, s, c.z), fmaf(a.w, s, c.w));
-}
-__device__ __forceinline__ float4 f4_add(float4 a, float4 b) {
-    return make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w);
-}
+__device__ __forceinline__ float2 f2_add(float2 a, float2 b) { return make_float2(a.x + b.x, a.y + b.y); }
 }  // namespace
 
 template <typename IO>
-__global__ void __launch_bounds__(kDecodeThreads, 2)
+__global__ void __launch_bounds__(kDecodeThreads, 4)
     decode_kernel(int H, int K, int V, const IO* __restrict__ q, const IO* __restrict__ k,
                   const IO* __restrict__ v, const IO* __restrict__ z, const IO* __restrict__ beta,
                   const float* __restrict__ A_log, const float* __restrict__ dt_bias, float scale,
                   float* __restrict__ state, IO* __restrict__ out) {
-    __shared__ float s_k[128], s_q[128], s_alpha[128], s_v[128];
-    __shared__ float4 s_red_k[kDecodeWarps][32], s_red_q[kDecodeWarps][32];
+    __shared__ float s_k[128], s_q[128], s_alpha[128], s_v[64];
+    __shared__ float2 s_red_k[kDecodeWarps][32], s_red_q[kDecodeWarps][32];
     __shared__ float s_kq;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const size_t bh = blockIdx.x;
+    const size_t bh = blockIdx.x >> 1;
     const int h = (int)(bh % H);
+    const int Vh = V >> 1, j0 = (blockIdx.x & 1) * Vh;  // this CTA's half of the columns
     const int rows = (K + kDecodeWarps - 1) / kDecodeWarps;
     const int r0 = warp * rows;
-    const bool col_ok = lane * 4 < V;
-    float* S = state + bh * (size_t)K * V;
+    const bool col_ok = lane * 2 < Vh;
+    float* S = state + bh * (size_t)K * V + j0;
 
     // Issue the state loads first: they are the long-latency part of the step.
-    float4 s[kMaxRowsPerWarp];
+    float2 s[kMaxRowsPerWarp];
 #pragma unroll
     for (int i = 0; i < kMaxRowsPerWarp; ++i) {
         const int r = r0 + i;
         if (i < rows && r < K && col_ok)
-            s[i] = __ldcs(reinterpret_cast<const float4*>(S + (size_t)r * V + lane * 4));
+            s[i] = __ldcs(reinterpret_cast<const float2*>(S + (size_t)r * V + lane * 2));
         else
-            s[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+            s[i] = make_float2(0.f, 0.f);
     }
 
     if (tid < K) {
@@ -74,7 +74,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 2)
         s_k[tid] = ld_io(k + idx);
         s_q[tid] = scale * ld_io(q + idx);  // the read scale is folded into q
     }
-    if (tid < V) s_v[tid] = ld_io(v + bh * V + tid);
+    if (tid < Vh) s_v[tid] = ld_io(v + bh * V + j0 + tid);
     const float b = ld_io(beta + bh);
     __syncthreads();
 
@@ -87,50 +87,45 @@ __global__ void __launch_bounds__(kDecodeThreads, 2)
     }
 
     // S' = diag(alpha) S and the two partial column reductions of this warp's rows.
-    float4 pk = make_float4(0.f, 0.f, 0.f, 0.f), pq = pk;
+    float2 pk = make_float2(0.f, 0.f), pq = pk;
 #pragma unroll
     for (int i = 0; i < kMaxRowsPerWarp; ++i) {
         const int r = r0 + i;
         if (i < rows && r < K) {
-            s[i] = f4_scale(s[i], s_alpha[r]);
-            pk = f4_fma(s[i], s_k[r], pk);
-            pq = f4_fma(s[i], s_q[r], pq);
+            s[i] = f2_scale(s[i], s_alpha[r]);
+            pk = f2_fma(s[i], s_k[r], pk);
+            pq = f2_fma(s[i], s_q[r], pq);
         }
     }
     s_red_k[warp][lane] = pk;
     s_red_q[warp][lane] = pq;
     __syncthreads();
 
-    float4 tk = s_red_k[0][lane], tq = s_red_q[0][lane];
+    float2 tk = s_red_k[0][lane], tq = s_red_q[0][lane];
 #pragma unroll
     for (int w = 1; w < kDecodeWarps; ++w) {
-        tk = f4_add(tk, s_red_k[w][lane]);
-        tq = f4_add(tq, s_red_q[w][lane]);
+        tk = f2_add(tk, s_red_k[w][lane]);
+        tq = f2_add(tq, s_red_q[w][lane]);
     }
     if (!col_ok) return;
-    const float4 vv = *reinterpret_cast<const float4*>(&s_v[lane * 4]);
-    const float4 u = make_float4(vv.x - tk.x, vv.y - tk.y, vv.z - tk.z, vv.w - tk.w);
-    const float4 bu = f4_scale(u, b);
+    const float2 bu = make_float2(b * (s_v[lane * 2] - tk.x), b * (s_v[lane * 2 + 1] - tk.y));
 
 #pragma unroll
     for (int i = 0; i < kMaxRowsPerWarp; ++i) {
         const int r = r0 + i;
         if (i < rows && r < K)
-            __stcs(reinterpret_cast<float4*>(S + (size_t)r * V + lane * 4), f4_fma(bu, s_k[r], s[i]));
+            __stcs(reinterpret_cast<float2*>(S + (size_t)r * V + lane * 2), f2_fma(bu, s_k[r], s[i]));
     }
     if (warp == 0) {
-        const float kq = s_kq;
-        const float4 o = f4_fma(bu, kq, tq);
-        IO* op = out + bh * V + lane * 4;
+        const float2 o = f2_fma(bu, s_kq, tq);
+        IO* op = out + bh * V + j0 + lane * 2;
         st_io(op + 0, o.x);
         st_io(op + 1, o.y);
-        st_io(op + 2, o.z);
-        st_io(op + 3, o.w);
     }
 }
 
 cudaError_t launch_decode(const StepArgs& a, cudaStream_t s) {
-    const unsigned grid = (unsigned)(a.B * a.H);
+    const unsigned grid = (unsigned)(a.B * a.H) * 2u;
     if (a.io == KDA_BF16)
         decode_kernel<__nv_bfloat16><<<grid, kDecodeThreads, 0, s>>>(
             a.H, a.K, a.V, (const __nv_bfloat16*)a.q, (const __nv_bfloat16*)a.k,
