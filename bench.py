@@ -103,10 +103,8 @@ class ClockSampler:
 
 
 def dist_env():
-    ws = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    return ws, rank, local
+    from gated_delta_rule_26_gb300 import dist as kdist
+    return kdist.env()
 
 
 def timed(fn, steps, stream, events=True):
@@ -208,6 +206,8 @@ def run_decode(args, kda, inputs, peaks, ws, barrier):
         dstep()
     barrier()
     dsecs = timed(dstep, dec.steps, stream)
+    from gated_delta_rule_26_gb300 import dist as kdist
+    dsecs = kdist.max_over_ranks(dsecs, device="cuda")
     dper = dsecs / dec.steps
     dbytes = 2 * dec.B * dec.H * dec.K * dec.V * 4 + dec.B * dec.H * (3 * dec.K + 2 * dec.V + 1) * 2
     decode = {"value": ws * dec.B / dper, "unit": "tokens/s", "us_per_step": dper * 1e6,
@@ -253,9 +253,10 @@ def main():
     kbuild.build()
     from gated_delta_rule_26_gb300 import inputs, kda
 
+    from gated_delta_rule_26_gb300 import dist as kdist
+
     def barrier():
-        if ws > 1:
-            torch.distributed.barrier()
+        kdist.barrier()
 
     peaks = load_peaks()
     if args.only == "decode":
@@ -286,10 +287,7 @@ def main():
     launches = kda.launch_count() - n0
     clocks = sampler.stop()
     barrier()
-    if ws > 1:
-        t = torch.tensor([secs], device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        secs = float(t.item())
+    secs = kdist.max_over_ranks(secs, device="cuda")
     per_step = secs / args.steps
     tokens = B * T
     token_heads = B * H * T
@@ -336,10 +334,7 @@ def main():
     e2e_steps = max(3, min(args.steps, 10))
     barrier()
     e2e_secs = timed(e2e_step, e2e_steps, stream)
-    if ws > 1:
-        t = torch.tensor([e2e_secs], device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_secs = float(t.item())
+    e2e_secs = kdist.max_over_ranks(e2e_secs, device="cuda")
     e2e = {"value": ws * tokens / (e2e_secs / e2e_steps), "unit": "tokens/s",
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
     del host, dev, out_h, hT_h

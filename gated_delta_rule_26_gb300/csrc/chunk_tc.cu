@@ -4,7 +4,8 @@
 // One CTA (8 warps) owns one (b, h) sequence and walks its chunks in order.
 // The fp32 state S (K x V) lives in TMEM for the whole sequence; per chunk:
 //
-//   P1  TMA: q, k, v, z tiles (64 x 128 bf16 each) into shared memory.
+//   P1  TMA: q, k, v, z tiles (64 x 128 bf16 each) into shared memory; the
+//       next chunk's tiles are requested as soon as this chunk's are consumed.
 //   P2  gate g = -exp(A_log) softplus(z + dt_bias) and the in-chunk cumulative
 //       log decay G (kdafix-2026-10-02 "Fix 1"; kda-adjoint-2026-10-01 sec. 2).
 //   P3  decay-folded scores  A[t,i] = beta_t sum_c k_tc k_ic e^{G_tc - G_ic}  (i < t)
@@ -18,15 +19,18 @@
 //       <= 1.  Four levels (h = 32, 16, 8, 4) are four GEMMs of scaled operands
 //       (M = 128: k rows then q rows; N = 64; K = 128); pairs inside a 4-token
 //       block take the exact pairwise exponential on CUDA cores.
-//   P4  T = (I + A)^{-1} by blocked forward substitution (16 x 16 diagonal
-//       blocks, then the off-diagonal blocks), fp32 on CUDA cores.
+//   P4  T = (I + A)^{-1}: 16 x 16 diagonal blocks by forward substitution,
+//       then two block merges (16 -> 32 -> 64, T_21 = -T_22 A_21 T_11), fp32 on
+//       CUDA cores.
 //   P5  W^T = (diag(beta) K Gamma)^T T^T and U^T = (diag(beta) V)^T T^T  (tcgen05),
-//       then Q'^T = (Q Gamma)^T - W^T M^T and U'^T = U^T M^T  (tcgen05), so that
+//       then Q'^T = (Q Gamma)^T I - W^T M^T (identity and negated-B MMAs) and
+//       U'^T = U^T M^T  (tcgen05), so that
 //       o = scale (Q' S + U') and Delta = U - W S both come from ONE product with S.
-//   C1  D = [W ; Q'] S     (M = 128, N = 128, K = 128; S as bf16 operand).
-//   C2  Delta = U - D[0:64]; o = scale (D[64:128] + U')  -> bf16 to HBM.
-//       Meanwhile the fp32 state in TMEM is scaled by Gamma_last (row c by
-//       e^{G_last,c}).
+//   C1  D = S^T [W^T | Q'^T] = [(W S)^T | (Q' S)^T]  (M = 128 value channels,
+//       N = 128, K = 128; S as bf16 operand).  Before it, the fp32 state in
+//       TMEM is scaled by Gamma_last (row c by e^{G_last,c}).
+//   C2  from TMEM, one value channel per thread: Delta^T = U^T - (W S)^T and
+//       o = scale ((Q' S)^T + U'^T)^T -> bf16 to HBM.
 //   C3  S += (K * e^{G_last - G})^T Delta   accumulated in TMEM in fp32
 //       (the carry with a single exponential of the log-space difference,
 //       kda-adjoint-2026-10-01 sections 2 and 5b), then S -> bf16 operand.
@@ -37,6 +41,7 @@
 // Every mbarrier wait is bounded; on a timeout the CTA records it in
 // g_kda_tc_timeout, releases its TMEM and exits.
 #include <cuda.h>
+#include <stddef.h>
 
 #include "common.cuh"
 #include "tc_ptx.cuh"
@@ -58,7 +63,8 @@ constexpr uint32_t OFF_K = OFF_Q + 16384;       // 16 KB bf16 k tile
 constexpr uint32_t OFF_V = OFF_K + 16384;       // 16 KB bf16 v tile, later T fp32 [t][i]
 constexpr uint32_t OFF_A1 = OFF_V + 16384;      // 32 KB [W^T | Q'^T], MN-major (2 atoms)
 constexpr uint32_t OFF_S = OFF_A1 + 32768;      // 32 KB S bf16, MN-major [c][v] (2 atoms)
-constexpr uint32_t OFF_MISC = OFF_S + 32768;
+constexpr uint32_t OFF_ID = OFF_S + 32768;      // 8 KB 64 x 64 identity, K-major bf16
+constexpr uint32_t OFF_MISC = OFF_ID + 8192;
 // multi-use region, in order of use within a chunk
 constexpr uint32_t LV_Z = 0;        // z tile (16 KB)                    P1-P2
 constexpr uint32_t LV_L0 = 0;       // level operand buffer 0 (32 KB)    P3
@@ -68,35 +74,39 @@ constexpr uint32_t LV_MB = 16384;   // M bf16 K-major [t][i] (8 KB)      P3-P5
 constexpr uint32_t LV_TB = 24576;   // T bf16 K-major [t][i] (8 KB)      P4-P5
 constexpr uint32_t LV_BKG = 32768;  // beta K Gamma, MN-major [t][c]     P3-P5
 constexpr uint32_t LV_BV = 49152;   // beta V, MN-major [t][v]           P3-P5
-constexpr uint32_t LV_UT = 0;       // U^T K-major [v][i] (16 KB)        P5-C2
-constexpr uint32_t LV_UPT = 32768;  // U'^T plain [v][t] (16 KB)         P5-C2
+constexpr uint32_t LV_UT = 0;       // U^T K-major [v][i] (16 KB)        P5
+constexpr uint32_t LV_QG = 32768;   // Q Gamma, MN-major [t][c] (16 KB)  P5
 constexpr uint32_t LV_KT = 49152;   // K~ MN-major [t][c] (16 KB)        P5-C3
-constexpr uint32_t LV_DELTA = 16384;// Delta MN-major [t][v] (16 KB)     C2-C3
+constexpr uint32_t LV_DELTA = 16384;// Delta^T K-major [v][t] (16 KB)    C2-C3
 
 struct Misc {
-    uint64_t bar_tma, bar_mma;
+    alignas(16) float dt[KD];      // read as float4
+    alignas(16) float beta[C];
+    alignas(16) float diag[16][16];
+    alignas(16) uint64_t bar_tma;
+    uint64_t bar_mma;
     uint32_t tmem_base;
-    int pad;
-    float beta[C];
-    float gamma_last[KD];
-    float dt[KD];
-    float diag[16][16];
 };
+static_assert(offsetof(Misc, dt) % 16 == 0 && offsetof(Misc, beta) % 16 == 0 &&
+                  offsetof(Misc, bar_tma) % 8 == 0 && OFF_MISC % 16 == 0,
+              "shared-memory block alignment");
 constexpr uint32_t SMEM_BYTES = OFF_MISC + sizeof(Misc) + 1024;
 
 // ---- TMEM columns (512 allocated)
 constexpr uint32_t TM_S = 0;      // fp32 state, lanes = key channel c, cols = v   (128)
 constexpr uint32_t TM_LVL = 128;  // four level score tiles                        (4 x 64)
-constexpr uint32_t TM_QP = 128;   // W^T M^T                                       (64)
-constexpr uint32_t TM_UP = 192;   // U^T M^T                                       (64)
-constexpr uint32_t TM_D1 = 256;   // [W ; Q'] S                                    (128)
+constexpr uint32_t TM_QP = 128;   // Q'^T = (Q Gamma)^T - W^T M^T                  (64)
+constexpr uint32_t TM_UP = 192;   // U'^T = U^T M^T                                (64)
+constexpr uint32_t TM_D1 = 256;   // S^T [W^T | Q'^T]                              (128)
 constexpr uint32_t TM_W = 384;    // W^T                                           (64)
 constexpr uint32_t TM_U = 448;    // U^T                                           (64)
 
 constexpr uint32_t IDESC_LVL = tc::idesc_bf16(128, 64, 0, 0);
 constexpr uint32_t IDESC_WU = tc::idesc_bf16(128, 64, 1, 0);
 constexpr uint32_t IDESC_QU = tc::idesc_bf16(128, 64, 0, 0);
+constexpr uint32_t IDESC_QNEG = tc::idesc_bf16(128, 64, 0, 0) | (1u << 14);  // negate B
 constexpr uint32_t IDESC_SQ = tc::idesc_bf16(128, 128, 1, 1);
+constexpr uint32_t IDESC_SK = tc::idesc_bf16(128, 128, 1, 0);
 
 __device__ __forceinline__ float ex2(float x) {
     float y;
@@ -113,8 +123,14 @@ __device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
     return make_uint4(tc::pack_bf16x2(f[0], f[1]), tc::pack_bf16x2(f[2], f[3]),
                       tc::pack_bf16x2(f[4], f[5]), tc::pack_bf16x2(f[6], f[7]));
 }
-__device__ __forceinline__ float bf16_at(const uint8_t* p) {
-    return __uint_as_float(((uint32_t) * reinterpret_cast<const uint16_t*>(p)) << 16);
+__device__ __forceinline__ void load8(const float* p, float (&f)[8]) {
+    const float4 a = *reinterpret_cast<const float4*>(p);
+    const float4 b = *reinterpret_cast<const float4*>(p + 4);
+    f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w; f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
+}
+// softplus(x) = max(x, 0) + log(1 + e^{-|x|}) with the hardware exp2/log2 approximations.
+__device__ __forceinline__ float softplus_fast(float x) {
+    return fmaxf(x, 0.f) + __logf(1.f + __expf(-fabsf(x)));
 }
 
 // K-major tile with `rows` rows: byte offset of element (row, k); k atoms of 64.
@@ -124,6 +140,21 @@ __device__ __forceinline__ uint32_t kmaj_off(int row, int k, int rows) {
 // MN-major tile: element (krow, mn), MN atoms of 64 elements `atom` bytes apart.
 __device__ __forceinline__ uint32_t mnmaj_off(int krow, int mn, uint32_t atom) {
     return (uint32_t)(mn >> 6) * atom + tc::sw128_offset(krow, (mn & 63) >> 3) + (mn & 7) * 2;
+}
+// 16 consecutive elements (two 16-byte chunks) of one row of a K-major / MN-major tile.
+__device__ __forceinline__ void store16_k(uint8_t* base, int row, int k0, int rows, const float (&f)[16]) {
+    float lo[8], hi[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) { lo[j] = f[j]; hi[j] = f[8 + j]; }
+    *reinterpret_cast<uint4*>(base + kmaj_off(row, k0, rows)) = pack8(lo);
+    *reinterpret_cast<uint4*>(base + kmaj_off(row, k0 + 8, rows)) = pack8(hi);
+}
+__device__ __forceinline__ void store16_mn(uint8_t* base, int krow, int mn0, uint32_t atom, const float (&f)[16]) {
+    float lo[8], hi[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) { lo[j] = f[j]; hi[j] = f[8 + j]; }
+    *reinterpret_cast<uint4*>(base + mnmaj_off(krow, mn0, atom)) = pack8(lo);
+    *reinterpret_cast<uint4*>(base + mnmaj_off(krow, mn0 + 8, atom)) = pack8(hi);
 }
 __device__ __forceinline__ uint64_t desc_k(uint32_t saddr, int rows, int ks) {
     const int k0 = ks * 16;
@@ -137,9 +168,10 @@ __device__ __forceinline__ uint32_t taddr(uint32_t base, int warp, uint32_t col)
 }
 
 // Build two levels' operands: rows 0..63 hold k_t scaled to the level's reference,
-// rows 64..127 hold q_t scaled (upper-half tokens only).
+// rows 64..127 hold q_t scaled (upper-half tokens only).  G2 is the in-chunk
+// cumulative log decay in log2 units, so every factor is one ex2 of a difference <= 0.
 __device__ __forceinline__ void build_levels(uint8_t* sm, int li0, int tid) {
-    const float* G = reinterpret_cast<const float*>(sm + OFF_G);
+    const float* G2 = reinterpret_cast<const float*>(sm + OFF_G);
     const int c8 = tid & 15;
 #pragma unroll 1
     for (int r = 0; r < 4; ++r) {
@@ -147,31 +179,33 @@ __device__ __forceinline__ void build_levels(uint8_t* sm, int li0, int tid) {
         float kf[8], qf[8], g8[8];
         unpack8(*reinterpret_cast<const uint4*>(sm + OFF_K + t * 256 + c8 * 16), kf);
         unpack8(*reinterpret_cast<const uint4*>(sm + OFF_Q + t * 256 + c8 * 16), qf);
-        const float4 ga = *reinterpret_cast<const float4*>(G + t * KD + c8 * 8);
-        const float4 gb = *reinterpret_cast<const float4*>(G + t * KD + c8 * 8 + 4);
-        g8[0] = ga.x; g8[1] = ga.y; g8[2] = ga.z; g8[3] = ga.w;
-        g8[4] = gb.x; g8[5] = gb.y; g8[6] = gb.z; g8[7] = gb.w;
+        load8(G2 + t * KD + c8 * 8, g8);
 #pragma unroll
         for (int l = 0; l < 2; ++l) {
             const int li = li0 + l;
             const int h = 32 >> li;
             const int ref = (t & ~(2 * h - 1)) + h - 1;
             const bool upper = (t & h) != 0;
-            const float4 ra = *reinterpret_cast<const float4*>(G + ref * KD + c8 * 8);
-            const float4 rb = *reinterpret_cast<const float4*>(G + ref * KD + c8 * 8 + 4);
-            const float r8[8] = {ra.x, ra.y, ra.z, ra.w, rb.x, rb.y, rb.z, rb.w};
-            float f[8], kv[8], qv[8];
+            float r8[8], kv[8], qv[8];
+            load8(G2 + ref * KD + c8 * 8, r8);
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
-                f[j] = ex2((upper ? g8[j] - r8[j] : r8[j] - g8[j]) * LOG2E);
-                kv[j] = kf[j] * f[j];
-                qv[j] = qf[j] * f[j];
+                const float f = ex2(upper ? g8[j] - r8[j] : r8[j] - g8[j]);
+                kv[j] = kf[j] * f;
+                qv[j] = qf[j] * f;
             }
             uint8_t* L = sm + OFF_LVL + (l ? LV_L1 : LV_L0);
             *reinterpret_cast<uint4*>(L + kmaj_off(t, c8 * 8, 128)) = pack8(kv);
             if (upper) *reinterpret_cast<uint4*>(L + kmaj_off(64 + t, c8 * 8, 128)) = pack8(qv);
         }
     }
+}
+
+// Float index of element (t, i) of a 64 x 64 fp32 matrix whose 16-byte column groups are
+// XOR-swizzled by the row, so that row-wise and column-wise float4 accesses by
+// consecutive threads fall into distinct banks.
+__device__ __forceinline__ int swz(int t, int i) {
+    return t * 64 + ((((i >> 2) ^ (t & 15))) << 2) + (i & 3);
 }
 
 }  // namespace
@@ -190,7 +224,7 @@ __global__ void __launch_bounds__(NT, 1)
                                              ~static_cast<uintptr_t>(1023));
     const uint32_t sb = tc::smem_u32(sm);
     Misc& ms = *reinterpret_cast<Misc*>(sm + OFF_MISC);
-    float* G = reinterpret_cast<float*>(sm + OFF_G);
+    float* G2 = reinterpret_cast<float*>(sm + OFF_G);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const size_t bh = blockIdx.x;
     const int h = (int)(bh % H);
@@ -217,6 +251,8 @@ __global__ void __launch_bounds__(NT, 1)
     tc::fence_after_sync();
     const uint32_t tmem = ms.tmem_base;
 
+    // 64 x 64 identity, K-major bf16: the B operand that copies (Q Gamma)^T into an accumulator
+    if (tid < 64) *reinterpret_cast<uint16_t*>(sm + OFF_ID + kmaj_off(tid, tid, 64)) = 0x3F80u;
     // Initial state: fp32 into TMEM (lane c), bf16 copy as the MN-major operand [c][v].
     if (tid < KD) {
         const int c = tid;
@@ -233,11 +269,7 @@ __global__ void __launch_bounds__(NT, 1)
 #pragma unroll
             for (int j = 0; j < 16; ++j) r[j] = __float_as_uint(f[j]);
             tc::tmem_st16(taddr(tmem, warp, TM_S + v0), r);
-            float lo[8], hi[8];
-#pragma unroll
-            for (int j = 0; j < 8; ++j) { lo[j] = f[j]; hi[j] = f[8 + j]; }
-            *reinterpret_cast<uint4*>(sm + OFF_S + mnmaj_off(c, v0, 16384)) = pack8(lo);
-            *reinterpret_cast<uint4*>(sm + OFF_S + mnmaj_off(c, v0 + 8, 16384)) = pack8(hi);
+            store16_mn(sm + OFF_S, c, v0, 16384, f);
         }
         tc::tmem_st_wait();
     }
@@ -249,6 +281,13 @@ __global__ void __launch_bounds__(NT, 1)
     uint32_t tma_phase = 0, mma_phase = 0;
     bool failed = false;
     const int nchunks = (T + C - 1) / C;
+    if (tid == 0 && nchunks > 0) {
+        tc::mbar_arrive_expect_tx(&ms.bar_tma, 4u * 16384u);
+        tc::tma_load_3d(sm + OFF_Q, &tm_q, 0, 0, (int)bh, &ms.bar_tma);
+        tc::tma_load_3d(sm + OFF_K, &tm_k, 0, 0, (int)bh, &ms.bar_tma);
+        tc::tma_load_3d(sm + OFF_V, &tm_v, 0, 0, (int)bh, &ms.bar_tma);
+        tc::tma_load_3d(sm + OFF_LVL + LV_Z, &tm_z, 0, 0, (int)bh, &ms.bar_tma);
+    }
 
 #define KDA_WAIT_MMA()                                                   \
     do {                                                                 \
@@ -268,13 +307,7 @@ __global__ void __launch_bounds__(NT, 1)
     for (int n = 0; n < nchunks && !failed; ++n) {
         const int t0 = n * C, cn = min(C, T - t0);
         // ---------------------------------------------------------------- P1
-        if (tid == 0) {
-            tc::mbar_arrive_expect_tx(&ms.bar_tma, 4u * 16384u);
-            tc::tma_load_3d(sm + OFF_Q, &tm_q, 0, t0, (int)bh, &ms.bar_tma);
-            tc::tma_load_3d(sm + OFF_K, &tm_k, 0, t0, (int)bh, &ms.bar_tma);
-            tc::tma_load_3d(sm + OFF_V, &tm_v, 0, t0, (int)bh, &ms.bar_tma);
-            tc::tma_load_3d(sm + OFF_LVL + LV_Z, &tm_z, 0, t0, (int)bh, &ms.bar_tma);
-        }
+        // (this chunk's tiles were requested by the previous chunk, or above for chunk 0)
         if (tid < C)
             ms.beta[tid] = tid < cn ? __bfloat162float(beta[bh * T + t0 + tid]) : 0.f;
         {
@@ -284,24 +317,40 @@ __global__ void __launch_bounds__(NT, 1)
         }
         // ---------------------------------------------------------------- P2
         {
-            const int c = tid & 127, half = tid >> 7;
-            const float dt = ms.dt[c];
-            const uint8_t* zt = sm + OFF_LVL + LV_Z;
-            float acc = 0.f;
-#pragma unroll 4
-            for (int t = half * 32; t < half * 32 + 32; ++t) {
-                const float x = bf16_at(zt + t * 256 + c * 2) + dt;
-                const float sp = fmaxf(x, 0.f) + __logf(1.f + __expf(-fabsf(x)));
-                acc += (t < cn) ? -(exp_A * sp) : 0.f;
-                G[t * KD + c] = acc;
+            // warp w: tokens 8w..8w+7; lane: channels 4*lane..4*lane+3 (G2 in log2 units)
+            const int c4 = lane * 4;
+            const float4 dt = *reinterpret_cast<const float4*>(&ms.dt[c4]);
+            const float mult = -exp_A * LOG2E;
+            float acc0 = 0.f, acc1 = 0.f, acc2 = 0.f, acc3 = 0.f;
+#pragma unroll
+            for (int a = 0; a < 8; ++a) {
+                const int t = 8 * warp + a;
+                const uint2 zr = *reinterpret_cast<const uint2*>(sm + OFF_LVL + LV_Z + t * 256 + c4 * 2);
+                const float x0 = bf_lo(zr.x) + dt.x, x1 = bf_hi(zr.x) + dt.y;
+                const float x2 = bf_lo(zr.y) + dt.z, x3 = bf_hi(zr.y) + dt.w;
+                const float m = (t < cn) ? mult : 0.f;
+                acc0 = fmaf(m, softplus_fast(x0), acc0);
+                acc1 = fmaf(m, softplus_fast(x1), acc1);
+                acc2 = fmaf(m, softplus_fast(x2), acc2);
+                acc3 = fmaf(m, softplus_fast(x3), acc3);
+                *reinterpret_cast<float4*>(G2 + t * KD + c4) = make_float4(acc0, acc1, acc2, acc3);
             }
-        }
-        __syncthreads();
-        if (tid >= 128) {
-            const int c = tid - 128;
-            const float base = G[31 * KD + c];
-#pragma unroll 4
-            for (int t = 32; t < 64; ++t) G[t * KD + c] += base;
+            __syncthreads();
+            float4 pre = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int g = 0; g < warp; ++g) {
+                const float4 x = *reinterpret_cast<const float4*>(G2 + (8 * g + 7) * KD + c4);
+                pre.x += x.x; pre.y += x.y; pre.z += x.z; pre.w += x.w;
+            }
+            __syncthreads();
+            if (warp > 0) {
+#pragma unroll
+                for (int a = 0; a < 8; ++a) {
+                    float4* p = reinterpret_cast<float4*>(G2 + (8 * warp + a) * KD + c4);
+                    float4 x = *p;
+                    x.x += pre.x; x.y += pre.y; x.z += pre.z; x.w += pre.w;
+                    *p = x;
+                }
+            }
         }
         __syncthreads();
         // ---------------------------------------------------------------- P3: levels 32, 16
@@ -327,8 +376,7 @@ __global__ void __launch_bounds__(NT, 1)
                 const int t = 4 * b4 + a;
                 unpack8(*reinterpret_cast<const uint4*>(sm + OFF_K + t * 256 + c8 * 16), kk[a]);
                 unpack8(*reinterpret_cast<const uint4*>(sm + OFF_Q + t * 256 + c8 * 16), qq[a]);
-#pragma unroll
-                for (int j = 0; j < 8; ++j) gg[a][j] = G[t * KD + c8 * 8 + j];
+                load8(G2 + t * KD + c8 * 8, gg[a]);
             }
             float v[16];
 #pragma unroll
@@ -345,7 +393,7 @@ __global__ void __launch_bounds__(NT, 1)
                     float sa = 0.f, sq = 0.f;
 #pragma unroll
                     for (int j = 0; j < 8; ++j) {
-                        const float kd = kk[b][j] * ex2((gg[a][j] - gg[b][j]) * LOG2E);
+                        const float kd = kk[b][j] * ex2(gg[a][j] - gg[b][j]);
                         sa = fmaf(kk[a][j], kd, sa);
                         sq = fmaf(qq[a][j], kd, sq);
                     }
@@ -391,42 +439,56 @@ __global__ void __launch_bounds__(NT, 1)
             // TMEM lane r: rows 0..63 are A rows (k side), rows 64..127 are M rows (q side)
             const int r = tid, t = r & 63;
             const bool is_m = r >= 64;
+            const int wt0 = (warp & 1) * 32;  // first token row of this warp
             const float bt = ms.beta[t];
             float* Af = reinterpret_cast<float*>(sm + OFF_LVL + LV_AF);
 #pragma unroll 1
             for (int i0 = 0; i0 < 64; i0 += 16) {
-                uint32_t d0[16], d1[16], d2[16], d3[16];
-                tc::tmem_ld16(taddr(tmem, warp, TM_LVL + i0), d0);
-                tc::tmem_ld16(taddr(tmem, warp, TM_LVL + 64 + i0), d1);
-                tc::tmem_ld16(taddr(tmem, warp, TM_LVL + 128 + i0), d2);
-                tc::tmem_ld16(taddr(tmem, warp, TM_LVL + 192 + i0), d3);
-                tc::tmem_ld_wait();
                 float o16[16];
+                if (i0 > wt0 + 31) {  // every pair of this column block is above the diagonal
 #pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    const int i = i0 + j;
-                    const int x = t ^ i;
-                    float val = __uint_as_float(x >= 32 ? d0[j] : x >= 16 ? d1[j] : x >= 8 ? d2[j] : d3[j]);
-                    if (x < 4) {
-                        const int tl = t & 3, il = i & 3;
-                        const int idx = (tl == il) ? 6 + tl
-                                                   : (is_m ? 10 : 0) + tl * (tl - 1) / 2 + il;
-                        val = ms.diag[t >> 2][tl >= il ? idx : 0];
+                    for (int j = 0; j < 16; ++j) o16[j] = 0.f;
+                } else {
+                    uint32_t d0[16], d1[16], d2[16], d3[16];
+                    tc::tmem_ld16(taddr(tmem, warp, TM_LVL + i0), d0);
+                    tc::tmem_ld16(taddr(tmem, warp, TM_LVL + 64 + i0), d1);
+                    tc::tmem_ld16(taddr(tmem, warp, TM_LVL + 128 + i0), d2);
+                    tc::tmem_ld16(taddr(tmem, warp, TM_LVL + 192 + i0), d3);
+                    tc::tmem_ld_wait();
+                    const int xb = (t ^ i0) & 48;  // level bits shared by the whole block
+                    if (xb >= 16) {
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) {
+                            const float val = __uint_as_float(xb >= 32 ? d0[j] : d1[j]);
+                            const bool valid = is_m ? (i0 + j <= t) : (i0 + j < t);
+                            o16[j] = valid ? (is_m ? val : bt * val) : 0.f;
+                        }
+                    } else {
+                        const float* dg = ms.diag[t >> 2];
+                        const int tl = t & 3;
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) {
+                            const int i = i0 + j;
+                            const int x = t ^ i;
+                            float val = __uint_as_float(x >= 8 ? d2[j] : d3[j]);
+                            if (x < 4) {
+                                const int il = i & 3;
+                                const int idx = (tl == il) ? 6 + tl
+                                                           : (is_m ? 10 : 0) + ((tl * (tl - 1)) >> 1) + il;
+                                val = dg[tl >= il ? idx : 0];
+                            }
+                            const bool valid = is_m ? (i <= t) : (i < t);
+                            o16[j] = valid ? (is_m ? val : bt * val) : 0.f;
+                        }
                     }
-                    const bool valid = is_m ? (i <= t) : (i < t);
-                    o16[j] = valid ? (is_m ? val : bt * val) : 0.f;
                 }
                 if (!is_m) {
 #pragma unroll
                     for (int j = 0; j < 16; j += 4)
-                        *reinterpret_cast<float4*>(Af + t * 64 + i0 + j) =
+                        *reinterpret_cast<float4*>(Af + swz(t, i0 + j)) =
                             make_float4(o16[j], o16[j + 1], o16[j + 2], o16[j + 3]);
                 } else {
-                    float lo[8], hi[8];
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) { lo[j] = o16[j]; hi[j] = o16[8 + j]; }
-                    *reinterpret_cast<uint4*>(sm + OFF_LVL + LV_MB + kmaj_off(t, i0, 64)) = pack8(lo);
-                    *reinterpret_cast<uint4*>(sm + OFF_LVL + LV_MB + kmaj_off(t, i0 + 8, 64)) = pack8(hi);
+                    store16_k(sm + OFF_LVL + LV_MB, t, i0, 64, o16);
                 }
             }
         } else {
@@ -436,11 +498,12 @@ __global__ void __launch_bounds__(NT, 1)
             for (int it = 0; it < 8; ++it) {
                 const int item = tt + 128 * it, t = item >> 4, c8 = item & 15;
                 const float bt = ms.beta[t];
-                float kf[8], vf[8], o[8];
+                float kf[8], vf[8], g8[8], o[8];
                 unpack8(*reinterpret_cast<const uint4*>(sm + OFF_K + t * 256 + c8 * 16), kf);
                 unpack8(*reinterpret_cast<const uint4*>(sm + OFF_V + t * 256 + c8 * 16), vf);
+                load8(G2 + t * KD + c8 * 8, g8);
 #pragma unroll
-                for (int j = 0; j < 8; ++j) o[j] = bt * kf[j] * ex2(G[t * KD + c8 * 8 + j] * LOG2E);
+                for (int j = 0; j < 8; ++j) o[j] = bt * kf[j] * ex2(g8[j]);
                 *reinterpret_cast<uint4*>(sm + OFF_LVL + LV_BKG + mnmaj_off(t, c8 * 8, 8192)) = pack8(o);
 #pragma unroll
                 for (int j = 0; j < 8; ++j) o[j] = bt * vf[j];
@@ -452,62 +515,88 @@ __global__ void __launch_bounds__(NT, 1)
         // ---------------------------------------------------------------- P4: T = (I + A)^{-1}
         {
             const float* Af = reinterpret_cast<const float*>(sm + OFF_LVL + LV_AF);
-            float* Tf = reinterpret_cast<float*>(sm + OFF_V);  // v tile is consumed
-            // zero the strictly upper blocks
-            for (int e = tid; e < 64 * 64; e += NT) {
-                const int t = e >> 6, i = e & 63;
-                if ((i >> 4) > (t >> 4)) Tf[e] = 0.f;
-            }
+            float* Tf = reinterpret_cast<float*>(sm + OFF_V);  // the v tile is consumed
+            // (a) the four 16 x 16 diagonal blocks by forward substitution, one column each;
+            //     the other threads clear the strictly upper blocks.
             if (tid < 64) {
                 const int R = tid >> 4, j = tid & 15;
                 float x[16];
 #pragma unroll
                 for (int t = 0; t < 16; ++t) x[t] = (t == j) ? 1.f : 0.f;
 #pragma unroll
-                for (int i = 0; i < 16; ++i)
+                for (int i = 0; i < 15; ++i)
 #pragma unroll
                     for (int t = i + 1; t < 16; ++t)
-                        x[t] = fmaf(-Af[(16 * R + t) * 64 + 16 * R + i], x[i], x[t]);
+                        x[t] = fmaf(-Af[swz(16 * R + t, 16 * R + i)], x[i], x[t]);
 #pragma unroll
-                for (int t = 0; t < 16; ++t) Tf[(16 * R + t) * 64 + 16 * R + j] = x[t];
+                for (int t = 0; t < 16; ++t) Tf[swz(16 * R + t, 16 * R + j)] = x[t];
+            } else {
+                for (int e = tid - 64; e < 6 * 64; e += NT - 64) {  // 6 blocks x 64 float4
+                    const int blk = e >> 6, q = e & 63;
+                    const int R = blk < 3 ? 0 : (blk < 5 ? 1 : 2);
+                    const int Cb = blk < 3 ? blk + 1 : (blk < 5 ? blk - 1 : 3);
+                    const int t = 16 * R + (q >> 2), i = 16 * Cb + (q & 3) * 4;
+                    *reinterpret_cast<float4*>(Tf + swz(t, i)) = make_float4(0.f, 0.f, 0.f, 0.f);
+                }
             }
             __syncthreads();
-            const int r = tid >> 4, cc = tid & 15;
-#pragma unroll 1
-            for (int d = 1; d < 4; ++d) {
-                // X_RC = sum_{j=C}^{R-1} A_Rj T_jC, stored in the (R, C) block
-                for (int m = 0; m < 4 - d; ++m) {
-                    const int R = d + m, Cb = m;
-                    float s = 0.f;
-                    for (int jb = Cb; jb < R; ++jb)
+            // (b) 16 -> 32: T_RC = -T_RR (A_RC T_CC) for (R, C) = (1, 0), (3, 2)
+            {
+                const int blk = tid >> 7, rr = (tid >> 3) & 15, cp = (tid & 7) * 2;
+                const int R = 2 * blk + 1, Cb = 2 * blk;
+                float x0 = 0.f, x1 = 0.f;
 #pragma unroll
-                        for (int l = 0; l < 16; ++l)
-                            s = fmaf(Af[(16 * R + r) * 64 + 16 * jb + l],
-                                     Tf[(16 * jb + l) * 64 + 16 * Cb + cc], s);
-                    Tf[(16 * R + r) * 64 + 16 * Cb + cc] = s;
+                for (int l = 0; l < 16; ++l) {
+                    const float a = Af[swz(16 * R + rr, 16 * Cb + l)];
+                    const float2 tv = *reinterpret_cast<const float2*>(Tf + swz(16 * Cb + l, 16 * Cb + cp));
+                    x0 = fmaf(a, tv.x, x0);
+                    x1 = fmaf(a, tv.y, x1);
+                }
+                *reinterpret_cast<float2*>(Tf + swz(16 * R + rr, 16 * Cb + cp)) = make_float2(x0, x1);
+                __syncthreads();
+                float y0 = 0.f, y1 = 0.f;
+#pragma unroll
+                for (int l = 0; l < 16; ++l) {
+                    const float a = Tf[swz(16 * R + rr, 16 * R + l)];
+                    const float2 xv = *reinterpret_cast<const float2*>(Tf + swz(16 * R + l, 16 * Cb + cp));
+                    y0 = fmaf(a, xv.x, y0);
+                    y1 = fmaf(a, xv.y, y1);
                 }
                 __syncthreads();
-                float y[3];
-                for (int m = 0; m < 4 - d; ++m) {
-                    const int R = d + m, Cb = m;
-                    float s = 0.f;
-#pragma unroll
-                    for (int l = 0; l < 16; ++l)
-                        s = fmaf(Tf[(16 * R + r) * 64 + 16 * R + l],
-                                 Tf[(16 * R + l) * 64 + 16 * Cb + cc], s);
-                    y[m] = -s;
-                }
-                __syncthreads();
-                for (int m = 0; m < 4 - d; ++m)
-                    Tf[(16 * (d + m) + r) * 64 + 16 * m + cc] = y[m];
-                __syncthreads();
+                *reinterpret_cast<float2*>(Tf + swz(16 * R + rr, 16 * Cb + cp)) = make_float2(-y0, -y1);
             }
+            __syncthreads();
+            // (c) 32 -> 64: T[32:64, 0:32] = -T[32:64, 32:64] (A[32:64, 0:32] T[0:32, 0:32])
+            {
+                const int rr = tid >> 3, cq = (tid & 7) * 4;
+                float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 8
+                for (int l = 0; l < 32; ++l) {
+                    const float a = Af[swz(32 + rr, l)];
+                    const float4 tv = *reinterpret_cast<const float4*>(Tf + swz(l, cq));
+                    x.x = fmaf(a, tv.x, x.x); x.y = fmaf(a, tv.y, x.y);
+                    x.z = fmaf(a, tv.z, x.z); x.w = fmaf(a, tv.w, x.w);
+                }
+                *reinterpret_cast<float4*>(Tf + swz(32 + rr, cq)) = x;
+                __syncthreads();
+                float4 y = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 8
+                for (int l = 0; l < 32; ++l) {
+                    const float a = Tf[swz(32 + rr, 32 + l)];
+                    const float4 xv = *reinterpret_cast<const float4*>(Tf + swz(32 + l, cq));
+                    y.x = fmaf(a, xv.x, y.x); y.y = fmaf(a, xv.y, y.y);
+                    y.z = fmaf(a, xv.z, y.z); y.w = fmaf(a, xv.w, y.w);
+                }
+                __syncthreads();
+                *reinterpret_cast<float4*>(Tf + swz(32 + rr, cq)) = make_float4(-y.x, -y.y, -y.z, -y.w);
+            }
+            __syncthreads();
             // T -> bf16 K-major [t][i]
             for (int it = tid; it < 64 * 8; it += NT) {
                 const int t = it >> 3, i8 = it & 7;
-                float f[8];
-#pragma unroll
-                for (int j = 0; j < 8; ++j) f[j] = Tf[t * 64 + i8 * 8 + j];
+                const float4 a = *reinterpret_cast<const float4*>(Tf + swz(t, i8 * 8));
+                const float4 b = *reinterpret_cast<const float4*>(Tf + swz(t, i8 * 8 + 4));
+                const float f[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
                 *reinterpret_cast<uint4*>(sm + OFF_LVL + LV_TB + kmaj_off(t, i8 * 8, 64)) = pack8(f);
             }
         }
@@ -525,7 +614,7 @@ __global__ void __launch_bounds__(NT, 1)
         KDA_WAIT_MMA();
         if (failed) break;
         {
-            // lanes of warps 0-3: W^T row c -> [W^T | .] operand; warps 4-7: U^T row v
+            // warps 0-3: W^T row c -> [W^T | .] operand; warps 4-7: U^T row v -> K-major operand
             const int row = tid & 127;
             const uint32_t col = warp < 4 ? TM_W : TM_U;
 #pragma unroll 1
@@ -533,35 +622,57 @@ __global__ void __launch_bounds__(NT, 1)
                 uint32_t d[16];
                 tc::tmem_ld16(taddr(tmem, warp, col + t0c), d);
                 tc::tmem_ld_wait();
-                float lo[8], hi[8];
+                float f[16];
 #pragma unroll
-                for (int j = 0; j < 8; ++j) { lo[j] = __uint_as_float(d[j]); hi[j] = __uint_as_float(d[8 + j]); }
-                if (warp < 4) {
-                    *reinterpret_cast<uint4*>(sm + OFF_A1 + mnmaj_off(row, t0c, 16384)) = pack8(lo);
-                    *reinterpret_cast<uint4*>(sm + OFF_A1 + mnmaj_off(row, t0c + 8, 16384)) = pack8(hi);
-                } else {
-                    *reinterpret_cast<uint4*>(sm + OFF_LVL + LV_UT + kmaj_off(row, t0c, 128)) = pack8(lo);
-                    *reinterpret_cast<uint4*>(sm + OFF_LVL + LV_UT + kmaj_off(row, t0c + 8, 128)) = pack8(hi);
-                }
+                for (int j = 0; j < 16; ++j) f[j] = __uint_as_float(d[j]);
+                if (warp < 4) store16_mn(sm + OFF_A1, row, t0c, 16384, f);
+                else store16_k(sm + OFF_LVL + LV_UT, row, t0c, 128, f);
+            }
+            // Q Gamma (MN-major [t][c]) and K~ = K e^{G_last - G} (MN-major [t][c])
+#pragma unroll 1
+            for (int it = 0; it < 4; ++it) {
+                const int item = tid + NT * it, t = item >> 4, c8 = item & 15;
+                float qf[8], kf[8], g8[8], gl[8], o[8];
+                unpack8(*reinterpret_cast<const uint4*>(sm + OFF_Q + t * 256 + c8 * 16), qf);
+                unpack8(*reinterpret_cast<const uint4*>(sm + OFF_K + t * 256 + c8 * 16), kf);
+                load8(G2 + t * KD + c8 * 8, g8);
+                load8(G2 + 63 * KD + c8 * 8, gl);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) o[j] = qf[j] * ex2(g8[j]);
+                *reinterpret_cast<uint4*>(sm + OFF_LVL + LV_QG + mnmaj_off(t, c8 * 8, 8192)) = pack8(o);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) o[j] = kf[j] * ex2(gl[j] - g8[j]);
+                *reinterpret_cast<uint4*>(sm + OFF_LVL + LV_KT + mnmaj_off(t, c8 * 8, 8192)) = pack8(o);
             }
         }
         KDA_SYNC_FOR_MMA();
-        // ---------------------------------------------------------------- P5: W^T M^T, U^T M^T
+        // ---------------------------------------------------------------- P5: Q'^T and U'^T
         if (tid == 0) {
+            // Q'^T = (Q Gamma)^T I - W^T M^T ;  U'^T = U^T M^T
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks)
+                tc::mma_bf16(tmem + TM_QP, desc_mn(sb + OFF_LVL + LV_QG, 8192, ks),
+                             desc_k(sb + OFF_ID, 64, ks), IDESC_WU, ks > 0);
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks) {
                 const uint64_t b = desc_k(sb + OFF_LVL + LV_MB, 64, ks);
-                tc::mma_bf16(tmem + TM_QP, desc_k(sb + OFF_A1, 128, ks), b, IDESC_QU, ks > 0);
+                tc::mma_bf16(tmem + TM_QP, desc_k(sb + OFF_A1, 128, ks), b, IDESC_QNEG, 1u);
                 tc::mma_bf16(tmem + TM_UP, desc_k(sb + OFF_LVL + LV_UT, 128, ks), b, IDESC_QU, ks > 0);
             }
             tc::mma_commit(&ms.bar_mma);
         }
         KDA_WAIT_MMA();
         if (failed) break;
+        // the next chunk's tiles: every reader of q, k, v, z and of the z slot is done
+        if (tid == 0 && n + 1 < nchunks) {
+            tc::mbar_arrive_expect_tx(&ms.bar_tma, 4u * 16384u);
+            tc::tma_load_3d(sm + OFF_Q, &tm_q, 0, t0 + C, (int)bh, &ms.bar_tma);
+            tc::tma_load_3d(sm + OFF_K, &tm_k, 0, t0 + C, (int)bh, &ms.bar_tma);
+            tc::tma_load_3d(sm + OFF_V, &tm_v, 0, t0 + C, (int)bh, &ms.bar_tma);
+            tc::tma_load_3d(sm + OFF_LVL + LV_Z, &tm_z, 0, t0 + C, (int)bh, &ms.bar_tma);
+        }
         if (warp < 4) {
-            // Q'^T[c][t] = q[t][c] Gamma[t][c] - (W^T M^T)[c][t]
             const int c = tid;
-            const uint8_t* qt = sm + OFF_Q + c * 2;
 #pragma unroll 1
             for (int t0c = 0; t0c < 64; t0c += 16) {
                 uint32_t d[16];
@@ -569,97 +680,13 @@ __global__ void __launch_bounds__(NT, 1)
                 tc::tmem_ld_wait();
                 float f[16];
 #pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    const int t = t0c + j;
-                    f[j] = bf16_at(qt + t * 256) * ex2(G[t * KD + c] * LOG2E) - __uint_as_float(d[j]);
-                }
-                float lo[8], hi[8];
-#pragma unroll
-                for (int j = 0; j < 8; ++j) { lo[j] = f[j]; hi[j] = f[8 + j]; }
-                *reinterpret_cast<uint4*>(sm + OFF_A1 + mnmaj_off(c, 64 + t0c, 16384)) = pack8(lo);
-                *reinterpret_cast<uint4*>(sm + OFF_A1 + mnmaj_off(c, 64 + t0c + 8, 16384)) = pack8(hi);
-            }
-            ms.gamma_last[c] = ex2(G[63 * KD + c] * LOG2E);
-        } else {
-            // U'^T[v][t] (plain rows of 64 bf16)
-            const int v = tid - 128;
-#pragma unroll 1
-            for (int t0c = 0; t0c < 64; t0c += 16) {
-                uint32_t d[16];
-                tc::tmem_ld16(taddr(tmem, warp, TM_UP + t0c), d);
-                tc::tmem_ld_wait();
-                float lo[8], hi[8];
-#pragma unroll
-                for (int j = 0; j < 8; ++j) { lo[j] = __uint_as_float(d[j]); hi[j] = __uint_as_float(d[8 + j]); }
-                *reinterpret_cast<uint4*>(sm + OFF_LVL + LV_UPT + v * 128 + t0c * 2) = pack8(lo);
-                *reinterpret_cast<uint4*>(sm + OFF_LVL + LV_UPT + v * 128 + t0c * 2 + 16) = pack8(hi);
-            }
-        }
-        // K~ = K * e^{G_last - G}, MN-major [t][c]
-        for (int it = 0; it < 4; ++it) {
-            const int item = tid + NT * it, t = item >> 4, c8 = item & 15;
-            float kf[8], o[8];
-            unpack8(*reinterpret_cast<const uint4*>(sm + OFF_K + t * 256 + c8 * 16), kf);
-#pragma unroll
-            for (int j = 0; j < 8; ++j)
-                o[j] = kf[j] * ex2((G[63 * KD + c8 * 8 + j] - G[t * KD + c8 * 8 + j]) * LOG2E);
-            *reinterpret_cast<uint4*>(sm + OFF_LVL + LV_KT + mnmaj_off(t, c8 * 8, 8192)) = pack8(o);
-        }
-        KDA_SYNC_FOR_MMA();
-        // ---------------------------------------------------------------- C1: [W ; Q'] S
-        if (tid == 0) {
-#pragma unroll
-            for (int ks = 0; ks < 8; ++ks)
-                tc::mma_bf16(tmem + TM_D1, desc_mn(sb + OFF_A1, 16384, ks),
-                             desc_mn(sb + OFF_S, 16384, ks), IDESC_SQ, ks > 0);
-            tc::mma_commit(&ms.bar_mma);
-        }
-        KDA_WAIT_MMA();
-        if (failed) break;
-        // ---------------------------------------------------------------- C2
-        if (warp < 2) {
-            // Delta[t][v] = U[t][v] - (W S)[t][v]   -> MN-major [t][v] operand
-            const int t = tid;
-#pragma unroll 1
-            for (int v0 = 0; v0 < VD; v0 += 16) {
-                uint32_t d[16];
-                tc::tmem_ld16(taddr(tmem, warp, TM_D1 + v0), d);
-                tc::tmem_ld_wait();
-                float lo[8], hi[8];
-#pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    const float u = bf16_at(sm + OFF_LVL + LV_UT + kmaj_off(v0 + j, t, 128));
-                    const float x = u - __uint_as_float(d[j]);
-                    if (j < 8) lo[j] = x; else hi[j - 8] = x;
-                }
-                *reinterpret_cast<uint4*>(sm + OFF_LVL + LV_DELTA + mnmaj_off(t, v0, 8192)) = pack8(lo);
-                *reinterpret_cast<uint4*>(sm + OFF_LVL + LV_DELTA + mnmaj_off(t, v0 + 8, 8192)) = pack8(hi);
-            }
-        } else if (warp < 4) {
-            // o[t][v] = scale ((Q' S)[t][v] + U'[t][v])
-            const int t = tid - 64;
-            __nv_bfloat16* orow = out + (bh * T + t0 + t) * VD;
-#pragma unroll 1
-            for (int v0 = 0; v0 < VD; v0 += 16) {
-                uint32_t d[16];
-                tc::tmem_ld16(taddr(tmem, warp, TM_D1 + v0), d);
-                tc::tmem_ld_wait();
-                float lo[8], hi[8];
-#pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    const float up = bf16_at(sm + OFF_LVL + LV_UPT + (v0 + j) * 128 + t * 2);
-                    const float x = scale * (__uint_as_float(d[j]) + up);
-                    if (j < 8) lo[j] = x; else hi[j - 8] = x;
-                }
-                if (t < cn) {
-                    *reinterpret_cast<uint4*>(orow + v0) = pack8(lo);
-                    *reinterpret_cast<uint4*>(orow + v0 + 8) = pack8(hi);
-                }
+                for (int j = 0; j < 16; ++j) f[j] = __uint_as_float(d[j]);
+                store16_mn(sm + OFF_A1, c, 64 + t0c, 16384, f);
             }
         } else {
-            // S <- diag(Gamma_last) S in TMEM (lane c)
+            // S <- diag(Gamma_last) S in TMEM (lane c); the bf16 copy for this chunk is unscaled
             const int c = tid - 128;
-            const float gl = ms.gamma_last[c];
+            const float gl = ex2(G2[63 * KD + c]);
 #pragma unroll 1
             for (int v0 = 0; v0 < VD; v0 += 16) {
                 uint32_t d[16];
@@ -672,28 +699,67 @@ __global__ void __launch_bounds__(NT, 1)
             tc::tmem_st_wait();
         }
         KDA_SYNC_FOR_MMA();
+        // ---------------------------------------------------------------- C1: (S^T [W^T | Q'^T])
+        if (tid == 0) {
+            // D[v][t'] = sum_c S[c][v] A1[c][t']: t' < 64 gives (W S)^T, t' >= 64 gives (Q' S)^T
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks)
+                tc::mma_bf16(tmem + TM_D1, desc_mn(sb + OFF_S, 16384, ks),
+                             desc_mn(sb + OFF_A1, 16384, ks), IDESC_SQ, ks > 0);
+            tc::mma_commit(&ms.bar_mma);
+        }
+        KDA_WAIT_MMA();
+        if (failed) break;
+        // ---------------------------------------------------------------- C2
+        if (warp < 4) {
+            // lane v: Delta^T[v][t] = U^T[v][t] - (W S)^T[v][t]  -> K-major B operand [v][t]
+            //         o[t][v] = scale ((Q' S)^T[v][t] + U'^T[v][t])
+            const int v = tid;
+            __nv_bfloat16* ocol = out + (bh * T + t0) * VD + v;
+#pragma unroll 1
+            for (int t0c = 0; t0c < 64; t0c += 16) {
+                uint32_t dw[16], du[16], dq[16], dp[16];
+                tc::tmem_ld16(taddr(tmem, warp, TM_D1 + t0c), dw);
+                tc::tmem_ld16(taddr(tmem, warp, TM_U + t0c), du);
+                tc::tmem_ld16(taddr(tmem, warp, TM_D1 + 64 + t0c), dq);
+                tc::tmem_ld16(taddr(tmem, warp, TM_UP + t0c), dp);
+                tc::tmem_ld_wait();
+                float f[16];
+#pragma unroll
+                for (int j = 0; j < 16; ++j) f[j] = __uint_as_float(du[j]) - __uint_as_float(dw[j]);
+                store16_k(sm + OFF_LVL + LV_DELTA, v, t0c, 128, f);
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const int t = t0c + j;
+                    if (t < cn)
+                        ocol[(size_t)t * VD] =
+                            __float2bfloat16_rn(scale * (__uint_as_float(dq[j]) + __uint_as_float(dp[j])));
+                }
+            }
+        }
+        KDA_SYNC_FOR_MMA();
         // ---------------------------------------------------------------- C3: S += K~^T Delta
         if (tid == 0) {
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks)
                 tc::mma_bf16(tmem + TM_S, desc_mn(sb + OFF_LVL + LV_KT, 8192, ks),
-                             desc_mn(sb + OFF_LVL + LV_DELTA, 8192, ks), IDESC_SQ, 1u);
+                             desc_k(sb + OFF_LVL + LV_DELTA, 128, ks), IDESC_SK, 1u);
             tc::mma_commit(&ms.bar_mma);
         }
         KDA_WAIT_MMA();
         if (failed) break;
-        if (warp < 4) {
-            const int c = tid;
+        {
+            // S (fp32, TMEM) -> bf16 operand [c][v]; warps 0-3 take v < 64, warps 4-7 v >= 64
+            const int c = tid & 127, vb = (warp >> 2) * 64;
 #pragma unroll 1
-            for (int v0 = 0; v0 < VD; v0 += 16) {
+            for (int v0 = vb; v0 < vb + 64; v0 += 16) {
                 uint32_t d[16];
                 tc::tmem_ld16(taddr(tmem, warp, TM_S + v0), d);
                 tc::tmem_ld_wait();
-                float lo[8], hi[8];
+                float f[16];
 #pragma unroll
-                for (int j = 0; j < 8; ++j) { lo[j] = __uint_as_float(d[j]); hi[j] = __uint_as_float(d[8 + j]); }
-                *reinterpret_cast<uint4*>(sm + OFF_S + mnmaj_off(c, v0, 16384)) = pack8(lo);
-                *reinterpret_cast<uint4*>(sm + OFF_S + mnmaj_off(c, v0 + 8, 16384)) = pack8(hi);
+                for (int j = 0; j < 16; ++j) f[j] = __uint_as_float(d[j]);
+                store16_mn(sm + OFF_S, c, v0, 16384, f);
             }
         }
         KDA_SYNC_FOR_MMA();
@@ -717,8 +783,9 @@ __global__ void __launch_bounds__(NT, 1)
     }
     if (failed && tid == 0) {
         atomicExch(&g_kda_tc_timeout, 1);
-        // give any tensor-core work still in flight a bounded chance to finish
+        // give any tensor-core or TMA work still in flight a bounded chance to finish
         tc::mbar_wait(&ms.bar_mma, mma_phase, 200000000ull);
+        tc::mbar_wait(&ms.bar_tma, tma_phase, 200000000ull);
     }
     tc::fence_before_sync();
     __syncthreads();
