@@ -1,7 +1,7 @@
 // chunk_tc.cu -- the KDA chunked forward on the 5th-generation tensor cores
 // (tcgen05 + TMEM + TMA), for bf16 I/O with K = V = 128 and chunk C = 64.
 //
-// One CTA (8 warps) owns one (b, h) sequence and walks its chunks in order.
+// One CTA (16 warps) owns one (b, h) sequence and walks its chunks in order.
 // The fp32 state S (K x V) lives in TMEM for the whole sequence; per chunk:
 //
 //   P1  TMA: q, k, v, z tiles (64 x 128 bf16 each) into shared memory; the
@@ -52,7 +52,7 @@ __device__ int g_kda_tc_timeout;
 
 namespace {
 
-constexpr int C = 64, KD = 128, VD = 128, NT = 256;
+constexpr int C = 64, KD = 128, VD = 128, NT = 512;
 constexpr float LOG2E = 1.4426950408889634f;
 
 // ---- shared memory map (bytes from a 1024-byte aligned base)
@@ -174,8 +174,8 @@ __device__ __forceinline__ void build_levels(uint8_t* sm, int li0, int tid) {
     const float* G2 = reinterpret_cast<const float*>(sm + OFF_G);
     const int c8 = tid & 15;
 #pragma unroll 1
-    for (int r = 0; r < 4; ++r) {
-        const int t = (tid >> 4) + 16 * r;
+    for (int r = 0; r < 2; ++r) {
+        const int t = (tid >> 4) + 32 * r;
         float kf[8], qf[8], g8[8];
         unpack8(*reinterpret_cast<const uint4*>(sm + OFF_K + t * 256 + c8 * 16), kf);
         unpack8(*reinterpret_cast<const uint4*>(sm + OFF_Q + t * 256 + c8 * 16), qf);
@@ -226,6 +226,9 @@ __global__ void __launch_bounds__(NT, 1)
     Misc& ms = *reinterpret_cast<Misc*>(sm + OFF_MISC);
     float* G2 = reinterpret_cast<float*>(sm + OFF_G);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    // TMEM is read in 32-lane quarters: warp w reaches lanes 32*(w & 3) .. +31; the four
+    // warps sharing a quarter split the columns by `part`.
+    const int q4 = warp & 3, part = warp >> 2, row = q4 * 32 + lane;
     const size_t bh = blockIdx.x;
     const int h = (int)(bh % H);
     const float exp_A = expf(A_log[h]);
@@ -253,11 +256,11 @@ __global__ void __launch_bounds__(NT, 1)
 
     // 64 x 64 identity, K-major bf16: the B operand that copies (Q Gamma)^T into an accumulator
     if (tid < 64) *reinterpret_cast<uint16_t*>(sm + OFF_ID + kmaj_off(tid, tid, 64)) = 0x3F80u;
-    // Initial state: fp32 into TMEM (lane c), bf16 copy as the MN-major operand [c][v].
-    if (tid < KD) {
-        const int c = tid;
+    // Initial state: fp32 into TMEM (lane c = row), bf16 copy as the MN-major operand [c][v].
+    {
+        const int c = row;
 #pragma unroll 1
-        for (int v0 = 0; v0 < VD; v0 += 16) {
+        for (int v0 = 32 * part; v0 < 32 * part + 32; v0 += 16) {
             float f[16];
 #pragma unroll
             for (int j = 0; j < 16; j += 4) {
@@ -317,14 +320,14 @@ __global__ void __launch_bounds__(NT, 1)
         }
         // ---------------------------------------------------------------- P2
         {
-            // warp w: tokens 8w..8w+7; lane: channels 4*lane..4*lane+3 (G2 in log2 units)
+            // warp w: tokens 4w..4w+3; lane: channels 4*lane..4*lane+3 (G2 in log2 units)
             const int c4 = lane * 4;
             const float4 dt = *reinterpret_cast<const float4*>(&ms.dt[c4]);
             const float mult = -exp_A * LOG2E;
             float acc0 = 0.f, acc1 = 0.f, acc2 = 0.f, acc3 = 0.f;
 #pragma unroll
-            for (int a = 0; a < 8; ++a) {
-                const int t = 8 * warp + a;
+            for (int a = 0; a < 4; ++a) {
+                const int t = 4 * warp + a;
                 const uint2 zr = *reinterpret_cast<const uint2*>(sm + OFF_LVL + LV_Z + t * 256 + c4 * 2);
                 const float x0 = bf_lo(zr.x) + dt.x, x1 = bf_hi(zr.x) + dt.y;
                 const float x2 = bf_lo(zr.y) + dt.z, x3 = bf_hi(zr.y) + dt.w;
@@ -338,14 +341,14 @@ __global__ void __launch_bounds__(NT, 1)
             __syncthreads();
             float4 pre = make_float4(0.f, 0.f, 0.f, 0.f);
             for (int g = 0; g < warp; ++g) {
-                const float4 x = *reinterpret_cast<const float4*>(G2 + (8 * g + 7) * KD + c4);
+                const float4 x = *reinterpret_cast<const float4*>(G2 + (4 * g + 3) * KD + c4);
                 pre.x += x.x; pre.y += x.y; pre.z += x.z; pre.w += x.w;
             }
             __syncthreads();
             if (warp > 0) {
 #pragma unroll
-                for (int a = 0; a < 8; ++a) {
-                    float4* p = reinterpret_cast<float4*>(G2 + (8 * warp + a) * KD + c4);
+                for (int a = 0; a < 4; ++a) {
+                    float4* p = reinterpret_cast<float4*>(G2 + (4 * warp + a) * KD + c4);
                     float4 x = *p;
                     x.x += pre.x; x.y += pre.y; x.z += pre.z; x.w += pre.w;
                     *p = x;
@@ -367,23 +370,27 @@ __global__ void __launch_bounds__(NT, 1)
             }
             tc::mma_commit(&ms.bar_mma);
         }
-        // pairs inside 4-token blocks: exact pairwise decay, CUDA cores
+        // pairs inside 4-token blocks: exact pairwise decay, CUDA cores.
+        // warp w = 4-token block w; lane = channels 4*lane..4*lane+3.
         {
-            const int b4 = tid >> 4, c8 = tid & 15;
-            float kk[4][8], qq[4][8], gg[4][8];
+            const int b4 = warp, c4 = lane * 4;
+            float kk[4][4], qq[4][4], gg[4][4];
 #pragma unroll
             for (int a = 0; a < 4; ++a) {
                 const int t = 4 * b4 + a;
-                unpack8(*reinterpret_cast<const uint4*>(sm + OFF_K + t * 256 + c8 * 16), kk[a]);
-                unpack8(*reinterpret_cast<const uint4*>(sm + OFF_Q + t * 256 + c8 * 16), qq[a]);
-                load8(G2 + t * KD + c8 * 8, gg[a]);
+                const uint2 kr = *reinterpret_cast<const uint2*>(sm + OFF_K + t * 256 + c4 * 2);
+                const uint2 qr = *reinterpret_cast<const uint2*>(sm + OFF_Q + t * 256 + c4 * 2);
+                kk[a][0] = bf_lo(kr.x); kk[a][1] = bf_hi(kr.x); kk[a][2] = bf_lo(kr.y); kk[a][3] = bf_hi(kr.y);
+                qq[a][0] = bf_lo(qr.x); qq[a][1] = bf_hi(qr.x); qq[a][2] = bf_lo(qr.y); qq[a][3] = bf_hi(qr.y);
+                const float4 g = *reinterpret_cast<const float4*>(G2 + t * KD + c4);
+                gg[a][0] = g.x; gg[a][1] = g.y; gg[a][2] = g.z; gg[a][3] = g.w;
             }
             float v[16];
 #pragma unroll
             for (int a = 0; a < 4; ++a) {  // M diagonal
                 float s = 0.f;
 #pragma unroll
-                for (int j = 0; j < 8; ++j) s = fmaf(qq[a][j], kk[a][j], s);
+                for (int j = 0; j < 4; ++j) s = fmaf(qq[a][j], kk[a][j], s);
                 v[6 + a] = s;
             }
 #pragma unroll
@@ -392,7 +399,7 @@ __global__ void __launch_bounds__(NT, 1)
                 for (int b = 0; b < a; ++b) {
                     float sa = 0.f, sq = 0.f;
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) {
+                    for (int j = 0; j < 4; ++j) {
                         const float kd = kk[b][j] * ex2(gg[a][j] - gg[b][j]);
                         sa = fmaf(kk[a][j], kd, sa);
                         sq = fmaf(qq[a][j], kd, sq);
@@ -401,9 +408,9 @@ __global__ void __launch_bounds__(NT, 1)
                     v[idx] = sa;
                     v[10 + idx] = sq;
                 }
-            // reduce-scatter across the 16 lanes that share this 4-token block
+            // reduce-scatter over the 32 lanes: lane l ends with value (l >> 1) & 15
 #pragma unroll
-            for (int off = 8, w = 8; off >= 1; off >>= 1, w >>= 1) {
+            for (int off = 16, w = 8; off >= 2; off >>= 1, w >>= 1) {
                 const bool hi = (lane & off) != 0;
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
@@ -414,7 +421,8 @@ __global__ void __launch_bounds__(NT, 1)
                     }
                 }
             }
-            ms.diag[b4][c8] = v[0];
+            v[0] += __shfl_xor_sync(0xffffffffu, v[0], 1);
+            if ((lane & 1) == 0) ms.diag[b4][lane >> 1] = v[0];
         }
         KDA_WAIT_MMA();
         if (failed) break;
@@ -435,79 +443,75 @@ __global__ void __launch_bounds__(NT, 1)
         KDA_WAIT_MMA();
         if (failed) break;
         // ---------------------------------------------------------------- P3 epilogue
-        if (warp < 4) {
-            // TMEM lane r: rows 0..63 are A rows (k side), rows 64..127 are M rows (q side)
-            const int r = tid, t = r & 63;
-            const bool is_m = r >= 64;
-            const int wt0 = (warp & 1) * 32;  // first token row of this warp
-            const float bt = ms.beta[t];
-            float* Af = reinterpret_cast<float*>(sm + OFF_LVL + LV_AF);
-#pragma unroll 1
-            for (int i0 = 0; i0 < 64; i0 += 16) {
-                float o16[16];
-                if (i0 > wt0 + 31) {  // every pair of this column block is above the diagonal
+        {
+            // TMEM lane `row`: rows 0..63 are A rows (k side), rows 64..127 are M rows (q side);
+            // this warp takes the 16 columns i0 = 16 * part.
+            const int t = row & 63, i0 = 16 * part;
+            const bool is_m = row >= 64;
+            const int wt0 = (q4 & 1) * 32;  // first token row of this warp
+            float o16[16];
+            if (i0 > wt0 + 31) {  // every pair of this column block is above the diagonal
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) o16[j] = 0.f;
+                for (int j = 0; j < 16; ++j) o16[j] = 0.f;
+            } else {
+                const float bt = ms.beta[t];
+                uint32_t d0[16], d1[16], d2[16], d3[16];
+                tc::tmem_ld16(taddr(tmem, warp, TM_LVL + i0), d0);
+                tc::tmem_ld16(taddr(tmem, warp, TM_LVL + 64 + i0), d1);
+                tc::tmem_ld16(taddr(tmem, warp, TM_LVL + 128 + i0), d2);
+                tc::tmem_ld16(taddr(tmem, warp, TM_LVL + 192 + i0), d3);
+                tc::tmem_ld_wait();
+                const int xb = (t ^ i0) & 48;  // level bits shared by the whole block
+                if (xb >= 16) {
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const float val = __uint_as_float(xb >= 32 ? d0[j] : d1[j]);
+                        const bool valid = is_m ? (i0 + j <= t) : (i0 + j < t);
+                        o16[j] = valid ? (is_m ? val : bt * val) : 0.f;
+                    }
                 } else {
-                    uint32_t d0[16], d1[16], d2[16], d3[16];
-                    tc::tmem_ld16(taddr(tmem, warp, TM_LVL + i0), d0);
-                    tc::tmem_ld16(taddr(tmem, warp, TM_LVL + 64 + i0), d1);
-                    tc::tmem_ld16(taddr(tmem, warp, TM_LVL + 128 + i0), d2);
-                    tc::tmem_ld16(taddr(tmem, warp, TM_LVL + 192 + i0), d3);
-                    tc::tmem_ld_wait();
-                    const int xb = (t ^ i0) & 48;  // level bits shared by the whole block
-                    if (xb >= 16) {
+                    const float* dg = ms.diag[t >> 2];
+                    const int tl = t & 3;
 #pragma unroll
-                        for (int j = 0; j < 16; ++j) {
-                            const float val = __uint_as_float(xb >= 32 ? d0[j] : d1[j]);
-                            const bool valid = is_m ? (i0 + j <= t) : (i0 + j < t);
-                            o16[j] = valid ? (is_m ? val : bt * val) : 0.f;
+                    for (int j = 0; j < 16; ++j) {
+                        const int i = i0 + j;
+                        const int x = t ^ i;
+                        float val = __uint_as_float(x >= 8 ? d2[j] : d3[j]);
+                        if (x < 4) {
+                            const int il = i & 3;
+                            const int idx = (tl == il) ? 6 + tl
+                                                       : (is_m ? 10 : 0) + ((tl * (tl - 1)) >> 1) + il;
+                            val = dg[tl >= il ? idx : 0];
                         }
-                    } else {
-                        const float* dg = ms.diag[t >> 2];
-                        const int tl = t & 3;
-#pragma unroll
-                        for (int j = 0; j < 16; ++j) {
-                            const int i = i0 + j;
-                            const int x = t ^ i;
-                            float val = __uint_as_float(x >= 8 ? d2[j] : d3[j]);
-                            if (x < 4) {
-                                const int il = i & 3;
-                                const int idx = (tl == il) ? 6 + tl
-                                                           : (is_m ? 10 : 0) + ((tl * (tl - 1)) >> 1) + il;
-                                val = dg[tl >= il ? idx : 0];
-                            }
-                            const bool valid = is_m ? (i <= t) : (i < t);
-                            o16[j] = valid ? (is_m ? val : bt * val) : 0.f;
-                        }
+                        const bool valid = is_m ? (i <= t) : (i < t);
+                        o16[j] = valid ? (is_m ? val : bt * val) : 0.f;
                     }
                 }
-                if (!is_m) {
-#pragma unroll
-                    for (int j = 0; j < 16; j += 4)
-                        *reinterpret_cast<float4*>(Af + swz(t, i0 + j)) =
-                            make_float4(o16[j], o16[j + 1], o16[j + 2], o16[j + 3]);
-                } else {
-                    store16_k(sm + OFF_LVL + LV_MB, t, i0, 64, o16);
-                }
             }
-        } else {
+            if (!is_m) {
+                float* Af = reinterpret_cast<float*>(sm + OFF_LVL + LV_AF);
+#pragma unroll
+                for (int j = 0; j < 16; j += 4)
+                    *reinterpret_cast<float4*>(Af + swz(t, i0 + j)) =
+                        make_float4(o16[j], o16[j + 1], o16[j + 2], o16[j + 3]);
+            } else {
+                store16_k(sm + OFF_LVL + LV_MB, t, i0, 64, o16);
+            }
             // beta K Gamma and beta V as MN-major [t][.] operands
-            const int tt = tid - 128;
 #pragma unroll 1
-            for (int it = 0; it < 8; ++it) {
-                const int item = tt + 128 * it, t = item >> 4, c8 = item & 15;
-                const float bt = ms.beta[t];
+            for (int it = 0; it < 2; ++it) {
+                const int item = tid + NT * it, tt = item >> 4, c8 = item & 15;
+                const float bt = ms.beta[tt];
                 float kf[8], vf[8], g8[8], o[8];
-                unpack8(*reinterpret_cast<const uint4*>(sm + OFF_K + t * 256 + c8 * 16), kf);
-                unpack8(*reinterpret_cast<const uint4*>(sm + OFF_V + t * 256 + c8 * 16), vf);
-                load8(G2 + t * KD + c8 * 8, g8);
+                unpack8(*reinterpret_cast<const uint4*>(sm + OFF_K + tt * 256 + c8 * 16), kf);
+                unpack8(*reinterpret_cast<const uint4*>(sm + OFF_V + tt * 256 + c8 * 16), vf);
+                load8(G2 + tt * KD + c8 * 8, g8);
 #pragma unroll
                 for (int j = 0; j < 8; ++j) o[j] = bt * kf[j] * ex2(g8[j]);
-                *reinterpret_cast<uint4*>(sm + OFF_LVL + LV_BKG + mnmaj_off(t, c8 * 8, 8192)) = pack8(o);
+                *reinterpret_cast<uint4*>(sm + OFF_LVL + LV_BKG + mnmaj_off(tt, c8 * 8, 8192)) = pack8(o);
 #pragma unroll
                 for (int j = 0; j < 8; ++j) o[j] = bt * vf[j];
-                *reinterpret_cast<uint4*>(sm + OFF_LVL + LV_BV + mnmaj_off(t, c8 * 8, 8192)) = pack8(o);
+                *reinterpret_cast<uint4*>(sm + OFF_LVL + LV_BV + mnmaj_off(tt, c8 * 8, 8192)) = pack8(o);
             }
         }
         tc::fence_before_sync();
@@ -520,6 +524,7 @@ __global__ void __launch_bounds__(NT, 1)
             //     the other threads clear the strictly upper blocks.
             if (tid < 64) {
                 const int R = tid >> 4, j = tid & 15;
+                const float* Ab = Af + 16 * R * 64;  // rows 16R.. ; (row & 15) == t
                 float x[16];
 #pragma unroll
                 for (int t = 0; t < 16; ++t) x[t] = (t == j) ? 1.f : 0.f;
@@ -527,9 +532,11 @@ __global__ void __launch_bounds__(NT, 1)
                 for (int i = 0; i < 15; ++i)
 #pragma unroll
                     for (int t = i + 1; t < 16; ++t)
-                        x[t] = fmaf(-Af[swz(16 * R + t, 16 * R + i)], x[i], x[t]);
+                        x[t] = fmaf(-Ab[t * 64 + ((((4 * R + (i >> 2)) ^ t)) << 2) + (i & 3)], x[i], x[t]);
+                float* Tb = Tf + 16 * R * 64;
 #pragma unroll
-                for (int t = 0; t < 16; ++t) Tf[swz(16 * R + t, 16 * R + j)] = x[t];
+                for (int t = 0; t < 16; ++t)
+                    Tb[t * 64 + ((((4 * R + (j >> 2)) ^ t)) << 2) + (j & 3)] = x[t];
             } else {
                 for (int e = tid - 64; e < 6 * 64; e += NT - 64) {  // 6 blocks x 64 float4
                     const int blk = e >> 6, q = e & 63;
@@ -540,60 +547,63 @@ __global__ void __launch_bounds__(NT, 1)
                 }
             }
             __syncthreads();
-            // (b) 16 -> 32: T_RC = -T_RR (A_RC T_CC) for (R, C) = (1, 0), (3, 2)
+            // (b) 16 -> 32: T_RC = -T_RR (A_RC T_CC) for (R, C) = (1, 0), (3, 2); one output each
             {
-                const int blk = tid >> 7, rr = (tid >> 3) & 15, cp = (tid & 7) * 2;
+                const int blk = tid >> 8, rr = (tid >> 4) & 15, cc = tid & 15;
                 const int R = 2 * blk + 1, Cb = 2 * blk;
-                float x0 = 0.f, x1 = 0.f;
+                const float* arow = Af + (16 * R + rr) * 64;           // (row & 15) == rr
+                const int cch = 4 * Cb + (cc >> 2), cl = cc & 3;
+                float x = 0.f;
 #pragma unroll
                 for (int l = 0; l < 16; ++l) {
-                    const float a = Af[swz(16 * R + rr, 16 * Cb + l)];
-                    const float2 tv = *reinterpret_cast<const float2*>(Tf + swz(16 * Cb + l, 16 * Cb + cp));
+                    const float a = arow[(((4 * Cb + (l >> 2)) ^ rr) << 2) + (l & 3)];
+                    x = fmaf(a, Tf[(16 * Cb + l) * 64 + ((cch ^ l) << 2) + cl], x);
+                }
+                Tf[(16 * R + rr) * 64 + ((cch ^ rr) << 2) + cl] = x;
+                __syncthreads();
+                const float* trow = Tf + (16 * R + rr) * 64;
+                float y = 0.f;
+#pragma unroll
+                for (int l = 0; l < 16; ++l) {
+                    const float a = trow[(((4 * R + (l >> 2)) ^ rr) << 2) + (l & 3)];
+                    y = fmaf(a, Tf[(16 * R + l) * 64 + ((cch ^ l) << 2) + cl], y);
+                }
+                __syncthreads();
+                Tf[(16 * R + rr) * 64 + ((cch ^ rr) << 2) + cl] = -y;
+            }
+            __syncthreads();
+            // (c) 32 -> 64: T[32:64, 0:32] = -T[32:64, 32:64] (A[32:64, 0:32] T[0:32, 0:32]);
+            //     two adjacent outputs per thread
+            {
+                const int rr = tid >> 4, cp = (tid & 15) * 2;
+                const int rx = rr & 15, cch = cp >> 2, cl = cp & 3;
+                const float* arow = Af + (32 + rr) * 64;
+                float x0 = 0.f, x1 = 0.f;
+#pragma unroll
+                for (int l = 0; l < 32; ++l) {
+                    const float a = arow[((((l >> 2)) ^ rx) << 2) + (l & 3)];
+                    const float2 tv = *reinterpret_cast<const float2*>(Tf + l * 64 + ((cch ^ (l & 15)) << 2) + cl);
                     x0 = fmaf(a, tv.x, x0);
                     x1 = fmaf(a, tv.y, x1);
                 }
-                *reinterpret_cast<float2*>(Tf + swz(16 * R + rr, 16 * Cb + cp)) = make_float2(x0, x1);
+                *reinterpret_cast<float2*>(Tf + (32 + rr) * 64 + ((cch ^ rx) << 2) + cl) = make_float2(x0, x1);
                 __syncthreads();
+                const float* trow = Tf + (32 + rr) * 64;
                 float y0 = 0.f, y1 = 0.f;
 #pragma unroll
-                for (int l = 0; l < 16; ++l) {
-                    const float a = Tf[swz(16 * R + rr, 16 * R + l)];
-                    const float2 xv = *reinterpret_cast<const float2*>(Tf + swz(16 * R + l, 16 * Cb + cp));
+                for (int l = 0; l < 32; ++l) {
+                    const float a = trow[((((32 + l) >> 2) ^ rx) << 2) + (l & 3)];
+                    const float2 xv = *reinterpret_cast<const float2*>(Tf + (32 + l) * 64 + ((cch ^ (l & 15)) << 2) + cl);
                     y0 = fmaf(a, xv.x, y0);
                     y1 = fmaf(a, xv.y, y1);
                 }
                 __syncthreads();
-                *reinterpret_cast<float2*>(Tf + swz(16 * R + rr, 16 * Cb + cp)) = make_float2(-y0, -y1);
+                *reinterpret_cast<float2*>(Tf + (32 + rr) * 64 + ((cch ^ rx) << 2) + cl) = make_float2(-y0, -y1);
             }
             __syncthreads();
-            // (c) 32 -> 64: T[32:64, 0:32] = -T[32:64, 32:64] (A[32:64, 0:32] T[0:32, 0:32])
+            // T -> bf16 K-major [t][i], one 8-element group per thread
             {
-                const int rr = tid >> 3, cq = (tid & 7) * 4;
-                float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 8
-                for (int l = 0; l < 32; ++l) {
-                    const float a = Af[swz(32 + rr, l)];
-                    const float4 tv = *reinterpret_cast<const float4*>(Tf + swz(l, cq));
-                    x.x = fmaf(a, tv.x, x.x); x.y = fmaf(a, tv.y, x.y);
-                    x.z = fmaf(a, tv.z, x.z); x.w = fmaf(a, tv.w, x.w);
-                }
-                *reinterpret_cast<float4*>(Tf + swz(32 + rr, cq)) = x;
-                __syncthreads();
-                float4 y = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 8
-                for (int l = 0; l < 32; ++l) {
-                    const float a = Tf[swz(32 + rr, 32 + l)];
-                    const float4 xv = *reinterpret_cast<const float4*>(Tf + swz(32 + l, cq));
-                    y.x = fmaf(a, xv.x, y.x); y.y = fmaf(a, xv.y, y.y);
-                    y.z = fmaf(a, xv.z, y.z); y.w = fmaf(a, xv.w, y.w);
-                }
-                __syncthreads();
-                *reinterpret_cast<float4*>(Tf + swz(32 + rr, cq)) = make_float4(-y.x, -y.y, -y.z, -y.w);
-            }
-            __syncthreads();
-            // T -> bf16 K-major [t][i]
-            for (int it = tid; it < 64 * 8; it += NT) {
-                const int t = it >> 3, i8 = it & 7;
+                const int t = tid >> 3, i8 = tid & 7;
                 const float4 a = *reinterpret_cast<const float4*>(Tf + swz(t, i8 * 8));
                 const float4 b = *reinterpret_cast<const float4*>(Tf + swz(t, i8 * 8 + 4));
                 const float f[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
@@ -614,23 +624,24 @@ __global__ void __launch_bounds__(NT, 1)
         KDA_WAIT_MMA();
         if (failed) break;
         {
-            // warps 0-3: W^T row c -> [W^T | .] operand; warps 4-7: U^T row v -> K-major operand
-            const int row = tid & 127;
-            const uint32_t col = warp < 4 ? TM_W : TM_U;
-#pragma unroll 1
-            for (int t0c = 0; t0c < 64; t0c += 16) {
+            // parts 0-1: W^T row c, columns 32*part.. -> [W^T | .]; parts 2-3: U^T row v -> K-major
+            const bool is_u = part >= 2;
+            const int cb = 32 * (part & 1);
+            const uint32_t col = is_u ? TM_U : TM_W;
+#pragma unroll
+            for (int t0c = cb; t0c < cb + 32; t0c += 16) {
                 uint32_t d[16];
                 tc::tmem_ld16(taddr(tmem, warp, col + t0c), d);
                 tc::tmem_ld_wait();
                 float f[16];
 #pragma unroll
                 for (int j = 0; j < 16; ++j) f[j] = __uint_as_float(d[j]);
-                if (warp < 4) store16_mn(sm + OFF_A1, row, t0c, 16384, f);
+                if (!is_u) store16_mn(sm + OFF_A1, row, t0c, 16384, f);
                 else store16_k(sm + OFF_LVL + LV_UT, row, t0c, 128, f);
             }
             // Q Gamma (MN-major [t][c]) and K~ = K e^{G_last - G} (MN-major [t][c])
 #pragma unroll 1
-            for (int it = 0; it < 4; ++it) {
+            for (int it = 0; it < 2; ++it) {
                 const int item = tid + NT * it, t = item >> 4, c8 = item & 15;
                 float qf[8], kf[8], g8[8], gl[8], o[8];
                 unpack8(*reinterpret_cast<const uint4*>(sm + OFF_Q + t * 256 + c8 * 16), qf);
@@ -671,24 +682,22 @@ __global__ void __launch_bounds__(NT, 1)
             tc::tma_load_3d(sm + OFF_V, &tm_v, 0, t0 + C, (int)bh, &ms.bar_tma);
             tc::tma_load_3d(sm + OFF_LVL + LV_Z, &tm_z, 0, t0 + C, (int)bh, &ms.bar_tma);
         }
-        if (warp < 4) {
-            const int c = tid;
-#pragma unroll 1
-            for (int t0c = 0; t0c < 64; t0c += 16) {
+        {
+            // Q'^T row c, columns 16*part.. -> [. | Q'^T];  S <- diag(Gamma_last) S in TMEM
+            // (this chunk's bf16 copy of S stays unscaled)
+            const int c = row;
+            {
                 uint32_t d[16];
-                tc::tmem_ld16(taddr(tmem, warp, TM_QP + t0c), d);
+                tc::tmem_ld16(taddr(tmem, warp, TM_QP + 16 * part), d);
                 tc::tmem_ld_wait();
                 float f[16];
 #pragma unroll
                 for (int j = 0; j < 16; ++j) f[j] = __uint_as_float(d[j]);
-                store16_mn(sm + OFF_A1, c, 64 + t0c, 16384, f);
+                store16_mn(sm + OFF_A1, c, 64 + 16 * part, 16384, f);
             }
-        } else {
-            // S <- diag(Gamma_last) S in TMEM (lane c); the bf16 copy for this chunk is unscaled
-            const int c = tid - 128;
             const float gl = ex2(G2[63 * KD + c]);
-#pragma unroll 1
-            for (int v0 = 0; v0 < VD; v0 += 16) {
+#pragma unroll
+            for (int v0 = 32 * part; v0 < 32 * part + 32; v0 += 16) {
                 uint32_t d[16];
                 tc::tmem_ld16(taddr(tmem, warp, TM_S + v0), d);
                 tc::tmem_ld_wait();
@@ -711,30 +720,26 @@ __global__ void __launch_bounds__(NT, 1)
         KDA_WAIT_MMA();
         if (failed) break;
         // ---------------------------------------------------------------- C2
-        if (warp < 4) {
+        {
             // lane v: Delta^T[v][t] = U^T[v][t] - (W S)^T[v][t]  -> K-major B operand [v][t]
-            //         o[t][v] = scale ((Q' S)^T[v][t] + U'^T[v][t])
-            const int v = tid;
-            __nv_bfloat16* ocol = out + (bh * T + t0) * VD + v;
-#pragma unroll 1
-            for (int t0c = 0; t0c < 64; t0c += 16) {
-                uint32_t dw[16], du[16], dq[16], dp[16];
-                tc::tmem_ld16(taddr(tmem, warp, TM_D1 + t0c), dw);
-                tc::tmem_ld16(taddr(tmem, warp, TM_U + t0c), du);
-                tc::tmem_ld16(taddr(tmem, warp, TM_D1 + 64 + t0c), dq);
-                tc::tmem_ld16(taddr(tmem, warp, TM_UP + t0c), dp);
-                tc::tmem_ld_wait();
-                float f[16];
+            //         o[t][v] = scale ((Q' S)^T[v][t] + U'^T[v][t]);  this warp: t in 16*part..
+            const int v = row, tb = 16 * part;
+            uint32_t dw[16], du[16], dq[16], dp[16];
+            tc::tmem_ld16(taddr(tmem, warp, TM_D1 + tb), dw);
+            tc::tmem_ld16(taddr(tmem, warp, TM_U + tb), du);
+            tc::tmem_ld16(taddr(tmem, warp, TM_D1 + 64 + tb), dq);
+            tc::tmem_ld16(taddr(tmem, warp, TM_UP + tb), dp);
+            tc::tmem_ld_wait();
+            float f[16];
 #pragma unroll
-                for (int j = 0; j < 16; ++j) f[j] = __uint_as_float(du[j]) - __uint_as_float(dw[j]);
-                store16_k(sm + OFF_LVL + LV_DELTA, v, t0c, 128, f);
+            for (int j = 0; j < 16; ++j) f[j] = __uint_as_float(du[j]) - __uint_as_float(dw[j]);
+            store16_k(sm + OFF_LVL + LV_DELTA, v, tb, 128, f);
+            __nv_bfloat16* ocol = out + (bh * T + t0 + tb) * VD + v;
 #pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    const int t = t0c + j;
-                    if (t < cn)
-                        ocol[(size_t)t * VD] =
-                            __float2bfloat16_rn(scale * (__uint_as_float(dq[j]) + __uint_as_float(dp[j])));
-                }
+            for (int j = 0; j < 16; ++j) {
+                if (tb + j < cn)
+                    ocol[(size_t)j * VD] =
+                        __float2bfloat16_rn(scale * (__uint_as_float(dq[j]) + __uint_as_float(dp[j])));
             }
         }
         KDA_SYNC_FOR_MMA();
@@ -749,10 +754,10 @@ __global__ void __launch_bounds__(NT, 1)
         KDA_WAIT_MMA();
         if (failed) break;
         {
-            // S (fp32, TMEM) -> bf16 operand [c][v]; warps 0-3 take v < 64, warps 4-7 v >= 64
-            const int c = tid & 127, vb = (warp >> 2) * 64;
-#pragma unroll 1
-            for (int v0 = vb; v0 < vb + 64; v0 += 16) {
+            // S (fp32, TMEM) -> bf16 operand [c][v]; this warp: v in 32*part..
+            const int c = row;
+#pragma unroll
+            for (int v0 = 32 * part; v0 < 32 * part + 32; v0 += 16) {
                 uint32_t d[16];
                 tc::tmem_ld16(taddr(tmem, warp, TM_S + v0), d);
                 tc::tmem_ld_wait();
@@ -767,10 +772,10 @@ __global__ void __launch_bounds__(NT, 1)
 #undef KDA_WAIT_MMA
 #undef KDA_SYNC_FOR_MMA
 
-    if (!failed && hT && tid < KD) {
-        const int c = tid;
-#pragma unroll 1
-        for (int v0 = 0; v0 < VD; v0 += 16) {
+    if (!failed && hT) {
+        const int c = row;
+#pragma unroll
+        for (int v0 = 32 * part; v0 < 32 * part + 32; v0 += 16) {
             uint32_t d[16];
             tc::tmem_ld16(taddr(tmem, warp, TM_S + v0), d);
             tc::tmem_ld_wait();
