@@ -42,6 +42,20 @@ def bytes_per_token_head(K, V, io_bytes=2):
     return io_bytes * (3 * K + V) + io_bytes * V + io_bytes
 
 
+def measured_traffic(kernel, source):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary (profiles/traffic.json),
+    or None when the kernel's source has changed since those counters were taken."""
+    import hashlib
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as fh:
+            entry = json.load(fh)[kernel]
+        with open(os.path.join(ROOT, "gated_delta_rule_26_gb300", "csrc", source), "rb") as fh:
+            digest = hashlib.sha256(fh.read()).hexdigest()
+    except (OSError, KeyError, ValueError):
+        return None
+    return entry["dram_bytes_per_launch"] if entry.get("source_sha256") == digest else None
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -214,7 +228,10 @@ def run_decode(args, kda, inputs, peaks, ws, barrier):
               "state_GBps": dbytes / dper / 1e9,
               "roofline": {"bound": "hbm", "achieved": dbytes / dper / 1e9,
                            "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                           "frac": dbytes / dper / 1e9 / peaks["hbm_gbs"], "traffic": None},
+                           "frac": dbytes / dper / 1e9 / peaks["hbm_gbs"],
+                           "traffic": measured_traffic("decode_kernel", "decode.cu")
+                           if dec.B == 256 else None,
+                           "algorithmic_bytes": dbytes},
               "config": {"workload": f"decode_bf16 B{dec.B} H{dec.H} K={dec.K} V={dec.V}, "
                                      f"{dec.steps} consecutive steps",
                          "bytes_per_step": dbytes}}
@@ -300,7 +317,9 @@ def main():
     # kernel the step time is that kernel's time.
     achieved_gbs = alg_bytes / per_step / 1e9
     roofline = {"bound": "hbm", "achieved": achieved_gbs, "peak": peaks["hbm_gbs"],
-                "unit": "GB/s", "frac": achieved_gbs / peaks["hbm_gbs"], "traffic": None,
+                "unit": "GB/s", "frac": achieved_gbs / peaks["hbm_gbs"],
+                "traffic": measured_traffic("kda_chunk_tc_kernel", "chunk_tc.cu"),
+                "algorithmic_bytes": alg_bytes,
                 "kernel": "kda chunked forward", "kernels_per_step": kernels_per_step,
                 "peak_source": peaks["source"]}
     tflops = flops / per_step / 1e12

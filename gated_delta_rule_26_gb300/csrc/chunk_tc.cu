@@ -4,10 +4,12 @@
 // One CTA (16 warps) owns one (b, h) sequence and walks its chunks in order.
 // The fp32 state S (K x V) lives in TMEM for the whole sequence; per chunk:
 //
-//   P1  TMA: q, k, v, z tiles (64 x 128 bf16 each) into shared memory; the
-//       next chunk's tiles are requested as soon as this chunk's are consumed.
+//   P1  TMA: q, k, z tiles (64 x 128 bf16 each) and the v tile, on two
+//       mbarriers; the next chunk's tiles are requested as soon as each slot is
+//       consumed (q, k, z during P5, v after C3).
 //   P2  gate g = -exp(A_log) softplus(z + dt_bias) and the in-chunk cumulative
-//       log decay G (kdafix-2026-10-02 "Fix 1"; kda-adjoint-2026-10-01 sec. 2).
+//       log decay G (kdafix-2026-10-02 "Fix 1"; kda-adjoint-2026-10-01 sec. 2);
+//       for chunk n+1 this runs on warps 8-15 while warps 0-7 do chunk n's C1-C3.
 //   P3  decay-folded scores  A[t,i] = beta_t sum_c k_tc k_ic e^{G_tc - G_ic}  (i < t)
 //       and M[t,i] = sum_c q_tc k_ic e^{G_tc - G_ic}  (i <= t) on the tensor cores.
 //       e^{G_t - G_i} cannot be split as e^{G_t} e^{-G_i} (e^{-G_i} overflows
@@ -66,29 +68,31 @@ constexpr uint32_t OFF_S = OFF_A1 + 32768;      // 32 KB S bf16, MN-major [c][v]
 constexpr uint32_t OFF_ID = OFF_S + 32768;      // 8 KB 64 x 64 identity, K-major bf16
 constexpr uint32_t OFF_MISC = OFF_ID + 8192;
 // multi-use region, in order of use within a chunk
-constexpr uint32_t LV_Z = 0;        // z tile (16 KB)                    P1-P2
-constexpr uint32_t LV_L0 = 0;       // level operand buffer 0 (32 KB)    P3
-constexpr uint32_t LV_L1 = 32768;   // level operand buffer 1 (32 KB)    P3
-constexpr uint32_t LV_AF = 0;       // A fp32 [t][i] (16 KB)             P3-P4
-constexpr uint32_t LV_MB = 16384;   // M bf16 K-major [t][i] (8 KB)      P3-P5
-constexpr uint32_t LV_TB = 24576;   // T bf16 K-major [t][i] (8 KB)      P4-P5
-constexpr uint32_t LV_BKG = 32768;  // beta K Gamma, MN-major [t][c]     P3-P5
-constexpr uint32_t LV_BV = 49152;   // beta V, MN-major [t][v]           P3-P5
-constexpr uint32_t LV_UT = 0;       // U^T K-major [v][i] (16 KB)        P5
-constexpr uint32_t LV_QG = 32768;   // Q Gamma, MN-major [t][c] (16 KB)  P5
-constexpr uint32_t LV_KT = 49152;   // K~ MN-major [t][c] (16 KB)        P5-C3
-constexpr uint32_t LV_DELTA = 16384;// Delta^T K-major [v][t] (16 KB)    C2-C3
+constexpr uint32_t LV_L0 = 0;       // level operand buffer 0 (32 KB)        P3
+constexpr uint32_t LV_L1 = 32768;   // level operand buffer 1 (32 KB)        P3
+constexpr uint32_t LV_AF = 0;       // A fp32 [t][i] (16 KB, swizzled)       P3-P4
+constexpr uint32_t LV_MB = 16384;   // M bf16 K-major [t][i] (8 KB)          P3-P5
+constexpr uint32_t LV_TB = 24576;   // T bf16 K-major [t][i] (8 KB)          P4-P5
+constexpr uint32_t LV_BKG = 32768;  // beta K Gamma, MN-major [t][c]         P3-P5
+constexpr uint32_t LV_BV = 49152;   // beta V, MN-major [t][v]               P3-P5
+constexpr uint32_t LV_QG = 0;       // Q Gamma, MN-major [t][c] (16 KB)      P5
+constexpr uint32_t LV_UT = 32768;   // U^T K-major [v][i] (16 KB)            P5
+constexpr uint32_t LV_Z = 49152;    // z tile of the NEXT chunk (16 KB)      P5-P2
+constexpr uint32_t LV_DELTA = 16384;// Delta^T K-major [v][t] (16 KB)        C2-C3
+constexpr uint32_t LV_OST = 0;      // o staging, row-major [t][v] bf16      C2
+// K~ (K e^{G_last - G}, MN-major [t][c]) lives in the v-tile slot OFF_V from P5 to C3.
 
 struct Misc {
     alignas(16) float dt[KD];      // read as float4
     alignas(16) float beta[C];
     alignas(16) float diag[16][16];
-    alignas(16) uint64_t bar_tma;
-    uint64_t bar_mma;
+    alignas(16) uint64_t bar_qkz;  // TMA: q, k, z tiles of a chunk
+    uint64_t bar_v;                // TMA: v tile of a chunk
+    uint64_t bar_m0, bar_m1;       // tensor-core commits, alternating
     uint32_t tmem_base;
 };
 static_assert(offsetof(Misc, dt) % 16 == 0 && offsetof(Misc, beta) % 16 == 0 &&
-                  offsetof(Misc, bar_tma) % 8 == 0 && OFF_MISC % 16 == 0,
+                  offsetof(Misc, bar_qkz) % 8 == 0 && OFF_MISC % 16 == 0,
               "shared-memory block alignment");
 constexpr uint32_t SMEM_BYTES = OFF_MISC + sizeof(Misc) + 1024;
 
@@ -123,9 +127,15 @@ __device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
     return make_uint4(tc::pack_bf16x2(f[0], f[1]), tc::pack_bf16x2(f[2], f[3]),
                       tc::pack_bf16x2(f[4], f[5]), tc::pack_bf16x2(f[6], f[7]));
 }
-__device__ __forceinline__ void load8(const float* p, float (&f)[8]) {
-    const float4 a = *reinterpret_cast<const float4*>(p);
-    const float4 b = *reinterpret_cast<const float4*>(p + 4);
+// G2 (fp32, 64 tokens x 128 channels) keeps each row as two halves: channel
+// c = 8 a + 4 h + j sits at 64 h + 4 a + j, so that both the 8-channel groups read by
+// (token, 8 channels) items and the 4-channel groups read by (token, lane) items are
+// contiguous across a warp.
+__device__ __forceinline__ int gsw(int c) { return ((c >> 2) & 1) * 64 + (c >> 3) * 4 + (c & 3); }
+__device__ __forceinline__ int g4off(int lane) { return (lane & 1) * 64 + (lane >> 1) * 4; }
+__device__ __forceinline__ void load8g(const float* G2, int t, int c8, float (&f)[8]) {
+    const float4 a = *reinterpret_cast<const float4*>(G2 + t * 128 + c8 * 4);
+    const float4 b = *reinterpret_cast<const float4*>(G2 + t * 128 + 64 + c8 * 4);
     f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w; f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
 }
 // softplus(x) = max(x, 0) + log(1 + e^{-|x|}) with the hardware exp2/log2 approximations.
@@ -167,36 +177,34 @@ __device__ __forceinline__ uint32_t taddr(uint32_t base, int warp, uint32_t col)
     return base + ((uint32_t)((warp & 3) * 32) << 16) + col;
 }
 
-// Build two levels' operands: rows 0..63 hold k_t scaled to the level's reference,
-// rows 64..127 hold q_t scaled (upper-half tokens only).  G2 is the in-chunk
+// Build one level's operand in `buf`: rows 0..63 hold k_t scaled to the level's
+// reference, rows 64..127 hold q_t scaled (upper-half tokens only).  G2 is the in-chunk
 // cumulative log decay in log2 units, so every factor is one ex2 of a difference <= 0.
-__device__ __forceinline__ void build_levels(uint8_t* sm, int li0, int tid) {
+__device__ __forceinline__ void build_level(uint8_t* sm, int li, uint32_t buf, int tid) {
     const float* G2 = reinterpret_cast<const float*>(sm + OFF_G);
     const int c8 = tid & 15;
-#pragma unroll 1
+    const int h = 32 >> li;
+    uint8_t* L = sm + OFF_LVL + buf;
+#pragma unroll
     for (int r = 0; r < 2; ++r) {
         const int t = (tid >> 4) + 32 * r;
-        float kf[8], qf[8], g8[8];
+        const int ref = (t & ~(2 * h - 1)) + h - 1;
+        const bool upper = (t & h) != 0;
+        float kf[8], qf[8], g8[8], r8[8], f[8], kv[8], qv[8];
         unpack8(*reinterpret_cast<const uint4*>(sm + OFF_K + t * 256 + c8 * 16), kf);
-        unpack8(*reinterpret_cast<const uint4*>(sm + OFF_Q + t * 256 + c8 * 16), qf);
-        load8(G2 + t * KD + c8 * 8, g8);
+        load8g(G2, t, c8, g8);
+        load8g(G2, ref, c8, r8);
 #pragma unroll
-        for (int l = 0; l < 2; ++l) {
-            const int li = li0 + l;
-            const int h = 32 >> li;
-            const int ref = (t & ~(2 * h - 1)) + h - 1;
-            const bool upper = (t & h) != 0;
-            float r8[8], kv[8], qv[8];
-            load8(G2 + ref * KD + c8 * 8, r8);
+        for (int j = 0; j < 8; ++j) {
+            f[j] = ex2(upper ? g8[j] - r8[j] : r8[j] - g8[j]);
+            kv[j] = kf[j] * f[j];
+        }
+        *reinterpret_cast<uint4*>(L + kmaj_off(t, c8 * 8, 128)) = pack8(kv);
+        if (upper) {
+            unpack8(*reinterpret_cast<const uint4*>(sm + OFF_Q + t * 256 + c8 * 16), qf);
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const float f = ex2(upper ? g8[j] - r8[j] : r8[j] - g8[j]);
-                kv[j] = kf[j] * f;
-                qv[j] = qf[j] * f;
-            }
-            uint8_t* L = sm + OFF_LVL + (l ? LV_L1 : LV_L0);
-            *reinterpret_cast<uint4*>(L + kmaj_off(t, c8 * 8, 128)) = pack8(kv);
-            if (upper) *reinterpret_cast<uint4*>(L + kmaj_off(64 + t, c8 * 8, 128)) = pack8(qv);
+            for (int j = 0; j < 8; ++j) qv[j] = qf[j] * f[j];
+            *reinterpret_cast<uint4*>(L + kmaj_off(64 + t, c8 * 8, 128)) = pack8(qv);
         }
     }
 }
@@ -237,8 +245,10 @@ __global__ void __launch_bounds__(NT, 1)
         reinterpret_cast<uint4*>(sm)[i] = make_uint4(0u, 0u, 0u, 0u);
     if (tid < KD) ms.dt[tid] = dt_bias[(size_t)h * KD + tid];
     if (tid == 0) {
-        tc::mbar_init(&ms.bar_tma, 1);
-        tc::mbar_init(&ms.bar_mma, 1);
+        tc::mbar_init(&ms.bar_qkz, 1);
+        tc::mbar_init(&ms.bar_v, 1);
+        tc::mbar_init(&ms.bar_m0, 1);
+        tc::mbar_init(&ms.bar_m1, 1);
         tc::fence_barrier_init();
         tc::tma_prefetch_desc(&tm_q);
         tc::tma_prefetch_desc(&tm_k);
@@ -281,21 +291,72 @@ __global__ void __launch_bounds__(NT, 1)
     __syncthreads();
     tc::fence_after_sync();
 
-    uint32_t tma_phase = 0, mma_phase = 0;
+    uint32_t ph_qkz = 0, ph_v = 0, ph0 = 0, ph1 = 0;
     bool failed = false;
     const int nchunks = (T + C - 1) / C;
+    const bool group_c = warp < 8;  // carry group; warps 8-15 form the gate group
     if (tid == 0 && nchunks > 0) {
-        tc::mbar_arrive_expect_tx(&ms.bar_tma, 4u * 16384u);
-        tc::tma_load_3d(sm + OFF_Q, &tm_q, 0, 0, (int)bh, &ms.bar_tma);
-        tc::tma_load_3d(sm + OFF_K, &tm_k, 0, 0, (int)bh, &ms.bar_tma);
-        tc::tma_load_3d(sm + OFF_V, &tm_v, 0, 0, (int)bh, &ms.bar_tma);
-        tc::tma_load_3d(sm + OFF_LVL + LV_Z, &tm_z, 0, 0, (int)bh, &ms.bar_tma);
+        tc::mbar_arrive_expect_tx(&ms.bar_qkz, 3u * 16384u);
+        tc::tma_load_3d(sm + OFF_Q, &tm_q, 0, 0, (int)bh, &ms.bar_qkz);
+        tc::tma_load_3d(sm + OFF_K, &tm_k, 0, 0, (int)bh, &ms.bar_qkz);
+        tc::tma_load_3d(sm + OFF_LVL + LV_Z, &tm_z, 0, 0, (int)bh, &ms.bar_qkz);
+        tc::mbar_arrive_expect_tx(&ms.bar_v, 16384u);
+        tc::tma_load_3d(sm + OFF_V, &tm_v, 0, 0, (int)bh, &ms.bar_v);
     }
 
-#define KDA_WAIT_MMA()                                                   \
+    // Gate of chunk `nc` by the gate group (warps 8-15, named barrier 2): waits for its
+    // q/k/z tiles, loads beta, and writes G2 = in-chunk cumulative log2 decay.
+    auto gate_scan = [&](int nc) -> bool {
+        const int wg = warp - 8;
+        const bool ok = !tc::named_sync_or(2, 256, !(tid != 256 || tc::mbar_wait(&ms.bar_qkz, ph_qkz)));
+        const int tn = nc * C, cnn = min(C, T - tn);
+        const int tg = wg * 32 + lane;
+        if (tg < C) ms.beta[tg] = tg < cnn ? __bfloat162float(beta[bh * T + tn + tg]) : 0.f;
+        const int c4 = lane * 4;
+        const float4 dt = *reinterpret_cast<const float4*>(&ms.dt[c4]);
+        const float mult = -exp_A * LOG2E;
+        float acc0 = 0.f, acc1 = 0.f, acc2 = 0.f, acc3 = 0.f;
+#pragma unroll
+        for (int a = 0; a < 8; ++a) {
+            const int t = 8 * wg + a;
+            const uint2 zr = *reinterpret_cast<const uint2*>(sm + OFF_LVL + LV_Z + t * 256 + c4 * 2);
+            const float x0 = bf_lo(zr.x) + dt.x, x1 = bf_hi(zr.x) + dt.y;
+            const float x2 = bf_lo(zr.y) + dt.z, x3 = bf_hi(zr.y) + dt.w;
+            const float m = (t < cnn) ? mult : 0.f;
+            acc0 = fmaf(m, softplus_fast(x0), acc0);
+            acc1 = fmaf(m, softplus_fast(x1), acc1);
+            acc2 = fmaf(m, softplus_fast(x2), acc2);
+            acc3 = fmaf(m, softplus_fast(x3), acc3);
+            *reinterpret_cast<float4*>(G2 + t * KD + g4off(lane)) = make_float4(acc0, acc1, acc2, acc3);
+        }
+        tc::named_sync(2, 256);
+        float4 pre = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int g = 0; g < wg; ++g) {
+            const float4 x = *reinterpret_cast<const float4*>(G2 + (8 * g + 7) * KD + g4off(lane));
+            pre.x += x.x; pre.y += x.y; pre.z += x.z; pre.w += x.w;
+        }
+        tc::named_sync(2, 256);
+        if (wg > 0) {
+#pragma unroll
+            for (int a = 0; a < 8; ++a) {
+                float4* p = reinterpret_cast<float4*>(G2 + (8 * wg + a) * KD + g4off(lane));
+                float4 x = *p;
+                x.x += pre.x; x.y += pre.y; x.z += pre.z; x.w += pre.w;
+                *p = x;
+            }
+        }
+        return ok;
+    };
+
+    if (nchunks > 0 && !group_c) failed = !gate_scan(0);
+    ph_qkz ^= 1u;
+    if (__syncthreads_or(failed)) failed = true;
+
+// One thread polls the mbarrier; the others sleep in the CTA barrier that follows.
+#define KDA_WAIT(bar, ph)                                                \
     do {                                                                 \
-        const bool ok_ = tc::mbar_wait(&ms.bar_mma, mma_phase);          \
-        mma_phase ^= 1u;                                                 \
+        const bool ok_ = tid != 0 || tc::mbar_wait(&ms.bar, ph);         \
+        ph ^= 1u;                                                        \
         if (__syncthreads_or(!ok_)) failed = true;                       \
         tc::fence_after_sync();                                          \
     } while (0)
@@ -306,70 +367,41 @@ __global__ void __launch_bounds__(NT, 1)
         __syncthreads();                                                 \
         tc::fence_after_sync();                                          \
     } while (0)
+#define KDA_LEVEL_MMA(buf, col, bar)                                     \
+    do {                                                                 \
+        if (tid == 0) {                                                  \
+            const uint32_t L_ = sb + OFF_LVL + (buf);                    \
+            _Pragma("unroll") for (int ks = 0; ks < 8; ++ks)             \
+                tc::mma_bf16(tmem + (col), desc_k(L_, 128, ks),          \
+                             desc_k(L_, 128, ks), IDESC_LVL, ks > 0);    \
+            tc::mma_commit(&ms.bar);                                     \
+        }                                                                \
+    } while (0)
 
     for (int n = 0; n < nchunks && !failed; ++n) {
         const int t0 = n * C, cn = min(C, T - t0);
-        // ---------------------------------------------------------------- P1
-        // (this chunk's tiles were requested by the previous chunk, or above for chunk 0)
-        if (tid < C)
-            ms.beta[tid] = tid < cn ? __bfloat162float(beta[bh * T + t0 + tid]) : 0.f;
-        {
-            const bool ok = tc::mbar_wait(&ms.bar_tma, tma_phase);
-            tma_phase ^= 1u;
-            if (__syncthreads_or(!ok)) { failed = true; break; }
-        }
-        // ---------------------------------------------------------------- P2
-        {
-            // warp w: tokens 4w..4w+3; lane: channels 4*lane..4*lane+3 (G2 in log2 units)
-            const int c4 = lane * 4;
-            const float4 dt = *reinterpret_cast<const float4*>(&ms.dt[c4]);
-            const float mult = -exp_A * LOG2E;
-            float acc0 = 0.f, acc1 = 0.f, acc2 = 0.f, acc3 = 0.f;
-#pragma unroll
-            for (int a = 0; a < 4; ++a) {
-                const int t = 4 * warp + a;
-                const uint2 zr = *reinterpret_cast<const uint2*>(sm + OFF_LVL + LV_Z + t * 256 + c4 * 2);
-                const float x0 = bf_lo(zr.x) + dt.x, x1 = bf_hi(zr.x) + dt.y;
-                const float x2 = bf_lo(zr.y) + dt.z, x3 = bf_hi(zr.y) + dt.w;
-                const float m = (t < cn) ? mult : 0.f;
-                acc0 = fmaf(m, softplus_fast(x0), acc0);
-                acc1 = fmaf(m, softplus_fast(x1), acc1);
-                acc2 = fmaf(m, softplus_fast(x2), acc2);
-                acc3 = fmaf(m, softplus_fast(x3), acc3);
-                *reinterpret_cast<float4*>(G2 + t * KD + c4) = make_float4(acc0, acc1, acc2, acc3);
-            }
-            __syncthreads();
-            float4 pre = make_float4(0.f, 0.f, 0.f, 0.f);
-            for (int g = 0; g < warp; ++g) {
-                const float4 x = *reinterpret_cast<const float4*>(G2 + (4 * g + 3) * KD + c4);
-                pre.x += x.x; pre.y += x.y; pre.z += x.z; pre.w += x.w;
-            }
-            __syncthreads();
-            if (warp > 0) {
-#pragma unroll
-                for (int a = 0; a < 4; ++a) {
-                    float4* p = reinterpret_cast<float4*>(G2 + (4 * warp + a) * KD + c4);
-                    float4 x = *p;
-                    x.x += pre.x; x.y += pre.y; x.z += pre.z; x.w += pre.w;
-                    *p = x;
-                }
-            }
-        }
-        __syncthreads();
-        // ---------------------------------------------------------------- P3: levels 32, 16
-        build_levels(sm, 0, tid);
+        // ---------------------------------------------------------------- P3: level 32
+        // one level per buffer, so each level's GEMM overlaps the next level's build
+        build_level(sm, 0, LV_L0, tid);
         KDA_SYNC_FOR_MMA();
-        if (tid == 0) {
-#pragma unroll
-            for (int l = 0; l < 2; ++l) {
-                const uint32_t L = sb + OFF_LVL + (l ? LV_L1 : LV_L0);
-#pragma unroll
-                for (int ks = 0; ks < 8; ++ks)
-                    tc::mma_bf16(tmem + TM_LVL + 64 * l, desc_k(L, 128, ks), desc_k(L, 128, ks),
-                                 IDESC_LVL, ks > 0);
-            }
-            tc::mma_commit(&ms.bar_mma);
-        }
+        KDA_LEVEL_MMA(LV_L0, TM_LVL, bar_m0);
+        // ---------------------------------------------------------------- P3: level 16
+        build_level(sm, 1, LV_L1, tid);
+        KDA_SYNC_FOR_MMA();
+        KDA_LEVEL_MMA(LV_L1, TM_LVL + 64, bar_m1);
+        // ---------------------------------------------------------------- P3: level 8
+        KDA_WAIT(bar_m0, ph0);
+        if (failed) break;
+        build_level(sm, 2, LV_L0, tid);
+        KDA_SYNC_FOR_MMA();
+        KDA_LEVEL_MMA(LV_L0, TM_LVL + 128, bar_m0);
+        // ---------------------------------------------------------------- P3: level 4
+        KDA_WAIT(bar_m1, ph1);
+        if (failed) break;
+        build_level(sm, 3, LV_L1, tid);
+        KDA_SYNC_FOR_MMA();
+        KDA_LEVEL_MMA(LV_L1, TM_LVL + 192, bar_m1);
+        // ---------------------------------------------------------------- P3: 4-token blocks
         // pairs inside 4-token blocks: exact pairwise decay, CUDA cores.
         // warp w = 4-token block w; lane = channels 4*lane..4*lane+3.
         {
@@ -382,7 +414,7 @@ __global__ void __launch_bounds__(NT, 1)
                 const uint2 qr = *reinterpret_cast<const uint2*>(sm + OFF_Q + t * 256 + c4 * 2);
                 kk[a][0] = bf_lo(kr.x); kk[a][1] = bf_hi(kr.x); kk[a][2] = bf_lo(kr.y); kk[a][3] = bf_hi(kr.y);
                 qq[a][0] = bf_lo(qr.x); qq[a][1] = bf_hi(qr.x); qq[a][2] = bf_lo(qr.y); qq[a][3] = bf_hi(qr.y);
-                const float4 g = *reinterpret_cast<const float4*>(G2 + t * KD + c4);
+                const float4 g = *reinterpret_cast<const float4*>(G2 + t * KD + g4off(lane));
                 gg[a][0] = g.x; gg[a][1] = g.y; gg[a][2] = g.z; gg[a][3] = g.w;
             }
             float v[16];
@@ -424,24 +456,15 @@ __global__ void __launch_bounds__(NT, 1)
             v[0] += __shfl_xor_sync(0xffffffffu, v[0], 1);
             if ((lane & 1) == 0) ms.diag[b4][lane >> 1] = v[0];
         }
-        KDA_WAIT_MMA();
-        if (failed) break;
-        // ---------------------------------------------------------------- P3: levels 8, 4
-        build_levels(sm, 2, tid);
-        KDA_SYNC_FOR_MMA();
-        if (tid == 0) {
-#pragma unroll
-            for (int l = 0; l < 2; ++l) {
-                const uint32_t L = sb + OFF_LVL + (l ? LV_L1 : LV_L0);
-#pragma unroll
-                for (int ks = 0; ks < 8; ++ks)
-                    tc::mma_bf16(tmem + TM_LVL + 128 + 64 * l, desc_k(L, 128, ks),
-                                 desc_k(L, 128, ks), IDESC_LVL, ks > 0);
-            }
-            tc::mma_commit(&ms.bar_mma);
+        {
+            const bool okv = tid != 0 || tc::mbar_wait(&ms.bar_v, ph_v);
+            const bool ok0 = tid != 0 || tc::mbar_wait(&ms.bar_m0, ph0);
+            const bool ok1 = tid != 0 || tc::mbar_wait(&ms.bar_m1, ph1);
+            ph_v ^= 1u; ph0 ^= 1u; ph1 ^= 1u;
+            if (__syncthreads_or(!(okv && ok0 && ok1))) failed = true;
+            tc::fence_after_sync();
+            if (failed) break;
         }
-        KDA_WAIT_MMA();
-        if (failed) break;
         // ---------------------------------------------------------------- P3 epilogue
         {
             // TMEM lane `row`: rows 0..63 are A rows (k side), rows 64..127 are M rows (q side);
@@ -505,7 +528,7 @@ __global__ void __launch_bounds__(NT, 1)
                 float kf[8], vf[8], g8[8], o[8];
                 unpack8(*reinterpret_cast<const uint4*>(sm + OFF_K + tt * 256 + c8 * 16), kf);
                 unpack8(*reinterpret_cast<const uint4*>(sm + OFF_V + tt * 256 + c8 * 16), vf);
-                load8(G2 + tt * KD + c8 * 8, g8);
+                load8g(G2, tt, c8, g8);
 #pragma unroll
                 for (int j = 0; j < 8; ++j) o[j] = bt * kf[j] * ex2(g8[j]);
                 *reinterpret_cast<uint4*>(sm + OFF_LVL + LV_BKG + mnmaj_off(tt, c8 * 8, 8192)) = pack8(o);
@@ -520,19 +543,31 @@ __global__ void __launch_bounds__(NT, 1)
         {
             const float* Af = reinterpret_cast<const float*>(sm + OFF_LVL + LV_AF);
             float* Tf = reinterpret_cast<float*>(sm + OFF_V);  // the v tile is consumed
-            // (a) the four 16 x 16 diagonal blocks by forward substitution, one column each;
-            //     the other threads clear the strictly upper blocks.
+            // Every A and T access below moves a 16-byte group (4 consecutive columns); the
+            // XOR swizzle keeps the groups a warp touches in distinct banks.
+            // (a) the four 16 x 16 diagonal blocks by forward substitution, one column each
+            //     (left-looking: x_t = delta_tj - sum_{i<t} A_ti x_i); the other threads clear the
+            //     strictly upper blocks.
             if (tid < 64) {
                 const int R = tid >> 4, j = tid & 15;
                 const float* Ab = Af + 16 * R * 64;  // rows 16R.. ; (row & 15) == t
                 float x[16];
 #pragma unroll
-                for (int t = 0; t < 16; ++t) x[t] = (t == j) ? 1.f : 0.f;
+                for (int t = 0; t < 16; ++t) {
+                    float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                for (int i = 0; i < 15; ++i)
+                    for (int q = 0; q < 4; ++q) {
+                        if (4 * q < t) {
+                            const float4 a4 =
+                                *reinterpret_cast<const float4*>(Ab + t * 64 + (((4 * R + q) ^ t) << 2));
+                            const float av[4] = {a4.x, a4.y, a4.z, a4.w};
 #pragma unroll
-                    for (int t = i + 1; t < 16; ++t)
-                        x[t] = fmaf(-Ab[t * 64 + ((((4 * R + (i >> 2)) ^ t)) << 2) + (i & 3)], x[i], x[t]);
+                            for (int u = 0; u < 4; ++u)
+                                if (4 * q + u < t) acc[u] = fmaf(av[u], x[4 * q + u], acc[u]);
+                        }
+                    }
+                    x[t] = ((t == j) ? 1.f : 0.f) - ((acc[0] + acc[1]) + (acc[2] + acc[3]));
+                }
                 float* Tb = Tf + 16 * R * 64;
 #pragma unroll
                 for (int t = 0; t < 16; ++t)
@@ -547,60 +582,103 @@ __global__ void __launch_bounds__(NT, 1)
                 }
             }
             __syncthreads();
-            // (b) 16 -> 32: T_RC = -T_RR (A_RC T_CC) for (R, C) = (1, 0), (3, 2); one output each
+        // ---------------------------------------------------------------- P4b: 16 -> 32 merge
+            // (b) 16 -> 32: T_RC = -T_RR (A_RC T_CC) for (R, C) = (1, 0), (3, 2);
+            //     warps 0-3, four adjacent outputs per thread
             {
-                const int blk = tid >> 8, rr = (tid >> 4) & 15, cc = tid & 15;
+                const int blk = tid >> 6, rr = (tid >> 2) & 15, cq = (tid & 3) * 4;
                 const int R = 2 * blk + 1, Cb = 2 * blk;
-                const float* arow = Af + (16 * R + rr) * 64;           // (row & 15) == rr
-                const int cch = 4 * Cb + (cc >> 2), cl = cc & 3;
-                float x = 0.f;
+                const int och = ((4 * Cb + (cq >> 2)) ^ rr) << 2;  // this thread's group in row rr
+                float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (tid < 128) {
+                    const float* arow = Af + (16 * R + rr) * 64;
 #pragma unroll
-                for (int l = 0; l < 16; ++l) {
-                    const float a = arow[(((4 * Cb + (l >> 2)) ^ rr) << 2) + (l & 3)];
-                    x = fmaf(a, Tf[(16 * Cb + l) * 64 + ((cch ^ l) << 2) + cl], x);
-                }
-                Tf[(16 * R + rr) * 64 + ((cch ^ rr) << 2) + cl] = x;
-                __syncthreads();
-                const float* trow = Tf + (16 * R + rr) * 64;
-                float y = 0.f;
+                    for (int q = 0; q < 4; ++q) {
+                        const float4 a4 = *reinterpret_cast<const float4*>(arow + (((4 * Cb + q) ^ rr) << 2));
+                        const float av[4] = {a4.x, a4.y, a4.z, a4.w};
 #pragma unroll
-                for (int l = 0; l < 16; ++l) {
-                    const float a = trow[(((4 * R + (l >> 2)) ^ rr) << 2) + (l & 3)];
-                    y = fmaf(a, Tf[(16 * R + l) * 64 + ((cch ^ l) << 2) + cl], y);
+                        for (int u = 0; u < 4; ++u) {
+                            const int l = 4 * q + u;
+                            const float4 tv = *reinterpret_cast<const float4*>(
+                                Tf + (16 * Cb + l) * 64 + (((4 * Cb + (cq >> 2)) ^ l) << 2));
+                            x.x = fmaf(av[u], tv.x, x.x); x.y = fmaf(av[u], tv.y, x.y);
+                            x.z = fmaf(av[u], tv.z, x.z); x.w = fmaf(av[u], tv.w, x.w);
+                        }
+                    }
+                    *reinterpret_cast<float4*>(Tf + (16 * R + rr) * 64 + och) = x;
                 }
                 __syncthreads();
-                Tf[(16 * R + rr) * 64 + ((cch ^ rr) << 2) + cl] = -y;
+                float4 y = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (tid < 128) {
+                    const float* trow = Tf + (16 * R + rr) * 64;
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const float4 a4 = *reinterpret_cast<const float4*>(trow + (((4 * R + q) ^ rr) << 2));
+                        const float av[4] = {a4.x, a4.y, a4.z, a4.w};
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) {
+                            const int l = 4 * q + u;
+                            const float4 xv = *reinterpret_cast<const float4*>(
+                                Tf + (16 * R + l) * 64 + (((4 * Cb + (cq >> 2)) ^ l) << 2));
+                            y.x = fmaf(av[u], xv.x, y.x); y.y = fmaf(av[u], xv.y, y.y);
+                            y.z = fmaf(av[u], xv.z, y.z); y.w = fmaf(av[u], xv.w, y.w);
+                        }
+                    }
+                }
+                __syncthreads();
+                if (tid < 128)
+                    *reinterpret_cast<float4*>(Tf + (16 * R + rr) * 64 + och) =
+                        make_float4(-y.x, -y.y, -y.z, -y.w);
             }
             __syncthreads();
+        // ---------------------------------------------------------------- P4c: 32 -> 64 merge
             // (c) 32 -> 64: T[32:64, 0:32] = -T[32:64, 32:64] (A[32:64, 0:32] T[0:32, 0:32]);
-            //     two adjacent outputs per thread
+            //     warps 0-7, four adjacent outputs per thread
             {
-                const int rr = tid >> 4, cp = (tid & 15) * 2;
-                const int rx = rr & 15, cch = cp >> 2, cl = cp & 3;
-                const float* arow = Af + (32 + rr) * 64;
-                float x0 = 0.f, x1 = 0.f;
+                const int rr = tid >> 3, cq = (tid & 7) * 4;
+                const int rx = rr & 15, cg = cq >> 2;
+                const int och = (cg ^ rx) << 2;
+                float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (tid < 256) {
+                    const float* arow = Af + (32 + rr) * 64;
 #pragma unroll
-                for (int l = 0; l < 32; ++l) {
-                    const float a = arow[((((l >> 2)) ^ rx) << 2) + (l & 3)];
-                    const float2 tv = *reinterpret_cast<const float2*>(Tf + l * 64 + ((cch ^ (l & 15)) << 2) + cl);
-                    x0 = fmaf(a, tv.x, x0);
-                    x1 = fmaf(a, tv.y, x1);
-                }
-                *reinterpret_cast<float2*>(Tf + (32 + rr) * 64 + ((cch ^ rx) << 2) + cl) = make_float2(x0, x1);
-                __syncthreads();
-                const float* trow = Tf + (32 + rr) * 64;
-                float y0 = 0.f, y1 = 0.f;
+                    for (int q = 0; q < 8; ++q) {
+                        const float4 a4 = *reinterpret_cast<const float4*>(arow + ((q ^ rx) << 2));
+                        const float av[4] = {a4.x, a4.y, a4.z, a4.w};
 #pragma unroll
-                for (int l = 0; l < 32; ++l) {
-                    const float a = trow[((((32 + l) >> 2) ^ rx) << 2) + (l & 3)];
-                    const float2 xv = *reinterpret_cast<const float2*>(Tf + (32 + l) * 64 + ((cch ^ (l & 15)) << 2) + cl);
-                    y0 = fmaf(a, xv.x, y0);
-                    y1 = fmaf(a, xv.y, y1);
+                        for (int u = 0; u < 4; ++u) {
+                            const int l = 4 * q + u;
+                            const float4 tv = *reinterpret_cast<const float4*>(Tf + l * 64 + ((cg ^ (l & 15)) << 2));
+                            x.x = fmaf(av[u], tv.x, x.x); x.y = fmaf(av[u], tv.y, x.y);
+                            x.z = fmaf(av[u], tv.z, x.z); x.w = fmaf(av[u], tv.w, x.w);
+                        }
+                    }
+                    *reinterpret_cast<float4*>(Tf + (32 + rr) * 64 + och) = x;
                 }
                 __syncthreads();
-                *reinterpret_cast<float2*>(Tf + (32 + rr) * 64 + ((cch ^ rx) << 2) + cl) = make_float2(-y0, -y1);
+                float4 y = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (tid < 256) {
+                    const float* trow = Tf + (32 + rr) * 64;
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) {
+                        const float4 a4 = *reinterpret_cast<const float4*>(trow + (((8 + q) ^ rx) << 2));
+                        const float av[4] = {a4.x, a4.y, a4.z, a4.w};
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) {
+                            const int l = 4 * q + u;
+                            const float4 xv = *reinterpret_cast<const float4*>(Tf + (32 + l) * 64 + ((cg ^ (l & 15)) << 2));
+                            y.x = fmaf(av[u], xv.x, y.x); y.y = fmaf(av[u], xv.y, y.y);
+                            y.z = fmaf(av[u], xv.z, y.z); y.w = fmaf(av[u], xv.w, y.w);
+                        }
+                    }
+                }
+                __syncthreads();
+                if (tid < 256)
+                    *reinterpret_cast<float4*>(Tf + (32 + rr) * 64 + och) =
+                        make_float4(-y.x, -y.y, -y.z, -y.w);
             }
             __syncthreads();
+        // ---------------------------------------------------------------- P4d: T to bf16
             // T -> bf16 K-major [t][i], one 8-element group per thread
             {
                 const int t = tid >> 3, i8 = tid & 7;
@@ -619,10 +697,34 @@ __global__ void __launch_bounds__(NT, 1)
                 tc::mma_bf16(tmem + TM_W, desc_mn(sb + OFF_LVL + LV_BKG, 8192, ks), b, IDESC_WU, ks > 0);
                 tc::mma_bf16(tmem + TM_U, desc_mn(sb + OFF_LVL + LV_BV, 8192, ks), b, IDESC_WU, ks > 0);
             }
-            tc::mma_commit(&ms.bar_mma);
+            tc::mma_commit(&ms.bar_m0);
         }
-        KDA_WAIT_MMA();
+        // while it runs: Q Gamma -> LV_QG and K~ = K e^{G_last - G} -> the v-tile slot (both
+        // MN-major [t][c]); neither region is read by this GEMM
+#pragma unroll 1
+        for (int it = 0; it < 2; ++it) {
+            const int item = tid + NT * it, t = item >> 4, c8 = item & 15;
+            float qf[8], kf[8], g8[8], gl[8], o[8];
+            unpack8(*reinterpret_cast<const uint4*>(sm + OFF_Q + t * 256 + c8 * 16), qf);
+            unpack8(*reinterpret_cast<const uint4*>(sm + OFF_K + t * 256 + c8 * 16), kf);
+            load8g(G2, t, c8, g8);
+            load8g(G2, 63, c8, gl);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) o[j] = qf[j] * ex2(g8[j]);
+            *reinterpret_cast<uint4*>(sm + OFF_LVL + LV_QG + mnmaj_off(t, c8 * 8, 8192)) = pack8(o);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) o[j] = kf[j] * ex2(gl[j] - g8[j]);
+            *reinterpret_cast<uint4*>(sm + OFF_V + mnmaj_off(t, c8 * 8, 8192)) = pack8(o);
+        }
+        KDA_WAIT(bar_m0, ph0);
         if (failed) break;
+        // q, k and the z slot are free: request the next chunk's q, k, z
+        if (tid == 0 && n + 1 < nchunks) {
+            tc::mbar_arrive_expect_tx(&ms.bar_qkz, 3u * 16384u);
+            tc::tma_load_3d(sm + OFF_Q, &tm_q, 0, t0 + C, (int)bh, &ms.bar_qkz);
+            tc::tma_load_3d(sm + OFF_K, &tm_k, 0, t0 + C, (int)bh, &ms.bar_qkz);
+            tc::tma_load_3d(sm + OFF_LVL + LV_Z, &tm_z, 0, t0 + C, (int)bh, &ms.bar_qkz);
+        }
         {
             // parts 0-1: W^T row c, columns 32*part.. -> [W^T | .]; parts 2-3: U^T row v -> K-major
             const bool is_u = part >= 2;
@@ -639,22 +741,6 @@ __global__ void __launch_bounds__(NT, 1)
                 if (!is_u) store16_mn(sm + OFF_A1, row, t0c, 16384, f);
                 else store16_k(sm + OFF_LVL + LV_UT, row, t0c, 128, f);
             }
-            // Q Gamma (MN-major [t][c]) and K~ = K e^{G_last - G} (MN-major [t][c])
-#pragma unroll 1
-            for (int it = 0; it < 2; ++it) {
-                const int item = tid + NT * it, t = item >> 4, c8 = item & 15;
-                float qf[8], kf[8], g8[8], gl[8], o[8];
-                unpack8(*reinterpret_cast<const uint4*>(sm + OFF_Q + t * 256 + c8 * 16), qf);
-                unpack8(*reinterpret_cast<const uint4*>(sm + OFF_K + t * 256 + c8 * 16), kf);
-                load8(G2 + t * KD + c8 * 8, g8);
-                load8(G2 + 63 * KD + c8 * 8, gl);
-#pragma unroll
-                for (int j = 0; j < 8; ++j) o[j] = qf[j] * ex2(g8[j]);
-                *reinterpret_cast<uint4*>(sm + OFF_LVL + LV_QG + mnmaj_off(t, c8 * 8, 8192)) = pack8(o);
-#pragma unroll
-                for (int j = 0; j < 8; ++j) o[j] = kf[j] * ex2(gl[j] - g8[j]);
-                *reinterpret_cast<uint4*>(sm + OFF_LVL + LV_KT + mnmaj_off(t, c8 * 8, 8192)) = pack8(o);
-            }
         }
         KDA_SYNC_FOR_MMA();
         // ---------------------------------------------------------------- P5: Q'^T and U'^T
@@ -670,18 +756,10 @@ __global__ void __launch_bounds__(NT, 1)
                 tc::mma_bf16(tmem + TM_QP, desc_k(sb + OFF_A1, 128, ks), b, IDESC_QNEG, 1u);
                 tc::mma_bf16(tmem + TM_UP, desc_k(sb + OFF_LVL + LV_UT, 128, ks), b, IDESC_QU, ks > 0);
             }
-            tc::mma_commit(&ms.bar_mma);
+            tc::mma_commit(&ms.bar_m1);
         }
-        KDA_WAIT_MMA();
+        KDA_WAIT(bar_m1, ph1);
         if (failed) break;
-        // the next chunk's tiles: every reader of q, k, v, z and of the z slot is done
-        if (tid == 0 && n + 1 < nchunks) {
-            tc::mbar_arrive_expect_tx(&ms.bar_tma, 4u * 16384u);
-            tc::tma_load_3d(sm + OFF_Q, &tm_q, 0, t0 + C, (int)bh, &ms.bar_tma);
-            tc::tma_load_3d(sm + OFF_K, &tm_k, 0, t0 + C, (int)bh, &ms.bar_tma);
-            tc::tma_load_3d(sm + OFF_V, &tm_v, 0, t0 + C, (int)bh, &ms.bar_tma);
-            tc::tma_load_3d(sm + OFF_LVL + LV_Z, &tm_z, 0, t0 + C, (int)bh, &ms.bar_tma);
-        }
         {
             // Q'^T row c, columns 16*part.. -> [. | Q'^T];  S <- diag(Gamma_last) S in TMEM
             // (this chunk's bf16 copy of S stays unscaled)
@@ -695,7 +773,7 @@ __global__ void __launch_bounds__(NT, 1)
                 for (int j = 0; j < 16; ++j) f[j] = __uint_as_float(d[j]);
                 store16_mn(sm + OFF_A1, c, 64 + 16 * part, 16384, f);
             }
-            const float gl = ex2(G2[63 * KD + c]);
+            const float gl = ex2(G2[63 * KD + gsw(c)]);
 #pragma unroll
             for (int v0 = 32 * part; v0 < 32 * part + 32; v0 += 16) {
                 uint32_t d[16];
@@ -708,69 +786,101 @@ __global__ void __launch_bounds__(NT, 1)
             tc::tmem_st_wait();
         }
         KDA_SYNC_FOR_MMA();
-        // ---------------------------------------------------------------- C1: (S^T [W^T | Q'^T])
-        if (tid == 0) {
-            // D[v][t'] = sum_c S[c][v] A1[c][t']: t' < 64 gives (W S)^T, t' >= 64 gives (Q' S)^T
+        // ---------------------------------------------------------------- C: carry | next gate
+        if (group_c) {
+            // C1: D[v][t'] = sum_c S[c][v] A1[c][t']  -> (W S)^T for t' < 64, (Q' S)^T above
+            if (tid == 0) {
 #pragma unroll
-            for (int ks = 0; ks < 8; ++ks)
-                tc::mma_bf16(tmem + TM_D1, desc_mn(sb + OFF_S, 16384, ks),
-                             desc_mn(sb + OFF_A1, 16384, ks), IDESC_SQ, ks > 0);
-            tc::mma_commit(&ms.bar_mma);
-        }
-        KDA_WAIT_MMA();
-        if (failed) break;
-        // ---------------------------------------------------------------- C2
-        {
-            // lane v: Delta^T[v][t] = U^T[v][t] - (W S)^T[v][t]  -> K-major B operand [v][t]
-            //         o[t][v] = scale ((Q' S)^T[v][t] + U'^T[v][t]);  this warp: t in 16*part..
-            const int v = row, tb = 16 * part;
-            uint32_t dw[16], du[16], dq[16], dp[16];
-            tc::tmem_ld16(taddr(tmem, warp, TM_D1 + tb), dw);
-            tc::tmem_ld16(taddr(tmem, warp, TM_U + tb), du);
-            tc::tmem_ld16(taddr(tmem, warp, TM_D1 + 64 + tb), dq);
-            tc::tmem_ld16(taddr(tmem, warp, TM_UP + tb), dp);
-            tc::tmem_ld_wait();
-            float f[16];
-#pragma unroll
-            for (int j = 0; j < 16; ++j) f[j] = __uint_as_float(du[j]) - __uint_as_float(dw[j]);
-            store16_k(sm + OFF_LVL + LV_DELTA, v, tb, 128, f);
-            __nv_bfloat16* ocol = out + (bh * T + t0 + tb) * VD + v;
-#pragma unroll
-            for (int j = 0; j < 16; ++j) {
-                if (tb + j < cn)
-                    ocol[(size_t)j * VD] =
-                        __float2bfloat16_rn(scale * (__uint_as_float(dq[j]) + __uint_as_float(dp[j])));
+                for (int ks = 0; ks < 8; ++ks)
+                    tc::mma_bf16(tmem + TM_D1, desc_mn(sb + OFF_S, 16384, ks),
+                                 desc_mn(sb + OFF_A1, 16384, ks), IDESC_SQ, ks > 0);
+                tc::mma_commit(&ms.bar_m0);
             }
-        }
-        KDA_SYNC_FOR_MMA();
-        // ---------------------------------------------------------------- C3: S += K~^T Delta
-        if (tid == 0) {
-#pragma unroll
-            for (int ks = 0; ks < 4; ++ks)
-                tc::mma_bf16(tmem + TM_S, desc_mn(sb + OFF_LVL + LV_KT, 8192, ks),
-                             desc_k(sb + OFF_LVL + LV_DELTA, 128, ks), IDESC_SK, 1u);
-            tc::mma_commit(&ms.bar_mma);
-        }
-        KDA_WAIT_MMA();
-        if (failed) break;
-        {
-            // S (fp32, TMEM) -> bf16 operand [c][v]; this warp: v in 32*part..
-            const int c = row;
-#pragma unroll
-            for (int v0 = 32 * part; v0 < 32 * part + 32; v0 += 16) {
-                uint32_t d[16];
-                tc::tmem_ld16(taddr(tmem, warp, TM_S + v0), d);
-                tc::tmem_ld_wait();
-                float f[16];
-#pragma unroll
-                for (int j = 0; j < 16; ++j) f[j] = __uint_as_float(d[j]);
-                store16_mn(sm + OFF_S, c, v0, 16384, f);
+            {
+                const bool ok = tid != 0 || tc::mbar_wait(&ms.bar_m0, ph0);
+                if (tc::named_sync_or(1, 256, !ok)) failed = true;
+                tc::fence_after_sync();
             }
+            // C2: lane v, tokens 32*half..: Delta^T = U^T - (W S)^T -> K-major [v][t];
+            //     o[t][v] = scale ((Q' S)^T + U'^T) -> row-major staging [t][v]
+            const int half = warp >> 2, v = row;
+            if (!failed) {
+#pragma unroll 1
+                for (int tb = 32 * half; tb < 32 * half + 32; tb += 16) {
+                    uint32_t dw[16], du[16], dq[16], dp[16];
+                    tc::tmem_ld16(taddr(tmem, warp, TM_D1 + tb), dw);
+                    tc::tmem_ld16(taddr(tmem, warp, TM_U + tb), du);
+                    tc::tmem_ld16(taddr(tmem, warp, TM_D1 + 64 + tb), dq);
+                    tc::tmem_ld16(taddr(tmem, warp, TM_UP + tb), dp);
+                    tc::tmem_ld_wait();
+                    float f[16];
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) f[j] = __uint_as_float(du[j]) - __uint_as_float(dw[j]);
+                    store16_k(sm + OFF_LVL + LV_DELTA, v, tb, 128, f);
+                    __nv_bfloat16* ost = reinterpret_cast<__nv_bfloat16*>(sm + OFF_LVL + LV_OST);
+#pragma unroll
+                    for (int j = 0; j < 16; ++j)
+                        ost[(tb + j) * VD + v] =
+                            __float2bfloat16_rn(scale * (__uint_as_float(dq[j]) + __uint_as_float(dp[j])));
+                }
+            }
+            tc::fence_proxy_async_smem();
+            tc::fence_before_sync();
+            tc::named_sync(1, 256);
+            tc::fence_after_sync();
+            // C3: S += K~^T Delta (K~ in the v-tile slot), while the staged o rows go out
+            if (tid == 0 && !failed) {
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks)
+                    tc::mma_bf16(tmem + TM_S, desc_mn(sb + OFF_V, 8192, ks),
+                                 desc_k(sb + OFF_LVL + LV_DELTA, 128, ks), IDESC_SK, 1u);
+                tc::mma_commit(&ms.bar_m1);
+            }
+#pragma unroll
+            for (int it = 0; it < 4; ++it) {
+                const int q = tid + 256 * it, tr = q >> 4, c16 = q & 15;
+                if (tr < cn)
+                    *reinterpret_cast<uint4*>(out + (bh * T + t0 + tr) * VD + c16 * 8) =
+                        *reinterpret_cast<const uint4*>(sm + OFF_LVL + LV_OST + tr * 256 + c16 * 16);
+            }
+            {
+                const bool ok = failed || tid != 0 || tc::mbar_wait(&ms.bar_m1, ph1);
+                if (tc::named_sync_or(1, 256, !ok)) failed = true;
+                tc::fence_after_sync();
+            }
+            // S (fp32, TMEM) -> bf16 operand [c][v]; this warp: v in 64*half..
+            if (!failed) {
+                const int c = row;
+#pragma unroll 1
+                for (int v0 = 64 * half; v0 < 64 * half + 64; v0 += 16) {
+                    uint32_t d[16];
+                    tc::tmem_ld16(taddr(tmem, warp, TM_S + v0), d);
+                    tc::tmem_ld_wait();
+                    float f[16];
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) f[j] = __uint_as_float(d[j]);
+                    store16_mn(sm + OFF_S, c, v0, 16384, f);
+                }
+                // K~ is consumed: request the next chunk's v tile into its slot
+                if (tid == 0 && n + 1 < nchunks) {
+                    tc::mbar_arrive_expect_tx(&ms.bar_v, 16384u);
+                    tc::tma_load_3d(sm + OFF_V, &tm_v, 0, t0 + C, (int)bh, &ms.bar_v);
+                }
+            }
+        } else if (n + 1 < nchunks) {
+            if (!gate_scan(n + 1)) failed = true;
         }
-        KDA_SYNC_FOR_MMA();
+        ph0 ^= 1u;  // C1's and C3's commits, waited by the carry group only
+        ph1 ^= 1u;
+        if (n + 1 < nchunks) ph_qkz ^= 1u;
+        tc::fence_proxy_async_smem();
+        tc::fence_before_sync();
+        if (__syncthreads_or(failed)) failed = true;
+        tc::fence_after_sync();
     }
-#undef KDA_WAIT_MMA
+#undef KDA_WAIT
 #undef KDA_SYNC_FOR_MMA
+#undef KDA_LEVEL_MMA
 
     if (!failed && hT) {
         const int c = row;
@@ -789,8 +899,10 @@ __global__ void __launch_bounds__(NT, 1)
     if (failed && tid == 0) {
         atomicExch(&g_kda_tc_timeout, 1);
         // give any tensor-core or TMA work still in flight a bounded chance to finish
-        tc::mbar_wait(&ms.bar_mma, mma_phase, 200000000ull);
-        tc::mbar_wait(&ms.bar_tma, tma_phase, 200000000ull);
+        tc::mbar_wait(&ms.bar_m0, ph0, 200000000ull);
+        tc::mbar_wait(&ms.bar_m1, ph1, 200000000ull);
+        tc::mbar_wait(&ms.bar_qkz, ph_qkz, 200000000ull);
+        tc::mbar_wait(&ms.bar_v, ph_v, 200000000ull);
     }
     tc::fence_before_sync();
     __syncthreads();
