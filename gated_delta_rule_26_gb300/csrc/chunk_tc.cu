@@ -521,7 +521,7 @@ __global__ void __launch_bounds__(NT, 1)
                 store16_k(sm + OFF_LVL + LV_MB, t, i0, 64, o16);
             }
             // beta K Gamma and beta V as MN-major [t][.] operands
-#pragma unroll 1
+#pragma unroll
             for (int it = 0; it < 2; ++it) {
                 const int item = tid + NT * it, tt = item >> 4, c8 = item & 15;
                 const float bt = ms.beta[tt];
@@ -552,15 +552,22 @@ __global__ void __launch_bounds__(NT, 1)
                 const int R = tid >> 4, j = tid & 15;
                 const float* Ab = Af + 16 * R * 64;  // rows 16R.. ; (row & 15) == t
                 float x[16];
+                // the strictly lower part of this block row by row, in 16-byte groups, all
+                // issued before the substitution starts (36 groups)
+                float4 ar[16][4];
+#pragma unroll
+                for (int t = 1; t < 16; ++t)
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        if (4 * q < t)
+                            ar[t][q] = *reinterpret_cast<const float4*>(Ab + t * 64 + (((4 * R + q) ^ t) << 2));
 #pragma unroll
                 for (int t = 0; t < 16; ++t) {
                     float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
                         if (4 * q < t) {
-                            const float4 a4 =
-                                *reinterpret_cast<const float4*>(Ab + t * 64 + (((4 * R + q) ^ t) << 2));
-                            const float av[4] = {a4.x, a4.y, a4.z, a4.w};
+                            const float av[4] = {ar[t][q].x, ar[t][q].y, ar[t][q].z, ar[t][q].w};
 #pragma unroll
                             for (int u = 0; u < 4; ++u)
                                 if (4 * q + u < t) acc[u] = fmaf(av[u], x[4 * q + u], acc[u]);
@@ -593,16 +600,21 @@ __global__ void __launch_bounds__(NT, 1)
                 if (tid < 128) {
                     const float* arow = Af + (16 * R + rr) * 64;
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        const float4 a4 = *reinterpret_cast<const float4*>(arow + (((4 * Cb + q) ^ rr) << 2));
-                        const float av[4] = {a4.x, a4.y, a4.z, a4.w};
+                    for (int g = 0; g < 2; ++g) {
+                        float4 tv[8];
+                        const float4 a4a = *reinterpret_cast<const float4*>(arow + (((4 * Cb + 2 * g) ^ rr) << 2));
+                        const float4 a4b = *reinterpret_cast<const float4*>(arow + (((4 * Cb + 2 * g + 1) ^ rr) << 2));
 #pragma unroll
-                        for (int u = 0; u < 4; ++u) {
-                            const int l = 4 * q + u;
-                            const float4 tv = *reinterpret_cast<const float4*>(
+                        for (int u = 0; u < 8; ++u) {
+                            const int l = 8 * g + u;
+                            tv[u] = *reinterpret_cast<const float4*>(
                                 Tf + (16 * Cb + l) * 64 + (((4 * Cb + (cq >> 2)) ^ l) << 2));
-                            x.x = fmaf(av[u], tv.x, x.x); x.y = fmaf(av[u], tv.y, x.y);
-                            x.z = fmaf(av[u], tv.z, x.z); x.w = fmaf(av[u], tv.w, x.w);
+                        }
+                        const float av[8] = {a4a.x, a4a.y, a4a.z, a4a.w, a4b.x, a4b.y, a4b.z, a4b.w};
+#pragma unroll
+                        for (int u = 0; u < 8; ++u) {
+                            x.x = fmaf(av[u], tv[u].x, x.x); x.y = fmaf(av[u], tv[u].y, x.y);
+                            x.z = fmaf(av[u], tv[u].z, x.z); x.w = fmaf(av[u], tv[u].w, x.w);
                         }
                     }
                     *reinterpret_cast<float4*>(Tf + (16 * R + rr) * 64 + och) = x;
@@ -612,16 +624,21 @@ __global__ void __launch_bounds__(NT, 1)
                 if (tid < 128) {
                     const float* trow = Tf + (16 * R + rr) * 64;
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        const float4 a4 = *reinterpret_cast<const float4*>(trow + (((4 * R + q) ^ rr) << 2));
-                        const float av[4] = {a4.x, a4.y, a4.z, a4.w};
+                    for (int g = 0; g < 2; ++g) {
+                        float4 xv[8];
+                        const float4 a4a = *reinterpret_cast<const float4*>(trow + (((4 * R + 2 * g) ^ rr) << 2));
+                        const float4 a4b = *reinterpret_cast<const float4*>(trow + (((4 * R + 2 * g + 1) ^ rr) << 2));
 #pragma unroll
-                        for (int u = 0; u < 4; ++u) {
-                            const int l = 4 * q + u;
-                            const float4 xv = *reinterpret_cast<const float4*>(
+                        for (int u = 0; u < 8; ++u) {
+                            const int l = 8 * g + u;
+                            xv[u] = *reinterpret_cast<const float4*>(
                                 Tf + (16 * R + l) * 64 + (((4 * Cb + (cq >> 2)) ^ l) << 2));
-                            y.x = fmaf(av[u], xv.x, y.x); y.y = fmaf(av[u], xv.y, y.y);
-                            y.z = fmaf(av[u], xv.z, y.z); y.w = fmaf(av[u], xv.w, y.w);
+                        }
+                        const float av[8] = {a4a.x, a4a.y, a4a.z, a4a.w, a4b.x, a4b.y, a4b.z, a4b.w};
+#pragma unroll
+                        for (int u = 0; u < 8; ++u) {
+                            y.x = fmaf(av[u], xv[u].x, y.x); y.y = fmaf(av[u], xv[u].y, y.y);
+                            y.z = fmaf(av[u], xv[u].z, y.z); y.w = fmaf(av[u], xv[u].w, y.w);
                         }
                     }
                 }
@@ -641,16 +658,22 @@ __global__ void __launch_bounds__(NT, 1)
                 float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
                 if (tid < 256) {
                     const float* arow = Af + (32 + rr) * 64;
+                    // loads are issued in batches of eight ahead of their FMAs
 #pragma unroll
-                    for (int q = 0; q < 8; ++q) {
-                        const float4 a4 = *reinterpret_cast<const float4*>(arow + ((q ^ rx) << 2));
-                        const float av[4] = {a4.x, a4.y, a4.z, a4.w};
+                    for (int g = 0; g < 4; ++g) {
+                        float4 tv[8];
+                        const float4 a4a = *reinterpret_cast<const float4*>(arow + (((2 * g) ^ rx) << 2));
+                        const float4 a4b = *reinterpret_cast<const float4*>(arow + (((2 * g + 1) ^ rx) << 2));
 #pragma unroll
-                        for (int u = 0; u < 4; ++u) {
-                            const int l = 4 * q + u;
-                            const float4 tv = *reinterpret_cast<const float4*>(Tf + l * 64 + ((cg ^ (l & 15)) << 2));
-                            x.x = fmaf(av[u], tv.x, x.x); x.y = fmaf(av[u], tv.y, x.y);
-                            x.z = fmaf(av[u], tv.z, x.z); x.w = fmaf(av[u], tv.w, x.w);
+                        for (int u = 0; u < 8; ++u) {
+                            const int l = 8 * g + u;
+                            tv[u] = *reinterpret_cast<const float4*>(Tf + l * 64 + ((cg ^ (l & 15)) << 2));
+                        }
+                        const float av[8] = {a4a.x, a4a.y, a4a.z, a4a.w, a4b.x, a4b.y, a4b.z, a4b.w};
+#pragma unroll
+                        for (int u = 0; u < 8; ++u) {
+                            x.x = fmaf(av[u], tv[u].x, x.x); x.y = fmaf(av[u], tv[u].y, x.y);
+                            x.z = fmaf(av[u], tv[u].z, x.z); x.w = fmaf(av[u], tv[u].w, x.w);
                         }
                     }
                     *reinterpret_cast<float4*>(Tf + (32 + rr) * 64 + och) = x;
@@ -660,15 +683,20 @@ __global__ void __launch_bounds__(NT, 1)
                 if (tid < 256) {
                     const float* trow = Tf + (32 + rr) * 64;
 #pragma unroll
-                    for (int q = 0; q < 8; ++q) {
-                        const float4 a4 = *reinterpret_cast<const float4*>(trow + (((8 + q) ^ rx) << 2));
-                        const float av[4] = {a4.x, a4.y, a4.z, a4.w};
+                    for (int g = 0; g < 4; ++g) {
+                        float4 xv[8];
+                        const float4 a4a = *reinterpret_cast<const float4*>(trow + (((8 + 2 * g) ^ rx) << 2));
+                        const float4 a4b = *reinterpret_cast<const float4*>(trow + (((9 + 2 * g) ^ rx) << 2));
 #pragma unroll
-                        for (int u = 0; u < 4; ++u) {
-                            const int l = 4 * q + u;
-                            const float4 xv = *reinterpret_cast<const float4*>(Tf + (32 + l) * 64 + ((cg ^ (l & 15)) << 2));
-                            y.x = fmaf(av[u], xv.x, y.x); y.y = fmaf(av[u], xv.y, y.y);
-                            y.z = fmaf(av[u], xv.z, y.z); y.w = fmaf(av[u], xv.w, y.w);
+                        for (int u = 0; u < 8; ++u) {
+                            const int l = 8 * g + u;
+                            xv[u] = *reinterpret_cast<const float4*>(Tf + (32 + l) * 64 + ((cg ^ (l & 15)) << 2));
+                        }
+                        const float av[8] = {a4a.x, a4a.y, a4a.z, a4a.w, a4b.x, a4b.y, a4b.z, a4b.w};
+#pragma unroll
+                        for (int u = 0; u < 8; ++u) {
+                            y.x = fmaf(av[u], xv[u].x, y.x); y.y = fmaf(av[u], xv[u].y, y.y);
+                            y.z = fmaf(av[u], xv[u].z, y.z); y.w = fmaf(av[u], xv[u].w, y.w);
                         }
                     }
                 }
@@ -701,7 +729,7 @@ __global__ void __launch_bounds__(NT, 1)
         }
         // while it runs: Q Gamma -> LV_QG and K~ = K e^{G_last - G} -> the v-tile slot (both
         // MN-major [t][c]); neither region is read by this GEMM
-#pragma unroll 1
+#pragma unroll
         for (int it = 0; it < 2; ++it) {
             const int item = tid + NT * it, t = item >> 4, c8 = item & 15;
             float qf[8], kf[8], g8[8], gl[8], o[8];
@@ -730,16 +758,21 @@ __global__ void __launch_bounds__(NT, 1)
             const bool is_u = part >= 2;
             const int cb = 32 * (part & 1);
             const uint32_t col = is_u ? TM_U : TM_W;
-#pragma unroll
-            for (int t0c = cb; t0c < cb + 32; t0c += 16) {
-                uint32_t d[16];
-                tc::tmem_ld16(taddr(tmem, warp, col + t0c), d);
+            {
+                uint32_t d0[16], d1[16];
+                tc::tmem_ld16(taddr(tmem, warp, col + cb), d0);
+                tc::tmem_ld16(taddr(tmem, warp, col + cb + 16), d1);
                 tc::tmem_ld_wait();
-                float f[16];
+                float f0[16], f1[16];
 #pragma unroll
-                for (int j = 0; j < 16; ++j) f[j] = __uint_as_float(d[j]);
-                if (!is_u) store16_mn(sm + OFF_A1, row, t0c, 16384, f);
-                else store16_k(sm + OFF_LVL + LV_UT, row, t0c, 128, f);
+                for (int j = 0; j < 16; ++j) { f0[j] = __uint_as_float(d0[j]); f1[j] = __uint_as_float(d1[j]); }
+                if (!is_u) {
+                    store16_mn(sm + OFF_A1, row, cb, 16384, f0);
+                    store16_mn(sm + OFF_A1, row, cb + 16, 16384, f1);
+                } else {
+                    store16_k(sm + OFF_LVL + LV_UT, row, cb, 128, f0);
+                    store16_k(sm + OFF_LVL + LV_UT, row, cb + 16, 128, f1);
+                }
             }
         }
         KDA_SYNC_FOR_MMA();
@@ -774,14 +807,19 @@ __global__ void __launch_bounds__(NT, 1)
                 store16_mn(sm + OFF_A1, c, 64 + 16 * part, 16384, f);
             }
             const float gl = ex2(G2[63 * KD + gsw(c)]);
-#pragma unroll
-            for (int v0 = 32 * part; v0 < 32 * part + 32; v0 += 16) {
-                uint32_t d[16];
-                tc::tmem_ld16(taddr(tmem, warp, TM_S + v0), d);
+            {
+                const int v0 = 32 * part;
+                uint32_t d0[16], d1[16];
+                tc::tmem_ld16(taddr(tmem, warp, TM_S + v0), d0);
+                tc::tmem_ld16(taddr(tmem, warp, TM_S + v0 + 16), d1);
                 tc::tmem_ld_wait();
 #pragma unroll
-                for (int j = 0; j < 16; ++j) d[j] = __float_as_uint(__uint_as_float(d[j]) * gl);
-                tc::tmem_st16(taddr(tmem, warp, TM_S + v0), d);
+                for (int j = 0; j < 16; ++j) {
+                    d0[j] = __float_as_uint(__uint_as_float(d0[j]) * gl);
+                    d1[j] = __float_as_uint(__uint_as_float(d1[j]) * gl);
+                }
+                tc::tmem_st16(taddr(tmem, warp, TM_S + v0), d0);
+                tc::tmem_st16(taddr(tmem, warp, TM_S + v0 + 16), d1);
             }
             tc::tmem_st_wait();
         }
@@ -852,14 +890,18 @@ __global__ void __launch_bounds__(NT, 1)
             if (!failed) {
                 const int c = row;
 #pragma unroll 1
-                for (int v0 = 64 * half; v0 < 64 * half + 64; v0 += 16) {
-                    uint32_t d[16];
-                    tc::tmem_ld16(taddr(tmem, warp, TM_S + v0), d);
+                for (int v0 = 64 * half; v0 < 64 * half + 64; v0 += 32) {
+                    uint32_t d0[16], d1[16];
+                    tc::tmem_ld16(taddr(tmem, warp, TM_S + v0), d0);
+                    tc::tmem_ld16(taddr(tmem, warp, TM_S + v0 + 16), d1);
                     tc::tmem_ld_wait();
                     float f[16];
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) f[j] = __uint_as_float(d[j]);
+                    for (int j = 0; j < 16; ++j) f[j] = __uint_as_float(d0[j]);
                     store16_mn(sm + OFF_S, c, v0, 16384, f);
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) f[j] = __uint_as_float(d1[j]);
+                    store16_mn(sm + OFF_S, c, v0 + 16, 16384, f);
                 }
                 // K~ is consumed: request the next chunk's v tile into its slot
                 if (tid == 0 && n + 1 < nchunks) {
