@@ -9,6 +9,8 @@
 
 namespace kda {
 cudaError_t launch_chunk_tc(const ChunkArgs& a, cudaStream_t s, bool* taken);
+cudaError_t launch_bounded_wait_selftest(unsigned long long limit_ns, cudaStream_t s);
+cudaError_t read_and_clear_timeout(cudaStream_t s, int* timed_out);
 }
 
 namespace kda {
@@ -73,6 +75,7 @@ const char* kda_status_string(int status) {
         case KDA_ERR_MISALIGNED: return "pointer not 16-byte aligned";
         case KDA_ERR_CUDA: return "CUDA error";
         case KDA_ERR_NO_MEMORY: return "out of device memory";
+        case KDA_ERR_TIMEOUT: return "a kernel gave up on a bounded wait";
         default: return "unknown status";
     }
 }
@@ -115,6 +118,18 @@ int kda_chunk_forward(const kda_dims* dims, kda_dtype io_dtype, const void* q, c
     cudaError_t e = kda::launch_chunk_tc(a, (cudaStream_t)stream, &taken);
     if (taken) return e == cudaErrorMemoryAllocation ? KDA_ERR_NO_MEMORY : from_cuda(e);
     return from_cuda(kda::launch_chunk_simt(a, (cudaStream_t)stream));
+}
+
+int kda_device_status(kda_stream_t stream) {
+    int timed_out = 0;
+    if (kda::read_and_clear_timeout((cudaStream_t)stream, &timed_out) != cudaSuccess)
+        return KDA_ERR_CUDA;
+    return timed_out ? KDA_ERR_TIMEOUT : KDA_OK;
+}
+
+int kda_selftest_bounded_wait(unsigned long long limit_ns, kda_stream_t stream) {
+    if (limit_ns == 0 || limit_ns > 10000000000ull) return KDA_ERR_INVALID_ARG;
+    return from_cuda(kda::launch_bounded_wait_selftest(limit_ns, (cudaStream_t)stream));
 }
 
 int kda_recurrent_step(const kda_dims* dims, kda_dtype io_dtype, const void* q, const void* k,

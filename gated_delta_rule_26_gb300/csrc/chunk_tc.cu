@@ -988,6 +988,40 @@ bool make_tile_map(CUtensorMap* map, const void* base, int T, int BH) {
 
 }  // namespace
 
+// A wait that nothing ever satisfies: one thread initialises an mbarrier that expects one
+// arrival, never arrives, and waits with the bounded wait every kernel here uses.  The wait
+// gives up after `limit_ns` and records the timeout in the same flag the chunk kernel sets,
+// which is how the host-side failure report is exercised without faulting or hanging a GPU.
+__global__ void kda_bounded_wait_selftest_kernel(unsigned long long limit_ns) {
+    __shared__ uint64_t bar;
+    if (threadIdx.x == 0) {
+        tc::mbar_init(&bar, 1);
+        tc::fence_barrier_init();
+        if (!tc::mbar_wait(&bar, 0, limit_ns)) atomicExch(&g_kda_tc_timeout, 1);
+    }
+}
+
+cudaError_t launch_bounded_wait_selftest(unsigned long long limit_ns, cudaStream_t s) {
+    kda_bounded_wait_selftest_kernel<<<1, 32, 0, s>>>(limit_ns);
+    count_launches(1);
+    return cudaGetLastError();
+}
+
+// Reads and clears the timeout flag after the stream has drained; *timed_out = flag.
+cudaError_t read_and_clear_timeout(cudaStream_t s, int* timed_out) {
+    cudaError_t e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return e;
+    int v = 0;
+    e = cudaMemcpyFromSymbol(&v, g_kda_tc_timeout, sizeof(int));
+    if (e != cudaSuccess) return e;
+    *timed_out = v;
+    if (v) {
+        const int zero = 0;
+        e = cudaMemcpyToSymbol(g_kda_tc_timeout, &zero, sizeof(int));
+    }
+    return e;
+}
+
 cudaError_t launch_chunk_tc(const ChunkArgs& a, cudaStream_t s, bool* taken) {
     *taken = false;
     if (a.io != KDA_BF16 || a.K != 128 || a.V != 128 || a.chunk != 64 || a.T <= 0) return cudaSuccess;

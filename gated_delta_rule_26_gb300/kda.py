@@ -21,7 +21,8 @@ _lib = None
 KDA_F32, KDA_BF16 = 0, 1
 _DTYPES = {torch.float32: KDA_F32, torch.bfloat16: KDA_BF16}
 STATUS = {0: "ok", -1: "invalid argument", -2: "unsupported size or chunk",
-          -3: "pointer not 16-byte aligned", -4: "CUDA error", -5: "out of device memory"}
+          -3: "pointer not 16-byte aligned", -4: "CUDA error", -5: "out of device memory",
+          -6: "a kernel gave up on a bounded wait"}
 
 
 class KdaError(RuntimeError):
@@ -55,12 +56,28 @@ def load() -> ctypes.CDLL:
         lib.kda_recurrent_step.argtypes = [dp, i, vp, vp, vp, vp, vp, vp, vp, f, vp, vp, vp]
         lib.kda_status_string.argtypes = [i]
         lib.kda_status_string.restype = ctypes.c_char_p
+        lib.kda_device_status.argtypes = [vp]
+        lib.kda_device_status.restype = i
+        lib.kda_selftest_bounded_wait.argtypes = [ctypes.c_ulonglong, vp]
+        lib.kda_selftest_bounded_wait.restype = i
         lib.kda_launch_count.argtypes = []
         lib.kda_launch_count.restype = ctypes.c_ulonglong
         for fn in (lib.kda_gate, lib.kda_chunk_forward, lib.kda_recurrent_step):
             fn.restype = i
         _lib = lib
     return _lib
+
+
+def device_status(stream=None) -> int:
+    """Drain the stream and return (and clear) the library's bounded-wait timeout report:
+    0 when no kernel gave up on a wait, -6 (KDA_ERR_TIMEOUT) otherwise."""
+    return int(load().kda_device_status(_stream(stream)))
+
+
+def selftest_bounded_wait(limit_ns: int, stream=None) -> None:
+    """Launch a kernel whose wait can never be satisfied; it ends after `limit_ns`."""
+    _check("kda_selftest_bounded_wait", load().kda_selftest_bounded_wait(int(limit_ns),
+                                                                          _stream(stream)))
 
 
 def launch_count() -> int:

@@ -65,7 +65,8 @@ enum {
     KDA_ERR_UNSUPPORTED = -2, /* size or chunk outside the supported set */
     KDA_ERR_MISALIGNED = -3,  /* a pointer not 16-byte aligned */
     KDA_ERR_CUDA = -4,        /* a CUDA runtime call or launch failed */
-    KDA_ERR_NO_MEMORY = -5    /* scratch allocation failed */
+    KDA_ERR_NO_MEMORY = -5,   /* scratch allocation failed */
+    KDA_ERR_TIMEOUT = -6      /* a kernel gave up on a bounded wait (see kda_device_status) */
 };
 
 /*
@@ -105,6 +106,24 @@ int kda_recurrent_step(const kda_dims* dims, kda_dtype io_dtype, const void* q, 
 
 /* A static, human-readable name for a status code. */
 const char* kda_status_string(int status);
+
+/*
+ * kda_device_status -- waits for `stream` to drain, then reports whether any kernel of this
+ * library gave up on one of its bounded waits since the last call (KDA_ERR_TIMEOUT; the
+ * outputs of that call are not valid) and clears the report.  Every wait on a tensor-core or
+ * copy completion inside the kernels is bounded (about two seconds), so a lost completion
+ * ends the kernel with this report instead of hanging the GPU.  Returns KDA_OK, or
+ * KDA_ERR_CUDA if the stream itself failed.
+ */
+int kda_device_status(kda_stream_t stream);
+
+/*
+ * kda_selftest_bounded_wait -- launches one tiny kernel whose wait can never be satisfied
+ * (an mbarrier nobody arrives on) with the given limit in nanoseconds (1 .. 1e10).  It ends
+ * after the limit and leaves a KDA_ERR_TIMEOUT report for kda_device_status: a way to
+ * exercise the failure path without faulting the GPU.
+ */
+int kda_selftest_bounded_wait(unsigned long long limit_ns, kda_stream_t stream);
 
 /*
  * Diagnostic: the number of CUDA kernels this library has launched in this

@@ -255,3 +255,17 @@ def test_decode_matches_chunk_forward(kda):
     o_r = torch.cat(outs, dim=2)
     assert (o_r - o_c).abs().max() / o_c.abs().max() < 1e-4
     assert (state - h_c).abs().max() / h_c.abs().max() < 1e-4
+
+
+# ---------------------------------------------------------------- failure reporting
+def test_bounded_wait_reports_timeout_and_clears(kda):
+    """A wait nothing can satisfy ends after its limit and is reported, not hung on; the report
+    clears after it is read, and a normal call afterwards reports nothing."""
+    assert kda.device_status() == 0
+    kda.selftest_bounded_wait(2_000_000)  # 2 ms
+    assert kda.device_status() == -6
+    assert kda.device_status() == 0
+    inp = inputs.make(1, 2, 64, 128, 128, chunk=64, dtype="bf16", seed=77)
+    d = inp.to("cuda")
+    kda.chunk_forward(d.q, d.k, d.v, d.z, d.beta, d.A_log, d.dt_bias, inp.scale, None, 64)
+    assert kda.device_status() == 0
