@@ -120,6 +120,23 @@ int kda_chunk_forward(const kda_dims* dims, kda_dtype io_dtype, const void* q, c
     return from_cuda(kda::launch_chunk_simt(a, (cudaStream_t)stream));
 }
 
+int kda_fused_recurrent(const kda_dims* dims, kda_dtype io_dtype, const void* q, const void* k,
+                        const void* v, const void* z, const void* beta, const float* A_log,
+                        const float* dt_bias, float scale, float* state, void* out,
+                        kda_stream_t stream) {
+    int st = check_dims(dims, true);
+    if (st) return st;
+    if (!dtype_ok(io_dtype)) return KDA_ERR_INVALID_ARG;
+    if ((long long)dims->B * dims->H > 0x3fffffffLL) return KDA_ERR_UNSUPPORTED;
+    if (dims->T == 0) return check_ptrs({state}, {});
+    st = check_ptrs({state}, {}, {q, k, v, z, beta, out}, io_bytes(io_dtype));
+    if (!st) st = check_ptrs({}, {}, {A_log, dt_bias}, 4);
+    if (st) return st;
+    kda::StepArgs a{dims->B, dims->H, dims->K, dims->V, io_dtype, q, k, v, z, beta,
+                    A_log, dt_bias, scale, state, out};
+    return from_cuda(kda::launch_recurrent(a, dims->T, (cudaStream_t)stream));
+}
+
 int kda_device_status(kda_stream_t stream) {
     int timed_out = 0;
     if (kda::read_and_clear_timeout((cudaStream_t)stream, &timed_out) != cudaSuccess)

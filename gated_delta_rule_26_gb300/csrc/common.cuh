@@ -55,6 +55,7 @@ cudaError_t launch_gate(int B, int H, int T, int K, kda_dtype zdt, const void* z
                         const float* A_log, const float* dt_bias, int chunk, float* g,
                         cudaStream_t s);
 cudaError_t launch_decode(const StepArgs& a, cudaStream_t s);
+cudaError_t launch_recurrent(const StepArgs& a, int T, cudaStream_t s);
 cudaError_t launch_chunk_simt(const ChunkArgs& a, cudaStream_t s);
 
 }  // namespace kda

@@ -54,6 +54,7 @@ def load() -> ctypes.CDLL:
         lib.kda_gate.argtypes = [dp, i, vp, vp, vp, i, vp, vp]
         lib.kda_chunk_forward.argtypes = [dp, i, vp, vp, vp, vp, vp, vp, vp, f, vp, i, vp, vp, vp]
         lib.kda_recurrent_step.argtypes = [dp, i, vp, vp, vp, vp, vp, vp, vp, f, vp, vp, vp]
+        lib.kda_fused_recurrent.argtypes = [dp, i, vp, vp, vp, vp, vp, vp, vp, f, vp, vp, vp]
         lib.kda_status_string.argtypes = [i]
         lib.kda_status_string.restype = ctypes.c_char_p
         lib.kda_device_status.argtypes = [vp]
@@ -62,7 +63,8 @@ def load() -> ctypes.CDLL:
         lib.kda_selftest_bounded_wait.restype = i
         lib.kda_launch_count.argtypes = []
         lib.kda_launch_count.restype = ctypes.c_ulonglong
-        for fn in (lib.kda_gate, lib.kda_chunk_forward, lib.kda_recurrent_step):
+        for fn in (lib.kda_gate, lib.kda_chunk_forward, lib.kda_recurrent_step,
+                   lib.kda_fused_recurrent):
             fn.restype = i
         _lib = lib
     return _lib
@@ -167,4 +169,24 @@ def recurrent_step(q, k, v, z, beta, A_log, dt_bias, state: torch.Tensor,
                                    _ptr(z), _ptr(beta), _ptr(_f32(A_log)), _ptr(_f32(dt_bias)),
                                    float(scale), _ptr(state), _ptr(out), _stream(stream))
     _check("kda_recurrent_step", st)
+    return out
+
+
+def fused_recurrent(q, k, v, z, beta, A_log, dt_bias, state: torch.Tensor,
+                    scale: Optional[float] = None, out: Optional[torch.Tensor] = None,
+                    stream=None) -> torch.Tensor:
+    """T tokens per (b, h) applied one by one with the state kept on chip; updates ``state``
+    (B, H, K, V) float32 in place and returns o (B, H, T, V).  q, k, z are (B, H, T, K),
+    v (B, H, T, V), beta (B, H, T)."""
+    B, H, T, K = q.shape
+    V = v.shape[-1]
+    if scale is None:
+        scale = default_scale(K)
+    if out is None:
+        out = torch.empty(B, H, T, V, device=q.device, dtype=q.dtype)
+    d = Dims(B, H, T, K, V)
+    st = load().kda_fused_recurrent(ctypes.byref(d), _DTYPES[q.dtype], _ptr(q), _ptr(k), _ptr(v),
+                                    _ptr(z), _ptr(beta), _ptr(_f32(A_log)), _ptr(_f32(dt_bias)),
+                                    float(scale), _ptr(state), _ptr(out), _stream(stream))
+    _check("kda_fused_recurrent", st)
     return out

@@ -104,6 +104,19 @@ int kda_recurrent_step(const kda_dims* dims, kda_dtype io_dtype, const void* q, 
                        const float* dt_bias, float scale, float* state, void* out,
                        kda_stream_t stream);
 
+/*
+ * kda_fused_recurrent -- dims->T >= 0 consecutive tokens per (b, h) applied token by token
+ * (the step of kda_recurrent_step, T times), with the state kept on chip between tokens:
+ * `state` (B,H,K,V) float32 is read once and written once, in place.  q, k, z are
+ * (B,H,T,K), v and out (B,H,T,V), beta (B,H,T), all in io_dtype (the chunked layouts).
+ * For short sequences (multi-token decode, small prefills) it moves far fewer bytes
+ * than T calls of kda_recurrent_step; kda_recurrent_step is the T = 1 case.
+ */
+int kda_fused_recurrent(const kda_dims* dims, kda_dtype io_dtype, const void* q, const void* k,
+                        const void* v, const void* z, const void* beta, const float* A_log,
+                        const float* dt_bias, float scale, float* state, void* out,
+                        kda_stream_t stream);
+
 /* A static, human-readable name for a status code. */
 const char* kda_status_string(int status);
 

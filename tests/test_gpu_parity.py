@@ -269,3 +269,40 @@ def test_bounded_wait_reports_timeout_and_clears(kda):
     d = inp.to("cuda")
     kda.chunk_forward(d.q, d.k, d.v, d.z, d.beta, d.A_log, d.dt_bias, inp.scale, None, 64)
     assert kda.device_status() == 0
+
+
+# ---------------------------------------------------------------- fused recurrent (T tokens per launch)
+@pytest.mark.parametrize("B,H,T,K,V,dtype", [
+    (2, 3, 1, 8, 8, "f32"),
+    (2, 3, 33, 64, 32, "f32"),
+    (1, 2, 70, 128, 128, "f32"),
+    (4, 8, 64, 128, 128, "bf16"),
+    (1, 1, 5, 24, 40, "f32"),
+])
+def test_fused_recurrent_matches_oracle(kda, B, H, T, K, V, dtype):
+    inp = inputs.make(B, H, T, K, V, dtype=dtype, seed=T * 31 + K, h0_std=0.1)
+    d = inp.to("cuda")
+    state = d.h0.clone()
+    o = kda.fused_recurrent(d.q, d.k, d.v, d.z, d.beta, d.A_log, d.dt_bias, state, inp.scale)
+    torch.cuda.synchronize()
+    o_ref, h_ref = oracle.forward(inp.q, inp.k, inp.v, inp.z, inp.beta, inp.A_log, inp.dt_bias,
+                                  inp.scale, inp.h0, threads=4)
+    check("o", o, o_ref, dtype)
+    check("state", state, h_ref, dtype)
+
+
+def test_fused_recurrent_equals_repeated_steps(kda):
+    """T tokens in one launch and T single-token launches do the same arithmetic: bit-identical."""
+    inp = inputs.make(3, 4, 12, 128, 128, dtype="bf16", seed=21, h0_std=0.1)
+    d = inp.to("cuda")
+    s1 = d.h0.clone()
+    o1 = kda.fused_recurrent(d.q, d.k, d.v, d.z, d.beta, d.A_log, d.dt_bias, s1, inp.scale)
+    s2 = d.h0.clone()
+    outs = []
+    for t in range(12):
+        sl = lambda x: x[:, :, t:t + 1].contiguous()
+        outs.append(kda.recurrent_step(sl(d.q), sl(d.k), sl(d.v), sl(d.z), sl(d.beta), d.A_log,
+                                       d.dt_bias, s2, inp.scale))
+    torch.cuda.synchronize()
+    assert torch.equal(o1, torch.cat(outs, dim=2))
+    assert torch.equal(s1, s2)
