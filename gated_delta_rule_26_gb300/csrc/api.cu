@@ -134,6 +134,7 @@ int kda_fused_recurrent(const kda_dims* dims, kda_dtype io_dtype, const void* q,
     if (st) return st;
     kda::StepArgs a{dims->B, dims->H, dims->K, dims->V, io_dtype, q, k, v, z, beta,
                     A_log, dt_bias, scale, state, out};
+    if (dims->T == 1) return from_cuda(kda::launch_decode(a, (cudaStream_t)stream));
     return from_cuda(kda::launch_recurrent(a, dims->T, (cudaStream_t)stream));
 }
 
