@@ -177,10 +177,30 @@ __device__ __forceinline__ uint32_t taddr(uint32_t base, int warp, uint32_t col)
     return base + ((uint32_t)((warp & 3) * 32) << 16) + col;
 }
 
+// This thread's two (token, 8-channel) items of the level operands: t = tid/16 + 32 r,
+// channels 8 (tid % 16) ..; loaded once per chunk and shared by the four level builds.
+struct LevelItems {
+    uint4 k[2], q[2];
+    float g[2][8];
+};
+
+__device__ __forceinline__ void load_level_items(const uint8_t* sm, int tid, LevelItems& it) {
+    const float* G2 = reinterpret_cast<const float*>(sm + OFF_G);
+    const int c8 = tid & 15;
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+        const int t = (tid >> 4) + 32 * r;
+        it.k[r] = *reinterpret_cast<const uint4*>(sm + OFF_K + t * 256 + c8 * 16);
+        it.q[r] = *reinterpret_cast<const uint4*>(sm + OFF_Q + t * 256 + c8 * 16);
+        load8g(G2, t, c8, it.g[r]);
+    }
+}
+
 // Build one level's operand in `buf`: rows 0..63 hold k_t scaled to the level's
 // reference, rows 64..127 hold q_t scaled (upper-half tokens only).  G2 is the in-chunk
 // cumulative log decay in log2 units, so every factor is one ex2 of a difference <= 0.
-__device__ __forceinline__ void build_level(uint8_t* sm, int li, uint32_t buf, int tid) {
+__device__ __forceinline__ void build_level(uint8_t* sm, int li, uint32_t buf, int tid,
+                                            const LevelItems& it) {
     const float* G2 = reinterpret_cast<const float*>(sm + OFF_G);
     const int c8 = tid & 15;
     const int h = 32 >> li;
@@ -190,18 +210,17 @@ __device__ __forceinline__ void build_level(uint8_t* sm, int li, uint32_t buf, i
         const int t = (tid >> 4) + 32 * r;
         const int ref = (t & ~(2 * h - 1)) + h - 1;
         const bool upper = (t & h) != 0;
-        float kf[8], qf[8], g8[8], r8[8], f[8], kv[8], qv[8];
-        unpack8(*reinterpret_cast<const uint4*>(sm + OFF_K + t * 256 + c8 * 16), kf);
-        load8g(G2, t, c8, g8);
+        float kf[8], qf[8], r8[8], f[8], kv[8], qv[8];
+        unpack8(it.k[r], kf);
         load8g(G2, ref, c8, r8);
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-            f[j] = ex2(upper ? g8[j] - r8[j] : r8[j] - g8[j]);
+            f[j] = ex2(upper ? it.g[r][j] - r8[j] : r8[j] - it.g[r][j]);
             kv[j] = kf[j] * f[j];
         }
         *reinterpret_cast<uint4*>(L + kmaj_off(t, c8 * 8, 128)) = pack8(kv);
         if (upper) {
-            unpack8(*reinterpret_cast<const uint4*>(sm + OFF_Q + t * 256 + c8 * 16), qf);
+            unpack8(it.q[r], qf);
 #pragma unroll
             for (int j = 0; j < 8; ++j) qv[j] = qf[j] * f[j];
             *reinterpret_cast<uint4*>(L + kmaj_off(64 + t, c8 * 8, 128)) = pack8(qv);
@@ -382,23 +401,25 @@ __global__ void __launch_bounds__(NT, 1)
         const int t0 = n * C, cn = min(C, T - t0);
         // ---------------------------------------------------------------- P3: level 32
         // one level per buffer, so each level's GEMM overlaps the next level's build
-        build_level(sm, 0, LV_L0, tid);
+        LevelItems items;
+        load_level_items(sm, tid, items);
+        build_level(sm, 0, LV_L0, tid, items);
         KDA_SYNC_FOR_MMA();
         KDA_LEVEL_MMA(LV_L0, TM_LVL, bar_m0);
         // ---------------------------------------------------------------- P3: level 16
-        build_level(sm, 1, LV_L1, tid);
+        build_level(sm, 1, LV_L1, tid, items);
         KDA_SYNC_FOR_MMA();
         KDA_LEVEL_MMA(LV_L1, TM_LVL + 64, bar_m1);
         // ---------------------------------------------------------------- P3: level 8
         KDA_WAIT(bar_m0, ph0);
         if (failed) break;
-        build_level(sm, 2, LV_L0, tid);
+        build_level(sm, 2, LV_L0, tid, items);
         KDA_SYNC_FOR_MMA();
         KDA_LEVEL_MMA(LV_L0, TM_LVL + 128, bar_m0);
         // ---------------------------------------------------------------- P3: level 4
         KDA_WAIT(bar_m1, ph1);
         if (failed) break;
-        build_level(sm, 3, LV_L1, tid);
+        build_level(sm, 3, LV_L1, tid, items);
         KDA_SYNC_FOR_MMA();
         KDA_LEVEL_MMA(LV_L1, TM_LVL + 192, bar_m1);
         // ---------------------------------------------------------------- P3: 4-token blocks
