@@ -6,7 +6,8 @@ chunk 64, bf16 I/O, fp32 state) through the C ABI: gate, intra-chunk WY,
 inter-chunk carry and output.  After the timed prefill steps the decode
 workload (B256 H32 K=V=128, fp32 state 512 MiB updated in place) is timed for
 64 consecutive single-token steps and reported in the same JSON line under
-"decode".
+"decode", and the long-sequence workload (B1 H32 T65536, h0 given; the split
+chunk-parallel form) under "long".
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 Under torchrun (N > 1) every rank runs the whole workload on its own GPU (weak
@@ -239,6 +240,49 @@ def run_decode(args, kda, inputs, peaks, ws, barrier):
     return decode
 
 
+def run_long(args, kda, inputs, peaks, ws, barrier):
+    """Time the long-sequence workload (few heads, 65536 tokens, h0 given) through the public
+    entry point, which takes the split form here; reported under "long"."""
+    import torch
+    stream = torch.cuda.current_stream()
+    inp = inputs.workload("long_bf16")
+    B, H, T, K, V, C = inp.B, inp.H, inp.T, inp.K, inp.V, inp.chunk
+    d = inp.to("cuda")
+    out = torch.empty(B, H, T, V, device="cuda", dtype=torch.bfloat16)
+    hT = torch.empty(B, H, K, V, device="cuda", dtype=torch.float32)
+
+    def step():
+        kda.chunk_forward(d.q, d.k, d.v, d.z, d.beta, d.A_log, d.dt_bias, inp.scale, d.h0, C,
+                          out=out, hT=hT)
+
+    for _ in range(3):
+        step()
+    barrier()
+    n0 = kda.launch_count()
+    secs = timed(step, args.long_steps, stream)
+    launches = kda.launch_count() - n0
+    from gated_delta_rule_26_gb300 import dist as kdist
+    secs = kdist.max_over_ranks(secs, device="cuda")
+    per = secs / args.long_steps
+    th = B * H * T
+    alg_bytes = th * bytes_per_token_head(K, V) + 2 * B * H * K * V * 4
+    flops = th * flops_per_token_head(C, K, V)
+    gbs = alg_bytes / per / 1e9
+    res = {"value": ws * B * T / per, "unit": "tokens/s", "ms_per_step": per * 1e3,
+           "steps": args.long_steps, "tflops": flops / per / 1e12,
+           "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                        "frac": gbs / peaks["hbm_gbs"], "traffic": None,
+                        "algorithmic_bytes": alg_bytes, "kernel": "kda chunked forward, split form",
+                        "kernels_per_step": launches / args.long_steps,
+                        "peak_source": peaks["source"]},
+           "gpu_launches": launches,
+           "config": {"workload": f"long_bf16 B{B} H{H} T{T} K={K} V={V} chunk {C}, h0 given",
+                      "form": "split (chosen by kda_chunk_forward for this shape)"}}
+    del d, out, hT
+    torch.cuda.empty_cache()
+    return res
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -249,7 +293,9 @@ def main():
     ap.add_argument("--decode-steps", type=int, default=64)
     ap.add_argument("--decode-batch", type=int, default=None,
                     help="decode batch B (default: the decode workload's 256)")
-    ap.add_argument("--only", default="all", choices=["all", "prefill", "decode"],
+    ap.add_argument("--long-steps", type=int, default=5,
+                    help="timed steps of the long-sequence workload")
+    ap.add_argument("--only", default="all", choices=["all", "prefill", "decode", "long"],
                     help="time only one of the two workloads (for profiler captures)")
     ap.add_argument("--prefill-T", type=int, default=None,
                     help="sequence length of the prefill workload (default 4096; smaller for "
@@ -276,6 +322,11 @@ def main():
         kdist.barrier()
 
     peaks = load_peaks()
+    if args.only == "long":
+        res = run_long(args, kda, inputs, peaks, ws, barrier)
+        if rank == 0:
+            print(json.dumps({"metric": "long only", "long": res}), flush=True)
+        return 0
     if args.only == "decode":
         decode = run_decode(args, kda, inputs, peaks, ws, barrier)
         if rank == 0:
@@ -359,6 +410,9 @@ def main():
     del host, dev, out_h, hT_h
 
     decode = None if args.only == "prefill" else run_decode(args, kda, inputs, peaks, ws, barrier)
+    del d
+    torch.cuda.empty_cache()
+    long_res = run_long(args, kda, inputs, peaks, ws, barrier)
     line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws,
             "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": per_step * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
@@ -371,7 +425,7 @@ def main():
             "tflops": tflops, "tflops_frac_bf16_burst": tflops / peaks["bf16_tflops"],
             "tflops_convention": "algorithmic (triangular) FLOPs 6KV+3CK+2CV+C^2/3 per token-head",
             "roofline": roofline, "e2e": e2e, "clocks": clocks, "gpu_launches": launches,
-            "decode": decode}
+            "decode": decode, "long": long_res}
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(inp_cpu)
     if rank == 0:

@@ -8,7 +8,8 @@
 #include "common.cuh"
 
 namespace kda {
-cudaError_t launch_chunk_tc(const ChunkArgs& a, cudaStream_t s, bool* taken);
+cudaError_t launch_chunk_tc(const ChunkArgs& a, cudaStream_t s, int mode, bool* taken);
+cudaError_t read_and_clear_carry_timeout(int* timed_out);
 cudaError_t launch_bounded_wait_selftest(unsigned long long limit_ns, cudaStream_t s);
 cudaError_t read_and_clear_timeout(cudaStream_t s, int* timed_out);
 }
@@ -96,10 +97,16 @@ int kda_gate(const kda_dims* dims, kda_dtype z_dtype, const void* z, const float
                                       dt_bias, chunk, g_out, (cudaStream_t)stream));
 }
 
-int kda_chunk_forward(const kda_dims* dims, kda_dtype io_dtype, const void* q, const void* k,
-                      const void* v, const void* z, const void* beta, const float* A_log,
-                      const float* dt_bias, float scale, const float* h0, int chunk, void* out,
-                      float* hT, kda_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// mode 0: the faster tensor-core form (or the fp32 path where it does not apply);
+// 1 / 2: only the fused / split tensor-core form, KDA_ERR_UNSUPPORTED elsewhere.
+int chunk_forward(int mode, const kda_dims* dims, kda_dtype io_dtype, const void* q,
+                  const void* k, const void* v, const void* z, const void* beta,
+                  const float* A_log, const float* dt_bias, float scale, const float* h0,
+                  int chunk, void* out, float* hT, kda_stream_t stream) {
     int st = check_dims(dims, true);
     if (st) return st;
     if (!dtype_ok(io_dtype)) return KDA_ERR_INVALID_ARG;
@@ -111,13 +118,45 @@ int kda_chunk_forward(const kda_dims* dims, kda_dtype io_dtype, const void* q, c
         st = check_ptrs({}, {h0, hT});
     }
     if (st) return st;
+    if (mode != 0 && dims->T == 0) return KDA_ERR_UNSUPPORTED;
     if (dims->T == 0 && !hT) return KDA_OK;
     kda::ChunkArgs a{dims->B, dims->H, dims->T, dims->K, dims->V, chunk, io_dtype, q, k, v, z,
                      beta, A_log, dt_bias, h0, scale, out, hT};
     bool taken = false;
-    cudaError_t e = kda::launch_chunk_tc(a, (cudaStream_t)stream, &taken);
+    cudaError_t e = kda::launch_chunk_tc(a, (cudaStream_t)stream, mode, &taken);
     if (taken) return e == cudaErrorMemoryAllocation ? KDA_ERR_NO_MEMORY : from_cuda(e);
+    if (mode != 0) return KDA_ERR_UNSUPPORTED;
     return from_cuda(kda::launch_chunk_simt(a, (cudaStream_t)stream));
+}
+
+}  // namespace
+
+extern "C" {
+
+int kda_chunk_forward(const kda_dims* dims, kda_dtype io_dtype, const void* q, const void* k,
+                      const void* v, const void* z, const void* beta, const float* A_log,
+                      const float* dt_bias, float scale, const float* h0, int chunk, void* out,
+                      float* hT, kda_stream_t stream) {
+    return chunk_forward(0, dims, io_dtype, q, k, v, z, beta, A_log, dt_bias, scale, h0, chunk,
+                         out, hT, stream);
+}
+
+int kda_chunk_forward_split(const kda_dims* dims, kda_dtype io_dtype, const void* q,
+                            const void* k, const void* v, const void* z, const void* beta,
+                            const float* A_log, const float* dt_bias, float scale,
+                            const float* h0, int chunk, void* out, float* hT,
+                            kda_stream_t stream) {
+    return chunk_forward(2, dims, io_dtype, q, k, v, z, beta, A_log, dt_bias, scale, h0, chunk,
+                         out, hT, stream);
+}
+
+int kda_chunk_forward_fused(const kda_dims* dims, kda_dtype io_dtype, const void* q,
+                            const void* k, const void* v, const void* z, const void* beta,
+                            const float* A_log, const float* dt_bias, float scale,
+                            const float* h0, int chunk, void* out, float* hT,
+                            kda_stream_t stream) {
+    return chunk_forward(1, dims, io_dtype, q, k, v, z, beta, A_log, dt_bias, scale, h0, chunk,
+                         out, hT, stream);
 }
 
 int kda_fused_recurrent(const kda_dims* dims, kda_dtype io_dtype, const void* q, const void* k,
@@ -140,8 +179,11 @@ int kda_fused_recurrent(const kda_dims* dims, kda_dtype io_dtype, const void* q,
 
 int kda_device_status(kda_stream_t stream) {
     int timed_out = 0;
-    if (kda::read_and_clear_timeout((cudaStream_t)stream, &timed_out) != cudaSuccess)
+    int carry_timed_out = 0;
+    if (kda::read_and_clear_timeout((cudaStream_t)stream, &timed_out) != cudaSuccess ||
+        kda::read_and_clear_carry_timeout(&carry_timed_out) != cudaSuccess)
         return KDA_ERR_CUDA;
+    timed_out |= carry_timed_out;
     return timed_out ? KDA_ERR_TIMEOUT : KDA_OK;
 }
 

@@ -1,0 +1,318 @@
+// chunk_carry.cu -- the sequential half of the split KDA chunked forward (bf16 I/O,
+// K = V = 128, chunk C = 64): the inter-chunk state carry and the output, fed by the
+// per-chunk operands that the chunk-parallel prep kernel wrote.
+//
+// Per (b, h) sequence one CTA (16 warps) keeps the fp32 state S (K x V) in TMEM and walks
+// the chunks of a segment in order; per chunk n (kda-adjoint-2026-10-01, section 2, with
+// the read scale of kdafix-2026-10-02 "Fix 2"):
+//
+//   C1  D = S^T [W^T | Q'^T] = [(W S)^T | (Q' S)^T]       tcgen05, S as a bf16 operand
+//   C2  Delta^T = U^T - (W S)^T   and   o = scale ((Q' S)^T + U'^T)^T   -> bf16 to HBM
+//   C3  S <- diag(Gamma_last) S + K~^T Delta,  K~ = K e^{G_last - G}      tcgen05, fp32 in TMEM
+//
+// which is the chunked WY form of the per-token recurrence S <- diag(alpha) S,
+// u = v - S^T k, S <- S + beta k u^T, o = S^T (scale q).  The operands of a chunk arrive by
+// TMA into one of two stages while the previous chunk is processed.
+#include <cuda.h>
+#include <stddef.h>
+
+#include "chunk_tiles.cuh"
+#include "common.cuh"
+#include "tc_ptx.cuh"
+
+namespace kda {
+
+__device__ int g_kda_carry_timeout;
+
+namespace {
+
+using namespace tile;
+constexpr int NT2 = 512;
+
+// ---- shared memory map (bytes from a 1024-byte aligned base)
+constexpr uint32_t K2_S = 0;            // 32 KB S bf16, MN-major [c][v] (2 atoms)
+constexpr uint32_t K2_DELTA = 32768;    // 16 KB Delta^T, K-major [v][t]
+constexpr uint32_t K2_STAGE = 49152;    // two operand stages
+// one stage: [W^T | Q'^T] (MN-major, 2 atoms), [U^T | U'^T] (K-major [v][t], 2 atoms),
+// K~ (MN-major [t][c], 2 atoms of 8 KB), Gamma_last; the o tile of the chunk is staged
+// row-major [t][v] over the [W^T | Q'^T] slot once C1 has consumed it.
+constexpr uint32_t ST_WQ = 0, ST_UU = 32768, ST_KT = 65536, ST_GL = 81920;
+constexpr uint32_t ST_BYTES = 82944;  // 81 KB, a multiple of 1024
+constexpr uint32_t ST_TX = (uint32_t)kItemBytes;
+constexpr uint32_t K2_MISC = K2_STAGE + 2 * ST_BYTES;
+
+struct CarryMisc {
+    alignas(8) uint64_t bar_full[2];  // TMA: one stage's operands
+    uint64_t bar_mma;                 // tensor-core commits (C1, C3 alternate)
+    uint32_t tmem_base;
+};
+constexpr uint32_t K2_SMEM = K2_MISC + sizeof(CarryMisc) + 1024;
+static_assert(K2_SMEM <= 227 * 1024, "carry kernel shared memory");
+static_assert(ST_TX <= ST_BYTES && ST_GL + kItemGL <= ST_BYTES, "stage layout");
+
+constexpr uint32_t TM_S2 = 0;    // fp32 state, lanes = key channel c, cols = v   (128)
+constexpr uint32_t TM_D2 = 128;  // S^T [W^T | Q'^T]                              (128)
+constexpr uint32_t IDESC_SQ2 = tc::idesc_bf16(128, 128, 1, 1);
+constexpr uint32_t IDESC_SK2 = tc::idesc_bf16(128, 128, 1, 0);
+
+}  // namespace
+
+__global__ void __launch_bounds__(NT2, 1)
+    kda_chunk_carry_kernel(const __grid_constant__ CUtensorMap tm_wq,
+                           const __grid_constant__ CUtensorMap tm_uu,
+                           const __grid_constant__ CUtensorMap tm_kt,
+                           const float* __restrict__ gl, int T, int seg_n0, int seg_len,
+                           float scale, const float* h_in, __nv_bfloat16* __restrict__ out,
+                           float* h_out) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+    const uint32_t sb = tc::smem_u32(sm);
+    CarryMisc& ms = *reinterpret_cast<CarryMisc*>(sm + K2_MISC);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    // warp w reaches TMEM lanes 32 (w & 3) ..; the four warps of a quarter split the columns
+    const int q4 = warp & 3, part = warp >> 2, row = q4 * 32 + lane;
+    const size_t bh = blockIdx.x;
+
+    if (tid == 0) {
+        tc::mbar_init(&ms.bar_full[0], 1);
+        tc::mbar_init(&ms.bar_full[1], 1);
+        tc::mbar_init(&ms.bar_mma, 1);
+        tc::fence_barrier_init();
+        tc::tma_prefetch_desc(&tm_wq);
+        tc::tma_prefetch_desc(&tm_uu);
+        tc::tma_prefetch_desc(&tm_kt);
+    }
+    if (warp == 0) {
+        tc::tmem_alloc(&ms.tmem_base, 256);
+        tc::tmem_relinquish();
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = ms.tmem_base;
+
+    // the operands of chunk j of the segment into stage s
+    auto issue = [&](int j, int s) {
+        uint8_t* st = sm + K2_STAGE + s * ST_BYTES;
+        const int item = (int)bh * seg_len + j;
+        uint64_t* bar = &ms.bar_full[s];
+        tc::mbar_arrive_expect_tx(bar, ST_TX);
+        tc::tma_load_3d(st + ST_WQ, &tm_wq, 0, 0, 2 * item, bar);
+        tc::tma_load_3d(st + ST_WQ + 16384, &tm_wq, 0, 0, 2 * item + 1, bar);
+        tc::tma_load_3d(st + ST_UU, &tm_uu, 0, 0, 2 * item, bar);
+        tc::tma_load_3d(st + ST_UU + 16384, &tm_uu, 0, 0, 2 * item + 1, bar);
+        tc::tma_load_3d(st + ST_KT, &tm_kt, 0, 0, item, bar);
+        tc::tma_load_3d(st + ST_KT + 8192, &tm_kt, 64, 0, item, bar);
+        tc::bulk_load(st + ST_GL, gl + (size_t)item * KD, (uint32_t)kItemGL, bar);
+    };
+    if (tid == 0 && seg_len > 0) {
+        issue(0, 0);
+        if (seg_len > 1) issue(1, 1);
+    }
+
+    // Initial state: fp32 into TMEM (lane c), bf16 copy as the MN-major operand [c][v].
+    {
+        const int c = row;
+#pragma unroll 1
+        for (int v0 = 32 * part; v0 < 32 * part + 32; v0 += 16) {
+            float f[16];
+#pragma unroll
+            for (int j = 0; j < 16; j += 4) {
+                float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (h_in) x = *reinterpret_cast<const float4*>(h_in + (bh * KD + c) * VD + v0 + j);
+                f[j] = x.x; f[j + 1] = x.y; f[j + 2] = x.z; f[j + 3] = x.w;
+            }
+            uint32_t r[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) r[j] = __float_as_uint(f[j]);
+            tc::tmem_st16(taddr(tmem, warp, TM_S2 + v0), r);
+            store16_mn(sm + K2_S, c, v0, 16384, f);
+        }
+        tc::tmem_st_wait();
+    }
+    tc::fence_proxy_async_smem();
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+
+    uint32_t ph_full = 0u, ph_m = 0u;  // ph_full: bit s = parity of stage s
+    bool failed = false;
+#define KDA_CARRY_WAIT(bar, ph)                                          \
+    do {                                                                 \
+        const bool ok_ = tid != 0 || tc::mbar_wait(&(bar), ph);          \
+        ph ^= 1u;                                                        \
+        if (__syncthreads_or(!ok_)) failed = true;                       \
+        tc::fence_after_sync();                                          \
+    } while (0)
+
+    for (int j = 0; j < seg_len && !failed; ++j) {
+        const int s = j & 1;
+        uint8_t* st = sm + K2_STAGE + s * ST_BYTES;
+        const uint32_t stb = sb + K2_STAGE + s * ST_BYTES;
+        const int t0 = (seg_n0 + j) * C, cn = min(C, T - t0);
+        // ---------------------------------------------------------------- K2: wait operands
+        {
+            const bool ok = tid != 0 || tc::mbar_wait(&ms.bar_full[s], (ph_full >> s) & 1u);
+            ph_full ^= 1u << s;
+            if (__syncthreads_or(!ok)) failed = true;
+            tc::fence_after_sync();
+            if (failed) break;
+        }
+        // ---------------------------------------------------------------- K2: C1 + decay
+        // C1: D[v][t'] = sum_c S[c][v] [W^T | Q'^T][c][t']
+        if (tid == 0) {
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks)
+                tc::mma_bf16(tmem + TM_D2, desc_mn(sb + K2_S, 16384, ks),
+                             desc_mn(stb + ST_WQ, 16384, ks), IDESC_SQ2, ks > 0);
+            tc::mma_commit(&ms.bar_mma);
+        }
+        // meanwhile: S <- diag(Gamma_last) S in TMEM (row c, this warp's 32 columns)
+        {
+            const float g = reinterpret_cast<const float*>(st + ST_GL)[row];
+            {
+                const int v0 = 32 * part;
+                uint32_t d0[16], d1[16];
+                tc::tmem_ld16(taddr(tmem, warp, TM_S2 + v0), d0);
+                tc::tmem_ld16(taddr(tmem, warp, TM_S2 + v0 + 16), d1);
+                tc::tmem_ld_wait();
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    d0[i] = __float_as_uint(__uint_as_float(d0[i]) * g);
+                    d1[i] = __float_as_uint(__uint_as_float(d1[i]) * g);
+                }
+                tc::tmem_st16(taddr(tmem, warp, TM_S2 + v0), d0);
+                tc::tmem_st16(taddr(tmem, warp, TM_S2 + v0 + 16), d1);
+            }
+            tc::tmem_st_wait();
+        }
+        tc::fence_before_sync();
+        KDA_CARRY_WAIT(ms.bar_mma, ph_m);
+        if (failed) break;
+        // ---------------------------------------------------------------- K2: C2
+        // C2: lane v, tokens 16 part ..: Delta^T -> K-major [v][t]; o -> staging [t][v]
+        {
+            const int v = row;
+            __nv_bfloat16* ost = reinterpret_cast<__nv_bfloat16*>(st + ST_WQ);
+            {
+                const int tb = 16 * part;
+                uint32_t dw[16], dq[16];
+                tc::tmem_ld16(taddr(tmem, warp, TM_D2 + tb), dw);
+                tc::tmem_ld16(taddr(tmem, warp, TM_D2 + 64 + tb), dq);
+                float u[16], up[16];
+                load16_k(st + ST_UU, v, tb, 128, u);
+                load16_k(st + ST_UU + 16384, v, tb, 128, up);
+                tc::tmem_ld_wait();
+                float f[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) f[i] = u[i] - __uint_as_float(dw[i]);
+                store16_k(sm + K2_DELTA, v, tb, 128, f);
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                    ost[(tb + i) * VD + v] = __float2bfloat16_rn(scale * (__uint_as_float(dq[i]) + up[i]));
+            }
+        }
+        tc::fence_proxy_async_smem();
+        tc::fence_before_sync();
+        __syncthreads();
+        tc::fence_after_sync();
+        // ---------------------------------------------------------------- K2: C3 + o out
+        // C3: S += K~^T Delta, while the staged o rows go out
+        if (tid == 0) {
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks)
+                tc::mma_bf16(tmem + TM_S2, desc_mn(stb + ST_KT, 8192, ks),
+                             desc_k(sb + K2_DELTA, 128, ks), IDESC_SK2, 1u);
+            tc::mma_commit(&ms.bar_mma);
+        }
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+            const int q = tid + NT2 * r, tr = q >> 4, c16 = q & 15;
+            if (tr < cn)
+                *reinterpret_cast<uint4*>(out + (bh * T + t0 + tr) * VD + c16 * 8) =
+                    *reinterpret_cast<const uint4*>(st + ST_WQ + tr * 256 + c16 * 16);
+        }
+        KDA_CARRY_WAIT(ms.bar_mma, ph_m);
+        if (failed) break;
+        // ---------------------------------------------------------------- K2: S to bf16
+        // S (fp32, TMEM) -> bf16 operand [c][v]
+        {
+            const int c = row;
+            {
+                const int v0 = 32 * part;
+                uint32_t d0[16], d1[16];
+                tc::tmem_ld16(taddr(tmem, warp, TM_S2 + v0), d0);
+                tc::tmem_ld16(taddr(tmem, warp, TM_S2 + v0 + 16), d1);
+                tc::tmem_ld_wait();
+                float f[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) f[i] = __uint_as_float(d0[i]);
+                store16_mn(sm + K2_S, c, v0, 16384, f);
+#pragma unroll
+                for (int i = 0; i < 16; ++i) f[i] = __uint_as_float(d1[i]);
+                store16_mn(sm + K2_S, c, v0 + 16, 16384, f);
+            }
+        }
+        tc::fence_proxy_async_smem();
+        tc::fence_before_sync();
+        __syncthreads();
+        tc::fence_after_sync();
+        // stage s is consumed (C1, C2, C3 and the o rows): refill it two chunks ahead
+        if (tid == 0 && j + 2 < seg_len) issue(j + 2, s);
+    }
+#undef KDA_CARRY_WAIT
+
+    if (!failed && h_out) {
+        const int c = row;
+#pragma unroll 1
+        for (int v0 = 32 * part; v0 < 32 * part + 32; v0 += 16) {
+            uint32_t d[16];
+            tc::tmem_ld16(taddr(tmem, warp, TM_S2 + v0), d);
+            tc::tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 16; i += 4)
+                *reinterpret_cast<float4*>(h_out + (bh * KD + c) * VD + v0 + i) =
+                    make_float4(__uint_as_float(d[i]), __uint_as_float(d[i + 1]),
+                                __uint_as_float(d[i + 2]), __uint_as_float(d[i + 3]));
+        }
+    }
+    if (failed && tid == 0) {
+        atomicExch(&g_kda_carry_timeout, 1);
+        // give the tensor-core and TMA work still in flight a bounded chance to finish
+        tc::mbar_wait(&ms.bar_mma, ph_m, 200000000ull);
+        tc::mbar_wait(&ms.bar_full[0], ph_full & 1u, 200000000ull);
+        tc::mbar_wait(&ms.bar_full[1], (ph_full >> 1) & 1u, 200000000ull);
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 0) tc::tmem_dealloc(tmem, 256);
+}
+
+cudaError_t launch_chunk_carry(const CUtensorMap& wq, const CUtensorMap& uu, const CUtensorMap& kt,
+                               const float* gl, int BH, int T, int seg_n0, int seg_len,
+                               float scale, const float* h_in, __nv_bfloat16* out, float* h_out,
+                               cudaStream_t s) {
+    cudaError_t err = cudaFuncSetAttribute(kda_chunk_carry_kernel,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           (int)K2_SMEM);
+    if (err != cudaSuccess) return err;
+    kda_chunk_carry_kernel<<<BH, NT2, K2_SMEM, s>>>(wq, uu, kt, gl, T, seg_n0, seg_len, scale, h_in,
+                                                     out, h_out);
+    count_launches(1);
+    return cudaGetLastError();
+}
+
+cudaError_t read_and_clear_carry_timeout(int* timed_out) {
+    int v = 0;
+    cudaError_t e = cudaMemcpyFromSymbol(&v, g_kda_carry_timeout, sizeof(int));
+    if (e != cudaSuccess) return e;
+    *timed_out = v;
+    if (v) {
+        const int zero = 0;
+        e = cudaMemcpyToSymbol(g_kda_carry_timeout, &zero, sizeof(int));
+    }
+    return e;
+}
+
+}  // namespace kda

@@ -45,6 +45,7 @@
 #include <cuda.h>
 #include <stddef.h>
 
+#include "chunk_tiles.cuh"
 #include "common.cuh"
 #include "tc_ptx.cuh"
 
@@ -54,7 +55,8 @@ __device__ int g_kda_tc_timeout;
 
 namespace {
 
-constexpr int C = 64, KD = 128, VD = 128, NT = 512;
+using namespace tile;
+constexpr int NT = 512;
 constexpr float LOG2E = 1.4426950408889634f;
 
 // ---- shared memory map (bytes from a 1024-byte aligned base)
@@ -80,6 +82,7 @@ constexpr uint32_t LV_UT = 32768;   // U^T K-major [v][i] (16 KB)            P5
 constexpr uint32_t LV_Z = 49152;    // z tile of the NEXT chunk (16 KB)      P5-P2
 constexpr uint32_t LV_DELTA = 16384;// Delta^T K-major [v][t] (16 KB)        C2-C3
 constexpr uint32_t LV_OST = 0;      // o staging, row-major [t][v] bf16      C2
+constexpr uint32_t LV_UPS = 0;      // prep kernel: U'^T staging, K-major [v][t] (16 KB)
 // K~ (K e^{G_last - G}, MN-major [t][c]) lives in the v-tile slot OFF_V from P5 to C3.
 
 struct Misc {
@@ -112,21 +115,6 @@ constexpr uint32_t IDESC_QNEG = tc::idesc_bf16(128, 64, 0, 0) | (1u << 14);  // 
 constexpr uint32_t IDESC_SQ = tc::idesc_bf16(128, 128, 1, 1);
 constexpr uint32_t IDESC_SK = tc::idesc_bf16(128, 128, 1, 0);
 
-__device__ __forceinline__ float ex2(float x) {
-    float y;
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
-}
-__device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
-__device__ __forceinline__ void unpack8(uint4 r, float (&f)[8]) {
-    f[0] = bf_lo(r.x); f[1] = bf_hi(r.x); f[2] = bf_lo(r.y); f[3] = bf_hi(r.y);
-    f[4] = bf_lo(r.z); f[5] = bf_hi(r.z); f[6] = bf_lo(r.w); f[7] = bf_hi(r.w);
-}
-__device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
-    return make_uint4(tc::pack_bf16x2(f[0], f[1]), tc::pack_bf16x2(f[2], f[3]),
-                      tc::pack_bf16x2(f[4], f[5]), tc::pack_bf16x2(f[6], f[7]));
-}
 // G2 (fp32, 64 tokens x 128 channels) keeps each row as two halves: channel
 // c = 8 a + 4 h + j sits at 64 h + 4 a + j, so that both the 8-channel groups read by
 // (token, 8 channels) items and the 4-channel groups read by (token, lane) items are
@@ -141,40 +129,6 @@ __device__ __forceinline__ void load8g(const float* G2, int t, int c8, float (&f
 // softplus(x) = max(x, 0) + log(1 + e^{-|x|}) with the hardware exp2/log2 approximations.
 __device__ __forceinline__ float softplus_fast(float x) {
     return fmaxf(x, 0.f) + __logf(1.f + __expf(-fabsf(x)));
-}
-
-// K-major tile with `rows` rows: byte offset of element (row, k); k atoms of 64.
-__device__ __forceinline__ uint32_t kmaj_off(int row, int k, int rows) {
-    return (uint32_t)((k >> 6) * (rows * 128)) + tc::sw128_offset(row, (k & 63) >> 3) + (k & 7) * 2;
-}
-// MN-major tile: element (krow, mn), MN atoms of 64 elements `atom` bytes apart.
-__device__ __forceinline__ uint32_t mnmaj_off(int krow, int mn, uint32_t atom) {
-    return (uint32_t)(mn >> 6) * atom + tc::sw128_offset(krow, (mn & 63) >> 3) + (mn & 7) * 2;
-}
-// 16 consecutive elements (two 16-byte chunks) of one row of a K-major / MN-major tile.
-__device__ __forceinline__ void store16_k(uint8_t* base, int row, int k0, int rows, const float (&f)[16]) {
-    float lo[8], hi[8];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) { lo[j] = f[j]; hi[j] = f[8 + j]; }
-    *reinterpret_cast<uint4*>(base + kmaj_off(row, k0, rows)) = pack8(lo);
-    *reinterpret_cast<uint4*>(base + kmaj_off(row, k0 + 8, rows)) = pack8(hi);
-}
-__device__ __forceinline__ void store16_mn(uint8_t* base, int krow, int mn0, uint32_t atom, const float (&f)[16]) {
-    float lo[8], hi[8];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) { lo[j] = f[j]; hi[j] = f[8 + j]; }
-    *reinterpret_cast<uint4*>(base + mnmaj_off(krow, mn0, atom)) = pack8(lo);
-    *reinterpret_cast<uint4*>(base + mnmaj_off(krow, mn0 + 8, atom)) = pack8(hi);
-}
-__device__ __forceinline__ uint64_t desc_k(uint32_t saddr, int rows, int ks) {
-    const int k0 = ks * 16;
-    return tc::smem_desc(saddr + (k0 >> 6) * (rows * 128) + (k0 & 63) * 2, 16, 1024);
-}
-__device__ __forceinline__ uint64_t desc_mn(uint32_t saddr, uint32_t atom, int ks) {
-    return tc::smem_desc(saddr + ks * 2048, atom, 1024);
-}
-__device__ __forceinline__ uint32_t taddr(uint32_t base, int warp, uint32_t col) {
-    return base + ((uint32_t)((warp & 3) * 32) << 16) + col;
 }
 
 // This thread's two (token, 8-channel) items of the level operands: t = tid/16 + 32 r,
@@ -235,17 +189,30 @@ __device__ __forceinline__ int swz(int t, int i) {
     return t * 64 + ((((i >> 2) ^ (t & 15))) << 2) + (i & 3);
 }
 
-}  // namespace
+// What the chunk-parallel prep kernel writes per work item (one chunk of one sequence):
+// [W^T | Q'^T] and [U^T | U'^T] through the tile maps tm_wq / tm_uu (z = 2 item, 2 item + 1),
+// K~ through tm_kt (z = item) and Gamma_last (fp32) at gl + 128 item.  Items are the chunks
+// [seg_n0, seg_n0 + seg_len) of every sequence, item = bh * seg_len + (n - seg_n0).
+struct PrepSeg {
+    int seg_n0, seg_len, items;
+    float* gl;
+};
 
-__global__ void __launch_bounds__(NT, 1)
-    kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
-                        const __grid_constant__ CUtensorMap tm_k,
-                        const __grid_constant__ CUtensorMap tm_v,
-                        const __grid_constant__ CUtensorMap tm_z, int H, int T,
-                        const __nv_bfloat16* __restrict__ beta, const float* __restrict__ A_log,
-                        const float* __restrict__ dt_bias, float scale,
-                        const float* __restrict__ h0, __nv_bfloat16* __restrict__ out,
-                        float* __restrict__ hT) {
+// The chunk loop shared by the fused kernel (kSplit = false: one CTA per sequence, the
+// state carried in TMEM from chunk to chunk) and the prep kernel (kSplit = true: CTAs
+// stride over the chunks of all sequences, and everything that does not depend on the
+// state is written out for the carry kernel).
+template <bool kSplit>
+__device__ __forceinline__ void chunk_loop(const CUtensorMap* tm_q, const CUtensorMap* tm_k,
+                                           const CUtensorMap* tm_v, const CUtensorMap* tm_z,
+                                           const CUtensorMap* tm_wq, const CUtensorMap* tm_uu,
+                                           const CUtensorMap* tm_kt, int H, int T,
+                                           const __nv_bfloat16* __restrict__ beta,
+                                           const float* __restrict__ A_log,
+                                           const float* __restrict__ dt_bias, float scale,
+                                           const float* __restrict__ h0,
+                                           __nv_bfloat16* __restrict__ out, float* __restrict__ hT,
+                                           PrepSeg seg) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -256,23 +223,32 @@ __global__ void __launch_bounds__(NT, 1)
     // TMEM is read in 32-lane quarters: warp w reaches lanes 32*(w & 3) .. +31; the four
     // warps sharing a quarter split the columns by `part`.
     const int q4 = warp & 3, part = warp >> 2, row = q4 * 32 + lane;
-    const size_t bh = blockIdx.x;
-    const int h = (int)(bh % H);
-    const float exp_A = expf(A_log[h]);
+    const int nchunks = (T + C - 1) / C;
+    // Work items: the chunks of sequence blockIdx.x (fused), or every gridDim.x-th item of
+    // the segment (prep).
+    const int it_begin = kSplit ? (int)blockIdx.x : 0;
+    const int it_end = kSplit ? seg.items : nchunks;
+    const int it_step = kSplit ? (int)gridDim.x : 1;
+    auto item_bh = [&](int it) -> size_t {
+        return kSplit ? (size_t)(it / seg.seg_len) : (size_t)blockIdx.x;
+    };
+    auto item_n = [&](int it) -> int { return kSplit ? seg.seg_n0 + it % seg.seg_len : it; };
+    const int h_cta = (int)(item_bh(it_begin) % H);  // the fused kernel's head
+    const float exp_A = expf(A_log[h_cta]);
 
     for (int i = tid; i < (int)(OFF_MISC / 16); i += NT)
         reinterpret_cast<uint4*>(sm)[i] = make_uint4(0u, 0u, 0u, 0u);
-    if (tid < KD) ms.dt[tid] = dt_bias[(size_t)h * KD + tid];
+    if (tid < KD) ms.dt[tid] = dt_bias[(size_t)h_cta * KD + tid];
     if (tid == 0) {
         tc::mbar_init(&ms.bar_qkz, 1);
         tc::mbar_init(&ms.bar_v, 1);
         tc::mbar_init(&ms.bar_m0, 1);
         tc::mbar_init(&ms.bar_m1, 1);
         tc::fence_barrier_init();
-        tc::tma_prefetch_desc(&tm_q);
-        tc::tma_prefetch_desc(&tm_k);
-        tc::tma_prefetch_desc(&tm_v);
-        tc::tma_prefetch_desc(&tm_z);
+        tc::tma_prefetch_desc(tm_q);
+        tc::tma_prefetch_desc(tm_k);
+        tc::tma_prefetch_desc(tm_v);
+        tc::tma_prefetch_desc(tm_z);
     }
     if (warp == 0) {
         tc::tmem_alloc(&ms.tmem_base, 512);
@@ -286,7 +262,8 @@ __global__ void __launch_bounds__(NT, 1)
     // 64 x 64 identity, K-major bf16: the B operand that copies (Q Gamma)^T into an accumulator
     if (tid < 64) *reinterpret_cast<uint16_t*>(sm + OFF_ID + kmaj_off(tid, tid, 64)) = 0x3F80u;
     // Initial state: fp32 into TMEM (lane c = row), bf16 copy as the MN-major operand [c][v].
-    {
+    if (!kSplit) {
+        const size_t bh = blockIdx.x;
         const int c = row;
 #pragma unroll 1
         for (int v0 = 32 * part; v0 < 32 * part + 32; v0 += 16) {
@@ -312,32 +289,60 @@ __global__ void __launch_bounds__(NT, 1)
 
     uint32_t ph_qkz = 0, ph_v = 0, ph0 = 0, ph1 = 0;
     bool failed = false;
-    const int nchunks = (T + C - 1) / C;
-    const bool group_c = warp < 8;  // carry group; warps 8-15 form the gate group
-    if (tid == 0 && nchunks > 0) {
+    const bool group_c = warp < 8;  // fused: carry group; warps 8-15 form the gate group
+    if (tid == 0 && it_begin < it_end) {
+        const int bh0 = (int)item_bh(it_begin), y0 = item_n(it_begin) * C;
         tc::mbar_arrive_expect_tx(&ms.bar_qkz, 3u * 16384u);
-        tc::tma_load_3d(sm + OFF_Q, &tm_q, 0, 0, (int)bh, &ms.bar_qkz);
-        tc::tma_load_3d(sm + OFF_K, &tm_k, 0, 0, (int)bh, &ms.bar_qkz);
-        tc::tma_load_3d(sm + OFF_LVL + LV_Z, &tm_z, 0, 0, (int)bh, &ms.bar_qkz);
+        tc::tma_load_3d(sm + OFF_Q, tm_q, 0, y0, bh0, &ms.bar_qkz);
+        tc::tma_load_3d(sm + OFF_K, tm_k, 0, y0, bh0, &ms.bar_qkz);
+        tc::tma_load_3d(sm + OFF_LVL + LV_Z, tm_z, 0, y0, bh0, &ms.bar_qkz);
         tc::mbar_arrive_expect_tx(&ms.bar_v, 16384u);
-        tc::tma_load_3d(sm + OFF_V, &tm_v, 0, 0, (int)bh, &ms.bar_v);
+        tc::tma_load_3d(sm + OFF_V, tm_v, 0, y0, bh0, &ms.bar_v);
     }
 
-    // Gate of chunk `nc` by the gate group (warps 8-15, named barrier 2): waits for its
-    // q/k/z tiles, loads beta, and writes G2 = in-chunk cumulative log2 decay.
-    auto gate_scan = [&](int nc) -> bool {
-        const int wg = warp - 8;
-        const bool ok = !tc::named_sync_or(2, 256, !(tid != 256 || tc::mbar_wait(&ms.bar_qkz, ph_qkz)));
-        const int tn = nc * C, cnn = min(C, T - tn);
+    // Gate of item (gbh, gn) by warps GLO .. GLO + GW - 1 (named barrier 2): waits for its
+    // q/k/z tiles, loads beta, and writes G2 = in-chunk cumulative log2 decay.  The fused
+    // kernel runs it on warps 8-15 during the carry; the prep kernel on all warps.
+    constexpr int GLO = kSplit ? 0 : 8, GW = kSplit ? 16 : 8, TPW = C / GW;
+    // The gate's global reads (beta; for the prep kernel also dt_bias and A_log of the item's
+    // head) are issued early by the gate threads, so that their latency is hidden by the
+    // tensor-core work in between.
+    struct GatePre {  // raw loaded values: nothing here waits for the loads to land
+        unsigned short beta_bits;
+        float A_log_h;
+        float4 dt;
+    };
+    auto gate_fetch = [&](size_t gbh, int gn) -> GatePre {
+        GatePre p;
+        // an in-bounds token for every thread; gate_scan keeps the value only for tg < cnn
+        const int tg = (warp - GLO) * 32 + lane, tn = gn * C, cnn = min(C, T - tn);
+        const int tc = max(0, min(tg, cnn - 1));
+        p.beta_bits = __ldg(reinterpret_cast<const unsigned short*>(beta) + gbh * T + tn + tc);
+        if (kSplit) {
+            const int hh = (int)(gbh % H);
+            const float* db = dt_bias + (size_t)hh * KD + lane * 4;
+            p.dt = make_float4(__ldg(db), __ldg(db + 1), __ldg(db + 2), __ldg(db + 3));
+            p.A_log_h = __ldg(A_log + hh);
+        } else {
+            p.dt = make_float4(0.f, 0.f, 0.f, 0.f);
+            p.A_log_h = 0.f;
+        }
+        return p;
+    };
+    auto gate_scan = [&](size_t gbh, int gn, const GatePre& gp) -> bool {
+        const int wg = warp - GLO;
+        const bool ok = !tc::named_sync_or(2, 32 * GW,
+                                           !(tid != 32 * GLO || tc::mbar_wait(&ms.bar_qkz, ph_qkz)));
+        const int tn = gn * C, cnn = min(C, T - tn);
         const int tg = wg * 32 + lane;
-        if (tg < C) ms.beta[tg] = tg < cnn ? __bfloat162float(beta[bh * T + tn + tg]) : 0.f;
+        if (tg < C) ms.beta[tg] = tg < cnn ? __uint_as_float((uint32_t)gp.beta_bits << 16) : 0.f;
         const int c4 = lane * 4;
-        const float4 dt = *reinterpret_cast<const float4*>(&ms.dt[c4]);
-        const float mult = -exp_A * LOG2E;
+        const float4 dt = kSplit ? gp.dt : *reinterpret_cast<const float4*>(&ms.dt[c4]);
+        const float mult = -(kSplit ? expf(gp.A_log_h) : exp_A) * LOG2E;
         float acc0 = 0.f, acc1 = 0.f, acc2 = 0.f, acc3 = 0.f;
 #pragma unroll
-        for (int a = 0; a < 8; ++a) {
-            const int t = 8 * wg + a;
+        for (int a = 0; a < TPW; ++a) {
+            const int t = TPW * wg + a;
             const uint2 zr = *reinterpret_cast<const uint2*>(sm + OFF_LVL + LV_Z + t * 256 + c4 * 2);
             const float x0 = bf_lo(zr.x) + dt.x, x1 = bf_hi(zr.x) + dt.y;
             const float x2 = bf_lo(zr.y) + dt.z, x3 = bf_hi(zr.y) + dt.w;
@@ -348,17 +353,17 @@ __global__ void __launch_bounds__(NT, 1)
             acc3 = fmaf(m, softplus_fast(x3), acc3);
             *reinterpret_cast<float4*>(G2 + t * KD + g4off(lane)) = make_float4(acc0, acc1, acc2, acc3);
         }
-        tc::named_sync(2, 256);
+        tc::named_sync(2, 32 * GW);
         float4 pre = make_float4(0.f, 0.f, 0.f, 0.f);
         for (int g = 0; g < wg; ++g) {
-            const float4 x = *reinterpret_cast<const float4*>(G2 + (8 * g + 7) * KD + g4off(lane));
+            const float4 x = *reinterpret_cast<const float4*>(G2 + (TPW * g + TPW - 1) * KD + g4off(lane));
             pre.x += x.x; pre.y += x.y; pre.z += x.z; pre.w += x.w;
         }
-        tc::named_sync(2, 256);
+        tc::named_sync(2, 32 * GW);
         if (wg > 0) {
 #pragma unroll
-            for (int a = 0; a < 8; ++a) {
-                float4* p = reinterpret_cast<float4*>(G2 + (8 * wg + a) * KD + g4off(lane));
+            for (int a = 0; a < TPW; ++a) {
+                float4* p = reinterpret_cast<float4*>(G2 + (TPW * wg + a) * KD + g4off(lane));
                 float4 x = *p;
                 x.x += pre.x; x.y += pre.y; x.z += pre.z; x.w += pre.w;
                 *p = x;
@@ -367,7 +372,10 @@ __global__ void __launch_bounds__(NT, 1)
         return ok;
     };
 
-    if (nchunks > 0 && !group_c) failed = !gate_scan(0);
+    if (it_begin < it_end && (kSplit || !group_c)) {
+        const GatePre gp = gate_fetch(item_bh(it_begin), item_n(it_begin));
+        failed = !gate_scan(item_bh(it_begin), item_n(it_begin), gp);
+    }
     ph_qkz ^= 1u;
     if (__syncthreads_or(failed)) failed = true;
 
@@ -397,8 +405,19 @@ __global__ void __launch_bounds__(NT, 1)
         }                                                                \
     } while (0)
 
-    for (int n = 0; n < nchunks && !failed; ++n) {
-        const int t0 = n * C, cn = min(C, T - t0);
+    for (int it = it_begin; it < it_end && !failed; it += it_step) {
+        const size_t bh = item_bh(it);
+        const int t0 = item_n(it) * C, cn = min(C, T - t0);
+        const bool has_next = it + it_step < it_end;
+        const size_t nbh = has_next ? item_bh(it + it_step) : bh;
+        const int nt0 = has_next ? item_n(it + it_step) * C : t0;
+        if (kSplit && tid == 0 && has_next) {
+            // the next item's tiles into L2 now, so that its loads later find them there
+            tc::tma_prefetch_l2_3d(tm_z, 0, nt0, (int)nbh);
+            tc::tma_prefetch_l2_3d(tm_q, 0, nt0, (int)nbh);
+            tc::tma_prefetch_l2_3d(tm_k, 0, nt0, (int)nbh);
+            tc::tma_prefetch_l2_3d(tm_v, 0, nt0, (int)nbh);
+        }
         // ---------------------------------------------------------------- P3: level 32
         // one level per buffer, so each level's GEMM overlaps the next level's build
         LevelItems items;
@@ -543,8 +562,8 @@ __global__ void __launch_bounds__(NT, 1)
             }
             // beta K Gamma and beta V as MN-major [t][.] operands
 #pragma unroll
-            for (int it = 0; it < 2; ++it) {
-                const int item = tid + NT * it, tt = item >> 4, c8 = item & 15;
+            for (int ii = 0; ii < 2; ++ii) {
+                const int item = tid + NT * ii, tt = item >> 4, c8 = item & 15;
                 const float bt = ms.beta[tt];
                 float kf[8], vf[8], g8[8], o[8];
                 unpack8(*reinterpret_cast<const uint4*>(sm + OFF_K + tt * 256 + c8 * 16), kf);
@@ -751,8 +770,8 @@ __global__ void __launch_bounds__(NT, 1)
         // while it runs: Q Gamma -> LV_QG and K~ = K e^{G_last - G} -> the v-tile slot (both
         // MN-major [t][c]); neither region is read by this GEMM
 #pragma unroll
-        for (int it = 0; it < 2; ++it) {
-            const int item = tid + NT * it, t = item >> 4, c8 = item & 15;
+        for (int ii = 0; ii < 2; ++ii) {
+            const int item = tid + NT * ii, t = item >> 4, c8 = item & 15;
             float qf[8], kf[8], g8[8], gl[8], o[8];
             unpack8(*reinterpret_cast<const uint4*>(sm + OFF_Q + t * 256 + c8 * 16), qf);
             unpack8(*reinterpret_cast<const uint4*>(sm + OFF_K + t * 256 + c8 * 16), kf);
@@ -768,11 +787,11 @@ __global__ void __launch_bounds__(NT, 1)
         KDA_WAIT(bar_m0, ph0);
         if (failed) break;
         // q, k and the z slot are free: request the next chunk's q, k, z
-        if (tid == 0 && n + 1 < nchunks) {
+        if (tid == 0 && has_next) {
             tc::mbar_arrive_expect_tx(&ms.bar_qkz, 3u * 16384u);
-            tc::tma_load_3d(sm + OFF_Q, &tm_q, 0, t0 + C, (int)bh, &ms.bar_qkz);
-            tc::tma_load_3d(sm + OFF_K, &tm_k, 0, t0 + C, (int)bh, &ms.bar_qkz);
-            tc::tma_load_3d(sm + OFF_LVL + LV_Z, &tm_z, 0, t0 + C, (int)bh, &ms.bar_qkz);
+            tc::tma_load_3d(sm + OFF_Q, tm_q, 0, nt0, (int)nbh, &ms.bar_qkz);
+            tc::tma_load_3d(sm + OFF_K, tm_k, 0, nt0, (int)nbh, &ms.bar_qkz);
+            tc::tma_load_3d(sm + OFF_LVL + LV_Z, tm_z, 0, nt0, (int)nbh, &ms.bar_qkz);
         }
         {
             // parts 0-1: W^T row c, columns 32*part.. -> [W^T | .]; parts 2-3: U^T row v -> K-major
@@ -798,6 +817,16 @@ __global__ void __launch_bounds__(NT, 1)
         }
         KDA_SYNC_FOR_MMA();
         // ---------------------------------------------------------------- P5: Q'^T and U'^T
+        // (without a next item this fetches the current one again, unused)
+        const GatePre gp = gate_fetch(nbh, nt0 / C);
+        if (kSplit && tid == 0) {
+            // W^T, U^T and K~ are final: out while the next GEMM reads them too
+            tc::tma_store_3d(tm_wq, sm + OFF_A1, 0, 0, 2 * it);
+            tc::tma_store_3d(tm_uu, sm + OFF_LVL + LV_UT, 0, 0, 2 * it);
+            tc::tma_store_3d(tm_kt, sm + OFF_V, 0, 0, it);
+            tc::tma_store_3d(tm_kt, sm + OFF_V + 8192, 64, 0, it);
+            tc::bulk_commit();
+        }
         if (tid == 0) {
             // Q'^T = (Q Gamma)^T I - W^T M^T ;  U'^T = U^T M^T
 #pragma unroll
@@ -814,128 +843,169 @@ __global__ void __launch_bounds__(NT, 1)
         }
         KDA_WAIT(bar_m1, ph1);
         if (failed) break;
-        {
-            // Q'^T row c, columns 16*part.. -> [. | Q'^T];  S <- diag(Gamma_last) S in TMEM
-            // (this chunk's bf16 copy of S stays unscaled)
-            const int c = row;
+        // ---------------------------------------------------------------- S: operands out | next gate
+        if constexpr (kSplit) {
+            // Q'^T -> [. | Q'^T], U'^T -> staging (K-major [v][t]), Gamma_last -> global; then
+            // these two tiles go out by TMA (W^T, U^T and K~ left before the last GEMM) while
+            // every warp computes the next item's gate.
             {
-                uint32_t d[16];
+                uint32_t d[16], e[16];
                 tc::tmem_ld16(taddr(tmem, warp, TM_QP + 16 * part), d);
+                tc::tmem_ld16(taddr(tmem, warp, TM_UP + 16 * part), e);
                 tc::tmem_ld_wait();
                 float f[16];
 #pragma unroll
                 for (int j = 0; j < 16; ++j) f[j] = __uint_as_float(d[j]);
-                store16_mn(sm + OFF_A1, c, 64 + 16 * part, 16384, f);
-            }
-            const float gl = ex2(G2[63 * KD + gsw(c)]);
-            {
-                const int v0 = 32 * part;
-                uint32_t d0[16], d1[16];
-                tc::tmem_ld16(taddr(tmem, warp, TM_S + v0), d0);
-                tc::tmem_ld16(taddr(tmem, warp, TM_S + v0 + 16), d1);
-                tc::tmem_ld_wait();
+                store16_mn(sm + OFF_A1, row, 64 + 16 * part, 16384, f);
 #pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    d0[j] = __float_as_uint(__uint_as_float(d0[j]) * gl);
-                    d1[j] = __float_as_uint(__uint_as_float(d1[j]) * gl);
-                }
-                tc::tmem_st16(taddr(tmem, warp, TM_S + v0), d0);
-                tc::tmem_st16(taddr(tmem, warp, TM_S + v0 + 16), d1);
-            }
-            tc::tmem_st_wait();
-        }
-        KDA_SYNC_FOR_MMA();
-        // ---------------------------------------------------------------- C: carry | next gate
-        if (group_c) {
-            // C1: D[v][t'] = sum_c S[c][v] A1[c][t']  -> (W S)^T for t' < 64, (Q' S)^T above
-            if (tid == 0) {
-#pragma unroll
-                for (int ks = 0; ks < 8; ++ks)
-                    tc::mma_bf16(tmem + TM_D1, desc_mn(sb + OFF_S, 16384, ks),
-                                 desc_mn(sb + OFF_A1, 16384, ks), IDESC_SQ, ks > 0);
-                tc::mma_commit(&ms.bar_m0);
-            }
-            {
-                const bool ok = tid != 0 || tc::mbar_wait(&ms.bar_m0, ph0);
-                if (tc::named_sync_or(1, 256, !ok)) failed = true;
-                tc::fence_after_sync();
-            }
-            // C2: lane v, tokens 32*half..: Delta^T = U^T - (W S)^T -> K-major [v][t];
-            //     o[t][v] = scale ((Q' S)^T + U'^T) -> row-major staging [t][v]
-            const int half = warp >> 2, v = row;
-            if (!failed) {
-#pragma unroll 1
-                for (int tb = 32 * half; tb < 32 * half + 32; tb += 16) {
-                    uint32_t dw[16], du[16], dq[16], dp[16];
-                    tc::tmem_ld16(taddr(tmem, warp, TM_D1 + tb), dw);
-                    tc::tmem_ld16(taddr(tmem, warp, TM_U + tb), du);
-                    tc::tmem_ld16(taddr(tmem, warp, TM_D1 + 64 + tb), dq);
-                    tc::tmem_ld16(taddr(tmem, warp, TM_UP + tb), dp);
-                    tc::tmem_ld_wait();
-                    float f[16];
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) f[j] = __uint_as_float(du[j]) - __uint_as_float(dw[j]);
-                    store16_k(sm + OFF_LVL + LV_DELTA, v, tb, 128, f);
-                    __nv_bfloat16* ost = reinterpret_cast<__nv_bfloat16*>(sm + OFF_LVL + LV_OST);
-#pragma unroll
-                    for (int j = 0; j < 16; ++j)
-                        ost[(tb + j) * VD + v] =
-                            __float2bfloat16_rn(scale * (__uint_as_float(dq[j]) + __uint_as_float(dp[j])));
-                }
+                for (int j = 0; j < 16; ++j) f[j] = __uint_as_float(e[j]);
+                store16_k(sm + OFF_LVL + LV_UPS, row, 16 * part, 128, f);
+                if (part == 0) seg.gl[(size_t)it * KD + row] = ex2(G2[63 * KD + gsw(row)]);
             }
             tc::fence_proxy_async_smem();
             tc::fence_before_sync();
-            tc::named_sync(1, 256);
+            __syncthreads();
             tc::fence_after_sync();
-            // C3: S += K~^T Delta (K~ in the v-tile slot), while the staged o rows go out
-            if (tid == 0 && !failed) {
-#pragma unroll
-                for (int ks = 0; ks < 4; ++ks)
-                    tc::mma_bf16(tmem + TM_S, desc_mn(sb + OFF_V, 8192, ks),
-                                 desc_k(sb + OFF_LVL + LV_DELTA, 128, ks), IDESC_SK, 1u);
-                tc::mma_commit(&ms.bar_m1);
+            if (tid == 0) {
+                tc::tma_store_3d(tm_wq, sm + OFF_A1 + 16384, 0, 0, 2 * it + 1);
+                tc::tma_store_3d(tm_uu, sm + OFF_LVL + LV_UPS, 0, 0, 2 * it + 1);
+                tc::bulk_commit();
             }
-#pragma unroll
-            for (int it = 0; it < 4; ++it) {
-                const int q = tid + 256 * it, tr = q >> 4, c16 = q & 15;
-                if (tr < cn)
-                    *reinterpret_cast<uint4*>(out + (bh * T + t0 + tr) * VD + c16 * 8) =
-                        *reinterpret_cast<const uint4*>(sm + OFF_LVL + LV_OST + tr * 256 + c16 * 16);
+        // ---------------------------------------------------------------- S2: next gate
+            if (has_next && !gate_scan(nbh, nt0 / C, gp)) failed = true;
+        // ---------------------------------------------------------------- S3: drain stores
+            if (tid == 0) {
+                // the stores have read the v-tile slot, A1 and the staging: refill / reuse them
+                tc::bulk_wait_read_all();
+                if (has_next) {
+                    tc::mbar_arrive_expect_tx(&ms.bar_v, 16384u);
+                    tc::tma_load_3d(sm + OFF_V, tm_v, 0, nt0, (int)nbh, &ms.bar_v);
+                }
             }
+        } else {
             {
-                const bool ok = failed || tid != 0 || tc::mbar_wait(&ms.bar_m1, ph1);
-                if (tc::named_sync_or(1, 256, !ok)) failed = true;
-                tc::fence_after_sync();
-            }
-            // S (fp32, TMEM) -> bf16 operand [c][v]; this warp: v in 64*half..
-            if (!failed) {
+                // Q'^T row c, columns 16*part.. -> [. | Q'^T];  S <- diag(Gamma_last) S in TMEM
+                // (this chunk's bf16 copy of S stays unscaled)
                 const int c = row;
-#pragma unroll 1
-                for (int v0 = 64 * half; v0 < 64 * half + 64; v0 += 32) {
+                {
+                    uint32_t d[16];
+                    tc::tmem_ld16(taddr(tmem, warp, TM_QP + 16 * part), d);
+                    tc::tmem_ld_wait();
+                    float f[16];
+    #pragma unroll
+                    for (int j = 0; j < 16; ++j) f[j] = __uint_as_float(d[j]);
+                    store16_mn(sm + OFF_A1, c, 64 + 16 * part, 16384, f);
+                }
+                const float gl = ex2(G2[63 * KD + gsw(c)]);
+                {
+                    const int v0 = 32 * part;
                     uint32_t d0[16], d1[16];
                     tc::tmem_ld16(taddr(tmem, warp, TM_S + v0), d0);
                     tc::tmem_ld16(taddr(tmem, warp, TM_S + v0 + 16), d1);
                     tc::tmem_ld_wait();
-                    float f[16];
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) f[j] = __uint_as_float(d0[j]);
-                    store16_mn(sm + OFF_S, c, v0, 16384, f);
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) f[j] = __uint_as_float(d1[j]);
-                    store16_mn(sm + OFF_S, c, v0 + 16, 16384, f);
+    #pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        d0[j] = __float_as_uint(__uint_as_float(d0[j]) * gl);
+                        d1[j] = __float_as_uint(__uint_as_float(d1[j]) * gl);
+                    }
+                    tc::tmem_st16(taddr(tmem, warp, TM_S + v0), d0);
+                    tc::tmem_st16(taddr(tmem, warp, TM_S + v0 + 16), d1);
                 }
-                // K~ is consumed: request the next chunk's v tile into its slot
-                if (tid == 0 && n + 1 < nchunks) {
-                    tc::mbar_arrive_expect_tx(&ms.bar_v, 16384u);
-                    tc::tma_load_3d(sm + OFF_V, &tm_v, 0, t0 + C, (int)bh, &ms.bar_v);
-                }
+                tc::tmem_st_wait();
             }
-        } else if (n + 1 < nchunks) {
-            if (!gate_scan(n + 1)) failed = true;
+            KDA_SYNC_FOR_MMA();
+        // ---------------------------------------------------------------- C: carry | next gate
+            if (group_c) {
+                // C1: D[v][t'] = sum_c S[c][v] A1[c][t']  -> (W S)^T for t' < 64, (Q' S)^T above
+                if (tid == 0) {
+    #pragma unroll
+                    for (int ks = 0; ks < 8; ++ks)
+                        tc::mma_bf16(tmem + TM_D1, desc_mn(sb + OFF_S, 16384, ks),
+                                     desc_mn(sb + OFF_A1, 16384, ks), IDESC_SQ, ks > 0);
+                    tc::mma_commit(&ms.bar_m0);
+                }
+                {
+                    const bool ok = tid != 0 || tc::mbar_wait(&ms.bar_m0, ph0);
+                    if (tc::named_sync_or(1, 256, !ok)) failed = true;
+                    tc::fence_after_sync();
+                }
+                // C2: lane v, tokens 32*half..: Delta^T = U^T - (W S)^T -> K-major [v][t];
+                //     o[t][v] = scale ((Q' S)^T + U'^T) -> row-major staging [t][v]
+                const int half = warp >> 2, v = row;
+                if (!failed) {
+    #pragma unroll 1
+                    for (int tb = 32 * half; tb < 32 * half + 32; tb += 16) {
+                        uint32_t dw[16], du[16], dq[16], dp[16];
+                        tc::tmem_ld16(taddr(tmem, warp, TM_D1 + tb), dw);
+                        tc::tmem_ld16(taddr(tmem, warp, TM_U + tb), du);
+                        tc::tmem_ld16(taddr(tmem, warp, TM_D1 + 64 + tb), dq);
+                        tc::tmem_ld16(taddr(tmem, warp, TM_UP + tb), dp);
+                        tc::tmem_ld_wait();
+                        float f[16];
+    #pragma unroll
+                        for (int j = 0; j < 16; ++j) f[j] = __uint_as_float(du[j]) - __uint_as_float(dw[j]);
+                        store16_k(sm + OFF_LVL + LV_DELTA, v, tb, 128, f);
+                        __nv_bfloat16* ost = reinterpret_cast<__nv_bfloat16*>(sm + OFF_LVL + LV_OST);
+    #pragma unroll
+                        for (int j = 0; j < 16; ++j)
+                            ost[(tb + j) * VD + v] =
+                                __float2bfloat16_rn(scale * (__uint_as_float(dq[j]) + __uint_as_float(dp[j])));
+                    }
+                }
+                tc::fence_proxy_async_smem();
+                tc::fence_before_sync();
+                tc::named_sync(1, 256);
+                tc::fence_after_sync();
+                // C3: S += K~^T Delta (K~ in the v-tile slot), while the staged o rows go out
+                if (tid == 0 && !failed) {
+    #pragma unroll
+                    for (int ks = 0; ks < 4; ++ks)
+                        tc::mma_bf16(tmem + TM_S, desc_mn(sb + OFF_V, 8192, ks),
+                                     desc_k(sb + OFF_LVL + LV_DELTA, 128, ks), IDESC_SK, 1u);
+                    tc::mma_commit(&ms.bar_m1);
+                }
+    #pragma unroll
+                for (int r = 0; r < 4; ++r) {
+                    const int q = tid + 256 * r, tr = q >> 4, c16 = q & 15;
+                    if (tr < cn)
+                        *reinterpret_cast<uint4*>(out + (bh * T + t0 + tr) * VD + c16 * 8) =
+                            *reinterpret_cast<const uint4*>(sm + OFF_LVL + LV_OST + tr * 256 + c16 * 16);
+                }
+                {
+                    const bool ok = failed || tid != 0 || tc::mbar_wait(&ms.bar_m1, ph1);
+                    if (tc::named_sync_or(1, 256, !ok)) failed = true;
+                    tc::fence_after_sync();
+                }
+                // S (fp32, TMEM) -> bf16 operand [c][v]; this warp: v in 64*half..
+                if (!failed) {
+                    const int c = row;
+    #pragma unroll 1
+                    for (int v0 = 64 * half; v0 < 64 * half + 64; v0 += 32) {
+                        uint32_t d0[16], d1[16];
+                        tc::tmem_ld16(taddr(tmem, warp, TM_S + v0), d0);
+                        tc::tmem_ld16(taddr(tmem, warp, TM_S + v0 + 16), d1);
+                        tc::tmem_ld_wait();
+                        float f[16];
+    #pragma unroll
+                        for (int j = 0; j < 16; ++j) f[j] = __uint_as_float(d0[j]);
+                        store16_mn(sm + OFF_S, c, v0, 16384, f);
+    #pragma unroll
+                        for (int j = 0; j < 16; ++j) f[j] = __uint_as_float(d1[j]);
+                        store16_mn(sm + OFF_S, c, v0 + 16, 16384, f);
+                    }
+                    // K~ is consumed: request the next chunk's v tile into its slot
+                    if (tid == 0 && has_next) {
+                        tc::mbar_arrive_expect_tx(&ms.bar_v, 16384u);
+                        tc::tma_load_3d(sm + OFF_V, tm_v, 0, nt0, (int)nbh, &ms.bar_v);
+                    }
+                }
+            } else if (has_next) {
+                if (!gate_scan(nbh, nt0 / C, gp)) failed = true;
+            }
+            ph0 ^= 1u;  // C1's and C3's commits, waited by the carry group only
+            ph1 ^= 1u;
         }
-        ph0 ^= 1u;  // C1's and C3's commits, waited by the carry group only
-        ph1 ^= 1u;
-        if (n + 1 < nchunks) ph_qkz ^= 1u;
+        if (has_next) ph_qkz ^= 1u;
         tc::fence_proxy_async_smem();
         tc::fence_before_sync();
         if (__syncthreads_or(failed)) failed = true;
@@ -945,8 +1015,9 @@ __global__ void __launch_bounds__(NT, 1)
 #undef KDA_SYNC_FOR_MMA
 #undef KDA_LEVEL_MMA
 
-    if (!failed && hT) {
+    if (!kSplit && !failed && hT) {
         const int c = row;
+        const size_t bh = blockIdx.x;
 #pragma unroll
         for (int v0 = 32 * part; v0 < 32 * part + 32; v0 += 16) {
             uint32_t d[16];
@@ -967,9 +1038,41 @@ __global__ void __launch_bounds__(NT, 1)
         tc::mbar_wait(&ms.bar_qkz, ph_qkz, 200000000ull);
         tc::mbar_wait(&ms.bar_v, ph_v, 200000000ull);
     }
+    if (kSplit && tid == 0) tc::bulk_wait_all();
     tc::fence_before_sync();
     __syncthreads();
     if (warp == 0) tc::tmem_dealloc(tmem, 512);
+}
+
+}  // namespace
+
+__global__ void __launch_bounds__(NT, 1)
+    kda_chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
+                        const __grid_constant__ CUtensorMap tm_k,
+                        const __grid_constant__ CUtensorMap tm_v,
+                        const __grid_constant__ CUtensorMap tm_z, int H, int T,
+                        const __nv_bfloat16* __restrict__ beta, const float* __restrict__ A_log,
+                        const float* __restrict__ dt_bias, float scale,
+                        const float* __restrict__ h0, __nv_bfloat16* __restrict__ out,
+                        float* __restrict__ hT) {
+    chunk_loop<false>(&tm_q, &tm_k, &tm_v, &tm_z, nullptr, nullptr, nullptr, H, T, beta, A_log,
+                      dt_bias, scale, h0, out, hT, PrepSeg{0, 1, 0, nullptr});
+}
+
+// The chunk-parallel half of the split forward: every chunk of the segment is one work
+// item, independent of the state; CTAs take items gridDim.x apart.
+__global__ void __launch_bounds__(NT, 1)
+    kda_chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q,
+                          const __grid_constant__ CUtensorMap tm_k,
+                          const __grid_constant__ CUtensorMap tm_v,
+                          const __grid_constant__ CUtensorMap tm_z,
+                          const __grid_constant__ CUtensorMap tm_wq,
+                          const __grid_constant__ CUtensorMap tm_uu,
+                          const __grid_constant__ CUtensorMap tm_kt, int H, int T,
+                          const __nv_bfloat16* __restrict__ beta, const float* __restrict__ A_log,
+                          const float* __restrict__ dt_bias, PrepSeg seg) {
+    chunk_loop<true>(&tm_q, &tm_k, &tm_v, &tm_z, &tm_wq, &tm_uu, &tm_kt, H, T, beta, A_log,
+                     dt_bias, 0.f, nullptr, nullptr, nullptr, seg);
 }
 
 namespace {
@@ -993,19 +1096,41 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
-// 3-D view (channel, token, b*h) of a (B, H, T, 128) bf16 tensor; 64 x 128 tiles, no swizzle.
-bool make_tile_map(CUtensorMap* map, const void* base, int T, int BH) {
+// 3-D bf16 tile map: extents d0 (innermost) .. d2, row pitches s1 / s2 in bytes, box b0 x b1 x 1.
+bool make_map3(CUtensorMap* map, const void* base, cuuint64_t d0, cuuint64_t d1, cuuint64_t d2,
+               cuuint64_t s1, cuuint64_t s2, cuuint32_t b0, cuuint32_t b1, CUtensorMapSwizzle sw) {
     EncodeTiledFn enc = encode_fn();
     if (!enc) return false;
-    cuuint64_t dims[3] = {128, (cuuint64_t)T, (cuuint64_t)BH};
-    cuuint64_t strides[2] = {128 * 2, (cuuint64_t)T * 128 * 2};
-    cuuint32_t box[3] = {128, 64, 1};
+    cuuint64_t dims[3] = {d0, d1, d2};
+    cuuint64_t strides[2] = {s1, s2};
+    cuuint32_t box[3] = {b0, b1, 1};
     cuuint32_t estr[3] = {1, 1, 1};
     return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
-               box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-               CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
+
+// 3-D view (channel, token, b*h) of a (B, H, T, 128) bf16 tensor; 64 x 128 tiles, no swizzle.
+bool make_tile_map(CUtensorMap* map, const void* base, int T, int BH) {
+    return make_map3(map, base, 128, (cuuint64_t)T, (cuuint64_t)BH, 128 * 2, (cuuint64_t)T * 128 * 2,
+                     128, 64, CU_TENSOR_MAP_SWIZZLE_NONE);
+}
+
+bool make_input_maps(const ChunkArgs& a, CUtensorMap (&m)[4]) {
+    const int BH = a.B * a.H;
+    return make_tile_map(&m[0], a.q, a.T, BH) && make_tile_map(&m[1], a.k, a.T, BH) &&
+           make_tile_map(&m[2], a.v, a.T, BH) && make_tile_map(&m[3], a.z, a.T, BH);
+}
+
+int sm_count() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1)
+        return 1;
+    return n;
+}
+
+size_t round_up(size_t x, size_t m) { return (x + m - 1) / m * m; }
 
 }  // namespace
 
@@ -1043,24 +1168,121 @@ cudaError_t read_and_clear_timeout(cudaStream_t s, int* timed_out) {
     return e;
 }
 
-cudaError_t launch_chunk_tc(const ChunkArgs& a, cudaStream_t s, bool* taken) {
-    *taken = false;
-    if (a.io != KDA_BF16 || a.K != 128 || a.V != 128 || a.chunk != 64 || a.T <= 0) return cudaSuccess;
-    *taken = true;
-    const int BH = a.B * a.H;
-    CUtensorMap mq, mk, mv, mz;
-    if (!make_tile_map(&mq, a.q, a.T, BH) || !make_tile_map(&mk, a.k, a.T, BH) ||
-        !make_tile_map(&mv, a.v, a.T, BH) || !make_tile_map(&mz, a.z, a.T, BH))
+namespace {
+
+bool chunk_tc_eligible(const ChunkArgs& a) {
+    return a.io == KDA_BF16 && a.K == 128 && a.V == 128 && a.chunk == 64 && a.T > 0;
+}
+
+size_t split_scratch_bytes(const ChunkArgs& a, int seg_len) {
+    const size_t BH = (size_t)a.B * a.H;
+    return round_up(BH * seg_len * kItemBytes, 256) + (a.hT ? 0 : BH * KD * VD * sizeof(float));
+}
+
+// Chunks per segment of the split forward that fit in `bytes` of scratch (0: none fit).
+int split_segment_len(const ChunkArgs& a, size_t bytes) {
+    const int N = (a.T + C - 1) / C;
+    const size_t BH = (size_t)a.B * a.H;
+    const size_t state = a.hT ? 0 : BH * KD * VD * sizeof(float);
+    if (bytes < state) return 0;
+    const size_t per_chunk = BH * kItemBytes;
+    size_t len = (bytes - state) / per_chunk;
+    if (len > (size_t)N) len = N;
+    while (len > 0 && round_up(len * per_chunk, 256) + state > bytes) --len;
+    return (int)len;
+}
+
+// The split forward with caller-provided scratch: per segment of chunks, the prep kernel
+// (all chunks of all sequences in parallel) then the carry kernel (one CTA per sequence).
+cudaError_t run_chunk_split(const ChunkArgs& a, cudaStream_t s, void* scratch, size_t bytes) {
+    const int N = (a.T + C - 1) / C, BH = a.B * a.H;
+    const int seg_len = split_segment_len(a, bytes);
+    if (seg_len < 1) return cudaErrorMemoryAllocation;
+    const size_t items_max = (size_t)BH * seg_len;
+    uint8_t* p = static_cast<uint8_t*>(scratch);
+    uint8_t* wq = p;
+    uint8_t* uu = wq + items_max * kItemWQ;
+    uint8_t* kt = uu + items_max * kItemUU;
+    float* gl = reinterpret_cast<float*>(kt + items_max * kItemKT);
+    float* state = reinterpret_cast<float*>(p + round_up(items_max * kItemBytes, 256));
+    CUtensorMap m[4], mwq, muu, mkt;
+    if (!make_input_maps(a, m) ||
+        !make_map3(&mwq, wq, 64, 128, 2 * items_max, 128, 16384, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_map3(&muu, uu, 64, 128, 2 * items_max, 128, 16384, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_map3(&mkt, kt, 128, 64, items_max, 256, 16384, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
+    cudaError_t err = cudaFuncSetAttribute(kda_chunk_prep_kernel,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           (int)SMEM_BYTES);
+    if (err != cudaSuccess) return err;
+    float* h_state = a.hT ? a.hT : state;
+    const int nsm = sm_count();
+    for (int n0 = 0; n0 < N; n0 += seg_len) {
+        const int len = min(seg_len, N - n0), items = BH * len;
+        kda_chunk_prep_kernel<<<min(items, nsm), NT, SMEM_BYTES, s>>>(
+            m[0], m[1], m[2], m[3], mwq, muu, mkt, a.H, a.T, (const __nv_bfloat16*)a.beta, a.A_log,
+            a.dt_bias, PrepSeg{n0, len, items, gl});
+        count_launches(1);
+        if ((err = cudaGetLastError()) != cudaSuccess) return err;
+        err = launch_chunk_carry(mwq, muu, mkt, gl, BH, a.T, n0, len, a.scale,
+                                 n0 == 0 ? a.h0 : h_state, (__nv_bfloat16*)a.out, h_state, s);
+        if (err != cudaSuccess) return err;
+    }
+    return cudaSuccess;
+}
+
+// Scratch of the allocating split forward: at most this much per call (longer inputs are
+// processed in segments of chunks).
+constexpr size_t kSplitScratchCap = size_t(1) << 30;
+
+cudaError_t launch_chunk_split(const ChunkArgs& a, cudaStream_t s) {
+    const int seg_len = split_segment_len(a, kSplitScratchCap);
+    if (seg_len < 1) return cudaErrorMemoryAllocation;
+    const size_t bytes = split_scratch_bytes(a, seg_len);
+    void* p = nullptr;
+    if (cudaMallocAsync(&p, bytes, s) != cudaSuccess) {
+        cudaGetLastError();
+        return cudaErrorMemoryAllocation;
+    }
+    const cudaError_t err = run_chunk_split(a, s, p, bytes);
+    const cudaError_t ferr = cudaFreeAsync(p, s);
+    return err != cudaSuccess ? err : ferr;
+}
+
+cudaError_t launch_chunk_fused(const ChunkArgs& a, cudaStream_t s) {
+    const int BH = a.B * a.H;
+    CUtensorMap m[4];
+    if (!make_input_maps(a, m)) return cudaErrorInvalidValue;
     cudaError_t err = cudaFuncSetAttribute(kda_chunk_tc_kernel,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            (int)SMEM_BYTES);
     if (err != cudaSuccess) return err;
     kda_chunk_tc_kernel<<<BH, NT, SMEM_BYTES, s>>>(
-        mq, mk, mv, mz, a.H, a.T, (const __nv_bfloat16*)a.beta, a.A_log, a.dt_bias, a.scale, a.h0,
-        (__nv_bfloat16*)a.out, a.hT);
+        m[0], m[1], m[2], m[3], a.H, a.T, (const __nv_bfloat16*)a.beta, a.A_log, a.dt_bias, a.scale,
+        a.h0, (__nv_bfloat16*)a.out, a.hT);
     count_launches(1);
     return cudaGetLastError();
+}
+
+// Which tensor-core form is faster: the fused kernel runs ceil(BH / SMs) waves of whole
+// sequences, the split form spreads all chunks over the SMs and adds a short sequential
+// carry (about a tenth of a fused chunk step) per chunk.
+bool prefer_split(const ChunkArgs& a) {
+    const long long BH = (long long)a.B * a.H, N = (a.T + C - 1) / C, S = sm_count();
+    const long long fused = (BH + S - 1) / S * N * 10;
+    const long long split = (BH * N + S - 1) / S * 9 + (BH + S - 1) / S * N;
+    return split * 100 < fused * 85;
+}
+
+}  // namespace
+
+// mode 0: pick the faster form, 1: fused kernel, 2: split form.
+cudaError_t launch_chunk_tc(const ChunkArgs& a, cudaStream_t s, int mode, bool* taken) {
+    *taken = false;
+    if (!chunk_tc_eligible(a)) return cudaSuccess;
+    *taken = true;
+    const bool split = mode == 2 || (mode == 0 && prefer_split(a));
+    return split ? launch_chunk_split(a, s) : launch_chunk_fused(a, s);
 }
 
 }  // namespace kda

@@ -53,6 +53,8 @@ def load() -> ctypes.CDLL:
         dp = ctypes.POINTER(Dims)
         lib.kda_gate.argtypes = [dp, i, vp, vp, vp, i, vp, vp]
         lib.kda_chunk_forward.argtypes = [dp, i, vp, vp, vp, vp, vp, vp, vp, f, vp, i, vp, vp, vp]
+        lib.kda_chunk_forward_split.argtypes = lib.kda_chunk_forward.argtypes
+        lib.kda_chunk_forward_fused.argtypes = lib.kda_chunk_forward.argtypes
         lib.kda_recurrent_step.argtypes = [dp, i, vp, vp, vp, vp, vp, vp, vp, f, vp, vp, vp]
         lib.kda_fused_recurrent.argtypes = [dp, i, vp, vp, vp, vp, vp, vp, vp, f, vp, vp, vp]
         lib.kda_status_string.argtypes = [i]
@@ -130,12 +132,20 @@ def gate(z: torch.Tensor, A_log: torch.Tensor, dt_bias: torch.Tensor, chunk: int
     return out
 
 
+_CHUNK_FORMS = {"auto": "kda_chunk_forward", "split": "kda_chunk_forward_split",
+                "fused": "kda_chunk_forward_fused"}
+
+
 def chunk_forward(q, k, v, z, beta, A_log, dt_bias, scale: Optional[float] = None,
                   h0: Optional[torch.Tensor] = None, chunk: int = 64,
                   out: Optional[torch.Tensor] = None, hT: Optional[torch.Tensor] = None,
-                  output_final_state: bool = True, stream=None
+                  output_final_state: bool = True, stream=None, form: str = "auto"
                   ) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
-    """KDA forward over (B, H, T) tokens; returns (o, hT) with o in q's dtype, hT float32."""
+    """KDA forward over (B, H, T) tokens; returns (o, hT) with o in q's dtype, hT float32.
+
+    ``form`` selects the entry point: "auto" (kda_chunk_forward, which picks the faster
+    form), "split" (kda_chunk_forward_split) or "fused" (kda_chunk_forward_fused)."""
+    fn = _CHUNK_FORMS[form]
     B, H, T, K = q.shape
     V = v.shape[-1]
     if scale is None:
@@ -146,10 +156,10 @@ def chunk_forward(q, k, v, z, beta, A_log, dt_bias, scale: Optional[float] = Non
         hT = torch.empty(B, H, K, V, device=q.device, dtype=torch.float32)
     d = Dims(B, H, T, K, V)
     A32, dt32 = _f32(A_log), _f32(dt_bias)
-    st = load().kda_chunk_forward(ctypes.byref(d), _DTYPES[q.dtype], _ptr(q), _ptr(k), _ptr(v),
-                                  _ptr(z), _ptr(beta), _ptr(A32), _ptr(dt32), float(scale),
-                                  _ptr(h0), int(chunk), _ptr(out), _ptr(hT), _stream(stream))
-    _check("kda_chunk_forward", st)
+    st = getattr(load(), fn)(ctypes.byref(d), _DTYPES[q.dtype], _ptr(q), _ptr(k), _ptr(v),
+                             _ptr(z), _ptr(beta), _ptr(A32), _ptr(dt32), float(scale),
+                             _ptr(h0), int(chunk), _ptr(out), _ptr(hT), _stream(stream))
+    _check(fn, st)
     return out, hT
 
 

@@ -94,6 +94,35 @@ int kda_chunk_forward(const kda_dims* dims, kda_dtype io_dtype, const void* q, c
                       float* hT, kda_stream_t stream);
 
 /*
+ * kda_chunk_forward_split / kda_chunk_forward_fused -- kda_chunk_forward restricted to one of
+ * its two tensor-core forms (bf16 I/O, K = V = 128, chunk 64, T >= 1; anything else returns
+ * KDA_ERR_UNSUPPORTED).  kda_chunk_forward picks between them by the shape; these exist to
+ * run and compare each form on any shape.
+ *   fused : one CTA per (b, h) walks its chunks with the state on chip; the whole forward is
+ *           one kernel and reads each input once.
+ *   split : the chunk-parallel WY form of kda-adjoint-2026-10-01 section 2 as two kernels.  A
+ *           prep kernel spreads every chunk of every sequence over the GPU and writes, per
+ *           chunk, the state-independent operands ([W^T | Q'^T], [U^T | U'^T], K~ =
+ *           K e^{G_last - G} in bf16, Gamma_last in fp32: 82,432 bytes); a carry kernel then
+ *           walks the chunks of each sequence with the fp32 state on chip (S <- Gamma_last S
+ *           + K~^T (U - W S), o = scale (Q' S + U')).  Suited to few, long sequences, where
+ *           the fused form leaves most of the GPU idle.  The operands live in scratch that
+ *           the call allocates and frees on `stream` (cudaMallocAsync / cudaFreeAsync, at most
+ *           1 GiB: longer inputs run as consecutive segments of chunks); KDA_ERR_NO_MEMORY if
+ *           that allocation fails.
+ */
+int kda_chunk_forward_split(const kda_dims* dims, kda_dtype io_dtype, const void* q,
+                            const void* k, const void* v, const void* z, const void* beta,
+                            const float* A_log, const float* dt_bias, float scale,
+                            const float* h0, int chunk, void* out, float* hT,
+                            kda_stream_t stream);
+int kda_chunk_forward_fused(const kda_dims* dims, kda_dtype io_dtype, const void* q,
+                            const void* k, const void* v, const void* z, const void* beta,
+                            const float* A_log, const float* dt_bias, float scale,
+                            const float* h0, int chunk, void* out, float* hT,
+                            kda_stream_t stream);
+
+/*
  * kda_recurrent_step -- one decode token per (b, h): the step above applied
  * once, in place on `state` (B,H,K,V) float32.  dims->T must be 1; q, k, z are
  * (B,H,1,K), v and out (B,H,1,V), beta (B,H,1), all in io_dtype.

@@ -56,15 +56,15 @@ class Dims(ctypes.Structure):
                 ("K", ctypes.c_int), ("V", ctypes.c_int)]
 
 
-def _fwd(lib, dims, chunk=64, dtype=1, misalign=0, null_q=False):
+def _fwd(lib, dims, chunk=64, dtype=1, misalign=0, null_q=False, fn="kda_chunk_forward"):
     p = 1 << 20  # fake, never dereferenced: every call below is rejected on the host
     vp = ctypes.c_void_p
-    lib.kda_chunk_forward.argtypes = [ctypes.c_void_p, ctypes.c_int] + [vp] * 7 + \
+    f = getattr(lib, fn)
+    f.argtypes = [ctypes.c_void_p, ctypes.c_int] + [vp] * 7 + \
         [ctypes.c_float, vp, ctypes.c_int, vp, vp, vp]
     q = None if null_q else vp(p + misalign)
-    return lib.kda_chunk_forward(ctypes.byref(dims) if dims is not None else None, dtype, q,
-                                 vp(p), vp(p), vp(p), vp(p), vp(p), vp(p), 0.1, None, chunk,
-                                 vp(p), None, None)
+    return f(ctypes.byref(dims) if dims is not None else None, dtype, q,
+             vp(p), vp(p), vp(p), vp(p), vp(p), vp(p), 0.1, None, chunk, vp(p), None, None)
 
 
 def test_host_validation_rejects_bad_arguments(lib):
@@ -78,6 +78,19 @@ def test_host_validation_rejects_bad_arguments(lib):
     assert _fwd(lib, Dims(1, 1, 8, 128, 128), chunk=48) == -2 # chunk not in {16, 32, 64}
     assert _fwd(lib, Dims(1, 1, 8, 128, 128), misalign=2) == -3
     assert _fwd(lib, Dims(1, 1, 8, 128, 128), null_q=True) == -1
+
+
+@pytest.mark.parametrize("fn", ["kda_chunk_forward_split", "kda_chunk_forward_fused"])
+def test_tensor_core_forms_reject_other_shapes(lib, fn):
+    # each form exists for bf16, K = V = 128, chunk 64 and T >= 1 only; everything else is
+    # refused on the host (nothing is launched, so fake pointers are fine)
+    assert _fwd(lib, Dims(1, 1, 64, 128, 128), dtype=0, fn=fn) == -2  # fp32 I/O
+    assert _fwd(lib, Dims(1, 1, 64, 64, 128), fn=fn) == -2            # K = 64
+    assert _fwd(lib, Dims(1, 1, 64, 128, 64), fn=fn) == -2            # V = 64
+    assert _fwd(lib, Dims(1, 1, 64, 128, 128), chunk=32, fn=fn) == -2 # chunk 32
+    assert _fwd(lib, Dims(1, 1, 0, 128, 128), fn=fn) == -2            # T = 0
+    assert _fwd(lib, Dims(1, 1, 64, 128, 128), misalign=2, fn=fn) == -3
+    assert _fwd(lib, None, fn=fn) == -1
 
 
 def test_recurrent_step_requires_one_token(lib):

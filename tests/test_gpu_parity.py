@@ -37,11 +37,11 @@ def check(name, got, ref, dtype):
         assert diff.max() <= BF16_ABS, f"{name}: max abs {diff.max():.3e} > {BF16_ABS}"
 
 
-def run_and_compare(kda, inp, chunk=None, with_h0=True, want_hT=True, threads=4):
+def run_and_compare(kda, inp, chunk=None, with_h0=True, want_hT=True, threads=4, form="auto"):
     d = inp.to("cuda")
     h0 = d.h0 if with_h0 else None
     o, hT = kda.chunk_forward(d.q, d.k, d.v, d.z, d.beta, d.A_log, d.dt_bias, inp.scale, h0,
-                              chunk or inp.chunk, output_final_state=want_hT)
+                              chunk or inp.chunk, output_final_state=want_hT, form=form)
     torch.cuda.synchronize()
     o_ref, h_ref = oracle.forward(inp.q, inp.k, inp.v, inp.z, inp.beta, inp.A_log, inp.dt_bias,
                                   inp.scale, inp.h0 if with_h0 else None, threads=threads)
@@ -119,15 +119,18 @@ def test_empty_sequence_copies_state(kda):
 
 
 def test_resume_equals_whole(kda):
+    # the fused form on all three calls (the automatic choice depends on the length)
     inp = inputs.make(2, 2, 160, 128, 128, chunk=64, dtype="bf16", seed=9, h0_std=0.1)
     d = inp.to("cuda")
-    o, h = kda.chunk_forward(d.q, d.k, d.v, d.z, d.beta, d.A_log, d.dt_bias, inp.scale, d.h0, 64)
+    o, h = kda.chunk_forward(d.q, d.k, d.v, d.z, d.beta, d.A_log, d.dt_bias, inp.scale, d.h0, 64,
+                             form="fused")
     sl = lambda t, a, b: t[:, :, a:b].contiguous()
     o1, h1 = kda.chunk_forward(sl(d.q, 0, 64), sl(d.k, 0, 64), sl(d.v, 0, 64), sl(d.z, 0, 64),
-                               sl(d.beta, 0, 64), d.A_log, d.dt_bias, inp.scale, d.h0, 64)
+                               sl(d.beta, 0, 64), d.A_log, d.dt_bias, inp.scale, d.h0, 64,
+                               form="fused")
     o2, h2 = kda.chunk_forward(sl(d.q, 64, 160), sl(d.k, 64, 160), sl(d.v, 64, 160),
                                sl(d.z, 64, 160), sl(d.beta, 64, 160), d.A_log, d.dt_bias,
-                               inp.scale, h1, 64)
+                               inp.scale, h1, 64, form="fused")
     torch.cuda.synchronize()
     # same chunk boundaries => same arithmetic: bit-identical
     assert torch.equal(torch.cat([o1, o2], dim=2), o)
@@ -153,6 +156,54 @@ def test_scale_enters_only_the_read_on_gpu(kda):
     torch.testing.assert_close(o8, 0.125 * o1, rtol=1e-6, atol=1e-7)
 
 
+# ---------------------------------------------------------------- the two tensor-core forms
+@pytest.mark.parametrize("form", ["fused", "split"])
+@pytest.mark.parametrize("B,H,T,seed,A_log_value", [
+    (1, 1, 64, 21, None),               # a single chunk
+    (1, 2, 200, 22, None),              # ragged last chunk
+    (2, 3, 700, 23, math.log(16.0)),    # the strongest decay of the workloads' range
+    (1, 4, 1024, 24, None),             # sixteen chunks of carry
+])
+def test_tensor_core_forms_match_oracle(kda, form, B, H, T, seed, A_log_value):
+    inp = inputs.make(B, H, T, 128, 128, chunk=64, dtype="bf16", seed=seed, dt_std=0.1,
+                      h0_std=0.1, A_log_value=A_log_value)
+    run_and_compare(kda, inp, form=form)
+    assert kda.device_status() == 0
+
+
+def test_split_form_resume_equals_whole(kda):
+    # chunk-aligned cut: the carry kernel starts the second call from the fp32 state the
+    # first call left, which is the state the whole run carries at that chunk: bit-identical
+    inp = inputs.make(2, 2, 300, 128, 128, chunk=64, dtype="bf16", seed=25, h0_std=0.1)
+    d = inp.to("cuda")
+    f = lambda a, b, h0: kda.chunk_forward(*(t[:, :, a:b].contiguous() for t in
+                                             (d.q, d.k, d.v, d.z, d.beta)),
+                                           d.A_log, d.dt_bias, inp.scale, h0, 64, form="split")
+    o, h = f(0, 300, d.h0)
+    o1, h1 = f(0, 128, d.h0)
+    o2, h2 = f(128, 300, h1)
+    torch.cuda.synchronize()
+    assert torch.equal(torch.cat([o1, o2], dim=2), o)
+    assert torch.equal(h2, h)
+
+
+def test_split_form_run_twice_is_bitwise_identical(kda):
+    inp = inputs.make(3, 5, 333, 128, 128, chunk=64, dtype="bf16", seed=26, h0_std=0.1)
+    d = inp.to("cuda")
+    a = kda.chunk_forward(d.q, d.k, d.v, d.z, d.beta, d.A_log, d.dt_bias, inp.scale, d.h0, 64,
+                          form="split")
+    b = kda.chunk_forward(d.q, d.k, d.v, d.z, d.beta, d.A_log, d.dt_bias, inp.scale, d.h0, 64,
+                          form="split")
+    torch.cuda.synchronize()
+    assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+
+
+def test_split_form_without_final_state(kda):
+    # no hT: the carry keeps its state in the call's own scratch
+    inp = inputs.make(1, 3, 260, 128, 128, chunk=64, dtype="bf16", seed=27, h0_std=0.1)
+    run_and_compare(kda, inp, want_hT=False, form="split")
+
+
 # ---------------------------------------------------------------- full-size workloads, sampled
 def _sample_pairs(inp, pairs):
     """Gather (b, h) sequences into a (1, n, T, *) problem the oracle can run."""
@@ -164,18 +215,26 @@ def _sample_pairs(inp, pairs):
             inp.dt_bias[hs], h0)
 
 
+_SAMPLED_REF = {}
+
+
+@pytest.mark.parametrize("form", ["auto", "fused", "split"])
 @pytest.mark.parametrize("name,pairs", [
     ("prefill_bf16", [(0, 0), (3, 17), (7, 31)]),
     ("long_bf16", [(0, 5), (0, 30)]),
 ])
-def test_full_size_sampled(kda, name, pairs):
+def test_full_size_sampled(kda, name, pairs, form):
     inp = inputs.workload(name)
     d = inp.to("cuda")
     o, hT = kda.chunk_forward(d.q, d.k, d.v, d.z, d.beta, d.A_log, d.dt_bias, inp.scale, d.h0,
-                              inp.chunk)
+                              inp.chunk, form=form)
     torch.cuda.synchronize()
-    q, k, v, z, beta, A, dt, h0 = _sample_pairs(inp, pairs)
-    o_ref, h_ref = oracle.forward(q, k, v, z, beta, A, dt, inp.scale, h0, threads=len(pairs))
+    assert kda.device_status() == 0
+    if name not in _SAMPLED_REF:  # the oracle runs once per workload, for all three forms
+        q, k, v, z, beta, A, dt, h0 = _sample_pairs(inp, pairs)
+        _SAMPLED_REF[name] = oracle.forward(q, k, v, z, beta, A, dt, inp.scale, h0,
+                                            threads=len(pairs))
+    o_ref, h_ref = _SAMPLED_REF[name]
     bs = [p[0] for p in pairs]
     hs = [p[1] for p in pairs]
     check(f"{name} o", o[bs, hs].unsqueeze(0), o_ref, "bf16")
