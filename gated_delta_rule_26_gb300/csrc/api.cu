@@ -10,6 +10,7 @@
 namespace kda {
 cudaError_t launch_chunk_tc(const ChunkArgs& a, cudaStream_t s, int mode, bool* taken);
 cudaError_t read_and_clear_carry_timeout(int* timed_out);
+cudaError_t launch_chunk_split_noalloc(const ChunkArgs& a, cudaStream_t s, bool* fits);
 cudaError_t launch_bounded_wait_selftest(unsigned long long limit_ns, cudaStream_t s);
 cudaError_t read_and_clear_timeout(cudaStream_t s, int* timed_out);
 }
@@ -157,6 +158,27 @@ int kda_chunk_forward_fused(const kda_dims* dims, kda_dtype io_dtype, const void
                             kda_stream_t stream) {
     return chunk_forward(1, dims, io_dtype, q, k, v, z, beta, A_log, dt_bias, scale, h0, chunk,
                          out, hT, stream);
+}
+
+int kda_chunk_forward_split_noalloc(const kda_dims* dims, kda_dtype io_dtype, const void* q,
+                                    const void* k, const void* v, const void* z,
+                                    const void* beta, const float* A_log, const float* dt_bias,
+                                    float scale, const float* h0, int chunk, void* out,
+                                    float* hT, kda_stream_t stream) {
+    int st = check_dims(dims, true);
+    if (st) return st;
+    if (!dtype_ok(io_dtype)) return KDA_ERR_INVALID_ARG;
+    if (chunk != 16 && chunk != 32 && chunk != 64) return KDA_ERR_UNSUPPORTED;
+    if (dims->T == 0) return KDA_ERR_UNSUPPORTED;
+    st = check_ptrs({q, k, v, z, out}, {h0, hT}, {beta}, io_bytes(io_dtype));
+    if (!st) st = check_ptrs({}, {}, {A_log, dt_bias}, 4);
+    if (st) return st;
+    kda::ChunkArgs a{dims->B, dims->H, dims->T, dims->K, dims->V, chunk, io_dtype, q, k, v, z,
+                     beta, A_log, dt_bias, h0, scale, out, hT};
+    bool fits = false;
+    const cudaError_t e = kda::launch_chunk_split_noalloc(a, (cudaStream_t)stream, &fits);
+    if (!fits) return KDA_ERR_UNSUPPORTED;
+    return from_cuda(e);
 }
 
 int kda_fused_recurrent(const kda_dims* dims, kda_dtype io_dtype, const void* q, const void* k,

@@ -45,6 +45,8 @@
 #include <cuda.h>
 #include <stddef.h>
 
+#include <mutex>
+
 #include "chunk_tiles.cuh"
 #include "common.cuh"
 #include "tc_ptx.cuh"
@@ -1275,6 +1277,57 @@ bool prefer_split(const ChunkArgs& a) {
 }
 
 }  // namespace
+
+// ---- the split form without allocation (kda_chunk_forward_split_noalloc)
+//
+// Some callers cannot allocate device memory while they run this forward: a serving loop
+// whose memory is carved up up front, code running where an allocation could stall or
+// fail at the wrong moment.  For them the split form's per-chunk operands go to one fixed
+// array in device memory instead of cudaMallocAsync scratch.  Every GPU that loads this
+// library reserves the array until the process exits, so it is kept modest; inputs longer
+// than it holds are processed in consecutive segments of chunks, and only the number of
+// sequences B * H is bounded (see kda_chunk_forward_split_noalloc in kda.h).
+constexpr size_t kNoAllocScratchBytes = size_t(64) << 20;
+static __device__ __align__(256) uint8_t g_kda_noalloc_scratch[kNoAllocScratchBytes];
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+// Device address of the array on the current device.  Host code cannot use the array's name
+// as an address, so it is looked up with cudaGetSymbolAddress, once per device, on the first
+// call made with that device current.
+cudaError_t noalloc_scratch(void** p) {
+    static std::mutex mu;
+    static void* addr[kMaxDevices] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!addr[dev]) {
+        void* q = nullptr;
+        e = cudaGetSymbolAddress(&q, g_kda_noalloc_scratch);
+        if (e != cudaSuccess) return e;
+        addr[dev] = q;
+    }
+    *p = addr[dev];
+    return cudaSuccess;
+}
+
+}  // namespace
+
+// The split form on the fixed array.  *fits = false (nothing launched) when one segment of a
+// chunk per sequence does not fit in it.  Nothing in the array needs clearing: every byte a
+// call reads was written earlier by the same call.
+cudaError_t launch_chunk_split_noalloc(const ChunkArgs& a, cudaStream_t s, bool* fits) {
+    *fits = chunk_tc_eligible(a) && split_segment_len(a, kNoAllocScratchBytes) >= 1;
+    if (!*fits) return cudaSuccess;
+    void* p = nullptr;
+    const cudaError_t e = noalloc_scratch(&p);
+    if (e != cudaSuccess) return e;
+    return run_chunk_split(a, s, p, kNoAllocScratchBytes);
+}
 
 // mode 0: pick the faster form, 1: fused kernel, 2: split form.
 cudaError_t launch_chunk_tc(const ChunkArgs& a, cudaStream_t s, int mode, bool* taken) {

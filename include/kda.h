@@ -123,6 +123,30 @@ int kda_chunk_forward_fused(const kda_dims* dims, kda_dtype io_dtype, const void
                             kda_stream_t stream);
 
 /*
+ * kda_chunk_forward_split_noalloc -- kda_chunk_forward_split for callers that cannot allocate
+ * device memory during the call (memory budgeted up front by a serving runtime, code where an
+ * allocation may stall or fail at the wrong moment).  The pages this library follows have no
+ * counterpart: it is the same computation, with the per-chunk operands kept in one fixed
+ * array of 64 MiB that every GPU loading the library reserves until the process exits.  The
+ * call makes no cudaMalloc / cudaMallocAsync / cudaFree call of its own.
+ *   Limit: one chunk of every sequence must fit, i.e. B*H*82,432 bytes, plus B*H*65,536 when
+ *   hT is NULL (the carried state then lives in the array too), at most 64 MiB: B*H <= 814
+ *   with hT, B*H <= 453 without.  Larger B*H returns KDA_ERR_UNSUPPORTED and launches
+ *   nothing.  Any T: longer inputs run as consecutive segments of chunks.
+ *   Shapes as kda_chunk_forward_split (bf16, K = V = 128, chunk 64, T >= 1).
+ *   The first call on each device looks up the array's device address (cudaGetSymbolAddress
+ *   with that device current); make that first call before any stream capture.
+ *   All calls share the array and it keeps the last call's contents; nothing needs clearing
+ *   (every byte a call reads, the same call wrote first).  Calls that overlap on the GPU
+ *   (other streams, other host threads) race on it: serialise them.
+ */
+int kda_chunk_forward_split_noalloc(const kda_dims* dims, kda_dtype io_dtype, const void* q,
+                                    const void* k, const void* v, const void* z,
+                                    const void* beta, const float* A_log, const float* dt_bias,
+                                    float scale, const float* h0, int chunk, void* out,
+                                    float* hT, kda_stream_t stream);
+
+/*
  * kda_recurrent_step -- one decode token per (b, h): the step above applied
  * once, in place on `state` (B,H,K,V) float32.  dims->T must be 1; q, k, z are
  * (B,H,1,K), v and out (B,H,1,V), beta (B,H,1), all in io_dtype.
