@@ -245,7 +245,7 @@ def run_long(args, kda, inputs, peaks, ws, barrier):
     entry point, which takes the split form here; reported under "long"."""
     import torch
     stream = torch.cuda.current_stream()
-    inp = inputs.workload("long_bf16")
+    inp = inputs.workload("long_bf16", **({"T": args.long_T} if args.long_T else {}))
     B, H, T, K, V, C = inp.B, inp.H, inp.T, inp.K, inp.V, inp.chunk
     d = inp.to("cuda")
     out = torch.empty(B, H, T, V, device="cuda", dtype=torch.bfloat16)
@@ -295,6 +295,9 @@ def main():
                     help="decode batch B (default: the decode workload's 256)")
     ap.add_argument("--long-steps", type=int, default=5,
                     help="timed steps of the long-sequence workload")
+    ap.add_argument("--long-T", type=int, default=None,
+                    help="sequence length of the long-sequence workload (default 65536; smaller "
+                         "for profiler captures)")
     ap.add_argument("--only", default="all", choices=["all", "prefill", "decode", "long"],
                     help="time only one of the two workloads (for profiler captures)")
     ap.add_argument("--prefill-T", type=int, default=None,

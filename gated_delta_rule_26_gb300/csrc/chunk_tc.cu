@@ -77,8 +77,6 @@ constexpr uint32_t LV_L1 = 32768;   // level operand buffer 1 (32 KB)        P3
 constexpr uint32_t LV_AF = 0;       // A fp32 [t][i] (16 KB, swizzled)       P3-P4
 constexpr uint32_t LV_MB = 16384;   // M bf16 K-major [t][i] (8 KB)          P3-P5
 constexpr uint32_t LV_TB = 24576;   // T bf16 K-major [t][i] (8 KB)          P4-P5
-constexpr uint32_t LV_BKG = 32768;  // beta K Gamma, MN-major [t][c]         P3-P5
-constexpr uint32_t LV_BV = 49152;   // beta V, MN-major [t][v]               P3-P5
 constexpr uint32_t LV_QG = 0;       // Q Gamma, MN-major [t][c] (16 KB)      P5
 constexpr uint32_t LV_UT = 32768;   // U^T K-major [v][i] (16 KB)            P5
 constexpr uint32_t LV_Z = 49152;    // z tile of the NEXT chunk (16 KB)      P5-P2
@@ -86,6 +84,9 @@ constexpr uint32_t LV_DELTA = 16384;// Delta^T K-major [v][t] (16 KB)        C2-
 constexpr uint32_t LV_OST = 0;      // o staging, row-major [t][v] bf16      C2
 constexpr uint32_t LV_UPS = 0;      // prep kernel: U'^T staging, K-major [v][t] (16 KB)
 // K~ (K e^{G_last - G}, MN-major [t][c]) lives in the v-tile slot OFF_V from P5 to C3.
+// beta K Gamma and beta V (MN-major [t][.], 16 KB each) live in the A1 slot from P3 until
+// the W/U GEMM has read them; then A1 takes [W^T | Q'^T].
+constexpr uint32_t OFF_BKG = OFF_A1, OFF_BV = OFF_A1 + 16384;
 
 struct Misc {
     alignas(16) float dt[KD];      // read as float4
@@ -396,13 +397,18 @@ __device__ __forceinline__ void chunk_loop(const CUtensorMap* tm_q, const CUtens
         __syncthreads();                                                 \
         tc::fence_after_sync();                                          \
     } while (0)
-#define KDA_LEVEL_MMA(buf, col, bar)                                     \
+// The GEMMs of two levels (one operand buffer each), one commit for both.
+#define KDA_LEVEL_MMA2(bufA, colA, bufB, colB, bar)                      \
     do {                                                                 \
         if (tid == 0) {                                                  \
-            const uint32_t L_ = sb + OFF_LVL + (buf);                    \
+            const uint32_t La_ = sb + OFF_LVL + (bufA);                  \
+            const uint32_t Lb_ = sb + OFF_LVL + (bufB);                  \
             _Pragma("unroll") for (int ks = 0; ks < 8; ++ks)             \
-                tc::mma_bf16(tmem + (col), desc_k(L_, 128, ks),          \
-                             desc_k(L_, 128, ks), IDESC_LVL, ks > 0);    \
+                tc::mma_bf16(tmem + (colA), desc_k(La_, 128, ks),        \
+                             desc_k(La_, 128, ks), IDESC_LVL, ks > 0);   \
+            _Pragma("unroll") for (int ks = 0; ks < 8; ++ks)             \
+                tc::mma_bf16(tmem + (colB), desc_k(Lb_, 128, ks),        \
+                             desc_k(Lb_, 128, ks), IDESC_LVL, ks > 0);   \
             tc::mma_commit(&ms.bar);                                     \
         }                                                                \
     } while (0)
@@ -420,29 +426,14 @@ __device__ __forceinline__ void chunk_loop(const CUtensorMap* tm_q, const CUtens
             tc::tma_prefetch_l2_3d(tm_k, 0, nt0, (int)nbh);
             tc::tma_prefetch_l2_3d(tm_v, 0, nt0, (int)nbh);
         }
-        // ---------------------------------------------------------------- P3: level 32
-        // one level per buffer, so each level's GEMM overlaps the next level's build
+        // ---------------------------------------------------------------- P3: levels 32, 16
+        // two levels per pass, one buffer each; their GEMMs run under the 4-token blocks
         LevelItems items;
         load_level_items(sm, tid, items);
         build_level(sm, 0, LV_L0, tid, items);
-        KDA_SYNC_FOR_MMA();
-        KDA_LEVEL_MMA(LV_L0, TM_LVL, bar_m0);
-        // ---------------------------------------------------------------- P3: level 16
         build_level(sm, 1, LV_L1, tid, items);
         KDA_SYNC_FOR_MMA();
-        KDA_LEVEL_MMA(LV_L1, TM_LVL + 64, bar_m1);
-        // ---------------------------------------------------------------- P3: level 8
-        KDA_WAIT(bar_m0, ph0);
-        if (failed) break;
-        build_level(sm, 2, LV_L0, tid, items);
-        KDA_SYNC_FOR_MMA();
-        KDA_LEVEL_MMA(LV_L0, TM_LVL + 128, bar_m0);
-        // ---------------------------------------------------------------- P3: level 4
-        KDA_WAIT(bar_m1, ph1);
-        if (failed) break;
-        build_level(sm, 3, LV_L1, tid, items);
-        KDA_SYNC_FOR_MMA();
-        KDA_LEVEL_MMA(LV_L1, TM_LVL + 192, bar_m1);
+        KDA_LEVEL_MMA2(LV_L0, TM_LVL, LV_L1, TM_LVL + 64, bar_m0);
         // ---------------------------------------------------------------- P3: 4-token blocks
         // pairs inside 4-token blocks: exact pairwise decay, CUDA cores.
         // warp w = 4-token block w; lane = channels 4*lane..4*lane+3.
@@ -501,12 +492,34 @@ __device__ __forceinline__ void chunk_loop(const CUtensorMap* tm_q, const CUtens
         {
             const bool okv = tid != 0 || tc::mbar_wait(&ms.bar_v, ph_v);
             const bool ok0 = tid != 0 || tc::mbar_wait(&ms.bar_m0, ph0);
-            const bool ok1 = tid != 0 || tc::mbar_wait(&ms.bar_m1, ph1);
-            ph_v ^= 1u; ph0 ^= 1u; ph1 ^= 1u;
-            if (__syncthreads_or(!(okv && ok0 && ok1))) failed = true;
+            ph_v ^= 1u; ph0 ^= 1u;
+            if (__syncthreads_or(!(okv && ok0))) failed = true;
             tc::fence_after_sync();
             if (failed) break;
         }
+        // ---------------------------------------------------------------- P3: levels 8, 4
+        build_level(sm, 2, LV_L0, tid, items);
+        build_level(sm, 3, LV_L1, tid, items);
+        KDA_SYNC_FOR_MMA();
+        KDA_LEVEL_MMA2(LV_L0, TM_LVL + 128, LV_L1, TM_LVL + 192, bar_m1);
+        // while they run: beta K Gamma and beta V as MN-major [t][.] operands in the A1 slot
+#pragma unroll
+        for (int ii = 0; ii < 2; ++ii) {
+            const int item = tid + NT * ii, tt = item >> 4, c8 = item & 15;
+            const float bt = ms.beta[tt];
+            float kf[8], vf[8], g8[8], o[8];
+            unpack8(*reinterpret_cast<const uint4*>(sm + OFF_K + tt * 256 + c8 * 16), kf);
+            unpack8(*reinterpret_cast<const uint4*>(sm + OFF_V + tt * 256 + c8 * 16), vf);
+            load8g(G2, tt, c8, g8);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) o[j] = bt * kf[j] * ex2(g8[j]);
+            *reinterpret_cast<uint4*>(sm + OFF_BKG + mnmaj_off(tt, c8 * 8, 8192)) = pack8(o);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) o[j] = bt * vf[j];
+            *reinterpret_cast<uint4*>(sm + OFF_BV + mnmaj_off(tt, c8 * 8, 8192)) = pack8(o);
+        }
+        KDA_WAIT(bar_m1, ph1);
+        if (failed) break;
         // ---------------------------------------------------------------- P3 epilogue
         {
             // TMEM lane `row`: rows 0..63 are A rows (k side), rows 64..127 are M rows (q side);
@@ -561,22 +574,6 @@ __device__ __forceinline__ void chunk_loop(const CUtensorMap* tm_q, const CUtens
                         make_float4(o16[j], o16[j + 1], o16[j + 2], o16[j + 3]);
             } else {
                 store16_k(sm + OFF_LVL + LV_MB, t, i0, 64, o16);
-            }
-            // beta K Gamma and beta V as MN-major [t][.] operands
-#pragma unroll
-            for (int ii = 0; ii < 2; ++ii) {
-                const int item = tid + NT * ii, tt = item >> 4, c8 = item & 15;
-                const float bt = ms.beta[tt];
-                float kf[8], vf[8], g8[8], o[8];
-                unpack8(*reinterpret_cast<const uint4*>(sm + OFF_K + tt * 256 + c8 * 16), kf);
-                unpack8(*reinterpret_cast<const uint4*>(sm + OFF_V + tt * 256 + c8 * 16), vf);
-                load8g(G2, tt, c8, g8);
-#pragma unroll
-                for (int j = 0; j < 8; ++j) o[j] = bt * kf[j] * ex2(g8[j]);
-                *reinterpret_cast<uint4*>(sm + OFF_LVL + LV_BKG + mnmaj_off(tt, c8 * 8, 8192)) = pack8(o);
-#pragma unroll
-                for (int j = 0; j < 8; ++j) o[j] = bt * vf[j];
-                *reinterpret_cast<uint4*>(sm + OFF_LVL + LV_BV + mnmaj_off(tt, c8 * 8, 8192)) = pack8(o);
             }
         }
         tc::fence_before_sync();
@@ -764,8 +761,8 @@ __device__ __forceinline__ void chunk_loop(const CUtensorMap* tm_q, const CUtens
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks) {
                 const uint64_t b = desc_k(sb + OFF_LVL + LV_TB, 64, ks);
-                tc::mma_bf16(tmem + TM_W, desc_mn(sb + OFF_LVL + LV_BKG, 8192, ks), b, IDESC_WU, ks > 0);
-                tc::mma_bf16(tmem + TM_U, desc_mn(sb + OFF_LVL + LV_BV, 8192, ks), b, IDESC_WU, ks > 0);
+                tc::mma_bf16(tmem + TM_W, desc_mn(sb + OFF_BKG, 8192, ks), b, IDESC_WU, ks > 0);
+                tc::mma_bf16(tmem + TM_U, desc_mn(sb + OFF_BV, 8192, ks), b, IDESC_WU, ks > 0);
             }
             tc::mma_commit(&ms.bar_m0);
         }
@@ -1015,7 +1012,7 @@ __device__ __forceinline__ void chunk_loop(const CUtensorMap* tm_q, const CUtens
     }
 #undef KDA_WAIT
 #undef KDA_SYNC_FOR_MMA
-#undef KDA_LEVEL_MMA
+#undef KDA_LEVEL_MMA2
 
     if (!kSplit && !failed && hT) {
         const int c = row;
