@@ -72,8 +72,8 @@ constexpr uint32_t OFF_S = OFF_A1 + 32768;      // 32 KB S bf16, MN-major [c][v]
 constexpr uint32_t OFF_ID = OFF_S + 32768;      // 8 KB 64 x 64 identity, K-major bf16
 constexpr uint32_t OFF_MISC = OFF_ID + 8192;
 // multi-use region, in order of use within a chunk
-constexpr uint32_t LV_L0 = 0;       // level operand buffer 0 (32 KB)        P3
-constexpr uint32_t LV_L1 = 32768;   // level operand buffer 1 (32 KB)        P3
+constexpr uint32_t LV_PA = 0;       // level pair A operand, K-major 128 rows (32 KB)   P3
+constexpr uint32_t LV_PB = 32768;   // level pair B operand, K-major 64 rows (16 KB)    P3
 constexpr uint32_t LV_AF = 0;       // A fp32 [t][i] (16 KB, swizzled)       P3-P4
 constexpr uint32_t LV_MB = 16384;   // M bf16 K-major [t][i] (8 KB)          P3-P5
 constexpr uint32_t LV_TB = 24576;   // T bf16 K-major [t][i] (8 KB)          P4-P5
@@ -104,7 +104,7 @@ constexpr uint32_t SMEM_BYTES = OFF_MISC + sizeof(Misc) + 1024;
 
 // ---- TMEM columns (512 allocated)
 constexpr uint32_t TM_S = 0;      // fp32 state, lanes = key channel c, cols = v   (128)
-constexpr uint32_t TM_LVL = 128;  // four level score tiles                        (4 x 64)
+constexpr uint32_t TM_LVL = 128;  // two level-pair score tiles                    (2 x 64)
 constexpr uint32_t TM_QP = 128;   // Q'^T = (Q Gamma)^T - W^T M^T                  (64)
 constexpr uint32_t TM_UP = 192;   // U'^T = U^T M^T                                (64)
 constexpr uint32_t TM_D1 = 256;   // S^T [W^T | Q'^T]                              (128)
@@ -153,20 +153,29 @@ __device__ __forceinline__ void load_level_items(const uint8_t* sm, int tid, Lev
     }
 }
 
-// Build one level's operand in `buf`: rows 0..63 hold k_t scaled to the level's
-// reference, rows 64..127 hold q_t scaled (upper-half tokens only).  G2 is the in-chunk
-// cumulative log decay in log2 units, so every factor is one ex2 of a difference <= 0.
-__device__ __forceinline__ void build_level(uint8_t* sm, int li, uint32_t buf, int tid,
-                                            const LevelItems& it) {
+// Level li (half-width h = 32 >> li) splits every 2h-block of tokens into a lower and an
+// upper half; a token's rank among the 32 tokens of its half is its index with bit log2(h)
+// removed.  Two levels share one GEMM: the A operand (128 rows) holds, per level slot
+// (li & 1), the upper-half k_t (rows 64 slot + rank) and q_t (rows 64 slot + 32 + rank) scaled
+// by e^{G_t - G_r}; the B operand (64 rows) holds the lower-half k_i (rows 32 slot + rank)
+// scaled by e^{G_r - G_i}, r the last token of the lower half.  Both factors are <= 1.  The
+// product's diagonal 64 x 32 blocks are the two levels' scores; G2 is in log2 units, so every
+// factor is one ex2 of a difference <= 0.
+__device__ __forceinline__ int level_rank(int t, int s) {
+    return ((t >> (s + 1)) << s) | (t & ((1 << s) - 1));
+}
+__device__ __forceinline__ void build_level(uint8_t* sm, int li, int tid, const LevelItems& it) {
     const float* G2 = reinterpret_cast<const float*>(sm + OFF_G);
     const int c8 = tid & 15;
-    const int h = 32 >> li;
-    uint8_t* L = sm + OFF_LVL + buf;
+    const int s = 5 - li, h = 1 << s, slot = li & 1;
+    uint8_t* A = sm + OFF_LVL + LV_PA;
+    uint8_t* Bop = sm + OFF_LVL + LV_PB;
 #pragma unroll
     for (int r = 0; r < 2; ++r) {
         const int t = (tid >> 4) + 32 * r;
         const int ref = (t & ~(2 * h - 1)) + h - 1;
         const bool upper = (t & h) != 0;
+        const int rank = level_rank(t, s);
         float kf[8], qf[8], r8[8], f[8], kv[8], qv[8];
         unpack8(it.k[r], kf);
         load8g(G2, ref, c8, r8);
@@ -175,12 +184,14 @@ __device__ __forceinline__ void build_level(uint8_t* sm, int li, uint32_t buf, i
             f[j] = ex2(upper ? it.g[r][j] - r8[j] : r8[j] - it.g[r][j]);
             kv[j] = kf[j] * f[j];
         }
-        *reinterpret_cast<uint4*>(L + kmaj_off(t, c8 * 8, 128)) = pack8(kv);
         if (upper) {
+            *reinterpret_cast<uint4*>(A + kmaj_off(64 * slot + rank, c8 * 8, 128)) = pack8(kv);
             unpack8(it.q[r], qf);
 #pragma unroll
             for (int j = 0; j < 8; ++j) qv[j] = qf[j] * f[j];
-            *reinterpret_cast<uint4*>(L + kmaj_off(64 + t, c8 * 8, 128)) = pack8(qv);
+            *reinterpret_cast<uint4*>(A + kmaj_off(64 * slot + 32 + rank, c8 * 8, 128)) = pack8(qv);
+        } else {
+            *reinterpret_cast<uint4*>(Bop + kmaj_off(32 * slot + rank, c8 * 8, 64)) = pack8(kv);
         }
     }
 }
@@ -342,7 +353,9 @@ __device__ __forceinline__ void chunk_loop(const CUtensorMap* tm_q, const CUtens
         const int c4 = lane * 4;
         const float4 dt = kSplit ? gp.dt : *reinterpret_cast<const float4*>(&ms.dt[c4]);
         const float mult = -(kSplit ? expf(gp.A_log_h) : exp_A) * LOG2E;
-        float acc0 = 0.f, acc1 = 0.f, acc2 = 0.f, acc3 = 0.f;
+        // this warp's TPW tokens: running sums in registers; only the warp totals are exchanged
+        float4 acc[TPW];
+        float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
 #pragma unroll
         for (int a = 0; a < TPW; ++a) {
             const int t = TPW * wg + a;
@@ -350,12 +363,14 @@ __device__ __forceinline__ void chunk_loop(const CUtensorMap* tm_q, const CUtens
             const float x0 = bf_lo(zr.x) + dt.x, x1 = bf_hi(zr.x) + dt.y;
             const float x2 = bf_lo(zr.y) + dt.z, x3 = bf_hi(zr.y) + dt.w;
             const float m = (t < cnn) ? mult : 0.f;
-            acc0 = fmaf(m, softplus_fast(x0), acc0);
-            acc1 = fmaf(m, softplus_fast(x1), acc1);
-            acc2 = fmaf(m, softplus_fast(x2), acc2);
-            acc3 = fmaf(m, softplus_fast(x3), acc3);
-            *reinterpret_cast<float4*>(G2 + t * KD + g4off(lane)) = make_float4(acc0, acc1, acc2, acc3);
+            a0 = fmaf(m, softplus_fast(x0), a0);
+            a1 = fmaf(m, softplus_fast(x1), a1);
+            a2 = fmaf(m, softplus_fast(x2), a2);
+            a3 = fmaf(m, softplus_fast(x3), a3);
+            acc[a] = make_float4(a0, a1, a2, a3);
         }
+        // the warp total goes to its last row for the later warps to read
+        *reinterpret_cast<float4*>(G2 + (TPW * wg + TPW - 1) * KD + g4off(lane)) = acc[TPW - 1];
         tc::named_sync(2, 32 * GW);
         float4 pre = make_float4(0.f, 0.f, 0.f, 0.f);
         for (int g = 0; g < wg; ++g) {
@@ -363,15 +378,10 @@ __device__ __forceinline__ void chunk_loop(const CUtensorMap* tm_q, const CUtens
             pre.x += x.x; pre.y += x.y; pre.z += x.z; pre.w += x.w;
         }
         tc::named_sync(2, 32 * GW);
-        if (wg > 0) {
 #pragma unroll
-            for (int a = 0; a < TPW; ++a) {
-                float4* p = reinterpret_cast<float4*>(G2 + (TPW * wg + a) * KD + g4off(lane));
-                float4 x = *p;
-                x.x += pre.x; x.y += pre.y; x.z += pre.z; x.w += pre.w;
-                *p = x;
-            }
-        }
+        for (int a = 0; a < TPW; ++a)
+            *reinterpret_cast<float4*>(G2 + (TPW * wg + a) * KD + g4off(lane)) =
+                make_float4(acc[a].x + pre.x, acc[a].y + pre.y, acc[a].z + pre.z, acc[a].w + pre.w);
         return ok;
     };
 
@@ -397,18 +407,13 @@ __device__ __forceinline__ void chunk_loop(const CUtensorMap* tm_q, const CUtens
         __syncthreads();                                                 \
         tc::fence_after_sync();                                          \
     } while (0)
-// The GEMMs of two levels (one operand buffer each), one commit for both.
-#define KDA_LEVEL_MMA2(bufA, colA, bufB, colB, bar)                      \
+// The GEMM of one level pair (operands built by build_level), committed to `bar`.
+#define KDA_PAIR_MMA(col, bar)                                           \
     do {                                                                 \
         if (tid == 0) {                                                  \
-            const uint32_t La_ = sb + OFF_LVL + (bufA);                  \
-            const uint32_t Lb_ = sb + OFF_LVL + (bufB);                  \
             _Pragma("unroll") for (int ks = 0; ks < 8; ++ks)             \
-                tc::mma_bf16(tmem + (colA), desc_k(La_, 128, ks),        \
-                             desc_k(La_, 128, ks), IDESC_LVL, ks > 0);   \
-            _Pragma("unroll") for (int ks = 0; ks < 8; ++ks)             \
-                tc::mma_bf16(tmem + (colB), desc_k(Lb_, 128, ks),        \
-                             desc_k(Lb_, 128, ks), IDESC_LVL, ks > 0);   \
+                tc::mma_bf16(tmem + (col), desc_k(sb + OFF_LVL + LV_PA, 128, ks), \
+                             desc_k(sb + OFF_LVL + LV_PB, 64, ks), IDESC_LVL, ks > 0); \
             tc::mma_commit(&ms.bar);                                     \
         }                                                                \
     } while (0)
@@ -427,13 +432,13 @@ __device__ __forceinline__ void chunk_loop(const CUtensorMap* tm_q, const CUtens
             tc::tma_prefetch_l2_3d(tm_v, 0, nt0, (int)nbh);
         }
         // ---------------------------------------------------------------- P3: levels 32, 16
-        // two levels per pass, one buffer each; their GEMMs run under the 4-token blocks
+        // one GEMM per pair of levels; the first pair's runs under the 4-token blocks
         LevelItems items;
         load_level_items(sm, tid, items);
-        build_level(sm, 0, LV_L0, tid, items);
-        build_level(sm, 1, LV_L1, tid, items);
+        build_level(sm, 0, tid, items);
+        build_level(sm, 1, tid, items);
         KDA_SYNC_FOR_MMA();
-        KDA_LEVEL_MMA2(LV_L0, TM_LVL, LV_L1, TM_LVL + 64, bar_m0);
+        KDA_PAIR_MMA(TM_LVL, bar_m0);
         // ---------------------------------------------------------------- P3: 4-token blocks
         // pairs inside 4-token blocks: exact pairwise decay, CUDA cores.
         // warp w = 4-token block w; lane = channels 4*lane..4*lane+3.
@@ -498,21 +503,21 @@ __device__ __forceinline__ void chunk_loop(const CUtensorMap* tm_q, const CUtens
             if (failed) break;
         }
         // ---------------------------------------------------------------- P3: levels 8, 4
-        build_level(sm, 2, LV_L0, tid, items);
-        build_level(sm, 3, LV_L1, tid, items);
+        build_level(sm, 2, tid, items);
+        build_level(sm, 3, tid, items);
         KDA_SYNC_FOR_MMA();
-        KDA_LEVEL_MMA2(LV_L0, TM_LVL + 128, LV_L1, TM_LVL + 192, bar_m1);
+        KDA_PAIR_MMA(TM_LVL + 64, bar_m1);
         // while they run: beta K Gamma and beta V as MN-major [t][.] operands in the A1 slot
 #pragma unroll
         for (int ii = 0; ii < 2; ++ii) {
+            // the same (token, 8 channels) items as the level operands: k and G from registers
             const int item = tid + NT * ii, tt = item >> 4, c8 = item & 15;
             const float bt = ms.beta[tt];
-            float kf[8], vf[8], g8[8], o[8];
-            unpack8(*reinterpret_cast<const uint4*>(sm + OFF_K + tt * 256 + c8 * 16), kf);
+            float kf[8], vf[8], o[8];
+            unpack8(items.k[ii], kf);
             unpack8(*reinterpret_cast<const uint4*>(sm + OFF_V + tt * 256 + c8 * 16), vf);
-            load8g(G2, tt, c8, g8);
 #pragma unroll
-            for (int j = 0; j < 8; ++j) o[j] = bt * kf[j] * ex2(g8[j]);
+            for (int j = 0; j < 8; ++j) o[j] = bt * kf[j] * ex2(items.g[ii][j]);
             *reinterpret_cast<uint4*>(sm + OFF_BKG + mnmaj_off(tt, c8 * 8, 8192)) = pack8(o);
 #pragma unroll
             for (int j = 0; j < 8; ++j) o[j] = bt * vf[j];
@@ -522,58 +527,89 @@ __device__ __forceinline__ void chunk_loop(const CUtensorMap* tm_q, const CUtens
         if (failed) break;
         // ---------------------------------------------------------------- P3 epilogue
         {
-            // TMEM lane `row`: rows 0..63 are A rows (k side), rows 64..127 are M rows (q side);
-            // this warp takes the 16 columns i0 = 16 * part.
-            const int t = row & 63, i0 = 16 * part;
-            const bool is_m = row >= 64;
-            const int wt0 = (q4 & 1) * 32;  // first token row of this warp
-            float o16[16];
-            if (i0 > wt0 + 31) {  // every pair of this column block is above the diagonal
-#pragma unroll
-                for (int j = 0; j < 16; ++j) o16[j] = 0.f;
-            } else {
-                const float bt = ms.beta[t];
-                uint32_t d0[16], d1[16], d2[16], d3[16];
-                tc::tmem_ld16(taddr(tmem, warp, TM_LVL + i0), d0);
-                tc::tmem_ld16(taddr(tmem, warp, TM_LVL + 64 + i0), d1);
-                tc::tmem_ld16(taddr(tmem, warp, TM_LVL + 128 + i0), d2);
-                tc::tmem_ld16(taddr(tmem, warp, TM_LVL + 192 + i0), d3);
+            float* Af = reinterpret_cast<float*>(sm + OFF_LVL + LV_AF);
+            uint8_t* MB = sm + OFF_LVL + LV_MB;
+            // (a) level scores.  TMEM lane `row` of the tile of pair part / 2: rows 64 slot ..
+            //     belong to level li = 2 (part / 2) + slot, k rows (A scores) first, then q rows
+            //     (M scores), by the upper token's rank; the level's 32 columns are the lower
+            //     tokens' ranks.  Only pairs inside one 2h-block are scores.
+            {
+                const int p = part >> 1, slot = row >> 6, s = 5 - (2 * p + slot), h = 1 << s;
+                const bool is_m = (row & 32) != 0;
+                const int rt = row & 31, rb = 16 * (part & 1);
+                const int t = ((rt >> s) << (s + 1)) | h | (rt & (h - 1));
+                uint32_t d[16];
+                tc::tmem_ld16(taddr(tmem, warp, TM_LVL + 64 * p + 32 * slot + rb), d);
                 tc::tmem_ld_wait();
-                const int xb = (t ^ i0) & 48;  // level bits shared by the whole block
-                if (xb >= 16) {
+                // The valid columns of this thread's 16 form one run of len = min(h, 16) starting at
+                // a multiple of len (none when the run lies in the other 16): move it to the front
+                // with selects, so the stores below index registers statically.
+                const int blk = rt >> s, len = min(h, 16);
+                const int j0 = (blk << s) - rb;  // first valid column; the run is [j0, j0 + len)
+                const bool any = j0 < 16 && j0 + h > 0;
+                const int i0 = rb + max(j0, 0) + (blk << s);  // token of the run's first column
+                float w[16];
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        const float val = __uint_as_float(xb >= 32 ? d0[j] : d1[j]);
-                        const bool valid = is_m ? (i0 + j <= t) : (i0 + j < t);
-                        o16[j] = valid ? (is_m ? val : bt * val) : 0.f;
-                    }
-                } else {
-                    const float* dg = ms.diag[t >> 2];
-                    const int tl = t & 3;
+                for (int k = 0; k < 16; ++k) w[k] = __uint_as_float(d[k]);
+                if (len <= 8) {
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        const int i = i0 + j;
-                        const int x = t ^ i;
-                        float val = __uint_as_float(x >= 8 ? d2[j] : d3[j]);
-                        if (x < 4) {
-                            const int il = i & 3;
-                            const int idx = (tl == il) ? 6 + tl
-                                                       : (is_m ? 10 : 0) + ((tl * (tl - 1)) >> 1) + il;
-                            val = dg[tl >= il ? idx : 0];
-                        }
-                        const bool valid = is_m ? (i <= t) : (i < t);
-                        o16[j] = valid ? (is_m ? val : bt * val) : 0.f;
+                    for (int k = 0; k < 8; ++k) w[k] = (j0 & 8) ? w[8 + k] : w[k];
+                }
+                if (len <= 4) {
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) w[k] = (j0 & 4) ? w[4 + k] : w[k];
+                }
+                // the run is 4, 8 or 16 consecutive tokens from i0 (a multiple of its length):
+                // whole 8- or 16-byte stores
+                if (any && is_m) {
+                    uint32_t pk[8];
+#pragma unroll
+                    for (int m = 0; m < 8; ++m) pk[m] = tc::pack_bf16x2(w[2 * m], w[2 * m + 1]);
+                    if (len == 4) {
+                        *reinterpret_cast<uint2*>(MB + kmaj_off(t, i0, 64)) = make_uint2(pk[0], pk[1]);
+                    } else {
+                        *reinterpret_cast<uint4*>(MB + kmaj_off(t, i0, 64)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                        if (len == 16)
+                            *reinterpret_cast<uint4*>(MB + kmaj_off(t, i0 + 8, 64)) =
+                                make_uint4(pk[4], pk[5], pk[6], pk[7]);
                     }
+                } else if (any) {
+                    const float bt = ms.beta[t];
+#pragma unroll
+                    for (int m = 0; m < 4; ++m)
+                        if (4 * m < len)
+                            *reinterpret_cast<float4*>(Af + swz(t, i0 + 4 * m)) =
+                                make_float4(bt * w[4 * m], bt * w[4 * m + 1], bt * w[4 * m + 2], bt * w[4 * m + 3]);
                 }
             }
-            if (!is_m) {
-                float* Af = reinterpret_cast<float*>(sm + OFF_LVL + LV_AF);
+            // (b) row t, 4-column groups 2 g8, 2 g8 + 1: the 4-token block on the diagonal from the
+            //     CUDA-core dot products (A strictly below the diagonal, M on and below), M zero
+            //     above it.  A above the diagonal is never read.
+            {
+                const int t = tid >> 3, g8 = tid & 7, tb = t >> 2, tl = t & 3;
+                const float* dg = ms.diag[tb];
+                const float bt = ms.beta[t];
 #pragma unroll
-                for (int j = 0; j < 16; j += 4)
-                    *reinterpret_cast<float4*>(Af + swz(t, i0 + j)) =
-                        make_float4(o16[j], o16[j + 1], o16[j + 2], o16[j + 3]);
-            } else {
-                store16_k(sm + OFF_LVL + LV_MB, t, i0, 64, o16);
+                for (int hg = 0; hg < 2; ++hg) {
+                    const int g = 2 * g8 + hg;
+                    if (g < tb) continue;  // level scores, written in (a)
+                    float m4[4] = {0.f, 0.f, 0.f, 0.f};
+                    if (g == tb) {
+                        float a4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                        for (int il = 0; il < 4; ++il) {
+                            if (il < tl) {
+                                a4[il] = bt * dg[((tl * (tl - 1)) >> 1) + il];
+                                m4[il] = dg[10 + ((tl * (tl - 1)) >> 1) + il];
+                            } else if (il == tl) {
+                                m4[il] = dg[6 + tl];
+                            }
+                        }
+                        *reinterpret_cast<float4*>(Af + swz(t, 4 * g)) = make_float4(a4[0], a4[1], a4[2], a4[3]);
+                    }
+                    *reinterpret_cast<uint2*>(MB + kmaj_off(t, 4 * g, 64)) =
+                        make_uint2(tc::pack_bf16x2(m4[0], m4[1]), tc::pack_bf16x2(m4[2], m4[3]));
+                }
             }
         }
         tc::fence_before_sync();
@@ -1012,7 +1048,7 @@ __device__ __forceinline__ void chunk_loop(const CUtensorMap* tm_q, const CUtens
     }
 #undef KDA_WAIT
 #undef KDA_SYNC_FOR_MMA
-#undef KDA_LEVEL_MMA2
+#undef KDA_PAIR_MMA
 
     if (!kSplit && !failed && hT) {
         const int c = row;

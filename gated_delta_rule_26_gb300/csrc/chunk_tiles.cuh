@@ -70,12 +70,16 @@ __device__ __forceinline__ void load16_k(const uint8_t* base, int row, int k0, i
 #pragma unroll
     for (int j = 0; j < 8; ++j) { f[j] = lo[j]; f[8 + j] = hi[j]; }
 }
+// Descriptors of the 16-element K step `ks` of a tile at `saddr`.  The start address sits in
+// the descriptor's low bits (in 16-byte units, 14 bits: shared addresses stay below 256 KB), so
+// a step's descriptor is the tile's plus a constant: one base per tile, then additions.
 __device__ __forceinline__ uint64_t desc_k(uint32_t saddr, int rows, int ks) {
     const int k0 = ks * 16;
-    return tc::smem_desc(saddr + (k0 >> 6) * (rows * 128) + (k0 & 63) * 2, 16, 1024);
+    const uint32_t off = (uint32_t)((k0 >> 6) * (rows * 128) + (k0 & 63) * 2);
+    return tc::smem_desc(saddr, 16, 1024) + (uint64_t)(off >> 4);
 }
 __device__ __forceinline__ uint64_t desc_mn(uint32_t saddr, uint32_t atom, int ks) {
-    return tc::smem_desc(saddr + ks * 2048, atom, 1024);
+    return tc::smem_desc(saddr, atom, 1024) + (uint64_t)(ks * (2048 >> 4));
 }
 // TMEM address of lane quarter (warp & 3) at column `col`.
 __device__ __forceinline__ uint32_t taddr(uint32_t base, int warp, uint32_t col) {
