@@ -196,6 +196,84 @@ __device__ __forceinline__ void build_level(uint8_t* sm, int li, int tid, const 
     }
 }
 
+// Pairs inside the 4-token block b4: the exact pairwise decay e^{G_t - G_i} per channel on
+// CUDA cores (one warp, lane = channels 4 lane .. 4 lane + 3), dot products reduced over the
+// lanes into ms.diag[b4]: [0, 6) the A pairs, [6, 10) M's diagonal, [10, 16) the M pairs.
+__device__ __forceinline__ void diag_block(const uint8_t* sm, Misc& ms, int b4, int lane) {
+    const float* G2 = reinterpret_cast<const float*>(sm + OFF_G);
+    const int c4 = lane * 4;
+    float kk[4][4], qq[4][4], gg[4][4];
+#pragma unroll
+    for (int a = 0; a < 4; ++a) {
+        const int t = 4 * b4 + a;
+        const uint2 kr = *reinterpret_cast<const uint2*>(sm + OFF_K + t * 256 + c4 * 2);
+        const uint2 qr = *reinterpret_cast<const uint2*>(sm + OFF_Q + t * 256 + c4 * 2);
+        kk[a][0] = bf_lo(kr.x); kk[a][1] = bf_hi(kr.x); kk[a][2] = bf_lo(kr.y); kk[a][3] = bf_hi(kr.y);
+        qq[a][0] = bf_lo(qr.x); qq[a][1] = bf_hi(qr.x); qq[a][2] = bf_lo(qr.y); qq[a][3] = bf_hi(qr.y);
+        const float4 g = *reinterpret_cast<const float4*>(G2 + t * KD + g4off(lane));
+        gg[a][0] = g.x; gg[a][1] = g.y; gg[a][2] = g.z; gg[a][3] = g.w;
+    }
+    float v[16];
+#pragma unroll
+    for (int a = 0; a < 4; ++a) {  // M diagonal
+        float s = 0.f;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) s = fmaf(qq[a][j], kk[a][j], s);
+        v[6 + a] = s;
+    }
+#pragma unroll
+    for (int a = 1; a < 4; ++a)
+#pragma unroll
+        for (int b = 0; b < a; ++b) {
+            float sa = 0.f, sq = 0.f;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const float kd = kk[b][j] * ex2(gg[a][j] - gg[b][j]);
+                sa = fmaf(kk[a][j], kd, sa);
+                sq = fmaf(qq[a][j], kd, sq);
+            }
+            const int idx = a * (a - 1) / 2 + b;
+            v[idx] = sa;
+            v[10 + idx] = sq;
+        }
+    // reduce-scatter over the 32 lanes: lane l ends with value (l >> 1) & 15
+#pragma unroll
+    for (int off = 16, w = 8; off >= 2; off >>= 1, w >>= 1) {
+        const bool hi = (lane & off) != 0;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            if (j < w) {
+                const float send = hi ? v[j] : v[j + w];
+                const float keep = hi ? v[j + w] : v[j];
+                v[j] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+            }
+        }
+    }
+    v[0] += __shfl_xor_sync(0xffffffffu, v[0], 1);
+    if ((lane & 1) == 0) ms.diag[b4][lane >> 1] = v[0];
+}
+
+// beta K Gamma and beta V as MN-major [t][.] operands in the A1 slot, for the same
+// (token, 8 channels) items as the level operands (k and G from their registers).
+__device__ __forceinline__ void build_bkg_bv(uint8_t* sm, const Misc& ms, int tid,
+                                             const LevelItems& items) {
+#pragma unroll
+    for (int ii = 0; ii < 2; ++ii) {
+        // the same (token, 8 channels) items as the level operands: k and G from registers
+        const int item = tid + NT * ii, tt = item >> 4, c8 = item & 15;
+        const float bt = ms.beta[tt];
+        float kf[8], vf[8], o[8];
+        unpack8(items.k[ii], kf);
+        unpack8(*reinterpret_cast<const uint4*>(sm + OFF_V + tt * 256 + c8 * 16), vf);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) o[j] = bt * kf[j] * ex2(items.g[ii][j]);
+        *reinterpret_cast<uint4*>(sm + OFF_BKG + mnmaj_off(tt, c8 * 8, 8192)) = pack8(o);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) o[j] = bt * vf[j];
+        *reinterpret_cast<uint4*>(sm + OFF_BV + mnmaj_off(tt, c8 * 8, 8192)) = pack8(o);
+    }
+}
+
 // Float index of element (t, i) of a 64 x 64 fp32 matrix whose 16-byte column groups are
 // XOR-swizzled by the row, so that row-wise and column-wise float4 accesses by
 // consecutive threads fall into distinct banks.
@@ -388,6 +466,11 @@ __device__ __forceinline__ void chunk_loop(const CUtensorMap* tm_q, const CUtens
     if (it_begin < it_end && (kSplit || !group_c)) {
         const GatePre gp = gate_fetch(item_bh(it_begin), item_n(it_begin));
         failed = !gate_scan(item_bh(it_begin), item_n(it_begin), gp);
+        if (!kSplit) {  // the fused kernel's gate group also does the first chunk's 4-token blocks
+            __syncwarp();
+            diag_block(sm, ms, 2 * (warp - 8), lane);
+            diag_block(sm, ms, 2 * (warp - 8) + 1, lane);
+        }
     }
     ph_qkz ^= 1u;
     if (__syncthreads_or(failed)) failed = true;
@@ -440,62 +523,17 @@ __device__ __forceinline__ void chunk_loop(const CUtensorMap* tm_q, const CUtens
         KDA_SYNC_FOR_MMA();
         KDA_PAIR_MMA(TM_LVL, bar_m0);
         // ---------------------------------------------------------------- P3: 4-token blocks
-        // pairs inside 4-token blocks: exact pairwise decay, CUDA cores.
-        // warp w = 4-token block w; lane = channels 4*lane..4*lane+3.
-        {
-            const int b4 = warp, c4 = lane * 4;
-            float kk[4][4], qq[4][4], gg[4][4];
-#pragma unroll
-            for (int a = 0; a < 4; ++a) {
-                const int t = 4 * b4 + a;
-                const uint2 kr = *reinterpret_cast<const uint2*>(sm + OFF_K + t * 256 + c4 * 2);
-                const uint2 qr = *reinterpret_cast<const uint2*>(sm + OFF_Q + t * 256 + c4 * 2);
-                kk[a][0] = bf_lo(kr.x); kk[a][1] = bf_hi(kr.x); kk[a][2] = bf_lo(kr.y); kk[a][3] = bf_hi(kr.y);
-                qq[a][0] = bf_lo(qr.x); qq[a][1] = bf_hi(qr.x); qq[a][2] = bf_lo(qr.y); qq[a][3] = bf_hi(qr.y);
-                const float4 g = *reinterpret_cast<const float4*>(G2 + t * KD + g4off(lane));
-                gg[a][0] = g.x; gg[a][1] = g.y; gg[a][2] = g.z; gg[a][3] = g.w;
-            }
-            float v[16];
-#pragma unroll
-            for (int a = 0; a < 4; ++a) {  // M diagonal
-                float s = 0.f;
-#pragma unroll
-                for (int j = 0; j < 4; ++j) s = fmaf(qq[a][j], kk[a][j], s);
-                v[6 + a] = s;
-            }
-#pragma unroll
-            for (int a = 1; a < 4; ++a)
-#pragma unroll
-                for (int b = 0; b < a; ++b) {
-                    float sa = 0.f, sq = 0.f;
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        const float kd = kk[b][j] * ex2(gg[a][j] - gg[b][j]);
-                        sa = fmaf(kk[a][j], kd, sa);
-                        sq = fmaf(qq[a][j], kd, sq);
-                    }
-                    const int idx = a * (a - 1) / 2 + b;
-                    v[idx] = sa;
-                    v[10 + idx] = sq;
-                }
-            // reduce-scatter over the 32 lanes: lane l ends with value (l >> 1) & 15
-#pragma unroll
-            for (int off = 16, w = 8; off >= 2; off >>= 1, w >>= 1) {
-                const bool hi = (lane & off) != 0;
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    if (j < w) {
-                        const float send = hi ? v[j] : v[j + w];
-                        const float keep = hi ? v[j + w] : v[j];
-                        v[j] = keep + __shfl_xor_sync(0xffffffffu, send, off);
-                    }
-                }
-            }
-            v[0] += __shfl_xor_sync(0xffffffffu, v[0], 1);
-            if ((lane & 1) == 0) ms.diag[b4][lane >> 1] = v[0];
+        // under the first pair's GEMM: the 4-token blocks (prep kernel; the fused kernel's gate
+        // group did them during the previous carry) or beta K Gamma / beta V (fused kernel)
+        bool okv_all = true;
+        if constexpr (kSplit) {
+            diag_block(sm, ms, warp, lane);
+        } else {
+            okv_all = tc::mbar_wait(&ms.bar_v, ph_v);
+            build_bkg_bv(sm, ms, tid, items);
         }
         {
-            const bool okv = tid != 0 || tc::mbar_wait(&ms.bar_v, ph_v);
+            const bool okv = kSplit ? (tid != 0 || tc::mbar_wait(&ms.bar_v, ph_v)) : okv_all;
             const bool ok0 = tid != 0 || tc::mbar_wait(&ms.bar_m0, ph0);
             ph_v ^= 1u; ph0 ^= 1u;
             if (__syncthreads_or(!(okv && ok0))) failed = true;
@@ -507,22 +545,8 @@ __device__ __forceinline__ void chunk_loop(const CUtensorMap* tm_q, const CUtens
         build_level(sm, 3, tid, items);
         KDA_SYNC_FOR_MMA();
         KDA_PAIR_MMA(TM_LVL + 64, bar_m1);
-        // while they run: beta K Gamma and beta V as MN-major [t][.] operands in the A1 slot
-#pragma unroll
-        for (int ii = 0; ii < 2; ++ii) {
-            // the same (token, 8 channels) items as the level operands: k and G from registers
-            const int item = tid + NT * ii, tt = item >> 4, c8 = item & 15;
-            const float bt = ms.beta[tt];
-            float kf[8], vf[8], o[8];
-            unpack8(items.k[ii], kf);
-            unpack8(*reinterpret_cast<const uint4*>(sm + OFF_V + tt * 256 + c8 * 16), vf);
-#pragma unroll
-            for (int j = 0; j < 8; ++j) o[j] = bt * kf[j] * ex2(items.g[ii][j]);
-            *reinterpret_cast<uint4*>(sm + OFF_BKG + mnmaj_off(tt, c8 * 8, 8192)) = pack8(o);
-#pragma unroll
-            for (int j = 0; j < 8; ++j) o[j] = bt * vf[j];
-            *reinterpret_cast<uint4*>(sm + OFF_BV + mnmaj_off(tt, c8 * 8, 8192)) = pack8(o);
-        }
+        // prep kernel: beta K Gamma and beta V while the second pair's GEMM runs
+        if constexpr (kSplit) build_bkg_bv(sm, ms, tid, items);
         KDA_WAIT(bar_m1, ph1);
         if (failed) break;
         // ---------------------------------------------------------------- P3 epilogue
@@ -1036,6 +1060,10 @@ __device__ __forceinline__ void chunk_loop(const CUtensorMap* tm_q, const CUtens
                 }
             } else if (has_next) {
                 if (!gate_scan(nbh, nt0 / C, gp)) failed = true;
+                // the next chunk's 4-token blocks: this warp's own 8 tokens of G2
+                __syncwarp();
+                diag_block(sm, ms, 2 * (warp - 8), lane);
+                diag_block(sm, ms, 2 * (warp - 8) + 1, lane);
             }
             ph0 ^= 1u;  // C1's and C3's commits, waited by the carry group only
             ph1 ^= 1u;
