@@ -34,8 +34,7 @@ constexpr uint32_t K2_S = 0;            // 32 KB S bf16, MN-major [c][v] (2 atom
 constexpr uint32_t K2_DELTA = 32768;    // 16 KB Delta^T, K-major [v][t]
 constexpr uint32_t K2_STAGE = 49152;    // two operand stages
 // one stage: [W^T | Q'^T] (MN-major, 2 atoms), [U^T | U'^T] (K-major [v][t], 2 atoms),
-// K~ (MN-major [t][c], 2 atoms of 8 KB), Gamma_last; the o tile of the chunk is staged
-// row-major [t][v] over the [W^T | Q'^T] slot once C1 has consumed it.
+// K~ (MN-major [t][c], 2 atoms of 8 KB), Gamma_last.
 constexpr uint32_t ST_WQ = 0, ST_UU = 32768, ST_KT = 65536, ST_GL = 81920;
 constexpr uint32_t ST_BYTES = 82944;  // 81 KB, a multiple of 1024
 constexpr uint32_t ST_TX = (uint32_t)kItemBytes;
@@ -191,34 +190,30 @@ __global__ void __launch_bounds__(NT2, 1)
         KDA_CARRY_WAIT(ms.bar_mma, ph_m);
         if (failed) break;
         // ---------------------------------------------------------------- K2: C2
-        // C2: lane v, tokens 16 part ..: Delta^T -> K-major [v][t]; o -> staging [t][v]
+        // C2: lane v, tokens 16 part ..: Delta^T -> K-major [v][t] (C3 waits for it); o is
+        // computed and written to HBM after C3 has been issued
+        const int v = row, tb = 16 * part;
+        uint32_t dq[16];
+        float up[16];
         {
-            const int v = row;
-            __nv_bfloat16* ost = reinterpret_cast<__nv_bfloat16*>(st + ST_WQ);
-            {
-                const int tb = 16 * part;
-                uint32_t dw[16], dq[16];
-                tc::tmem_ld16(taddr(tmem, warp, TM_D2 + tb), dw);
-                tc::tmem_ld16(taddr(tmem, warp, TM_D2 + 64 + tb), dq);
-                float u[16], up[16];
-                load16_k(st + ST_UU, v, tb, 128, u);
-                load16_k(st + ST_UU + 16384, v, tb, 128, up);
-                tc::tmem_ld_wait();
-                float f[16];
+            uint32_t dw[16];
+            tc::tmem_ld16(taddr(tmem, warp, TM_D2 + tb), dw);
+            tc::tmem_ld16(taddr(tmem, warp, TM_D2 + 64 + tb), dq);
+            float u[16];
+            load16_k(st + ST_UU, v, tb, 128, u);
+            load16_k(st + ST_UU + 16384, v, tb, 128, up);
+            tc::tmem_ld_wait();
+            float f[16];
 #pragma unroll
-                for (int i = 0; i < 16; ++i) f[i] = u[i] - __uint_as_float(dw[i]);
-                store16_k(sm + K2_DELTA, v, tb, 128, f);
-#pragma unroll
-                for (int i = 0; i < 16; ++i)
-                    ost[(tb + i) * VD + v] = __float2bfloat16_rn(scale * (__uint_as_float(dq[i]) + up[i]));
-            }
+            for (int i = 0; i < 16; ++i) f[i] = u[i] - __uint_as_float(dw[i]);
+            store16_k(sm + K2_DELTA, v, tb, 128, f);
         }
         tc::fence_proxy_async_smem();
         tc::fence_before_sync();
         __syncthreads();
         tc::fence_after_sync();
         // ---------------------------------------------------------------- K2: C3 + o out
-        // C3: S += K~^T Delta, while the staged o rows go out
+        // C3: S += K~^T Delta, while this thread's o values go out
         if (tid == 0) {
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks)
@@ -226,12 +221,11 @@ __global__ void __launch_bounds__(NT2, 1)
                              desc_k(sb + K2_DELTA, 128, ks), IDESC_SK2, 1u);
             tc::mma_commit(&ms.bar_mma);
         }
+        {
+            float o[16];
 #pragma unroll
-        for (int r = 0; r < 2; ++r) {
-            const int q = tid + NT2 * r, tr = q >> 4, c16 = q & 15;
-            if (tr < cn)
-                *reinterpret_cast<uint4*>(out + (bh * T + t0 + tr) * VD + c16 * 8) =
-                    *reinterpret_cast<const uint4*>(st + ST_WQ + tr * 256 + c16 * 16);
+            for (int i = 0; i < 16; ++i) o[i] = scale * (__uint_as_float(dq[i]) + up[i]);
+            store_o16_pairs(out + (bh * T + t0 + tb) * VD, v, lane, cn - tb, o);
         }
         KDA_CARRY_WAIT(ms.bar_mma, ph_m);
         if (failed) break;

@@ -81,7 +81,6 @@ constexpr uint32_t LV_QG = 0;       // Q Gamma, MN-major [t][c] (16 KB)      P5
 constexpr uint32_t LV_UT = 32768;   // U^T K-major [v][i] (16 KB)            P5
 constexpr uint32_t LV_Z = 49152;    // z tile of the NEXT chunk (16 KB)      P5-P2
 constexpr uint32_t LV_DELTA = 16384;// Delta^T K-major [v][t] (16 KB)        C2-C3
-constexpr uint32_t LV_OST = 0;      // o staging, row-major [t][v] bf16      C2
 constexpr uint32_t LV_UPS = 0;      // prep kernel: U'^T staging, K-major [v][t] (16 KB)
 // K~ (K e^{G_last - G}, MN-major [t][c]) lives in the v-tile slot OFF_V from P5 to C3.
 // beta K Gamma and beta V (MN-major [t][.], 16 KB each) live in the A1 slot from P3 until
@@ -988,47 +987,48 @@ __device__ __forceinline__ void chunk_loop(const CUtensorMap* tm_q, const CUtens
                     if (tc::named_sync_or(1, 256, !ok)) failed = true;
                     tc::fence_after_sync();
                 }
-                // C2: lane v, tokens 32*half..: Delta^T = U^T - (W S)^T -> K-major [v][t];
-                //     o[t][v] = scale ((Q' S)^T + U'^T) -> row-major staging [t][v]
+                // C2: lane v, tokens 32*half..: Delta^T = U^T - (W S)^T -> K-major [v][t] (C3
+                //     waits for it); o is computed and written to HBM after C3 has been issued
                 const int half = warp >> 2, v = row;
                 if (!failed) {
-    #pragma unroll 1
+#pragma unroll 1
                     for (int tb = 32 * half; tb < 32 * half + 32; tb += 16) {
-                        uint32_t dw[16], du[16], dq[16], dp[16];
+                        uint32_t dw[16], du[16];
                         tc::tmem_ld16(taddr(tmem, warp, TM_D1 + tb), dw);
                         tc::tmem_ld16(taddr(tmem, warp, TM_U + tb), du);
-                        tc::tmem_ld16(taddr(tmem, warp, TM_D1 + 64 + tb), dq);
-                        tc::tmem_ld16(taddr(tmem, warp, TM_UP + tb), dp);
                         tc::tmem_ld_wait();
                         float f[16];
-    #pragma unroll
+#pragma unroll
                         for (int j = 0; j < 16; ++j) f[j] = __uint_as_float(du[j]) - __uint_as_float(dw[j]);
                         store16_k(sm + OFF_LVL + LV_DELTA, v, tb, 128, f);
-                        __nv_bfloat16* ost = reinterpret_cast<__nv_bfloat16*>(sm + OFF_LVL + LV_OST);
-    #pragma unroll
-                        for (int j = 0; j < 16; ++j)
-                            ost[(tb + j) * VD + v] =
-                                __float2bfloat16_rn(scale * (__uint_as_float(dq[j]) + __uint_as_float(dp[j])));
                     }
                 }
                 tc::fence_proxy_async_smem();
                 tc::fence_before_sync();
                 tc::named_sync(1, 256);
                 tc::fence_after_sync();
-                // C3: S += K~^T Delta (K~ in the v-tile slot), while the staged o rows go out
+                // C3: S += K~^T Delta (K~ in the v-tile slot), while o = scale ((Q' S)^T + U'^T)^T
+                //     goes out from TMEM (columns C3 does not touch)
                 if (tid == 0 && !failed) {
-    #pragma unroll
+#pragma unroll
                     for (int ks = 0; ks < 4; ++ks)
                         tc::mma_bf16(tmem + TM_S, desc_mn(sb + OFF_V, 8192, ks),
                                      desc_k(sb + OFF_LVL + LV_DELTA, 128, ks), IDESC_SK, 1u);
                     tc::mma_commit(&ms.bar_m1);
                 }
-    #pragma unroll
-                for (int r = 0; r < 4; ++r) {
-                    const int q = tid + 256 * r, tr = q >> 4, c16 = q & 15;
-                    if (tr < cn)
-                        *reinterpret_cast<uint4*>(out + (bh * T + t0 + tr) * VD + c16 * 8) =
-                            *reinterpret_cast<const uint4*>(sm + OFF_LVL + LV_OST + tr * 256 + c16 * 16);
+                if (!failed) {
+#pragma unroll 1
+                    for (int tb = 32 * half; tb < 32 * half + 32; tb += 16) {
+                        uint32_t dq[16], dp[16];
+                        tc::tmem_ld16(taddr(tmem, warp, TM_D1 + 64 + tb), dq);
+                        tc::tmem_ld16(taddr(tmem, warp, TM_UP + tb), dp);
+                        tc::tmem_ld_wait();
+                        float o[16];
+#pragma unroll
+                        for (int j = 0; j < 16; ++j)
+                            o[j] = scale * (__uint_as_float(dq[j]) + __uint_as_float(dp[j]));
+                        store_o16_pairs(out + (bh * T + t0 + tb) * VD, v, lane, cn - tb, o);
+                    }
                 }
                 {
                     const bool ok = failed || tid != 0 || tc::mbar_wait(&ms.bar_m1, ph1);

@@ -81,6 +81,24 @@ __device__ __forceinline__ uint64_t desc_k(uint32_t saddr, int rows, int ks) {
 __device__ __forceinline__ uint64_t desc_mn(uint32_t saddr, uint32_t atom, int ks) {
     return tc::smem_desc(saddr, atom, 1024) + (uint64_t)(ks * (2048 >> 4));
 }
+// Row-major bf16 output from a lane-per-column layout: lane l of a warp holds o[t][v] for one
+// column v (v even on even lanes) and the 16 tokens t = t0 + i.  Neighbouring lanes swap one
+// value per token pair, so each lane writes 32-bit pairs (v, v + 1): even lanes the even
+// tokens, odd lanes the odd ones.  Rows at or beyond `rows` are not written.
+__device__ __forceinline__ void store_o16_pairs(__nv_bfloat16* out_t0, int v, int lane, int rows,
+                                                const float (&o)[16]) {
+    const bool odd = (lane & 1) != 0;
+#pragma unroll
+    for (int i = 0; i < 16; i += 2) {
+        const float send = odd ? o[i] : o[i + 1];
+        const float recv = __shfl_xor_sync(0xffffffffu, send, 1);
+        const int t = odd ? i + 1 : i;
+        const uint32_t pr = odd ? tc::pack_bf16x2(recv, o[i + 1]) : tc::pack_bf16x2(o[i], recv);
+        if (t < rows)
+            *reinterpret_cast<uint32_t*>(out_t0 + (size_t)t * VD + (v & ~1)) = pr;
+    }
+}
+
 // TMEM address of lane quarter (warp & 3) at column `col`.
 __device__ __forceinline__ uint32_t taddr(uint32_t base, int warp, uint32_t col) {
     return base + ((uint32_t)((warp & 3) * 32) << 16) + col;
