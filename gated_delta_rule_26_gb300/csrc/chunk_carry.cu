@@ -145,20 +145,22 @@ __global__ void __launch_bounds__(NT2, 1)
         tc::fence_after_sync();                                          \
     } while (0)
 
+    // The operands of chunk j are waited for at the barrier that ends chunk j - 1 (or here).
+    if (seg_len > 0) {
+        const bool ok = tid != 0 || tc::mbar_wait(&ms.bar_full[0], 0u);
+        ph_full ^= 1u;
+        if (__syncthreads_or(!ok)) failed = true;
+        tc::fence_after_sync();
+    }
     for (int j = 0; j < seg_len && !failed; ++j) {
         const int s = j & 1;
         uint8_t* st = sm + K2_STAGE + s * ST_BYTES;
         const uint32_t stb = sb + K2_STAGE + s * ST_BYTES;
         const int t0 = (seg_n0 + j) * C, cn = min(C, T - t0);
-        // ---------------------------------------------------------------- K2: wait operands
-        {
-            const bool ok = tid != 0 || tc::mbar_wait(&ms.bar_full[s], (ph_full >> s) & 1u);
-            ph_full ^= 1u << s;
-            if (__syncthreads_or(!ok)) failed = true;
-            tc::fence_after_sync();
-            if (failed) break;
-        }
         // ---------------------------------------------------------------- K2: C1 + decay
+        // stage s ^ 1 was consumed by the previous chunk: refill it two chunks ahead of that one
+        // (a thread of warp 1, so that thread 0 issues C1 at once)
+        if (tid == 32 && j >= 1 && j + 1 < seg_len) issue(j + 1, s ^ 1);
         // C1: D[v][t'] = sum_c S[c][v] [W^T | Q'^T][c][t']
         if (tid == 0) {
 #pragma unroll
@@ -229,6 +231,7 @@ __global__ void __launch_bounds__(NT2, 1)
         }
         KDA_CARRY_WAIT(ms.bar_mma, ph_m);
         if (failed) break;
+
         // ---------------------------------------------------------------- K2: S to bf16
         // S (fp32, TMEM) -> bf16 operand [c][v]
         {
@@ -250,10 +253,16 @@ __global__ void __launch_bounds__(NT2, 1)
         }
         tc::fence_proxy_async_smem();
         tc::fence_before_sync();
-        __syncthreads();
+        {
+            // S is ready for the next C1; the next chunk's operands are waited for here too
+            bool ok = true;
+            if (j + 1 < seg_len) {
+                ok = tid != 0 || tc::mbar_wait(&ms.bar_full[s ^ 1], (ph_full >> (s ^ 1)) & 1u);
+                ph_full ^= 1u << (s ^ 1);
+            }
+            if (__syncthreads_or(!ok)) failed = true;
+        }
         tc::fence_after_sync();
-        // stage s is consumed (C1, C2, C3 and the o rows): refill it two chunks ahead
-        if (tid == 0 && j + 2 < seg_len) issue(j + 2, s);
     }
 #undef KDA_CARRY_WAIT
 
