@@ -43,18 +43,23 @@ def bytes_per_token_head(K, V, io_bytes=2):
     return io_bytes * (3 * K + V) + io_bytes * V + io_bytes
 
 
-def measured_traffic(kernel, source):
-    """DRAM bytes per launch of `kernel` from the committed ncu summary (profiles/traffic.json),
-    or None when the kernel's source has changed since those counters were taken."""
+def measured_traffic(kernel, source, key="dram_bytes_per_launch"):
+    """DRAM bytes of `kernel` from the committed ncu summary (profiles/traffic.json), or None
+    when a source it was built from has changed since those counters were taken.  `source`
+    is one file name or a tuple of them (all must match)."""
     import hashlib
+    sources = (source,) if isinstance(source, str) else tuple(source)
     try:
         with open(os.path.join(ROOT, "profiles", "traffic.json")) as fh:
             entry = json.load(fh)[kernel]
-        with open(os.path.join(ROOT, "gated_delta_rule_26_gb300", "csrc", source), "rb") as fh:
-            digest = hashlib.sha256(fh.read()).hexdigest()
-    except (OSError, KeyError, ValueError):
+        for src in sources:
+            with open(os.path.join(ROOT, "gated_delta_rule_26_gb300", "csrc", src), "rb") as fh:
+                digest = hashlib.sha256(fh.read()).hexdigest()
+            if entry.get("source_sha256", {}).get(src) != digest:
+                return None
+    except (OSError, KeyError, ValueError, AttributeError):
         return None
-    return entry["dram_bytes_per_launch"] if entry.get("source_sha256") == digest else None
+    return entry.get(key)
 
 
 def load_peaks():
@@ -230,7 +235,7 @@ def run_decode(args, kda, inputs, peaks, ws, barrier):
               "roofline": {"bound": "hbm", "achieved": dbytes / dper / 1e9,
                            "peak": peaks["hbm_gbs"], "unit": "GB/s",
                            "frac": dbytes / dper / 1e9 / peaks["hbm_gbs"],
-                           "traffic": measured_traffic("decode_kernel", "decode.cu")
+                           "traffic": measured_traffic("decode_kernel", ("decode.cu",))
                            if dec.B == 256 else None,
                            "algorithmic_bytes": dbytes},
               "config": {"workload": f"decode_bf16 B{dec.B} H{dec.H} K={dec.K} V={dec.V}, "
@@ -271,7 +276,13 @@ def run_long(args, kda, inputs, peaks, ws, barrier):
     res = {"value": ws * B * T / per, "unit": "tokens/s", "ms_per_step": per * 1e3,
            "steps": args.long_steps, "tflops": flops / per / 1e12,
            "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                        "frac": gbs / peaks["hbm_gbs"], "traffic": None,
+                        "frac": gbs / peaks["hbm_gbs"],
+                        "traffic": measured_traffic("split_form_long_bf16",
+                                                    ("chunk_tc.cu", "chunk_carry.cu",
+                                                     "chunk_tiles.cuh", "tc_ptx.cuh"),
+                                                    key="dram_bytes_per_step")
+                        if T == 65536 else None,
+                        "traffic_scope": "all kernels of one step (prep + carry), DRAM read + write",
                         "algorithmic_bytes": alg_bytes, "kernel": "kda chunked forward, split form",
                         "kernels_per_step": launches / args.long_steps,
                         "peak_source": peaks["source"]},
@@ -372,7 +383,8 @@ def main():
     achieved_gbs = alg_bytes / per_step / 1e9
     roofline = {"bound": "hbm", "achieved": achieved_gbs, "peak": peaks["hbm_gbs"],
                 "unit": "GB/s", "frac": achieved_gbs / peaks["hbm_gbs"],
-                "traffic": measured_traffic("kda_chunk_tc_kernel", "chunk_tc.cu"),
+                "traffic": measured_traffic("kda_chunk_tc_kernel", ("chunk_tc.cu", "chunk_tiles.cuh",
+                                                                     "tc_ptx.cuh")),
                 "algorithmic_bytes": alg_bytes,
                 "kernel": "kda chunked forward", "kernels_per_step": kernels_per_step,
                 "peak_source": peaks["source"]}
