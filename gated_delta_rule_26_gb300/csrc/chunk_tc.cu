@@ -88,15 +88,15 @@ constexpr uint32_t LV_UPS = 0;      // prep kernel: U'^T staging, K-major [v][t]
 constexpr uint32_t OFF_BKG = OFF_A1, OFF_BV = OFF_A1 + 16384;
 
 struct Misc {
-    alignas(16) float dt[KD];      // read as float4
     alignas(16) float beta[C];
     alignas(16) float diag[16][16];
     alignas(16) uint64_t bar_qkz;  // TMA: q, k, z tiles of a chunk
     uint64_t bar_v;                // TMA: v tile of a chunk
     uint64_t bar_m0, bar_m1;       // tensor-core commits, alternating
     uint32_t tmem_base;
+    int next_item;                 // fused kernel: the work item taken for after this one
 };
-static_assert(offsetof(Misc, dt) % 16 == 0 && offsetof(Misc, beta) % 16 == 0 &&
+static_assert(offsetof(Misc, beta) % 16 == 0 &&
                   offsetof(Misc, bar_qkz) % 8 == 0 && OFF_MISC % 16 == 0,
               "shared-memory block alignment");
 constexpr uint32_t SMEM_BYTES = OFF_MISC + sizeof(Misc) + 1024;
@@ -289,6 +289,20 @@ struct PrepSeg {
     float* gl;
 };
 
+// Work items of the fused kernel: item i is segment j = i / BH (chunks [j seg_len,
+// (j + 1) seg_len)) of sequence i % BH.  With `counter` null every CTA takes item blockIdx.x
+// (one whole sequence, seg_len = all chunks).  Otherwise a grid of at most one CTA per SM
+// takes items from *counter in order; the fp32 state passes from a sequence's segment j - 1
+// to segment j through `handoff` (B, H, K, V), and flags[bh] = j says that it is there.
+// Items are handed out segment-major, so the item a CTA waits for was taken earlier by a
+// CTA that is running: the waits always end.
+struct FusedSched {
+    int BH, seg_len, n_items;
+    int* counter;
+    unsigned* flags;
+    float* handoff;
+};
+
 // The chunk loop shared by the fused kernel (kSplit = false: one CTA per sequence, the
 // state carried in TMEM from chunk to chunk) and the prep kernel (kSplit = true: CTAs
 // stride over the chunks of all sequences, and everything that does not depend on the
@@ -303,7 +317,7 @@ __device__ __forceinline__ void chunk_loop(const CUtensorMap* tm_q, const CUtens
                                            const float* __restrict__ dt_bias, float scale,
                                            const float* __restrict__ h0,
                                            __nv_bfloat16* __restrict__ out, float* __restrict__ hT,
-                                           PrepSeg seg) {
+                                           PrepSeg seg, FusedSched fs) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -315,27 +329,28 @@ __device__ __forceinline__ void chunk_loop(const CUtensorMap* tm_q, const CUtens
     // warps sharing a quarter split the columns by `part`.
     const int q4 = warp & 3, part = warp >> 2, row = q4 * 32 + lane;
     const int nchunks = (T + C - 1) / C;
-    // Work items: the chunks of sequence blockIdx.x (fused), or every gridDim.x-th item of
-    // the segment (prep).
-    const int it_begin = kSplit ? (int)blockIdx.x : 0;
-    const int it_end = kSplit ? seg.items : nchunks;
-    const int it_step = kSplit ? (int)gridDim.x : 1;
+    // Work items.  Prep kernel: one chunk each, every gridDim.x-th item of the segment.
+    // Fused kernel: a segment of one sequence's chunks (see FusedSched).
+    const int n_items = kSplit ? seg.items : fs.n_items;
+    const bool dynamic = !kSplit && fs.counter != nullptr;
     auto item_bh = [&](int it) -> size_t {
-        return kSplit ? (size_t)(it / seg.seg_len) : (size_t)blockIdx.x;
+        return kSplit ? (size_t)(it / seg.seg_len) : (size_t)(it % fs.BH);
     };
-    auto item_n = [&](int it) -> int { return kSplit ? seg.seg_n0 + it % seg.seg_len : it; };
-    const int h_cta = (int)(item_bh(it_begin) % H);  // the fused kernel's head
-    const float exp_A = expf(A_log[h_cta]);
-
+    auto item_nb = [&](int it) -> int {  // first chunk of the item
+        return kSplit ? seg.seg_n0 + it % seg.seg_len : (it / fs.BH) * fs.seg_len;
+    };
+    auto item_ne = [&](int it) -> int {  // one past its last chunk
+        return kSplit ? item_nb(it) + 1 : min(nchunks, item_nb(it) + fs.seg_len);
+    };
     for (int i = tid; i < (int)(OFF_MISC / 16); i += NT)
         reinterpret_cast<uint4*>(sm)[i] = make_uint4(0u, 0u, 0u, 0u);
-    if (tid < KD) ms.dt[tid] = dt_bias[(size_t)h_cta * KD + tid];
     if (tid == 0) {
         tc::mbar_init(&ms.bar_qkz, 1);
         tc::mbar_init(&ms.bar_v, 1);
         tc::mbar_init(&ms.bar_m0, 1);
         tc::mbar_init(&ms.bar_m1, 1);
         tc::fence_barrier_init();
+        if (dynamic) ms.next_item = atomicAdd(fs.counter, 1);
         tc::tma_prefetch_desc(tm_q);
         tc::tma_prefetch_desc(tm_k);
         tc::tma_prefetch_desc(tm_v);
@@ -352,17 +367,40 @@ __device__ __forceinline__ void chunk_loop(const CUtensorMap* tm_q, const CUtens
 
     // 64 x 64 identity, K-major bf16: the B operand that copies (Q Gamma)^T into an accumulator
     if (tid < 64) *reinterpret_cast<uint16_t*>(sm + OFF_ID + kmaj_off(tid, tid, 64)) = 0x3F80u;
-    // Initial state: fp32 into TMEM (lane c = row), bf16 copy as the MN-major operand [c][v].
-    if (!kSplit) {
-        const size_t bh = blockIdx.x;
+    tc::fence_proxy_async_smem();
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+
+    uint32_t ph_qkz = 0, ph_v = 0, ph0 = 0, ph1 = 0;
+    bool failed = false;
+    const bool group_c = warp < 8;  // fused: carry group; warps 8-15 form the gate group
+    // the current chunk: item cur_it, chunk cur_n of its sequence
+    int cur_it = dynamic ? ms.next_item : (int)blockIdx.x;
+    int cur_n = cur_it < n_items ? item_nb(cur_it) : 0;
+    if (tid == 0 && cur_it < n_items) {
+        const int bh0 = (int)item_bh(cur_it), y0 = cur_n * C;
+        tc::mbar_arrive_expect_tx(&ms.bar_qkz, 3u * 16384u);
+        tc::tma_load_3d(sm + OFF_Q, tm_q, 0, y0, bh0, &ms.bar_qkz);
+        tc::tma_load_3d(sm + OFF_K, tm_k, 0, y0, bh0, &ms.bar_qkz);
+        tc::tma_load_3d(sm + OFF_LVL + LV_Z, tm_z, 0, y0, bh0, &ms.bar_qkz);
+        tc::mbar_arrive_expect_tx(&ms.bar_v, 16384u);
+        tc::tma_load_3d(sm + OFF_V, tm_v, 0, y0, bh0, &ms.bar_v);
+    }
+
+    // The fused kernel's state of sequence sbh: fp32 in TMEM (lane c = row) and bf16 as the
+    // MN-major operand [c][v], this thread's columns [v0b, v0b + nv).  It comes from h0 (a
+    // sequence's first segment) or from the handoff of the previous segment (read past L1:
+    // another SM wrote it), and leaves to the handoff or to hT.
+    auto state_in = [&](size_t sbh, const float* src, int v0b, int nv) {
         const int c = row;
 #pragma unroll 1
-        for (int v0 = 32 * part; v0 < 32 * part + 32; v0 += 16) {
+        for (int v0 = v0b; v0 < v0b + nv; v0 += 16) {
             float f[16];
 #pragma unroll
             for (int j = 0; j < 16; j += 4) {
                 float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (h0) x = *reinterpret_cast<const float4*>(h0 + (bh * KD + c) * VD + v0 + j);
+                if (src) x = __ldcg(reinterpret_cast<const float4*>(src + (sbh * KD + c) * VD + v0 + j));
                 f[j] = x.x; f[j + 1] = x.y; f[j + 2] = x.z; f[j + 3] = x.w;
             }
             uint32_t r[16];
@@ -372,32 +410,35 @@ __device__ __forceinline__ void chunk_loop(const CUtensorMap* tm_q, const CUtens
             store16_mn(sm + OFF_S, c, v0, 16384, f);
         }
         tc::tmem_st_wait();
-    }
-    tc::fence_proxy_async_smem();
-    tc::fence_before_sync();
-    __syncthreads();
-    tc::fence_after_sync();
-
-    uint32_t ph_qkz = 0, ph_v = 0, ph0 = 0, ph1 = 0;
-    bool failed = false;
-    const bool group_c = warp < 8;  // fused: carry group; warps 8-15 form the gate group
-    if (tid == 0 && it_begin < it_end) {
-        const int bh0 = (int)item_bh(it_begin), y0 = item_n(it_begin) * C;
-        tc::mbar_arrive_expect_tx(&ms.bar_qkz, 3u * 16384u);
-        tc::tma_load_3d(sm + OFF_Q, tm_q, 0, y0, bh0, &ms.bar_qkz);
-        tc::tma_load_3d(sm + OFF_K, tm_k, 0, y0, bh0, &ms.bar_qkz);
-        tc::tma_load_3d(sm + OFF_LVL + LV_Z, tm_z, 0, y0, bh0, &ms.bar_qkz);
-        tc::mbar_arrive_expect_tx(&ms.bar_v, 16384u);
-        tc::tma_load_3d(sm + OFF_V, tm_v, 0, y0, bh0, &ms.bar_v);
+    };
+    auto state_out = [&](size_t sbh, float* dst, int v0b, int nv) {
+        const int c = row;
+#pragma unroll 1
+        for (int v0 = v0b; v0 < v0b + nv; v0 += 16) {
+            uint32_t d[16];
+            tc::tmem_ld16(taddr(tmem, warp, TM_S + v0), d);
+            tc::tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < 16; j += 4)
+                *reinterpret_cast<float4*>(dst + (sbh * KD + c) * VD + v0 + j) =
+                    make_float4(__uint_as_float(d[j]), __uint_as_float(d[j + 1]),
+                                __uint_as_float(d[j + 2]), __uint_as_float(d[j + 3]));
+        }
+    };
+    if (!kSplit && cur_it < n_items) {  // the first item's initial state
+        const int j0 = cur_it / fs.BH;
+        bool ok = true;
+        if (j0 > 0) ok = tid != 0 || tc::flag_wait_geq(fs.flags + item_bh(cur_it), (unsigned)j0);
+        if (__syncthreads_or(!ok)) failed = true;
+        if (!failed) state_in(item_bh(cur_it), j0 > 0 ? fs.handoff : h0, 32 * part, 32);
     }
 
     // Gate of item (gbh, gn) by warps GLO .. GLO + GW - 1 (named barrier 2): waits for its
     // q/k/z tiles, loads beta, and writes G2 = in-chunk cumulative log2 decay.  The fused
     // kernel runs it on warps 8-15 during the carry; the prep kernel on all warps.
     constexpr int GLO = kSplit ? 0 : 8, GW = kSplit ? 16 : 8, TPW = C / GW;
-    // The gate's global reads (beta; for the prep kernel also dt_bias and A_log of the item's
-    // head) are issued early by the gate threads, so that their latency is hidden by the
-    // tensor-core work in between.
+    // The gate's global reads (beta, dt_bias and A_log of the chunk's head) are issued early
+    // by the gate threads, so that their latency is hidden by the tensor-core work in between.
     struct GatePre {  // raw loaded values: nothing here waits for the loads to land
         unsigned short beta_bits;
         float A_log_h;
@@ -409,15 +450,10 @@ __device__ __forceinline__ void chunk_loop(const CUtensorMap* tm_q, const CUtens
         const int tg = (warp - GLO) * 32 + lane, tn = gn * C, cnn = min(C, T - tn);
         const int tc = max(0, min(tg, cnn - 1));
         p.beta_bits = __ldg(reinterpret_cast<const unsigned short*>(beta) + gbh * T + tn + tc);
-        if (kSplit) {
-            const int hh = (int)(gbh % H);
-            const float* db = dt_bias + (size_t)hh * KD + lane * 4;
-            p.dt = make_float4(__ldg(db), __ldg(db + 1), __ldg(db + 2), __ldg(db + 3));
-            p.A_log_h = __ldg(A_log + hh);
-        } else {
-            p.dt = make_float4(0.f, 0.f, 0.f, 0.f);
-            p.A_log_h = 0.f;
-        }
+        const int hh = (int)(gbh % H);
+        const float* db = dt_bias + (size_t)hh * KD + lane * 4;
+        p.dt = make_float4(__ldg(db), __ldg(db + 1), __ldg(db + 2), __ldg(db + 3));
+        p.A_log_h = __ldg(A_log + hh);
         return p;
     };
     auto gate_scan = [&](size_t gbh, int gn, const GatePre& gp) -> bool {
@@ -428,8 +464,8 @@ __device__ __forceinline__ void chunk_loop(const CUtensorMap* tm_q, const CUtens
         const int tg = wg * 32 + lane;
         if (tg < C) ms.beta[tg] = tg < cnn ? __uint_as_float((uint32_t)gp.beta_bits << 16) : 0.f;
         const int c4 = lane * 4;
-        const float4 dt = kSplit ? gp.dt : *reinterpret_cast<const float4*>(&ms.dt[c4]);
-        const float mult = -(kSplit ? expf(gp.A_log_h) : exp_A) * LOG2E;
+        const float4 dt = gp.dt;
+        const float mult = -expf(gp.A_log_h) * LOG2E;
         // this warp's TPW tokens: running sums in registers; only the warp totals are exchanged
         float4 acc[TPW];
         float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
@@ -462,9 +498,9 @@ __device__ __forceinline__ void chunk_loop(const CUtensorMap* tm_q, const CUtens
         return ok;
     };
 
-    if (it_begin < it_end && (kSplit || !group_c)) {
-        const GatePre gp = gate_fetch(item_bh(it_begin), item_n(it_begin));
-        failed = !gate_scan(item_bh(it_begin), item_n(it_begin), gp);
+    if (cur_it < n_items && (kSplit || !group_c)) {
+        const GatePre gp = gate_fetch(item_bh(cur_it), cur_n);
+        failed = !gate_scan(item_bh(cur_it), cur_n, gp);
         if (!kSplit) {  // the fused kernel's gate group also does the first chunk's 4-token blocks
             __syncwarp();
             diag_block(sm, ms, 2 * (warp - 8), lane);
@@ -500,19 +536,21 @@ __device__ __forceinline__ void chunk_loop(const CUtensorMap* tm_q, const CUtens
         }                                                                \
     } while (0)
 
-    for (int it = it_begin; it < it_end && !failed; it += it_step) {
+    while (cur_it < n_items && !failed) {
+        const int it = cur_it;
         const size_t bh = item_bh(it);
-        const int t0 = item_n(it) * C, cn = min(C, T - t0);
-        const bool has_next = it + it_step < it_end;
-        const size_t nbh = has_next ? item_bh(it + it_step) : bh;
-        const int nt0 = has_next ? item_n(it + it_step) * C : t0;
-        if (kSplit && tid == 0 && has_next) {
-            // the next item's tiles into L2 now, so that its loads later find them there
-            tc::tma_prefetch_l2_3d(tm_z, 0, nt0, (int)nbh);
-            tc::tma_prefetch_l2_3d(tm_q, 0, nt0, (int)nbh);
-            tc::tma_prefetch_l2_3d(tm_k, 0, nt0, (int)nbh);
-            tc::tma_prefetch_l2_3d(tm_v, 0, nt0, (int)nbh);
-        }
+        const int t0 = cur_n * C, cn = min(C, T - t0);
+        const int seg_j = kSplit ? 0 : it / fs.BH;
+        const bool last_of_item = cur_n + 1 >= item_ne(it);
+        // The chunk after this one: the next of this item, or the first of the next item.  A
+        // dynamic fused kernel takes that item now; it is known to all threads after the
+        // first barrier below (next_pending).
+        int nxt_it = last_of_item ? (kSplit ? it + (int)gridDim.x : n_items) : it;
+        const bool next_pending = dynamic && last_of_item;
+        if (next_pending && tid == 0) ms.next_item = atomicAdd(fs.counter, 1);
+        bool has_next = !next_pending && nxt_it < n_items;
+        size_t nbh = has_next ? item_bh(nxt_it) : bh;
+        int nt0 = has_next ? (last_of_item ? item_nb(nxt_it) : cur_n + 1) * C : t0;
         // ---------------------------------------------------------------- P3: levels 32, 16
         // one GEMM per pair of levels; the first pair's runs under the 4-token blocks
         LevelItems items;
@@ -521,6 +559,12 @@ __device__ __forceinline__ void chunk_loop(const CUtensorMap* tm_q, const CUtens
         build_level(sm, 1, tid, items);
         KDA_SYNC_FOR_MMA();
         KDA_PAIR_MMA(TM_LVL, bar_m0);
+        if (next_pending) {
+            nxt_it = ms.next_item;
+            has_next = nxt_it < n_items;
+            nbh = has_next ? item_bh(nxt_it) : bh;
+            nt0 = has_next ? item_nb(nxt_it) * C : t0;
+        }
         // ---------------------------------------------------------------- P3: 4-token blocks
         // under the first pair's GEMM: the 4-token blocks (prep kernel; the fused kernel's gate
         // group did them during the previous carry) or beta K Gamma / beta V (fused kernel)
@@ -1058,6 +1102,26 @@ __device__ __forceinline__ void chunk_loop(const CUtensorMap* tm_q, const CUtens
                         tc::tma_load_3d(sm + OFF_V, tm_v, 0, nt0, (int)nbh, &ms.bar_v);
                     }
                 }
+                // last chunk of an item (while the gate group finishes the next gate): the state
+                // goes to the next segment (handoff, then its flag) or to hT, and the next item's
+                // state comes in, unless that item is this one's next segment (already here)
+                if (!failed && last_of_item) {
+                    const bool more = item_ne(it) < nchunks;
+                    float* dst = more ? fs.handoff : hT;
+                    if (dst) state_out(bh, dst, 64 * half, 64);
+                    if (more) __threadfence();
+                    tc::fence_before_sync();
+                    tc::named_sync(1, 256);
+                    tc::fence_after_sync();
+                    if (more && tid == 0) tc::st_release_gpu(fs.flags + bh, (unsigned)(seg_j + 1));
+                    if (has_next && nxt_it != it + fs.BH) {
+                        const int nj = nxt_it / fs.BH;
+                        bool ok = true;
+                        if (nj > 0) ok = tid != 0 || tc::flag_wait_geq(fs.flags + nbh, (unsigned)nj);
+                        if (tc::named_sync_or(1, 256, !ok)) failed = true;
+                        if (!failed) state_in(nbh, nj > 0 ? fs.handoff : h0, 64 * half, 64);
+                    }
+                }
             } else if (has_next) {
                 if (!gate_scan(nbh, nt0 / C, gp)) failed = true;
                 // the next chunk's 4-token blocks: this warp's own 8 tokens of G2
@@ -1073,26 +1137,17 @@ __device__ __forceinline__ void chunk_loop(const CUtensorMap* tm_q, const CUtens
         tc::fence_before_sync();
         if (__syncthreads_or(failed)) failed = true;
         tc::fence_after_sync();
+        if (last_of_item) {
+            cur_it = nxt_it;
+            cur_n = has_next ? item_nb(nxt_it) : 0;
+        } else {
+            ++cur_n;
+        }
     }
 #undef KDA_WAIT
 #undef KDA_SYNC_FOR_MMA
 #undef KDA_PAIR_MMA
 
-    if (!kSplit && !failed && hT) {
-        const int c = row;
-        const size_t bh = blockIdx.x;
-#pragma unroll
-        for (int v0 = 32 * part; v0 < 32 * part + 32; v0 += 16) {
-            uint32_t d[16];
-            tc::tmem_ld16(taddr(tmem, warp, TM_S + v0), d);
-            tc::tmem_ld_wait();
-#pragma unroll
-            for (int j = 0; j < 16; j += 4)
-                *reinterpret_cast<float4*>(hT + (bh * KD + c) * VD + v0 + j) =
-                    make_float4(__uint_as_float(d[j]), __uint_as_float(d[j + 1]),
-                                __uint_as_float(d[j + 2]), __uint_as_float(d[j + 3]));
-        }
-    }
     if (failed && tid == 0) {
         atomicExch(&g_kda_tc_timeout, 1);
         // give any tensor-core or TMA work still in flight a bounded chance to finish
@@ -1117,9 +1172,9 @@ __global__ void __launch_bounds__(NT, 1)
                         const __nv_bfloat16* __restrict__ beta, const float* __restrict__ A_log,
                         const float* __restrict__ dt_bias, float scale,
                         const float* __restrict__ h0, __nv_bfloat16* __restrict__ out,
-                        float* __restrict__ hT) {
+                        float* __restrict__ hT, FusedSched fs) {
     chunk_loop<false>(&tm_q, &tm_k, &tm_v, &tm_z, nullptr, nullptr, nullptr, H, T, beta, A_log,
-                      dt_bias, scale, h0, out, hT, PrepSeg{0, 1, 0, nullptr});
+                      dt_bias, scale, h0, out, hT, PrepSeg{0, 1, 0, nullptr}, fs);
 }
 
 // The chunk-parallel half of the split forward: every chunk of the segment is one work
@@ -1135,7 +1190,8 @@ __global__ void __launch_bounds__(NT, 1)
                           const __nv_bfloat16* __restrict__ beta, const float* __restrict__ A_log,
                           const float* __restrict__ dt_bias, PrepSeg seg) {
     chunk_loop<true>(&tm_q, &tm_k, &tm_v, &tm_z, &tm_wq, &tm_uu, &tm_kt, H, T, beta, A_log,
-                     dt_bias, 0.f, nullptr, nullptr, nullptr, seg);
+                     dt_bias, 0.f, nullptr, nullptr, nullptr, seg,
+                     FusedSched{0, 1, 0, nullptr, nullptr, nullptr});
 }
 
 namespace {
@@ -1312,29 +1368,77 @@ cudaError_t launch_chunk_split(const ChunkArgs& a, cudaStream_t s) {
     return err != cudaSuccess ? err : ferr;
 }
 
+// Schedule of the fused kernel: *seg_len = chunks per work item (0: one CTA per whole
+// sequence) and the cost in chunk steps.  With more sequences than SMs the last wave of whole
+// sequences leaves SMs idle; items of a few chunks spread the same work evenly, at about a
+// quarter chunk step per item for handing the state on.
+double fused_schedule(long long BH, long long N, long long S, int* seg_len) {
+    double best = (double)((BH + S - 1) / S) * (double)N;
+    *seg_len = 0;
+    if (BH <= S) return best;
+    for (long long L = N / 2; L >= 2; L /= 2) {
+        const long long items = (N + L - 1) / L * BH;
+        const double cost = (double)((items + S - 1) / S) * ((double)L + 0.25);
+        if (cost < 0.97 * best) {
+            best = cost;
+            *seg_len = (int)L;
+        }
+    }
+    return best;
+}
+
 cudaError_t launch_chunk_fused(const ChunkArgs& a, cudaStream_t s) {
-    const int BH = a.B * a.H;
+    const int BH = a.B * a.H, N = (a.T + C - 1) / C, nsm = sm_count();
     CUtensorMap m[4];
     if (!make_input_maps(a, m)) return cudaErrorInvalidValue;
     cudaError_t err = cudaFuncSetAttribute(kda_chunk_tc_kernel,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            (int)SMEM_BYTES);
     if (err != cudaSuccess) return err;
-    kda_chunk_tc_kernel<<<BH, NT, SMEM_BYTES, s>>>(
-        m[0], m[1], m[2], m[3], a.H, a.T, (const __nv_bfloat16*)a.beta, a.A_log, a.dt_bias, a.scale,
-        a.h0, (__nv_bfloat16*)a.out, a.hT);
-    count_launches(1);
-    return cudaGetLastError();
+    int L = 0;
+    fused_schedule(BH, N, nsm, &L);
+    if (L == 0) {  // one CTA per sequence
+        kda_chunk_tc_kernel<<<BH, NT, SMEM_BYTES, s>>>(
+            m[0], m[1], m[2], m[3], a.H, a.T, (const __nv_bfloat16*)a.beta, a.A_log, a.dt_bias,
+            a.scale, a.h0, (__nv_bfloat16*)a.out, a.hT,
+            FusedSched{BH, N, BH, nullptr, nullptr, nullptr});
+        count_launches(1);
+        return cudaGetLastError();
+    }
+    // items of L chunks taken in order by one CTA per SM: a counter and one flag per sequence
+    // (cleared here), and the state between segments in hT (or in scratch when hT is not wanted)
+    const int n_items = (N + L - 1) / L * BH;
+    const size_t flag_bytes = round_up(sizeof(unsigned) * (1 + (size_t)BH), 256);
+    const size_t bytes = flag_bytes + (a.hT ? 0 : (size_t)BH * KD * VD * sizeof(float));
+    void* p = nullptr;
+    if (cudaMallocAsync(&p, bytes, s) != cudaSuccess) {
+        cudaGetLastError();
+        return cudaErrorMemoryAllocation;
+    }
+    err = cudaMemsetAsync(p, 0, flag_bytes, s);
+    if (err == cudaSuccess) {
+        unsigned* w = static_cast<unsigned*>(p);
+        float* handoff = a.hT ? a.hT : reinterpret_cast<float*>(static_cast<uint8_t*>(p) + flag_bytes);
+        kda_chunk_tc_kernel<<<min(n_items, nsm), NT, SMEM_BYTES, s>>>(
+            m[0], m[1], m[2], m[3], a.H, a.T, (const __nv_bfloat16*)a.beta, a.A_log, a.dt_bias,
+            a.scale, a.h0, (__nv_bfloat16*)a.out, a.hT,
+            FusedSched{BH, L, n_items, reinterpret_cast<int*>(w), w + 1, handoff});
+        count_launches(1);
+        err = cudaGetLastError();
+    }
+    const cudaError_t ferr = cudaFreeAsync(p, s);
+    return err != cudaSuccess ? err : ferr;
 }
 
-// Which tensor-core form is faster: the fused kernel runs ceil(BH / SMs) waves of whole
-// sequences, the split form spreads all chunks over the SMs and adds a short sequential
-// carry (about a tenth of a fused chunk step) per chunk.
+// Which tensor-core form is faster: the fused kernel's schedule (above) against the split
+// form, which spreads all chunks over the SMs and adds a short sequential carry (about a tenth
+// of a fused chunk step) per chunk.
 bool prefer_split(const ChunkArgs& a) {
     const long long BH = (long long)a.B * a.H, N = (a.T + C - 1) / C, S = sm_count();
-    const long long fused = (BH + S - 1) / S * N * 10;
-    const long long split = (BH * N + S - 1) / S * 9 + (BH + S - 1) / S * N;
-    return split * 100 < fused * 85;
+    int L = 0;
+    const double fused = fused_schedule(BH, N, S, &L);
+    const double split = (double)((BH * N + S - 1) / S) * 0.9 + (double)((BH + S - 1) / S) * N * 0.1;
+    return split < 0.85 * fused;
 }
 
 }  // namespace

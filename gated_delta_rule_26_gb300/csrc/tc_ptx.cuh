@@ -62,6 +62,28 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
     }
 }
 
+// Flags between CTAs of one kernel (device scope): the writer makes its data visible
+// (__threadfence) before a release store; the reader's acquire load orders its later reads.
+__device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned* p) {
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_release_gpu(unsigned* p, unsigned v) {
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+// Wait until *flag >= target; gives up after `limit_ns` and returns false.
+__device__ __forceinline__ bool flag_wait_geq(const unsigned* flag, unsigned target,
+                                              uint64_t limit_ns = 2000000000ull) {
+    if (ld_acquire_gpu(flag) >= target) return true;
+    const uint64_t t0 = global_timer_ns();
+    for (;;) {
+        __nanosleep(200);
+        if (ld_acquire_gpu(flag) >= target) return true;
+        if (global_timer_ns() - t0 > limit_ns) return false;
+    }
+}
+
 // Named barriers for warp subsets (id 0 is the one __syncthreads uses).
 __device__ __forceinline__ void named_sync(uint32_t id, uint32_t nthreads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");

@@ -171,6 +171,35 @@ def test_tensor_core_forms_match_oracle(kda, form, B, H, T, seed, A_log_value):
     assert kda.device_status() == 0
 
 
+@pytest.mark.parametrize("want_hT", [True, False])
+def test_fused_persistent_schedule_is_bitwise_per_sequence(kda, want_hT):
+    # 160 sequences are more than the SMs: the fused kernel runs as one CTA per SM taking
+    # (segment, sequence) items and handing the state between segments; 80 sequences run one
+    # CTA per sequence.  The per-chunk arithmetic is the same, so every sequence's output and
+    # final state must be bit-identical between the two.
+    inp = inputs.make(2, 80, 512, 128, 128, chunk=64, dtype="bf16", seed=28, h0_std=0.1)
+    d = inp.to("cuda")
+    o, h = kda.chunk_forward(d.q, d.k, d.v, d.z, d.beta, d.A_log, d.dt_bias, inp.scale, d.h0, 64,
+                             form="fused", output_final_state=want_hT)
+    torch.cuda.synchronize()
+    assert kda.device_status() == 0
+    for b in range(2):
+        sl = lambda t: t[b:b + 1].contiguous()
+        ob, hb = kda.chunk_forward(sl(d.q), sl(d.k), sl(d.v), sl(d.z), sl(d.beta), d.A_log,
+                                   d.dt_bias, inp.scale, sl(d.h0), 64, form="fused")
+        torch.cuda.synchronize()
+        assert torch.equal(ob, o[b:b + 1])
+        if want_hT:
+            assert torch.equal(hb, h[b:b + 1])
+    # and against the oracle on a few sequences
+    pairs = [(0, 3), (1, 79)]
+    q, k, v, z, beta, A, dt, h0 = _sample_pairs(inp, pairs)
+    o_ref, h_ref = oracle.forward(q, k, v, z, beta, A, dt, inp.scale, h0, threads=2)
+    check("o", o[[0, 1], [3, 79]].unsqueeze(0), o_ref, "bf16")
+    if want_hT:
+        check("hT", h[[0, 1], [3, 79]].unsqueeze(0), h_ref, "bf16")
+
+
 def test_split_form_resume_equals_whole(kda):
     # chunk-aligned cut: the carry kernel starts the second call from the fp32 state the
     # first call left, which is the state the whole run carries at that chunk: bit-identical
