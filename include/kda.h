@@ -98,8 +98,14 @@ int kda_chunk_forward(const kda_dims* dims, kda_dtype io_dtype, const void* q, c
  * its two tensor-core forms (bf16 I/O, K = V = 128, chunk 64, T >= 1; anything else returns
  * KDA_ERR_UNSUPPORTED).  kda_chunk_forward picks between them by the shape; these exist to
  * run and compare each form on any shape.
- *   fused : one CTA per (b, h) walks its chunks with the state on chip; the whole forward is
- *           one kernel and reads each input once.
+ *   fused : the whole forward in one kernel that reads each input once, the state on chip.
+ *           With at most one sequence per SM, one CTA per (b, h) walks its chunks.  With more
+ *           sequences than SMs, one CTA per SM takes (segment, sequence) work items of a few
+ *           chunks in order and the fp32 state passes between a sequence's segments through
+ *           hT (or, when hT is NULL, a B*H*K*V*4-byte scratch buffer); a counter and one flag
+ *           per sequence (4*(B*H + 1) bytes) are cleared and freed on `stream` by the call
+ *           (cudaMallocAsync / cudaMemsetAsync / cudaFreeAsync; KDA_ERR_NO_MEMORY if the
+ *           allocation fails).
  *   split : the chunk-parallel WY form of kda-adjoint-2026-10-01 section 2 as two kernels.  A
  *           prep kernel spreads every chunk of every sequence over the GPU and writes, per
  *           chunk, the state-independent operands ([W^T | Q'^T], [U^T | U'^T], K~ =
