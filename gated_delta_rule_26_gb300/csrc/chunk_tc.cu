@@ -77,12 +77,13 @@ constexpr uint32_t LV_PB = 32768;   // level pair B operand, K-major 64 rows (16
 constexpr uint32_t LV_AF = 0;       // A fp32 [t][i] (16 KB, swizzled)       P3-P4
 constexpr uint32_t LV_MB = 16384;   // M bf16 K-major [t][i] (8 KB)          P3-P5
 constexpr uint32_t LV_TB = 24576;   // T bf16 K-major [t][i] (8 KB)          P4-P5
-constexpr uint32_t LV_QG = 0;       // Q Gamma, MN-major [t][c] (16 KB)      P5
-constexpr uint32_t LV_UT = 32768;   // U^T K-major [v][i] (16 KB)            P5
+constexpr uint32_t LV_QG = 32768;   // Q Gamma, MN-major [t][c] (16 KB)      P4-P5
+constexpr uint32_t LV_UT = 0;       // U^T K-major [v][i] (16 KB)            P5
 constexpr uint32_t LV_Z = 49152;    // z tile of the NEXT chunk (16 KB)      P5-P2
+constexpr uint32_t LV_TF = 49152;   // T fp32 [t][i] (16 KB, swizzled), in the z slot   P4
 constexpr uint32_t LV_DELTA = 16384;// Delta^T K-major [v][t] (16 KB)        C2-C3
-constexpr uint32_t LV_UPS = 0;      // prep kernel: U'^T staging, K-major [v][t] (16 KB)
-// K~ (K e^{G_last - G}, MN-major [t][c]) lives in the v-tile slot OFF_V from P5 to C3.
+constexpr uint32_t LV_UPS = 32768;  // prep kernel: U'^T staging, K-major [v][t] (16 KB)
+// K~ (K e^{G_last - G}, MN-major [t][c]) lives in the v-tile slot OFF_V from P4 to C3.
 // beta K Gamma and beta V (MN-major [t][.], 16 KB each) live in the A1 slot from P3 until
 // the W/U GEMM has read them; then A1 takes [W^T | Q'^T].
 constexpr uint32_t OFF_BKG = OFF_A1, OFF_BV = OFF_A1 + 16384;
@@ -392,37 +393,45 @@ __device__ __forceinline__ void chunk_loop(const CUtensorMap* tm_q, const CUtens
     // MN-major operand [c][v], this thread's columns [v0b, v0b + nv).  It comes from h0 (a
     // sequence's first segment) or from the handoff of the previous segment (read past L1:
     // another SM wrote it), and leaves to the handoff or to hT.
-    auto state_in = [&](size_t sbh, const float* src, int v0b, int nv) {
+    // 32 columns per call, every load issued before the first is used (L2 latency once)
+    auto state_in32 = [&](size_t sbh, const float* src, int v0b) {
         const int c = row;
-#pragma unroll 1
-        for (int v0 = v0b; v0 < v0b + nv; v0 += 16) {
-            float f[16];
+        float4 x[8];
 #pragma unroll
-            for (int j = 0; j < 16; j += 4) {
-                float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (src) x = __ldcg(reinterpret_cast<const float4*>(src + (sbh * KD + c) * VD + v0 + j));
-                f[j] = x.x; f[j + 1] = x.y; f[j + 2] = x.z; f[j + 3] = x.w;
-            }
+        for (int j = 0; j < 8; ++j)
+            x[j] = src ? __ldcg(reinterpret_cast<const float4*>(src + (sbh * KD + c) * VD + v0b + 4 * j))
+                       : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            float f[16];
             uint32_t r[16];
 #pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const float4 y = x[4 * h + j];
+                f[4 * j] = y.x; f[4 * j + 1] = y.y; f[4 * j + 2] = y.z; f[4 * j + 3] = y.w;
+            }
+#pragma unroll
             for (int j = 0; j < 16; ++j) r[j] = __float_as_uint(f[j]);
-            tc::tmem_st16(taddr(tmem, warp, TM_S + v0), r);
-            store16_mn(sm + OFF_S, c, v0, 16384, f);
+            tc::tmem_st16(taddr(tmem, warp, TM_S + v0b + 16 * h), r);
+            store16_mn(sm + OFF_S, c, v0b + 16 * h, 16384, f);
         }
         tc::tmem_st_wait();
     };
-    auto state_out = [&](size_t sbh, float* dst, int v0b, int nv) {
+    auto state_out32 = [&](size_t sbh, float* dst, int v0b) {
         const int c = row;
-#pragma unroll 1
-        for (int v0 = v0b; v0 < v0b + nv; v0 += 16) {
-            uint32_t d[16];
-            tc::tmem_ld16(taddr(tmem, warp, TM_S + v0), d);
-            tc::tmem_ld_wait();
+        uint32_t d0[16], d1[16];
+        tc::tmem_ld16(taddr(tmem, warp, TM_S + v0b), d0);
+        tc::tmem_ld16(taddr(tmem, warp, TM_S + v0b + 16), d1);
+        tc::tmem_ld_wait();
+        float* p = dst + (sbh * KD + c) * VD + v0b;
 #pragma unroll
-            for (int j = 0; j < 16; j += 4)
-                *reinterpret_cast<float4*>(dst + (sbh * KD + c) * VD + v0 + j) =
-                    make_float4(__uint_as_float(d[j]), __uint_as_float(d[j + 1]),
-                                __uint_as_float(d[j + 2]), __uint_as_float(d[j + 3]));
+        for (int j = 0; j < 16; j += 4) {
+            *reinterpret_cast<float4*>(p + j) =
+                make_float4(__uint_as_float(d0[j]), __uint_as_float(d0[j + 1]),
+                            __uint_as_float(d0[j + 2]), __uint_as_float(d0[j + 3]));
+            *reinterpret_cast<float4*>(p + 16 + j) =
+                make_float4(__uint_as_float(d1[j]), __uint_as_float(d1[j + 1]),
+                            __uint_as_float(d1[j + 2]), __uint_as_float(d1[j + 3]));
         }
     };
     if (!kSplit && cur_it < n_items) {  // the first item's initial state
@@ -430,7 +439,7 @@ __device__ __forceinline__ void chunk_loop(const CUtensorMap* tm_q, const CUtens
         bool ok = true;
         if (j0 > 0) ok = tid != 0 || tc::flag_wait_geq(fs.flags + item_bh(cur_it), (unsigned)j0);
         if (__syncthreads_or(!ok)) failed = true;
-        if (!failed) state_in(item_bh(cur_it), j0 > 0 ? fs.handoff : h0, 32 * part, 32);
+        if (!failed) state_in32(item_bh(cur_it), j0 > 0 ? fs.handoff : h0, 32 * part);
     }
 
     // Gate of item (gbh, gn) by warps GLO .. GLO + GW - 1 (named barrier 2): waits for its
@@ -684,7 +693,7 @@ __device__ __forceinline__ void chunk_loop(const CUtensorMap* tm_q, const CUtens
         // ---------------------------------------------------------------- P4: T = (I + A)^{-1}
         {
             const float* Af = reinterpret_cast<const float*>(sm + OFF_LVL + LV_AF);
-            float* Tf = reinterpret_cast<float*>(sm + OFF_V);  // the v tile is consumed
+            float* Tf = reinterpret_cast<float*>(sm + OFF_LVL + LV_TF);  // free until P5
             // Every A and T access below moves a 16-byte group (4 consecutive columns); the
             // XOR swizzle keeps the groups a warp touches in distinct banks.
             // (a) the four 16 x 16 diagonal blocks by forward substitution, one column each
@@ -728,6 +737,23 @@ __device__ __forceinline__ void chunk_loop(const CUtensorMap* tm_q, const CUtens
                     const int Cb = blk < 3 ? blk + 1 : (blk < 5 ? blk - 1 : 3);
                     const int t = 16 * R + (q >> 2), i = 16 * Cb + (q & 3) * 4;
                     *reinterpret_cast<float4*>(Tf + swz(t, i)) = make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+                // meanwhile the other warps build two operands that do not depend on T:
+                // Q Gamma -> LV_QG and K~ = K e^{G_last - G} -> the v-tile slot (MN-major [t][c])
+#pragma unroll 1
+                for (int item = tid - 64; item < C * 16; item += NT - 64) {
+                    const int t = item >> 4, c8 = item & 15;
+                    float qf[8], kf[8], g8[8], gl[8], o[8];
+                    unpack8(*reinterpret_cast<const uint4*>(sm + OFF_Q + t * 256 + c8 * 16), qf);
+                    unpack8(*reinterpret_cast<const uint4*>(sm + OFF_K + t * 256 + c8 * 16), kf);
+                    load8g(G2, t, c8, g8);
+                    load8g(G2, 63, c8, gl);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) o[j] = qf[j] * ex2(g8[j]);
+                    *reinterpret_cast<uint4*>(sm + OFF_LVL + LV_QG + mnmaj_off(t, c8 * 8, 8192)) = pack8(o);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) o[j] = kf[j] * ex2(gl[j] - g8[j]);
+                    *reinterpret_cast<uint4*>(sm + OFF_V + mnmaj_off(t, c8 * 8, 8192)) = pack8(o);
                 }
             }
             __syncthreads();
@@ -868,23 +894,6 @@ __device__ __forceinline__ void chunk_loop(const CUtensorMap* tm_q, const CUtens
                 tc::mma_bf16(tmem + TM_U, desc_mn(sb + OFF_BV, 8192, ks), b, IDESC_WU, ks > 0);
             }
             tc::mma_commit(&ms.bar_m0);
-        }
-        // while it runs: Q Gamma -> LV_QG and K~ = K e^{G_last - G} -> the v-tile slot (both
-        // MN-major [t][c]); neither region is read by this GEMM
-#pragma unroll
-        for (int ii = 0; ii < 2; ++ii) {
-            const int item = tid + NT * ii, t = item >> 4, c8 = item & 15;
-            float qf[8], kf[8], g8[8], gl[8], o[8];
-            unpack8(*reinterpret_cast<const uint4*>(sm + OFF_Q + t * 256 + c8 * 16), qf);
-            unpack8(*reinterpret_cast<const uint4*>(sm + OFF_K + t * 256 + c8 * 16), kf);
-            load8g(G2, t, c8, g8);
-            load8g(G2, 63, c8, gl);
-#pragma unroll
-            for (int j = 0; j < 8; ++j) o[j] = qf[j] * ex2(g8[j]);
-            *reinterpret_cast<uint4*>(sm + OFF_LVL + LV_QG + mnmaj_off(t, c8 * 8, 8192)) = pack8(o);
-#pragma unroll
-            for (int j = 0; j < 8; ++j) o[j] = kf[j] * ex2(gl[j] - g8[j]);
-            *reinterpret_cast<uint4*>(sm + OFF_V + mnmaj_off(t, c8 * 8, 8192)) = pack8(o);
         }
         KDA_WAIT(bar_m0, ph0);
         if (failed) break;
@@ -1108,7 +1117,10 @@ __device__ __forceinline__ void chunk_loop(const CUtensorMap* tm_q, const CUtens
                 if (!failed && last_of_item) {
                     const bool more = item_ne(it) < nchunks;
                     float* dst = more ? fs.handoff : hT;
-                    if (dst) state_out(bh, dst, 64 * half, 64);
+                    if (dst) {
+                        state_out32(bh, dst, 64 * half);
+                        state_out32(bh, dst, 64 * half + 32);
+                    }
                     if (more) __threadfence();
                     tc::fence_before_sync();
                     tc::named_sync(1, 256);
@@ -1119,7 +1131,10 @@ __device__ __forceinline__ void chunk_loop(const CUtensorMap* tm_q, const CUtens
                         bool ok = true;
                         if (nj > 0) ok = tid != 0 || tc::flag_wait_geq(fs.flags + nbh, (unsigned)nj);
                         if (tc::named_sync_or(1, 256, !ok)) failed = true;
-                        if (!failed) state_in(nbh, nj > 0 ? fs.handoff : h0, 64 * half, 64);
+                        if (!failed) {
+                            state_in32(nbh, nj > 0 ? fs.handoff : h0, 64 * half);
+                            state_in32(nbh, nj > 0 ? fs.handoff : h0, 64 * half + 32);
+                        }
                     }
                 }
             } else if (has_next) {
