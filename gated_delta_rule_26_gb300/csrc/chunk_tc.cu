@@ -83,7 +83,7 @@ constexpr uint32_t LV_Z = 49152;    // z tile of the NEXT chunk (16 KB)      P5-
 constexpr uint32_t LV_TF = 49152;   // T fp32 [t][i] (16 KB, swizzled), in the z slot   P4
 constexpr uint32_t LV_DELTA = 16384;// Delta^T K-major [v][t] (16 KB)        C2-C3
 constexpr uint32_t LV_UPS = 32768;  // prep kernel: U'^T staging, K-major [v][t] (16 KB)
-// K~ (K e^{G_last - G}, MN-major [t][c]) lives in the v-tile slot OFF_V from P4 to C3.
+// K~ (K e^{G_last - G}, MN-major [t][c]) lives in the v-tile slot OFF_V from P5 to C3.
 // beta K Gamma and beta V (MN-major [t][.], 16 KB each) live in the A1 slot from P3 until
 // the W/U GEMM has read them; then A1 takes [W^T | Q'^T].
 constexpr uint32_t OFF_BKG = OFF_A1, OFF_BV = OFF_A1 + 16384;
@@ -738,22 +738,17 @@ __device__ __forceinline__ void chunk_loop(const CUtensorMap* tm_q, const CUtens
                     const int t = 16 * R + (q >> 2), i = 16 * Cb + (q & 3) * 4;
                     *reinterpret_cast<float4*>(Tf + swz(t, i)) = make_float4(0.f, 0.f, 0.f, 0.f);
                 }
-                // meanwhile the other warps build two operands that do not depend on T:
-                // Q Gamma -> LV_QG and K~ = K e^{G_last - G} -> the v-tile slot (MN-major [t][c])
+                // meanwhile the other warps build Q Gamma -> LV_QG (MN-major [t][c]), which does
+                // not depend on T
 #pragma unroll 1
                 for (int item = tid - 64; item < C * 16; item += NT - 64) {
                     const int t = item >> 4, c8 = item & 15;
-                    float qf[8], kf[8], g8[8], gl[8], o[8];
+                    float qf[8], g8[8], o[8];
                     unpack8(*reinterpret_cast<const uint4*>(sm + OFF_Q + t * 256 + c8 * 16), qf);
-                    unpack8(*reinterpret_cast<const uint4*>(sm + OFF_K + t * 256 + c8 * 16), kf);
                     load8g(G2, t, c8, g8);
-                    load8g(G2, 63, c8, gl);
 #pragma unroll
                     for (int j = 0; j < 8; ++j) o[j] = qf[j] * ex2(g8[j]);
                     *reinterpret_cast<uint4*>(sm + OFF_LVL + LV_QG + mnmaj_off(t, c8 * 8, 8192)) = pack8(o);
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) o[j] = kf[j] * ex2(gl[j] - g8[j]);
-                    *reinterpret_cast<uint4*>(sm + OFF_V + mnmaj_off(t, c8 * 8, 8192)) = pack8(o);
                 }
             }
             __syncthreads();
@@ -894,6 +889,18 @@ __device__ __forceinline__ void chunk_loop(const CUtensorMap* tm_q, const CUtens
                 tc::mma_bf16(tmem + TM_U, desc_mn(sb + OFF_BV, 8192, ks), b, IDESC_WU, ks > 0);
             }
             tc::mma_commit(&ms.bar_m0);
+        }
+        // while it runs: K~ = K e^{G_last - G} -> the v-tile slot (MN-major [t][c])
+#pragma unroll
+        for (int ii = 0; ii < 2; ++ii) {
+            const int item = tid + NT * ii, t = item >> 4, c8 = item & 15;
+            float kf[8], g8[8], gl[8], o[8];
+            unpack8(*reinterpret_cast<const uint4*>(sm + OFF_K + t * 256 + c8 * 16), kf);
+            load8g(G2, t, c8, g8);
+            load8g(G2, 63, c8, gl);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) o[j] = kf[j] * ex2(gl[j] - g8[j]);
+            *reinterpret_cast<uint4*>(sm + OFF_V + mnmaj_off(t, c8 * 8, 8192)) = pack8(o);
         }
         KDA_WAIT(bar_m0, ph0);
         if (failed) break;
