@@ -200,6 +200,25 @@ def test_fused_persistent_schedule_is_bitwise_per_sequence(kda, want_hT):
         check("hT", h[[0, 1], [3, 79]].unsqueeze(0), h_ref, "bf16")
 
 
+def test_fused_persistent_schedule_ragged_and_in_place(kda):
+    # T = 300: five chunks, the last one partial, in items of two chunks (2, 2, 1); the state
+    # advanced in place (h0 and hT the same buffer).  Bit-identical to one CTA per sequence.
+    inp = inputs.make(2, 80, 300, 128, 128, chunk=64, dtype="bf16", seed=29, h0_std=0.1)
+    d = inp.to("cuda")
+    state = d.h0.clone()
+    o, h = kda.chunk_forward(d.q, d.k, d.v, d.z, d.beta, d.A_log, d.dt_bias, inp.scale, state, 64,
+                             hT=state, form="fused")
+    torch.cuda.synchronize()
+    assert kda.device_status() == 0 and h.data_ptr() == state.data_ptr()
+    for b in range(2):
+        sl = lambda t: t[b:b + 1].contiguous()
+        ob, hb = kda.chunk_forward(sl(d.q), sl(d.k), sl(d.v), sl(d.z), sl(d.beta), d.A_log,
+                                   d.dt_bias, inp.scale, sl(d.h0), 64, form="fused")
+        torch.cuda.synchronize()
+        assert torch.equal(ob, o[b:b + 1])
+        assert torch.equal(hb, state[b:b + 1])
+
+
 def test_split_form_resume_equals_whole(kda):
     # chunk-aligned cut: the carry kernel starts the second call from the fp32 state the
     # first call left, which is the state the whole run carries at that chunk: bit-identical
