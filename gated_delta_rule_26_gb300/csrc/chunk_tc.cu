@@ -1372,11 +1372,90 @@ cudaError_t run_chunk_split(const ChunkArgs& a, cudaStream_t s, void* scratch, s
     return cudaSuccess;
 }
 
+// The split form with the carry of segment i (one CTA per sequence, on a second stream)
+// running beside the prep of segment i + 1 (on the remaining SMs): two operand buffers,
+// events between the streams, `s` waits for all of it at the end.  For few sequences
+// (B*H at most half the SMs) and two or more segments.
+cudaError_t run_chunk_split_overlap(const ChunkArgs& a, cudaStream_t s, void* scratch, int seg_len) {
+    const int N = (a.T + C - 1) / C, BH = a.B * a.H, nsm = sm_count();
+    const size_t items_max = (size_t)BH * seg_len, buf_bytes = round_up(items_max * kItemBytes, 256);
+    CUtensorMap m[4], mwq[2], muu[2], mkt[2];
+    float* gl[2];
+    if (!make_input_maps(a, m)) return cudaErrorInvalidValue;
+    for (int b = 0; b < 2; ++b) {
+        uint8_t* wq = static_cast<uint8_t*>(scratch) + b * buf_bytes;
+        uint8_t* uu = wq + items_max * kItemWQ;
+        uint8_t* kt = uu + items_max * kItemUU;
+        gl[b] = reinterpret_cast<float*>(kt + items_max * kItemKT);
+        if (!make_map3(&mwq[b], wq, 64, 128, 2 * items_max, 128, 16384, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
+            !make_map3(&muu[b], uu, 64, 128, 2 * items_max, 128, 16384, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
+            !make_map3(&mkt[b], kt, 128, 64, items_max, 256, 16384, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B))
+            return cudaErrorInvalidValue;
+    }
+    float* h_state = a.hT ? a.hT
+                          : reinterpret_cast<float*>(static_cast<uint8_t*>(scratch) + 2 * buf_bytes);
+    cudaError_t err = cudaFuncSetAttribute(kda_chunk_prep_kernel,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           (int)SMEM_BYTES);
+    if (err != cudaSuccess) return err;
+    cudaStream_t s2 = nullptr;
+    cudaEvent_t ev[5] = {};  // fork, prep done [2], carry done [2]
+    if ((err = cudaStreamCreateWithFlags(&s2, cudaStreamNonBlocking)) != cudaSuccess) return err;
+    for (int e = 0; e < 5 && err == cudaSuccess; ++e)
+        err = cudaEventCreateWithFlags(&ev[e], cudaEventDisableTiming);
+    if (err == cudaSuccess) err = cudaEventRecord(ev[0], s);
+    if (err == cudaSuccess) err = cudaStreamWaitEvent(s2, ev[0], 0);
+    const int prep_grid = max(1, nsm - BH);  // leave one SM per carry CTA
+    for (int n0 = 0, i = 0; n0 < N && err == cudaSuccess; n0 += seg_len, ++i) {
+        const int b = i & 1, len = min(seg_len, N - n0), items = BH * len;
+        if (i >= 2) err = cudaStreamWaitEvent(s, ev[3 + b], 0);  // carry of segment i - 2 read buffer b
+        if (err != cudaSuccess) break;
+        kda_chunk_prep_kernel<<<min(items, prep_grid), NT, SMEM_BYTES, s>>>(
+            m[0], m[1], m[2], m[3], mwq[b], muu[b], mkt[b], a.H, a.T, (const __nv_bfloat16*)a.beta,
+            a.A_log, a.dt_bias, PrepSeg{n0, len, items, gl[b]});
+        count_launches(1);
+        if ((err = cudaGetLastError()) != cudaSuccess) break;
+        if ((err = cudaEventRecord(ev[1 + b], s)) != cudaSuccess) break;
+        if ((err = cudaStreamWaitEvent(s2, ev[1 + b], 0)) != cudaSuccess) break;
+        err = launch_chunk_carry(mwq[b], muu[b], mkt[b], gl[b], BH, a.T, n0, len, a.scale,
+                                 n0 == 0 ? a.h0 : h_state, (__nv_bfloat16*)a.out, h_state, s2);
+        if (err == cudaSuccess) err = cudaEventRecord(ev[3 + b], s2);
+    }
+    // join: `s` continues only after the last carry (also on failure, so nothing is left behind)
+    const cudaError_t jerr = cudaEventRecord(ev[0], s2) == cudaSuccess
+                                 ? cudaStreamWaitEvent(s, ev[0], 0)
+                                 : cudaErrorUnknown;
+    for (int e = 0; e < 5; ++e)
+        if (ev[e]) cudaEventDestroy(ev[e]);
+    cudaStreamDestroy(s2);
+    return err != cudaSuccess ? err : jerr;
+}
+
 // Scratch of the allocating split forward: at most this much per call (longer inputs are
 // processed in segments of chunks).
 constexpr size_t kSplitScratchCap = size_t(1) << 30;
 
 cudaError_t launch_chunk_split(const ChunkArgs& a, cudaStream_t s) {
+    const int N = (a.T + C - 1) / C, BH = a.B * a.H, nsm = sm_count();
+    // few sequences: two operand buffers and the carry beside the next segment's prep, in at
+    // least four segments
+    if (2 * BH <= nsm && N >= 4) {
+        int seg_len = split_segment_len(a, kSplitScratchCap / 2);  // per buffer (and the state)
+        seg_len = min(seg_len, (N + 3) / 4);
+        if (seg_len >= 1) {
+            const size_t items_max = (size_t)BH * seg_len;
+            const size_t bytes = 2 * round_up(items_max * kItemBytes, 256) +
+                                 (a.hT ? 0 : (size_t)BH * KD * VD * sizeof(float));
+            void* p = nullptr;
+            if (cudaMallocAsync(&p, bytes, s) != cudaSuccess) {
+                cudaGetLastError();
+                return cudaErrorMemoryAllocation;
+            }
+            const cudaError_t err = run_chunk_split_overlap(a, s, p, seg_len);
+            const cudaError_t ferr = cudaFreeAsync(p, s);
+            return err != cudaSuccess ? err : ferr;
+        }
+    }
     const int seg_len = split_segment_len(a, kSplitScratchCap);
     if (seg_len < 1) return cudaErrorMemoryAllocation;
     const size_t bytes = split_scratch_bytes(a, seg_len);
