@@ -1437,11 +1437,11 @@ constexpr size_t kSplitScratchCap = size_t(1) << 30;
 
 cudaError_t launch_chunk_split(const ChunkArgs& a, cudaStream_t s) {
     const int N = (a.T + C - 1) / C, BH = a.B * a.H, nsm = sm_count();
-    // few sequences: two operand buffers and the carry beside the next segment's prep, in at
-    // least four segments
+    // few sequences: two operand buffers and the carry beside the next segment's prep, in up to
+    // sixteen segments of at least 16 chunks (a short last carry)
     if (2 * BH <= nsm && N >= 4) {
         int seg_len = split_segment_len(a, kSplitScratchCap / 2);  // per buffer (and the state)
-        seg_len = min(seg_len, (N + 3) / 4);
+        seg_len = min(seg_len, max(16, (N + 15) / 16));
         if (seg_len >= 1) {
             const size_t items_max = (size_t)BH * seg_len;
             const size_t bytes = 2 * round_up(items_max * kItemBytes, 256) +

@@ -163,6 +163,7 @@ def test_scale_enters_only_the_read_on_gpu(kda):
     (1, 2, 200, 22, None),              # ragged last chunk
     (2, 3, 700, 23, math.log(16.0)),    # the strongest decay of the workloads' range
     (1, 4, 1024, 24, None),             # sixteen chunks of carry
+    (1, 4, 4096, 30, None),             # split form: four segments on two operand buffers
 ])
 def test_tensor_core_forms_match_oracle(kda, form, B, H, T, seed, A_log_value):
     inp = inputs.make(B, H, T, 128, 128, chunk=64, dtype="bf16", seed=seed, dt_std=0.1,
