@@ -115,7 +115,10 @@ int kda_chunk_forward(const kda_dims* dims, kda_dtype io_dtype, const void* q, c
  *           the fused form leaves most of the GPU idle.  The operands live in scratch that
  *           the call allocates and frees on `stream` (cudaMallocAsync / cudaFreeAsync, at most
  *           1 GiB: longer inputs run as consecutive segments of chunks); KDA_ERR_NO_MEMORY if
- *           that allocation fails.
+ *           that allocation fails.  With B*H at most half the SMs and four or more chunks,
+ *           the call runs each segment's carry on a second stream of its own, beside the next
+ *           segment's prep, with two operand buffers; that stream is created and destroyed
+ *           by the call and joined back into `stream` (events) before it returns.
  */
 int kda_chunk_forward_split(const kda_dims* dims, kda_dtype io_dtype, const void* q,
                             const void* k, const void* v, const void* z, const void* beta,
