@@ -1,47 +1,47 @@
 // chunk_tc.cu -- the KDA chunked forward on the 5th-generation tensor cores
 // (tcgen05 + TMEM + TMA), for bf16 I/O with K = V = 128 and chunk C = 64.
 //
-// One CTA (16 warps) owns one (b, h) sequence and walks its chunks in order.
-// The fp32 state S (K x V) lives in TMEM for the whole sequence; per chunk:
+// Two kernels share the chunk loop below.  The fused kernel keeps the fp32 state S (K x V)
+// in TMEM and walks the chunks of a sequence in order: one CTA (16 warps) per (b, h), or,
+// with more sequences than SMs, one CTA per SM taking (segment, sequence) work items and
+// handing the state between segments (FusedSched).  The prep kernel of the split form runs
+// P2-P5 for every (sequence, chunk) item in parallel and writes the state-independent
+// operands for the carry kernel (chunk_carry.cu).  Per chunk:
 //
-//   P1  TMA: q, k, z tiles (64 x 128 bf16 each) and the v tile, on two
-//       mbarriers; the next chunk's tiles are requested as soon as each slot is
-//       consumed (q, k, z during P5, v after C3).
-//   P2  gate g = -exp(A_log) softplus(z + dt_bias) and the in-chunk cumulative
-//       log decay G (kdafix-2026-10-02 "Fix 1"; kda-adjoint-2026-10-01 sec. 2);
-//       for chunk n+1 this runs on warps 8-15 while warps 0-7 do chunk n's C1-C3.
-//   P3  decay-folded scores  A[t,i] = beta_t sum_c k_tc k_ic e^{G_tc - G_ic}  (i < t)
-//       and M[t,i] = sum_c q_tc k_ic e^{G_tc - G_ic}  (i <= t) on the tensor cores.
-//       e^{G_t - G_i} cannot be split as e^{G_t} e^{-G_i} (e^{-G_i} overflows
-//       fp32 within a chunk when the decay is strong), so pairs are grouped by
-//       the level of the binary tree over the 64 tokens at which t and i part:
-//       at a level with half-width h, t in the upper half and i in the lower
-//       half of the same 2h-block share the reference r = last token of the
-//       lower half, e^{G_t - G_i} = e^{G_t - G_r} e^{G_r - G_i}, both factors
-//       <= 1.  Four levels (h = 32, 16, 8, 4) are four GEMMs of scaled operands
-//       (M = 128: k rows then q rows; N = 64; K = 128); pairs inside a 4-token
-//       block take the exact pairwise exponential on CUDA cores.
-//   P4  T = (I + A)^{-1}: 16 x 16 diagonal blocks by forward substitution,
-//       then two block merges (16 -> 32 -> 64, T_21 = -T_22 A_21 T_11), fp32 on
-//       CUDA cores.
-//   P5  W^T = (diag(beta) K Gamma)^T T^T and U^T = (diag(beta) V)^T T^T  (tcgen05),
-//       then Q'^T = (Q Gamma)^T I - W^T M^T (identity and negated-B MMAs) and
-//       U'^T = U^T M^T  (tcgen05), so that
-//       o = scale (Q' S + U') and Delta = U - W S both come from ONE product with S.
-//   C1  D = S^T [W^T | Q'^T] = [(W S)^T | (Q' S)^T]  (M = 128 value channels,
-//       N = 128, K = 128; S as bf16 operand).  Before it, the fp32 state in
-//       TMEM is scaled by Gamma_last (row c by e^{G_last,c}).
-//   C2  from TMEM, one value channel per thread: Delta^T = U^T - (W S)^T and
-//       o = scale ((Q' S)^T + U'^T)^T -> bf16 to HBM.
-//   C3  S += (K * e^{G_last - G})^T Delta   accumulated in TMEM in fp32
-//       (the carry with a single exponential of the log-space difference,
-//       kda-adjoint-2026-10-01 sections 2 and 5b), then S -> bf16 operand.
+//   P1  TMA: q, k, z tiles (64 x 128 bf16 each) and the v tile, on two mbarriers; the
+//       next chunk's tiles are requested as soon as each slot is consumed (q, k, z in
+//       P5, v after C3).
+//   P2  gate g = -exp(A_log) softplus(z + dt_bias) and the in-chunk cumulative log decay
+//       G (kdafix-2026-10-02 "Fix 1"; kda-adjoint-2026-10-01 sec. 2), and the pairs
+//       inside 4-token blocks (exact pairwise exponential, CUDA cores); in the fused
+//       kernel warps 8-15 do both for chunk n+1 while warps 0-7 do chunk n's C1-C3.
+//   P3  decay-folded scores  A[t,i] = beta_t sum_c k_tc k_ic e^{G_tc - G_ic}  (i < t) and
+//       M[t,i] = sum_c q_tc k_ic e^{G_tc - G_ic}  (i <= t).  e^{G_t - G_i} cannot be split
+//       as e^{G_t} e^{-G_i} (e^{-G_i} overflows fp32 within a chunk when the decay is
+//       strong), so pairs are grouped by the level of the binary tree over the 64 tokens
+//       at which t and i part: at half-width h, t in the upper half and i in the lower half
+//       of one 2h-block share the reference r = last token of the lower half, and
+//       e^{G_t - G_i} = e^{G_t - G_r} e^{G_r - G_i} with both factors <= 1.  Levels
+//       h = 32, 16, 8, 4 go two per tcgen05 GEMM (each level's upper k and q rows against
+//       its lower k rows, tokens in rank order); an epilogue scatters them to A and M.
+//   P4  T = (I + A)^{-1}: 16 x 16 diagonal blocks by forward substitution, then two
+//       block merges (16 -> 32 -> 64, T_21 = -T_22 A_21 T_11), fp32 on CUDA cores.
+//   P5  W^T = (diag(beta) K Gamma)^T T^T and U^T = (diag(beta) V)^T T^T  (tcgen05), then
+//       Q'^T = (Q Gamma)^T I - W^T M^T (identity and negated-B MMAs) and U'^T = U^T M^T,
+//       so that o = scale (Q' S + U') and Delta = U - W S come from ONE product with S.
+//   C1  D = S^T [W^T | Q'^T] = [(W S)^T | (Q' S)^T]  (M = 128 value channels, N = 128,
+//       K = 128; S as bf16 operand).  Before it, the fp32 state in TMEM is scaled by
+//       Gamma_last (row c by e^{G_last,c}).
+//   C2  from TMEM, one value channel per thread: Delta^T = U^T - (W S)^T; then, while C3
+//       runs, o = scale ((Q' S)^T + U'^T)^T -> bf16 to HBM.
+//   C3  S += (K * e^{G_last - G})^T Delta   accumulated in TMEM in fp32 (the carry with a
+//       single exponential of the log-space difference, kda-adjoint-2026-10-01 sections 2
+//       and 5b), then S -> bf16 operand.
 //
-// Operand layouts are the tcgen05 canonical 128-byte-swizzled layouts, either
-// K-major (rows of 128 B along the contraction) or MN-major (rows of 128 B
-// along M/N); both are written directly by the threads that produce them.
-// Every mbarrier wait is bounded; on a timeout the CTA records it in
-// g_kda_tc_timeout, releases its TMEM and exits.
+// Operand layouts are the tcgen05 canonical 128-byte-swizzled layouts, either K-major
+// (rows of 128 B along the contraction) or MN-major (rows of 128 B along M/N); both are
+// written directly by the threads that produce them.  Every mbarrier and flag wait is
+// bounded; on a timeout the CTA records it in g_kda_tc_timeout, releases its TMEM and exits.
 #include <cuda.h>
 #include <stddef.h>
 
@@ -561,7 +561,7 @@ __device__ __forceinline__ void chunk_loop(const CUtensorMap* tm_q, const CUtens
         size_t nbh = has_next ? item_bh(nxt_it) : bh;
         int nt0 = has_next ? (last_of_item ? item_nb(nxt_it) : cur_n + 1) * C : t0;
         // ---------------------------------------------------------------- P3: levels 32, 16
-        // one GEMM per pair of levels; the first pair's runs under the 4-token blocks
+        // one GEMM per pair of levels; the first pair's runs under the next phase
         LevelItems items;
         load_level_items(sm, tid, items);
         build_level(sm, 0, tid, items);
