@@ -247,9 +247,11 @@ def test_split_form_run_twice_is_bitwise_identical(kda):
     assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
 
 
-def test_split_form_without_final_state(kda):
-    # no hT: the carry keeps its state in the call's own scratch
-    inp = inputs.make(1, 3, 260, 128, 128, chunk=64, dtype="bf16", seed=27, h0_std=0.1)
+@pytest.mark.parametrize("T", [260, 2100])
+def test_split_form_without_final_state(kda, T):
+    # no hT: the carry keeps its state in the call's own scratch (T = 2100: three segments
+    # of the overlapped form, the state passing between them through that scratch)
+    inp = inputs.make(1, 3, T, 128, 128, chunk=64, dtype="bf16", seed=27, h0_std=0.1)
     run_and_compare(kda, inp, want_hT=False, form="split")
 
 
