@@ -12,6 +12,12 @@ by step:
   u = v - S^T k, S <- S + beta k u^T, o = S^T (scale q)
   (kdafix-2026-10-02, "Fix 2 -- read scale": scale folded into q, read only).
 * ``forward``    -- gate + recurrence from raw inputs, threaded over (b, h).
+* ``backward``   -- the gradients of ``forward``'s outputs' adjoints with respect to
+  every input, by reverse-mode differentiation of the same steps token by token
+  (kda-adjoint-2026-10-01: the backward and its gradients dq, dk, dv, dg, dbeta and
+  the state gradient).  Pinned by ``jvp`` below and by central differences.
+* ``jvp``        -- forward-mode derivative (tangent propagation) of the same forward,
+  written separately in numpy: the directional derivative of <d_o, o> + <dhT, hT>.
 * ``chunked.chunked_wy`` -- an independent f64 chunked (WY) evaluation of the
   same function, used to check that the chunked and recurrent forms agree
   (kda-adjoint-2026-10-01, section 2: carry with decay_last = exp(G_last - G)).
@@ -68,6 +74,9 @@ def _load():
             lib.kda_oracle_forward_range.argtypes = [i, i, i, i, i, _D, _D, _D, _D, _D, _D, _D,
                                                      ctypes.c_double, _D, _D, _D, i, i]
             lib.kda_oracle_forward_range.restype = None
+            lib.kda_oracle_backward_range.argtypes = [i, i, i, i, i] + [_D] * 7 + [
+                ctypes.c_double] + [_D] * 11 + [i, i, i]
+            lib.kda_oracle_backward_range.restype = None
             _lib = lib
     return _lib
 
@@ -161,3 +170,84 @@ def _run_ranges(fn, n, threads):
         return
     with ThreadPoolExecutor(max_workers=len(ranges)) as ex:
         list(ex.map(fn, ranges))
+
+
+def backward(q, k, v, z, beta, A_log, dt_bias, scale, h0, d_o, dhT=None, threads: int = 1,
+             mutant: int = 0) -> dict:
+    """Gradients of L (with dL/do = d_o and dL/dhT = dhT) with respect to every input.
+
+    Returns float64 arrays: dq, dk, dz (B,H,T,K), dv (B,H,T,V), dbeta (B,H,T), dA_log (H),
+    ddt_bias (H,K) and dh0 (B,H,K,V) (the gradient with respect to the initial state, a zero
+    state when h0 is None).  `mutant` plants a known mistake (tests only).
+    """
+    q, k, v, z, beta, A_log, dt_bias, h0, d_o, dhT = (
+        f64(a) for a in (q, k, v, z, beta, A_log, dt_bias, h0, d_o, dhT))
+    B, H, T, K, V = _dims(q, v)
+    assert k.shape == q.shape and z.shape == q.shape and beta.shape == (B, H, T)
+    assert A_log.shape == (H,) and dt_bias.shape == (H, K) and d_o.shape == v.shape
+    for s_ in (h0, dhT):
+        assert s_ is None or s_.shape == (B, H, K, V)
+    out = {n: np.zeros(q.shape) for n in ("dq", "dk", "dz")}
+    out["dv"] = np.zeros(v.shape)
+    out["dbeta"] = np.zeros((B, H, T))
+    out["dh0"] = np.zeros((B, H, K, V))
+    dA_part = np.zeros((B, H))
+    ddt_part = np.zeros((B, H, K))
+    lib = _load()
+
+    def run(r):
+        lib.kda_oracle_backward_range(
+            B, H, T, K, V, _p(q), _p(k), _p(v), _p(z), _p(beta), _p(A_log), _p(dt_bias),
+            float(scale), _p(h0), _p(d_o), _p(dhT), _p(out["dq"]), _p(out["dk"]), _p(out["dv"]),
+            _p(out["dz"]), _p(out["dbeta"]), _p(dA_part), _p(ddt_part), _p(out["dh0"]),
+            int(mutant), r[0], r[1])
+
+    _run_ranges(run, B * H, threads)
+    out["dA_log"] = dA_part.sum(axis=0)
+    out["ddt_bias"] = ddt_part.sum(axis=0)
+    return out
+
+
+def jvp(q, k, v, z, beta, A_log, dt_bias, scale, h0, d_o, dhT, tangents: dict) -> float:
+    """Directional derivative of <d_o, o> + <dhT, hT> along `tangents` (forward mode).
+
+    `tangents` maps input names (q, k, v, z, beta, A_log, dt_bias, h0) to arrays of the
+    inputs' shapes (missing = 0).  Every forward step is carried as a (value, tangent) pair
+    with the product rule; this shares nothing with ``backward``.
+    """
+    q, k, v, z, beta, A_log, dt_bias, h0, d_o, dhT = (
+        f64(a) for a in (q, k, v, z, beta, A_log, dt_bias, h0, d_o, dhT))
+    B, H, T, K, V = _dims(q, v)
+    tg = {n: (np.zeros_like(x) if tangents.get(n) is None else f64(tangents[n]))
+          for n, x in (("q", q), ("k", k), ("v", v), ("z", z), ("beta", beta),
+                       ("A_log", A_log), ("dt_bias", dt_bias))}
+    S = np.zeros((B, H, K, V)) if h0 is None else h0.copy()
+    dS_ = np.zeros((B, H, K, V)) if tangents.get("h0") is None else f64(tangents["h0"]).copy()
+    x = z + dt_bias[None, :, None, :]
+    dx = tg["z"] + tg["dt_bias"][None, :, None, :]
+    sp = np.maximum(x, 0.0) + np.log1p(np.exp(-np.abs(x)))
+    sig = np.where(x >= 0, 1.0 / (1.0 + np.exp(-np.abs(x))), np.exp(-np.abs(x)) / (1.0 + np.exp(-np.abs(x))))
+    m = np.exp(A_log)[None, :, None, None]
+    dm = (np.exp(A_log) * tg["A_log"])[None, :, None, None]
+    g = -m * sp
+    dg = -dm * sp - m * sig * dx
+    a = np.exp(g)
+    da = a * dg
+    total = 0.0
+    for t in range(T):
+        at, dat = a[:, :, t, :, None], da[:, :, t, :, None]
+        kt, dkt = k[:, :, t], tg["k"][:, :, t]
+        Sd = at * S
+        dSd = dat * S + at * dS_
+        u = v[:, :, t] - np.einsum("bhcj,bhc->bhj", Sd, kt)
+        du = tg["v"][:, :, t] - np.einsum("bhcj,bhc->bhj", dSd, kt) - np.einsum("bhcj,bhc->bhj", Sd, dkt)
+        bt, dbt = beta[:, :, t, None, None], tg["beta"][:, :, t, None, None]
+        S = Sd + bt * kt[..., None] * u[:, :, None, :]
+        dS_ = (dSd + dbt * kt[..., None] * u[:, :, None, :] + bt * dkt[..., None] * u[:, :, None, :]
+               + bt * kt[..., None] * du[:, :, None, :])
+        do_t = scale * (np.einsum("bhcj,bhc->bhj", dS_, q[:, :, t])
+                        + np.einsum("bhcj,bhc->bhj", S, tg["q"][:, :, t]))
+        total += float(np.sum(d_o[:, :, t] * do_t))
+    if dhT is not None:
+        total += float(np.sum(dhT * dS_))
+    return total
