@@ -199,6 +199,32 @@ int kda_fused_recurrent(const kda_dims* dims, kda_dtype io_dtype, const void* q,
     return from_cuda(kda::launch_recurrent(a, dims->T, (cudaStream_t)stream));
 }
 
+int kda_chunk_backward(const kda_dims* dims, kda_dtype io_dtype, const void* q, const void* k,
+                       const void* v, const void* z, const void* beta, const float* A_log,
+                       const float* dt_bias, float scale, const float* h0, const void* d_o,
+                       const float* dhT, float* dq, float* dk, float* dv, float* dz,
+                       float* dbeta, float* dA_log, float* ddt_bias, float* dh0,
+                       kda_stream_t stream) {
+    int st = check_dims(dims, true);
+    if (st) return st;
+    if (!dtype_ok(io_dtype)) return KDA_ERR_INVALID_ARG;
+    if (dims->T > 0) {
+        st = check_ptrs({q, k, v, z, d_o, dq, dk, dv, dz}, {h0, dhT, dh0}, {beta}, io_bytes(io_dtype));
+        if (!st) st = check_ptrs({}, {}, {A_log, dt_bias, dbeta, dA_log, ddt_bias}, 4);
+    } else {
+        st = check_ptrs({}, {h0, dhT, dh0}, {A_log, dt_bias, dA_log, ddt_bias}, 4);
+    }
+    if (st) return st;
+    kda::BwdLaunch L{dims->B, dims->H, dims->T, dims->K, dims->V, io_dtype, q, k, v, z, beta, d_o,
+                     A_log, dt_bias, h0, dhT, scale, dq, dk, dv, dz, dbeta, dA_log, ddt_bias, dh0};
+    const cudaError_t e = kda::launch_chunk_backward(L, (cudaStream_t)stream);
+    if (e == cudaErrorMemoryAllocation) {
+        (void)cudaGetLastError();
+        return KDA_ERR_NO_MEMORY;
+    }
+    return from_cuda(e);
+}
+
 int kda_device_status(kda_stream_t stream) {
     int timed_out = 0;
     int carry_timed_out = 0;

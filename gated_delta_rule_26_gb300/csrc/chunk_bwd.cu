@@ -1,0 +1,608 @@
+// chunk_bwd.cu -- the backward of the KDA forward: from dL/do and dL/dhT, the gradients of
+// q, k, v, z, beta, A_log, dt_bias and h0 (the kda-adjoint-2026-10-01 page names this
+// backward and its gradients dq, dk, dv, dg, dbeta and the state gradient; each step below
+// is the chain rule applied to the chunked form of the forward).
+//
+// One CTA (512 threads) per (b, h), fp32 throughout, chunks of 16 tokens.  Phase 1 walks
+// the chunks forward and keeps the state entering each chunk in a scratch buffer.  Phase 2
+// walks them in reverse with dS, the adjoint of the state leaving the chunk.  Per chunk,
+// with S the state entering it, G the in-chunk cumulative log decay, Gamma = e^G,
+// gamma = e^{G_last}, Kg = K Gamma, Qg = Q Gamma, Kt = K e^{G_last - G},
+// A'[t,i] = sum_c k_tc k_ic e^{G_tc - G_ic} (i < t), M[t,i] = sum_c q_tc k_ic e^{G_tc - G_ic}
+// (i <= t), T = (I + diag(beta) A')^{-1}, R = V - Kg S, Delta = T diag(beta) R, the forward is
+//     o = scale (Qg S + M Delta),   S_out = diag(gamma) S + Kt^T Delta,
+// and the adjoints are, in order:
+//     dDelta = Kt dS + scale M^T dO            dY = T^T dDelta
+//     dKt = Delta dS^T                         dgamma = rowsum(S .* dS)
+//     dQg = scale dO S^T                       P = dY S^T  (dKg = -diag(beta) P)
+//     dM = scale dO Delta^T (i <= t)           dB = -dY Delta^T (i < t), dA' = diag(beta) dB
+//     dbeta_t = sum_v R_tv dY_tv + sum_{i<t} A'_ti dB_ti          dV = diag(beta) dY
+//     the pairwise terms of dA' and dM into dq, dk and dG (exact e^{G_t - G_i} per pair),
+//     the Gamma factors into dq, dk and dG,
+//     dS <- diag(gamma) dS + scale Qg^T dO - Kg^T diag(beta) dY,
+// then dg = the reverse in-chunk cumulative sum of dG and the gate's own derivative:
+//     dz = dg (-e^{A_log}) sigmoid(z + dt_bias), ddt_bias += dz, dA_log += dg g.
+// The state and its adjoint sit in shared memory (XOR-swizzled so that both row and column
+// walks are free of bank conflicts); every per-(token, channel) gradient term is produced by
+// the same thread, so dq, dk and dG accumulate in registers.
+#include "common.cuh"
+
+namespace kda {
+namespace {
+
+constexpr int BC = 16;    // tokens per chunk
+constexpr int BNT = 512;  // threads per CTA
+constexpr int KM = 128, VM = 128;
+
+// shared memory map (floats)
+constexpr int O_S = 0;                    // S   [KM][VM], (c, v) at sw(c, v)
+constexpr int O_DS = O_S + KM * VM;       // dS  [KM][VM]
+constexpr int O_Q = O_DS + KM * VM;       // q   [BC][KM]
+constexpr int O_K = O_Q + BC * KM;        // k   [BC][KM]
+constexpr int O_G = O_K + BC * KM;        // G   [BC][KM] (natural log units)
+constexpr int O_KGT = O_G + BC * KM;      // Kg  [KM][BC]
+constexpr int O_QGT = O_KGT + BC * KM;    // Qg  [KM][BC]
+constexpr int O_KTT = O_QGT + BC * KM;    // Kt  [KM][BC]
+constexpr int O_R = O_KTT + BC * KM;      // v, then R = V - Kg S   [BC][VM]
+constexpr int O_DO = O_R + BC * VM;       // dO  [BC][VM]
+constexpr int O_DL = O_DO + BC * VM;      // Delta [BC][VM]
+constexpr int O_DY = O_DL + BC * VM;      // dDelta, then dY [BC][VM]
+constexpr int O_XT = O_DY + BC * VM;      // one C x V array transposed [VM][BC]; dG [BC][KM]
+constexpr int O_AP = O_XT + BC * VM;      // A'  [BC][BC]
+constexpr int O_TM = O_AP + BC * BC;      // T
+constexpr int O_MM = O_TM + BC * BC;      // M
+constexpr int O_DB = O_MM + BC * BC;      // dB
+constexpr int O_DM = O_DB + BC * BC;      // dM
+constexpr int O_BET = O_DM + BC * BC;     // beta [BC]
+constexpr int O_GAM = O_BET + BC;         // gamma [KM]
+constexpr int O_RED = O_GAM + KM;         // [4][KM] partial sums
+constexpr int SMEM_FLOATS = O_RED + 4 * KM;
+constexpr size_t BWD_SMEM_BYTES = sizeof(float) * SMEM_FLOATS;
+static_assert(BWD_SMEM_BYTES <= 232448, "backward shared memory");
+
+__device__ __forceinline__ int sw(int c, int v) { return c * VM + (v ^ (c & 31)); }
+
+template <typename IO>
+struct BwdArgs {
+    int H, T, K, V;
+    const IO *q, *k, *v, *z, *beta, *d_o;
+    const float *A_log, *dt_bias, *h0, *dhT;
+    float scale;
+    float *dq, *dk, *dv, *dz, *dbeta, *dh0;
+    float* ckpt;      // (B H, N, K, V): the state entering each chunk
+    float* dA_part;   // (B H)
+    float* ddt_part;  // (B H, K)
+};
+
+__device__ __forceinline__ float sigmoid_f32(float x) {
+    return x >= 0.f ? 1.f / (1.f + expf(-x)) : expf(x) / (1.f + expf(x));
+}
+
+template <typename IO>
+__global__ void __launch_bounds__(BNT, 1) kda_chunk_bwd_kernel(const BwdArgs<IO> a) {
+    extern __shared__ float4 smem_f4[];
+    float* sm = reinterpret_cast<float*>(smem_f4);
+    float* S = sm + O_S;
+    float* dS = sm + O_DS;
+    float* Qr = sm + O_Q;
+    float* Kr = sm + O_K;
+    float* Gc = sm + O_G;
+    float* KgT = sm + O_KGT;
+    float* QgT = sm + O_QGT;
+    float* KtT = sm + O_KTT;
+    float* Rv = sm + O_R;
+    float* dO = sm + O_DO;
+    float* Dl = sm + O_DL;
+    float* dY = sm + O_DY;
+    float* XT = sm + O_XT;
+    float* Ap = sm + O_AP;
+    float* Tm = sm + O_TM;
+    float* Mm = sm + O_MM;
+    float* dB = sm + O_DB;
+    float* dM = sm + O_DM;
+    float* bet = sm + O_BET;
+    float* gam = sm + O_GAM;
+    float* red = sm + O_RED;
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int K = a.K, V = a.V, T = a.T;
+    const size_t bh = blockIdx.x;
+    const int h = (int)(bh % a.H);
+    const int N = (T + BC - 1) / BC;
+    const float eA = expf(a.A_log[h]);
+    const size_t KV = (size_t)K * V;
+    // thread roles: (v or c) = tid % 128, quarter = tid / 128
+    const int col = tid & 127, qtr = tid >> 7;
+
+    // ---- the state entering the sequence
+    for (int j = 0; j < 32; ++j) {
+        const int c = qtr + 4 * j;
+        if (c < K && col < V) S[sw(c, col)] = a.h0 ? a.h0[bh * KV + (size_t)c * V + col] : 0.f;
+    }
+    __syncthreads();
+
+    // Load chunk n: q (optional), k, v (into R), dO (optional), beta, and G from z.
+    auto load_chunk = [&](int n, bool full) {
+        const int t0 = n * BC, cn = min(BC, T - t0);
+        for (int idx = tid; idx < BC * K; idx += BNT) {
+            const int t = idx / K, c = idx - t * K;
+            const bool in = t < cn;
+            const size_t gi = ((bh * T) + t0 + t) * K + c;
+            Kr[t * KM + c] = in ? ld_io(a.k + gi) : 0.f;
+            if (full) Qr[t * KM + c] = in ? ld_io(a.q + gi) : 0.f;
+            Gc[t * KM + c] = in ? kda_log_decay(ld_io(a.z + gi), a.dt_bias[(size_t)h * K + c], eA) : 0.f;
+        }
+        for (int idx = tid; idx < BC * V; idx += BNT) {
+            const int t = idx / V, vv = idx - t * V;
+            const bool in = t < cn;
+            const size_t gi = ((bh * T) + t0 + t) * V + vv;
+            Rv[t * VM + vv] = in ? ld_io(a.v + gi) : 0.f;
+            if (full) dO[t * VM + vv] = in ? ld_io(a.d_o + gi) : 0.f;
+        }
+        if (tid < BC) bet[tid] = tid < cn ? ld_io(a.beta + bh * T + t0 + tid) : 0.f;
+        __syncthreads();
+        if (tid < K) {  // in-chunk cumulative sum of the log decay
+            float run = 0.f;
+            for (int t = 0; t < BC; ++t) {
+                run += Gc[t * KM + tid];
+                Gc[t * KM + tid] = run;
+            }
+            gam[tid] = expf(run);
+        }
+        __syncthreads();
+        // the decay-scaled operands, channel-major
+        for (int idx = tid; idx < BC * K; idx += BNT) {
+            const int c = idx >> 4, t = idx & 15;
+            const float g = Gc[t * KM + c], gl = Gc[(BC - 1) * KM + c];
+            const float kk = Kr[t * KM + c];
+            KgT[c * BC + t] = kk * expf(g);
+            KtT[c * BC + t] = kk * expf(gl - g);
+            if (full) QgT[c * BC + t] = Qr[t * KM + c] * expf(g);
+        }
+        // A' (i < t) and M (i <= t): warp per pair, lanes over channels (exact pairwise decay)
+        for (int e = tid; e < BC * BC; e += BNT) {
+            Ap[e] = 0.f;
+            if (full) Mm[e] = 0.f;
+        }
+        __syncthreads();
+        int p = 0;
+        for (int t = 0; t < BC; ++t)
+            for (int i = 0; i <= t; ++i, ++p) {
+                if ((p & 15) != warp) continue;
+                if (i == t && !full) continue;
+                float sa = 0.f, sq = 0.f;
+                for (int c = lane; c < K; c += 32) {
+                    const float E = __expf(Gc[t * KM + c] - Gc[i * KM + c]);
+                    const float kiE = Kr[i * KM + c] * E;
+                    sa = fmaf(Kr[t * KM + c], kiE, sa);
+                    if (full) sq = fmaf(Qr[t * KM + c], kiE, sq);
+                }
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) {
+                    sa += __shfl_xor_sync(0xffffffffu, sa, off);
+                    sq += __shfl_xor_sync(0xffffffffu, sq, off);
+                }
+                if (lane == 0) {
+                    if (i < t) Ap[t * BC + i] = sa;
+                    if (full) Mm[t * BC + i] = sq;
+                }
+            }
+        __syncthreads();
+        // T = (I + diag(beta) A')^{-1} by forward substitution, one column per thread
+        if (tid < BC) {
+            const int j = tid;
+            float x[BC];
+#pragma unroll
+            for (int t = 0; t < BC; ++t) {
+                float acc = 0.f;
+#pragma unroll
+                for (int i = 0; i < t; ++i) acc = fmaf(Ap[t * BC + i], x[i], acc);
+                x[t] = (t == j ? 1.f : 0.f) - bet[t] * acc;
+                Tm[t * BC + j] = x[t];
+            }
+        }
+        // R = V - Kg S: thread (v = col, tokens 4 qtr ..)
+        if (col < V) {
+            float acc[4] = {0.f, 0.f, 0.f, 0.f};
+            for (int c = 0; c < K; ++c) {
+                const float s = S[sw(c, col)];
+                const float4 kg = *reinterpret_cast<const float4*>(KgT + c * BC + 4 * qtr);
+                acc[0] = fmaf(kg.x, s, acc[0]);
+                acc[1] = fmaf(kg.y, s, acc[1]);
+                acc[2] = fmaf(kg.z, s, acc[2]);
+                acc[3] = fmaf(kg.w, s, acc[3]);
+            }
+#pragma unroll
+            for (int r = 0; r < 4; ++r) Rv[(4 * qtr + r) * VM + col] -= acc[r];
+        }
+        __syncthreads();
+        // Delta = T diag(beta) R
+        if (col < V) {
+            float rb[BC];
+#pragma unroll
+            for (int i = 0; i < BC; ++i) rb[i] = bet[i] * Rv[i * VM + col];
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                const int t = 4 * qtr + r;
+                float acc = 0.f;
+#pragma unroll
+                for (int i = 0; i < BC; ++i)
+                    if (i <= t) acc = fmaf(Tm[t * BC + i], rb[i], acc);
+                Dl[t * VM + col] = acc;
+            }
+        }
+        __syncthreads();
+    };
+
+    // ======================================================= phase 1: chunk states forward
+    for (int n = 0; n < N; ++n) {
+        float* ck = a.ckpt + (bh * N + n) * KV;
+        for (int j = 0; j < 32; ++j) {
+            const int c = qtr + 4 * j;
+            if (c < K && col < V) ck[(size_t)c * V + col] = S[sw(c, col)];
+        }
+        load_chunk(n, false);
+        // S <- diag(gamma) S + Kt^T Delta: thread (v = col, channels qtr + 4 j)
+        if (col < V) {
+            float d[BC];
+#pragma unroll
+            for (int t = 0; t < BC; ++t) d[t] = Dl[t * VM + col];
+            for (int j = 0; j < 32; ++j) {
+                const int c = qtr + 4 * j;
+                if (c >= K) break;
+                const float4* kt = reinterpret_cast<const float4*>(KtT + c * BC);
+                float acc = S[sw(c, col)] * gam[c];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const float4 x = kt[u];
+                    acc = fmaf(x.x, d[4 * u], acc);
+                    acc = fmaf(x.y, d[4 * u + 1], acc);
+                    acc = fmaf(x.z, d[4 * u + 2], acc);
+                    acc = fmaf(x.w, d[4 * u + 3], acc);
+                }
+                S[sw(c, col)] = acc;
+            }
+        }
+        __syncthreads();
+    }
+
+    // ======================================================= phase 2: reverse
+    for (int j = 0; j < 32; ++j) {
+        const int c = qtr + 4 * j;
+        if (c < K && col < V) dS[sw(c, col)] = a.dhT ? a.dhT[bh * KV + (size_t)c * V + col] : 0.f;
+    }
+    float dA_acc = 0.f, ddt_acc = 0.f;  // this thread's channel col, tokens of quarter qtr
+    // Transposed copy of a [BC][VM] array into XT ([VM][BC]).
+    auto transpose_cv = [&](const float* src) {
+        for (int idx = tid; idx < BC * V; idx += BNT) {
+            const int vv = idx >> 4, t = idx & 15;
+            XT[vv * BC + t] = src[t * VM + vv];
+        }
+    };
+    // out[r] = sum_v XT[v][4 qtr + r] M[c][v] for this thread's channel c = col (M = S or dS).
+    auto contract_v = [&](const float* Mat, float (&out)[4]) {
+        out[0] = out[1] = out[2] = out[3] = 0.f;
+        for (int vv = 0; vv < V; ++vv) {
+            const float m = Mat[sw(col, vv)];
+            const float4 x = *reinterpret_cast<const float4*>(XT + vv * BC + 4 * qtr);
+            out[0] = fmaf(x.x, m, out[0]);
+            out[1] = fmaf(x.y, m, out[1]);
+            out[2] = fmaf(x.z, m, out[2]);
+            out[3] = fmaf(x.w, m, out[3]);
+        }
+    };
+
+    for (int n = N - 1; n >= 0; --n) {
+        const int t0 = n * BC, cn = min(BC, T - t0);
+        const float* ck = a.ckpt + (bh * N + n) * KV;
+        for (int j = 0; j < 32; ++j) {
+            const int c = qtr + 4 * j;
+            if (c < K && col < V) S[sw(c, col)] = ck[(size_t)c * V + col];
+        }
+        __syncthreads();
+        load_chunk(n, true);  // ends with a barrier
+
+        // dDelta = Kt dS + scale M^T dO  -> dY buffer; and this thread's share of dgamma
+        if (col < V) {
+            float acc[4] = {0.f, 0.f, 0.f, 0.f};
+            for (int c = 0; c < K; ++c) {
+                const float s = dS[sw(c, col)];
+                const float4 kt = *reinterpret_cast<const float4*>(KtT + c * BC + 4 * qtr);
+                acc[0] = fmaf(kt.x, s, acc[0]);
+                acc[1] = fmaf(kt.y, s, acc[1]);
+                acc[2] = fmaf(kt.z, s, acc[2]);
+                acc[3] = fmaf(kt.w, s, acc[3]);
+            }
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                const int t = 4 * qtr + r;
+                float m = 0.f;
+                for (int s2 = t; s2 < BC; ++s2) m = fmaf(Mm[s2 * BC + t], dO[s2 * VM + col], m);
+                dY[t * VM + col] = acc[r] + a.scale * m;
+            }
+        }
+        if (col < K) {  // dgamma_c partial over the value quarter qtr, times gamma_c
+            float sacc = 0.f;
+            const int v0 = 32 * qtr;
+            for (int vv = v0; vv < min(V, v0 + 32); ++vv) sacc = fmaf(S[sw(col, vv)], dS[sw(col, vv)], sacc);
+            red[qtr * KM + col] = sacc * gam[col];
+        }
+        __syncthreads();
+        // dY = T^T dDelta (in place: the column is read into registers first)
+        {
+            float dd[BC];
+            if (col < V) {
+#pragma unroll
+                for (int t = 0; t < BC; ++t) dd[t] = dY[t * VM + col];
+            }
+            __syncthreads();
+            if (col < V) {
+#pragma unroll
+                for (int r = 0; r < 4; ++r) {
+                    const int i = 4 * qtr + r;
+                    float acc = 0.f;
+#pragma unroll
+                    for (int t = 0; t < BC; ++t)
+                        if (t >= i) acc = fmaf(Tm[t * BC + i], dd[t], acc);
+                    dY[i * VM + col] = acc;
+                }
+            }
+        }
+        // the contractions over v, thread (c = col, tokens 4 qtr + r)
+        float dq_r[4] = {0.f, 0.f, 0.f, 0.f}, dk_r[4] = {0.f, 0.f, 0.f, 0.f};
+        float dG_r[4] = {0.f, 0.f, 0.f, 0.f};
+        float dgl_part = 0.f;
+        transpose_cv(Dl);
+        __syncthreads();
+        if (col < K) {  // dKt = Delta dS^T
+            float x[4];
+            contract_v(dS, x);
+            const float gl = Gc[(BC - 1) * KM + col];
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                const int t = 4 * qtr + r;
+                const float eL = expf(gl - Gc[t * KM + col]);
+                const float kk = Kr[t * KM + col];
+                dk_r[r] += x[r] * eL;
+                dG_r[r] -= x[r] * kk * eL;
+                dgl_part += x[r] * kk * eL;
+            }
+        }
+        __syncthreads();
+        transpose_cv(dO);
+        __syncthreads();
+        if (col < K) {  // dQg = scale dO S^T
+            float x[4];
+            contract_v(S, x);
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                const int t = 4 * qtr + r;
+                const float Ga = expf(Gc[t * KM + col]);
+                const float dqg = a.scale * x[r];
+                dq_r[r] += dqg * Ga;
+                dG_r[r] += dqg * Qr[t * KM + col] * Ga;
+            }
+        }
+        __syncthreads();
+        transpose_cv(dY);
+        __syncthreads();
+        if (col < K) {  // P = dY S^T, dKg = -diag(beta) P
+            float x[4];
+            contract_v(S, x);
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                const int t = 4 * qtr + r;
+                const float Ga = expf(Gc[t * KM + col]);
+                const float dkg = -bet[t] * x[r];
+                dk_r[r] += dkg * Ga;
+                dG_r[r] += dkg * Kr[t * KM + col] * Ga;
+            }
+        }
+        // dM (i <= t) and dB (i < t): warp per pair, lanes over value columns
+        {
+            int p = 0;
+            for (int t = 0; t < BC; ++t)
+                for (int i = 0; i <= t; ++i, ++p) {
+                    if ((p & 15) != warp) continue;
+                    float sm_ = 0.f, sb = 0.f;
+                    for (int vv = lane; vv < V; vv += 32) {
+                        const float dl = Dl[i * VM + vv];
+                        sm_ = fmaf(dO[t * VM + vv], dl, sm_);
+                        sb = fmaf(dY[t * VM + vv], dl, sb);
+                    }
+#pragma unroll
+                    for (int off = 16; off > 0; off >>= 1) {
+                        sm_ += __shfl_xor_sync(0xffffffffu, sm_, off);
+                        sb += __shfl_xor_sync(0xffffffffu, sb, off);
+                    }
+                    if (lane == 0) {
+                        dM[t * BC + i] = a.scale * sm_;
+                        dB[t * BC + i] = i < t ? -sb : 0.f;
+                    }
+                }
+        }
+        __syncthreads();
+        // dbeta_t = sum_v R_tv dY_tv + sum_{i<t} A'_ti dB_ti  (warp t);  dV = diag(beta) dY
+        {
+            const int t = warp;
+            float s = 0.f;
+            for (int vv = lane; vv < V; vv += 32) s = fmaf(Rv[t * VM + vv], dY[t * VM + vv], s);
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+            if (lane == 0 && t < cn) {
+                for (int i = 0; i < t; ++i) s = fmaf(Ap[t * BC + i], dB[t * BC + i], s);
+                a.dbeta[bh * T + t0 + t] = s;
+            }
+        }
+        for (int idx = tid; idx < cn * V; idx += BNT) {
+            const int t = idx / V, vv = idx - t * V;
+            a.dv[((bh * T) + t0 + t) * V + vv] = bet[t] * dY[t * VM + vv];
+        }
+        // pairwise terms of dA' = diag(beta) dB and dM, thread (c = col, tokens 4 qtr + r)
+        if (col < K) {
+            const int c = col;
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                const int t = 4 * qtr + r;
+                const float gt = Gc[t * KM + c], kt = Kr[t * KM + c], qt = Qr[t * KM + c];
+                float rowA = 0.f, rowM = 0.f, colA = 0.f, colM = 0.f;
+                for (int i = 0; i <= t; ++i) {  // t as the row (later) token
+                    const float kiE = Kr[i * KM + c] * __expf(gt - Gc[i * KM + c]);
+                    rowM = fmaf(dM[t * BC + i], kiE, rowM);
+                    if (i < t) rowA = fmaf(bet[t] * dB[t * BC + i], kiE, rowA);
+                }
+                for (int s2 = t; s2 < BC; ++s2) {  // t as the column (earlier) token
+                    const float E = __expf(Gc[s2 * KM + c] - gt);
+                    colM = fmaf(dM[s2 * BC + t], Qr[s2 * KM + c] * E, colM);
+                    if (s2 > t) colA = fmaf(bet[s2] * dB[s2 * BC + t], Kr[s2 * KM + c] * E, colA);
+                }
+                dq_r[r] += rowM;
+                dk_r[r] += rowA + colA + colM;
+                dG_r[r] += kt * rowA + qt * rowM - kt * (colA + colM);
+            }
+        }
+        // dS <- diag(gamma) dS + scale Qg^T dO - Kg^T diag(beta) dY  (thread (v = col, c = qtr + 4 j))
+        if (col < V) {
+            float dov[BC], dyv[BC];
+#pragma unroll
+            for (int t = 0; t < BC; ++t) {
+                dov[t] = a.scale * dO[t * VM + col];
+                dyv[t] = bet[t] * dY[t * VM + col];
+            }
+            for (int j = 0; j < 32; ++j) {
+                const int c = qtr + 4 * j;
+                if (c >= K) break;
+                const float4* qg = reinterpret_cast<const float4*>(QgT + c * BC);
+                const float4* kg = reinterpret_cast<const float4*>(KgT + c * BC);
+                float acc = dS[sw(c, col)] * gam[c];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const float4 x = qg[u], y = kg[u];
+                    acc = fmaf(x.x, dov[4 * u], acc);
+                    acc = fmaf(x.y, dov[4 * u + 1], acc);
+                    acc = fmaf(x.z, dov[4 * u + 2], acc);
+                    acc = fmaf(x.w, dov[4 * u + 3], acc);
+                    acc = fmaf(-y.x, dyv[4 * u], acc);
+                    acc = fmaf(-y.y, dyv[4 * u + 1], acc);
+                    acc = fmaf(-y.z, dyv[4 * u + 2], acc);
+                    acc = fmaf(-y.w, dyv[4 * u + 3], acc);
+                }
+                dS[sw(c, col)] = acc;
+            }
+        }
+        __syncthreads();  // every read of XT (dY^T) and of red is done
+        // dG exchange ([BC][KM] in XT), the last token's share of d(G_last), reverse cumsum,
+        // gate derivative; dq and dk out
+        if (col < K) {
+#pragma unroll
+            for (int r = 0; r < 4; ++r) XT[(4 * qtr + r) * KM + col] = dG_r[r];
+            red[qtr * KM + col] += dgl_part;
+        }
+        __syncthreads();
+        if (col < K) {
+            const int c = col;
+            const float dgl = red[c] + red[KM + c] + red[2 * KM + c] + red[3 * KM + c];
+            float suffix = dgl;  // d(G_last) enters G_{BC-1}
+            for (int t = BC - 1; t > 4 * qtr + 3; --t) suffix += XT[t * KM + c];
+            const float dtc = a.dt_bias[(size_t)h * K + c];
+#pragma unroll
+            for (int r = 3; r >= 0; --r) {
+                const int t = 4 * qtr + r;
+                suffix += XT[t * KM + c];
+                if (t < cn) {
+                    const size_t gi = ((bh * T) + t0 + t) * K + c;
+                    const float x = ld_io(a.z + gi) + dtc;
+                    const float g = -(eA * softplus_f32(x));
+                    const float dz = suffix * (-eA) * sigmoid_f32(x);
+                    a.dz[gi] = dz;
+                    ddt_acc += dz;
+                    dA_acc = fmaf(suffix, g, dA_acc);
+                    a.dq[gi] = dq_r[r];
+                    a.dk[gi] = dk_r[r];
+                }
+            }
+        }
+        __syncthreads();
+    }
+
+    // ---- dh0, and the per-(b, h) partial sums of dA_log and ddt_bias
+    if (a.dh0) {
+        for (int j = 0; j < 32; ++j) {
+            const int c = qtr + 4 * j;
+            if (c < K && col < V) a.dh0[bh * KV + (size_t)c * V + col] = dS[sw(c, col)];
+        }
+    }
+    if (col < K) red[qtr * KM + col] = ddt_acc;
+    for (int off = 16; off > 0; off >>= 1) dA_acc += __shfl_xor_sync(0xffffffffu, dA_acc, off);
+    __syncthreads();
+    if (lane == 0) XT[warp] = dA_acc;
+    if (tid < K) a.ddt_part[bh * K + tid] = red[tid] + red[KM + tid] + red[2 * KM + tid] + red[3 * KM + tid];
+    __syncthreads();
+    if (tid == 0) {
+        float s = 0.f;
+        for (int w = 0; w < BNT / 32; ++w) s += XT[w];
+        a.dA_part[bh] = s;
+    }
+}
+
+// dA_log[h] = sum_b dA_part[b, h];  ddt_bias[h, c] = sum_b ddt_part[b, h, c]
+__global__ void kda_bwd_reduce_kernel(int B, int H, int K, const float* __restrict__ dA_part,
+                                      const float* __restrict__ ddt_part, float* __restrict__ dA_log,
+                                      float* __restrict__ ddt_bias) {
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i < H) {
+        float s = 0.f;
+        for (int b = 0; b < B; ++b) s += dA_part[(size_t)b * H + i];
+        dA_log[i] = s;
+    }
+    if (i < H * K) {
+        float s = 0.f;
+        for (int b = 0; b < B; ++b) s += ddt_part[(size_t)b * H * K + i];
+        ddt_bias[i] = s;
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_chunk_backward(const BwdLaunch& L, cudaStream_t s) {
+    const int B = L.B, H = L.H, T = L.T, K = L.K, V = L.V;
+    const int N = (T + BC - 1) / BC;
+    const size_t BH = (size_t)B * H;
+    const size_t ck_bytes = sizeof(float) * BH * (size_t)N * K * V;
+    const size_t part_bytes = sizeof(float) * BH * (size_t)(1 + K);
+    char* scratch = nullptr;
+    cudaError_t e = cudaMallocAsync(reinterpret_cast<void**>(&scratch), ck_bytes + part_bytes + 256, s);
+    if (e != cudaSuccess) return e;
+    float* dA_part = reinterpret_cast<float*>(scratch);
+    float* ddt_part = dA_part + BH;
+    float* ckpt = reinterpret_cast<float*>(scratch + ((part_bytes + 255) & ~(size_t)255));
+    auto run = [&](auto io_tag) -> cudaError_t {
+        using IO = decltype(io_tag);
+        BwdArgs<IO> a;
+        a.H = H; a.T = T; a.K = K; a.V = V;
+        a.q = static_cast<const IO*>(L.q); a.k = static_cast<const IO*>(L.k);
+        a.v = static_cast<const IO*>(L.v); a.z = static_cast<const IO*>(L.z);
+        a.beta = static_cast<const IO*>(L.beta); a.d_o = static_cast<const IO*>(L.d_o);
+        a.A_log = L.A_log; a.dt_bias = L.dt_bias; a.h0 = L.h0; a.dhT = L.dhT; a.scale = L.scale;
+        a.dq = L.dq; a.dk = L.dk; a.dv = L.dv; a.dz = L.dz; a.dbeta = L.dbeta; a.dh0 = L.dh0;
+        a.ckpt = ckpt; a.dA_part = dA_part; a.ddt_part = ddt_part;
+        cudaError_t err = cudaFuncSetAttribute(kda_chunk_bwd_kernel<IO>,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               (int)BWD_SMEM_BYTES);
+        if (err != cudaSuccess) return err;
+        kda_chunk_bwd_kernel<IO><<<(unsigned)BH, BNT, BWD_SMEM_BYTES, s>>>(a);
+        return cudaGetLastError();
+    };
+    e = L.io == KDA_BF16 ? run(__nv_bfloat16{}) : run(float{});
+    if (e == cudaSuccess) {
+        const int n = H * K;
+        kda_bwd_reduce_kernel<<<(n + 255) / 256, 256, 0, s>>>(B, H, K, dA_part, ddt_part, L.dA_log,
+                                                               L.ddt_bias);
+        e = cudaGetLastError();
+        count_launches(2);
+    }
+    const cudaError_t ef = cudaFreeAsync(scratch, s);
+    return e != cudaSuccess ? e : ef;
+}
+
+}  // namespace kda

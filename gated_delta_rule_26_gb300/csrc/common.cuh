@@ -47,6 +47,16 @@ struct StepArgs {
     void* out;
 };
 
+// Arguments of the backward (chunk_bwd.cu); gradients are float32.
+struct BwdLaunch {
+    int B, H, T, K, V;
+    kda_dtype io;
+    const void *q, *k, *v, *z, *beta, *d_o;
+    const float *A_log, *dt_bias, *h0, *dhT;
+    float scale;
+    float *dq, *dk, *dv, *dz, *dbeta, *dA_log, *ddt_bias, *dh0;
+};
+
 // Count `n` kernel launches (read through kda_launch_count()).
 void count_launches(int n);
 
@@ -57,5 +67,6 @@ cudaError_t launch_gate(int B, int H, int T, int K, kda_dtype zdt, const void* z
 cudaError_t launch_decode(const StepArgs& a, cudaStream_t s);
 cudaError_t launch_recurrent(const StepArgs& a, int T, cudaStream_t s);
 cudaError_t launch_chunk_simt(const ChunkArgs& a, cudaStream_t s);
+cudaError_t launch_chunk_backward(const BwdLaunch& L, cudaStream_t s);
 
 }  // namespace kda

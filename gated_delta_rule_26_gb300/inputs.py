@@ -115,6 +115,23 @@ def make(B, H, T, K, V, *, chunk=16, dtype="f32", seed=0, dt_std=0.1, h0_std=0.0
                      beta.to(td), a, dt_bias, h0, float(K ** -0.5 if scale is None else scale))
 
 
+@dataclass
+class Adjoints:
+    d_o: torch.Tensor               # (B, H, T, V) in the inputs' I/O dtype
+    dhT: Optional[torch.Tensor]     # (B, H, K, V) float32
+
+
+def adjoints(inp: KdaInputs, seed: int, with_dhT: bool = True, dhT_std: float = 1.0) -> Adjoints:
+    """Seeded gradients of a loss with respect to o and hT (standard normal draws), the
+    inputs of a backward pass: d_o in the I/O dtype, dhT in float32."""
+    gen = torch.Generator(device="cpu")
+    gen.manual_seed(int(seed))
+    f = torch.float32
+    d_o = torch.randn(inp.B, inp.H, inp.T, inp.V, generator=gen, dtype=f)
+    dhT = torch.randn(inp.B, inp.H, inp.K, inp.V, generator=gen, dtype=f) * dhT_std
+    return Adjoints(d_o.to(_TORCH_DTYPE[inp.dtype]), dhT if with_dhT else None)
+
+
 def workload(name: str, **overrides) -> KdaInputs:
     """The named workload with its fixed seed; keyword overrides replace recipe fields."""
     cfg = dict(WORKLOADS[name])

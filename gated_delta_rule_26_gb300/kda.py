@@ -58,6 +58,7 @@ def load() -> ctypes.CDLL:
         lib.kda_chunk_forward_split_noalloc.argtypes = lib.kda_chunk_forward.argtypes
         lib.kda_recurrent_step.argtypes = [dp, i, vp, vp, vp, vp, vp, vp, vp, f, vp, vp, vp]
         lib.kda_fused_recurrent.argtypes = [dp, i, vp, vp, vp, vp, vp, vp, vp, f, vp, vp, vp]
+        lib.kda_chunk_backward.argtypes = [dp, i] + [vp] * 7 + [f] + [vp] * 12
         lib.kda_status_string.argtypes = [i]
         lib.kda_status_string.restype = ctypes.c_char_p
         lib.kda_device_status.argtypes = [vp]
@@ -67,7 +68,7 @@ def load() -> ctypes.CDLL:
         lib.kda_launch_count.argtypes = []
         lib.kda_launch_count.restype = ctypes.c_ulonglong
         for fn in (lib.kda_gate, lib.kda_chunk_forward, lib.kda_recurrent_step,
-                   lib.kda_fused_recurrent):
+                   lib.kda_fused_recurrent, lib.kda_chunk_backward):
             fn.restype = i
         _lib = lib
     return _lib
@@ -205,3 +206,33 @@ def fused_recurrent(q, k, v, z, beta, A_log, dt_bias, state: torch.Tensor,
                                     float(scale), _ptr(state), _ptr(out), _stream(stream))
     _check("kda_fused_recurrent", st)
     return out
+
+
+def chunk_backward(q, k, v, z, beta, A_log, dt_bias, d_o, scale: Optional[float] = None,
+                   h0: Optional[torch.Tensor] = None, dhT: Optional[torch.Tensor] = None,
+                   want_dh0: bool = True, stream=None) -> dict:
+    """Gradients of the chunked forward's inputs from d_o = dL/do and dhT = dL/dhT.
+
+    Returns float32 tensors: dq, dk, dz (B, H, T, K), dv (B, H, T, V), dbeta (B, H, T),
+    dA_log (H), ddt_bias (H, K) and dh0 (B, H, K, V) (None unless ``want_dh0``)."""
+    B, H, T, K = q.shape
+    V = v.shape[-1]
+    if scale is None:
+        scale = default_scale(K)
+    dev, f32 = q.device, torch.float32
+    g = {"dq": torch.empty(B, H, T, K, device=dev, dtype=f32),
+         "dk": torch.empty(B, H, T, K, device=dev, dtype=f32),
+         "dv": torch.empty(B, H, T, V, device=dev, dtype=f32),
+         "dz": torch.empty(B, H, T, K, device=dev, dtype=f32),
+         "dbeta": torch.empty(B, H, T, device=dev, dtype=f32),
+         "dA_log": torch.empty(H, device=dev, dtype=f32),
+         "ddt_bias": torch.empty(H, K, device=dev, dtype=f32),
+         "dh0": torch.empty(B, H, K, V, device=dev, dtype=f32) if want_dh0 else None}
+    d = Dims(B, H, T, K, V)
+    st = load().kda_chunk_backward(
+        ctypes.byref(d), _DTYPES[q.dtype], _ptr(q), _ptr(k), _ptr(v), _ptr(z), _ptr(beta),
+        _ptr(_f32(A_log)), _ptr(_f32(dt_bias)), float(scale), _ptr(h0), _ptr(d_o), _ptr(dhT),
+        _ptr(g["dq"]), _ptr(g["dk"]), _ptr(g["dv"]), _ptr(g["dz"]), _ptr(g["dbeta"]),
+        _ptr(g["dA_log"]), _ptr(g["ddt_bias"]), _ptr(g["dh0"]), _stream(stream))
+    _check("kda_chunk_backward", st)
+    return g

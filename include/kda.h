@@ -179,6 +179,33 @@ int kda_fused_recurrent(const kda_dims* dims, kda_dtype io_dtype, const void* q,
                         const float* dt_bias, float scale, float* state, void* out,
                         kda_stream_t stream);
 
+/*
+ * kda_chunk_backward -- the gradients of the chunked forward (kda_chunk_forward with the same
+ * q, k, v, z, beta, A_log, dt_bias, scale and h0) with respect to all of its inputs, given
+ * the gradients of a loss with respect to its outputs: d_o = dL/do (B,H,T,V) in io_dtype and
+ * dhT = dL/dhT (B,H,K,V) float32 (NULL = 0).  The kda-adjoint-2026-10-01 page names this
+ * backward and its gradients (dq, dk, dv, dg, dbeta and the state gradient); the gate's own
+ * derivative carries dg on to z, A_log and dt_bias.
+ *
+ * Outputs, all float32, caller-owned, fully overwritten:
+ *   dq, dk, dz (B,H,T,K)   dv (B,H,T,V)   dbeta (B,H,T)
+ *   dA_log (H) and ddt_bias (H,K), summed over the batch
+ *   dh0 (B,H,K,V): the gradient with respect to the initial state (a zero state when h0 is
+ *   NULL); NULL skips it.
+ * Inputs in io_dtype and float32 as for kda_chunk_forward; K, V as there.  The pass runs in
+ * float32 in chunks of 16 tokens whatever the forward's chunk size (the gradient does not
+ * depend on it).  Scratch: (B*H*ceil(T/16)*K*V + B*H*(K+1)) float32 from cudaMallocAsync on
+ * `stream`, freed on it; KDA_ERR_NO_MEMORY if that fails.  Alignment: q, k, v, z, d_o, dq,
+ * dk, dv, dz, h0, dhT, dh0 16 bytes; beta, dbeta, dA_log, ddt_bias, A_log, dt_bias their
+ * element size.  Two kernels per call (the pass, then the batch sum of dA_log / ddt_bias).
+ */
+int kda_chunk_backward(const kda_dims* dims, kda_dtype io_dtype, const void* q, const void* k,
+                       const void* v, const void* z, const void* beta, const float* A_log,
+                       const float* dt_bias, float scale, const float* h0, const void* d_o,
+                       const float* dhT, float* dq, float* dk, float* dv, float* dz,
+                       float* dbeta, float* dA_log, float* ddt_bias, float* dh0,
+                       kda_stream_t stream);
+
 /* A static, human-readable name for a status code. */
 const char* kda_status_string(int status);
 

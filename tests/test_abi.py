@@ -112,3 +112,26 @@ def test_gate_rejects_bad_chunk(lib):
     lib.kda_gate.argtypes = [ctypes.c_void_p, ctypes.c_int, vp, vp, vp, ctypes.c_int, vp, vp]
     assert lib.kda_gate(ctypes.byref(Dims(1, 1, 8, 64, 0)), 0, p, p, p, 24, p, None) == -2
     assert lib.kda_gate(ctypes.byref(Dims(1, 1, 8, 64, 0)), 0, None, p, p, 0, p, None) == -1
+
+
+def _bwd(lib, dims, dtype=1, misalign=0, null_do=False, null_dq=False):
+    p = 1 << 20  # fake, never dereferenced: every call below is rejected on the host
+    vp = ctypes.c_void_p
+    f = lib.kda_chunk_backward
+    f.argtypes = [ctypes.c_void_p, ctypes.c_int] + [vp] * 7 + [ctypes.c_float] + [vp] * 12
+    d_o = None if null_do else vp(p + misalign)
+    dq = None if null_dq else vp(p)
+    return f(ctypes.byref(dims) if dims is not None else None, dtype,
+             vp(p), vp(p), vp(p), vp(p), vp(p), vp(p), vp(p), 0.1, None, d_o, None,
+             dq, vp(p), vp(p), vp(p), vp(p), vp(p), vp(p), None, None)
+
+
+def test_backward_rejects_bad_arguments(lib):
+    assert _bwd(lib, None) == -1
+    assert _bwd(lib, Dims(1, 1, 8, 128, 128), dtype=3) == -1
+    assert _bwd(lib, Dims(1, 0, 8, 128, 128)) == -1
+    assert _bwd(lib, Dims(1, 1, 8, 12, 128)) == -2
+    assert _bwd(lib, Dims(1, 1, 8, 128, 256)) == -2
+    assert _bwd(lib, Dims(1, 1, 8, 128, 128), misalign=4) == -3
+    assert _bwd(lib, Dims(1, 1, 8, 128, 128), null_do=True) == -1
+    assert _bwd(lib, Dims(1, 1, 8, 128, 128), null_dq=True) == -1
