@@ -6,8 +6,9 @@ chunk 64, bf16 I/O, fp32 state) through the C ABI: gate, intra-chunk WY,
 inter-chunk carry and output.  After the timed prefill steps the decode
 workload (B256 H32 K=V=128, fp32 state 512 MiB updated in place) is timed for
 64 consecutive single-token steps and reported in the same JSON line under
-"decode", and the long-sequence workload (B1 H32 T65536, h0 given; the split
-chunk-parallel form) under "long".
+"decode", the long-sequence workload (B1 H32 T65536, h0 given; the split
+chunk-parallel form) under "long", and the backward of the prefill workload
+(kda_chunk_backward: every input's gradient from dL/do and dL/dhT) under "backward".
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 Under torchrun (N > 1) every rank runs the whole workload on its own GPU (weak
@@ -37,6 +38,18 @@ WORKLOAD = "prefill_bf16"
 #   q, k, v, z read and o written in bf16 (5 x 256 B) plus beta (2 B).
 def flops_per_token_head(C, K, V):
     return 6 * K * V + 3 * C * K + 2 * C * V + C * C / 3.0
+
+
+# Algorithmic work per token-head of the backward (chunks of C = 16): the state terms are
+# twice the forward's (dDelta, dKt, dQg, dY S^T and the two products of the dS update:
+# 12KV) plus the intra-chunk terms counted as for the forward.
+def bwd_flops_per_token_head(C, K, V):
+    return 12 * K * V + 3 * C * K + 2 * C * V + C * C / 3.0
+
+
+# fp32 FMA peak of the CUDA cores: 152 SMs x 128 lanes x 2 FLOPs at the maximum SM clock
+def fp32_peak_tflops(sm_mhz=2070.0):
+    return 152 * 128 * 2 * sm_mhz * 1e6 / 1e12
 
 
 def bytes_per_token_head(K, V, io_bytes=2):
@@ -294,6 +307,51 @@ def run_long(args, kda, inputs, peaks, ws, barrier):
     return res
 
 
+def run_backward(args, kda, inputs, peaks, ws, barrier):
+    """Time the backward of the prefill workload (gradients of every input from seeded dL/do
+    and dL/dhT) through kda_chunk_backward; reported under "backward"."""
+    import torch
+    stream = torch.cuda.current_stream()
+    inp = inputs.workload(WORKLOAD, **({"T": args.backward_T} if args.backward_T else {}))
+    adj = inputs.adjoints(inp, seed=77)
+    B, H, T, K, V = inp.B, inp.H, inp.T, inp.K, inp.V
+    d = inp.to("cuda")
+    d_o, dhT = adj.d_o.to("cuda"), adj.dhT.to("cuda")
+
+    def step():
+        kda.chunk_backward(d.q, d.k, d.v, d.z, d.beta, d.A_log, d.dt_bias, d_o, inp.scale,
+                           h0=d.h0, dhT=dhT)
+
+    for _ in range(2):
+        step()
+    barrier()
+    n0 = kda.launch_count()
+    secs = timed(step, args.backward_steps, stream)
+    launches = kda.launch_count() - n0
+    from gated_delta_rule_26_gb300 import dist as kdist
+    secs = kdist.max_over_ranks(secs, device="cuda")
+    per = secs / args.backward_steps
+    C = 16
+    flops = B * H * T * bwd_flops_per_token_head(C, K, V)
+    achieved = flops / per / 1e12
+    peak = fp32_peak_tflops()
+    res = {"value": ws * B * T / per, "unit": "tokens/s", "ms_per_step": per * 1e3,
+           "steps": args.backward_steps,
+           "roofline": {"bound": "alu", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                        "frac": achieved / peak,
+                        "traffic": measured_traffic("kda_chunk_bwd_kernel", ("chunk_bwd.cu", "common.cuh"))
+                        if T == 4096 else None,
+                        "flops_convention": "12KV+3CK+2CV+C^2/3 per token-head, C=16",
+                        "peak_source": "fp32 FMA: 152 SMs x 128 lanes x 2 x 2070 MHz",
+                        "kernel": "kda_chunk_bwd_kernel (+ the batch sum of dA_log, ddt_bias)"},
+           "gpu_launches": launches,
+           "config": {"workload": f"{WORKLOAD} backward B{B} H{H} T{T} K={K} V={V}, "
+                                  "bf16 inputs, fp32 gradients, dL/dhT given"}}
+    del d, d_o, dhT
+    torch.cuda.empty_cache()
+    return res
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -309,7 +367,13 @@ def main():
     ap.add_argument("--long-T", type=int, default=None,
                     help="sequence length of the long-sequence workload (default 65536; smaller "
                          "for profiler captures)")
-    ap.add_argument("--only", default="all", choices=["all", "prefill", "decode", "long"],
+    ap.add_argument("--backward-steps", type=int, default=3,
+                    help="timed steps of the backward workload")
+    ap.add_argument("--backward-T", type=int, default=None,
+                    help="sequence length of the backward workload (default 4096; smaller for "
+                         "profiler captures)")
+    ap.add_argument("--only", default="all", choices=["all", "prefill", "decode", "long",
+                                                      "backward"],
                     help="time only one of the two workloads (for profiler captures)")
     ap.add_argument("--prefill-T", type=int, default=None,
                     help="sequence length of the prefill workload (default 4096; smaller for "
@@ -340,6 +404,11 @@ def main():
         res = run_long(args, kda, inputs, peaks, ws, barrier)
         if rank == 0:
             print(json.dumps({"metric": "long only", "long": res}), flush=True)
+        return 0
+    if args.only == "backward":
+        res = run_backward(args, kda, inputs, peaks, ws, barrier)
+        if rank == 0:
+            print(json.dumps({"metric": "backward only", "backward": res}), flush=True)
         return 0
     if args.only == "decode":
         decode = run_decode(args, kda, inputs, peaks, ws, barrier)
@@ -458,6 +527,7 @@ def main():
     del d
     torch.cuda.empty_cache()
     long_res = run_long(args, kda, inputs, peaks, ws, barrier)
+    backward = None if args.only == "prefill" else run_backward(args, kda, inputs, peaks, ws, barrier)
     line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws,
             "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": per_step * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
@@ -470,7 +540,7 @@ def main():
             "tflops": tflops, "tflops_frac_bf16_burst": tflops / peaks["bf16_tflops"],
             "tflops_convention": "algorithmic (triangular) FLOPs 6KV+3CK+2CV+C^2/3 per token-head",
             "roofline": roofline, "e2e": e2e, "clocks": clocks, "gpu_launches": launches,
-            "decode": decode, "long": long_res}
+            "decode": decode, "long": long_res, "backward": backward}
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(inp_cpu)
     if rank == 0:

@@ -74,6 +74,32 @@ struct BwdArgs {
     float* ddt_part;  // (B H, K)
 };
 
+// 4-byte asynchronous global -> shared copies (the state of the next chunk to process lands
+// while the current one finishes)
+__device__ __forceinline__ void cp_async4(float* dst_smem, const float* src) {
+    const unsigned d = (unsigned)__cvta_generic_to_shared(dst_smem);
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"(d), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;\n" ::: "memory"); }
+
+// Reduce-scatter over a warp: on entry every lane holds 32 partial values; on exit v[0] of
+// lane l is the sum over the 32 lanes of their value l (31 shuffles).
+__device__ __forceinline__ void warp_reduce_scatter32(float (&v)[32], int lane) {
+#pragma unroll
+    for (int off = 16, w = 16; off >= 1; off >>= 1, w >>= 1) {
+        const bool hi = (lane & off) != 0;
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            if (j < w) {
+                const float send = hi ? v[j] : v[j + w];
+                const float keep = hi ? v[j + w] : v[j];
+                v[j] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+            }
+        }
+    }
+}
+
 __device__ __forceinline__ float sigmoid_f32(float x) {
     return x >= 0.f ? 1.f / (1.f + expf(-x)) : expf(x) / (1.f + expf(x));
 }
@@ -114,32 +140,70 @@ __global__ void __launch_bounds__(BNT, 1) kda_chunk_bwd_kernel(const BwdArgs<IO>
     // thread roles: (v or c) = tid % 128, quarter = tid / 128
     const int col = tid & 127, qtr = tid >> 7;
 
+    // Copy a (K, V) float32 matrix from global memory into a swizzled shared one (zero when
+    // src is null): every load is issued before the first store.
+    auto load_kv = [&](float* dst, const float* src) {
+        float x[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+            const int c = qtr + 4 * j;
+            x[j] = (src && c < K && col < V) ? __ldcg(src + (size_t)c * V + col) : 0.f;
+        }
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+            const int c = qtr + 4 * j;
+            if (c < K && col < V) dst[sw(c, col)] = x[j];
+        }
+    };
     // ---- the state entering the sequence
-    for (int j = 0; j < 32; ++j) {
-        const int c = qtr + 4 * j;
-        if (c < K && col < V) S[sw(c, col)] = a.h0 ? a.h0[bh * KV + (size_t)c * V + col] : 0.f;
-    }
+    load_kv(S, a.h0 ? a.h0 + bh * KV : nullptr);
     __syncthreads();
 
     // Load chunk n: q (optional), k, v (into R), dO (optional), beta, and G from z.
     auto load_chunk = [&](int n, bool full) {
         const int t0 = n * BC, cn = min(BC, T - t0);
-        for (int idx = tid; idx < BC * K; idx += BNT) {
-            const int t = idx / K, c = idx - t * K;
-            const bool in = t < cn;
+        constexpr int PER = BC * KM / BNT;  // elements per thread of a (BC, K) or (BC, V) tile
+        float kx[PER], qx[PER], zx[PER], dtx[PER], vx[PER], ox[PER];
+        float bx = 0.f;
+        // every global load first (they overlap), then the shared-memory stores
+#pragma unroll
+        for (int r = 0; r < PER; ++r) {
+            const int idx = tid + r * BNT, t = idx / K, c = idx - t * K;
+            const bool in = idx < BC * K && t < cn;
             const size_t gi = ((bh * T) + t0 + t) * K + c;
-            Kr[t * KM + c] = in ? ld_io(a.k + gi) : 0.f;
-            if (full) Qr[t * KM + c] = in ? ld_io(a.q + gi) : 0.f;
-            Gc[t * KM + c] = in ? kda_log_decay(ld_io(a.z + gi), a.dt_bias[(size_t)h * K + c], eA) : 0.f;
+            kx[r] = in ? ld_io(a.k + gi) : 0.f;
+            qx[r] = (full && in) ? ld_io(a.q + gi) : 0.f;
+            zx[r] = in ? ld_io(a.z + gi) : 0.f;
+            dtx[r] = in ? __ldg(a.dt_bias + (size_t)h * K + c) : 0.f;
         }
-        for (int idx = tid; idx < BC * V; idx += BNT) {
-            const int t = idx / V, vv = idx - t * V;
-            const bool in = t < cn;
+#pragma unroll
+        for (int r = 0; r < PER; ++r) {
+            const int idx = tid + r * BNT, t = idx / V, vv = idx - t * V;
+            const bool in = idx < BC * V && t < cn;
             const size_t gi = ((bh * T) + t0 + t) * V + vv;
-            Rv[t * VM + vv] = in ? ld_io(a.v + gi) : 0.f;
-            if (full) dO[t * VM + vv] = in ? ld_io(a.d_o + gi) : 0.f;
+            vx[r] = in ? ld_io(a.v + gi) : 0.f;
+            ox[r] = (full && in) ? ld_io(a.d_o + gi) : 0.f;
         }
-        if (tid < BC) bet[tid] = tid < cn ? ld_io(a.beta + bh * T + t0 + tid) : 0.f;
+        if (tid < BC && tid < cn) bx = ld_io(a.beta + bh * T + t0 + tid);
+#pragma unroll
+        for (int r = 0; r < PER; ++r) {
+            const int idx = tid + r * BNT, t = idx / K, c = idx - t * K;
+            if (idx < BC * K) {
+                const bool in = t < cn;
+                Kr[t * KM + c] = kx[r];
+                if (full) Qr[t * KM + c] = qx[r];
+                Gc[t * KM + c] = in ? kda_log_decay(zx[r], dtx[r], eA) : 0.f;
+            }
+        }
+#pragma unroll
+        for (int r = 0; r < PER; ++r) {
+            const int idx = tid + r * BNT, t = idx / V, vv = idx - t * V;
+            if (idx < BC * V) {
+                Rv[t * VM + vv] = vx[r];
+                if (full) dO[t * VM + vv] = ox[r];
+            }
+        }
+        if (tid < BC) bet[tid] = bx;
         __syncthreads();
         if (tid < K) {  // in-chunk cumulative sum of the log decay
             float run = 0.f;
@@ -159,34 +223,41 @@ __global__ void __launch_bounds__(BNT, 1) kda_chunk_bwd_kernel(const BwdArgs<IO>
             KtT[c * BC + t] = kk * expf(gl - g);
             if (full) QgT[c * BC + t] = Qr[t * KM + c] * expf(g);
         }
-        // A' (i < t) and M (i <= t): warp per pair, lanes over channels (exact pairwise decay)
-        for (int e = tid; e < BC * BC; e += BNT) {
-            Ap[e] = 0.f;
-            if (full) Mm[e] = 0.f;
-        }
-        __syncthreads();
-        int p = 0;
-        for (int t = 0; t < BC; ++t)
-            for (int i = 0; i <= t; ++i, ++p) {
-                if ((p & 15) != warp) continue;
-                if (i == t && !full) continue;
-                float sa = 0.f, sq = 0.f;
-                for (int c = lane; c < K; c += 32) {
-                    const float E = __expf(Gc[t * KM + c] - Gc[i * KM + c]);
-                    const float kiE = Kr[i * KM + c] * E;
-                    sa = fmaf(Kr[t * KM + c], kiE, sa);
-                    if (full) sq = fmaf(Qr[t * KM + c], kiE, sq);
-                }
+        // A' (i < t) and M (i <= t), exact pairwise decay: warp t, lanes over channels; the
+        // 2 x 16 sums of the row are reduced together
+        {
+            const int t = warp;
+            float gt[4], kt[4], qt[4];
 #pragma unroll
-                for (int off = 16; off > 0; off >>= 1) {
-                    sa += __shfl_xor_sync(0xffffffffu, sa, off);
-                    sq += __shfl_xor_sync(0xffffffffu, sq, off);
-                }
-                if (lane == 0) {
-                    if (i < t) Ap[t * BC + i] = sa;
-                    if (full) Mm[t * BC + i] = sq;
-                }
+            for (int u = 0; u < 4; ++u) {
+                const int c = lane + 32 * u;
+                const bool ok = c < K;
+                gt[u] = ok ? Gc[t * KM + c] : 0.f;
+                kt[u] = ok ? Kr[t * KM + c] : 0.f;
+                qt[u] = (ok && full) ? Qr[t * KM + c] : 0.f;
             }
+            float w[32];
+#pragma unroll
+            for (int i = 0; i < BC; ++i) {
+                float sa = 0.f, sq = 0.f;
+                if (i <= t) {
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const int c = lane + 32 * u;
+                        if (c < K) {
+                            const float kiE = Kr[i * KM + c] * __expf(gt[u] - Gc[i * KM + c]);
+                            sa = fmaf(kt[u], kiE, sa);
+                            sq = fmaf(qt[u], kiE, sq);
+                        }
+                    }
+                }
+                w[i] = sa;
+                w[BC + i] = sq;
+            }
+            warp_reduce_scatter32(w, lane);
+            if (lane < BC) Ap[t * BC + lane] = lane < t ? w[0] : 0.f;
+            else if (full) Mm[t * BC + lane - BC] = lane - BC <= t ? w[0] : 0.f;
+        }
         __syncthreads();
         // T = (I + diag(beta) A')^{-1} by forward substitution, one column per thread
         if (tid < BC) {
@@ -204,6 +275,7 @@ __global__ void __launch_bounds__(BNT, 1) kda_chunk_bwd_kernel(const BwdArgs<IO>
         // R = V - Kg S: thread (v = col, tokens 4 qtr ..)
         if (col < V) {
             float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 8
             for (int c = 0; c < K; ++c) {
                 const float s = S[sw(c, col)];
                 const float4 kg = *reinterpret_cast<const float4*>(KgT + c * BC + 4 * qtr);
@@ -247,9 +319,10 @@ __global__ void __launch_bounds__(BNT, 1) kda_chunk_bwd_kernel(const BwdArgs<IO>
             float d[BC];
 #pragma unroll
             for (int t = 0; t < BC; ++t) d[t] = Dl[t * VM + col];
+#pragma unroll 4
             for (int j = 0; j < 32; ++j) {
                 const int c = qtr + 4 * j;
-                if (c >= K) break;
+                if (c >= K) continue;
                 const float4* kt = reinterpret_cast<const float4*>(KtT + c * BC);
                 float acc = S[sw(c, col)] * gam[c];
 #pragma unroll
@@ -267,10 +340,18 @@ __global__ void __launch_bounds__(BNT, 1) kda_chunk_bwd_kernel(const BwdArgs<IO>
     }
 
     // ======================================================= phase 2: reverse
-    for (int j = 0; j < 32; ++j) {
-        const int c = qtr + 4 * j;
-        if (c < K && col < V) dS[sw(c, col)] = a.dhT ? a.dhT[bh * KV + (size_t)c * V + col] : 0.f;
-    }
+    load_kv(dS, a.dhT ? a.dhT + bh * KV : nullptr);
+    // the state entering the last chunk, asynchronously (each later one is requested as soon
+    // as the chunk after it has finished reading S)
+    auto prefetch_state = [&](int n) {
+        const float* ck = a.ckpt + (bh * N + n) * KV;
+        for (int j = 0; j < 32; ++j) {
+            const int c = qtr + 4 * j;
+            if (c < K && col < V) cp_async4(S + sw(c, col), ck + (size_t)c * V + col);
+        }
+        cp_async_commit();
+    };
+    if (N > 0) prefetch_state(N - 1);
     float dA_acc = 0.f, ddt_acc = 0.f;  // this thread's channel col, tokens of quarter qtr
     // Transposed copy of a [BC][VM] array into XT ([VM][BC]).
     auto transpose_cv = [&](const float* src) {
@@ -282,6 +363,7 @@ __global__ void __launch_bounds__(BNT, 1) kda_chunk_bwd_kernel(const BwdArgs<IO>
     // out[r] = sum_v XT[v][4 qtr + r] M[c][v] for this thread's channel c = col (M = S or dS).
     auto contract_v = [&](const float* Mat, float (&out)[4]) {
         out[0] = out[1] = out[2] = out[3] = 0.f;
+#pragma unroll 8
         for (int vv = 0; vv < V; ++vv) {
             const float m = Mat[sw(col, vv)];
             const float4 x = *reinterpret_cast<const float4*>(XT + vv * BC + 4 * qtr);
@@ -294,17 +376,14 @@ __global__ void __launch_bounds__(BNT, 1) kda_chunk_bwd_kernel(const BwdArgs<IO>
 
     for (int n = N - 1; n >= 0; --n) {
         const int t0 = n * BC, cn = min(BC, T - t0);
-        const float* ck = a.ckpt + (bh * N + n) * KV;
-        for (int j = 0; j < 32; ++j) {
-            const int c = qtr + 4 * j;
-            if (c < K && col < V) S[sw(c, col)] = ck[(size_t)c * V + col];
-        }
-        __syncthreads();
-        load_chunk(n, true);  // ends with a barrier
+        cp_async_wait_all();  // this chunk's entering state (prefetch_state)
+        load_chunk(n, true);  // its first barrier publishes S
+
 
         // dDelta = Kt dS + scale M^T dO  -> dY buffer; and this thread's share of dgamma
         if (col < V) {
             float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 8
             for (int c = 0; c < K; ++c) {
                 const float s = dS[sw(c, col)];
                 const float4 kt = *reinterpret_cast<const float4*>(KtT + c * BC + 4 * qtr);
@@ -324,6 +403,7 @@ __global__ void __launch_bounds__(BNT, 1) kda_chunk_bwd_kernel(const BwdArgs<IO>
         if (col < K) {  // dgamma_c partial over the value quarter qtr, times gamma_c
             float sacc = 0.f;
             const int v0 = 32 * qtr;
+#pragma unroll 8
             for (int vv = v0; vv < min(V, v0 + 32); ++vv) sacc = fmaf(S[sw(col, vv)], dS[sw(col, vv)], sacc);
             red[qtr * KM + col] = sacc * gam[col];
         }
@@ -398,30 +478,41 @@ __global__ void __launch_bounds__(BNT, 1) kda_chunk_bwd_kernel(const BwdArgs<IO>
                 dG_r[r] += dkg * Kr[t * KM + col] * Ga;
             }
         }
-        // dM (i <= t) and dB (i < t): warp per pair, lanes over value columns
+            // dM (i <= t) and dB (i < t): warp t, lanes over value columns, reduced together
         {
-            int p = 0;
-            for (int t = 0; t < BC; ++t)
-                for (int i = 0; i <= t; ++i, ++p) {
-                    if ((p & 15) != warp) continue;
-                    float sm_ = 0.f, sb = 0.f;
-                    for (int vv = lane; vv < V; vv += 32) {
-                        const float dl = Dl[i * VM + vv];
-                        sm_ = fmaf(dO[t * VM + vv], dl, sm_);
-                        sb = fmaf(dY[t * VM + vv], dl, sb);
-                    }
+            const int t = warp;
+            float ot[4], yt[4];
 #pragma unroll
-                    for (int off = 16; off > 0; off >>= 1) {
-                        sm_ += __shfl_xor_sync(0xffffffffu, sm_, off);
-                        sb += __shfl_xor_sync(0xffffffffu, sb, off);
-                    }
-                    if (lane == 0) {
-                        dM[t * BC + i] = a.scale * sm_;
-                        dB[t * BC + i] = i < t ? -sb : 0.f;
+            for (int u = 0; u < 4; ++u) {
+                const int vv = lane + 32 * u;
+                const bool ok = vv < V;
+                ot[u] = ok ? dO[t * VM + vv] : 0.f;
+                yt[u] = ok ? dY[t * VM + vv] : 0.f;
+            }
+            float w[32];
+#pragma unroll
+            for (int i = 0; i < BC; ++i) {
+                float sm_ = 0.f, sb = 0.f;
+                if (i <= t) {
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const int vv = lane + 32 * u;
+                        if (vv < V) {
+                            const float dl = Dl[i * VM + vv];
+                            sm_ = fmaf(ot[u], dl, sm_);
+                            sb = fmaf(yt[u], dl, sb);
+                        }
                     }
                 }
+                w[i] = sm_;
+                w[BC + i] = sb;
+            }
+            warp_reduce_scatter32(w, lane);
+            if (lane < BC) dM[t * BC + lane] = lane <= t ? a.scale * w[0] : 0.f;
+            else dB[t * BC + lane - BC] = lane - BC < t ? -w[0] : 0.f;
         }
         __syncthreads();
+        if (n > 0) prefetch_state(n - 1);  // S is not read again in this chunk
         // dbeta_t = sum_v R_tv dY_tv + sum_{i<t} A'_ti dB_ti  (warp t);  dV = diag(beta) dY
         {
             const int t = warp;
@@ -469,9 +560,10 @@ __global__ void __launch_bounds__(BNT, 1) kda_chunk_bwd_kernel(const BwdArgs<IO>
                 dov[t] = a.scale * dO[t * VM + col];
                 dyv[t] = bet[t] * dY[t * VM + col];
             }
+#pragma unroll 2
             for (int j = 0; j < 32; ++j) {
                 const int c = qtr + 4 * j;
-                if (c >= K) break;
+                if (c >= K) continue;
                 const float4* qg = reinterpret_cast<const float4*>(QgT + c * BC);
                 const float4* kg = reinterpret_cast<const float4*>(KgT + c * BC);
                 float acc = dS[sw(c, col)] * gam[c];
@@ -505,13 +597,19 @@ __global__ void __launch_bounds__(BNT, 1) kda_chunk_bwd_kernel(const BwdArgs<IO>
             float suffix = dgl;  // d(G_last) enters G_{BC-1}
             for (int t = BC - 1; t > 4 * qtr + 3; --t) suffix += XT[t * KM + c];
             const float dtc = a.dt_bias[(size_t)h * K + c];
+            float zr[4];
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                const int t = 4 * qtr + r;
+                zr[r] = t < cn ? ld_io(a.z + ((bh * T) + t0 + t) * K + c) : 0.f;
+            }
 #pragma unroll
             for (int r = 3; r >= 0; --r) {
                 const int t = 4 * qtr + r;
                 suffix += XT[t * KM + c];
                 if (t < cn) {
                     const size_t gi = ((bh * T) + t0 + t) * K + c;
-                    const float x = ld_io(a.z + gi) + dtc;
+                    const float x = zr[r] + dtc;
                     const float g = -(eA * softplus_f32(x));
                     const float dz = suffix * (-eA) * sigmoid_f32(x);
                     a.dz[gi] = dz;
