@@ -4,8 +4,9 @@
 // is the chain rule applied to the chunked form of the forward).
 //
 // One CTA (512 threads) per (b, h), fp32 throughout, chunks of 16 tokens.  Phase 1 walks
-// the chunks forward and keeps the state entering each chunk in a scratch buffer.  Phase 2
-// walks them in reverse with dS, the adjoint of the state leaving the chunk.  Per chunk,
+// the chunks forward and keeps the state entering each chunk, and the chunk's R and Delta,
+// in a scratch buffer.  Phase 2 walks them in reverse with dS, the adjoint of the state
+// leaving the chunk.  Per chunk,
 // with S the state entering it, G the in-chunk cumulative log decay, Gamma = e^G,
 // gamma = e^{G_last}, Kg = K Gamma, Qg = Q Gamma, Kt = K e^{G_last - G},
 // A'[t,i] = sum_c k_tc k_ic e^{G_tc - G_ic} (i < t), M[t,i] = sum_c q_tc k_ic e^{G_tc - G_ic}
@@ -37,10 +38,11 @@ constexpr int KM = 128, VM = 128;
 // shared memory map (floats)
 constexpr int O_S = 0;                    // S   [KM][VM], (c, v) at sw(c, v)
 constexpr int O_DS = O_S + KM * VM;       // dS  [KM][VM]
-constexpr int O_Q = O_DS + KM * VM;       // q   [BC][KM]
-constexpr int O_K = O_Q + BC * KM;        // k   [BC][KM]
-constexpr int O_G = O_K + BC * KM;        // G   [BC][KM] (natural log units)
-constexpr int O_KGT = O_G + BC * KM;      // Kg  [KM][BC]
+constexpr int GP = BC + 1;                // row pitch of the channel-major q, k, G tiles
+constexpr int O_Q = O_DS + KM * VM;       // q   [KM][GP]: (c, t) at ci(c, t)
+constexpr int O_K = O_Q + KM * GP;        // k   [KM][GP]
+constexpr int O_G = O_K + KM * GP;        // G   [KM][GP] (natural log units)
+constexpr int O_KGT = O_G + KM * GP;      // Kg  [KM][BC]
 constexpr int O_QGT = O_KGT + BC * KM;    // Qg  [KM][BC]
 constexpr int O_KTT = O_QGT + BC * KM;    // Kt  [KM][BC]
 constexpr int O_R = O_KTT + BC * KM;      // v, then R = V - Kg S   [BC][VM]
@@ -61,6 +63,10 @@ constexpr size_t BWD_SMEM_BYTES = sizeof(float) * SMEM_FLOATS;
 static_assert(BWD_SMEM_BYTES <= 232448, "backward shared memory");
 
 __device__ __forceinline__ int sw(int c, int v) { return c * VM + (v ^ (c & 31)); }
+// q, k and G: channel-major with an odd pitch, so that a warp over 32 channels of one token
+// and a warp over (2 channels x 16 tokens) both hit distinct banks
+__device__ __forceinline__ int ci(int c, int t) { return c * GP + t; }
+static_assert(O_KGT % 4 == 0, "16-byte aligned channel-major operands");
 
 template <typename IO>
 struct BwdArgs {
@@ -70,6 +76,7 @@ struct BwdArgs {
     float scale;
     float *dq, *dk, *dv, *dz, *dbeta, *dh0;
     float* ckpt;      // (B H, N, K, V): the state entering each chunk
+    float* rd;        // (B H, N, 2, BC, V): R and Delta of each chunk, phase 1 -> phase 2
     float* dA_part;   // (B H)
     float* ddt_part;  // (B H, K)
 };
@@ -163,7 +170,8 @@ __global__ void __launch_bounds__(BNT, 1) kda_chunk_bwd_kernel(const BwdArgs<IO>
     auto load_chunk = [&](int n, bool full) {
         const int t0 = n * BC, cn = min(BC, T - t0);
         constexpr int PER = BC * KM / BNT;  // elements per thread of a (BC, K) or (BC, V) tile
-        float kx[PER], qx[PER], zx[PER], dtx[PER], vx[PER], ox[PER];
+        float kx[PER], qx[PER], zx[PER], dtx[PER], vx[PER], ox[PER], dx[PER];
+        const float* rdn = a.rd + (bh * N + n) * (size_t)(2 * BC * V);
         float bx = 0.f;
         // every global load first (they overlap), then the shared-memory stores
 #pragma unroll
@@ -181,7 +189,14 @@ __global__ void __launch_bounds__(BNT, 1) kda_chunk_bwd_kernel(const BwdArgs<IO>
             const int idx = tid + r * BNT, t = idx / V, vv = idx - t * V;
             const bool in = idx < BC * V && t < cn;
             const size_t gi = ((bh * T) + t0 + t) * V + vv;
-            vx[r] = in ? ld_io(a.v + gi) : 0.f;
+            // phase 2 takes R and Delta as phase 1 left them; phase 1 starts from v
+            if (full) {
+                vx[r] = idx < BC * V ? __ldcg(rdn + idx) : 0.f;
+                dx[r] = idx < BC * V ? __ldcg(rdn + BC * V + idx) : 0.f;
+            } else {
+                vx[r] = in ? ld_io(a.v + gi) : 0.f;
+                dx[r] = 0.f;
+            }
             ox[r] = (full && in) ? ld_io(a.d_o + gi) : 0.f;
         }
         if (tid < BC && tid < cn) bx = ld_io(a.beta + bh * T + t0 + tid);
@@ -190,9 +205,9 @@ __global__ void __launch_bounds__(BNT, 1) kda_chunk_bwd_kernel(const BwdArgs<IO>
             const int idx = tid + r * BNT, t = idx / K, c = idx - t * K;
             if (idx < BC * K) {
                 const bool in = t < cn;
-                Kr[t * KM + c] = kx[r];
-                if (full) Qr[t * KM + c] = qx[r];
-                Gc[t * KM + c] = in ? kda_log_decay(zx[r], dtx[r], eA) : 0.f;
+                Kr[ci(c, t)] = kx[r];
+                if (full) Qr[ci(c, t)] = qx[r];
+                Gc[ci(c, t)] = in ? kda_log_decay(zx[r], dtx[r], eA) : 0.f;
             }
         }
 #pragma unroll
@@ -200,7 +215,10 @@ __global__ void __launch_bounds__(BNT, 1) kda_chunk_bwd_kernel(const BwdArgs<IO>
             const int idx = tid + r * BNT, t = idx / V, vv = idx - t * V;
             if (idx < BC * V) {
                 Rv[t * VM + vv] = vx[r];
-                if (full) dO[t * VM + vv] = ox[r];
+                if (full) {
+                    dO[t * VM + vv] = ox[r];
+                    Dl[t * VM + vv] = dx[r];
+                }
             }
         }
         if (tid < BC) bet[tid] = bx;
@@ -208,8 +226,8 @@ __global__ void __launch_bounds__(BNT, 1) kda_chunk_bwd_kernel(const BwdArgs<IO>
         if (tid < K) {  // in-chunk cumulative sum of the log decay
             float run = 0.f;
             for (int t = 0; t < BC; ++t) {
-                run += Gc[t * KM + tid];
-                Gc[t * KM + tid] = run;
+                run += Gc[ci(tid, t)];
+                Gc[ci(tid, t)] = run;
             }
             gam[tid] = expf(run);
         }
@@ -217,11 +235,11 @@ __global__ void __launch_bounds__(BNT, 1) kda_chunk_bwd_kernel(const BwdArgs<IO>
         // the decay-scaled operands, channel-major
         for (int idx = tid; idx < BC * K; idx += BNT) {
             const int c = idx >> 4, t = idx & 15;
-            const float g = Gc[t * KM + c], gl = Gc[(BC - 1) * KM + c];
-            const float kk = Kr[t * KM + c];
+            const float g = Gc[ci(c, t)], gl = Gc[ci(c, (BC - 1))];
+            const float kk = Kr[ci(c, t)];
             KgT[c * BC + t] = kk * expf(g);
             KtT[c * BC + t] = kk * expf(gl - g);
-            if (full) QgT[c * BC + t] = Qr[t * KM + c] * expf(g);
+            if (full) QgT[c * BC + t] = Qr[ci(c, t)] * expf(g);
         }
         // A' (i < t) and M (i <= t), exact pairwise decay: warp t, lanes over channels; the
         // 2 x 16 sums of the row are reduced together
@@ -232,9 +250,9 @@ __global__ void __launch_bounds__(BNT, 1) kda_chunk_bwd_kernel(const BwdArgs<IO>
             for (int u = 0; u < 4; ++u) {
                 const int c = lane + 32 * u;
                 const bool ok = c < K;
-                gt[u] = ok ? Gc[t * KM + c] : 0.f;
-                kt[u] = ok ? Kr[t * KM + c] : 0.f;
-                qt[u] = (ok && full) ? Qr[t * KM + c] : 0.f;
+                gt[u] = ok ? Gc[ci(c, t)] : 0.f;
+                kt[u] = ok ? Kr[ci(c, t)] : 0.f;
+                qt[u] = (ok && full) ? Qr[ci(c, t)] : 0.f;
             }
             float w[32];
 #pragma unroll
@@ -245,7 +263,7 @@ __global__ void __launch_bounds__(BNT, 1) kda_chunk_bwd_kernel(const BwdArgs<IO>
                     for (int u = 0; u < 4; ++u) {
                         const int c = lane + 32 * u;
                         if (c < K) {
-                            const float kiE = Kr[i * KM + c] * __expf(gt[u] - Gc[i * KM + c]);
+                            const float kiE = Kr[ci(c, i)] * __expf(gt[u] - Gc[ci(c, i)]);
                             sa = fmaf(kt[u], kiE, sa);
                             sq = fmaf(qt[u], kiE, sq);
                         }
@@ -272,8 +290,8 @@ __global__ void __launch_bounds__(BNT, 1) kda_chunk_bwd_kernel(const BwdArgs<IO>
                 Tm[t * BC + j] = x[t];
             }
         }
-        // R = V - Kg S: thread (v = col, tokens 4 qtr ..)
-        if (col < V) {
+        // R = V - Kg S: thread (v = col, tokens 4 qtr ..)  (phase 1 only)
+        if (!full && col < V) {
             float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll 8
             for (int c = 0; c < K; ++c) {
@@ -288,6 +306,7 @@ __global__ void __launch_bounds__(BNT, 1) kda_chunk_bwd_kernel(const BwdArgs<IO>
             for (int r = 0; r < 4; ++r) Rv[(4 * qtr + r) * VM + col] -= acc[r];
         }
         __syncthreads();
+        if (full) return;
         // Delta = T diag(beta) R
         if (col < V) {
             float rb[BC];
@@ -314,6 +333,14 @@ __global__ void __launch_bounds__(BNT, 1) kda_chunk_bwd_kernel(const BwdArgs<IO>
             if (c < K && col < V) ck[(size_t)c * V + col] = S[sw(c, col)];
         }
         load_chunk(n, false);
+        {  // R and Delta for phase 2
+            float* rdn = a.rd + (bh * N + n) * (size_t)(2 * BC * V);
+            for (int idx = tid; idx < BC * V; idx += BNT) {
+                const int t = idx / V, vv = idx - t * V;
+                rdn[idx] = Rv[t * VM + vv];
+                rdn[BC * V + idx] = Dl[t * VM + vv];
+            }
+        }
         // S <- diag(gamma) S + Kt^T Delta: thread (v = col, channels qtr + 4 j)
         if (col < V) {
             float d[BC];
@@ -437,12 +464,12 @@ __global__ void __launch_bounds__(BNT, 1) kda_chunk_bwd_kernel(const BwdArgs<IO>
         if (col < K) {  // dKt = Delta dS^T
             float x[4];
             contract_v(dS, x);
-            const float gl = Gc[(BC - 1) * KM + col];
+            const float gl = Gc[ci(col, (BC - 1))];
 #pragma unroll
             for (int r = 0; r < 4; ++r) {
                 const int t = 4 * qtr + r;
-                const float eL = expf(gl - Gc[t * KM + col]);
-                const float kk = Kr[t * KM + col];
+                const float eL = expf(gl - Gc[ci(col, t)]);
+                const float kk = Kr[ci(col, t)];
                 dk_r[r] += x[r] * eL;
                 dG_r[r] -= x[r] * kk * eL;
                 dgl_part += x[r] * kk * eL;
@@ -457,10 +484,10 @@ __global__ void __launch_bounds__(BNT, 1) kda_chunk_bwd_kernel(const BwdArgs<IO>
 #pragma unroll
             for (int r = 0; r < 4; ++r) {
                 const int t = 4 * qtr + r;
-                const float Ga = expf(Gc[t * KM + col]);
+                const float Ga = expf(Gc[ci(col, t)]);
                 const float dqg = a.scale * x[r];
                 dq_r[r] += dqg * Ga;
-                dG_r[r] += dqg * Qr[t * KM + col] * Ga;
+                dG_r[r] += dqg * Qr[ci(col, t)] * Ga;
             }
         }
         __syncthreads();
@@ -472,10 +499,10 @@ __global__ void __launch_bounds__(BNT, 1) kda_chunk_bwd_kernel(const BwdArgs<IO>
 #pragma unroll
             for (int r = 0; r < 4; ++r) {
                 const int t = 4 * qtr + r;
-                const float Ga = expf(Gc[t * KM + col]);
+                const float Ga = expf(Gc[ci(col, t)]);
                 const float dkg = -bet[t] * x[r];
                 dk_r[r] += dkg * Ga;
-                dG_r[r] += dkg * Kr[t * KM + col] * Ga;
+                dG_r[r] += dkg * Kr[ci(col, t)] * Ga;
             }
         }
             // dM (i <= t) and dB (i < t): warp t, lanes over value columns, reduced together
@@ -535,17 +562,23 @@ __global__ void __launch_bounds__(BNT, 1) kda_chunk_bwd_kernel(const BwdArgs<IO>
 #pragma unroll
             for (int r = 0; r < 4; ++r) {
                 const int t = 4 * qtr + r;
-                const float gt = Gc[t * KM + c], kt = Kr[t * KM + c], qt = Qr[t * KM + c];
+                const float gt = Gc[ci(c, t)], kt = Kr[ci(c, t)], qt = Qr[ci(c, t)];
                 float rowA = 0.f, rowM = 0.f, colA = 0.f, colM = 0.f;
-                for (int i = 0; i <= t; ++i) {  // t as the row (later) token
-                    const float kiE = Kr[i * KM + c] * __expf(gt - Gc[i * KM + c]);
-                    rowM = fmaf(dM[t * BC + i], kiE, rowM);
-                    if (i < t) rowA = fmaf(bet[t] * dB[t * BC + i], kiE, rowA);
+#pragma unroll
+                for (int i = 0; i < BC; ++i) {  // t as the row (later) token
+                    if (i <= t) {
+                        const float kiE = Kr[ci(c, i)] * __expf(gt - Gc[ci(c, i)]);
+                        rowM = fmaf(dM[t * BC + i], kiE, rowM);
+                        rowA = fmaf(bet[t] * dB[t * BC + i], kiE, rowA);  // dB[t][t] = 0
+                    }
                 }
-                for (int s2 = t; s2 < BC; ++s2) {  // t as the column (earlier) token
-                    const float E = __expf(Gc[s2 * KM + c] - gt);
-                    colM = fmaf(dM[s2 * BC + t], Qr[s2 * KM + c] * E, colM);
-                    if (s2 > t) colA = fmaf(bet[s2] * dB[s2 * BC + t], Kr[s2 * KM + c] * E, colA);
+#pragma unroll
+                for (int s2 = 0; s2 < BC; ++s2) {  // t as the column (earlier) token
+                    if (s2 >= t) {
+                        const float E = __expf(Gc[ci(c, s2)] - gt);
+                        colM = fmaf(dM[s2 * BC + t], Qr[ci(c, s2)] * E, colM);
+                        colA = fmaf(bet[s2] * dB[s2 * BC + t], Kr[ci(c, s2)] * E, colA);  // dB[t][t] = 0
+                    }
                 }
                 dq_r[r] += rowM;
                 dk_r[r] += rowA + colA + colM;
@@ -667,13 +700,16 @@ cudaError_t launch_chunk_backward(const BwdLaunch& L, cudaStream_t s) {
     const int N = (T + BC - 1) / BC;
     const size_t BH = (size_t)B * H;
     const size_t ck_bytes = sizeof(float) * BH * (size_t)N * K * V;
+    const size_t rd_bytes = sizeof(float) * BH * (size_t)N * 2 * BC * V;
     const size_t part_bytes = sizeof(float) * BH * (size_t)(1 + K);
     char* scratch = nullptr;
-    cudaError_t e = cudaMallocAsync(reinterpret_cast<void**>(&scratch), ck_bytes + part_bytes + 256, s);
+    cudaError_t e = cudaMallocAsync(reinterpret_cast<void**>(&scratch),
+                                    ck_bytes + rd_bytes + part_bytes + 256, s);
     if (e != cudaSuccess) return e;
     float* dA_part = reinterpret_cast<float*>(scratch);
     float* ddt_part = dA_part + BH;
     float* ckpt = reinterpret_cast<float*>(scratch + ((part_bytes + 255) & ~(size_t)255));
+    float* rd = ckpt + BH * (size_t)N * K * V;
     auto run = [&](auto io_tag) -> cudaError_t {
         using IO = decltype(io_tag);
         BwdArgs<IO> a;
@@ -683,7 +719,7 @@ cudaError_t launch_chunk_backward(const BwdLaunch& L, cudaStream_t s) {
         a.beta = static_cast<const IO*>(L.beta); a.d_o = static_cast<const IO*>(L.d_o);
         a.A_log = L.A_log; a.dt_bias = L.dt_bias; a.h0 = L.h0; a.dhT = L.dhT; a.scale = L.scale;
         a.dq = L.dq; a.dk = L.dk; a.dv = L.dv; a.dz = L.dz; a.dbeta = L.dbeta; a.dh0 = L.dh0;
-        a.ckpt = ckpt; a.dA_part = dA_part; a.ddt_part = ddt_part;
+        a.ckpt = ckpt; a.rd = rd; a.dA_part = dA_part; a.ddt_part = ddt_part;
         cudaError_t err = cudaFuncSetAttribute(kda_chunk_bwd_kernel<IO>,
                                                cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                (int)BWD_SMEM_BYTES);

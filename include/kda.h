@@ -194,8 +194,9 @@ int kda_fused_recurrent(const kda_dims* dims, kda_dtype io_dtype, const void* q,
  *   NULL); NULL skips it.
  * Inputs in io_dtype and float32 as for kda_chunk_forward; K, V as there.  The pass runs in
  * float32 in chunks of 16 tokens whatever the forward's chunk size (the gradient does not
- * depend on it).  Scratch: (B*H*ceil(T/16)*K*V + B*H*(K+1)) float32 from cudaMallocAsync on
- * `stream`, freed on it; KDA_ERR_NO_MEMORY if that fails.  Alignment: q, k, v, z, d_o, dq,
+ * depend on it).  Scratch: (B*H*ceil(T/16)*(K*V + 32*V) + B*H*(K+1)) float32 (the state
+ * entering every 16-token chunk, and its R and Delta) from cudaMallocAsync on `stream`, freed
+ * on it; KDA_ERR_NO_MEMORY if that fails.  Alignment: q, k, v, z, d_o, dq,
  * dk, dv, dz, h0, dhT, dh0 16 bytes; beta, dbeta, dA_log, ddt_bias, A_log, dt_bias their
  * element size.  Two kernels per call (the pass, then the batch sum of dA_log / ddt_bias).
  */
