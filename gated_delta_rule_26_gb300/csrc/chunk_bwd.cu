@@ -87,6 +87,9 @@ __device__ __forceinline__ void cp_async4(float* dst_smem, const float* src) {
     const unsigned d = (unsigned)__cvta_generic_to_shared(dst_smem);
     asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"(d), "l"(src) : "memory");
 }
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+    asm volatile("prefetch.global.L2 [%0];\n" ::"l"(p));
+}
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;\n" ::: "memory"); }
 
@@ -166,6 +169,24 @@ __global__ void __launch_bounds__(BNT, 1) kda_chunk_bwd_kernel(const BwdArgs<IO>
     load_kv(S, a.h0 ? a.h0 + bh * KV : nullptr);
     __syncthreads();
 
+    // Ask L2 for the inputs of chunk n (one 128-byte line per thread): k, z, v or R and Delta,
+    // beta, and with `full` q and dO; issued one chunk ahead of load_chunk.
+    auto prefetch_chunk = [&](int n, bool full) {
+        if (n < 0 || n >= N) return;
+        const int t0 = n * BC, cn = min(BC, T - t0);
+        const int io = (int)sizeof(IO);
+        const int lk = (cn * K * io + 127) / 128, lv = (cn * V * io + 127) / 128;
+        const int lrd = (2 * BC * V * 4 + 127) / 128;
+        int i = tid;
+        const char* p = nullptr;
+        if (i < lk) p = reinterpret_cast<const char*>(a.k + ((bh * T) + t0) * K) + 128 * i;
+        else if ((i -= lk) < lk) p = reinterpret_cast<const char*>(a.z + ((bh * T) + t0) * K) + 128 * i;
+        else if (full && (i -= lk) < lk) p = reinterpret_cast<const char*>(a.q + ((bh * T) + t0) * K) + 128 * i;
+        else if (full && (i -= lk) < lv) p = reinterpret_cast<const char*>(a.d_o + ((bh * T) + t0) * V) + 128 * i;
+        else if (full && (i -= lv) < lrd) p = reinterpret_cast<const char*>(a.rd + (bh * N + n) * (size_t)(2 * BC * V)) + 128 * i;
+        else if (!full && (i -= lk) < lv) p = reinterpret_cast<const char*>(a.v + ((bh * T) + t0) * V) + 128 * i;
+        if (p) prefetch_l2(p);
+    };
     // Load chunk n: q (optional), k, v (into R), dO (optional), beta, and G from z.
     auto load_chunk = [&](int n, bool full) {
         const int t0 = n * BC, cn = min(BC, T - t0);
@@ -333,6 +354,7 @@ __global__ void __launch_bounds__(BNT, 1) kda_chunk_bwd_kernel(const BwdArgs<IO>
             if (c < K && col < V) ck[(size_t)c * V + col] = S[sw(c, col)];
         }
         load_chunk(n, false);
+        prefetch_chunk(n + 1, false);
         {  // R and Delta for phase 2
             float* rdn = a.rd + (bh * N + n) * (size_t)(2 * BC * V);
             for (int idx = tid; idx < BC * V; idx += BNT) {
@@ -405,6 +427,7 @@ __global__ void __launch_bounds__(BNT, 1) kda_chunk_bwd_kernel(const BwdArgs<IO>
         const int t0 = n * BC, cn = min(BC, T - t0);
         cp_async_wait_all();  // this chunk's entering state (prefetch_state)
         load_chunk(n, true);  // its first barrier publishes S
+        prefetch_chunk(n - 1, true);
 
 
         // dDelta = Kt dS + scale M^T dO  -> dY buffer; and this thread's share of dgamma
