@@ -6,8 +6,8 @@
 // One CTA (512 threads) per (b, h), fp32 throughout, chunks of 16 tokens.  Phase 1 walks
 // the chunks forward and keeps the state entering each chunk, and the chunk's R and Delta,
 // in a scratch buffer.  Phase 2 walks them in reverse with dS, the adjoint of the state
-// leaving the chunk.  Per chunk,
-// with S the state entering it, G the in-chunk cumulative log decay, Gamma = e^G,
+// leaving the chunk.  Per chunk, with S the state entering it, G the in-chunk cumulative
+// log decay, Gamma = e^G,
 // gamma = e^{G_last}, Kg = K Gamma, Qg = Q Gamma, Kt = K e^{G_last - G},
 // A'[t,i] = sum_c k_tc k_ic e^{G_tc - G_ic} (i < t), M[t,i] = sum_c q_tc k_ic e^{G_tc - G_ic}
 // (i <= t), T = (I + diag(beta) A')^{-1}, R = V - Kg S, Delta = T diag(beta) R, the forward is
@@ -45,7 +45,7 @@ constexpr int O_G = O_K + KM * GP;        // G   [KM][GP] (natural log units)
 constexpr int O_KGT = O_G + KM * GP;      // Kg  [KM][BC]
 constexpr int O_QGT = O_KGT + BC * KM;    // Qg  [KM][BC]
 constexpr int O_KTT = O_QGT + BC * KM;    // Kt  [KM][BC]
-constexpr int O_R = O_KTT + BC * KM;      // v, then R = V - Kg S   [BC][VM]
+constexpr int O_R = O_KTT + BC * KM;      // R = V - Kg S [BC][VM] (phase 1: v first)
 constexpr int O_DO = O_R + BC * VM;       // dO  [BC][VM]
 constexpr int O_DL = O_DO + BC * VM;      // Delta [BC][VM]
 constexpr int O_DY = O_DL + BC * VM;      // dDelta, then dY [BC][VM]
@@ -169,8 +169,8 @@ __global__ void __launch_bounds__(BNT, 1) kda_chunk_bwd_kernel(const BwdArgs<IO>
     load_kv(S, a.h0 ? a.h0 + bh * KV : nullptr);
     __syncthreads();
 
-    // Ask L2 for the inputs of chunk n (one 128-byte line per thread): k, z, v or R and Delta,
-    // beta, and with `full` q and dO; issued one chunk ahead of load_chunk.
+    // Ask L2 for the inputs of chunk n (one 128-byte line per thread): k, z, and v (phase 1)
+    // or q, dO, R and Delta (phase 2, `full`); issued one chunk ahead of load_chunk.
     auto prefetch_chunk = [&](int n, bool full) {
         if (n < 0 || n >= N) return;
         const int t0 = n * BC, cn = min(BC, T - t0);
@@ -187,7 +187,9 @@ __global__ void __launch_bounds__(BNT, 1) kda_chunk_bwd_kernel(const BwdArgs<IO>
         else if (!full && (i -= lk) < lv) p = reinterpret_cast<const char*>(a.v + ((bh * T) + t0) * V) + 128 * i;
         if (p) prefetch_l2(p);
     };
-    // Load chunk n: q (optional), k, v (into R), dO (optional), beta, and G from z.
+    // Load chunk n: k, beta and G (from z), then recompute A' and T; phase 1 (`full` false)
+    // also computes R and Delta from v and S, phase 2 loads q and dO, takes R and Delta as
+    // phase 1 stored them, and computes M.  Every exit follows a barrier.
     auto load_chunk = [&](int n, bool full) {
         const int t0 = n * BC, cn = min(BC, T - t0);
         constexpr int PER = BC * KM / BNT;  // elements per thread of a (BC, K) or (BC, V) tile
