@@ -303,3 +303,30 @@ def test_wrong_sign_in_u_is_caught():
         u = v[t] + S.T @ k[t]
         S = S + np.outer(k[t], u)
     assert not np.allclose(S.T @ k[1], v[1])
+
+
+def test_prefix_gate_mutant_is_caught():
+    """The superseded gate -softplus(exp(A) (z + dt_bias)) planted in place of the gate
+    (here, on the CPU) breaks the monotonicity pin: for z < 0 it increases with A_log."""
+    z = np.linspace(-6, -0.1, 200)
+    mutant = lambda a: -np.logaddexp(0.0, math.exp(a) * z)
+    g_lo, g_hi = mutant(-1.0), mutant(1.0)
+    assert not np.all(g_lo > g_hi)  # the pin above requires g to decrease in A_log
+    # and the oracle's own gate satisfies it on the same points
+    ref_lo = _gate_np(z.reshape(1, 1, -1, 1), [-1.0], [[0.0]]).ravel()
+    ref_hi = _gate_np(z.reshape(1, 1, -1, 1), [1.0], [[0.0]]).ravel()
+    assert np.all(ref_lo > ref_hi)
+
+
+def test_undecayed_read_mutant_is_caught():
+    """u read from the state before its decay (u = v - S^T k, then S <- diag(alpha) S + b k u^T),
+    planted here on the CPU, breaks the Householder-form pin whenever alpha != 1."""
+    q, k, v, z, beta, A, dt, S0 = _rand_problem(B=1, H=1, T=6, K=3, V=5, seed=9)
+    g = oracle.gate(z, A, dt)
+    o_ref, h_ref = oracle.forward(q, k, v, z, beta, A, dt, 0.6, S0)
+    S = S0[0, 0].copy()
+    for t in range(6):
+        kt = k[0, 0, t]
+        u = v[0, 0, t] - S.T @ kt                      # mutant: undecayed state
+        S = np.exp(g[0, 0, t])[:, None] * S + beta[0, 0, t] * np.outer(kt, u)
+    assert np.abs(S - h_ref[0, 0]).max() > 1e-3 * np.abs(h_ref).max()
