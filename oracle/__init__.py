@@ -75,7 +75,7 @@ def _load():
                                                      ctypes.c_double, _D, _D, _D, i, i]
             lib.kda_oracle_forward_range.restype = None
             lib.kda_oracle_backward_range.argtypes = [i, i, i, i, i] + [_D] * 7 + [
-                ctypes.c_double] + [_D] * 11 + [i, i, i]
+                ctypes.c_double] + [_D] * 12 + [i, i, i]
             lib.kda_oracle_backward_range.restype = None
             _lib = lib
     return _lib
@@ -176,9 +176,10 @@ def backward(q, k, v, z, beta, A_log, dt_bias, scale, h0, d_o, dhT=None, threads
              mutant: int = 0) -> dict:
     """Gradients of L (with dL/do = d_o and dL/dhT = dhT) with respect to every input.
 
-    Returns float64 arrays: dq, dk, dz (B,H,T,K), dv (B,H,T,V), dbeta (B,H,T), dA_log (H),
-    ddt_bias (H,K) and dh0 (B,H,K,V) (the gradient with respect to the initial state, a zero
-    state when h0 is None).  `mutant` plants a known mistake (tests only).
+    Returns float64 arrays: dq, dk, dz, dg (B,H,T,K; dg is the gradient with respect to the log
+    decay g), dv (B,H,T,V), dbeta (B,H,T), dA_log (H), ddt_bias (H,K) and dh0 (B,H,K,V) (the
+    gradient with respect to the initial state, a zero state when h0 is None).  `mutant`
+    plants a known mistake (tests only).
     """
     q, k, v, z, beta, A_log, dt_bias, h0, d_o, dhT = (
         f64(a) for a in (q, k, v, z, beta, A_log, dt_bias, h0, d_o, dhT))
@@ -187,7 +188,7 @@ def backward(q, k, v, z, beta, A_log, dt_bias, scale, h0, d_o, dhT=None, threads
     assert A_log.shape == (H,) and dt_bias.shape == (H, K) and d_o.shape == v.shape
     for s_ in (h0, dhT):
         assert s_ is None or s_.shape == (B, H, K, V)
-    out = {n: np.zeros(q.shape) for n in ("dq", "dk", "dz")}
+    out = {n: np.zeros(q.shape) for n in ("dq", "dk", "dz", "dg")}
     out["dv"] = np.zeros(v.shape)
     out["dbeta"] = np.zeros((B, H, T))
     out["dh0"] = np.zeros((B, H, K, V))
@@ -199,7 +200,8 @@ def backward(q, k, v, z, beta, A_log, dt_bias, scale, h0, d_o, dhT=None, threads
         lib.kda_oracle_backward_range(
             B, H, T, K, V, _p(q), _p(k), _p(v), _p(z), _p(beta), _p(A_log), _p(dt_bias),
             float(scale), _p(h0), _p(d_o), _p(dhT), _p(out["dq"]), _p(out["dk"]), _p(out["dv"]),
-            _p(out["dz"]), _p(out["dbeta"]), _p(dA_part), _p(ddt_part), _p(out["dh0"]),
+            _p(out["dz"]), _p(out["dg"]), _p(out["dbeta"]), _p(dA_part), _p(ddt_part),
+            _p(out["dh0"]),
             int(mutant), r[0], r[1])
 
     _run_ranges(run, B * H, threads)

@@ -158,7 +158,8 @@ void kda_oracle_forward_range(int B, int H, int T, int K, int V,
  * and through the gate x = z + dt_bias_h, g = -exp(A_log_h) softplus(x):
  *   dz = dg (-exp(A_log_h)) sigmoid(x),  ddt_bias_h += dz,  dA_log_h += dg g.
  * dh0 is dS after token 0.  dA_log and ddt_bias are returned per (b, h) (dA_part (B*H),
- * ddt_part (B*H, K)); the caller sums them over b.
+ * ddt_part (B*H, K)); the caller sums them over b.  dg (B,H,T,K), the gradient with respect
+ * to the log decay itself, is written when `dg_out` is not NULL.
  *
  * The states entering each token are recomputed forward from copies kept every 16 tokens
  * (storage only: the arithmetic of each step is the forward's).  `mutant` plants a known
@@ -190,8 +191,8 @@ void kda_oracle_backward_range(int B, int H, int T, int K, int V,
                                const double* z, const double* beta,
                                const double* A_log, const double* dt_bias, double scale,
                                const double* h0, const double* d_o, const double* dhT,
-                               double* dq, double* dk, double* dv, double* dz, double* dbeta,
-                               double* dA_part, double* ddt_part, double* dh0,
+                               double* dq, double* dk, double* dv, double* dz, double* dg_out,
+                               double* dbeta, double* dA_part, double* ddt_part, double* dh0,
                                int mutant, int bh_begin, int bh_end) {
     (void)B;
     const int L = 16;
@@ -305,6 +306,7 @@ void kda_oracle_backward_range(int B, int H, int T, int K, int V,
                     const double dg = at[c] * dal;
                     const double dzc = dg * (-mult) * sg[gi];
                     dz[((size_t)bh * T + t) * K + c] = dzc;
+                    if (dg_out) dg_out[((size_t)bh * T + t) * K + c] = dg;
                     ddt[c] += dzc;
                     dA += dg * g[gi];
                 }

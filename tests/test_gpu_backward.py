@@ -2,8 +2,13 @@
 reverse-mode gradients, on the same seeded inputs and output adjoints.
 
 Bar: the backward computes in float32 whatever the I/O dtype (bf16 inputs are read exactly),
-so every gradient tensor is held to the float32 bar, max|x - y| / max|y| <= 1e-4, against the
-oracle evaluated on the identical (rounded) inputs.  Small cases run whole; the full-size
+so every per-token gradient and dh0 is held to the float32 bar, max|x - y| / max|y| <= 1e-4,
+against the oracle evaluated on the identical (rounded) inputs.  dA_log[h] and
+ddt_bias[h, c] are sums over the batch and the tokens (and, for dA_log, the channels) whose
+terms can cancel by three orders of magnitude; the error of a float32 sum scales with the
+sum of the magnitudes of its terms, so for these two the bar is max|x - y| <= 1e-4 max
+sum|terms| per tensor (terms dg g and dz, from the oracle; max-normalised as for the other
+tensors, so that an element whose terms all vanish is held to the tensor's scale).  Small cases run whole; the full-size
 prefill workload runs whole on the GPU and is compared on one head (all 8 sequences, so that
 the batch sums dA_log[h] and ddt_bias[h] are complete) that the oracle recomputes.
 """
@@ -29,6 +34,30 @@ def check(name, got, ref):
         return
     err = np.abs(got - ref).max() / max(np.abs(ref).max(), 1e-30)
     assert err <= BAR, f"{name}: max rel {err:.3e} > {BAR}"
+
+
+def reduced_scales(inp, ref):
+    """sum |dg g| over (b, t, c) per head and sum |dz| over (b, t) per (head, channel)."""
+    g = oracle.gate(inp.z, inp.A_log, inp.dt_bias)
+    return {"dA_log": np.abs(ref["dg"] * g).sum(axis=(0, 2, 3)),
+            "ddt_bias": np.abs(ref["dz"]).sum(axis=(0, 2))}
+
+
+def check_reduced(name, got, ref, scale):
+    got = got.detach().double().cpu().numpy()
+    ref = np.asarray(ref, dtype=np.float64)
+    assert got.shape == ref.shape and np.all(np.isfinite(got)), name
+    err = np.abs(got - ref).max() / max(np.max(scale), 1e-30) if ref.size else 0.0
+    assert err <= BAR, f"{name}: error {err:.3e} of the largest sum of term magnitudes > {BAR}"
+
+
+def check_all(g, ref, inp):
+    scales = reduced_scales(inp, ref)
+    for n in NAMES:
+        if n in scales:
+            check_reduced(n, g[n], ref[n], scales[n])
+        else:
+            check(n, g[n], ref[n])
 
 
 def run_bwd(kda, inp, seed, with_dhT=True, threads=8):
@@ -59,15 +88,13 @@ def run_bwd(kda, inp, seed, with_dhT=True, threads=8):
 def test_backward_matches_oracle(kda, B, H, T, K, V, dtype, h0_std, A_log):
     inp = inputs.make(B, H, T, K, V, dtype=dtype, seed=100 + T + K, h0_std=h0_std, A_log=A_log)
     g, ref = run_bwd(kda, inp, seed=200 + T)
-    for n in NAMES:
-        check(n, g[n], ref[n])
+    check_all(g, ref, inp)
 
 
 def test_backward_without_final_state_gradient(kda):
     inp = inputs.make(1, 3, 90, 64, 32, dtype="f32", seed=31, h0_std=0.2)
     g, ref = run_bwd(kda, inp, seed=32, with_dhT=False)
-    for n in NAMES:
-        check(n, g[n], ref[n])
+    check_all(g, ref, inp)
 
 
 def test_backward_strong_decay_and_z_sweep(kda):
@@ -76,8 +103,7 @@ def test_backward_strong_decay_and_z_sweep(kda):
     inp = inputs.make(1, 2, 64, 32, 32, dtype="f32", seed=41, h0_std=0.1,
                       A_log_value=float(np.log(16.0)), z_sweep=(-6.0, 6.0))
     g, ref = run_bwd(kda, inp, seed=42)
-    for n in NAMES:
-        check(n, g[n], ref[n])
+    check_all(g, ref, inp)
 
 
 def test_backward_empty_sequence(kda):
@@ -122,5 +148,8 @@ def test_backward_full_size_sampled_head(kda):
                           sl(adj.d_o), sl(adj.dhT), threads=8)
     for n in ("dq", "dk", "dv", "dz", "dbeta", "dh0"):
         check(n, g[n][:, h:h + 1], ref[n])
-    check("dA_log", g["dA_log"][h:h + 1], ref["dA_log"])
-    check("ddt_bias", g["ddt_bias"][h:h + 1], ref["ddt_bias"])
+    gate = oracle.gate(sl(inp.z), inp.A_log[h:h + 1], inp.dt_bias[h:h + 1])
+    check_reduced("dA_log", g["dA_log"][h:h + 1], ref["dA_log"],
+                  np.abs(ref["dg"] * gate).sum(axis=(0, 2, 3)))
+    check_reduced("ddt_bias", g["ddt_bias"][h:h + 1], ref["ddt_bias"],
+                  np.abs(ref["dz"]).sum(axis=(0, 2)))

@@ -155,3 +155,30 @@ def test_planted_backward_mistakes_are_caught(mutant):
     j = oracle.jvp(*_args(p), d_o, dhT_, tan)
     bad = oracle.backward(*_args(p), d_o, dhT_, mutant=mutant)
     assert abs(_directional(bad, tan) - j) > 1e-3 * abs(j)
+
+
+def test_log_decay_gradient_against_central_differences():
+    """dg, the gradient with respect to the log decay itself, coordinate by coordinate against
+    central differences of the recurrence taken with g as its input (oracle.recurrent), on a
+    tiny problem; and dz = dg (-e^{A_log}) sigmoid(z + dt_bias) on a larger one."""
+    p, d_o, dhT_, _ = _problem(B=1, H=2, T=6, K=2, V=3, seed=13)
+    grads = oracle.backward(*_args(p), d_o, dhT_)
+    g = oracle.gate(p["z"], p["A_log"], p["dt_bias"])
+
+    def loss(gg):
+        o, hT = oracle.recurrent(p["q"], p["k"], p["v"], gg, p["beta"], p["scale"], p["h0"])
+        return float(np.sum(o * d_o) + np.sum(hT * dhT_))
+
+    eps = 1e-6
+    for idx in np.ndindex(g.shape):
+        gp, gm = g.copy(), g.copy()
+        gp[idx] += eps
+        gm[idx] -= eps
+        fd = (loss(gp) - loss(gm)) / (2 * eps)
+        assert grads["dg"][idx] == pytest.approx(fd, rel=1e-7, abs=1e-8), idx
+    p, d_o, dhT_, _ = _problem(seed=14)
+    grads = oracle.backward(*_args(p), d_o, dhT_)
+    x = p["z"] + p["dt_bias"][None, :, None, :]
+    sig = 1.0 / (1.0 + np.exp(-x))
+    np.testing.assert_allclose(grads["dz"], grads["dg"] * (-np.exp(p["A_log"]))[None, :, None, None] * sig,
+                               rtol=1e-12, atol=1e-15)
