@@ -404,24 +404,45 @@ __global__ void __launch_bounds__(BNT, 1) kda_chunk_bwd_kernel(const BwdArgs<IO>
     };
     if (N > 0) prefetch_state(N - 1);
     float dA_acc = 0.f, ddt_acc = 0.f;  // this thread's channel col, tokens of quarter qtr
-    // Transposed copy of a [BC][VM] array into XT ([VM][BC]).
-    auto transpose_cv = [&](const float* src) {
+    // Transposed copy of a [BC][VM] array into dst ([VM][BC]).
+    auto transpose_cv = [&](float* dst, const float* src) {
         for (int idx = tid; idx < BC * V; idx += BNT) {
             const int vv = idx >> 4, t = idx & 15;
-            XT[vv * BC + t] = src[t * VM + vv];
+            dst[vv * BC + t] = src[t * VM + vv];
         }
     };
-    // out[r] = sum_v XT[v][4 qtr + r] M[c][v] for this thread's channel c = col (M = S or dS).
-    auto contract_v = [&](const float* Mat, float (&out)[4]) {
+    // out[r] = sum_v X[v][4 qtr + r] M[c][v] for this thread's channel c = col (M = S or dS,
+    // X transposed [VM][BC]).
+    auto contract_v = [&](const float* Mat, const float* X, float (&out)[4]) {
         out[0] = out[1] = out[2] = out[3] = 0.f;
 #pragma unroll 8
         for (int vv = 0; vv < V; ++vv) {
             const float m = Mat[sw(col, vv)];
-            const float4 x = *reinterpret_cast<const float4*>(XT + vv * BC + 4 * qtr);
+            const float4 x = *reinterpret_cast<const float4*>(X + vv * BC + 4 * qtr);
             out[0] = fmaf(x.x, m, out[0]);
             out[1] = fmaf(x.y, m, out[1]);
             out[2] = fmaf(x.z, m, out[2]);
             out[3] = fmaf(x.w, m, out[3]);
+        }
+    };
+    // The same for two transposed operands against one pass over M.
+    auto contract_v2 = [&](const float* Mat, const float* X1, const float* X2, float (&o1)[4],
+                           float (&o2)[4]) {
+#pragma unroll
+        for (int r = 0; r < 4; ++r) o1[r] = o2[r] = 0.f;
+#pragma unroll 8
+        for (int vv = 0; vv < V; ++vv) {
+            const float m = Mat[sw(col, vv)];
+            const float4 x = *reinterpret_cast<const float4*>(X1 + vv * BC + 4 * qtr);
+            const float4 y = *reinterpret_cast<const float4*>(X2 + vv * BC + 4 * qtr);
+            o1[0] = fmaf(x.x, m, o1[0]);
+            o1[1] = fmaf(x.y, m, o1[1]);
+            o1[2] = fmaf(x.z, m, o1[2]);
+            o1[3] = fmaf(x.w, m, o1[3]);
+            o2[0] = fmaf(y.x, m, o2[0]);
+            o2[1] = fmaf(y.y, m, o2[1]);
+            o2[2] = fmaf(y.z, m, o2[2]);
+            o2[3] = fmaf(y.w, m, o2[3]);
         }
     };
 
@@ -484,11 +505,11 @@ __global__ void __launch_bounds__(BNT, 1) kda_chunk_bwd_kernel(const BwdArgs<IO>
         float dq_r[4] = {0.f, 0.f, 0.f, 0.f}, dk_r[4] = {0.f, 0.f, 0.f, 0.f};
         float dG_r[4] = {0.f, 0.f, 0.f, 0.f};
         float dgl_part = 0.f;
-        transpose_cv(Dl);
+        transpose_cv(XT, Dl);
         __syncthreads();
         if (col < K) {  // dKt = Delta dS^T
             float x[4];
-            contract_v(dS, x);
+            contract_v(dS, XT, x);
             const float gl = Gc[ci(col, (BC - 1))];
 #pragma unroll
             for (int r = 0; r < 4; ++r) {
@@ -500,37 +521,34 @@ __global__ void __launch_bounds__(BNT, 1) kda_chunk_bwd_kernel(const BwdArgs<IO>
                 dgl_part += x[r] * kk * eL;
             }
         }
+        {  // the first part of dbeta_t, sum_v R_tv dY_tv (warp t), into the M slot (M is done)
+            const int t = warp;
+            float sr = 0.f;
+            for (int vv = lane; vv < V; vv += 32) sr = fmaf(Rv[t * VM + vv], dY[t * VM + vv], sr);
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) sr += __shfl_xor_sync(0xffffffffu, sr, off);
+            if (lane == 0) Mm[t] = sr;
+        }
         __syncthreads();
-        transpose_cv(dO);
+        // dO^T and dY^T (the latter in the R slot, R is done) for one pass over S
+        transpose_cv(XT, dO);
+        transpose_cv(Rv, dY);
         __syncthreads();
-        if (col < K) {  // dQg = scale dO S^T
-            float x[4];
-            contract_v(S, x);
+        if (col < K) {  // dQg = scale dO S^T and P = dY S^T, dKg = -diag(beta) P
+            float x[4], y[4];
+            contract_v2(S, XT, Rv, x, y);
 #pragma unroll
             for (int r = 0; r < 4; ++r) {
                 const int t = 4 * qtr + r;
                 const float Ga = expf(Gc[ci(col, t)]);
                 const float dqg = a.scale * x[r];
+                const float dkg = -bet[t] * y[r];
                 dq_r[r] += dqg * Ga;
-                dG_r[r] += dqg * Qr[ci(col, t)] * Ga;
-            }
-        }
-        __syncthreads();
-        transpose_cv(dY);
-        __syncthreads();
-        if (col < K) {  // P = dY S^T, dKg = -diag(beta) P
-            float x[4];
-            contract_v(S, x);
-#pragma unroll
-            for (int r = 0; r < 4; ++r) {
-                const int t = 4 * qtr + r;
-                const float Ga = expf(Gc[ci(col, t)]);
-                const float dkg = -bet[t] * x[r];
                 dk_r[r] += dkg * Ga;
-                dG_r[r] += dkg * Kr[ci(col, t)] * Ga;
+                dG_r[r] += (dqg * Qr[ci(col, t)] + dkg * Kr[ci(col, t)]) * Ga;
             }
         }
-            // dM (i <= t) and dB (i < t): warp t, lanes over value columns, reduced together
+        // dM (i <= t) and dB (i < t): warp t, lanes over value columns, reduced together
         {
             const int t = warp;
             float ot[4], yt[4];
@@ -565,17 +583,12 @@ __global__ void __launch_bounds__(BNT, 1) kda_chunk_bwd_kernel(const BwdArgs<IO>
         }
         __syncthreads();
         if (n > 0) prefetch_state(n - 1);  // S is not read again in this chunk
-        // dbeta_t = sum_v R_tv dY_tv + sum_{i<t} A'_ti dB_ti  (warp t);  dV = diag(beta) dY
-        {
-            const int t = warp;
-            float s = 0.f;
-            for (int vv = lane; vv < V; vv += 32) s = fmaf(Rv[t * VM + vv], dY[t * VM + vv], s);
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
-            if (lane == 0 && t < cn) {
-                for (int i = 0; i < t; ++i) s = fmaf(Ap[t * BC + i], dB[t * BC + i], s);
-                a.dbeta[bh * T + t0 + t] = s;
-            }
+        // dbeta_t = sum_v R_tv dY_tv (above) + sum_{i<t} A'_ti dB_ti;  dV = diag(beta) dY
+        if (tid < cn) {
+            const int t = tid;
+            float s = Mm[t];
+            for (int i = 0; i < t; ++i) s = fmaf(Ap[t * BC + i], dB[t * BC + i], s);
+            a.dbeta[bh * T + t0 + t] = s;
         }
         for (int idx = tid; idx < cn * V; idx += BNT) {
             const int t = idx / V, vv = idx - t * V;
