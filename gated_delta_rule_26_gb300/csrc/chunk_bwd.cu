@@ -653,7 +653,7 @@ __global__ void __launch_bounds__(BNT, 1) kda_chunk_bwd_kernel(const BwdArgs<IO>
                 dS[sw(c, col)] = acc;
             }
         }
-        __syncthreads();  // every read of XT (dY^T) and of red is done
+        __syncthreads();  // every read of XT and of red is done
         // dG exchange ([BC][KM] in XT), the last token's share of d(G_last), reverse cumsum,
         // gate derivative; dq and dk out
         if (col < K) {
