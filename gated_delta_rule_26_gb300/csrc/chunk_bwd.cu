@@ -23,7 +23,7 @@
 //     dS <- diag(gamma) dS + scale Qg^T dO - Kg^T diag(beta) dY,
 // then dg = the reverse in-chunk cumulative sum of dG and the gate's own derivative:
 //     dz = dg (-e^{A_log}) sigmoid(z + dt_bias), ddt_bias += dz, dA_log += dg g.
-// The state and its adjoint sit in shared memory (XOR-swizzled so that both row and column
+// The state and its adjoint sit in shared memory (rows of odd pitch, so that both row and column
 // walks are free of bank conflicts); every per-(token, channel) gradient term is produced by
 // the same thread, so dq, dk and dG accumulate in registers.
 #include "common.cuh"
@@ -36,10 +36,11 @@ constexpr int BNT = 512;  // threads per CTA
 constexpr int KM = 128, VM = 128;
 
 // shared memory map (floats)
-constexpr int O_S = 0;                    // S   [KM][VM], (c, v) at sw(c, v)
-constexpr int O_DS = O_S + KM * VM;       // dS  [KM][VM]
+constexpr int SP = VM + 1;                // row pitch of S and dS
+constexpr int O_S = 0;                    // S   [KM][SP], (c, v) at sw(c, v)
+constexpr int O_DS = O_S + KM * SP;       // dS  [KM][SP]
 constexpr int GP = BC + 1;                // row pitch of the channel-major q, k, G tiles
-constexpr int O_Q = O_DS + KM * VM;       // q   [KM][GP]: (c, t) at ci(c, t)
+constexpr int O_Q = O_DS + KM * SP;       // q   [KM][GP]: (c, t) at ci(c, t)
 constexpr int O_K = O_Q + KM * GP;        // k   [KM][GP]
 constexpr int O_G = O_K + KM * GP;        // G   [KM][GP] (natural log units)
 constexpr int O_KGT = O_G + KM * GP;      // Kg  [KM][BC]
@@ -62,7 +63,9 @@ constexpr int SMEM_FLOATS = O_RED + 4 * KM;
 constexpr size_t BWD_SMEM_BYTES = sizeof(float) * SMEM_FLOATS;
 static_assert(BWD_SMEM_BYTES <= 232448, "backward shared memory");
 
-__device__ __forceinline__ int sw(int c, int v) { return c * VM + (v ^ (c & 31)); }
+// S and dS rows have an odd pitch: a warp walking one row (32 v) or one column (32 c) hits
+// 32 distinct banks, and every walk is a constant stride.
+__device__ __forceinline__ int sw(int c, int v) { return c * SP + v; }
 // q, k and G: channel-major with an odd pitch, so that a warp over 32 channels of one token
 // and a warp over (2 channels x 16 tokens) both hit distinct banks
 __device__ __forceinline__ int ci(int c, int t) { return c * GP + t; }
@@ -150,7 +153,7 @@ __global__ void __launch_bounds__(BNT, 1) kda_chunk_bwd_kernel(const BwdArgs<IO>
     // thread roles: (v or c) = tid % 128, quarter = tid / 128
     const int col = tid & 127, qtr = tid >> 7;
 
-    // Copy a (K, V) float32 matrix from global memory into a swizzled shared one (zero when
+    // Copy a (K, V) float32 matrix from global memory into a padded shared one (zero when
     // src is null): every load is issued before the first store.
     auto load_kv = [&](float* dst, const float* src) {
         float x[32];
