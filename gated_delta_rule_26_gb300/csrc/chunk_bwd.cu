@@ -26,6 +26,8 @@
 // The state and its adjoint sit in shared memory (rows of odd pitch, so that both row and column
 // walks are free of bank conflicts); every per-(token, channel) gradient term is produced by
 // the same thread, so dq, dk and dG accumulate in registers.
+#include <type_traits>
+
 #include "common.cuh"
 
 namespace kda {
@@ -117,7 +119,9 @@ __device__ __forceinline__ float sigmoid_f32(float x) {
     return x >= 0.f ? 1.f / (1.f + expf(-x)) : expf(x) / (1.f + expf(x));
 }
 
-template <typename IO>
+// KC = 128: the instance for K = V = 128, where every loop bound and size guard is a
+// constant; KC = 0: any K, V in the supported range.
+template <typename IO, int KC>
 __global__ void __launch_bounds__(BNT, 1) kda_chunk_bwd_kernel(const BwdArgs<IO> a) {
     extern __shared__ float4 smem_f4[];
     float* sm = reinterpret_cast<float*>(smem_f4);
@@ -144,7 +148,7 @@ __global__ void __launch_bounds__(BNT, 1) kda_chunk_bwd_kernel(const BwdArgs<IO>
     float* red = sm + O_RED;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int K = a.K, V = a.V, T = a.T;
+    const int K = KC ? KC : a.K, V = KC ? KC : a.V, T = a.T;
     const size_t bh = blockIdx.x;
     const int h = (int)(bh % a.H);
     const int N = (T + BC - 1) / BC;
@@ -751,8 +755,9 @@ cudaError_t launch_chunk_backward(const BwdLaunch& L, cudaStream_t s) {
     float* ddt_part = dA_part + BH;
     float* ckpt = reinterpret_cast<float*>(scratch + ((part_bytes + 255) & ~(size_t)255));
     float* rd = ckpt + BH * (size_t)N * K * V;
-    auto run = [&](auto io_tag) -> cudaError_t {
+    auto run = [&](auto io_tag, auto kc_tag) -> cudaError_t {
         using IO = decltype(io_tag);
+        constexpr int KC = decltype(kc_tag)::value;
         BwdArgs<IO> a;
         a.H = H; a.T = T; a.K = K; a.V = V;
         a.q = static_cast<const IO*>(L.q); a.k = static_cast<const IO*>(L.k);
@@ -761,14 +766,20 @@ cudaError_t launch_chunk_backward(const BwdLaunch& L, cudaStream_t s) {
         a.A_log = L.A_log; a.dt_bias = L.dt_bias; a.h0 = L.h0; a.dhT = L.dhT; a.scale = L.scale;
         a.dq = L.dq; a.dk = L.dk; a.dv = L.dv; a.dz = L.dz; a.dbeta = L.dbeta; a.dh0 = L.dh0;
         a.ckpt = ckpt; a.rd = rd; a.dA_part = dA_part; a.ddt_part = ddt_part;
-        cudaError_t err = cudaFuncSetAttribute(kda_chunk_bwd_kernel<IO>,
+        cudaError_t err = cudaFuncSetAttribute(kda_chunk_bwd_kernel<IO, KC>,
                                                cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                (int)BWD_SMEM_BYTES);
         if (err != cudaSuccess) return err;
-        kda_chunk_bwd_kernel<IO><<<(unsigned)BH, BNT, BWD_SMEM_BYTES, s>>>(a);
+        kda_chunk_bwd_kernel<IO, KC><<<(unsigned)BH, BNT, BWD_SMEM_BYTES, s>>>(a);
         return cudaGetLastError();
     };
-    e = L.io == KDA_BF16 ? run(__nv_bfloat16{}) : run(float{});
+    using Fixed = std::integral_constant<int, 128>;
+    using Any = std::integral_constant<int, 0>;
+    const bool fixed = K == 128 && V == 128;
+    if (L.io == KDA_BF16)
+        e = fixed ? run(__nv_bfloat16{}, Fixed{}) : run(__nv_bfloat16{}, Any{});
+    else
+        e = fixed ? run(float{}, Fixed{}) : run(float{}, Any{});
     if (e == cudaSuccess) {
         const int n = H * K;
         kda_bwd_reduce_kernel<<<(n + 255) / 256, 256, 0, s>>>(B, H, K, dA_part, ddt_part, L.dA_log,
