@@ -18,6 +18,8 @@ by step:
   the state gradient).  Pinned by ``jvp`` below and by central differences.
 * ``jvp``        -- forward-mode derivative (tangent propagation) of the same forward,
   written separately in numpy: the directional derivative of <d_o, o> + <dhT, hT>.
+* ``chunked_backward.chunked_backward`` -- the backward organised as chunk-level adjoint
+  equations (the form the GPU kernel takes), checked against ``backward`` in the tests.
 * ``chunked.chunked_wy`` -- an independent f64 chunked (WY) evaluation of the
   same function, used to check that the chunked and recurrent forms agree
   (kda-adjoint-2026-10-01, section 2: carry with decay_last = exp(G_last - G)).
