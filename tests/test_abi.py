@@ -135,3 +135,16 @@ def test_backward_rejects_bad_arguments(lib):
     assert _bwd(lib, Dims(1, 1, 8, 128, 128), misalign=4) == -3
     assert _bwd(lib, Dims(1, 1, 8, 128, 128), null_do=True) == -1
     assert _bwd(lib, Dims(1, 1, 8, 128, 128), null_dq=True) == -1
+
+
+def test_header_is_plain_c_and_links_against_the_library(tmp_path):
+    """include/kda.h compiles as C99 (no C++ or CUDA types in the signatures), and a C program
+    that takes the address of every declared entry point links against libkda."""
+    names = declared_functions()
+    src = tmp_path / "use_kda.c"
+    body = "\n".join(f"    (void)&{n};" for n in names)
+    src.write_text('#include "kda.h"\nint main(void) {\n' + body + "\n    return 0;\n}\n")
+    exe = tmp_path / "use_kda"
+    lib_dir = os.path.dirname(kbuild.build())
+    subprocess.run(["gcc", "-std=c99", "-Wall", "-Werror", "-I", os.path.join(ROOT, "include"),
+                    str(src), "-o", str(exe), "-L", lib_dir, "-lkda"], check=True)
