@@ -318,9 +318,14 @@ def run_backward(args, kda, inputs, peaks, ws, barrier):
     d = inp.to("cuda")
     d_o, dhT = adj.d_o.to("cuda"), adj.dhT.to("cuda")
 
+    from gated_delta_rule_26_gb300 import dist as kdist
+
     def step():
-        kda.chunk_backward(d.q, d.k, d.v, d.z, d.beta, d.A_log, d.dt_bias, d_o, inp.scale,
-                           h0=d.h0, dhT=dhT)
+        g = kda.chunk_backward(d.q, d.k, d.v, d.z, d.beta, d.A_log, d.dt_bias, d_o, inp.scale,
+                               h0=d.h0, dhT=dhT)
+        # data parallel over ranks: the gate parameters' gradients are summed over all ranks'
+        # batches (one all-reduce of H + H K floats; nothing on one GPU)
+        kdist.sum_param_grads(g)
 
     for _ in range(2):
         step()
@@ -328,7 +333,6 @@ def run_backward(args, kda, inputs, peaks, ws, barrier):
     n0 = kda.launch_count()
     secs = timed(step, args.backward_steps, stream)
     launches = kda.launch_count() - n0
-    from gated_delta_rule_26_gb300 import dist as kdist
     secs = kdist.max_over_ranks(secs, device="cuda")
     per = secs / args.backward_steps
     C = 16
@@ -346,7 +350,9 @@ def run_backward(args, kda, inputs, peaks, ws, barrier):
                         "kernel": "kda_chunk_bwd_kernel (+ the batch sum of dA_log, ddt_bias)"},
            "gpu_launches": launches,
            "config": {"workload": f"{WORKLOAD} backward B{B} H{H} T{T} K={K} V={V}, "
-                                  "bf16 inputs, fp32 gradients, dL/dhT given"}}
+                                  "bf16 inputs, fp32 gradients, dL/dhT given",
+                      "parallelism": (f"data parallel x{ws}: batch per rank, dA_log and "
+                                      "ddt_bias all-reduced") if ws > 1 else "single GPU"}}
     del d, d_o, dhT
     torch.cuda.empty_cache()
     return res
