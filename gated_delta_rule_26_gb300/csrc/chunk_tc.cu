@@ -1223,17 +1223,18 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
+// A driver API entry point, looked up through the runtime (no -lcuda link); null if absent.
+void* driver_entry(const char* name) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion(name, &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+        return nullptr;
+    return p;
+}
+
 EncodeTiledFn encode_fn() {
-    // The driver entry point is looked up once through the runtime (no -lcuda link).
-    static EncodeTiledFn fn = []() -> EncodeTiledFn {
-        void* p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                             &q) != cudaSuccess ||
-            q != cudaDriverEntryPointSuccess)
-            return nullptr;
-        return reinterpret_cast<EncodeTiledFn>(p);
-    }();
+    static EncodeTiledFn fn = reinterpret_cast<EncodeTiledFn>(driver_entry("cuTensorMapEncodeTiled"));
     return fn;
 }
 
@@ -1274,6 +1275,23 @@ int sm_count() {
 size_t round_up(size_t x, size_t m) { return (x + m - 1) / m * m; }
 
 }  // namespace
+
+// Unique id of the CUDA context current on this thread (0 when none is current yet).  A
+// device's primary context gets a new id when it is destroyed and created again (after
+// cudaDeviceReset); per-device caches of device addresses and CUDA objects compare it to
+// notice that what they hold belonged to a context that no longer exists.
+cudaError_t current_context_id(unsigned long long* id) {
+    typedef CUresult (*GetCurrentFn)(CUcontext*);
+    typedef CUresult (*GetIdFn)(CUcontext, unsigned long long*);
+    static GetCurrentFn get_current = reinterpret_cast<GetCurrentFn>(driver_entry("cuCtxGetCurrent"));
+    static GetIdFn get_id = reinterpret_cast<GetIdFn>(driver_entry("cuCtxGetId"));
+    *id = 0;
+    if (!get_current || !get_id) return cudaErrorNotSupported;
+    CUcontext ctx = nullptr;
+    if (get_current(&ctx) != CUDA_SUCCESS) return cudaErrorUnknown;
+    if (!ctx) return cudaSuccess;
+    return get_id(ctx, id) == CUDA_SUCCESS ? cudaSuccess : cudaErrorUnknown;
+}
 
 // A wait that nothing ever satisfies: one thread initialises an mbarrier that expects one
 // arrival, never arrives, and waits with the bounded wait every kernel here uses.  The wait
@@ -1372,6 +1390,37 @@ cudaError_t run_chunk_split(const ChunkArgs& a, cudaStream_t s, void* scratch, s
     return cudaSuccess;
 }
 
+// The second stream and the five events of the overlapped split form below: created on the
+// first call on a device (and again after that device's context was reset), then kept and
+// shared by every call on the device.  A call holds `mu` while it enqueues its work, so no
+// other call records the same events in between.
+constexpr int kMaxDevices = 64;
+struct OverlapRes {
+    std::mutex mu;
+    unsigned long long ctx = 0;
+    cudaStream_t s2 = nullptr;
+    cudaEvent_t ev[5] = {};  // fork, prep done [2], carry done [2]
+};
+OverlapRes g_overlap[kMaxDevices];
+
+// Makes r's stream and events valid for the current context (r.mu held).
+cudaError_t overlap_res_ready(OverlapRes& r) {
+    unsigned long long ctx = 0;
+    cudaError_t err = current_context_id(&ctx);
+    if (err != cudaSuccess) return err;
+    if (ctx != 0 && ctx == r.ctx) return cudaSuccess;
+    // first use, or the objects held belong to a context that is gone: make new ones
+    r.ctx = 0;
+    r.s2 = nullptr;
+    for (cudaEvent_t& e : r.ev) e = nullptr;
+    if ((err = cudaStreamCreateWithFlags(&r.s2, cudaStreamNonBlocking)) != cudaSuccess) return err;
+    for (cudaEvent_t& e : r.ev)
+        if ((err = cudaEventCreateWithFlags(&e, cudaEventDisableTiming)) != cudaSuccess) return err;
+    if ((err = current_context_id(&ctx)) != cudaSuccess) return err;
+    r.ctx = ctx;
+    return cudaSuccess;
+}
+
 // The split form with the carry of segment i (one CTA per sequence, on a second stream)
 // running beside the prep of segment i + 1 (on the remaining SMs): two operand buffers,
 // events between the streams, `s` waits for all of it at the end.  For few sequences
@@ -1398,12 +1447,15 @@ cudaError_t run_chunk_split_overlap(const ChunkArgs& a, cudaStream_t s, void* sc
                                            cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            (int)SMEM_BYTES);
     if (err != cudaSuccess) return err;
-    cudaStream_t s2 = nullptr;
-    cudaEvent_t ev[5] = {};  // fork, prep done [2], carry done [2]
-    if ((err = cudaStreamCreateWithFlags(&s2, cudaStreamNonBlocking)) != cudaSuccess) return err;
-    for (int e = 0; e < 5 && err == cudaSuccess; ++e)
-        err = cudaEventCreateWithFlags(&ev[e], cudaEventDisableTiming);
-    if (err == cudaSuccess) err = cudaEventRecord(ev[0], s);
+    int dev = 0;
+    if ((err = cudaGetDevice(&dev)) != cudaSuccess) return err;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    OverlapRes& res = g_overlap[dev];
+    std::lock_guard<std::mutex> lock(res.mu);
+    if ((err = overlap_res_ready(res)) != cudaSuccess) return err;
+    cudaStream_t s2 = res.s2;
+    cudaEvent_t* ev = res.ev;
+    err = cudaEventRecord(ev[0], s);
     if (err == cudaSuccess) err = cudaStreamWaitEvent(s2, ev[0], 0);
     const int prep_grid = max(1, nsm - BH);  // leave one SM per carry CTA
     for (int n0 = 0, i = 0; n0 < N && err == cudaSuccess; n0 += seg_len, ++i) {
@@ -1425,9 +1477,6 @@ cudaError_t run_chunk_split_overlap(const ChunkArgs& a, cudaStream_t s, void* sc
     const cudaError_t jerr = cudaEventRecord(ev[0], s2) == cudaSuccess
                                  ? cudaStreamWaitEvent(s, ev[0], 0)
                                  : cudaErrorUnknown;
-    for (int e = 0; e < 5; ++e)
-        if (ev[e]) cudaEventDestroy(ev[e]);
-    cudaStreamDestroy(s2);
     return err != cudaSuccess ? err : jerr;
 }
 
@@ -1544,55 +1593,15 @@ bool prefer_split(const ChunkArgs& a) {
 
 }  // namespace
 
-// ---- the split form without allocation (kda_chunk_forward_split_noalloc)
-//
-// Some callers cannot allocate device memory while they run this forward: a serving loop
-// whose memory is carved up up front, code running where an allocation could stall or
-// fail at the wrong moment.  For them the split form's per-chunk operands go to one fixed
-// array in device memory instead of cudaMallocAsync scratch.  Every GPU that loads this
-// library reserves the array until the process exits, so it is kept modest; inputs longer
-// than it holds are processed in consecutive segments of chunks, and only the number of
-// sequences B * H is bounded (see kda_chunk_forward_split_noalloc in kda.h).
-constexpr size_t kNoAllocScratchBytes = size_t(64) << 20;
-static __device__ __align__(256) uint8_t g_kda_noalloc_scratch[kNoAllocScratchBytes];
-
-namespace {
-
-constexpr int kMaxDevices = 64;
-
-// Device address of the array on the current device.  Host code cannot use the array's name
-// as an address, so it is looked up with cudaGetSymbolAddress, once per device, on the first
-// call made with that device current.
-cudaError_t noalloc_scratch(void** p) {
-    static std::mutex mu;
-    static void* addr[kMaxDevices] = {};
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-    std::lock_guard<std::mutex> lock(mu);
-    if (!addr[dev]) {
-        void* q = nullptr;
-        e = cudaGetSymbolAddress(&q, g_kda_noalloc_scratch);
-        if (e != cudaSuccess) return e;
-        addr[dev] = q;
-    }
-    *p = addr[dev];
-    return cudaSuccess;
+// The split form on caller-provided scratch of `bytes` (no allocation of its own).
+// chunk_split_fits: whether the shape takes the split form and one segment of a chunk per
+// sequence fits in `bytes`; run_chunk_split_in then runs it.  Every byte of the scratch that
+// a call reads, the same call wrote first.
+bool chunk_split_fits(const ChunkArgs& a, size_t bytes) {
+    return chunk_tc_eligible(a) && split_segment_len(a, bytes) >= 1;
 }
-
-}  // namespace
-
-// The split form on the fixed array.  *fits = false (nothing launched) when one segment of a
-// chunk per sequence does not fit in it.  Nothing in the array needs clearing: every byte a
-// call reads was written earlier by the same call.
-cudaError_t launch_chunk_split_noalloc(const ChunkArgs& a, cudaStream_t s, bool* fits) {
-    *fits = chunk_tc_eligible(a) && split_segment_len(a, kNoAllocScratchBytes) >= 1;
-    if (!*fits) return cudaSuccess;
-    void* p = nullptr;
-    const cudaError_t e = noalloc_scratch(&p);
-    if (e != cudaSuccess) return e;
-    return run_chunk_split(a, s, p, kNoAllocScratchBytes);
+cudaError_t run_chunk_split_in(const ChunkArgs& a, cudaStream_t s, void* scratch, size_t bytes) {
+    return run_chunk_split(a, s, scratch, bytes);
 }
 
 // mode 0: pick the faster form, 1: fused kernel, 2: split form.

@@ -31,7 +31,8 @@
  *   dt_bias (and, for kda_recurrent_step and kda_gate, the per-token vectors)
  *   need only their element alignment.
  * - The caller owns every buffer.  The library keeps no state between calls
- *   except the CUDA resources the runtime itself caches; it is re-entrant.
+ *   except the CUDA resources the runtime itself caches, the split form's second
+ *   stream and the no-alloc form's fixed array (both below); it is re-entrant.
  *   Scratch memory, where a path needs it, is taken with cudaMallocAsync on the
  *   caller's stream and released on the same stream before the call returns.
  * - Work is enqueued on `stream` (NULL = the legacy default stream); calls
@@ -116,9 +117,12 @@ int kda_chunk_forward(const kda_dims* dims, kda_dtype io_dtype, const void* q, c
  *           the call allocates and frees on `stream` (cudaMallocAsync / cudaFreeAsync, at most
  *           1 GiB: longer inputs run as consecutive segments of chunks); KDA_ERR_NO_MEMORY if
  *           that allocation fails.  With B*H at most half the SMs and four or more chunks,
- *           the call runs each segment's carry on a second stream of its own, beside the next
- *           segment's prep, with two operand buffers; that stream is created and destroyed
- *           by the call and joined back into `stream` (events) before it returns.
+ *           the call runs each segment's carry on a second stream, beside the next segment's
+ *           prep, with two operand buffers, and joins it back into `stream` (events) before
+ *           it returns.  That stream and its five events are created on the first such call
+ *           on a device (and again after the device's context was reset) and kept until the
+ *           process exits; calls on one device enqueue this part one at a time (a lock), and
+ *           their carries share that stream.
  */
 int kda_chunk_forward_split(const kda_dims* dims, kda_dtype io_dtype, const void* q,
                             const void* k, const void* v, const void* z, const void* beta,
@@ -136,15 +140,18 @@ int kda_chunk_forward_fused(const kda_dims* dims, kda_dtype io_dtype, const void
  * device memory during the call (memory budgeted up front by a serving runtime, code where an
  * allocation may stall or fail at the wrong moment).  The pages this library follows have no
  * counterpart: it is the same computation, with the per-chunk operands kept in one fixed
- * array of 64 MiB that every GPU loading the library reserves until the process exits.  The
- * call makes no cudaMalloc / cudaMallocAsync / cudaFree call of its own.
+ * array of 64 MiB, reserved on each GPU where this entry point is called (the library loads
+ * its module lazily), until the process exits.  The call makes no cudaMalloc /
+ * cudaMallocAsync / cudaFree call of its own.
  *   Limit: one chunk of every sequence must fit, i.e. B*H*82,432 bytes, plus B*H*65,536 when
  *   hT is NULL (the carried state then lives in the array too), at most 64 MiB: B*H <= 814
  *   with hT, B*H <= 453 without.  Larger B*H returns KDA_ERR_UNSUPPORTED and launches
  *   nothing.  Any T: longer inputs run as consecutive segments of chunks.
  *   Shapes as kda_chunk_forward_split (bf16, K = V = 128, chunk 64, T >= 1).
  *   The first call on each device looks up the array's device address (cudaGetSymbolAddress
- *   with that device current); make that first call before any stream capture.
+ *   with that device current); make that first call before any stream capture.  After a
+ *   cudaDeviceReset the next call looks it up again (the array may have moved), so that
+ *   call too belongs outside a capture.
  *   All calls share the array and it keeps the last call's contents; nothing needs clearing
  *   (every byte a call reads, the same call wrote first).  Calls that overlap on the GPU
  *   (other streams, other host threads) race on it: serialise them.
