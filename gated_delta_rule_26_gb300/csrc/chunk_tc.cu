@@ -24,8 +24,9 @@
 //       e^{G_t - G_i} = e^{G_t - G_r} e^{G_r - G_i} with both factors <= 1.  Levels
 //       h = 32, 16, 8, 4 go two per tcgen05 GEMM (each level's upper k and q rows against
 //       its lower k rows, tokens in rank order); an epilogue scatters them to A and M.
-//   P4  T = (I + A)^{-1}: 16 x 16 diagonal blocks by forward substitution, then two
-//       block merges (16 -> 32 -> 64, T_21 = -T_22 A_21 T_11), fp32 on CUDA cores.
+//   P4  T = (I + A)^{-1}: 16 x 16 diagonal blocks by forward substitution (fp32, CUDA
+//       cores), then the block merges T_21 = -T_22 A_21 T_11 (16 -> 32 for both halves at
+//       once, then 32 -> 64) as four small tcgen05 products with bf16 operands.
 //   P5  W^T = (diag(beta) K Gamma)^T T^T and U^T = (diag(beta) V)^T T^T  (tcgen05), then
 //       Q'^T = (Q Gamma)^T I - W^T M^T (identity and negated-B MMAs) and U'^T = U^T M^T,
 //       so that o = scale (Q' S + U') and Delta = U - W S come from ONE product with S.
@@ -74,13 +75,13 @@ constexpr uint32_t OFF_MISC = OFF_ID + 8192;
 // multi-use region, in order of use within a chunk
 constexpr uint32_t LV_PA = 0;       // level pair A operand, K-major 128 rows (32 KB)   P3
 constexpr uint32_t LV_PB = 32768;   // level pair B operand, K-major 64 rows (16 KB)    P3
-constexpr uint32_t LV_AF = 0;       // A fp32 [t][i] (16 KB, swizzled)       P3-P4
+constexpr uint32_t LV_AF = 0;       // A fp32 [t][i] (16 KB, swizzled; diagonal 16 x 16 blocks)  P3-P4
 constexpr uint32_t LV_MB = 16384;   // M bf16 K-major [t][i] (8 KB)          P3-P5
 constexpr uint32_t LV_TB = 24576;   // T bf16 K-major [t][i] (8 KB)          P4-P5
 constexpr uint32_t LV_QG = 32768;   // Q Gamma, MN-major [t][c] (16 KB)      P4-P5
 constexpr uint32_t LV_UT = 0;       // U^T K-major [v][i] (16 KB)            P5
 constexpr uint32_t LV_Z = 49152;    // z tile of the NEXT chunk (16 KB)      P5-P2
-constexpr uint32_t LV_TF = 49152;   // T fp32 [t][i] (16 KB, swizzled), in the z slot   P4
+constexpr uint32_t LV_AB = 49152;   // A bf16 K-major [t][i] (8 KB), in the z slot         P3-P4
 constexpr uint32_t LV_DELTA = 16384;// Delta^T K-major [v][t] (16 KB)        C2-C3
 constexpr uint32_t LV_UPS = 32768;  // prep kernel: U'^T staging, K-major [v][t] (16 KB)
 // K~ (K e^{G_last - G}, MN-major [t][c]) lives in the v-tile slot OFF_V from P5 to C3.
@@ -117,6 +118,8 @@ constexpr uint32_t IDESC_QU = tc::idesc_bf16(128, 64, 0, 0);
 constexpr uint32_t IDESC_QNEG = tc::idesc_bf16(128, 64, 0, 0) | (1u << 14);  // negate B
 constexpr uint32_t IDESC_SQ = tc::idesc_bf16(128, 128, 1, 1);
 constexpr uint32_t IDESC_SK = tc::idesc_bf16(128, 128, 1, 0);
+constexpr uint32_t IDESC_MG64 = tc::idesc_bf16(128, 64, 0, 1);  // inverse merges
+constexpr uint32_t IDESC_MG32 = tc::idesc_bf16(128, 32, 0, 1);
 
 // G2 (fp32, 64 tokens x 128 channels) keeps each row as two halves: channel
 // c = 8 a + 4 h + j sits at 64 h + 4 a + j, so that both the 8-channel groups read by
@@ -649,6 +652,13 @@ __device__ __forceinline__ void chunk_loop(const CUtensorMap* tm_q, const CUtens
                             *reinterpret_cast<uint4*>(MB + kmaj_off(t, i0 + 8, 64)) =
                                 make_uint4(pk[4], pk[5], pk[6], pk[7]);
                     }
+                } else if (any && p == 0) {
+                    // levels 32 and 16 lie off the 16 x 16 diagonal blocks: bf16, for the merges
+                    const float bt = ms.beta[t];
+                    float a16[16];
+#pragma unroll
+                    for (int k = 0; k < 16; ++k) a16[k] = bt * w[k];
+                    store16_k(sm + OFF_LVL + LV_AB, t, i0, 64, a16);
                 } else if (any) {
                     const float bt = ms.beta[t];
 #pragma unroll
@@ -691,14 +701,16 @@ __device__ __forceinline__ void chunk_loop(const CUtensorMap* tm_q, const CUtens
         tc::fence_before_sync();
         __syncthreads();
         // ---------------------------------------------------------------- P4: T = (I + A)^{-1}
+        // T (bf16, K-major [t][i] in LV_TB) blockwise: the four 16 x 16 diagonal blocks by
+        // forward substitution on CUDA cores in fp32 (from the diagonal blocks of Af), then the
+        // block merges T_RC = -T_RR A_RC T_CC as tcgen05 products (bf16 operands, fp32
+        // accumulation): 16 -> 32 for both halves at once, then 32 -> 64.
         {
             const float* Af = reinterpret_cast<const float*>(sm + OFF_LVL + LV_AF);
-            float* Tf = reinterpret_cast<float*>(sm + OFF_LVL + LV_TF);  // free until P5
-            // Every A and T access below moves a 16-byte group (4 consecutive columns); the
-            // XOR swizzle keeps the groups a warp touches in distinct banks.
-            // (a) the four 16 x 16 diagonal blocks by forward substitution, one column each
-            //     (left-looking: x_t = delta_tj - sum_{i<t} A_ti x_i); the other threads clear the
-            //     strictly upper blocks.
+            uint8_t* TB = sm + OFF_LVL + LV_TB;
+            // (a) the diagonal blocks, one column each (left-looking: x_t = delta_tj -
+            //     sum_{i<t} A_ti x_i); the other threads clear the off-diagonal blocks of T
+            //     and the blocks of A_bf that the merges multiply by zero, and build Q Gamma.
             if (tid < 64) {
                 const int R = tid >> 4, j = tid & 15;
                 const float* Ab = Af + 16 * R * 64;  // rows 16R.. ; (row & 15) == t
@@ -726,20 +738,32 @@ __device__ __forceinline__ void chunk_loop(const CUtensorMap* tm_q, const CUtens
                     }
                     x[t] = ((t == j) ? 1.f : 0.f) - ((acc[0] + acc[1]) + (acc[2] + acc[3]));
                 }
-                float* Tb = Tf + 16 * R * 64;
 #pragma unroll
                 for (int t = 0; t < 16; ++t)
-                    Tb[t * 64 + ((((4 * R + (j >> 2)) ^ t)) << 2) + (j & 3)] = x[t];
+                    *reinterpret_cast<__nv_bfloat16*>(TB + kmaj_off(16 * R + t, 16 * R + j, 64)) =
+                        __float2bfloat16_rn(x[t]);
             } else {
-                for (int e = tid - 64; e < 6 * 64; e += NT - 64) {  // 6 blocks x 64 float4
-                    const int blk = e >> 6, q = e & 63;
-                    const int R = blk < 3 ? 0 : (blk < 5 ? 1 : 2);
-                    const int Cb = blk < 3 ? blk + 1 : (blk < 5 ? blk - 1 : 3);
-                    const int t = 16 * R + (q >> 2), i = 16 * Cb + (q & 3) * 4;
-                    *reinterpret_cast<float4*>(Tf + swz(t, i)) = make_float4(0.f, 0.f, 0.f, 0.f);
+                // 16-byte groups of zeros: the 12 off-diagonal 16 x 16 blocks of T, and the 10
+                // blocks of A_bf on or above the diagonal (the merges read them against zeros
+                // of T; they must hold finite values)
+                for (int e = tid - 64; e < 22 * 32; e += NT - 64) {
+                    const int blk = e >> 5, q = e & 31;
+                    int R, Cb;
+                    uint8_t* base;
+                    if (blk < 12) {
+                        R = blk / 3;
+                        Cb = blk % 3 + (blk % 3 >= R ? 1 : 0);
+                        base = TB;
+                    } else {
+                        const int b2 = blk - 12;  // (R, Cb >= R) in row order
+                        R = b2 < 4 ? 0 : (b2 < 7 ? 1 : (b2 < 9 ? 2 : 3));
+                        Cb = R + b2 - (R == 0 ? 0 : (R == 1 ? 4 : (R == 2 ? 7 : 9)));
+                        base = sm + OFF_LVL + LV_AB;
+                    }
+                    *reinterpret_cast<uint4*>(base + kmaj_off(16 * R + (q >> 1), 16 * Cb + 8 * (q & 1), 64)) =
+                        make_uint4(0u, 0u, 0u, 0u);
                 }
-                // meanwhile the other warps build Q Gamma -> LV_QG (MN-major [t][c]), which does
-                // not depend on T
+                // meanwhile Q Gamma -> LV_QG (MN-major [t][c]), which does not depend on T
 #pragma unroll 1
                 for (int item = tid - 64; item < C * 16; item += NT - 64) {
                     const int t = item >> 4, c8 = item & 15;
@@ -751,132 +775,95 @@ __device__ __forceinline__ void chunk_loop(const CUtensorMap* tm_q, const CUtens
                     *reinterpret_cast<uint4*>(sm + OFF_LVL + LV_QG + mnmaj_off(t, c8 * 8, 8192)) = pack8(o);
                 }
             }
-            __syncthreads();
-        // ---------------------------------------------------------------- P4b: 16 -> 32 merge
-            // (b) 16 -> 32: T_RC = -T_RR (A_RC T_CC) for (R, C) = (1, 0), (3, 2);
-            //     warps 0-3, four adjacent outputs per thread
-            {
-                const int blk = tid >> 6, rr = (tid >> 2) & 15, cq = (tid & 3) * 4;
-                const int R = 2 * blk + 1, Cb = 2 * blk;
-                const int och = ((4 * Cb + (cq >> 2)) ^ rr) << 2;  // this thread's group in row rr
-                float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (tid < 128) {
-                    const float* arow = Af + (16 * R + rr) * 64;
+            KDA_SYNC_FOR_MMA();
+            // The four merge products.  Each is M = 128 rows of which the first 64 (or 32) are
+            // the blocks' rows: the other rows read whatever follows in shared memory and their
+            // results are never read.  T (LV_TB) serves as the K-major A operand [t][i] and, read
+            // MN-major, as the B operand T[k][n]; products go back to shared memory in the same
+            // K-major layout (row = TMEM lane) and are read MN-major by the next product.
+            // (b) 16 -> 32, first product: P = A_bf T_d  (T_d = the diagonal blocks; blocks (1,0)
+            //     and (3,2) of P are A_10 T_00 and A_32 T_22)
+            if (tid == 0) {
 #pragma unroll
-                    for (int g = 0; g < 2; ++g) {
-                        float4 tv[8];
-                        const float4 a4a = *reinterpret_cast<const float4*>(arow + (((4 * Cb + 2 * g) ^ rr) << 2));
-                        const float4 a4b = *reinterpret_cast<const float4*>(arow + (((4 * Cb + 2 * g + 1) ^ rr) << 2));
-#pragma unroll
-                        for (int u = 0; u < 8; ++u) {
-                            const int l = 8 * g + u;
-                            tv[u] = *reinterpret_cast<const float4*>(
-                                Tf + (16 * Cb + l) * 64 + (((4 * Cb + (cq >> 2)) ^ l) << 2));
-                        }
-                        const float av[8] = {a4a.x, a4a.y, a4a.z, a4a.w, a4b.x, a4b.y, a4b.z, a4b.w};
-#pragma unroll
-                        for (int u = 0; u < 8; ++u) {
-                            x.x = fmaf(av[u], tv[u].x, x.x); x.y = fmaf(av[u], tv[u].y, x.y);
-                            x.z = fmaf(av[u], tv[u].z, x.z); x.w = fmaf(av[u], tv[u].w, x.w);
-                        }
-                    }
-                    *reinterpret_cast<float4*>(Tf + (16 * R + rr) * 64 + och) = x;
-                }
-                __syncthreads();
-                float4 y = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (tid < 128) {
-                    const float* trow = Tf + (16 * R + rr) * 64;
-#pragma unroll
-                    for (int g = 0; g < 2; ++g) {
-                        float4 xv[8];
-                        const float4 a4a = *reinterpret_cast<const float4*>(trow + (((4 * R + 2 * g) ^ rr) << 2));
-                        const float4 a4b = *reinterpret_cast<const float4*>(trow + (((4 * R + 2 * g + 1) ^ rr) << 2));
-#pragma unroll
-                        for (int u = 0; u < 8; ++u) {
-                            const int l = 8 * g + u;
-                            xv[u] = *reinterpret_cast<const float4*>(
-                                Tf + (16 * R + l) * 64 + (((4 * Cb + (cq >> 2)) ^ l) << 2));
-                        }
-                        const float av[8] = {a4a.x, a4a.y, a4a.z, a4a.w, a4b.x, a4b.y, a4b.z, a4b.w};
-#pragma unroll
-                        for (int u = 0; u < 8; ++u) {
-                            y.x = fmaf(av[u], xv[u].x, y.x); y.y = fmaf(av[u], xv[u].y, y.y);
-                            y.z = fmaf(av[u], xv[u].z, y.z); y.w = fmaf(av[u], xv[u].w, y.w);
-                        }
-                    }
-                }
-                __syncthreads();
-                if (tid < 128)
-                    *reinterpret_cast<float4*>(Tf + (16 * R + rr) * 64 + och) =
-                        make_float4(-y.x, -y.y, -y.z, -y.w);
+                for (int ks = 0; ks < 4; ++ks)
+                    tc::mma_bf16(tmem + TM_D1, desc_k(sb + OFF_LVL + LV_AB, 64, ks),
+                                 desc_mn(sb + OFF_LVL + LV_TB, 8192, ks), IDESC_MG64, ks > 0);
+                tc::mma_commit(&ms.bar_m0);
             }
-            __syncthreads();
-        // ---------------------------------------------------------------- P4c: 32 -> 64 merge
-            // (c) 32 -> 64: T[32:64, 0:32] = -T[32:64, 32:64] (A[32:64, 0:32] T[0:32, 0:32]);
-            //     warps 0-7, four adjacent outputs per thread
-            {
-                const int rr = tid >> 3, cq = (tid & 7) * 4;
-                const int rx = rr & 15, cg = cq >> 2;
-                const int och = (cg ^ rx) << 2;
-                float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (tid < 256) {
-                    const float* arow = Af + (32 + rr) * 64;
-                    // loads are issued in batches of eight ahead of their FMAs
+            KDA_WAIT(bar_m0, ph0);
+            if (failed) break;
+            if (q4 < 2) {  // rows 0..63 of P -> bf16 tile in the v slot
+                uint32_t d[16];
+                tc::tmem_ld16(taddr(tmem, warp, TM_D1 + 16 * part), d);
+                tc::tmem_ld_wait();
+                float f[16];
 #pragma unroll
-                    for (int g = 0; g < 4; ++g) {
-                        float4 tv[8];
-                        const float4 a4a = *reinterpret_cast<const float4*>(arow + (((2 * g) ^ rx) << 2));
-                        const float4 a4b = *reinterpret_cast<const float4*>(arow + (((2 * g + 1) ^ rx) << 2));
-#pragma unroll
-                        for (int u = 0; u < 8; ++u) {
-                            const int l = 8 * g + u;
-                            tv[u] = *reinterpret_cast<const float4*>(Tf + l * 64 + ((cg ^ (l & 15)) << 2));
-                        }
-                        const float av[8] = {a4a.x, a4a.y, a4a.z, a4a.w, a4b.x, a4b.y, a4b.z, a4b.w};
-#pragma unroll
-                        for (int u = 0; u < 8; ++u) {
-                            x.x = fmaf(av[u], tv[u].x, x.x); x.y = fmaf(av[u], tv[u].y, x.y);
-                            x.z = fmaf(av[u], tv[u].z, x.z); x.w = fmaf(av[u], tv[u].w, x.w);
-                        }
-                    }
-                    *reinterpret_cast<float4*>(Tf + (32 + rr) * 64 + och) = x;
-                }
-                __syncthreads();
-                float4 y = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (tid < 256) {
-                    const float* trow = Tf + (32 + rr) * 64;
-#pragma unroll
-                    for (int g = 0; g < 4; ++g) {
-                        float4 xv[8];
-                        const float4 a4a = *reinterpret_cast<const float4*>(trow + (((8 + 2 * g) ^ rx) << 2));
-                        const float4 a4b = *reinterpret_cast<const float4*>(trow + (((9 + 2 * g) ^ rx) << 2));
-#pragma unroll
-                        for (int u = 0; u < 8; ++u) {
-                            const int l = 8 * g + u;
-                            xv[u] = *reinterpret_cast<const float4*>(Tf + (32 + l) * 64 + ((cg ^ (l & 15)) << 2));
-                        }
-                        const float av[8] = {a4a.x, a4a.y, a4a.z, a4a.w, a4b.x, a4b.y, a4b.z, a4b.w};
-#pragma unroll
-                        for (int u = 0; u < 8; ++u) {
-                            y.x = fmaf(av[u], xv[u].x, y.x); y.y = fmaf(av[u], xv[u].y, y.y);
-                            y.z = fmaf(av[u], xv[u].z, y.z); y.w = fmaf(av[u], xv[u].w, y.w);
-                        }
-                    }
-                }
-                __syncthreads();
-                if (tid < 256)
-                    *reinterpret_cast<float4*>(Tf + (32 + rr) * 64 + och) =
-                        make_float4(-y.x, -y.y, -y.z, -y.w);
+                for (int j = 0; j < 16; ++j) f[j] = __uint_as_float(d[j]);
+                store16_k(sm + OFF_V, row, 16 * part, 64, f);
             }
-            __syncthreads();
-        // ---------------------------------------------------------------- P4d: T to bf16
-            // T -> bf16 K-major [t][i], one 8-element group per thread
-            {
-                const int t = tid >> 3, i8 = tid & 7;
-                const float4 a = *reinterpret_cast<const float4*>(Tf + swz(t, i8 * 8));
-                const float4 b = *reinterpret_cast<const float4*>(Tf + swz(t, i8 * 8 + 4));
-                const float f[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-                *reinterpret_cast<uint4*>(sm + OFF_LVL + LV_TB + kmaj_off(t, i8 * 8, 64)) = pack8(f);
+            KDA_SYNC_FOR_MMA();
+            // (c) second product: Q = T_d P;  T_10 = -Q[16:32, 0:16], T_32 = -Q[48:64, 32:48]
+            if (tid == 0) {
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks)
+                    tc::mma_bf16(tmem + TM_D1 + 64, desc_k(sb + OFF_LVL + LV_TB, 64, ks),
+                                 desc_mn(sb + OFF_V, 8192, ks), IDESC_MG64, ks > 0);
+                tc::mma_commit(&ms.bar_m1);
+            }
+            KDA_WAIT(bar_m1, ph1);
+            if (failed) break;
+            if ((q4 == 0 && part == 0) || (q4 == 1 && part == 2)) {
+                uint32_t d[16];
+                tc::tmem_ld16(taddr(tmem, warp, TM_D1 + 64 + 16 * part), d);
+                tc::tmem_ld_wait();
+                if (lane >= 16) {
+                    float f[16];
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) f[j] = -__uint_as_float(d[j]);
+                    store16_k(TB, row, 16 * part, 64, f);
+                }
+            }
+            KDA_SYNC_FOR_MMA();
+            // (d) 32 -> 64, first product: P' = A_bf[:, 0:32] T[0:32, 0:32]; rows 32..63 are
+            //     A_21 T_11 (the rest of T's first 32 columns below row 31 is still zero)
+            if (tid == 0) {
+#pragma unroll
+                for (int ks = 0; ks < 2; ++ks)
+                    tc::mma_bf16(tmem + TM_D1, desc_k(sb + OFF_LVL + LV_AB, 64, ks),
+                                 desc_mn(sb + OFF_LVL + LV_TB, 8192, ks), IDESC_MG32, ks > 0);
+                tc::mma_commit(&ms.bar_m0);
+            }
+            KDA_WAIT(bar_m0, ph0);
+            if (failed) break;
+            if (q4 == 1 && part < 2) {  // rows 32..63 of P' -> tile rows 0..31
+                uint32_t d[16];
+                tc::tmem_ld16(taddr(tmem, warp, TM_D1 + 16 * part), d);
+                tc::tmem_ld_wait();
+                float f[16];
+#pragma unroll
+                for (int j = 0; j < 16; ++j) f[j] = __uint_as_float(d[j]);
+                store16_k(sm + OFF_V, lane, 16 * part, 64, f);
+            }
+            KDA_SYNC_FOR_MMA();
+            // (e) second product: Y = T_22 P'[32:64, :] (A from row 32 of T, K = columns 32..63);
+            //     T_21 = -Y
+            if (tid == 0) {
+#pragma unroll
+                for (int ks = 0; ks < 2; ++ks)
+                    tc::mma_bf16(tmem + TM_D1 + 64, desc_k(sb + OFF_LVL + LV_TB + 4096, 64, 2 + ks),
+                                 desc_mn(sb + OFF_V, 8192, ks), IDESC_MG32, ks > 0);
+                tc::mma_commit(&ms.bar_m1);
+            }
+            KDA_WAIT(bar_m1, ph1);
+            if (failed) break;
+            if (q4 == 0 && part < 2) {
+                uint32_t d[16];
+                tc::tmem_ld16(taddr(tmem, warp, TM_D1 + 64 + 16 * part), d);
+                tc::tmem_ld_wait();
+                float f[16];
+#pragma unroll
+                for (int j = 0; j < 16; ++j) f[j] = -__uint_as_float(d[j]);
+                store16_k(TB, 32 + lane, 16 * part, 64, f);
             }
         }
         KDA_SYNC_FOR_MMA();
