@@ -228,6 +228,18 @@ __device__ __forceinline__ void bulk_wait_read_all() {
 __device__ __forceinline__ void bulk_wait_all() {
     asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
+// Plain (untiled) shared -> global copy of `bytes` (multiple of 16, both ends 16-byte aligned),
+// tracked by the issuing thread's bulk groups.
+__device__ __forceinline__ void bulk_store(void* gdst, const void* ssrc, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst),
+                 "r"(smem_u32(ssrc)), "r"(bytes)
+                 : "memory");
+}
+// Wait until all but the most recently committed bulk group of this thread have finished
+// reading shared memory.
+__device__ __forceinline__ void bulk_wait_read_all_but_one() {
+    asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+}
 // Plain (untiled) global -> shared copy of `bytes` (multiple of 16, both ends 16-byte aligned).
 __device__ __forceinline__ void bulk_load(void* dst_smem, const void* src, uint32_t bytes,
                                           uint64_t* bar) {

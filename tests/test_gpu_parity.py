@@ -401,9 +401,13 @@ def test_fused_recurrent_matches_oracle(kda, B, H, T, K, V, dtype):
     check("state", state, h_ref, dtype)
 
 
-def test_fused_recurrent_equals_repeated_steps(kda):
-    """T tokens in one launch and T single-token launches do the same arithmetic: bit-identical."""
-    inp = inputs.make(3, 4, 12, 128, 128, dtype="bf16", seed=21, h0_std=0.1)
+@pytest.mark.parametrize("K,V", [(64, 64), (128, 128)])
+def test_fused_recurrent_equals_repeated_steps(kda, K, V):
+    """T tokens in one launch against T single-token launches.  Below K = V = 128 both kernels
+    share one thread layout and summation order: bit-identical.  At K = V = 128 the single step
+    is the streaming kernel, which sums the key rows in another order, so the fp32 states agree
+    to fp32 rounding and the bf16 outputs to within a bf16 unit in the last place."""
+    inp = inputs.make(3, 4, 12, K, V, dtype="bf16", seed=21, h0_std=0.1)
     d = inp.to("cuda")
     s1 = d.h0.clone()
     o1 = kda.fused_recurrent(d.q, d.k, d.v, d.z, d.beta, d.A_log, d.dt_bias, s1, inp.scale)
@@ -414,5 +418,11 @@ def test_fused_recurrent_equals_repeated_steps(kda):
         outs.append(kda.recurrent_step(sl(d.q), sl(d.k), sl(d.v), sl(d.z), sl(d.beta), d.A_log,
                                        d.dt_bias, s2, inp.scale))
     torch.cuda.synchronize()
-    assert torch.equal(o1, torch.cat(outs, dim=2))
-    assert torch.equal(s1, s2)
+    o2 = torch.cat(outs, dim=2)
+    if K < 128:
+        assert torch.equal(o1, o2)
+        assert torch.equal(s1, s2)
+    else:
+        assert (s1 - s2).abs().max().item() <= 1e-5 * s2.abs().max().item()
+        o1d, o2d = o1.double(), o2.double()
+        assert (o1d - o2d).abs().max().item() <= 2.0 ** -7 * o2d.abs().max().item()
