@@ -70,21 +70,22 @@ constexpr uint32_t OFF_K = OFF_Q + 16384;       // 16 KB bf16 k tile
 constexpr uint32_t OFF_V = OFF_K + 16384;       // 16 KB bf16 v tile, later T fp32 [t][i]
 constexpr uint32_t OFF_A1 = OFF_V + 16384;      // 32 KB [W^T | Q'^T], MN-major (2 atoms)
 constexpr uint32_t OFF_S = OFF_A1 + 32768;      // 32 KB S bf16, MN-major [c][v] (2 atoms)
-constexpr uint32_t OFF_ID = OFF_S + 32768;      // 8 KB 64 x 64 identity, K-major bf16
-constexpr uint32_t OFF_MISC = OFF_ID + 8192;
+constexpr uint32_t OFF_MISC = OFF_S + 32768;
 // multi-use region, in order of use within a chunk
 constexpr uint32_t LV_PA = 0;       // level pair A operand, K-major 128 rows (32 KB)   P3
 constexpr uint32_t LV_PB = 32768;   // level pair B operand, K-major 64 rows (16 KB)    P3
 constexpr uint32_t LV_AF = 0;       // A fp32 [t][i] (16 KB, swizzled; diagonal 16 x 16 blocks)  P3-P4
 constexpr uint32_t LV_MB = 16384;   // M bf16 K-major [t][i] (8 KB)          P3-P5
 constexpr uint32_t LV_TB = 24576;   // T bf16 K-major [t][i] (8 KB)          P4-P5
-constexpr uint32_t LV_QG = 32768;   // Q Gamma, MN-major [t][c] (16 KB)      P4-P5
 constexpr uint32_t LV_UT = 0;       // U^T K-major [v][i] (16 KB)            P5
 constexpr uint32_t LV_Z = 49152;    // z tile of the NEXT chunk (16 KB)      P5-P2
 constexpr uint32_t LV_AB = 49152;   // A bf16 K-major [t][i] (8 KB), in the z slot         P3-P4
+constexpr uint32_t LV_MG = 57344;   // merge products P, P' (8 KB), in the z slot            P4
 constexpr uint32_t LV_DELTA = 16384;// Delta^T K-major [v][t] (16 KB)        C2-C3
 constexpr uint32_t LV_UPS = 32768;  // prep kernel: U'^T staging, K-major [v][t] (16 KB)
-// K~ (K e^{G_last - G}, MN-major [t][c]) lives in the v-tile slot OFF_V from P5 to C3.
+// K~ (K e^{G_last - G}, MN-major [t][c]) lives in the v-tile slot OFF_V from its build (under
+// the second level pair's GEMM in the fused kernel, under the W/U GEMM in the prep kernel) to C3
+// or its store.
 // beta K Gamma and beta V (MN-major [t][.], 16 KB each) live in the A1 slot from P3 until
 // the W/U GEMM has read them; then A1 takes [W^T | Q'^T].
 constexpr uint32_t OFF_BKG = OFF_A1, OFF_BV = OFF_A1 + 16384;
@@ -92,7 +93,8 @@ constexpr uint32_t OFF_BKG = OFF_A1, OFF_BV = OFF_A1 + 16384;
 struct Misc {
     alignas(16) float beta[C];
     alignas(16) float diag[16][16];
-    alignas(16) uint64_t bar_qkz;  // TMA: q, k, z tiles of a chunk
+    alignas(16) uint64_t bar_qkz;  // TMA: q, k tiles of a chunk (and its z tile in the prep kernel)
+    uint64_t bar_z;                // TMA: z tile of a chunk (fused kernel)
     uint64_t bar_v;                // TMA: v tile of a chunk
     uint64_t bar_m0, bar_m1;       // tensor-core commits, alternating
     uint32_t tmem_base;
@@ -105,7 +107,8 @@ constexpr uint32_t SMEM_BYTES = OFF_MISC + sizeof(Misc) + 1024;
 
 // ---- TMEM columns (512 allocated)
 constexpr uint32_t TM_S = 0;      // fp32 state, lanes = key channel c, cols = v   (128)
-constexpr uint32_t TM_LVL = 128;  // two level-pair score tiles                    (2 x 64)
+constexpr uint32_t TM_LVL = 384;  // two level-pair score tiles                    (2 x 64)
+constexpr uint32_t TM_MG = 384;   // the inverse's merge products                  (2 x 64)
 constexpr uint32_t TM_QP = 128;   // Q'^T = (Q Gamma)^T - W^T M^T                  (64)
 constexpr uint32_t TM_UP = 192;   // U'^T = U^T M^T                                (64)
 constexpr uint32_t TM_D1 = 256;   // S^T [W^T | Q'^T]                              (128)
@@ -277,6 +280,24 @@ __device__ __forceinline__ void build_bkg_bv(uint8_t* sm, const Misc& ms, int ti
     }
 }
 
+// K~ = K e^{G_last - G} as the MN-major [t][c] operand in the v-tile slot, for the same
+// (token, 8 channels) items as the level operands (k and G from their registers).
+__device__ __forceinline__ void build_kt(uint8_t* sm, int tid, const LevelItems& items) {
+    const float* G2 = reinterpret_cast<const float*>(sm + OFF_G);
+    const int c8 = tid & 15;
+    float gl[8];
+    load8g(G2, 63, c8, gl);
+#pragma unroll
+    for (int ii = 0; ii < 2; ++ii) {
+        const int tt = (tid >> 4) + 32 * ii;
+        float kf[8], o[8];
+        unpack8(items.k[ii], kf);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) o[j] = kf[j] * ex2(gl[j] - items.g[ii][j]);
+        *reinterpret_cast<uint4*>(sm + OFF_V + mnmaj_off(tt, c8 * 8, 8192)) = pack8(o);
+    }
+}
+
 // Float index of element (t, i) of a 64 x 64 fp32 matrix whose 16-byte column groups are
 // XOR-swizzled by the row, so that row-wise and column-wise float4 accesses by
 // consecutive threads fall into distinct banks.
@@ -350,6 +371,7 @@ __device__ __forceinline__ void chunk_loop(const CUtensorMap* tm_q, const CUtens
         reinterpret_cast<uint4*>(sm)[i] = make_uint4(0u, 0u, 0u, 0u);
     if (tid == 0) {
         tc::mbar_init(&ms.bar_qkz, 1);
+        tc::mbar_init(&ms.bar_z, 1);
         tc::mbar_init(&ms.bar_v, 1);
         tc::mbar_init(&ms.bar_m0, 1);
         tc::mbar_init(&ms.bar_m1, 1);
@@ -369,14 +391,7 @@ __device__ __forceinline__ void chunk_loop(const CUtensorMap* tm_q, const CUtens
     tc::fence_after_sync();
     const uint32_t tmem = ms.tmem_base;
 
-    // 64 x 64 identity, K-major bf16: the B operand that copies (Q Gamma)^T into an accumulator
-    if (tid < 64) *reinterpret_cast<uint16_t*>(sm + OFF_ID + kmaj_off(tid, tid, 64)) = 0x3F80u;
-    tc::fence_proxy_async_smem();
-    tc::fence_before_sync();
-    __syncthreads();
-    tc::fence_after_sync();
-
-    uint32_t ph_qkz = 0, ph_v = 0, ph0 = 0, ph1 = 0;
+    uint32_t ph_qkz = 0, ph_z = 0, ph_v = 0, ph0 = 0, ph1 = 0;
     bool failed = false;
     const bool group_c = warp < 8;  // fused: carry group; warps 8-15 form the gate group
     // the current chunk: item cur_it, chunk cur_n of its sequence
@@ -384,10 +399,12 @@ __device__ __forceinline__ void chunk_loop(const CUtensorMap* tm_q, const CUtens
     int cur_n = cur_it < n_items ? item_nb(cur_it) : 0;
     if (tid == 0 && cur_it < n_items) {
         const int bh0 = (int)item_bh(cur_it), y0 = cur_n * C;
-        tc::mbar_arrive_expect_tx(&ms.bar_qkz, 3u * 16384u);
+        uint64_t* zb = kSplit ? &ms.bar_qkz : &ms.bar_z;
+        tc::mbar_arrive_expect_tx(&ms.bar_qkz, (kSplit ? 3u : 2u) * 16384u);
+        if (!kSplit) tc::mbar_arrive_expect_tx(zb, 16384u);
         tc::tma_load_3d(sm + OFF_Q, tm_q, 0, y0, bh0, &ms.bar_qkz);
         tc::tma_load_3d(sm + OFF_K, tm_k, 0, y0, bh0, &ms.bar_qkz);
-        tc::tma_load_3d(sm + OFF_LVL + LV_Z, tm_z, 0, y0, bh0, &ms.bar_qkz);
+        tc::tma_load_3d(sm + OFF_LVL + LV_Z, tm_z, 0, y0, bh0, zb);
         tc::mbar_arrive_expect_tx(&ms.bar_v, 16384u);
         tc::tma_load_3d(sm + OFF_V, tm_v, 0, y0, bh0, &ms.bar_v);
     }
@@ -445,9 +462,9 @@ __device__ __forceinline__ void chunk_loop(const CUtensorMap* tm_q, const CUtens
         if (!failed) state_in32(item_bh(cur_it), j0 > 0 ? fs.handoff : h0, 32 * part);
     }
 
-    // Gate of item (gbh, gn) by warps GLO .. GLO + GW - 1 (named barrier 2): waits for its
-    // q/k/z tiles, loads beta, and writes G2 = in-chunk cumulative log2 decay.  The fused
-    // kernel runs it on warps 8-15 during the carry; the prep kernel on all warps.
+    // Gate of item (gbh, gn) by warps GLO .. GLO + GW - 1 (named barrier 2): waits for its z
+    // tile, loads beta, and writes G2 = in-chunk cumulative log2 decay.  The fused kernel runs
+    // it on warps 8-15 during the carry; the prep kernel on all warps.
     constexpr int GLO = kSplit ? 0 : 8, GW = kSplit ? 16 : 8, TPW = C / GW;
     // The gate's global reads (beta, dt_bias and A_log of the chunk's head) are issued early
     // by the gate threads, so that their latency is hidden by the tensor-core work in between.
@@ -471,7 +488,9 @@ __device__ __forceinline__ void chunk_loop(const CUtensorMap* tm_q, const CUtens
     auto gate_scan = [&](size_t gbh, int gn, const GatePre& gp) -> bool {
         const int wg = warp - GLO;
         const bool ok = !tc::named_sync_or(2, 32 * GW,
-                                           !(tid != 32 * GLO || tc::mbar_wait(&ms.bar_qkz, ph_qkz)));
+                                           !(tid != 32 * GLO ||
+                                             tc::mbar_wait(kSplit ? &ms.bar_qkz : &ms.bar_z,
+                                                           kSplit ? ph_qkz : ph_z)));
         const int tn = gn * C, cnn = min(C, T - tn);
         const int tg = wg * 32 + lane;
         if (tg < C) ms.beta[tg] = tg < cnn ? __uint_as_float((uint32_t)gp.beta_bits << 16) : 0.f;
@@ -513,14 +532,17 @@ __device__ __forceinline__ void chunk_loop(const CUtensorMap* tm_q, const CUtens
     if (cur_it < n_items && (kSplit || !group_c)) {
         const GatePre gp = gate_fetch(item_bh(cur_it), cur_n);
         failed = !gate_scan(item_bh(cur_it), cur_n, gp);
-        if (!kSplit) {  // the fused kernel's gate group also does the first chunk's 4-token blocks
-            __syncwarp();
-            diag_block(sm, ms, 2 * (warp - 8), lane);
-            diag_block(sm, ms, 2 * (warp - 8) + 1, lane);
-        }
     }
-    ph_qkz ^= 1u;
-    if (__syncthreads_or(failed)) failed = true;
+    if constexpr (kSplit) {
+        ph_qkz ^= 1u;
+        if (__syncthreads_or(failed)) failed = true;
+    } else {
+        // the first chunk's q and k tiles (the gate waited for its z)
+        const bool okq = cur_it >= n_items || tid != 0 || tc::mbar_wait(&ms.bar_qkz, ph_qkz);
+        ph_z ^= 1u;
+        ph_qkz ^= 1u;
+        if (__syncthreads_or(failed || !okq)) failed = true;
+    }
 
 // One thread polls the mbarrier; the others sleep in the CTA barrier that follows.
 #define KDA_WAIT(bar, ph)                                                \
@@ -548,6 +570,25 @@ __device__ __forceinline__ void chunk_loop(const CUtensorMap* tm_q, const CUtens
         }                                                                \
     } while (0)
 
+    // The output of a chunk, o = scale ((Q' S)^T + U'^T)^T from TMEM (lanes = v), is written
+    // during the next chunk's inverse, by warps that the forward substitution leaves idle, or
+    // after the loop for the last chunk: (o_bh, o_t0, o_cn) name the chunk whose o is pending.
+    bool o_pend = false, s_pend = false;
+    size_t o_bh = 0;
+    int o_t0 = 0, o_cn = 0;
+    auto o_emit = [&](int tb0, int ntb) {  // this warp: lanes of its quarter, tokens [tb0, tb0 + ntb)
+#pragma unroll 1
+        for (int tb = tb0; tb < tb0 + ntb; tb += 16) {
+            uint32_t dq[16], dp[16];
+            tc::tmem_ld16(taddr(tmem, warp, TM_D1 + 64 + tb), dq);
+            tc::tmem_ld16(taddr(tmem, warp, TM_UP + tb), dp);
+            tc::tmem_ld_wait();
+            float o[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) o[j] = scale * (__uint_as_float(dq[j]) + __uint_as_float(dp[j]));
+            store_o16_pairs(out + (o_bh * T + o_t0 + tb) * VD, row, lane, o_cn - tb, o);
+        }
+    };
     while (cur_it < n_items && !failed) {
         const int it = cur_it;
         const size_t bh = item_bh(it);
@@ -600,8 +641,15 @@ __device__ __forceinline__ void chunk_loop(const CUtensorMap* tm_q, const CUtens
         build_level(sm, 3, tid, items);
         KDA_SYNC_FOR_MMA();
         KDA_PAIR_MMA(TM_LVL + 64, bar_m1);
-        // prep kernel: beta K Gamma and beta V while the second pair's GEMM runs
-        if constexpr (kSplit) build_bkg_bv(sm, ms, tid, items);
+        // while the second pair's GEMM runs: beta K Gamma and beta V (prep kernel), or K~ =
+        // K e^{G_last - G} from the level items' registers into the v slot, whose v tile the
+        // beta V build has already consumed, and the pairs inside 4-token blocks (fused kernel)
+        if constexpr (kSplit) {
+            build_bkg_bv(sm, ms, tid, items);
+        } else {
+            build_kt(sm, tid, items);
+            diag_block(sm, ms, warp, lane);  // the pairs inside 4-token blocks, one block per warp
+        }
         KDA_WAIT(bar_m1, ph1);
         if (failed) break;
         // ---------------------------------------------------------------- P3 epilogue
@@ -710,7 +758,7 @@ __device__ __forceinline__ void chunk_loop(const CUtensorMap* tm_q, const CUtens
             uint8_t* TB = sm + OFF_LVL + LV_TB;
             // (a) the diagonal blocks, one column each (left-looking: x_t = delta_tj -
             //     sum_{i<t} A_ti x_i); the other threads clear the off-diagonal blocks of T
-            //     and the blocks of A_bf that the merges multiply by zero, and build Q Gamma.
+            //     and the blocks of A_bf that the merges multiply by zero.
             if (tid < 64) {
                 const int R = tid >> 4, j = tid & 15;
                 const float* Ab = Af + 16 * R * 64;  // rows 16R.. ; (row & 15) == t
@@ -763,18 +811,16 @@ __device__ __forceinline__ void chunk_loop(const CUtensorMap* tm_q, const CUtens
                     *reinterpret_cast<uint4*>(base + kmaj_off(16 * R + (q >> 1), 16 * Cb + 8 * (q & 1), 64)) =
                         make_uint4(0u, 0u, 0u, 0u);
                 }
-                // meanwhile Q Gamma -> LV_QG (MN-major [t][c]), which does not depend on T
-#pragma unroll 1
-                for (int item = tid - 64; item < C * 16; item += NT - 64) {
-                    const int t = item >> 4, c8 = item & 15;
-                    float qf[8], g8[8], o[8];
-                    unpack8(*reinterpret_cast<const uint4*>(sm + OFF_Q + t * 256 + c8 * 16), qf);
-                    load8g(G2, t, c8, g8);
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) o[j] = qf[j] * ex2(g8[j]);
-                    *reinterpret_cast<uint4*>(sm + OFF_LVL + LV_QG + mnmaj_off(t, c8 * 8, 8192)) = pack8(o);
+                // the previous chunk's output (fused kernel): warps 2..15, each its TMEM lane
+                // quarter; quarters 2 and 3 have four such warps (16 tokens each), quarters 0 and
+                // 1 three (32, 16 and 16 tokens)
+                if (!kSplit && o_pend) {
+                    const int j = warp >> 2;
+                    if (q4 >= 2) o_emit(16 * j, 16);
+                    else o_emit(j == 1 ? 0 : 16 * j, j == 1 ? 32 : 16);
                 }
             }
+            o_pend = false;
             KDA_SYNC_FOR_MMA();
             // The four merge products.  Each is M = 128 rows of which the first 64 (or 32) are
             // the blocks' rows: the other rows read whatever follows in shared memory and their
@@ -786,35 +832,35 @@ __device__ __forceinline__ void chunk_loop(const CUtensorMap* tm_q, const CUtens
             if (tid == 0) {
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks)
-                    tc::mma_bf16(tmem + TM_D1, desc_k(sb + OFF_LVL + LV_AB, 64, ks),
+                    tc::mma_bf16(tmem + TM_MG, desc_k(sb + OFF_LVL + LV_AB, 64, ks),
                                  desc_mn(sb + OFF_LVL + LV_TB, 8192, ks), IDESC_MG64, ks > 0);
                 tc::mma_commit(&ms.bar_m0);
             }
             KDA_WAIT(bar_m0, ph0);
             if (failed) break;
-            if (q4 < 2) {  // rows 0..63 of P -> bf16 tile in the v slot
+            if (q4 < 2) {  // rows 0..63 of P -> bf16 tile LV_MG
                 uint32_t d[16];
-                tc::tmem_ld16(taddr(tmem, warp, TM_D1 + 16 * part), d);
+                tc::tmem_ld16(taddr(tmem, warp, TM_MG + 16 * part), d);
                 tc::tmem_ld_wait();
                 float f[16];
 #pragma unroll
                 for (int j = 0; j < 16; ++j) f[j] = __uint_as_float(d[j]);
-                store16_k(sm + OFF_V, row, 16 * part, 64, f);
+                store16_k(sm + OFF_LVL + LV_MG, row, 16 * part, 64, f);
             }
             KDA_SYNC_FOR_MMA();
             // (c) second product: Q = T_d P;  T_10 = -Q[16:32, 0:16], T_32 = -Q[48:64, 32:48]
             if (tid == 0) {
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks)
-                    tc::mma_bf16(tmem + TM_D1 + 64, desc_k(sb + OFF_LVL + LV_TB, 64, ks),
-                                 desc_mn(sb + OFF_V, 8192, ks), IDESC_MG64, ks > 0);
+                    tc::mma_bf16(tmem + TM_MG + 64, desc_k(sb + OFF_LVL + LV_TB, 64, ks),
+                                 desc_mn(sb + OFF_LVL + LV_MG, 8192, ks), IDESC_MG64, ks > 0);
                 tc::mma_commit(&ms.bar_m1);
             }
             KDA_WAIT(bar_m1, ph1);
             if (failed) break;
             if ((q4 == 0 && part == 0) || (q4 == 1 && part == 2)) {
                 uint32_t d[16];
-                tc::tmem_ld16(taddr(tmem, warp, TM_D1 + 64 + 16 * part), d);
+                tc::tmem_ld16(taddr(tmem, warp, TM_MG + 64 + 16 * part), d);
                 tc::tmem_ld_wait();
                 if (lane >= 16) {
                     float f[16];
@@ -829,7 +875,7 @@ __device__ __forceinline__ void chunk_loop(const CUtensorMap* tm_q, const CUtens
             if (tid == 0) {
 #pragma unroll
                 for (int ks = 0; ks < 2; ++ks)
-                    tc::mma_bf16(tmem + TM_D1, desc_k(sb + OFF_LVL + LV_AB, 64, ks),
+                    tc::mma_bf16(tmem + TM_MG, desc_k(sb + OFF_LVL + LV_AB, 64, ks),
                                  desc_mn(sb + OFF_LVL + LV_TB, 8192, ks), IDESC_MG32, ks > 0);
                 tc::mma_commit(&ms.bar_m0);
             }
@@ -837,12 +883,12 @@ __device__ __forceinline__ void chunk_loop(const CUtensorMap* tm_q, const CUtens
             if (failed) break;
             if (q4 == 1 && part < 2) {  // rows 32..63 of P' -> tile rows 0..31
                 uint32_t d[16];
-                tc::tmem_ld16(taddr(tmem, warp, TM_D1 + 16 * part), d);
+                tc::tmem_ld16(taddr(tmem, warp, TM_MG + 16 * part), d);
                 tc::tmem_ld_wait();
                 float f[16];
 #pragma unroll
                 for (int j = 0; j < 16; ++j) f[j] = __uint_as_float(d[j]);
-                store16_k(sm + OFF_V, lane, 16 * part, 64, f);
+                store16_k(sm + OFF_LVL + LV_MG, lane, 16 * part, 64, f);
             }
             KDA_SYNC_FOR_MMA();
             // (e) second product: Y = T_22 P'[32:64, :] (A from row 32 of T, K = columns 32..63);
@@ -850,15 +896,21 @@ __device__ __forceinline__ void chunk_loop(const CUtensorMap* tm_q, const CUtens
             if (tid == 0) {
 #pragma unroll
                 for (int ks = 0; ks < 2; ++ks)
-                    tc::mma_bf16(tmem + TM_D1 + 64, desc_k(sb + OFF_LVL + LV_TB + 4096, 64, 2 + ks),
-                                 desc_mn(sb + OFF_V, 8192, ks), IDESC_MG32, ks > 0);
+                    tc::mma_bf16(tmem + TM_MG + 64, desc_k(sb + OFF_LVL + LV_TB + 4096, 64, 2 + ks),
+                                 desc_mn(sb + OFF_LVL + LV_MG, 8192, ks), IDESC_MG32, ks > 0);
                 tc::mma_commit(&ms.bar_m1);
             }
             KDA_WAIT(bar_m1, ph1);
             if (failed) break;
+            // fused kernel: the z slot is free (A_bf and the merge tiles are read): the next
+            // chunk's z tile, for its gate under this chunk's Q'/U' GEMM
+            if (!kSplit && tid == 0 && has_next) {
+                tc::mbar_arrive_expect_tx(&ms.bar_z, 16384u);
+                tc::tma_load_3d(sm + OFF_LVL + LV_Z, tm_z, 0, nt0, (int)nbh, &ms.bar_z);
+            }
             if (q4 == 0 && part < 2) {
                 uint32_t d[16];
-                tc::tmem_ld16(taddr(tmem, warp, TM_D1 + 64 + 16 * part), d);
+                tc::tmem_ld16(taddr(tmem, warp, TM_MG + 64 + 16 * part), d);
                 tc::tmem_ld_wait();
                 float f[16];
 #pragma unroll
@@ -877,26 +929,44 @@ __device__ __forceinline__ void chunk_loop(const CUtensorMap* tm_q, const CUtens
             }
             tc::mma_commit(&ms.bar_m0);
         }
-        // while it runs: K~ = K e^{G_last - G} -> the v-tile slot (MN-major [t][c])
+        // while it runs: (Q Gamma)^T straight into TMEM (lane c, column t), the starting value
+        // of Q'^T; thread (quarter, part) takes channels 32 quarter + lane, tokens 16 part ..
+        {
+            const int c = row, tb = 16 * part;
+            uint32_t r[16];
 #pragma unroll
-        for (int ii = 0; ii < 2; ++ii) {
-            const int item = tid + NT * ii, t = item >> 4, c8 = item & 15;
-            float kf[8], g8[8], gl[8], o[8];
-            unpack8(*reinterpret_cast<const uint4*>(sm + OFF_K + t * 256 + c8 * 16), kf);
-            load8g(G2, t, c8, g8);
-            load8g(G2, 63, c8, gl);
+            for (int j = 0; j < 16; ++j) {
+                const int t = tb + j;
+                const float qv = __uint_as_float((uint32_t)*reinterpret_cast<const uint16_t*>(
+                                                     sm + OFF_Q + t * 256 + c * 2) << 16);
+                r[j] = __float_as_uint(qv * ex2(G2[t * KD + gsw(c)]));
+            }
+            tc::tmem_st16(taddr(tmem, warp, TM_QP + tb), r);
+            tc::tmem_st_wait();
+        }
+        // and, in the prep kernel, K~ = K e^{G_last - G} -> the v-tile slot (MN-major [t][c])
+        if constexpr (kSplit) {
 #pragma unroll
-            for (int j = 0; j < 8; ++j) o[j] = kf[j] * ex2(gl[j] - g8[j]);
-            *reinterpret_cast<uint4*>(sm + OFF_V + mnmaj_off(t, c8 * 8, 8192)) = pack8(o);
+            for (int ii = 0; ii < 2; ++ii) {
+                const int item = tid + NT * ii, t = item >> 4, c8 = item & 15;
+                float kf[8], g8[8], gl[8], o[8];
+                unpack8(*reinterpret_cast<const uint4*>(sm + OFF_K + t * 256 + c8 * 16), kf);
+                load8g(G2, t, c8, g8);
+                load8g(G2, 63, c8, gl);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) o[j] = kf[j] * ex2(gl[j] - g8[j]);
+                *reinterpret_cast<uint4*>(sm + OFF_V + mnmaj_off(t, c8 * 8, 8192)) = pack8(o);
+            }
         }
         KDA_WAIT(bar_m0, ph0);
         if (failed) break;
-        // q, k and the z slot are free: request the next chunk's q, k, z
+        // q and k are free: request the next chunk's q, k (and z, which the prep kernel keeps
+        // on the same barrier; the fused kernel requested it after the inverse)
         if (tid == 0 && has_next) {
-            tc::mbar_arrive_expect_tx(&ms.bar_qkz, 3u * 16384u);
+            tc::mbar_arrive_expect_tx(&ms.bar_qkz, (kSplit ? 3u : 2u) * 16384u);
             tc::tma_load_3d(sm + OFF_Q, tm_q, 0, nt0, (int)nbh, &ms.bar_qkz);
             tc::tma_load_3d(sm + OFF_K, tm_k, 0, nt0, (int)nbh, &ms.bar_qkz);
-            tc::tma_load_3d(sm + OFF_LVL + LV_Z, tm_z, 0, nt0, (int)nbh, &ms.bar_qkz);
+            if (kSplit) tc::tma_load_3d(sm + OFF_LVL + LV_Z, tm_z, 0, nt0, (int)nbh, &ms.bar_qkz);
         }
         {
             // parts 0-1: W^T row c, columns 32*part.. -> [W^T | .]; parts 2-3: U^T row v -> K-major
@@ -933,11 +1003,7 @@ __device__ __forceinline__ void chunk_loop(const CUtensorMap* tm_q, const CUtens
             tc::bulk_commit();
         }
         if (tid == 0) {
-            // Q'^T = (Q Gamma)^T I - W^T M^T ;  U'^T = U^T M^T
-#pragma unroll
-            for (int ks = 0; ks < 4; ++ks)
-                tc::mma_bf16(tmem + TM_QP, desc_mn(sb + OFF_LVL + LV_QG, 8192, ks),
-                             desc_k(sb + OFF_ID, 64, ks), IDESC_WU, ks > 0);
+            // Q'^T = (Q Gamma)^T - W^T M^T  (onto the values stored above);  U'^T = U^T M^T
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks) {
                 const uint64_t b = desc_k(sb + OFF_LVL + LV_MB, 64, ks);
@@ -946,6 +1012,23 @@ __device__ __forceinline__ void chunk_loop(const CUtensorMap* tm_q, const CUtens
             }
             tc::mma_commit(&ms.bar_m1);
         }
+        // while it runs (fused kernel): the state that the previous chunk's C3 left in TMEM ->
+        // bf16 operand [c][v] for this chunk's C1, unless an item change already loaded it
+        if (!kSplit && s_pend) {
+            const int c = row, v0 = 32 * part;
+            uint32_t d0[16], d1[16];
+            tc::tmem_ld16(taddr(tmem, warp, TM_S + v0), d0);
+            tc::tmem_ld16(taddr(tmem, warp, TM_S + v0 + 16), d1);
+            tc::tmem_ld_wait();
+            float f[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) f[j] = __uint_as_float(d0[j]);
+            store16_mn(sm + OFF_S, c, v0, 16384, f);
+#pragma unroll
+            for (int j = 0; j < 16; ++j) f[j] = __uint_as_float(d1[j]);
+            store16_mn(sm + OFF_S, c, v0 + 16, 16384, f);
+        }
+        s_pend = false;
         KDA_WAIT(bar_m1, ph1);
         if (failed) break;
         // ---------------------------------------------------------------- S: operands out | next gate
@@ -1035,7 +1118,7 @@ __device__ __forceinline__ void chunk_loop(const CUtensorMap* tm_q, const CUtens
                     tc::fence_after_sync();
                 }
                 // C2: lane v, tokens 32*half..: Delta^T = U^T - (W S)^T -> K-major [v][t] (C3
-                //     waits for it); o is computed and written to HBM after C3 has been issued
+                //     waits for it)
                 const int half = warp >> 2, v = row;
                 if (!failed) {
 #pragma unroll 1
@@ -1054,8 +1137,8 @@ __device__ __forceinline__ void chunk_loop(const CUtensorMap* tm_q, const CUtens
                 tc::fence_before_sync();
                 tc::named_sync(1, 256);
                 tc::fence_after_sync();
-                // C3: S += K~^T Delta (K~ in the v-tile slot), while o = scale ((Q' S)^T + U'^T)^T
-                //     goes out from TMEM (columns C3 does not touch)
+                // C3: S += K~^T Delta (K~ in the v-tile slot).  o = scale ((Q' S)^T + U'^T)^T is
+                //     written during the next chunk's inverse (o_emit): its TMEM columns live on
                 if (tid == 0 && !failed) {
 #pragma unroll
                     for (int ks = 0; ks < 4; ++ks)
@@ -1063,47 +1146,16 @@ __device__ __forceinline__ void chunk_loop(const CUtensorMap* tm_q, const CUtens
                                      desc_k(sb + OFF_LVL + LV_DELTA, 128, ks), IDESC_SK, 1u);
                     tc::mma_commit(&ms.bar_m1);
                 }
-                if (!failed) {
-#pragma unroll 1
-                    for (int tb = 32 * half; tb < 32 * half + 32; tb += 16) {
-                        uint32_t dq[16], dp[16];
-                        tc::tmem_ld16(taddr(tmem, warp, TM_D1 + 64 + tb), dq);
-                        tc::tmem_ld16(taddr(tmem, warp, TM_UP + tb), dp);
-                        tc::tmem_ld_wait();
-                        float o[16];
-#pragma unroll
-                        for (int j = 0; j < 16; ++j)
-                            o[j] = scale * (__uint_as_float(dq[j]) + __uint_as_float(dp[j]));
-                        store_o16_pairs(out + (bh * T + t0 + tb) * VD, v, lane, cn - tb, o);
-                    }
-                }
                 {
                     const bool ok = failed || tid != 0 || tc::mbar_wait(&ms.bar_m1, ph1);
                     if (tc::named_sync_or(1, 256, !ok)) failed = true;
                     tc::fence_after_sync();
                 }
-                // S (fp32, TMEM) -> bf16 operand [c][v]; this warp: v in 64*half..
-                if (!failed) {
-                    const int c = row;
-    #pragma unroll 1
-                    for (int v0 = 64 * half; v0 < 64 * half + 64; v0 += 32) {
-                        uint32_t d0[16], d1[16];
-                        tc::tmem_ld16(taddr(tmem, warp, TM_S + v0), d0);
-                        tc::tmem_ld16(taddr(tmem, warp, TM_S + v0 + 16), d1);
-                        tc::tmem_ld_wait();
-                        float f[16];
-    #pragma unroll
-                        for (int j = 0; j < 16; ++j) f[j] = __uint_as_float(d0[j]);
-                        store16_mn(sm + OFF_S, c, v0, 16384, f);
-    #pragma unroll
-                        for (int j = 0; j < 16; ++j) f[j] = __uint_as_float(d1[j]);
-                        store16_mn(sm + OFF_S, c, v0 + 16, 16384, f);
-                    }
-                    // K~ is consumed: request the next chunk's v tile into its slot
-                    if (tid == 0 && has_next) {
-                        tc::mbar_arrive_expect_tx(&ms.bar_v, 16384u);
-                        tc::tma_load_3d(sm + OFF_V, tm_v, 0, nt0, (int)nbh, &ms.bar_v);
-                    }
+                // K~ is consumed: request the next chunk's v tile into its slot.  The new state's
+                // bf16 copy for the next C1 is made under the next chunk's Q'/U' GEMM (s_pend).
+                if (tid == 0 && has_next && !failed) {
+                    tc::mbar_arrive_expect_tx(&ms.bar_v, 16384u);
+                    tc::tma_load_3d(sm + OFF_V, tm_v, 0, nt0, (int)nbh, &ms.bar_v);
                 }
                 // last chunk of an item (while the gate group finishes the next gate): the state
                 // goes to the next segment (handoff, then its flag) or to hT, and the next item's
@@ -1132,16 +1184,23 @@ __device__ __forceinline__ void chunk_loop(const CUtensorMap* tm_q, const CUtens
                     }
                 }
             } else if (has_next) {
+                // the next chunk's gate, then the wait for its q and k tiles
                 if (!gate_scan(nbh, nt0 / C, gp)) failed = true;
-                // the next chunk's 4-token blocks: this warp's own 8 tokens of G2
-                __syncwarp();
-                diag_block(sm, ms, 2 * (warp - 8), lane);
-                diag_block(sm, ms, 2 * (warp - 8) + 1, lane);
+                if (tc::named_sync_or(2, 256, !(tid != 256 || tc::mbar_wait(&ms.bar_qkz, ph_qkz))))
+                    failed = true;
             }
             ph0 ^= 1u;  // C1's and C3's commits, waited by the carry group only
             ph1 ^= 1u;
+            s_pend = !(last_of_item && has_next && nxt_it != it + fs.BH);
+            o_pend = true;  // this chunk's output goes out during the next chunk, or after the loop
+            o_bh = bh;
+            o_t0 = t0;
+            o_cn = cn;
         }
-        if (has_next) ph_qkz ^= 1u;
+        if (has_next) {
+            ph_qkz ^= 1u;
+            ph_z ^= 1u;
+        }
         tc::fence_proxy_async_smem();
         tc::fence_before_sync();
         if (__syncthreads_or(failed)) failed = true;
@@ -1156,6 +1215,10 @@ __device__ __forceinline__ void chunk_loop(const CUtensorMap* tm_q, const CUtens
 #undef KDA_WAIT
 #undef KDA_SYNC_FOR_MMA
 #undef KDA_PAIR_MMA
+    if (!kSplit && !failed && o_pend) {  // the last chunk's output: all warps, 16 tokens each
+        tc::fence_after_sync();
+        o_emit(16 * part, 16);
+    }
 
     if (failed && tid == 0) {
         atomicExch(&g_kda_tc_timeout, 1);
@@ -1163,6 +1226,7 @@ __device__ __forceinline__ void chunk_loop(const CUtensorMap* tm_q, const CUtens
         tc::mbar_wait(&ms.bar_m0, ph0, 200000000ull);
         tc::mbar_wait(&ms.bar_m1, ph1, 200000000ull);
         tc::mbar_wait(&ms.bar_qkz, ph_qkz, 200000000ull);
+        if (!kSplit) tc::mbar_wait(&ms.bar_z, ph_z, 200000000ull);
         tc::mbar_wait(&ms.bar_v, ph_v, 200000000ull);
     }
     if (kSplit && tid == 0) tc::bulk_wait_all();
