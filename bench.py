@@ -248,7 +248,8 @@ def run_decode(args, kda, inputs, peaks, ws, barrier):
               "roofline": {"bound": "hbm", "achieved": dbytes / dper / 1e9,
                            "peak": peaks["hbm_gbs"], "unit": "GB/s",
                            "frac": dbytes / dper / 1e9 / peaks["hbm_gbs"],
-                           "traffic": measured_traffic("decode_kernel", ("decode.cu",))
+                           "traffic": measured_traffic("decode_stream_kernel",
+                                                         ("decode.cu", "tc_ptx.cuh", "common.cuh"))
                            if dec.B == 256 else None,
                            "algorithmic_bytes": dbytes},
               "config": {"workload": f"decode_bf16 B{dec.B} H{dec.H} K={dec.K} V={dec.V}, "
