@@ -305,6 +305,42 @@ def run_long(args, kda, inputs, peaks, ws, barrier):
                       "form": "split (chosen by kda_chunk_forward for this shape)"}}
     del d, out, hT
     torch.cuda.empty_cache()
+    res["few_heads"] = run_long_few_heads(args, kda, inputs, peaks, ws, barrier)
+    return res
+
+
+def run_long_few_heads(args, kda, inputs, peaks, ws, barrier, H=4):
+    """The long workload with few heads (B1 H4 T65536): kda_chunk_forward takes the split form
+    with the chunk-parallel state scan here; the split form without it is timed beside it."""
+    import torch
+    stream = torch.cuda.current_stream()
+    inp = inputs.workload("long_bf16", H=H, **({"T": args.long_T} if args.long_T else {}))
+    B, T, K, V, C = inp.B, inp.T, inp.K, inp.V, inp.chunk
+    d = inp.to("cuda")
+    out = torch.empty(B, H, T, V, device="cuda", dtype=torch.bfloat16)
+    hT = torch.empty(B, H, K, V, device="cuda", dtype=torch.float32)
+    res = {}
+    for form in ("auto", "split"):
+        def step():
+            kda.chunk_forward(d.q, d.k, d.v, d.z, d.beta, d.A_log, d.dt_bias, inp.scale, d.h0, C,
+                              out=out, hT=hT, form=form)
+        for _ in range(3):
+            step()
+        barrier()
+        n0 = kda.launch_count()
+        secs = timed(step, args.long_steps, stream)
+        launches = kda.launch_count() - n0
+        from gated_delta_rule_26_gb300 import dist as kdist
+        per = kdist.max_over_ranks(secs, device="cuda") / args.long_steps
+        alg_bytes = B * H * T * bytes_per_token_head(K, V) + 2 * B * H * K * V * 4
+        res[form] = {"ms_per_step": per * 1e3, "value": ws * B * T / per, "unit": "tokens/s",
+                     "hbm_frac": alg_bytes / per / 1e9 / peaks["hbm_gbs"],
+                     "kernels_per_step": launches / args.long_steps}
+    res["config"] = {"workload": f"long_bf16 B{B} H{H} T{T} K={K} V={V} chunk {C}, h0 given",
+                     "forms": "auto = kda_chunk_forward (the split form with the state scan for "
+                              "this shape); split = kda_chunk_forward_split"}
+    del d, out, hT
+    torch.cuda.empty_cache()
     return res
 
 

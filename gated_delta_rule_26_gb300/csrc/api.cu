@@ -104,7 +104,8 @@ int kda_gate(const kda_dims* dims, kda_dtype z_dtype, const void* z, const float
 namespace {
 
 // mode 0: the faster tensor-core form (or the fp32 path where it does not apply);
-// 1 / 2: only the fused / split tensor-core form, KDA_ERR_UNSUPPORTED elsewhere.
+// 1 / 2 / 3: only the fused / split / split-with-scan tensor-core form, KDA_ERR_UNSUPPORTED
+// elsewhere.
 int chunk_forward(int mode, const kda_dims* dims, kda_dtype io_dtype, const void* q,
                   const void* k, const void* v, const void* z, const void* beta,
                   const float* A_log, const float* dt_bias, float scale, const float* h0,
@@ -158,6 +159,15 @@ int kda_chunk_forward_fused(const kda_dims* dims, kda_dtype io_dtype, const void
                             const float* h0, int chunk, void* out, float* hT,
                             kda_stream_t stream) {
     return chunk_forward(1, dims, io_dtype, q, k, v, z, beta, A_log, dt_bias, scale, h0, chunk,
+                         out, hT, stream);
+}
+
+int kda_chunk_forward_scan(const kda_dims* dims, kda_dtype io_dtype, const void* q,
+                           const void* k, const void* v, const void* z, const void* beta,
+                           const float* A_log, const float* dt_bias, float scale,
+                           const float* h0, int chunk, void* out, float* hT,
+                           kda_stream_t stream) {
+    return chunk_forward(3, dims, io_dtype, q, k, v, z, beta, A_log, dt_bias, scale, h0, chunk,
                          out, hT, stream);
 }
 

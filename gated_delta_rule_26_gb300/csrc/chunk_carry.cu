@@ -13,6 +13,16 @@
 // which is the chunked WY form of the per-token recurrence S <- diag(alpha) S,
 // u = v - S^T k, S <- S + beta k u^T, o = S^T (scale q).  The operands of a chunk arrive by
 // TMA into one of two stages while the previous chunk is processed.
+//
+// The chunk-parallel state scan.  Per chunk the carry is affine in the state,
+//     S_{n+1} = P_n S_n + Z_n,   P_n = diag(Gamma_last) - K~^T W,   Z_n = K~^T U,
+// so a run of chunks maps its entering state S to P S + Z with P the product of the P_n and
+// Z the state the run reaches from S = 0.  The kernel below therefore also runs
+// sub-segments of a sequence in parallel (grid = sequences x sub-segments), in three roles:
+// the plain carry from a given entering state (writing o), the carry from S = 0 (giving Z,
+// no o) and the carry of the K x K matrix P from the identity with U = 0 (giving P, no o).
+// kda_carry_combine_kernel then walks the sub-segments of each sequence in order,
+// S_{j+1} = P_j S_j + Z_j in fp32, and the plain carry runs every sub-segment from its S_j.
 #include <cuda.h>
 #include <stddef.h>
 
@@ -62,7 +72,7 @@ __global__ void __launch_bounds__(NT2, 1)
                            const __grid_constant__ CUtensorMap tm_kt,
                            const float* __restrict__ gl, int T, int seg_n0, int seg_len,
                            float scale, const float* h_in, __nv_bfloat16* __restrict__ out,
-                           float* h_out) {
+                           float* h_out, CarryGrid cg) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -71,7 +81,20 @@ __global__ void __launch_bounds__(NT2, 1)
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     // warp w reaches TMEM lanes 32 (w & 3) ..; the four warps of a quarter split the columns
     const int q4 = warp & 3, part = warp >> 2, row = q4 * 32 + lane;
-    const size_t bh = blockIdx.x;
+    // this CTA: sequence bh, sub-segment sub of the segment's chunks [j0, j1), and its role
+    const int nbs = cg.BH * cg.nsub;
+    const int role = cg.scan_roles ? 1 + (int)blockIdx.x / nbs : 0;  // 0: plain, 1: Z, 2: P
+    const int rid = (int)blockIdx.x % nbs;
+    const size_t bh = rid % cg.BH;
+    const int sub = rid / cg.BH;
+    const int j0 = min(seg_len, sub * cg.sub_len), j1 = min(seg_len, j0 + cg.sub_len);
+    const bool zero_u = role == 2, write_o = role == 0 && out != nullptr;
+    // entering state (plain role: h_in laid out [sub][bh]; Z role: zero; P role: identity) and
+    // where the leaving state goes (plain role: h_out of the sequence, last sub-segment only;
+    // Z and P roles: their [sub][bh] buffers)
+    const float* sin = role == 0 && h_in ? h_in + ((size_t)sub * cg.BH + bh) * KD * VD : nullptr;
+    float* sout = role == 0 ? (sub == cg.nsub - 1 && h_out ? h_out + bh * KD * VD : nullptr)
+                            : (role == 1 ? cg.zbuf : cg.pbuf) + ((size_t)sub * cg.BH + bh) * KD * VD;
 
     if (tid == 0) {
         tc::mbar_init(&ms.bar_full[0], 1);
@@ -96,18 +119,20 @@ __global__ void __launch_bounds__(NT2, 1)
         uint8_t* st = sm + K2_STAGE + s * ST_BYTES;
         const int item = (int)bh * seg_len + j;
         uint64_t* bar = &ms.bar_full[s];
-        tc::mbar_arrive_expect_tx(bar, ST_TX);
+        tc::mbar_arrive_expect_tx(bar, zero_u ? ST_TX - 32768u : ST_TX);
         tc::tma_load_3d(st + ST_WQ, &tm_wq, 0, 0, 2 * item, bar);
         tc::tma_load_3d(st + ST_WQ + 16384, &tm_wq, 0, 0, 2 * item + 1, bar);
-        tc::tma_load_3d(st + ST_UU, &tm_uu, 0, 0, 2 * item, bar);
-        tc::tma_load_3d(st + ST_UU + 16384, &tm_uu, 0, 0, 2 * item + 1, bar);
+        if (!zero_u) {  // the P role carries U = 0
+            tc::tma_load_3d(st + ST_UU, &tm_uu, 0, 0, 2 * item, bar);
+            tc::tma_load_3d(st + ST_UU + 16384, &tm_uu, 0, 0, 2 * item + 1, bar);
+        }
         tc::tma_load_3d(st + ST_KT, &tm_kt, 0, 0, item, bar);
         tc::tma_load_3d(st + ST_KT + 8192, &tm_kt, 64, 0, item, bar);
         tc::bulk_load(st + ST_GL, gl + (size_t)item * KD, (uint32_t)kItemGL, bar);
     };
-    if (tid == 0 && seg_len > 0) {
-        issue(0, 0);
-        if (seg_len > 1) issue(1, 1);
+    if (tid == 0 && j1 > j0) {
+        issue(j0, 0);
+        if (j1 > j0 + 1) issue(j0 + 1, 1);
     }
 
     // Initial state: fp32 into TMEM (lane c), bf16 copy as the MN-major operand [c][v].
@@ -119,8 +144,12 @@ __global__ void __launch_bounds__(NT2, 1)
 #pragma unroll
             for (int j = 0; j < 16; j += 4) {
                 float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (h_in) x = *reinterpret_cast<const float4*>(h_in + (bh * KD + c) * VD + v0 + j);
+                if (sin) x = *reinterpret_cast<const float4*>(sin + (size_t)c * VD + v0 + j);
                 f[j] = x.x; f[j + 1] = x.y; f[j + 2] = x.z; f[j + 3] = x.w;
+            }
+            if (role == 2) {  // the identity
+#pragma unroll
+                for (int j = 0; j < 16; ++j) f[j] = (c == v0 + j) ? 1.f : 0.f;
             }
             uint32_t r[16];
 #pragma unroll
@@ -146,21 +175,21 @@ __global__ void __launch_bounds__(NT2, 1)
     } while (0)
 
     // The operands of chunk j are waited for at the barrier that ends chunk j - 1 (or here).
-    if (seg_len > 0) {
+    if (j1 > j0) {
         const bool ok = tid != 0 || tc::mbar_wait(&ms.bar_full[0], 0u);
         ph_full ^= 1u;
         if (__syncthreads_or(!ok)) failed = true;
         tc::fence_after_sync();
     }
-    for (int j = 0; j < seg_len && !failed; ++j) {
-        const int s = j & 1;
+    for (int j = j0; j < j1 && !failed; ++j) {
+        const int s = (j - j0) & 1;
         uint8_t* st = sm + K2_STAGE + s * ST_BYTES;
         const uint32_t stb = sb + K2_STAGE + s * ST_BYTES;
         const int t0 = (seg_n0 + j) * C, cn = min(C, T - t0);
         // ---------------------------------------------------------------- K2: C1 + decay
         // stage s ^ 1 was consumed by the previous chunk: refill it two chunks ahead of that one
         // (a thread of warp 1, so that thread 0 issues C1 at once)
-        if (tid == 32 && j >= 1 && j + 1 < seg_len) issue(j + 1, s ^ 1);
+        if (tid == 32 && j >= j0 + 1 && j + 1 < j1) issue(j + 1, s ^ 1);
         // C1: D[v][t'] = sum_c S[c][v] [W^T | Q'^T][c][t']
         if (tid == 0) {
 #pragma unroll
@@ -202,8 +231,13 @@ __global__ void __launch_bounds__(NT2, 1)
             tc::tmem_ld16(taddr(tmem, warp, TM_D2 + tb), dw);
             tc::tmem_ld16(taddr(tmem, warp, TM_D2 + 64 + tb), dq);
             float u[16];
-            load16_k(st + ST_UU, v, tb, 128, u);
-            load16_k(st + ST_UU + 16384, v, tb, 128, up);
+            if (zero_u) {
+#pragma unroll
+                for (int i = 0; i < 16; ++i) u[i] = up[i] = 0.f;
+            } else {
+                load16_k(st + ST_UU, v, tb, 128, u);
+                load16_k(st + ST_UU + 16384, v, tb, 128, up);
+            }
             tc::tmem_ld_wait();
             float f[16];
 #pragma unroll
@@ -223,7 +257,7 @@ __global__ void __launch_bounds__(NT2, 1)
                              desc_k(sb + K2_DELTA, 128, ks), IDESC_SK2, 1u);
             tc::mma_commit(&ms.bar_mma);
         }
-        {
+        if (write_o) {
             float o[16];
 #pragma unroll
             for (int i = 0; i < 16; ++i) o[i] = scale * (__uint_as_float(dq[i]) + up[i]);
@@ -256,7 +290,7 @@ __global__ void __launch_bounds__(NT2, 1)
         {
             // S is ready for the next C1; the next chunk's operands are waited for here too
             bool ok = true;
-            if (j + 1 < seg_len) {
+            if (j + 1 < j1) {
                 ok = tid != 0 || tc::mbar_wait(&ms.bar_full[s ^ 1], (ph_full >> (s ^ 1)) & 1u);
                 ph_full ^= 1u << (s ^ 1);
             }
@@ -266,7 +300,7 @@ __global__ void __launch_bounds__(NT2, 1)
     }
 #undef KDA_CARRY_WAIT
 
-    if (!failed && h_out) {
+    if (!failed && sout) {
         const int c = row;
 #pragma unroll 1
         for (int v0 = 32 * part; v0 < 32 * part + 32; v0 += 16) {
@@ -275,7 +309,7 @@ __global__ void __launch_bounds__(NT2, 1)
             tc::tmem_ld_wait();
 #pragma unroll
             for (int i = 0; i < 16; i += 4)
-                *reinterpret_cast<float4*>(h_out + (bh * KD + c) * VD + v0 + i) =
+                *reinterpret_cast<float4*>(sout + (size_t)c * VD + v0 + i) =
                     make_float4(__uint_as_float(d[i]), __uint_as_float(d[i + 1]),
                                 __uint_as_float(d[i + 2]), __uint_as_float(d[i + 3]));
         }
@@ -296,12 +330,77 @@ cudaError_t launch_chunk_carry(const CUtensorMap& wq, const CUtensorMap& uu, con
                                const float* gl, int BH, int T, int seg_n0, int seg_len,
                                float scale, const float* h_in, __nv_bfloat16* out, float* h_out,
                                cudaStream_t s) {
+    return launch_chunk_carry_grid(wq, uu, kt, gl, T, seg_n0, seg_len, scale, h_in, out, h_out,
+                                   CarryGrid{BH, 1, seg_len, 0, nullptr, nullptr}, s);
+}
+
+cudaError_t launch_chunk_carry_grid(const CUtensorMap& wq, const CUtensorMap& uu,
+                                    const CUtensorMap& kt, const float* gl, int T, int seg_n0,
+                                    int seg_len, float scale, const float* h_in,
+                                    __nv_bfloat16* out, float* h_out, const CarryGrid& cg,
+                                    cudaStream_t s) {
     cudaError_t err = cudaFuncSetAttribute(kda_chunk_carry_kernel,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            (int)K2_SMEM);
     if (err != cudaSuccess) return err;
-    kda_chunk_carry_kernel<<<BH, NT2, K2_SMEM, s>>>(wq, uu, kt, gl, T, seg_n0, seg_len, scale, h_in,
-                                                     out, h_out);
+    const int grid = cg.BH * cg.nsub * (cg.scan_roles ? 2 : 1);
+    if (grid < 1) return cudaSuccess;
+    kda_chunk_carry_kernel<<<grid, NT2, K2_SMEM, s>>>(wq, uu, kt, gl, T, seg_n0, seg_len, scale,
+                                                       h_in, out, h_out, cg);
+    count_launches(1);
+    return cudaGetLastError();
+}
+
+// The sequential half of the scan: per sequence (blockIdx.x / 4) and 32-column tile of the
+// state (blockIdx.x % 4), S_0 = the segment's entering state (h_in, or zero when it is null),
+// then S_{j+1} = P_j S_j + Z_j for j = 0 .. nsub - 2, every S_j written to s_out [j][bh] for
+// the plain carry of sub-segment j.  fp32 throughout: P_j and Z_j come from the carry's TMEM
+// state, and S is kept in shared memory between steps.
+__global__ void __launch_bounds__(256)
+    kda_carry_combine_kernel(int BH, int nsub, const float* __restrict__ h_in,
+                             const float* __restrict__ pbuf, const float* __restrict__ zbuf,
+                             float* __restrict__ s_out) {
+    __shared__ float Ss[KD][33];  // odd pitch: the stores of a warp (16 rows) hit distinct banks
+    const int tid = threadIdx.x;
+    const size_t bh = blockIdx.x / 4;
+    const int v0 = 32 * (blockIdx.x % 4);
+    const size_t KV = (size_t)KD * VD;
+    // thread: row c = tid / 2, columns v0 + 16 (tid % 2) .. + 15
+    const int c = tid >> 1, vh = 16 * (tid & 1);
+    float acc[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+        acc[i] = h_in ? h_in[bh * KV + (size_t)c * VD + v0 + vh + i] : 0.f;
+    for (int j = 0;; ++j) {
+        float* dst = s_out + ((size_t)j * BH + bh) * KV + (size_t)c * VD + v0 + vh;
+#pragma unroll
+        for (int i = 0; i < 16; i += 4)
+            *reinterpret_cast<float4*>(dst + i) = make_float4(acc[i], acc[i + 1], acc[i + 2], acc[i + 3]);
+        if (j + 1 >= nsub) break;
+        __syncthreads();  // the previous step's readers of Ss are done
+#pragma unroll
+        for (int i = 0; i < 16; ++i) Ss[c][vh + i] = acc[i];
+        __syncthreads();
+        const float* P = pbuf + ((size_t)j * BH + bh) * KV + (size_t)c * KD;
+        const float* Z = zbuf + ((size_t)j * BH + bh) * KV + (size_t)c * VD + v0 + vh;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) acc[i] = Z[i];
+#pragma unroll 4
+        for (int k = 0; k < KD; k += 4) {
+            const float4 p = *reinterpret_cast<const float4*>(P + k);
+            const float pk[4] = {p.x, p.y, p.z, p.w};
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+#pragma unroll
+                for (int i = 0; i < 16; ++i) acc[i] = fmaf(pk[u], Ss[k + u][vh + i], acc[i]);
+            }
+        }
+    }
+}
+
+cudaError_t launch_carry_combine(int BH, int nsub, const float* h_in, const float* pbuf,
+                                 const float* zbuf, float* s_out, cudaStream_t s) {
+    kda_carry_combine_kernel<<<BH * 4, 256, 0, s>>>(BH, nsub, h_in, pbuf, zbuf, s_out);
     count_launches(1);
     return cudaGetLastError();
 }

@@ -46,6 +46,8 @@
 #include <cuda.h>
 #include <stddef.h>
 
+#include <algorithm>
+#include <cmath>
 #include <mutex>
 
 #include "chunk_tiles.cuh"
@@ -1631,6 +1633,122 @@ cudaError_t launch_chunk_fused(const ChunkArgs& a, cudaStream_t s) {
     return err != cudaSuccess ? err : ferr;
 }
 
+// ---- the split form with the chunk-parallel state scan (few sequences, many chunks)
+//
+// Sub-segments for a segment of `len` chunks and BH sequences: enough that the carry's Z and P
+// roles (2 BH (nsub - 1) CTAs) fill the SMs once, no more than about sqrt(2 len) (the combine
+// walks them one by one, a K x K by K x V product each), at least 4 chunks each.
+int scan_subsegments(long long BH, long long len, long long S) {
+    long long n = S / (2 * BH) + 1;
+    n = std::min(n, (long long)std::ceil(std::sqrt(2.0 * (double)len)));
+    n = std::min(n, (len + 3) / 4);
+    return (int)std::max(1LL, n);
+}
+
+// Costs in fused chunk steps (one prep item costs about one; a carry chunk about 0.17 of one):
+// the scan form (prep on every SM, then the Z/P roles, the combine and the plain carry over
+// the sub-segments), and the overlapped split form (prep beside a carry of one CTA per
+// sequence, so bound by the longer of the two).
+double scan_cost(long long BH, long long N, long long S) {
+    const long long nsub = scan_subsegments(BH, N, S), sub_len = (N + nsub - 1) / nsub;
+    const double c = 0.17;
+    return (double)((BH * N + S - 1) / S) +
+           c * (double)sub_len * (double)((2 * BH * (nsub - 1) + S - 1) / S) + c * (double)nsub +
+           c * (double)sub_len * (double)((BH * nsub + S - 1) / S);
+}
+double split_overlap_cost(long long BH, long long N, long long S) {
+    const long long prep_sms = std::max(1LL, S - BH);
+    return std::max((double)((BH * N + prep_sms - 1) / prep_sms), 0.17 * (double)N);
+}
+
+// Scratch of the scan form for segments of seg_len chunks: the operands of a segment, the
+// carried state when hT is not wanted, the Z and P maps of all sub-segments but the last and
+// the entering states of all of them.
+size_t scan_scratch_bytes(const ChunkArgs& a, int seg_len, int* nsub_max) {
+    const size_t BH = (size_t)a.B * a.H, KVB = (size_t)KD * VD * sizeof(float);
+    const int nsub = scan_subsegments((long long)BH, seg_len, sm_count());
+    *nsub_max = nsub;
+    return round_up(BH * seg_len * kItemBytes, 256) + (a.hT ? 0 : round_up(BH * KVB, 256)) +
+           2 * round_up((size_t)std::max(1, nsub - 1) * BH * KVB, 256) +
+           round_up((size_t)nsub * BH * KVB, 256);
+}
+
+cudaError_t run_chunk_split_scan(const ChunkArgs& a, cudaStream_t s, void* scratch, int seg_len,
+                                 int nsub_max) {
+    const int N = (a.T + C - 1) / C, BH = a.B * a.H, nsm = sm_count();
+    const size_t KVB = (size_t)KD * VD * sizeof(float), items_max = (size_t)BH * seg_len;
+    uint8_t* p = static_cast<uint8_t*>(scratch);
+    uint8_t* wq = p;
+    uint8_t* uu = wq + items_max * kItemWQ;
+    uint8_t* kt = uu + items_max * kItemUU;
+    float* gl = reinterpret_cast<float*>(kt + items_max * kItemKT);
+    size_t off = round_up(items_max * kItemBytes, 256);
+    float* state = a.hT;
+    if (!state) {
+        state = reinterpret_cast<float*>(p + off);
+        off += round_up(BH * KVB, 256);
+    }
+    const size_t map_bytes = round_up((size_t)std::max(1, nsub_max - 1) * BH * KVB, 256);
+    float* zbuf = reinterpret_cast<float*>(p + off);
+    float* pbuf = reinterpret_cast<float*>(p + off + map_bytes);
+    float* sbuf = reinterpret_cast<float*>(p + off + 2 * map_bytes);
+    CUtensorMap m[4], mwq, muu, mkt;
+    if (!make_input_maps(a, m) ||
+        !make_map3(&mwq, wq, 64, 128, 2 * items_max, 128, 16384, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_map3(&muu, uu, 64, 128, 2 * items_max, 128, 16384, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_map3(&mkt, kt, 128, 64, items_max, 256, 16384, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B))
+        return cudaErrorInvalidValue;
+    cudaError_t err = cudaFuncSetAttribute(kda_chunk_prep_kernel,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           (int)SMEM_BYTES);
+    if (err != cudaSuccess) return err;
+    for (int n0 = 0; n0 < N; n0 += seg_len) {
+        const int len = std::min(seg_len, N - n0), items = BH * len;
+        kda_chunk_prep_kernel<<<std::min(items, nsm), NT, SMEM_BYTES, s>>>(
+            m[0], m[1], m[2], m[3], mwq, muu, mkt, a.H, a.T, (const __nv_bfloat16*)a.beta, a.A_log,
+            a.dt_bias, PrepSeg{n0, len, items, gl});
+        count_launches(1);
+        if ((err = cudaGetLastError()) != cudaSuccess) return err;
+        const float* h_seg = n0 == 0 ? a.h0 : state;  // entering state of the segment (may be null)
+        int nsub = std::min(nsub_max, scan_subsegments(BH, len, nsm));
+        const int sub_len = (len + nsub - 1) / nsub;
+        nsub = (len + sub_len - 1) / sub_len;
+        if (nsub < 2) {
+            err = launch_chunk_carry(mwq, muu, mkt, gl, BH, a.T, n0, len, a.scale, h_seg,
+                                     (__nv_bfloat16*)a.out, state, s);
+        } else {
+            // the maps (P, Z) of sub-segments 0 .. nsub - 2, their entering states in order,
+            // then the plain carry of every sub-segment from its entering state
+            err = launch_chunk_carry_grid(mwq, muu, mkt, gl, a.T, n0, len, a.scale, nullptr, nullptr,
+                                          nullptr, CarryGrid{BH, nsub - 1, sub_len, 1, zbuf, pbuf}, s);
+            if (err == cudaSuccess) err = launch_carry_combine(BH, nsub, h_seg, pbuf, zbuf, sbuf, s);
+            if (err == cudaSuccess)
+                err = launch_chunk_carry_grid(mwq, muu, mkt, gl, a.T, n0, len, a.scale, sbuf,
+                                              (__nv_bfloat16*)a.out, state,
+                                              CarryGrid{BH, nsub, sub_len, 0, nullptr, nullptr}, s);
+        }
+        if (err != cudaSuccess) return err;
+    }
+    return cudaSuccess;
+}
+
+cudaError_t launch_chunk_scan(const ChunkArgs& a, cudaStream_t s) {
+    const int N = (a.T + C - 1) / C;
+    int seg_len = N, nsub_max = 1;
+    while (seg_len > 1 && scan_scratch_bytes(a, seg_len, &nsub_max) > kSplitScratchCap)
+        seg_len = (seg_len + 1) / 2;
+    const size_t bytes = scan_scratch_bytes(a, seg_len, &nsub_max);
+    if (bytes > kSplitScratchCap) return cudaErrorMemoryAllocation;
+    void* p = nullptr;
+    if (cudaMallocAsync(&p, bytes, s) != cudaSuccess) {
+        cudaGetLastError();
+        return cudaErrorMemoryAllocation;
+    }
+    const cudaError_t err = run_chunk_split_scan(a, s, p, seg_len, nsub_max);
+    const cudaError_t ferr = cudaFreeAsync(p, s);
+    return err != cudaSuccess ? err : ferr;
+}
+
 // Which tensor-core form is faster: the fused kernel's schedule (above) against the split
 // form, which spreads all chunks over the SMs and adds a short sequential carry (about a tenth
 // of a fused chunk step) per chunk.
@@ -1655,13 +1773,22 @@ cudaError_t run_chunk_split_in(const ChunkArgs& a, cudaStream_t s, void* scratch
     return run_chunk_split(a, s, scratch, bytes);
 }
 
-// mode 0: pick the faster form, 1: fused kernel, 2: split form.
+// mode 0: pick the faster form, 1: fused kernel, 2: split form, 3: split form with the
+// chunk-parallel state scan.  Mode 0 takes the scan where the overlapped split form would be
+// bound by its sequential carry (few sequences over many chunks).
 cudaError_t launch_chunk_tc(const ChunkArgs& a, cudaStream_t s, int mode, bool* taken) {
     *taken = false;
     if (!chunk_tc_eligible(a)) return cudaSuccess;
     *taken = true;
+    if (mode == 3) return launch_chunk_scan(a, s);
     const bool split = mode == 2 || (mode == 0 && prefer_split(a));
-    return split ? launch_chunk_split(a, s) : launch_chunk_fused(a, s);
+    if (!split) return launch_chunk_fused(a, s);
+    if (mode == 0) {
+        const long long BH = (long long)a.B * a.H, N = (a.T + C - 1) / C, S = sm_count();
+        if (2 * BH <= S && N >= 64 && scan_cost(BH, N, S) < 0.8 * split_overlap_cost(BH, N, S))
+            return launch_chunk_scan(a, s);
+    }
+    return launch_chunk_split(a, s);
 }
 
 }  // namespace kda

@@ -106,7 +106,22 @@ __device__ __forceinline__ uint32_t taddr(uint32_t base, int warp, uint32_t col)
 
 }  // namespace tile
 
-// Host side of the split forward's carry kernel (chunk_carry.cu).
+// Host side of the split forward's carry kernel (chunk_carry.cu).  CarryGrid: BH sequences x
+// nsub sub-segments of sub_len chunks per launch; with scan_roles the grid doubles into the
+// scan's Z role (from S = 0, into zbuf) and P role (from the identity with U = 0, into pbuf),
+// both laid out [sub][bh][K][V] and neither writing o.
+struct CarryGrid {
+    int BH, nsub, sub_len, scan_roles;
+    float* zbuf;
+    float* pbuf;
+};
+cudaError_t launch_chunk_carry_grid(const CUtensorMap& wq, const CUtensorMap& uu,
+                                    const CUtensorMap& kt, const float* gl, int T, int seg_n0,
+                                    int seg_len, float scale, const float* h_in,
+                                    __nv_bfloat16* out, float* h_out, const CarryGrid& cg,
+                                    cudaStream_t s);
+cudaError_t launch_carry_combine(int BH, int nsub, const float* h_in, const float* pbuf,
+                                 const float* zbuf, float* s_out, cudaStream_t s);
 cudaError_t launch_chunk_carry(const CUtensorMap& wq, const CUtensorMap& uu, const CUtensorMap& kt,
                                const float* gl, int BH, int T, int seg_n0, int seg_len,
                                float scale, const float* h_in, __nv_bfloat16* out, float* h_out,

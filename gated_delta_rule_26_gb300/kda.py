@@ -56,6 +56,7 @@ def load() -> ctypes.CDLL:
         lib.kda_chunk_forward_split.argtypes = lib.kda_chunk_forward.argtypes
         lib.kda_chunk_forward_fused.argtypes = lib.kda_chunk_forward.argtypes
         lib.kda_chunk_forward_split_noalloc.argtypes = lib.kda_chunk_forward.argtypes
+        lib.kda_chunk_forward_scan.argtypes = lib.kda_chunk_forward.argtypes
         lib.kda_recurrent_step.argtypes = [dp, i, vp, vp, vp, vp, vp, vp, vp, f, vp, vp, vp]
         lib.kda_fused_recurrent.argtypes = [dp, i, vp, vp, vp, vp, vp, vp, vp, f, vp, vp, vp]
         lib.kda_chunk_backward.argtypes = [dp, i] + [vp] * 7 + [f] + [vp] * 12
@@ -136,6 +137,8 @@ def gate(z: torch.Tensor, A_log: torch.Tensor, dt_bias: torch.Tensor, chunk: int
 
 _CHUNK_FORMS = {"auto": "kda_chunk_forward", "split": "kda_chunk_forward_split",
                 "fused": "kda_chunk_forward_fused",
+                # the split form with the chunk-parallel state scan
+                "scan": "kda_chunk_forward_scan",
                 # the split form on the library's fixed scratch array (no allocation)
                 "split_noalloc": "kda_chunk_forward_split_noalloc"}
 
@@ -148,7 +151,8 @@ def chunk_forward(q, k, v, z, beta, A_log, dt_bias, scale: Optional[float] = Non
     """KDA forward over (B, H, T) tokens; returns (o, hT) with o in q's dtype, hT float32.
 
     ``form`` selects the entry point: "auto" (kda_chunk_forward, which picks the faster
-    form), "split" (kda_chunk_forward_split), "fused" (kda_chunk_forward_fused) or
+    form), "split" (kda_chunk_forward_split), "fused" (kda_chunk_forward_fused), "scan"
+    (kda_chunk_forward_scan: the split form with the chunk-parallel state scan) or
     "split_noalloc" (kda_chunk_forward_split_noalloc: the split form without any device
     allocation, for B*H up to the limit its header comment states)."""
     fn = _CHUNK_FORMS[form]

@@ -96,9 +96,9 @@ int kda_chunk_forward(const kda_dims* dims, kda_dtype io_dtype, const void* q, c
 
 /*
  * kda_chunk_forward_split / kda_chunk_forward_fused -- kda_chunk_forward restricted to one of
- * its two tensor-core forms (bf16 I/O, K = V = 128, chunk 64, T >= 1; anything else returns
- * KDA_ERR_UNSUPPORTED).  kda_chunk_forward picks between them by the shape; these exist to
- * run and compare each form on any shape.
+ * its tensor-core forms (bf16 I/O, K = V = 128, chunk 64, T >= 1; anything else returns
+ * KDA_ERR_UNSUPPORTED).  kda_chunk_forward picks among them (and kda_chunk_forward_scan below)
+ * by the shape; these exist to run and compare each form on any shape.
  *   fused : the whole forward in one kernel that reads each input once, the state on chip.
  *           With at most one sequence per SM, one CTA per (b, h) walks its chunks.  With more
  *           sequences than SMs, one CTA per SM takes (segment, sequence) work items of a few
@@ -134,6 +134,31 @@ int kda_chunk_forward_fused(const kda_dims* dims, kda_dtype io_dtype, const void
                             const float* A_log, const float* dt_bias, float scale,
                             const float* h0, int chunk, void* out, float* hT,
                             kda_stream_t stream);
+
+/*
+ * kda_chunk_forward_scan -- kda_chunk_forward_split with the chunk-parallel state scan: for few
+ * sequences over many chunks, where the split form's one-CTA-per-sequence carry would walk
+ * every chunk of a sequence in order.  Per chunk n the carry is affine in the state,
+ *     S_{n+1} = P_n S_n + Z_n,   P_n = diag(Gamma_last) - K~^T W,   Z_n = K~^T U
+ * (the chunk carry of kda-adjoint-2026-10-01 section 2), so the chunks of a sequence are cut
+ * into sub-segments whose maps (P, the product of their P_n, and Z, the state they reach from
+ * S = 0) are computed in parallel by the carry kernel, combined in order in fp32 into every
+ * sub-segment's entering state, and then every sub-segment runs its plain carry (writing o)
+ * in parallel.  About three times the carry work of the split form, but the sequential part
+ * is one K x K by K x V product per sub-segment instead of one chunk step per chunk.
+ * kda_chunk_forward takes this form by itself where it is the faster one.
+ * Shapes, arguments and errors as kda_chunk_forward_split.  Scratch (cudaMallocAsync /
+ * cudaFreeAsync on `stream`, at most 1 GiB, longer inputs in segments of chunks): the
+ * per-chunk operands, 3 x B*H*K*V*4 bytes per sub-segment for the maps and the entering
+ * states, and B*H*K*V*4 for the carried state when hT is NULL; KDA_ERR_NO_MEMORY if that
+ * allocation fails.  The result equals the split form's to rounding (the state reaches each
+ * sub-segment along another order of products), not bit for bit.
+ */
+int kda_chunk_forward_scan(const kda_dims* dims, kda_dtype io_dtype, const void* q,
+                           const void* k, const void* v, const void* z, const void* beta,
+                           const float* A_log, const float* dt_bias, float scale,
+                           const float* h0, int chunk, void* out, float* hT,
+                           kda_stream_t stream);
 
 /*
  * kda_chunk_forward_split_noalloc -- kda_chunk_forward_split for callers that cannot allocate

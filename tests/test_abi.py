@@ -80,7 +80,8 @@ def test_host_validation_rejects_bad_arguments(lib):
     assert _fwd(lib, Dims(1, 1, 8, 128, 128), null_q=True) == -1
 
 
-@pytest.mark.parametrize("fn", ["kda_chunk_forward_split", "kda_chunk_forward_fused"])
+@pytest.mark.parametrize("fn", ["kda_chunk_forward_split", "kda_chunk_forward_fused",
+                                "kda_chunk_forward_scan"])
 def test_tensor_core_forms_reject_other_shapes(lib, fn):
     # each form exists for bf16, K = V = 128, chunk 64 and T >= 1 only; everything else is
     # refused on the host (nothing is launched, so fake pointers are fine)

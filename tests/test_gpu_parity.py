@@ -255,6 +255,52 @@ def test_split_form_without_final_state(kda, T):
     run_and_compare(kda, inp, want_hT=False, form="split")
 
 
+# ---------------------------------------------------------------- the chunk-parallel state scan
+@pytest.mark.parametrize("B,H,T,with_h0,want_hT", [
+    (1, 2, 2000, True, True),      # 32 chunks, the last one ragged, 8 sub-segments of 4
+    (1, 4, 8192 + 13, True, True),  # 129 chunks, 16 sub-segments
+    (2, 2, 5000, False, False),    # no h0, no hT (the carried state lives in scratch)
+])
+def test_scan_form_matches_oracle(kda, B, H, T, with_h0, want_hT):
+    inp = inputs.make(B, H, T, 128, 128, chunk=64, dtype="bf16", seed=61 + T, h0_std=0.1,
+                      dt_std=0.1)
+    run_and_compare(kda, inp, with_h0=with_h0, want_hT=want_hT, form="scan")
+    assert kda.device_status() == 0
+
+
+def test_scan_form_agrees_with_split_form(kda):
+    # the state reaches each sub-segment along another order of products: equal to rounding
+    inp = inputs.make(1, 3, 4096 + 64 * 7 + 5, 128, 128, chunk=64, dtype="bf16", seed=67,
+                      h0_std=0.1)
+    d = inp.to("cuda")
+    args = (d.q, d.k, d.v, d.z, d.beta, d.A_log, d.dt_bias, inp.scale, d.h0, 64)
+    o1, h1 = kda.chunk_forward(*args, form="scan")
+    o2, h2 = kda.chunk_forward(*args, form="split")
+    torch.cuda.synchronize()
+    check("o", o1, o2.double().cpu().numpy(), "bf16")
+    check("hT", h1, h2.double().cpu().numpy(), "bf16")
+
+
+def test_few_sequences_take_the_scan_and_match_the_oracle(kda):
+    """B1 H4 T65536: the split form would walk 1024 chunks per sequence in order, so
+    kda_chunk_forward takes the scan (one prep launch and three carry-side launches for the
+    single segment, where the overlapped split form launches 32 kernels); sampled sequences
+    against the oracle, token by token."""
+    inp = inputs.workload("long_bf16", H=4)
+    d = inp.to("cuda")
+    n0 = kda.launch_count()
+    o, hT = kda.chunk_forward(d.q, d.k, d.v, d.z, d.beta, d.A_log, d.dt_bias, inp.scale, d.h0, 64)
+    torch.cuda.synchronize()
+    assert kda.launch_count() - n0 == 4
+    assert kda.device_status() == 0
+    pairs = [(0, 1), (0, 3)]
+    q, k, v, z, beta, A, dt, h0 = _sample_pairs(inp, pairs)
+    o_ref, h_ref = oracle.forward(q, k, v, z, beta, A, dt, inp.scale, h0, threads=len(pairs))
+    bs, hs = [p[0] for p in pairs], [p[1] for p in pairs]
+    check("o", o[bs, hs].unsqueeze(0), o_ref, "bf16")
+    check("hT", hT[bs, hs].unsqueeze(0), h_ref, "bf16")
+
+
 # ---------------------------------------------------------------- full-size workloads, sampled
 def _sample_pairs(inp, pairs):
     """Gather (b, h) sequences into a (1, n, T, *) problem the oracle can run."""
@@ -269,7 +315,7 @@ def _sample_pairs(inp, pairs):
 _SAMPLED_REF = {}
 
 
-@pytest.mark.parametrize("form", ["auto", "fused", "split"])
+@pytest.mark.parametrize("form", ["auto", "fused", "split", "scan"])
 @pytest.mark.parametrize("name,pairs", [
     ("prefill_bf16", [(0, 0), (3, 17), (7, 31)]),
     ("long_bf16", [(0, 5), (0, 30)]),
