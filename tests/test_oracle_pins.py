@@ -266,6 +266,25 @@ def test_resume_from_final_state():
     np.testing.assert_array_equal(h2, h)
 
 
+def test_state_and_outputs_are_affine_in_the_initial_state():
+    """The chunk-parallel scan composes per-segment maps S -> P S + Z: the final state (and
+    every output) is affine in the initial state.  With a = f(0), f(S1) - a and f(S2) - a
+    must add up to f(S1 + S2) - a and scale with the state, to rounding, for K != V."""
+    q, k, v, z, beta, A, dt, S1 = _rand_problem(B=1, H=2, T=24, K=5, V=3, seed=11)
+    A = np.array([-2.0, -1.0])  # a slow decay, so that the initial state still shows at the end
+    rng = np.random.default_rng(12)
+    S2 = rng.standard_normal(S1.shape) * 0.3
+    f = lambda S: oracle.forward(q, k, v, z, beta, A, dt, 0.7, S)
+    o0, h0 = f(np.zeros_like(S1))
+    o1, h1 = f(S1)
+    o2, h2 = f(S2)
+    o12, h12 = f(S1 + 2.5 * S2)
+    np.testing.assert_allclose(h12 - h0, (h1 - h0) + 2.5 * (h2 - h0), rtol=0, atol=1e-12)
+    np.testing.assert_allclose(o12 - o0, (o1 - o0) + 2.5 * (o2 - o0), rtol=0, atol=1e-12)
+    # and the map is not trivial: the initial state matters and the zero-state run does too
+    assert np.abs(h1 - h0).max() > 1e-3 and np.abs(h0).max() > 1e-3
+
+
 def test_threaded_oracle_matches_single_thread():
     q, k, v, z, beta, A, dt, S0 = _rand_problem(B=3, H=4, T=20, K=4, V=4, seed=5)
     a = oracle.forward(q, k, v, z, beta, A, dt, 0.5, S0, threads=1)
