@@ -260,6 +260,7 @@ def test_split_form_without_final_state(kda, T):
     (1, 2, 2000, True, True),      # 32 chunks, the last one ragged, 8 sub-segments of 4
     (1, 4, 8192 + 13, True, True),  # 129 chunks, 16 sub-segments
     (2, 2, 5000, False, False),    # no h0, no hT (the carried state lives in scratch)
+    (1, 2, 100, True, True),       # two chunks: too few to cut, the plain carry runs
 ])
 def test_scan_form_matches_oracle(kda, B, H, T, with_h0, want_hT):
     inp = inputs.make(B, H, T, 128, 128, chunk=64, dtype="bf16", seed=61 + T, h0_std=0.1,
