@@ -184,22 +184,17 @@ __device__ __forceinline__ void build_level(uint8_t* sm, int li, int tid, const 
         const int ref = (t & ~(2 * h - 1)) + h - 1;
         const bool upper = (t & h) != 0;
         const int rank = level_rank(t, s);
-        float kf[8], qf[8], r8[8], f[8], kv[8], qv[8];
-        unpack8(it.k[r], kf);
+        float r8[8], f[8];
         load8g(G2, ref, c8, r8);
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            f[j] = ex2(upper ? it.g[r][j] - r8[j] : r8[j] - it.g[r][j]);
-            kv[j] = kf[j] * f[j];
-        }
+        for (int j = 0; j < 8; ++j) f[j] = ex2(upper ? it.g[r][j] - r8[j] : r8[j] - it.g[r][j]);
+        const uint4 kv = scale8_bf16(it.k[r], f);
         if (upper) {
-            *reinterpret_cast<uint4*>(A + kmaj_off(64 * slot + rank, c8 * 8, 128)) = pack8(kv);
-            unpack8(it.q[r], qf);
-#pragma unroll
-            for (int j = 0; j < 8; ++j) qv[j] = qf[j] * f[j];
-            *reinterpret_cast<uint4*>(A + kmaj_off(64 * slot + 32 + rank, c8 * 8, 128)) = pack8(qv);
+            *reinterpret_cast<uint4*>(A + kmaj_off(64 * slot + rank, c8 * 8, 128)) = kv;
+            *reinterpret_cast<uint4*>(A + kmaj_off(64 * slot + 32 + rank, c8 * 8, 128)) =
+                scale8_bf16(it.q[r], f);
         } else {
-            *reinterpret_cast<uint4*>(Bop + kmaj_off(32 * slot + rank, c8 * 8, 64)) = pack8(kv);
+            *reinterpret_cast<uint4*>(Bop + kmaj_off(32 * slot + rank, c8 * 8, 64)) = kv;
         }
     }
 }
@@ -269,16 +264,16 @@ __device__ __forceinline__ void build_bkg_bv(uint8_t* sm, const Misc& ms, int ti
     for (int ii = 0; ii < 2; ++ii) {
         // the same (token, 8 channels) items as the level operands: k and G from registers
         const int item = tid + NT * ii, tt = item >> 4, c8 = item & 15;
-        const float bt = ms.beta[tt];
-        float kf[8], vf[8], o[8];
-        unpack8(items.k[ii], kf);
-        unpack8(*reinterpret_cast<const uint4*>(sm + OFF_V + tt * 256 + c8 * 16), vf);
+        const float bt = ms.beta[tt];  // a bf16 value, so bt * v rounds once, as in fp32
+        float f[8], b8[8];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) o[j] = bt * kf[j] * ex2(items.g[ii][j]);
-        *reinterpret_cast<uint4*>(sm + OFF_BKG + mnmaj_off(tt, c8 * 8, 8192)) = pack8(o);
-#pragma unroll
-        for (int j = 0; j < 8; ++j) o[j] = bt * vf[j];
-        *reinterpret_cast<uint4*>(sm + OFF_BV + mnmaj_off(tt, c8 * 8, 8192)) = pack8(o);
+        for (int j = 0; j < 8; ++j) {
+            f[j] = bt * ex2(items.g[ii][j]);
+            b8[j] = bt;
+        }
+        *reinterpret_cast<uint4*>(sm + OFF_BKG + mnmaj_off(tt, c8 * 8, 8192)) = scale8_bf16(items.k[ii], f);
+        *reinterpret_cast<uint4*>(sm + OFF_BV + mnmaj_off(tt, c8 * 8, 8192)) =
+            scale8_bf16(*reinterpret_cast<const uint4*>(sm + OFF_V + tt * 256 + c8 * 16), b8);
     }
 }
 
@@ -292,11 +287,10 @@ __device__ __forceinline__ void build_kt(uint8_t* sm, int tid, const LevelItems&
 #pragma unroll
     for (int ii = 0; ii < 2; ++ii) {
         const int tt = (tid >> 4) + 32 * ii;
-        float kf[8], o[8];
-        unpack8(items.k[ii], kf);
+        float f[8];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) o[j] = kf[j] * ex2(gl[j] - items.g[ii][j]);
-        *reinterpret_cast<uint4*>(sm + OFF_V + mnmaj_off(tt, c8 * 8, 8192)) = pack8(o);
+        for (int j = 0; j < 8; ++j) f[j] = ex2(gl[j] - items.g[ii][j]);
+        *reinterpret_cast<uint4*>(sm + OFF_V + mnmaj_off(tt, c8 * 8, 8192)) = scale8_bf16(items.k[ii], f);
     }
 }
 
@@ -951,13 +945,13 @@ __device__ __forceinline__ void chunk_loop(const CUtensorMap* tm_q, const CUtens
 #pragma unroll
             for (int ii = 0; ii < 2; ++ii) {
                 const int item = tid + NT * ii, t = item >> 4, c8 = item & 15;
-                float kf[8], g8[8], gl[8], o[8];
-                unpack8(*reinterpret_cast<const uint4*>(sm + OFF_K + t * 256 + c8 * 16), kf);
+                float g8[8], gl[8], f[8];
                 load8g(G2, t, c8, g8);
                 load8g(G2, 63, c8, gl);
 #pragma unroll
-                for (int j = 0; j < 8; ++j) o[j] = kf[j] * ex2(gl[j] - g8[j]);
-                *reinterpret_cast<uint4*>(sm + OFF_V + mnmaj_off(t, c8 * 8, 8192)) = pack8(o);
+                for (int j = 0; j < 8; ++j) f[j] = ex2(gl[j] - g8[j]);
+                *reinterpret_cast<uint4*>(sm + OFF_V + mnmaj_off(t, c8 * 8, 8192)) =
+                    scale8_bf16(*reinterpret_cast<const uint4*>(sm + OFF_K + t * 256 + c8 * 16), f);
             }
         }
         KDA_WAIT(bar_m0, ph0);

@@ -39,6 +39,20 @@ __device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
                       tc::pack_bf16x2(f[4], f[5]), tc::pack_bf16x2(f[6], f[7]));
 }
 
+// Eight bf16 values (a uint4) times eight factors: the factors are rounded to bf16 pairwise and
+// each product, formed by the packed bf16x2 multiply, is rounded to bf16 once.
+__device__ __forceinline__ uint32_t mul_bf16x2(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+__device__ __forceinline__ uint4 scale8_bf16(uint4 x, const float (&f)[8]) {
+    return make_uint4(mul_bf16x2(x.x, tc::pack_bf16x2(f[0], f[1])),
+                      mul_bf16x2(x.y, tc::pack_bf16x2(f[2], f[3])),
+                      mul_bf16x2(x.z, tc::pack_bf16x2(f[4], f[5])),
+                      mul_bf16x2(x.w, tc::pack_bf16x2(f[6], f[7])));
+}
+
 // K-major tile with `rows` rows: byte offset of element (row, k); k atoms of 64.
 __device__ __forceinline__ uint32_t kmaj_off(int row, int k, int rows) {
     return (uint32_t)((k >> 6) * (rows * 128)) + tc::sw128_offset(row, (k & 63) >> 3) + (k & 7) * 2;
