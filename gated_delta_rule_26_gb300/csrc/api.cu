@@ -11,6 +11,7 @@ namespace kda {
 cudaError_t launch_chunk_tc(const ChunkArgs& a, cudaStream_t s, int mode, bool* taken);
 cudaError_t read_and_clear_carry_timeout(int* timed_out);
 cudaError_t read_and_clear_decode_timeout(int* timed_out);
+cudaError_t read_and_clear_bwd_timeout(int* timed_out);
 cudaError_t launch_chunk_split_noalloc(const ChunkArgs& a, cudaStream_t s, bool* fits);
 cudaError_t launch_bounded_wait_selftest(unsigned long long limit_ns, cudaStream_t s);
 cudaError_t read_and_clear_timeout(cudaStream_t s, int* timed_out);
@@ -238,12 +239,13 @@ int kda_chunk_backward(const kda_dims* dims, kda_dtype io_dtype, const void* q, 
 
 int kda_device_status(kda_stream_t stream) {
     int timed_out = 0;
-    int carry_timed_out = 0, decode_timed_out = 0;
+    int carry_timed_out = 0, decode_timed_out = 0, bwd_timed_out = 0;
     if (kda::read_and_clear_timeout((cudaStream_t)stream, &timed_out) != cudaSuccess ||
         kda::read_and_clear_carry_timeout(&carry_timed_out) != cudaSuccess ||
-        kda::read_and_clear_decode_timeout(&decode_timed_out) != cudaSuccess)
+        kda::read_and_clear_decode_timeout(&decode_timed_out) != cudaSuccess ||
+        kda::read_and_clear_bwd_timeout(&bwd_timed_out) != cudaSuccess)
         return KDA_ERR_CUDA;
-    timed_out |= carry_timed_out | decode_timed_out;
+    timed_out |= carry_timed_out | decode_timed_out | bwd_timed_out;
     return timed_out ? KDA_ERR_TIMEOUT : KDA_OK;
 }
 

@@ -28,9 +28,15 @@
 // the same thread, so dq, dk and dG accumulate in registers.
 #include <type_traits>
 
+#include "chunk_tiles.cuh"
 #include "common.cuh"
+#include "tc_ptx.cuh"
 
 namespace kda {
+
+// Set by the tensor-core backward when one of its bounded waits gives up.
+__device__ int g_kda_bwd_timeout;
+
 namespace {
 
 constexpr int BC = 16;    // tokens per chunk
@@ -721,6 +727,758 @@ __global__ void __launch_bounds__(BNT, 1) kda_chunk_bwd_kernel(const BwdArgs<IO>
     }
 }
 
+// ============================================================== tensor-core form, K = V = 128
+// The same chunk walk and adjoint equations, with the state (phase 1) and its adjoint (phase 2)
+// resident in TMEM as fp32 and every contraction with them on tcgen05:
+//   phase 1   R^T = V^T - S^T Kg^T                      M = v, N = 16 tokens, K = c
+//             S <- diag(gamma) S + Kt^T Delta           M = c, N = v, K = 16 tokens
+//   phase 2   dDelta^T = dS^T Kt^T (+ scale M^T dO on the CUDA cores)   M = v, N = 16
+//             dKt^T = dS Delta^T                        M = c, N = 16, K = v
+//             [dQg^T | P^T] = S [dO ; dY]^T             M = c, N = 32 (dQg = scale x)
+//             dS <- diag(gamma) dS + [scale Qg ; -beta Kg]^T [dO ; dY]   K = 32 tokens
+// Every operand x is split into bf16 x_hi = bf16(x) and x_lo = bf16(x - x_hi); a product A B
+// is accumulated in fp32 as A_hi B_hi + A_hi B_lo + A_lo B_hi.  x_hi + x_lo is within
+// 2^-16 |x| of x and the dropped A_lo B_lo is below 2^-16 |A| |B|, so each product term is
+// within about 3 * 2^-16 of its exact value, and the state and its adjoint stay fp32 in
+// TMEM.  The operand copy of the state (hi and lo, 64 KB) is also what phase 1 keeps per
+// chunk: phase 2 brings it back with one bulk copy, already in the operand layout.  The
+// pairwise terms, the T solve, the gate and the per-token outputs are the CUDA-core code of
+// the kernel above.
+namespace bwdtc {
+constexpr int NT = 512;
+// shared memory (bytes from a 1024-byte aligned base): tensor-core operand tiles, each a
+// K-major 128-byte-swizzled tile (read MN-major where a product needs its transpose)
+constexpr uint32_t OFF_ST = 0;                 // state / adjoint copy [c][v], 128 rows: hi
+constexpr uint32_t ST_LO = 32768;              //   lo
+constexpr uint32_t OFF_KT = 65536;             // Kt [t][c], 16 rows (hi, lo at +R16_LO)
+constexpr uint32_t OFF_DLT = OFF_KT + 8192;    // Delta [t][v], 16 rows
+constexpr uint32_t OFF_DOY = OFF_DLT + 8192;   // [dO ; dY] [t'][v], 32 rows (hi, lo at +R32_LO)
+constexpr uint32_t OFF_AQK = OFF_DOY + 16384;  // phase 2 [scale Qg ; -beta Kg] [t'][c], 32 rows;
+                                               // phase 1 Kg [t][c], 16 rows
+constexpr uint32_t R16_LO = 4096, R32_LO = 8192;
+constexpr uint32_t OFF_F = OFF_AQK + 16384;    // fp32 area (float offsets below)
+constexpr int F_Q = 0, F_K = F_Q + KM * GP, F_G = F_K + KM * GP;
+constexpr int F_R = F_G + KM * GP, F_DO = F_R + BC * VM, F_DL = F_DO + BC * VM;
+constexpr int F_DY = F_DL + BC * VM, F_XT = F_DY + BC * VM;
+constexpr int F_AP = F_XT + BC * KM, F_TM = F_AP + BC * BC, F_MM = F_TM + BC * BC;
+constexpr int F_DB = F_MM + BC * BC, F_DM = F_DB + BC * BC;
+constexpr int F_BET = F_DM + BC * BC, F_GAM = F_BET + BC, F_RED = F_GAM + KM;
+constexpr int F_END = F_RED + 4 * KM;
+constexpr uint32_t OFF_MISC = OFF_F + 4u * F_END;  // two mbarriers, TMEM base, failure flag
+constexpr size_t SMEM_BYTES = OFF_MISC + 64 + 1024;  // + slack for the 1024-byte alignment
+static_assert((OFF_F + 4u * F_R) % 16 == 0 && (OFF_F + 4u * F_DL) % 16 == 0 &&
+              (OFF_F + 4u * F_DO) % 16 == 0 && (OFF_F + 4u * F_DY) % 16 == 0, "float4 rows");
+static_assert(OFF_MISC % 8 == 0 && SMEM_BYTES <= 232448, "backward tensor-core shared memory");
+// TMEM columns: the state or its adjoint, and the three accumulators of the N = 16 / 32 products
+constexpr uint32_t TM_M = 0, TM_A = 128, TM_B = 160, TM_C = 192, TM_COLS = 256;
+constexpr uint32_t ID_MN_K16 = tc::idesc_bf16(128, 16, 1, 0);
+constexpr uint32_t ID_K_K16 = tc::idesc_bf16(128, 16, 0, 0);
+constexpr uint32_t ID_K_K32 = tc::idesc_bf16(128, 32, 0, 0);
+constexpr uint32_t ID_MN_MN128 = tc::idesc_bf16(128, 128, 1, 1);
+constexpr uint32_t kStateBytes = 65536;        // one operand copy of the state (hi + lo)
+}  // namespace bwdtc
+
+// x = hi + lo with hi = bf16(x), lo = bf16(x - hi), eight values at a time
+__device__ __forceinline__ void split8(const float (&f)[8], uint4& hi, uint4& lo) {
+    hi = tile::pack8(f);
+    float h[8], r[8];
+    tile::unpack8(hi, h);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) r[j] = f[j] - h[j];
+    lo = tile::pack8(r);
+}
+
+template <typename IO>
+__global__ void __launch_bounds__(bwdtc::NT, 1) kda_chunk_bwd_tc_kernel(const BwdArgs<IO> a) {
+    using namespace bwdtc;
+    extern __shared__ uint8_t smem_bwd_raw[];
+    uint8_t* sm8 = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_bwd_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    float* F = reinterpret_cast<float*>(sm8 + OFF_F);
+    float* Qr = F + F_Q;
+    float* Kr = F + F_K;
+    float* Gc = F + F_G;
+    float* Rv = F + F_R;
+    float* dO = F + F_DO;
+    float* Dl = F + F_DL;
+    float* dY = F + F_DY;
+    float* XT = F + F_XT;
+    float* Ap = F + F_AP;
+    float* Tm = F + F_TM;
+    float* Mm = F + F_MM;
+    float* dB = F + F_DB;
+    float* dM = F + F_DM;
+    float* bet = F + F_BET;
+    float* gam = F + F_GAM;
+    float* red = F + F_RED;
+    uint64_t* bar_mma = reinterpret_cast<uint64_t*>(sm8 + OFF_MISC);
+    uint64_t* bar_ld = bar_mma + 1;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm8 + OFF_MISC + 16);
+    volatile int* s_fail = reinterpret_cast<volatile int*>(sm8 + OFF_MISC + 20);
+    const uint32_t sb = tc::smem_u32(sm8);
+
+    constexpr int K = KM, V = VM;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int T = a.T;
+    const size_t bh = blockIdx.x;
+    const int h = (int)(bh % a.H);
+    const int N = (T + BC - 1) / BC;
+    const float eA = expf(a.A_log[h]);
+    const size_t KV = (size_t)K * V;
+    // thread roles: channel or value column col (= the TMEM lane this warp reaches), and the
+    // quarter qtr (tokens 4 qtr .. + 3, or TMEM columns 32 qtr .. + 31 of a 128-column matrix)
+    const int col = tid & 127, qtr = tid >> 7;
+
+    if (tid == 0) {
+        tc::mbar_init(bar_mma, 1);
+        tc::mbar_init(bar_ld, 1);
+        *s_fail = 0;
+        tc::fence_barrier_init();
+    }
+    if (warp == 0) {
+        tc::tmem_alloc(tmem_slot, TM_COLS);
+        tc::tmem_relinquish();
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tm = *tmem_slot;
+    uint32_t ph_mma = 0, ph_ld = 0;
+    auto fail = [&]() {
+        *s_fail = 1;
+        atomicExch(&g_kda_bwd_timeout, 1);
+    };
+    auto wait_mma = [&]() {
+        if (!tc::mbar_wait(bar_mma, ph_mma)) fail();
+        ph_mma ^= 1u;
+        tc::fence_after_sync();
+    };
+    auto wait_ld = [&]() {
+        if (!tc::mbar_wait(bar_ld, ph_ld)) fail();
+        ph_ld ^= 1u;
+    };
+    const uint32_t t_m0 = tile::taddr(tm + TM_M, warp, 32 * qtr);
+    auto master_ld = [&](uint32_t (&r0)[16], uint32_t (&r1)[16]) {
+        tc::tmem_ld16(t_m0, r0);
+        tc::tmem_ld16(t_m0 + 16, r1);
+        tc::tmem_ld_wait();
+    };
+    auto master_st = [&](const uint32_t (&r0)[16], const uint32_t (&r1)[16]) {
+        tc::tmem_st16(t_m0, r0);
+        tc::tmem_st16(t_m0 + 16, r1);
+        tc::tmem_st_wait();
+    };
+    // TMEM matrix <- src (K, V) row-major, or zero: row col, columns 32 qtr .. + 31
+    auto master_init = [&](const float* src) {
+        uint32_t r0[16], r1[16];
+        const float* p = src ? src + (size_t)col * V + 32 * qtr : nullptr;
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            r0[j] = __float_as_uint(p ? __ldcg(p + j) : 0.f);
+            r1[j] = __float_as_uint(p ? __ldcg(p + 16 + j) : 0.f);
+        }
+        master_st(r0, r1);
+    };
+    // The operand copy (hi, lo) of the TMEM matrix; with `decay`, the matrix is then scaled
+    // by gamma in place (the copy keeps the undecayed values).
+    auto master_copy = [&](bool decay) {
+        uint32_t r0[16], r1[16];
+        master_ld(r0, r1);
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+            float f[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) f[j] = __uint_as_float(g < 2 ? r0[8 * g + j] : r1[8 * (g - 2) + j]);
+            uint4 hi, lo;
+            split8(f, hi, lo);
+            const uint32_t off = tile::kmaj_off(col, 32 * qtr + 8 * g, 128);
+            *reinterpret_cast<uint4*>(sm8 + OFF_ST + off) = hi;
+            *reinterpret_cast<uint4*>(sm8 + OFF_ST + ST_LO + off) = lo;
+        }
+        tc::fence_proxy_async_smem();
+        if (decay) {
+            const float gm = gam[col];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                r0[j] = __float_as_uint(__uint_as_float(r0[j]) * gm);
+                r1[j] = __float_as_uint(__uint_as_float(r1[j]) * gm);
+            }
+            master_st(r0, r1);
+        }
+    };
+
+    // Ask L2 for the inputs of chunk n, one 128-byte line per thread (as the CUDA-core form)
+    // and, in phase 2, the state copy that phase 1 kept for it.
+    auto prefetch_chunk = [&](int n, bool full) {
+        if (n < 0 || n >= N) return;
+        const int t0 = n * BC, cn = min(BC, T - t0);
+        const int io = (int)sizeof(IO);
+        const int lk = (cn * K * io + 127) / 128, lv = (cn * V * io + 127) / 128;
+        const int lrd = (2 * BC * V * 4 + 127) / 128;
+        int i = tid;
+        const char* p = nullptr;
+        if (i < lk) p = reinterpret_cast<const char*>(a.k + ((bh * T) + t0) * K) + 128 * i;
+        else if ((i -= lk) < lk) p = reinterpret_cast<const char*>(a.z + ((bh * T) + t0) * K) + 128 * i;
+        else if (full && (i -= lk) < lk) p = reinterpret_cast<const char*>(a.q + ((bh * T) + t0) * K) + 128 * i;
+        else if (full && (i -= lk) < lv) p = reinterpret_cast<const char*>(a.d_o + ((bh * T) + t0) * V) + 128 * i;
+        else if (full && (i -= lv) < lrd) p = reinterpret_cast<const char*>(a.rd + (bh * N + n) * (size_t)(2 * BC * V)) + 128 * i;
+        else if (!full && (i -= lk) < lv) p = reinterpret_cast<const char*>(a.v + ((bh * T) + t0) * V) + 128 * i;
+        if (p) prefetch_l2(p);
+        if (full) prefetch_l2(reinterpret_cast<const char*>(a.ckpt + (bh * N + n) * KV) + 128 * tid);
+    };
+    // Inputs of chunk n into the fp32 tiles: k, G (from z), beta, and v (phase 1) or q, dO,
+    // R and Delta as phase 1 stored them (phase 2); then the in-chunk cumulative sum and gamma.
+    auto load_inputs = [&](int n, bool full) {
+        const int t0 = n * BC, cn = min(BC, T - t0);
+        constexpr int PER = BC * KM / NT;
+        float kx[PER], qx[PER], zx[PER], dtx[PER], vx[PER], ox[PER], dx[PER];
+        const float* rdn = a.rd + (bh * N + n) * (size_t)(2 * BC * V);
+        float bx = 0.f;
+#pragma unroll
+        for (int r = 0; r < PER; ++r) {
+            const int idx = tid + r * NT, t = idx / K, c = idx - t * K;
+            const bool in = t < cn;
+            const size_t gi = ((bh * T) + t0 + t) * K + c;
+            kx[r] = in ? ld_io(a.k + gi) : 0.f;
+            qx[r] = (full && in) ? ld_io(a.q + gi) : 0.f;
+            zx[r] = in ? ld_io(a.z + gi) : 0.f;
+            dtx[r] = __ldg(a.dt_bias + (size_t)h * K + c);
+        }
+#pragma unroll
+        for (int r = 0; r < PER; ++r) {
+            const int idx = tid + r * NT, t = idx / V, vv = idx - t * V;
+            const bool in = t < cn;
+            const size_t gi = ((bh * T) + t0 + t) * V + vv;
+            if (full) {
+                vx[r] = __ldcg(rdn + idx);
+                dx[r] = __ldcg(rdn + BC * V + idx);
+            } else {
+                vx[r] = in ? ld_io(a.v + gi) : 0.f;
+                dx[r] = 0.f;
+            }
+            ox[r] = (full && in) ? ld_io(a.d_o + gi) : 0.f;
+        }
+        if (tid < BC && tid < cn) bx = ld_io(a.beta + bh * T + t0 + tid);
+#pragma unroll
+        for (int r = 0; r < PER; ++r) {
+            const int idx = tid + r * NT, t = idx / K, c = idx - t * K;
+            Kr[ci(c, t)] = kx[r];
+            if (full) Qr[ci(c, t)] = qx[r];
+            Gc[ci(c, t)] = t < cn ? kda_log_decay(zx[r], dtx[r], eA) : 0.f;
+        }
+#pragma unroll
+        for (int r = 0; r < PER; ++r) {
+            const int idx = tid + r * NT;
+            Rv[idx] = vx[r];
+            if (full) {
+                dO[idx] = ox[r];
+                Dl[idx] = dx[r];
+            }
+        }
+        if (tid < BC) bet[tid] = bx;
+        __syncthreads();
+        if (tid < K) {
+            float run = 0.f;
+            for (int t = 0; t < BC; ++t) {
+                run += Gc[ci(tid, t)];
+                Gc[ci(tid, t)] = run;
+            }
+            gam[tid] = expf(run);
+        }
+        __syncthreads();
+    };
+    // The decay-scaled operand tiles of the chunk (hi, lo): Kt = K e^{G_last - G} always;
+    // phase 1 Kg = K e^G; phase 2 [scale Qg ; -beta Kg], Delta and the dO half of [dO ; dY].
+    auto build_tiles = [&](bool full) {
+        if (tid < 256) {
+            const int t = tid & 15, c0 = 8 * (tid >> 4);
+            float kt[8], kg[8], qg[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const int c = c0 + j;
+                const float g = Gc[ci(c, t)], gl = Gc[ci(c, BC - 1)], kk = Kr[ci(c, t)];
+                const float eg = expf(g);
+                kt[j] = kk * expf(gl - g);
+                kg[j] = kk * eg;
+                qg[j] = full ? Qr[ci(c, t)] * eg : 0.f;
+            }
+            uint4 hi, lo;
+            split8(kt, hi, lo);
+            *reinterpret_cast<uint4*>(sm8 + OFF_KT + tile::kmaj_off(t, c0, 16)) = hi;
+            *reinterpret_cast<uint4*>(sm8 + OFF_KT + R16_LO + tile::kmaj_off(t, c0, 16)) = lo;
+            if (!full) {
+                split8(kg, hi, lo);
+                *reinterpret_cast<uint4*>(sm8 + OFF_AQK + tile::kmaj_off(t, c0, 16)) = hi;
+                *reinterpret_cast<uint4*>(sm8 + OFF_AQK + R16_LO + tile::kmaj_off(t, c0, 16)) = lo;
+            } else {
+                const float nb = -bet[t];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    qg[j] *= a.scale;
+                    kg[j] *= nb;
+                }
+                split8(qg, hi, lo);
+                *reinterpret_cast<uint4*>(sm8 + OFF_AQK + tile::kmaj_off(t, c0, 32)) = hi;
+                *reinterpret_cast<uint4*>(sm8 + OFF_AQK + R32_LO + tile::kmaj_off(t, c0, 32)) = lo;
+                split8(kg, hi, lo);
+                *reinterpret_cast<uint4*>(sm8 + OFF_AQK + tile::kmaj_off(16 + t, c0, 32)) = hi;
+                *reinterpret_cast<uint4*>(sm8 + OFF_AQK + R32_LO + tile::kmaj_off(16 + t, c0, 32)) = lo;
+            }
+        } else if (full) {
+            const int i = tid - 256, t = i & 15, v0 = 8 * (i >> 4);
+            float d[8], o[8];
+            const float4 d0 = *reinterpret_cast<const float4*>(Dl + t * VM + v0);
+            const float4 d1 = *reinterpret_cast<const float4*>(Dl + t * VM + v0 + 4);
+            const float4 o0 = *reinterpret_cast<const float4*>(dO + t * VM + v0);
+            const float4 o1 = *reinterpret_cast<const float4*>(dO + t * VM + v0 + 4);
+            d[0] = d0.x; d[1] = d0.y; d[2] = d0.z; d[3] = d0.w; d[4] = d1.x; d[5] = d1.y; d[6] = d1.z; d[7] = d1.w;
+            o[0] = o0.x; o[1] = o0.y; o[2] = o0.z; o[3] = o0.w; o[4] = o1.x; o[5] = o1.y; o[6] = o1.z; o[7] = o1.w;
+            uint4 hi, lo;
+            split8(d, hi, lo);
+            *reinterpret_cast<uint4*>(sm8 + OFF_DLT + tile::kmaj_off(t, v0, 16)) = hi;
+            *reinterpret_cast<uint4*>(sm8 + OFF_DLT + R16_LO + tile::kmaj_off(t, v0, 16)) = lo;
+            split8(o, hi, lo);
+            *reinterpret_cast<uint4*>(sm8 + OFF_DOY + tile::kmaj_off(t, v0, 32)) = hi;
+            *reinterpret_cast<uint4*>(sm8 + OFF_DOY + R32_LO + tile::kmaj_off(t, v0, 32)) = lo;
+        }
+        tc::fence_proxy_async_smem();
+    };
+    // Rows of a [BC][VM] fp32 tile into rows row0 .. of a 16- or 32-row operand tile (hi, lo),
+    // one (row, 8 columns) item per thread of the first 256.
+    auto tile_rows = [&](const float* src, uint32_t off, int rows, uint32_t lo_off, int row0) {
+        if (tid < 256) {
+            const int t = tid & 15, v0 = 8 * (tid >> 4);
+            const float4 x0 = *reinterpret_cast<const float4*>(src + t * VM + v0);
+            const float4 x1 = *reinterpret_cast<const float4*>(src + t * VM + v0 + 4);
+            float f[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+            uint4 hi, lo;
+            split8(f, hi, lo);
+            *reinterpret_cast<uint4*>(sm8 + off + tile::kmaj_off(row0 + t, v0, rows)) = hi;
+            *reinterpret_cast<uint4*>(sm8 + off + lo_off + tile::kmaj_off(row0 + t, v0, rows)) = lo;
+        }
+        tc::fence_proxy_async_smem();
+    };
+    // A' (i < t) and, in phase 2, M (i <= t) with the exact pairwise decay: warp t
+    auto arows = [&](bool full) {
+        const int t = warp;
+        float gt[4], kt[4], qt[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int c = lane + 32 * u;
+            gt[u] = Gc[ci(c, t)];
+            kt[u] = Kr[ci(c, t)];
+            qt[u] = full ? Qr[ci(c, t)] : 0.f;
+        }
+        float w[32];
+#pragma unroll
+        for (int i = 0; i < BC; ++i) {
+            float sa = 0.f, sq = 0.f;
+            if (i <= t) {
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int c = lane + 32 * u;
+                    const float kiE = Kr[ci(c, i)] * __expf(gt[u] - Gc[ci(c, i)]);
+                    sa = fmaf(kt[u], kiE, sa);
+                    sq = fmaf(qt[u], kiE, sq);
+                }
+            }
+            w[i] = sa;
+            w[BC + i] = sq;
+        }
+        warp_reduce_scatter32(w, lane);
+        if (lane < BC) Ap[t * BC + lane] = lane < t ? w[0] : 0.f;
+        else if (full) Mm[t * BC + lane - BC] = lane - BC <= t ? w[0] : 0.f;
+    };
+    // T = (I + diag(beta) A')^{-1} by forward substitution, one column per thread
+    auto t_solve = [&]() {
+        if (tid < BC) {
+            const int j = tid;
+            float x[BC];
+#pragma unroll
+            for (int t = 0; t < BC; ++t) {
+                float acc = 0.f;
+#pragma unroll
+                for (int i = 0; i < t; ++i) acc = fmaf(Ap[t * BC + i], x[i], acc);
+                x[t] = (t == j ? 1.f : 0.f) - bet[t] * acc;
+                Tm[t * BC + j] = x[t];
+            }
+        }
+    };
+
+    // ======================================================= phase 1: chunk states forward
+    master_init(a.h0 ? a.h0 + bh * KV : nullptr);
+    tc::fence_before_sync();
+    __syncthreads();
+    for (int n = 0; n < N && !*s_fail; ++n) {
+        load_inputs(n, false);
+        prefetch_chunk(n + 1, false);
+        if (n > 0) wait_mma();  // the previous chunk's state update has read Kt and Delta
+        build_tiles(false);
+        arows(false);
+        if (tid == 0) tc::bulk_wait_read_all();  // the previous state copy has gone out
+        __syncthreads();
+        t_solve();
+        master_copy(true);  // S as an operand, then S <- diag(gamma) S in TMEM
+        tc::fence_before_sync();
+        __syncthreads();
+        if (tid == 0) {
+            tc::fence_after_sync();
+#pragma unroll 1
+            for (int p = 0; p < 3; ++p) {
+                const uint32_t ao = p == 2 ? ST_LO : 0u, bo = p == 1 ? R16_LO : 0u;
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks)
+                    tc::mma_bf16(tm + TM_A, tile::desc_mn(sb + OFF_ST + ao, 16384, ks),
+                                 tile::desc_k(sb + OFF_AQK + bo, 16, ks), ID_MN_K16, (p | ks) != 0);
+            }
+            tc::mma_commit(bar_mma);
+            tc::bulk_store(a.ckpt + (bh * N + n) * KV, sm8 + OFF_ST, kStateBytes);
+            tc::bulk_commit();
+        }
+        wait_mma();
+        // R = V - Kg S and Delta = T diag(beta) R, value column v = tid on warps 0..3
+        if (warp < 4) {
+            uint32_t r[16];
+            tc::tmem_ld16(tile::taddr(tm + TM_A, warp, 0), r);
+            tc::tmem_ld_wait();
+            float rr[BC];
+#pragma unroll
+            for (int t = 0; t < BC; ++t) rr[t] = Rv[t * VM + tid] - __uint_as_float(r[t]);
+#pragma unroll
+            for (int t = 0; t < BC; ++t) {
+                float acc = 0.f;
+#pragma unroll
+                for (int i = 0; i <= t; ++i) acc = fmaf(Tm[t * BC + i], bet[i] * rr[i], acc);
+                Rv[t * VM + tid] = rr[t];
+                Dl[t * VM + tid] = acc;
+            }
+        }
+        __syncthreads();
+        tile_rows(Dl, OFF_DLT, 16, R16_LO, 0);
+        {  // R and Delta for phase 2
+            float4* rdn = reinterpret_cast<float4*>(a.rd + (bh * N + n) * (size_t)(2 * BC * V));
+            rdn[tid] = reinterpret_cast<const float4*>(Rv)[tid];
+            rdn[NT + tid] = reinterpret_cast<const float4*>(Dl)[tid];
+        }
+        tc::fence_before_sync();
+        __syncthreads();
+        if (tid == 0) {  // S += Kt^T Delta
+            tc::fence_after_sync();
+#pragma unroll
+            for (int p = 0; p < 3; ++p) {
+                const uint32_t ao = p == 2 ? R16_LO : 0u, bo = p == 1 ? R16_LO : 0u;
+                tc::mma_bf16(tm + TM_M, tile::desc_mn(sb + OFF_KT + ao, 2048, 0),
+                             tile::desc_mn(sb + OFF_DLT + bo, 2048, 0), ID_MN_MN128, 1u);
+            }
+            tc::mma_commit(bar_mma);
+        }
+    }
+    if (N > 0 && !*s_fail) wait_mma();
+    if (tid == 0) tc::bulk_wait_all();  // every state copy is in global memory
+    prefetch_chunk(N - 1, true);
+    __syncthreads();
+
+    // ======================================================= phase 2: reverse
+    master_init(a.dhT ? a.dhT + bh * KV : nullptr);
+    tc::fence_before_sync();
+    __syncthreads();
+    float dA_acc = 0.f, ddt_acc = 0.f;  // this thread's channel col, tokens of quarter qtr
+    for (int n = N - 1; n >= 0 && !*s_fail; --n) {
+        const int t0 = n * BC, cn = min(BC, T - t0);
+        load_inputs(n, true);
+        prefetch_chunk(n - 1, true);
+        if (n < N - 1) wait_mma();  // the previous chunk's dS update has read its tiles
+        build_tiles(true);
+        arows(true);
+        __syncthreads();
+        t_solve();
+        master_copy(false);  // dS as an operand
+        tc::fence_before_sync();
+        __syncthreads();
+        if (tid == 0) {  // dDelta^T = dS^T Kt^T, dKt^T = dS Delta^T
+            tc::fence_after_sync();
+#pragma unroll 1
+            for (int p = 0; p < 3; ++p) {
+                const uint32_t ao = p == 2 ? ST_LO : 0u, bo = p == 1 ? R16_LO : 0u;
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks)
+                    tc::mma_bf16(tm + TM_A, tile::desc_mn(sb + OFF_ST + ao, 16384, ks),
+                                 tile::desc_k(sb + OFF_KT + bo, 16, ks), ID_MN_K16, (p | ks) != 0);
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks)
+                    tc::mma_bf16(tm + TM_B, tile::desc_k(sb + OFF_ST + ao, 128, ks),
+                                 tile::desc_k(sb + OFF_DLT + bo, 16, ks), ID_K_K16, (p | ks) != 0);
+            }
+            tc::mma_commit(bar_mma);
+        }
+        // scale M^T dO, value column v = tid on warps 0..3
+        float mdo[BC];
+        if (warp < 4) {
+#pragma unroll
+            for (int t = 0; t < BC; ++t) {
+                float m = 0.f;
+#pragma unroll
+                for (int s2 = t; s2 < BC; ++s2) m = fmaf(Mm[s2 * BC + t], dO[s2 * VM + tid], m);
+                mdo[t] = a.scale * m;
+            }
+        }
+        wait_mma();
+        if (tid == 0) {  // the state entering this chunk, as phase 1 kept it
+            tc::mbar_arrive_expect_tx(bar_ld, kStateBytes);
+            tc::bulk_load(sm8 + OFF_ST, a.ckpt + (bh * N + n) * KV, kStateBytes, bar_ld);
+        }
+        if (warp < 4) {  // dDelta, then dY = T^T dDelta
+            uint32_t r[16];
+            tc::tmem_ld16(tile::taddr(tm + TM_A, warp, 0), r);
+            tc::tmem_ld_wait();
+            float dd[BC];
+#pragma unroll
+            for (int t = 0; t < BC; ++t) dd[t] = __uint_as_float(r[t]) + mdo[t];
+#pragma unroll
+            for (int i = 0; i < BC; ++i) {
+                float acc = 0.f;
+#pragma unroll
+                for (int t = i; t < BC; ++t) acc = fmaf(Tm[t * BC + i], dd[t], acc);
+                dY[i * VM + tid] = acc;
+            }
+        }
+        float dq_r[4] = {0.f, 0.f, 0.f, 0.f}, dk_r[4] = {0.f, 0.f, 0.f, 0.f};
+        float dG_r[4] = {0.f, 0.f, 0.f, 0.f};
+        float dgl_part = 0.f;
+        {  // dKt = Delta dS^T: channel col, tokens 4 qtr ..
+            uint32_t r[4];
+            tc::tmem_ld4(tile::taddr(tm + TM_B, warp, 4 * qtr), r);
+            tc::tmem_ld_wait();
+            const float gl = Gc[ci(col, (BC - 1))];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int t = 4 * qtr + u;
+                const float x = __uint_as_float(r[u]);
+                const float eL = expf(gl - Gc[ci(col, t)]);
+                const float kk = Kr[ci(col, t)];
+                dk_r[u] += x * eL;
+                dG_r[u] -= x * kk * eL;
+                dgl_part += x * kk * eL;
+            }
+        }
+        __syncthreads();
+        tile_rows(dY, OFF_DOY, 32, R32_LO, 16);
+        {  // the first part of dbeta_t, sum_v R_tv dY_tv (warp t), into the M slot (M is done)
+            const int t = warp;
+            float sr = 0.f;
+            for (int vv = lane; vv < V; vv += 32) sr = fmaf(Rv[t * VM + vv], dY[t * VM + vv], sr);
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) sr += __shfl_xor_sync(0xffffffffu, sr, off);
+            if (lane == 0) Mm[t] = sr;
+        }
+        {  // dM (i <= t) and dB (i < t): warp t, lanes over value columns, reduced together
+            const int t = warp;
+            float ot[4], yt[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int vv = lane + 32 * u;
+                ot[u] = dO[t * VM + vv];
+                yt[u] = dY[t * VM + vv];
+            }
+            float w[32];
+#pragma unroll
+            for (int i = 0; i < BC; ++i) {
+                float sm_ = 0.f, sbb = 0.f;
+                if (i <= t) {
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const float dl = Dl[i * VM + lane + 32 * u];
+                        sm_ = fmaf(ot[u], dl, sm_);
+                        sbb = fmaf(yt[u], dl, sbb);
+                    }
+                }
+                w[i] = sm_;
+                w[BC + i] = sbb;
+            }
+            warp_reduce_scatter32(w, lane);
+            if (lane < BC) dM[t * BC + lane] = lane <= t ? a.scale * w[0] : 0.f;
+            else dB[t * BC + lane - BC] = lane - BC < t ? -w[0] : 0.f;
+        }
+        tc::fence_before_sync();
+        __syncthreads();
+        wait_ld();
+        if (tid == 0) {  // [dQg^T | P^T] = S [dO ; dY]^T
+            tc::fence_after_sync();
+#pragma unroll 1
+            for (int p = 0; p < 3; ++p) {
+                const uint32_t ao = p == 2 ? ST_LO : 0u, bo = p == 1 ? R32_LO : 0u;
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks)
+                    tc::mma_bf16(tm + TM_C, tile::desc_k(sb + OFF_ST + ao, 128, ks),
+                                 tile::desc_k(sb + OFF_DOY + bo, 32, ks), ID_K_K32, (p | ks) != 0);
+            }
+            tc::mma_commit(bar_mma);
+        }
+        {  // dgamma_c partial over the value quarter qtr (times gamma_c), then dS <- gamma dS
+            uint32_t r0[16], r1[16];
+            master_ld(r0, r1);
+            float sacc = 0.f;
+#pragma unroll
+            for (int g = 0; g < 4; ++g) {
+                const uint32_t off = tile::kmaj_off(col, 32 * qtr + 8 * g, 128);
+                float shi[8], slo[8];
+                tile::unpack8(*reinterpret_cast<const uint4*>(sm8 + OFF_ST + off), shi);
+                tile::unpack8(*reinterpret_cast<const uint4*>(sm8 + OFF_ST + ST_LO + off), slo);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const float d = __uint_as_float(g < 2 ? r0[8 * g + j] : r1[8 * (g - 2) + j]);
+                    sacc = fmaf(shi[j] + slo[j], d, sacc);
+                }
+            }
+            const float gm = gam[col];
+            red[qtr * KM + col] = sacc * gm;
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                r0[j] = __float_as_uint(__uint_as_float(r0[j]) * gm);
+                r1[j] = __float_as_uint(__uint_as_float(r1[j]) * gm);
+            }
+            master_st(r0, r1);
+        }
+        // dbeta_t = sum_v R_tv dY_tv + sum_{i<t} A'_ti dB_ti;  dV = diag(beta) dY
+        if (tid < cn) {
+            const int t = tid;
+            float s = Mm[t];
+            for (int i = 0; i < t; ++i) s = fmaf(Ap[t * BC + i], dB[t * BC + i], s);
+            a.dbeta[bh * T + t0 + t] = s;
+        }
+        for (int idx = tid; idx < cn * V; idx += NT) {
+            const int t = idx / V, vv = idx - t * V;
+            a.dv[((bh * T) + t0 + t) * V + vv] = bet[t] * dY[t * VM + vv];
+        }
+        wait_mma();
+        {  // dQg = scale dO S^T and P = dY S^T, dKg = -diag(beta) P
+            uint32_t rx[4], ry[4];
+            tc::tmem_ld4(tile::taddr(tm + TM_C, warp, 4 * qtr), rx);
+            tc::tmem_ld4(tile::taddr(tm + TM_C, warp, 16 + 4 * qtr), ry);
+            tc::tmem_ld_wait();
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int t = 4 * qtr + u;
+                const float Ga = expf(Gc[ci(col, t)]);
+                const float dqg = a.scale * __uint_as_float(rx[u]);
+                const float dkg = -bet[t] * __uint_as_float(ry[u]);
+                dq_r[u] += dqg * Ga;
+                dk_r[u] += dkg * Ga;
+                dG_r[u] += (dqg * Qr[ci(col, t)] + dkg * Kr[ci(col, t)]) * Ga;
+            }
+        }
+        tc::fence_before_sync();
+        __syncthreads();
+        if (tid == 0) {  // dS += [scale Qg ; -beta Kg]^T [dO ; dY]
+            tc::fence_after_sync();
+#pragma unroll
+            for (int p = 0; p < 3; ++p) {
+                const uint32_t ao = p == 2 ? R32_LO : 0u, bo = p == 1 ? R32_LO : 0u;
+#pragma unroll
+                for (int ks = 0; ks < 2; ++ks)
+                    tc::mma_bf16(tm + TM_M, tile::desc_mn(sb + OFF_AQK + ao, 4096, ks),
+                                 tile::desc_mn(sb + OFF_DOY + bo, 4096, ks), ID_MN_MN128, 1u);
+            }
+            tc::mma_commit(bar_mma);
+        }
+        // pairwise terms of dA' = diag(beta) dB and dM, thread (c = col, tokens 4 qtr + r)
+        {
+            const int c = col;
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                const int t = 4 * qtr + r;
+                const float gt = Gc[ci(c, t)], kt = Kr[ci(c, t)], qt = Qr[ci(c, t)];
+                float rowA = 0.f, rowM = 0.f, colA = 0.f, colM = 0.f;
+#pragma unroll
+                for (int i = 0; i < BC; ++i) {
+                    if (i <= t) {
+                        const float kiE = Kr[ci(c, i)] * __expf(gt - Gc[ci(c, i)]);
+                        rowM = fmaf(dM[t * BC + i], kiE, rowM);
+                        rowA = fmaf(bet[t] * dB[t * BC + i], kiE, rowA);
+                    }
+                }
+#pragma unroll
+                for (int s2 = 0; s2 < BC; ++s2) {
+                    if (s2 >= t) {
+                        const float E = __expf(Gc[ci(c, s2)] - gt);
+                        colM = fmaf(dM[s2 * BC + t], Qr[ci(c, s2)] * E, colM);
+                        colA = fmaf(bet[s2] * dB[s2 * BC + t], Kr[ci(c, s2)] * E, colA);
+                    }
+                }
+                dq_r[r] += rowM;
+                dk_r[r] += rowA + colA + colM;
+                dG_r[r] += kt * rowA + qt * rowM - kt * (colA + colM);
+            }
+        }
+        __syncthreads();
+        // dG exchange ([BC][KM] in XT), the last token's share of d(G_last), reverse cumsum,
+        // gate derivative; dq and dk out
+#pragma unroll
+        for (int r = 0; r < 4; ++r) XT[(4 * qtr + r) * KM + col] = dG_r[r];
+        red[qtr * KM + col] += dgl_part;
+        __syncthreads();
+        {
+            const int c = col;
+            const float dgl = red[c] + red[KM + c] + red[2 * KM + c] + red[3 * KM + c];
+            float suffix = dgl;
+            for (int t = BC - 1; t > 4 * qtr + 3; --t) suffix += XT[t * KM + c];
+            const float dtc = a.dt_bias[(size_t)h * K + c];
+            float zr[4];
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                const int t = 4 * qtr + r;
+                zr[r] = t < cn ? ld_io(a.z + ((bh * T) + t0 + t) * K + c) : 0.f;
+            }
+#pragma unroll
+            for (int r = 3; r >= 0; --r) {
+                const int t = 4 * qtr + r;
+                suffix += XT[t * KM + c];
+                if (t < cn) {
+                    const size_t gi = ((bh * T) + t0 + t) * K + c;
+                    const float x = zr[r] + dtc;
+                    const float g = -(eA * softplus_f32(x));
+                    const float dz = suffix * (-eA) * sigmoid_f32(x);
+                    a.dz[gi] = dz;
+                    ddt_acc += dz;
+                    dA_acc = fmaf(suffix, g, dA_acc);
+                    a.dq[gi] = dq_r[r];
+                    a.dk[gi] = dk_r[r];
+                }
+            }
+        }
+        __syncthreads();
+    }
+    if (N > 0 && !*s_fail) wait_mma();  // the last dS update
+
+    // ---- dh0, and the per-(b, h) partial sums of dA_log and ddt_bias
+    if (a.dh0) {
+        uint32_t r0[16], r1[16];
+        master_ld(r0, r1);
+        float* p = a.dh0 + bh * KV + (size_t)col * V + 32 * qtr;
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            p[j] = __uint_as_float(r0[j]);
+            p[16 + j] = __uint_as_float(r1[j]);
+        }
+    }
+    red[qtr * KM + col] = ddt_acc;
+    for (int off = 16; off > 0; off >>= 1) dA_acc += __shfl_xor_sync(0xffffffffu, dA_acc, off);
+    __syncthreads();
+    if (lane == 0) XT[warp] = dA_acc;
+    if (tid < K) a.ddt_part[bh * K + tid] = red[tid] + red[KM + tid] + red[2 * KM + tid] + red[3 * KM + tid];
+    tc::fence_before_sync();
+    __syncthreads();
+    if (tid == 0) {
+        float s = 0.f;
+        for (int w = 0; w < NT / 32; ++w) s += XT[w];
+        a.dA_part[bh] = s;
+    }
+    if (warp == 0) {
+        tc::fence_after_sync();
+        tc::tmem_dealloc(tm, TM_COLS);
+    }
+}
+
 // dA_log[h] = sum_b dA_part[b, h];  ddt_bias[h, c] = sum_b ddt_part[b, h, c]
 __global__ void kda_bwd_reduce_kernel(int B, int H, int K, const float* __restrict__ dA_part,
                                       const float* __restrict__ ddt_part, float* __restrict__ dA_log,
@@ -773,13 +1531,30 @@ cudaError_t launch_chunk_backward(const BwdLaunch& L, cudaStream_t s) {
         kda_chunk_bwd_kernel<IO, KC><<<(unsigned)BH, BNT, BWD_SMEM_BYTES, s>>>(a);
         return cudaGetLastError();
     };
-    using Fixed = std::integral_constant<int, 128>;
+    // K = V = 128: the tensor-core form (its state copies are the same 64 KB as an fp32 state)
+    auto run_tc = [&](auto io_tag) -> cudaError_t {
+        using IO = decltype(io_tag);
+        BwdArgs<IO> a;
+        a.H = H; a.T = T; a.K = K; a.V = V;
+        a.q = static_cast<const IO*>(L.q); a.k = static_cast<const IO*>(L.k);
+        a.v = static_cast<const IO*>(L.v); a.z = static_cast<const IO*>(L.z);
+        a.beta = static_cast<const IO*>(L.beta); a.d_o = static_cast<const IO*>(L.d_o);
+        a.A_log = L.A_log; a.dt_bias = L.dt_bias; a.h0 = L.h0; a.dhT = L.dhT; a.scale = L.scale;
+        a.dq = L.dq; a.dk = L.dk; a.dv = L.dv; a.dz = L.dz; a.dbeta = L.dbeta; a.dh0 = L.dh0;
+        a.ckpt = ckpt; a.rd = rd; a.dA_part = dA_part; a.ddt_part = ddt_part;
+        cudaError_t err = cudaFuncSetAttribute(kda_chunk_bwd_tc_kernel<IO>,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               (int)bwdtc::SMEM_BYTES);
+        if (err != cudaSuccess) return err;
+        kda_chunk_bwd_tc_kernel<IO><<<(unsigned)BH, bwdtc::NT, bwdtc::SMEM_BYTES, s>>>(a);
+        return cudaGetLastError();
+    };
     using Any = std::integral_constant<int, 0>;
     const bool fixed = K == 128 && V == 128;
     if (L.io == KDA_BF16)
-        e = fixed ? run(__nv_bfloat16{}, Fixed{}) : run(__nv_bfloat16{}, Any{});
+        e = fixed ? run_tc(__nv_bfloat16{}) : run(__nv_bfloat16{}, Any{});
     else
-        e = fixed ? run(float{}, Fixed{}) : run(float{}, Any{});
+        e = fixed ? run_tc(float{}) : run(float{}, Any{});
     if (e == cudaSuccess) {
         const int n = H * K;
         kda_bwd_reduce_kernel<<<(n + 255) / 256, 256, 0, s>>>(B, H, K, dA_part, ddt_part, L.dA_log,
@@ -789,6 +1564,18 @@ cudaError_t launch_chunk_backward(const BwdLaunch& L, cudaStream_t s) {
     }
     const cudaError_t ef = cudaFreeAsync(scratch, s);
     return e != cudaSuccess ? e : ef;
+}
+
+cudaError_t read_and_clear_bwd_timeout(int* timed_out) {
+    int v = 0;
+    cudaError_t e = cudaMemcpyFromSymbol(&v, g_kda_bwd_timeout, sizeof(int));
+    if (e != cudaSuccess) return e;
+    *timed_out = v;
+    if (v) {
+        const int zero = 0;
+        e = cudaMemcpyToSymbol(g_kda_bwd_timeout, &zero, sizeof(int));
+    }
+    return e;
 }
 
 }  // namespace kda
