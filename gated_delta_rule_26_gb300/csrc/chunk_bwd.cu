@@ -736,46 +736,60 @@ __global__ void __launch_bounds__(BNT, 1) kda_chunk_bwd_kernel(const BwdArgs<IO>
 //             dKt^T = dS Delta^T                        M = c, N = 16, K = v
 //             [dQg^T | P^T] = S [dO ; dY]^T             M = c, N = 32 (dQg = scale x)
 //             dS <- diag(gamma) dS + [scale Qg ; -beta Kg]^T [dO ; dY]   K = 32 tokens
-// Every operand x is split into bf16 x_hi = bf16(x) and x_lo = bf16(x - x_hi); a product A B
-// is accumulated in fp32 as A_hi B_hi + A_hi B_lo + A_lo B_hi.  x_hi + x_lo is within
-// 2^-16 |x| of x and the dropped A_lo B_lo is below 2^-16 |A| |B|, so each product term is
-// within about 3 * 2^-16 of its exact value, and the state and its adjoint stay fp32 in
-// TMEM.  The operand copy of the state (hi and lo, 64 KB) is also what phase 1 keeps per
+// Every operand x is split into bf16 x_hi = bf16(x) and x_lo = bf16(x - x_hi), within 2^-16 |x|
+// of x together, and a product A B is accumulated in fp32 as the four products of the halves.
+// The small operand's halves are stacked along N ([B_hi ; B_lo], 32 or 64 rows), so each K
+// step of the state is read by two MMAs (A_hi, A_lo) and the epilogue adds the two column
+// blocks; each product term is within about 2 * 2^-16 of its exact value, and the state and
+// its adjoint stay fp32 in TMEM.  The operand copy of the state (hi and lo, 64 KB) is also what phase 1 keeps per
 // chunk: phase 2 brings it back with one bulk copy, already in the operand layout.  The
 // pairwise terms, the T solve, the gate and the per-token outputs are the CUDA-core code of
 // the kernel above.
 namespace bwdtc {
 constexpr int NT = 512;
 // shared memory (bytes from a 1024-byte aligned base): tensor-core operand tiles, each a
-// K-major 128-byte-swizzled tile (read MN-major where a product needs its transpose)
+// K-major 128-byte-swizzled tile (read MN-major where a product needs its transpose); the
+// small tiles hold the hi rows first, then the lo rows
 constexpr uint32_t OFF_ST = 0;                 // state / adjoint copy [c][v], 128 rows: hi
 constexpr uint32_t ST_LO = 32768;              //   lo
-constexpr uint32_t OFF_KT = 65536;             // Kt [t][c], 16 rows (hi, lo at +R16_LO)
-constexpr uint32_t OFF_DLT = OFF_KT + 8192;    // Delta [t][v], 16 rows
-constexpr uint32_t OFF_DOY = OFF_DLT + 8192;   // [dO ; dY] [t'][v], 32 rows (hi, lo at +R32_LO)
-constexpr uint32_t OFF_AQK = OFF_DOY + 16384;  // phase 2 [scale Qg ; -beta Kg] [t'][c], 32 rows;
-                                               // phase 1 Kg [t][c], 16 rows
-constexpr uint32_t R16_LO = 4096, R32_LO = 8192;
+constexpr uint32_t OFF_KT = 65536;             // Kt [t][c]: 32 rows (hi 0..15, lo 16..31)
+constexpr uint32_t OFF_DLT = OFF_KT + 8192;    // Delta [t][v]: 32 rows
+constexpr uint32_t OFF_DOY = OFF_DLT + 8192;   // [dO ; dY] [t'][v]: 64 rows (hi 0..31, lo 32..63)
+constexpr uint32_t OFF_AQK = OFF_DOY + 16384;  // phase 2 [scale Qg ; -beta Kg] [t'][c]: 64 rows;
+                                               // phase 1 Kg [t][c]: 32 rows
 constexpr uint32_t OFF_F = OFF_AQK + 16384;    // fp32 area (float offsets below)
+// R, Delta, A', T, M are contiguous: phase 2 brings them back with one bulk copy
 constexpr int F_Q = 0, F_K = F_Q + KM * GP, F_G = F_K + KM * GP;
-constexpr int F_R = F_G + KM * GP, F_DO = F_R + BC * VM, F_DL = F_DO + BC * VM;
-constexpr int F_DY = F_DL + BC * VM, F_XT = F_DY + BC * VM;
-constexpr int F_AP = F_XT + BC * KM, F_TM = F_AP + BC * BC, F_MM = F_TM + BC * BC;
-constexpr int F_DB = F_MM + BC * BC, F_DM = F_DB + BC * BC;
+constexpr int F_R = F_G + KM * GP, F_DL = F_R + BC * VM;
+constexpr int F_AP = F_DL + BC * VM, F_TM = F_AP + BC * BC, F_MM = F_TM + BC * BC;
+constexpr int F_DO = F_MM + BC * BC, F_DY = F_DO + BC * VM, F_XT = F_DY + BC * VM;
+constexpr int F_DB = F_XT + BC * KM, F_DM = F_DB + BC * BC;
 constexpr int F_BET = F_DM + BC * BC, F_GAM = F_BET + BC, F_RED = F_GAM + KM;
-constexpr int F_END = F_RED + 4 * KM;
-constexpr uint32_t OFF_MISC = OFF_F + 4u * F_END;  // two mbarriers, TMEM base, failure flag
-constexpr size_t SMEM_BYTES = OFF_MISC + 64 + 1024;  // + slack for the 1024-byte alignment
+constexpr int F_GT = F_RED + 4 * KM;            // g (the per-token log decay) [KM][GP]
+constexpr int F_END = F_GT + KM * GP;
+constexpr uint32_t OFF_MISC = OFF_F + 4u * F_END;  // four mbarriers, TMEM base, failure flag
+// staging of the next chunk's raw q, k, z and v (phase 1) or dO (phase 2) rows, bulk-copied
+constexpr uint32_t OFF_STG = OFF_MISC + 64;
+template <typename IO>
+constexpr uint32_t stg_tile() { return (uint32_t)(BC * KM * sizeof(IO)); }
+template <typename IO>
+constexpr size_t smem_bytes() { return OFF_STG + 4 * stg_tile<IO>() + 1024; }  // + alignment slack
 static_assert((OFF_F + 4u * F_R) % 16 == 0 && (OFF_F + 4u * F_DL) % 16 == 0 &&
               (OFF_F + 4u * F_DO) % 16 == 0 && (OFF_F + 4u * F_DY) % 16 == 0, "float4 rows");
-static_assert(OFF_MISC % 8 == 0 && SMEM_BYTES <= 232448, "backward tensor-core shared memory");
-// TMEM columns: the state or its adjoint, and the three accumulators of the N = 16 / 32 products
+static_assert(OFF_MISC % 16 == 0 && OFF_STG % 16 == 0, "mbarriers and bulk-copy destinations");
+static_assert(smem_bytes<float>() <= 232448, "backward tensor-core shared memory");
+// TMEM columns: the state or its adjoint, and the accumulators of the N = 32 / 64 products
+// (one column block per half of the small operand)
 constexpr uint32_t TM_M = 0, TM_A = 128, TM_B = 160, TM_C = 192, TM_COLS = 256;
-constexpr uint32_t ID_MN_K16 = tc::idesc_bf16(128, 16, 1, 0);
-constexpr uint32_t ID_K_K16 = tc::idesc_bf16(128, 16, 0, 0);
+constexpr uint32_t ID_MN_K32 = tc::idesc_bf16(128, 32, 1, 0);
 constexpr uint32_t ID_K_K32 = tc::idesc_bf16(128, 32, 0, 0);
+constexpr uint32_t ID_K_K64 = tc::idesc_bf16(128, 64, 0, 0);
 constexpr uint32_t ID_MN_MN128 = tc::idesc_bf16(128, 128, 1, 1);
 constexpr uint32_t kStateBytes = 65536;        // one operand copy of the state (hi + lo)
+// floats phase 1 keeps per chunk for phase 2: R, Delta [BC][V], then A', T, M [BC][BC]
+constexpr int RD = 2 * BC * VM + 3 * BC * BC;
+static_assert(F_DL == F_R + BC * VM && F_AP == F_DL + BC * VM && F_TM == F_AP + BC * BC &&
+              F_MM == F_TM + BC * BC && F_MM + BC * BC == F_R + RD, "R, Delta, A', T, M contiguous");
 }  // namespace bwdtc
 
 // x = hi + lo with hi = bf16(x), lo = bf16(x - hi), eight values at a time
@@ -811,10 +825,13 @@ __global__ void __launch_bounds__(bwdtc::NT, 1) kda_chunk_bwd_tc_kernel(const Bw
     float* bet = F + F_BET;
     float* gam = F + F_GAM;
     float* red = F + F_RED;
+    float* Gt = F + F_GT;
     uint64_t* bar_mma = reinterpret_cast<uint64_t*>(sm8 + OFF_MISC);
-    uint64_t* bar_ld = bar_mma + 1;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm8 + OFF_MISC + 16);
-    volatile int* s_fail = reinterpret_cast<volatile int*>(sm8 + OFF_MISC + 20);
+    uint64_t* bar_ld = bar_mma + 1;   // the state copy (phase 2)
+    uint64_t* bar_in = bar_mma + 2;   // a chunk's staged raw rows
+    uint64_t* bar_rd = bar_mma + 3;   // a chunk's R, Delta, A', T, M (phase 2)
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm8 + OFF_MISC + 32);
+    volatile int* s_fail = reinterpret_cast<volatile int*>(sm8 + OFF_MISC + 36);
     const uint32_t sb = tc::smem_u32(sm8);
 
     constexpr int K = KM, V = VM;
@@ -823,7 +840,8 @@ __global__ void __launch_bounds__(bwdtc::NT, 1) kda_chunk_bwd_tc_kernel(const Bw
     const size_t bh = blockIdx.x;
     const int h = (int)(bh % a.H);
     const int N = (T + BC - 1) / BC;
-    const float eA = expf(a.A_log[h]);
+    const float eA = expf(a.A_log[h]), ieA = expf(-a.A_log[h]);
+    const float dtc = __ldg(a.dt_bias + (size_t)h * KM + (threadIdx.x & 127));
     const size_t KV = (size_t)K * V;
     // thread roles: channel or value column col (= the TMEM lane this warp reaches), and the
     // quarter qtr (tokens 4 qtr .. + 3, or TMEM columns 32 qtr .. + 31 of a 128-column matrix)
@@ -832,6 +850,8 @@ __global__ void __launch_bounds__(bwdtc::NT, 1) kda_chunk_bwd_tc_kernel(const Bw
     if (tid == 0) {
         tc::mbar_init(bar_mma, 1);
         tc::mbar_init(bar_ld, 1);
+        tc::mbar_init(bar_in, 1);
+        tc::mbar_init(bar_rd, 1);
         *s_fail = 0;
         tc::fence_barrier_init();
     }
@@ -843,7 +863,7 @@ __global__ void __launch_bounds__(bwdtc::NT, 1) kda_chunk_bwd_tc_kernel(const Bw
     __syncthreads();
     tc::fence_after_sync();
     const uint32_t tm = *tmem_slot;
-    uint32_t ph_mma = 0, ph_ld = 0;
+    uint32_t ph_mma = 0, ph_ld = 0, ph_in = 0, ph_rd = 0;
     auto fail = [&]() {
         *s_fail = 1;
         atomicExch(&g_kda_bwd_timeout, 1);
@@ -879,9 +899,8 @@ __global__ void __launch_bounds__(bwdtc::NT, 1) kda_chunk_bwd_tc_kernel(const Bw
         }
         master_st(r0, r1);
     };
-    // The operand copy (hi, lo) of the TMEM matrix; with `decay`, the matrix is then scaled
-    // by gamma in place (the copy keeps the undecayed values).
-    auto master_copy = [&](bool decay) {
+    // The operand copy (hi, lo) of the TMEM matrix.
+    auto master_copy = [&]() {
         uint32_t r0[16], r1[16];
         master_ld(r0, r1);
 #pragma unroll
@@ -896,87 +915,80 @@ __global__ void __launch_bounds__(bwdtc::NT, 1) kda_chunk_bwd_tc_kernel(const Bw
             *reinterpret_cast<uint4*>(sm8 + OFF_ST + ST_LO + off) = lo;
         }
         tc::fence_proxy_async_smem();
-        if (decay) {
-            const float gm = gam[col];
+    };
+    // The TMEM matrix scaled by gamma in place, row col.
+    auto master_decay = [&]() {
+        uint32_t r0[16], r1[16];
+        master_ld(r0, r1);
+        const float gm = gam[col];
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-                r0[j] = __float_as_uint(__uint_as_float(r0[j]) * gm);
-                r1[j] = __float_as_uint(__uint_as_float(r1[j]) * gm);
-            }
-            master_st(r0, r1);
+        for (int j = 0; j < 16; ++j) {
+            r0[j] = __float_as_uint(__uint_as_float(r0[j]) * gm);
+            r1[j] = __float_as_uint(__uint_as_float(r1[j]) * gm);
         }
+        master_st(r0, r1);
     };
 
-    // Ask L2 for the inputs of chunk n, one 128-byte line per thread (as the CUDA-core form)
-    // and, in phase 2, the state copy that phase 1 kept for it.
-    auto prefetch_chunk = [&](int n, bool full) {
-        if (n < 0 || n >= N) return;
-        const int t0 = n * BC, cn = min(BC, T - t0);
-        const int io = (int)sizeof(IO);
-        const int lk = (cn * K * io + 127) / 128, lv = (cn * V * io + 127) / 128;
-        const int lrd = (2 * BC * V * 4 + 127) / 128;
-        int i = tid;
-        const char* p = nullptr;
-        if (i < lk) p = reinterpret_cast<const char*>(a.k + ((bh * T) + t0) * K) + 128 * i;
-        else if ((i -= lk) < lk) p = reinterpret_cast<const char*>(a.z + ((bh * T) + t0) * K) + 128 * i;
-        else if (full && (i -= lk) < lk) p = reinterpret_cast<const char*>(a.q + ((bh * T) + t0) * K) + 128 * i;
-        else if (full && (i -= lk) < lv) p = reinterpret_cast<const char*>(a.d_o + ((bh * T) + t0) * V) + 128 * i;
-        else if (full && (i -= lv) < lrd) p = reinterpret_cast<const char*>(a.rd + (bh * N + n) * (size_t)(2 * BC * V)) + 128 * i;
-        else if (!full && (i -= lk) < lv) p = reinterpret_cast<const char*>(a.v + ((bh * T) + t0) * V) + 128 * i;
-        if (p) prefetch_l2(p);
-        if (full) prefetch_l2(reinterpret_cast<const char*>(a.ckpt + (bh * N + n) * KV) + 128 * tid);
+    // Ask L2 for the state copy phase 1 kept for chunk n, one 128-byte line per thread.
+    auto prefetch_state = [&](int n) {
+        if (n >= 0 && n < N) prefetch_l2(reinterpret_cast<const char*>(a.ckpt + (bh * N + n) * KV) + 128 * tid);
     };
-    // Inputs of chunk n into the fp32 tiles: k, G (from z), beta, and v (phase 1) or q, dO,
-    // R and Delta as phase 1 stored them (phase 2); then the in-chunk cumulative sum and gamma.
+    // Request chunk n's raw q, k, z and v (phase 1) or dO (phase 2) rows into the staging tiles
+    // (bulk copies on bar_in, issued by thread 0) and its beta into bnext (threads < BC).
+    float bnext = 0.f;
+    auto request = [&](int n, bool full) {
+        const int t0 = n * BC, cn = min(BC, T - t0);
+        if (tid == 0) {
+            const uint32_t bytes = (uint32_t)(cn * K * sizeof(IO));
+            const size_t g0 = (bh * T + t0) * (size_t)K;
+            tc::mbar_arrive_expect_tx(bar_in, 4 * bytes);
+            tc::bulk_load(sm8 + OFF_STG, a.q + g0, bytes, bar_in);
+            tc::bulk_load(sm8 + OFF_STG + stg_tile<IO>(), a.k + g0, bytes, bar_in);
+            tc::bulk_load(sm8 + OFF_STG + 2 * stg_tile<IO>(), a.z + g0, bytes, bar_in);
+            tc::bulk_load(sm8 + OFF_STG + 3 * stg_tile<IO>(), (full ? a.d_o : a.v) + g0, bytes, bar_in);
+        }
+        if (tid < BC) bnext = tid < cn ? ld_io(a.beta + bh * T + t0 + tid) : 0.f;
+    };
+    // Request chunk n's R, Delta, A', T, M (phase 2) into place (one bulk copy on bar_rd).
+    auto request_rd = [&](int n) {
+        if (tid == 0) {
+            tc::mbar_arrive_expect_tx(bar_rd, RD * 4);
+            tc::bulk_load(Rv, a.rd + (bh * N + n) * (size_t)RD, RD * 4, bar_rd);
+        }
+    };
+    // Chunk n's staged rows into the fp32 tiles: q, k, G and g (from z), beta, and v (phase 1,
+    // into R) or dO (phase 2, whose R, Delta, A', T, M arrive by request_rd); the staging is then
+    // free and the next chunk's rows are requested; then the in-chunk cumulative sum and gamma.
     auto load_inputs = [&](int n, bool full) {
         const int t0 = n * BC, cn = min(BC, T - t0);
-        constexpr int PER = BC * KM / NT;
-        float kx[PER], qx[PER], zx[PER], dtx[PER], vx[PER], ox[PER], dx[PER];
-        const float* rdn = a.rd + (bh * N + n) * (size_t)(2 * BC * V);
-        float bx = 0.f;
+        if (!tc::mbar_wait(bar_in, ph_in)) fail();
+        ph_in ^= 1u;
+        if (full) {
+            if (!tc::mbar_wait(bar_rd, ph_rd)) fail();
+            ph_rd ^= 1u;
+        }
+        const IO* sq = reinterpret_cast<const IO*>(sm8 + OFF_STG);
+        const IO* sk = sq + BC * K;
+        const IO* sz = sk + BC * K;
+        const IO* sv = sz + BC * K;
 #pragma unroll
-        for (int r = 0; r < PER; ++r) {
-            const int idx = tid + r * NT, t = idx / K, c = idx - t * K;
+        for (int r = 0; r < BC * KM / NT; ++r) {
+            const int idx = tid + r * NT, t = idx >> 7;  // column col
             const bool in = t < cn;
-            const size_t gi = ((bh * T) + t0 + t) * K + c;
-            kx[r] = in ? ld_io(a.k + gi) : 0.f;
-            qx[r] = (full && in) ? ld_io(a.q + gi) : 0.f;
-            zx[r] = in ? ld_io(a.z + gi) : 0.f;
-            dtx[r] = __ldg(a.dt_bias + (size_t)h * K + c);
+            const float g = in ? kda_log_decay(ld_io(sz + idx), dtc, eA) : 0.f;
+            Kr[ci(col, t)] = in ? ld_io(sk + idx) : 0.f;
+            Qr[ci(col, t)] = in ? ld_io(sq + idx) : 0.f;
+            Gc[ci(col, t)] = g;
+            Gt[ci(col, t)] = g;
+            const float x = in ? ld_io(sv + idx) : 0.f;
+            if (full) dO[idx] = x;
+            else Rv[idx] = x;
         }
-#pragma unroll
-        for (int r = 0; r < PER; ++r) {
-            const int idx = tid + r * NT, t = idx / V, vv = idx - t * V;
-            const bool in = t < cn;
-            const size_t gi = ((bh * T) + t0 + t) * V + vv;
-            if (full) {
-                vx[r] = __ldcg(rdn + idx);
-                dx[r] = __ldcg(rdn + BC * V + idx);
-            } else {
-                vx[r] = in ? ld_io(a.v + gi) : 0.f;
-                dx[r] = 0.f;
-            }
-            ox[r] = (full && in) ? ld_io(a.d_o + gi) : 0.f;
-        }
-        if (tid < BC && tid < cn) bx = ld_io(a.beta + bh * T + t0 + tid);
-#pragma unroll
-        for (int r = 0; r < PER; ++r) {
-            const int idx = tid + r * NT, t = idx / K, c = idx - t * K;
-            Kr[ci(c, t)] = kx[r];
-            if (full) Qr[ci(c, t)] = qx[r];
-            Gc[ci(c, t)] = t < cn ? kda_log_decay(zx[r], dtx[r], eA) : 0.f;
-        }
-#pragma unroll
-        for (int r = 0; r < PER; ++r) {
-            const int idx = tid + r * NT;
-            Rv[idx] = vx[r];
-            if (full) {
-                dO[idx] = ox[r];
-                Dl[idx] = dx[r];
-            }
-        }
-        if (tid < BC) bet[tid] = bx;
+        if (tid < BC) bet[tid] = bnext;
+        tc::fence_proxy_async_smem();
         __syncthreads();
+        const int nx = full ? n - 1 : n + 1;
+        if (nx >= 0 && nx < N) request(nx, full);
         if (tid < K) {
             float run = 0.f;
             for (int t = 0; t < BC; ++t) {
@@ -1004,12 +1016,12 @@ __global__ void __launch_bounds__(bwdtc::NT, 1) kda_chunk_bwd_tc_kernel(const Bw
             }
             uint4 hi, lo;
             split8(kt, hi, lo);
-            *reinterpret_cast<uint4*>(sm8 + OFF_KT + tile::kmaj_off(t, c0, 16)) = hi;
-            *reinterpret_cast<uint4*>(sm8 + OFF_KT + R16_LO + tile::kmaj_off(t, c0, 16)) = lo;
+            *reinterpret_cast<uint4*>(sm8 + OFF_KT + tile::kmaj_off(t, c0, 32)) = hi;
+            *reinterpret_cast<uint4*>(sm8 + OFF_KT + tile::kmaj_off(16 + t, c0, 32)) = lo;
             if (!full) {
                 split8(kg, hi, lo);
-                *reinterpret_cast<uint4*>(sm8 + OFF_AQK + tile::kmaj_off(t, c0, 16)) = hi;
-                *reinterpret_cast<uint4*>(sm8 + OFF_AQK + R16_LO + tile::kmaj_off(t, c0, 16)) = lo;
+                *reinterpret_cast<uint4*>(sm8 + OFF_AQK + tile::kmaj_off(t, c0, 32)) = hi;
+                *reinterpret_cast<uint4*>(sm8 + OFF_AQK + tile::kmaj_off(16 + t, c0, 32)) = lo;
             } else {
                 const float nb = -bet[t];
 #pragma unroll
@@ -1018,11 +1030,11 @@ __global__ void __launch_bounds__(bwdtc::NT, 1) kda_chunk_bwd_tc_kernel(const Bw
                     kg[j] *= nb;
                 }
                 split8(qg, hi, lo);
-                *reinterpret_cast<uint4*>(sm8 + OFF_AQK + tile::kmaj_off(t, c0, 32)) = hi;
-                *reinterpret_cast<uint4*>(sm8 + OFF_AQK + R32_LO + tile::kmaj_off(t, c0, 32)) = lo;
+                *reinterpret_cast<uint4*>(sm8 + OFF_AQK + tile::kmaj_off(t, c0, 64)) = hi;
+                *reinterpret_cast<uint4*>(sm8 + OFF_AQK + tile::kmaj_off(32 + t, c0, 64)) = lo;
                 split8(kg, hi, lo);
-                *reinterpret_cast<uint4*>(sm8 + OFF_AQK + tile::kmaj_off(16 + t, c0, 32)) = hi;
-                *reinterpret_cast<uint4*>(sm8 + OFF_AQK + R32_LO + tile::kmaj_off(16 + t, c0, 32)) = lo;
+                *reinterpret_cast<uint4*>(sm8 + OFF_AQK + tile::kmaj_off(16 + t, c0, 64)) = hi;
+                *reinterpret_cast<uint4*>(sm8 + OFF_AQK + tile::kmaj_off(48 + t, c0, 64)) = lo;
             }
         } else if (full) {
             const int i = tid - 256, t = i & 15, v0 = 8 * (i >> 4);
@@ -1035,17 +1047,17 @@ __global__ void __launch_bounds__(bwdtc::NT, 1) kda_chunk_bwd_tc_kernel(const Bw
             o[0] = o0.x; o[1] = o0.y; o[2] = o0.z; o[3] = o0.w; o[4] = o1.x; o[5] = o1.y; o[6] = o1.z; o[7] = o1.w;
             uint4 hi, lo;
             split8(d, hi, lo);
-            *reinterpret_cast<uint4*>(sm8 + OFF_DLT + tile::kmaj_off(t, v0, 16)) = hi;
-            *reinterpret_cast<uint4*>(sm8 + OFF_DLT + R16_LO + tile::kmaj_off(t, v0, 16)) = lo;
+            *reinterpret_cast<uint4*>(sm8 + OFF_DLT + tile::kmaj_off(t, v0, 32)) = hi;
+            *reinterpret_cast<uint4*>(sm8 + OFF_DLT + tile::kmaj_off(16 + t, v0, 32)) = lo;
             split8(o, hi, lo);
-            *reinterpret_cast<uint4*>(sm8 + OFF_DOY + tile::kmaj_off(t, v0, 32)) = hi;
-            *reinterpret_cast<uint4*>(sm8 + OFF_DOY + R32_LO + tile::kmaj_off(t, v0, 32)) = lo;
+            *reinterpret_cast<uint4*>(sm8 + OFF_DOY + tile::kmaj_off(t, v0, 64)) = hi;
+            *reinterpret_cast<uint4*>(sm8 + OFF_DOY + tile::kmaj_off(32 + t, v0, 64)) = lo;
         }
         tc::fence_proxy_async_smem();
     };
-    // Rows of a [BC][VM] fp32 tile into rows row0 .. of a 16- or 32-row operand tile (hi, lo),
-    // one (row, 8 columns) item per thread of the first 256.
-    auto tile_rows = [&](const float* src, uint32_t off, int rows, uint32_t lo_off, int row0) {
+    // Rows of a [BC][VM] fp32 tile into rows row0 .. (hi) and row0 + lo_row .. (lo) of a 32- or
+    // 64-row operand tile, one (row, 8 columns) item per thread of the first 256.
+    auto tile_rows = [&](const float* src, uint32_t off, int rows, int lo_row, int row0) {
         if (tid < 256) {
             const int t = tid & 15, v0 = 8 * (tid >> 4);
             const float4 x0 = *reinterpret_cast<const float4*>(src + t * VM + v0);
@@ -1054,12 +1066,12 @@ __global__ void __launch_bounds__(bwdtc::NT, 1) kda_chunk_bwd_tc_kernel(const Bw
             uint4 hi, lo;
             split8(f, hi, lo);
             *reinterpret_cast<uint4*>(sm8 + off + tile::kmaj_off(row0 + t, v0, rows)) = hi;
-            *reinterpret_cast<uint4*>(sm8 + off + lo_off + tile::kmaj_off(row0 + t, v0, rows)) = lo;
+            *reinterpret_cast<uint4*>(sm8 + off + tile::kmaj_off(row0 + lo_row + t, v0, rows)) = lo;
         }
         tc::fence_proxy_async_smem();
     };
-    // A' (i < t) and, in phase 2, M (i <= t) with the exact pairwise decay: warp t
-    auto arows = [&](bool full) {
+    // A' (i < t) and M (i <= t) with the exact pairwise decay: warp t
+    auto arows = [&]() {
         const int t = warp;
         float gt[4], kt[4], qt[4];
 #pragma unroll
@@ -1067,7 +1079,7 @@ __global__ void __launch_bounds__(bwdtc::NT, 1) kda_chunk_bwd_tc_kernel(const Bw
             const int c = lane + 32 * u;
             gt[u] = Gc[ci(c, t)];
             kt[u] = Kr[ci(c, t)];
-            qt[u] = full ? Qr[ci(c, t)] : 0.f;
+            qt[u] = Qr[ci(c, t)];
         }
         float w[32];
 #pragma unroll
@@ -1077,7 +1089,7 @@ __global__ void __launch_bounds__(bwdtc::NT, 1) kda_chunk_bwd_tc_kernel(const Bw
 #pragma unroll
                 for (int u = 0; u < 4; ++u) {
                     const int c = lane + 32 * u;
-                    const float kiE = Kr[ci(c, i)] * __expf(gt[u] - Gc[ci(c, i)]);
+                    const float kiE = i == t ? kt[u] : Kr[ci(c, i)] * __expf(gt[u] - Gc[ci(c, i)]);
                     sa = fmaf(kt[u], kiE, sa);
                     sq = fmaf(qt[u], kiE, sq);
                 }
@@ -1087,12 +1099,12 @@ __global__ void __launch_bounds__(bwdtc::NT, 1) kda_chunk_bwd_tc_kernel(const Bw
         }
         warp_reduce_scatter32(w, lane);
         if (lane < BC) Ap[t * BC + lane] = lane < t ? w[0] : 0.f;
-        else if (full) Mm[t * BC + lane - BC] = lane - BC <= t ? w[0] : 0.f;
+        else Mm[t * BC + lane - BC] = lane - BC <= t ? w[0] : 0.f;
     };
-    // T = (I + diag(beta) A')^{-1} by forward substitution, one column per thread
+    // T = (I + diag(beta) A')^{-1} by forward substitution, one column per thread of warp 4
     auto t_solve = [&]() {
-        if (tid < BC) {
-            const int j = tid;
+        if (tid >= 128 && tid < 128 + BC) {
+            const int j = tid - 128;
             float x[BC];
 #pragma unroll
             for (int t = 0; t < BC; ++t) {
@@ -1107,43 +1119,48 @@ __global__ void __launch_bounds__(bwdtc::NT, 1) kda_chunk_bwd_tc_kernel(const Bw
 
     // ======================================================= phase 1: chunk states forward
     master_init(a.h0 ? a.h0 + bh * KV : nullptr);
+    if (N > 0) request(0, false);
     tc::fence_before_sync();
     __syncthreads();
     for (int n = 0; n < N && !*s_fail; ++n) {
         load_inputs(n, false);
-        prefetch_chunk(n + 1, false);
         if (n > 0) wait_mma();  // the previous chunk's state update has read Kt and Delta
         build_tiles(false);
-        arows(false);
+        arows();
         if (tid == 0) tc::bulk_wait_read_all();  // the previous state copy has gone out
         __syncthreads();
-        t_solve();
-        master_copy(true);  // S as an operand, then S <- diag(gamma) S in TMEM
+        master_copy();  // S as an operand
         tc::fence_before_sync();
         __syncthreads();
         if (tid == 0) {
             tc::fence_after_sync();
 #pragma unroll 1
-            for (int p = 0; p < 3; ++p) {
-                const uint32_t ao = p == 2 ? ST_LO : 0u, bo = p == 1 ? R16_LO : 0u;
+            for (int p = 0; p < 2; ++p) {
 #pragma unroll
                 for (int ks = 0; ks < 8; ++ks)
-                    tc::mma_bf16(tm + TM_A, tile::desc_mn(sb + OFF_ST + ao, 16384, ks),
-                                 tile::desc_k(sb + OFF_AQK + bo, 16, ks), ID_MN_K16, (p | ks) != 0);
+                    tc::mma_bf16(tm + TM_A, tile::desc_mn(sb + OFF_ST + p * ST_LO, 16384, ks),
+                                 tile::desc_k(sb + OFF_AQK, 32, ks), ID_MN_K32, (p | ks) != 0);
             }
             tc::mma_commit(bar_mma);
+        }
+        master_decay();  // S <- diag(gamma) S in TMEM, and T, under the R products
+        t_solve();
+        wait_mma();
+        if (tid == 0) {  // the state copy is the chunk's checkpoint
             tc::bulk_store(a.ckpt + (bh * N + n) * KV, sm8 + OFF_ST, kStateBytes);
             tc::bulk_commit();
         }
-        wait_mma();
+        __syncthreads();  // T is published
         // R = V - Kg S and Delta = T diag(beta) R, value column v = tid on warps 0..3
         if (warp < 4) {
-            uint32_t r[16];
+            uint32_t r[16], r2[16];
             tc::tmem_ld16(tile::taddr(tm + TM_A, warp, 0), r);
+            tc::tmem_ld16(tile::taddr(tm + TM_A, warp, 16), r2);
             tc::tmem_ld_wait();
             float rr[BC];
 #pragma unroll
-            for (int t = 0; t < BC; ++t) rr[t] = Rv[t * VM + tid] - __uint_as_float(r[t]);
+            for (int t = 0; t < BC; ++t)
+                rr[t] = Rv[t * VM + tid] - (__uint_as_float(r[t]) + __uint_as_float(r2[t]));
 #pragma unroll
             for (int t = 0; t < BC; ++t) {
                 float acc = 0.f;
@@ -1154,29 +1171,36 @@ __global__ void __launch_bounds__(bwdtc::NT, 1) kda_chunk_bwd_tc_kernel(const Bw
             }
         }
         __syncthreads();
-        tile_rows(Dl, OFF_DLT, 16, R16_LO, 0);
-        {  // R and Delta for phase 2
-            float4* rdn = reinterpret_cast<float4*>(a.rd + (bh * N + n) * (size_t)(2 * BC * V));
+        tile_rows(Dl, OFF_DLT, 32, 16, 0);
+        {  // R, Delta, A', T and M for phase 2
+            float4* rdn = reinterpret_cast<float4*>(a.rd + (bh * N + n) * (size_t)RD);
             rdn[tid] = reinterpret_cast<const float4*>(Rv)[tid];
             rdn[NT + tid] = reinterpret_cast<const float4*>(Dl)[tid];
+            if (tid < 3 * BC * BC / 4) rdn[2 * NT + tid] = reinterpret_cast<const float4*>(Ap)[tid];
         }
         tc::fence_before_sync();
         __syncthreads();
-        if (tid == 0) {  // S += Kt^T Delta
+        if (tid == 0) {  // S += Kt^T Delta (K step 0 the hi rows, 1 the lo rows)
             tc::fence_after_sync();
 #pragma unroll
-            for (int p = 0; p < 3; ++p) {
-                const uint32_t ao = p == 2 ? R16_LO : 0u, bo = p == 1 ? R16_LO : 0u;
-                tc::mma_bf16(tm + TM_M, tile::desc_mn(sb + OFF_KT + ao, 2048, 0),
-                             tile::desc_mn(sb + OFF_DLT + bo, 2048, 0), ID_MN_MN128, 1u);
-            }
+            for (int p = 0; p < 4; ++p)
+                tc::mma_bf16(tm + TM_M, tile::desc_mn(sb + OFF_KT, 4096, p >> 1),
+                             tile::desc_mn(sb + OFF_DLT, 4096, p & 1), ID_MN_MN128, 1u);
             tc::mma_commit(bar_mma);
         }
     }
     if (N > 0 && !*s_fail) wait_mma();
-    if (tid == 0) tc::bulk_wait_all();  // every state copy is in global memory
-    prefetch_chunk(N - 1, true);
+    if (tid == 0) tc::bulk_wait_all();  // every checkpoint is in global memory
+    // R, Delta, A', T, M (generic stores) are read back by bulk copies, and the tiles phase 2
+    // fills by bulk copy were last written by generic stores
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+    tc::fence_proxy_async_smem();
     __syncthreads();
+    if (N > 0) {
+        request(N - 1, true);
+        request_rd(N - 1);
+        prefetch_state(N - 1);
+    }
 
     // ======================================================= phase 2: reverse
     master_init(a.dhT ? a.dhT + bh * KV : nullptr);
@@ -1186,28 +1210,25 @@ __global__ void __launch_bounds__(bwdtc::NT, 1) kda_chunk_bwd_tc_kernel(const Bw
     for (int n = N - 1; n >= 0 && !*s_fail; --n) {
         const int t0 = n * BC, cn = min(BC, T - t0);
         load_inputs(n, true);
-        prefetch_chunk(n - 1, true);
+        prefetch_state(n - 1);
         if (n < N - 1) wait_mma();  // the previous chunk's dS update has read its tiles
         build_tiles(true);
-        arows(true);
         __syncthreads();
-        t_solve();
-        master_copy(false);  // dS as an operand
+        master_copy();  // dS as an operand
         tc::fence_before_sync();
         __syncthreads();
-        if (tid == 0) {  // dDelta^T = dS^T Kt^T, dKt^T = dS Delta^T
+        if (tid == 128) {  // dDelta^T = dS^T Kt^T, dKt^T = dS Delta^T (warps 0..3 go on to M^T dO)
             tc::fence_after_sync();
 #pragma unroll 1
-            for (int p = 0; p < 3; ++p) {
-                const uint32_t ao = p == 2 ? ST_LO : 0u, bo = p == 1 ? R16_LO : 0u;
+            for (int p = 0; p < 2; ++p) {
 #pragma unroll
                 for (int ks = 0; ks < 8; ++ks)
-                    tc::mma_bf16(tm + TM_A, tile::desc_mn(sb + OFF_ST + ao, 16384, ks),
-                                 tile::desc_k(sb + OFF_KT + bo, 16, ks), ID_MN_K16, (p | ks) != 0);
+                    tc::mma_bf16(tm + TM_A, tile::desc_mn(sb + OFF_ST + p * ST_LO, 16384, ks),
+                                 tile::desc_k(sb + OFF_KT, 32, ks), ID_MN_K32, (p | ks) != 0);
 #pragma unroll
                 for (int ks = 0; ks < 8; ++ks)
-                    tc::mma_bf16(tm + TM_B, tile::desc_k(sb + OFF_ST + ao, 128, ks),
-                                 tile::desc_k(sb + OFF_DLT + bo, 16, ks), ID_K_K16, (p | ks) != 0);
+                    tc::mma_bf16(tm + TM_B, tile::desc_k(sb + OFF_ST + p * ST_LO, 128, ks),
+                                 tile::desc_k(sb + OFF_DLT, 32, ks), ID_K_K32, (p | ks) != 0);
             }
             tc::mma_commit(bar_mma);
         }
@@ -1228,12 +1249,13 @@ __global__ void __launch_bounds__(bwdtc::NT, 1) kda_chunk_bwd_tc_kernel(const Bw
             tc::bulk_load(sm8 + OFF_ST, a.ckpt + (bh * N + n) * KV, kStateBytes, bar_ld);
         }
         if (warp < 4) {  // dDelta, then dY = T^T dDelta
-            uint32_t r[16];
+            uint32_t r[16], r2[16];
             tc::tmem_ld16(tile::taddr(tm + TM_A, warp, 0), r);
+            tc::tmem_ld16(tile::taddr(tm + TM_A, warp, 16), r2);
             tc::tmem_ld_wait();
             float dd[BC];
 #pragma unroll
-            for (int t = 0; t < BC; ++t) dd[t] = __uint_as_float(r[t]) + mdo[t];
+            for (int t = 0; t < BC; ++t) dd[t] = (__uint_as_float(r[t]) + __uint_as_float(r2[t])) + mdo[t];
 #pragma unroll
             for (int i = 0; i < BC; ++i) {
                 float acc = 0.f;
@@ -1246,14 +1268,15 @@ __global__ void __launch_bounds__(bwdtc::NT, 1) kda_chunk_bwd_tc_kernel(const Bw
         float dG_r[4] = {0.f, 0.f, 0.f, 0.f};
         float dgl_part = 0.f;
         {  // dKt = Delta dS^T: channel col, tokens 4 qtr ..
-            uint32_t r[4];
+            uint32_t r[4], r2[4];
             tc::tmem_ld4(tile::taddr(tm + TM_B, warp, 4 * qtr), r);
+            tc::tmem_ld4(tile::taddr(tm + TM_B, warp, 16 + 4 * qtr), r2);
             tc::tmem_ld_wait();
             const float gl = Gc[ci(col, (BC - 1))];
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
                 const int t = 4 * qtr + u;
-                const float x = __uint_as_float(r[u]);
+                const float x = __uint_as_float(r[u]) + __uint_as_float(r2[u]);
                 const float eL = expf(gl - Gc[ci(col, t)]);
                 const float kk = Kr[ci(col, t)];
                 dk_r[u] += x * eL;
@@ -1262,7 +1285,7 @@ __global__ void __launch_bounds__(bwdtc::NT, 1) kda_chunk_bwd_tc_kernel(const Bw
             }
         }
         __syncthreads();
-        tile_rows(dY, OFF_DOY, 32, R32_LO, 16);
+        tile_rows(dY, OFF_DOY, 64, 32, 16);
         {  // the first part of dbeta_t, sum_v R_tv dY_tv (warp t), into the M slot (M is done)
             const int t = warp;
             float sr = 0.f;
@@ -1305,12 +1328,11 @@ __global__ void __launch_bounds__(bwdtc::NT, 1) kda_chunk_bwd_tc_kernel(const Bw
         if (tid == 0) {  // [dQg^T | P^T] = S [dO ; dY]^T
             tc::fence_after_sync();
 #pragma unroll 1
-            for (int p = 0; p < 3; ++p) {
-                const uint32_t ao = p == 2 ? ST_LO : 0u, bo = p == 1 ? R32_LO : 0u;
+            for (int p = 0; p < 2; ++p) {
 #pragma unroll
                 for (int ks = 0; ks < 8; ++ks)
-                    tc::mma_bf16(tm + TM_C, tile::desc_k(sb + OFF_ST + ao, 128, ks),
-                                 tile::desc_k(sb + OFF_DOY + bo, 32, ks), ID_K_K32, (p | ks) != 0);
+                    tc::mma_bf16(tm + TM_C, tile::desc_k(sb + OFF_ST + p * ST_LO, 128, ks),
+                                 tile::desc_k(sb + OFF_DOY, 64, ks), ID_K_K64, (p | ks) != 0);
             }
             tc::mma_commit(bar_mma);
         }
@@ -1352,65 +1374,88 @@ __global__ void __launch_bounds__(bwdtc::NT, 1) kda_chunk_bwd_tc_kernel(const Bw
         }
         wait_mma();
         {  // dQg = scale dO S^T and P = dY S^T, dKg = -diag(beta) P
-            uint32_t rx[4], ry[4];
+            uint32_t rx[4], ry[4], rx2[4], ry2[4];
             tc::tmem_ld4(tile::taddr(tm + TM_C, warp, 4 * qtr), rx);
             tc::tmem_ld4(tile::taddr(tm + TM_C, warp, 16 + 4 * qtr), ry);
+            tc::tmem_ld4(tile::taddr(tm + TM_C, warp, 32 + 4 * qtr), rx2);
+            tc::tmem_ld4(tile::taddr(tm + TM_C, warp, 48 + 4 * qtr), ry2);
             tc::tmem_ld_wait();
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
                 const int t = 4 * qtr + u;
                 const float Ga = expf(Gc[ci(col, t)]);
-                const float dqg = a.scale * __uint_as_float(rx[u]);
-                const float dkg = -bet[t] * __uint_as_float(ry[u]);
+                const float dqg = a.scale * (__uint_as_float(rx[u]) + __uint_as_float(rx2[u]));
+                const float dkg = -bet[t] * (__uint_as_float(ry[u]) + __uint_as_float(ry2[u]));
                 dq_r[u] += dqg * Ga;
                 dk_r[u] += dkg * Ga;
                 dG_r[u] += (dqg * Qr[ci(col, t)] + dkg * Kr[ci(col, t)]) * Ga;
             }
         }
+        tc::fence_proxy_async_smem();  // R, Delta, A', T, M are done: the next chunk's may land
         tc::fence_before_sync();
         __syncthreads();
-        if (tid == 0) {  // dS += [scale Qg ; -beta Kg]^T [dO ; dY]
+        if (n > 0) request_rd(n - 1);
+        if (tid == 0) {  // dS += [scale Qg ; -beta Kg]^T [dO ; dY] (K steps 0, 1 hi; 2, 3 lo)
             tc::fence_after_sync();
 #pragma unroll
-            for (int p = 0; p < 3; ++p) {
-                const uint32_t ao = p == 2 ? R32_LO : 0u, bo = p == 1 ? R32_LO : 0u;
+            for (int p = 0; p < 4; ++p) {
 #pragma unroll
                 for (int ks = 0; ks < 2; ++ks)
-                    tc::mma_bf16(tm + TM_M, tile::desc_mn(sb + OFF_AQK + ao, 4096, ks),
-                                 tile::desc_mn(sb + OFF_DOY + bo, 4096, ks), ID_MN_MN128, 1u);
+                    tc::mma_bf16(tm + TM_M, tile::desc_mn(sb + OFF_AQK, 8192, 2 * (p >> 1) + ks),
+                                 tile::desc_mn(sb + OFF_DOY, 8192, 2 * (p & 1) + ks), ID_MN_MN128, 1u);
             }
             tc::mma_commit(bar_mma);
         }
-        // pairwise terms of dA' = diag(beta) dB and dM, thread (c = col, tokens 4 qtr + r)
+        // pairwise terms of dA' = diag(beta) dB and dM, each pair's decay E = e^{G_s - G_t} (t < s)
+        // taken once: thread (c = col) takes the rows s in {qtr, 7 - qtr, 8 + qtr, 15 - qtr} (30
+        // pairs below the diagonal each) and sums the row terms of s and the column terms of every
+        // t <= s; the sums meet in the state-copy region (free until the next chunk's copy)
+        float* colP = reinterpret_cast<float*>(sm8 + OFF_ST);  // [4][BC][KM]
+        float* rowP = colP + 4 * BC * KM;                       // [BC][2][KM]
         {
             const int c = col;
+            float colS[BC];
 #pragma unroll
-            for (int r = 0; r < 4; ++r) {
-                const int t = 4 * qtr + r;
-                const float gt = Gc[ci(c, t)], kt = Kr[ci(c, t)], qt = Qr[ci(c, t)];
-                float rowA = 0.f, rowM = 0.f, colA = 0.f, colM = 0.f;
+            for (int t = 0; t < BC; ++t) colS[t] = 0.f;
 #pragma unroll
-                for (int i = 0; i < BC; ++i) {
-                    if (i <= t) {
-                        const float kiE = Kr[ci(c, i)] * __expf(gt - Gc[ci(c, i)]);
-                        rowM = fmaf(dM[t * BC + i], kiE, rowM);
-                        rowA = fmaf(bet[t] * dB[t * BC + i], kiE, rowA);
+            for (int u = 0; u < 4; ++u) {
+                const int s = u == 0 ? qtr : u == 1 ? 7 - qtr : u == 2 ? 8 + qtr : 15 - qtr;
+                const float gs = Gc[ci(c, s)], ks = Kr[ci(c, s)], qs = Qr[ci(c, s)], bs = bet[s];
+                const float dMd = dM[s * BC + s];
+                float rM = dMd * ks, rA = 0.f;  // the diagonal pair (E = 1, dB[s][s] = 0)
+#pragma unroll
+                for (int t = 0; t < BC; ++t) {
+                    if (t < s) {
+                        const float E = __expf(gs - Gc[ci(c, t)]);
+                        const float kt = Kr[ci(c, t)];
+                        const float w = dM[s * BC + t] * E, x = bs * dB[s * BC + t] * E;
+                        rM = fmaf(w, kt, rM);
+                        rA = fmaf(x, kt, rA);
+                        colS[t] = fmaf(w, qs, fmaf(x, ks, colS[t]));
+                    } else if (t == s) {
+                        colS[t] = fmaf(dMd, qs, colS[t]);
                     }
                 }
-#pragma unroll
-                for (int s2 = 0; s2 < BC; ++s2) {
-                    if (s2 >= t) {
-                        const float E = __expf(Gc[ci(c, s2)] - gt);
-                        colM = fmaf(dM[s2 * BC + t], Qr[ci(c, s2)] * E, colM);
-                        colA = fmaf(bet[s2] * dB[s2 * BC + t], Kr[ci(c, s2)] * E, colA);
-                    }
-                }
-                dq_r[r] += rowM;
-                dk_r[r] += rowA + colA + colM;
-                dG_r[r] += kt * rowA + qt * rowM - kt * (colA + colM);
+                rowP[(2 * s) * KM + c] = rM;
+                rowP[(2 * s + 1) * KM + c] = rA;
             }
+#pragma unroll
+            for (int t = 0; t < BC; ++t) colP[(qtr * BC + t) * KM + c] = colS[t];
         }
         __syncthreads();
+        // this thread's tokens t = 4 qtr + r: dq += rowM, dk += rowA + col, dG += k rowA + q rowM
+        // - k col (col = the column terms of dM and dA', summed over the four row owners)
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            const int t = 4 * qtr + r;
+            const float kt = Kr[ci(col, t)], qt = Qr[ci(col, t)];
+            const float cs = (colP[t * KM + col] + colP[(BC + t) * KM + col]) +
+                             (colP[(2 * BC + t) * KM + col] + colP[(3 * BC + t) * KM + col]);
+            const float rM = rowP[(2 * t) * KM + col], rA = rowP[(2 * t + 1) * KM + col];
+            dq_r[r] += rM;
+            dk_r[r] += rA + cs;
+            dG_r[r] += kt * rA + qt * rM - kt * cs;
+        }
         // dG exchange ([BC][KM] in XT), the last token's share of d(G_last), reverse cumsum,
         // gate derivative; dq and dk out
 #pragma unroll
@@ -1422,22 +1467,16 @@ __global__ void __launch_bounds__(bwdtc::NT, 1) kda_chunk_bwd_tc_kernel(const Bw
             const float dgl = red[c] + red[KM + c] + red[2 * KM + c] + red[3 * KM + c];
             float suffix = dgl;
             for (int t = BC - 1; t > 4 * qtr + 3; --t) suffix += XT[t * KM + c];
-            const float dtc = a.dt_bias[(size_t)h * K + c];
-            float zr[4];
-#pragma unroll
-            for (int r = 0; r < 4; ++r) {
-                const int t = 4 * qtr + r;
-                zr[r] = t < cn ? ld_io(a.z + ((bh * T) + t0 + t) * K + c) : 0.f;
-            }
 #pragma unroll
             for (int r = 3; r >= 0; --r) {
                 const int t = 4 * qtr + r;
                 suffix += XT[t * KM + c];
                 if (t < cn) {
                     const size_t gi = ((bh * T) + t0 + t) * K + c;
-                    const float x = zr[r] + dtc;
-                    const float g = -(eA * softplus_f32(x));
-                    const float dz = suffix * (-eA) * sigmoid_f32(x);
+                    // g = -e^{A_log} softplus(x) with x = z + dt_bias, and sigmoid(x) =
+                    // 1 - e^{-softplus(x)} = -expm1(g e^{-A_log})
+                    const float g = Gt[ci(c, t)];
+                    const float dz = suffix * (-eA) * -expm1f(g * ieA);
                     a.dz[gi] = dz;
                     ddt_acc += dz;
                     dA_acc = fmaf(suffix, g, dA_acc);
@@ -1503,7 +1542,8 @@ cudaError_t launch_chunk_backward(const BwdLaunch& L, cudaStream_t s) {
     const int N = (T + BC - 1) / BC;
     const size_t BH = (size_t)B * H;
     const size_t ck_bytes = sizeof(float) * BH * (size_t)N * K * V;
-    const size_t rd_bytes = sizeof(float) * BH * (size_t)N * 2 * BC * V;
+    const bool fixed = K == 128 && V == 128;
+    const size_t rd_bytes = sizeof(float) * BH * (size_t)N * (fixed ? (size_t)bwdtc::RD : (size_t)(2 * BC * V));
     const size_t part_bytes = sizeof(float) * BH * (size_t)(1 + K);
     char* scratch = nullptr;
     cudaError_t e = cudaMallocAsync(reinterpret_cast<void**>(&scratch),
@@ -1542,15 +1582,14 @@ cudaError_t launch_chunk_backward(const BwdLaunch& L, cudaStream_t s) {
         a.A_log = L.A_log; a.dt_bias = L.dt_bias; a.h0 = L.h0; a.dhT = L.dhT; a.scale = L.scale;
         a.dq = L.dq; a.dk = L.dk; a.dv = L.dv; a.dz = L.dz; a.dbeta = L.dbeta; a.dh0 = L.dh0;
         a.ckpt = ckpt; a.rd = rd; a.dA_part = dA_part; a.ddt_part = ddt_part;
+        constexpr size_t smem = bwdtc::smem_bytes<IO>();
         cudaError_t err = cudaFuncSetAttribute(kda_chunk_bwd_tc_kernel<IO>,
-                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               (int)bwdtc::SMEM_BYTES);
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (err != cudaSuccess) return err;
-        kda_chunk_bwd_tc_kernel<IO><<<(unsigned)BH, bwdtc::NT, bwdtc::SMEM_BYTES, s>>>(a);
+        kda_chunk_bwd_tc_kernel<IO><<<(unsigned)BH, bwdtc::NT, smem, s>>>(a);
         return cudaGetLastError();
     };
     using Any = std::integral_constant<int, 0>;
-    const bool fixed = K == 128 && V == 128;
     if (L.io == KDA_BF16)
         e = fixed ? run_tc(__nv_bfloat16{}) : run(__nv_bfloat16{}, Any{});
     else
