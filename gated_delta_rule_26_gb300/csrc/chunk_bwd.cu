@@ -971,31 +971,34 @@ __global__ void __launch_bounds__(bwdtc::NT, 1) kda_chunk_bwd_tc_kernel(const Bw
         const IO* sk = sq + BC * K;
         const IO* sz = sk + BC * K;
         const IO* sv = sz + BC * K;
+        float run[4];  // this thread's tokens 4 qtr + r: prefix sums of g within the four
 #pragma unroll
-        for (int r = 0; r < BC * KM / NT; ++r) {
-            const int idx = tid + r * NT, t = idx >> 7;  // column col
+        for (int r = 0; r < 4; ++r) {
+            const int t = 4 * qtr + r, idx = t * K + col;
             const bool in = t < cn;
             const float g = in ? kda_log_decay(ld_io(sz + idx), dtc, eA) : 0.f;
             Kr[ci(col, t)] = in ? ld_io(sk + idx) : 0.f;
             Qr[ci(col, t)] = in ? ld_io(sq + idx) : 0.f;
-            Gc[ci(col, t)] = g;
             Gt[ci(col, t)] = g;
+            run[r] = r ? run[r - 1] + g : g;
             const float x = in ? ld_io(sv + idx) : 0.f;
             if (full) dO[idx] = x;
             else Rv[idx] = x;
         }
+        red[qtr * KM + col] = run[3];
         if (tid < BC) bet[tid] = bnext;
         tc::fence_proxy_async_smem();
         __syncthreads();
         const int nx = full ? n - 1 : n + 1;
         if (nx >= 0 && nx < N) request(nx, full);
-        if (tid < K) {
-            float run = 0.f;
-            for (int t = 0; t < BC; ++t) {
-                run += Gc[ci(tid, t)];
-                Gc[ci(tid, t)] = run;
-            }
-            gam[tid] = expf(run);
+        {  // G = the in-chunk cumulative sum: the earlier quarters' totals, then the prefix
+            float off = 0.f;
+#pragma unroll
+            for (int q2 = 0; q2 < 3; ++q2)
+                if (q2 < qtr) off += red[q2 * KM + col];
+#pragma unroll
+            for (int r = 0; r < 4; ++r) Gc[ci(col, 4 * qtr + r)] = off + run[r];
+            if (qtr == 3) gam[col] = expf(off + run[3]);
         }
         __syncthreads();
     };
@@ -1009,8 +1012,8 @@ __global__ void __launch_bounds__(bwdtc::NT, 1) kda_chunk_bwd_tc_kernel(const Bw
             for (int j = 0; j < 8; ++j) {
                 const int c = c0 + j;
                 const float g = Gc[ci(c, t)], gl = Gc[ci(c, BC - 1)], kk = Kr[ci(c, t)];
-                const float eg = expf(g);
-                kt[j] = kk * expf(gl - g);
+                const float eg = __expf(g);
+                kt[j] = kk * __expf(gl - g);
                 kg[j] = kk * eg;
                 qg[j] = full ? Qr[ci(c, t)] * eg : 0.f;
             }
@@ -1213,6 +1216,7 @@ __global__ void __launch_bounds__(bwdtc::NT, 1) kda_chunk_bwd_tc_kernel(const Bw
         prefetch_state(n - 1);
         if (n < N - 1) wait_mma();  // the previous chunk's dS update has read its tiles
         build_tiles(true);
+        if (tid == 0) tc::bulk_wait_read_all();  // the previous chunk's dq, dk, dz have left
         __syncthreads();
         master_copy();  // dS as an operand
         tc::fence_before_sync();
@@ -1368,10 +1372,7 @@ __global__ void __launch_bounds__(bwdtc::NT, 1) kda_chunk_bwd_tc_kernel(const Bw
             for (int i = 0; i < t; ++i) s = fmaf(Ap[t * BC + i], dB[t * BC + i], s);
             a.dbeta[bh * T + t0 + t] = s;
         }
-        for (int idx = tid; idx < cn * V; idx += NT) {
-            const int t = idx / V, vv = idx - t * V;
-            a.dv[((bh * T) + t0 + t) * V + vv] = bet[t] * dY[t * VM + vv];
-        }
+        for (int idx = tid; idx < BC * V; idx += NT) XT[idx] = bet[idx >> 7] * dY[idx];  // dV, staged
         wait_mma();
         {  // dQg = scale dO S^T and P = dY S^T, dKg = -diag(beta) P
             uint32_t rx[4], ry[4], rx2[4], ry2[4];
@@ -1395,6 +1396,10 @@ __global__ void __launch_bounds__(bwdtc::NT, 1) kda_chunk_bwd_tc_kernel(const Bw
         tc::fence_before_sync();
         __syncthreads();
         if (n > 0) request_rd(n - 1);
+        if (tid == 0) {
+            tc::bulk_store(a.dv + (bh * T + t0) * (size_t)V, XT, (uint32_t)(cn * V * 4));
+            tc::bulk_commit();
+        }
         if (tid == 0) {  // dS += [scale Qg ; -beta Kg]^T [dO ; dY] (K steps 0, 1 hi; 2, 3 lo)
             tc::fence_after_sync();
 #pragma unroll
@@ -1442,6 +1447,7 @@ __global__ void __launch_bounds__(bwdtc::NT, 1) kda_chunk_bwd_tc_kernel(const Bw
 #pragma unroll
             for (int t = 0; t < BC; ++t) colP[(qtr * BC + t) * KM + c] = colS[t];
         }
+        if (tid == 0) tc::bulk_wait_read_all();  // dV has left XT
         __syncthreads();
         // this thread's tokens t = 4 qtr + r: dq += rowM, dk += rowA + col, dG += k rowA + q rowM
         // - k col (col = the column terms of dM and dA', summed over the four row owners)
@@ -1462,6 +1468,7 @@ __global__ void __launch_bounds__(bwdtc::NT, 1) kda_chunk_bwd_tc_kernel(const Bw
         for (int r = 0; r < 4; ++r) XT[(4 * qtr + r) * KM + col] = dG_r[r];
         red[qtr * KM + col] += dgl_part;
         __syncthreads();
+        float* ost = reinterpret_cast<float*>(sm8 + OFF_ST);  // dq, dk, dz [BC][KM] each, staged
         {
             const int c = col;
             const float dgl = red[c] + red[KM + c] + red[2 * KM + c] + red[3 * KM + c];
@@ -1472,22 +1479,31 @@ __global__ void __launch_bounds__(bwdtc::NT, 1) kda_chunk_bwd_tc_kernel(const Bw
                 const int t = 4 * qtr + r;
                 suffix += XT[t * KM + c];
                 if (t < cn) {
-                    const size_t gi = ((bh * T) + t0 + t) * K + c;
                     // g = -e^{A_log} softplus(x) with x = z + dt_bias, and sigmoid(x) =
                     // 1 - e^{-softplus(x)} = -expm1(g e^{-A_log})
                     const float g = Gt[ci(c, t)];
                     const float dz = suffix * (-eA) * -expm1f(g * ieA);
-                    a.dz[gi] = dz;
+                    ost[t * KM + c] = dq_r[r];
+                    ost[(BC + t) * KM + c] = dk_r[r];
+                    ost[(2 * BC + t) * KM + c] = dz;
                     ddt_acc += dz;
                     dA_acc = fmaf(suffix, g, dA_acc);
-                    a.dq[gi] = dq_r[r];
-                    a.dk[gi] = dk_r[r];
                 }
             }
         }
+        tc::fence_proxy_async_smem();
         __syncthreads();
+        if (tid == 0) {
+            const size_t g0 = (bh * T + t0) * (size_t)K;
+            const uint32_t bytes = (uint32_t)(cn * K * 4);
+            tc::bulk_store(a.dq + g0, ost, bytes);
+            tc::bulk_store(a.dk + g0, ost + BC * KM, bytes);
+            tc::bulk_store(a.dz + g0, ost + 2 * BC * KM, bytes);
+            tc::bulk_commit();
+        }
     }
     if (N > 0 && !*s_fail) wait_mma();  // the last dS update
+    if (tid == 0) tc::bulk_wait_all();  // the gradients are in global memory
 
     // ---- dh0, and the per-(b, h) partial sums of dA_log and ddt_bias
     if (a.dh0) {
