@@ -755,8 +755,9 @@ constexpr uint32_t ST_LO = 32768;              //   lo
 constexpr uint32_t OFF_KT = 65536;             // Kt [t][c]: 32 rows (hi 0..15, lo 16..31)
 constexpr uint32_t OFF_DLT = OFF_KT + 8192;    // Delta [t][v]: 32 rows
 constexpr uint32_t OFF_DOY = OFF_DLT + 8192;   // [dO ; dY] [t'][v]: 64 rows (hi 0..31, lo 32..63)
-constexpr uint32_t OFF_AQK = OFF_DOY + 16384;  // phase 2 [scale Qg ; -beta Kg] [t'][c]: 64 rows;
-                                               // phase 1 Kg [t][c]: 32 rows
+constexpr uint32_t OFF_AQK = OFF_DOY + 16384;  // phase 2 [scale Qg ; -beta Kg] [t'][c]: 64 rows
+                                               // (until the first products: scale M^T [t][s], 32
+                                               // rows); phase 1 Kg [t][c]: 32 rows
 constexpr uint32_t OFF_F = OFF_AQK + 16384;    // fp32 area (float offsets below)
 // R, Delta, A', T, M are contiguous: phase 2 brings them back with one bulk copy
 constexpr int F_Q = 0, F_K = F_Q + KM * GP, F_G = F_K + KM * GP;
@@ -1003,8 +1004,9 @@ __global__ void __launch_bounds__(bwdtc::NT, 1) kda_chunk_bwd_tc_kernel(const Bw
         __syncthreads();
     };
     // The decay-scaled operand tiles of the chunk (hi, lo): Kt = K e^{G_last - G} always;
-    // phase 1 Kg = K e^G; phase 2 [scale Qg ; -beta Kg], Delta and the dO half of [dO ; dY].
-    auto build_tiles = [&](bool full) {
+    // phase 1 Kg = K e^G; phase 2 (with aqk) [scale Qg ; -beta Kg], else Delta, the dO half of
+    // [dO ; dY] and scale M^T (B[t][s] = scale M[s][t], where [scale Qg ; -beta Kg] goes later).
+    auto build_tiles = [&](bool full, bool aqk) {
         if (tid < 256) {
             const int t = tid & 15, c0 = 8 * (tid >> 4);
             float kt[8], kg[8], qg[8];
@@ -1018,10 +1020,22 @@ __global__ void __launch_bounds__(bwdtc::NT, 1) kda_chunk_bwd_tc_kernel(const Bw
                 qg[j] = full ? Qr[ci(c, t)] * eg : 0.f;
             }
             uint4 hi, lo;
-            split8(kt, hi, lo);
-            *reinterpret_cast<uint4*>(sm8 + OFF_KT + tile::kmaj_off(t, c0, 32)) = hi;
-            *reinterpret_cast<uint4*>(sm8 + OFF_KT + tile::kmaj_off(16 + t, c0, 32)) = lo;
-            if (!full) {
+            if (!aqk) {
+                split8(kt, hi, lo);
+                *reinterpret_cast<uint4*>(sm8 + OFF_KT + tile::kmaj_off(t, c0, 32)) = hi;
+                *reinterpret_cast<uint4*>(sm8 + OFF_KT + tile::kmaj_off(16 + t, c0, 32)) = lo;
+            }
+            if (full && !aqk) {
+                if (tid < 32) {  // scale M^T: row t = tid & 15, columns s = 8 (tid >> 4) ..
+                    const int s0 = 8 * (tid >> 4);
+                    float m[8];
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) m[j] = a.scale * Mm[(s0 + j) * BC + t];
+                    split8(m, hi, lo);
+                    *reinterpret_cast<uint4*>(sm8 + OFF_AQK + tile::kmaj_off(t, s0, 32)) = hi;
+                    *reinterpret_cast<uint4*>(sm8 + OFF_AQK + tile::kmaj_off(16 + t, s0, 32)) = lo;
+                }
+            } else if (!full) {
                 split8(kg, hi, lo);
                 *reinterpret_cast<uint4*>(sm8 + OFF_AQK + tile::kmaj_off(t, c0, 32)) = hi;
                 *reinterpret_cast<uint4*>(sm8 + OFF_AQK + tile::kmaj_off(16 + t, c0, 32)) = lo;
@@ -1039,7 +1053,7 @@ __global__ void __launch_bounds__(bwdtc::NT, 1) kda_chunk_bwd_tc_kernel(const Bw
                 *reinterpret_cast<uint4*>(sm8 + OFF_AQK + tile::kmaj_off(16 + t, c0, 64)) = hi;
                 *reinterpret_cast<uint4*>(sm8 + OFF_AQK + tile::kmaj_off(48 + t, c0, 64)) = lo;
             }
-        } else if (full) {
+        } else if (full && !aqk) {
             const int i = tid - 256, t = i & 15, v0 = 8 * (i >> 4);
             float d[8], o[8];
             const float4 d0 = *reinterpret_cast<const float4*>(Dl + t * VM + v0);
@@ -1128,7 +1142,7 @@ __global__ void __launch_bounds__(bwdtc::NT, 1) kda_chunk_bwd_tc_kernel(const Bw
     for (int n = 0; n < N && !*s_fail; ++n) {
         load_inputs(n, false);
         if (n > 0) wait_mma();  // the previous chunk's state update has read Kt and Delta
-        build_tiles(false);
+        build_tiles(false, false);
         arows();
         if (tid == 0) tc::bulk_wait_read_all();  // the previous state copy has gone out
         __syncthreads();
@@ -1215,13 +1229,13 @@ __global__ void __launch_bounds__(bwdtc::NT, 1) kda_chunk_bwd_tc_kernel(const Bw
         load_inputs(n, true);
         prefetch_state(n - 1);
         if (n < N - 1) wait_mma();  // the previous chunk's dS update has read its tiles
-        build_tiles(true);
+        build_tiles(true, false);
         if (tid == 0) tc::bulk_wait_read_all();  // the previous chunk's dq, dk, dz have left
         __syncthreads();
         master_copy();  // dS as an operand
         tc::fence_before_sync();
         __syncthreads();
-        if (tid == 128) {  // dDelta^T = dS^T Kt^T, dKt^T = dS Delta^T (warps 0..3 go on to M^T dO)
+        if (tid == 128) {  // dDelta^T = dS^T Kt^T + dO^T (scale M), dKt^T = dS Delta^T
             tc::fence_after_sync();
 #pragma unroll 1
             for (int p = 0; p < 2; ++p) {
@@ -1233,19 +1247,11 @@ __global__ void __launch_bounds__(bwdtc::NT, 1) kda_chunk_bwd_tc_kernel(const Bw
                 for (int ks = 0; ks < 8; ++ks)
                     tc::mma_bf16(tm + TM_B, tile::desc_k(sb + OFF_ST + p * ST_LO, 128, ks),
                                  tile::desc_k(sb + OFF_DLT, 32, ks), ID_K_K32, (p | ks) != 0);
+                // A = dO^T (rows 0..15 hi, 32..47 lo of [dO ; dY] read MN-major), B = scale M^T
+                tc::mma_bf16(tm + TM_A, tile::desc_mn(sb + OFF_DOY, 8192, 2 * p),
+                             tile::desc_k(sb + OFF_AQK, 32, 0), ID_MN_K32, 1u);
             }
             tc::mma_commit(bar_mma);
-        }
-        // scale M^T dO, value column v = tid on warps 0..3
-        float mdo[BC];
-        if (warp < 4) {
-#pragma unroll
-            for (int t = 0; t < BC; ++t) {
-                float m = 0.f;
-#pragma unroll
-                for (int s2 = t; s2 < BC; ++s2) m = fmaf(Mm[s2 * BC + t], dO[s2 * VM + tid], m);
-                mdo[t] = a.scale * m;
-            }
         }
         wait_mma();
         if (tid == 0) {  // the state entering this chunk, as phase 1 kept it
@@ -1259,7 +1265,7 @@ __global__ void __launch_bounds__(bwdtc::NT, 1) kda_chunk_bwd_tc_kernel(const Bw
             tc::tmem_ld_wait();
             float dd[BC];
 #pragma unroll
-            for (int t = 0; t < BC; ++t) dd[t] = (__uint_as_float(r[t]) + __uint_as_float(r2[t])) + mdo[t];
+            for (int t = 0; t < BC; ++t) dd[t] = __uint_as_float(r[t]) + __uint_as_float(r2[t]);
 #pragma unroll
             for (int i = 0; i < BC; ++i) {
                 float acc = 0.f;
@@ -1288,6 +1294,7 @@ __global__ void __launch_bounds__(bwdtc::NT, 1) kda_chunk_bwd_tc_kernel(const Bw
                 dgl_part += x * kk * eL;
             }
         }
+        build_tiles(true, true);  // scale M^T has been read
         __syncthreads();
         tile_rows(dY, OFF_DOY, 64, 32, 16);
         {  // the first part of dbeta_t, sum_v R_tv dY_tv (warp t), into the M slot (M is done)
@@ -1297,34 +1304,6 @@ __global__ void __launch_bounds__(bwdtc::NT, 1) kda_chunk_bwd_tc_kernel(const Bw
 #pragma unroll
             for (int off = 16; off > 0; off >>= 1) sr += __shfl_xor_sync(0xffffffffu, sr, off);
             if (lane == 0) Mm[t] = sr;
-        }
-        {  // dM (i <= t) and dB (i < t): warp t, lanes over value columns, reduced together
-            const int t = warp;
-            float ot[4], yt[4];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int vv = lane + 32 * u;
-                ot[u] = dO[t * VM + vv];
-                yt[u] = dY[t * VM + vv];
-            }
-            float w[32];
-#pragma unroll
-            for (int i = 0; i < BC; ++i) {
-                float sm_ = 0.f, sbb = 0.f;
-                if (i <= t) {
-#pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        const float dl = Dl[i * VM + lane + 32 * u];
-                        sm_ = fmaf(ot[u], dl, sm_);
-                        sbb = fmaf(yt[u], dl, sbb);
-                    }
-                }
-                w[i] = sm_;
-                w[BC + i] = sbb;
-            }
-            warp_reduce_scatter32(w, lane);
-            if (lane < BC) dM[t * BC + lane] = lane <= t ? a.scale * w[0] : 0.f;
-            else dB[t * BC + lane - BC] = lane - BC < t ? -w[0] : 0.f;
         }
         tc::fence_before_sync();
         __syncthreads();
@@ -1338,6 +1317,11 @@ __global__ void __launch_bounds__(bwdtc::NT, 1) kda_chunk_bwd_tc_kernel(const Bw
                     tc::mma_bf16(tm + TM_C, tile::desc_k(sb + OFF_ST + p * ST_LO, 128, ks),
                                  tile::desc_k(sb + OFF_DOY, 64, ks), ID_K_K64, (p | ks) != 0);
             }
+            // [dO ; dY] Delta^T (rows 0..63 of D; the M = 128 read's rows 64..127 are ignored)
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks)
+                tc::mma_bf16(tm + TM_B, tile::desc_k(sb + OFF_DOY, 64, ks),
+                             tile::desc_k(sb + OFF_DLT, 32, ks), ID_K_K32, ks != 0);
             tc::mma_commit(bar_mma);
         }
         {  // dgamma_c partial over the value quarter qtr (times gamma_c), then dS <- gamma dS
@@ -1365,15 +1349,39 @@ __global__ void __launch_bounds__(bwdtc::NT, 1) kda_chunk_bwd_tc_kernel(const Bw
             }
             master_st(r0, r1);
         }
-        // dbeta_t = sum_v R_tv dY_tv + sum_{i<t} A'_ti dB_ti;  dV = diag(beta) dY
-        if (tid < cn) {
-            const int t = tid;
-            float s = Mm[t];
-            for (int i = 0; i < t; ++i) s = fmaf(Ap[t * BC + i], dB[t * BC + i], s);
-            a.dbeta[bh * T + t0 + t] = s;
-        }
+        // dV = diag(beta) dY
         for (int idx = tid; idx < BC * V; idx += NT) XT[idx] = bet[idx >> 7] * dY[idx];  // dV, staged
         wait_mma();
+        if (warp < 2) {  // dM = scale dO Delta^T (i <= t), dB = -dY Delta^T (i < t): rows of D
+            uint32_t r0[16], r1[16];
+            tc::tmem_ld16(tile::taddr(tm + TM_B, warp, 0), r0);
+            tc::tmem_ld16(tile::taddr(tm + TM_B, warp, 16), r1);
+            tc::tmem_ld_wait();
+            float x[BC];
+#pragma unroll
+            for (int i = 0; i < BC; ++i) x[i] = __uint_as_float(r0[i]) + __uint_as_float(r1[i]);
+            float* dst = lane < 16 ? dM + lane * BC : dB + (lane - 16) * BC;
+            if (warp == 1) {  // the lo rows' share
+#pragma unroll
+                for (int i = 0; i < BC; ++i) dst[i] = x[i];
+            }
+            tc::named_sync(1, 64);
+            if (warp == 0) {
+                const int t = lane & 15;
+#pragma unroll
+                for (int i = 0; i < BC; ++i) {
+                    const float v = x[i] + dst[i];
+                    dst[i] = lane < 16 ? (i <= t ? a.scale * v : 0.f) : (i < t ? -v : 0.f);
+                }
+                __syncwarp();
+                // dbeta_t = sum_v R_tv dY_tv + sum_{i<t} A'_ti dB_ti
+                if (lane < cn) {
+                    float sb2 = Mm[lane];
+                    for (int i = 0; i < lane; ++i) sb2 = fmaf(Ap[lane * BC + i], dB[lane * BC + i], sb2);
+                    a.dbeta[bh * T + t0 + lane] = sb2;
+                }
+            }
+        }
         {  // dQg = scale dO S^T and P = dY S^T, dKg = -diag(beta) P
             uint32_t rx[4], ry[4], rx2[4], ry2[4];
             tc::tmem_ld4(tile::taddr(tm + TM_C, warp, 4 * qtr), rx);
