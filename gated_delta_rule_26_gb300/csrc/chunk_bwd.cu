@@ -1142,11 +1142,11 @@ __global__ void __launch_bounds__(bwdtc::NT, 1) kda_chunk_bwd_tc_kernel(const Bw
     for (int n = 0; n < N && !*s_fail; ++n) {
         load_inputs(n, false);
         if (n > 0) wait_mma();  // the previous chunk's state update has read Kt and Delta
-        build_tiles(false, false);
-        arows();
         if (tid == 0) tc::bulk_wait_read_all();  // the previous state copy has gone out
         __syncthreads();
         master_copy();  // S as an operand
+        build_tiles(false, false);
+        arows();
         tc::fence_before_sync();
         __syncthreads();
         if (tid == 0) {
@@ -1163,10 +1163,6 @@ __global__ void __launch_bounds__(bwdtc::NT, 1) kda_chunk_bwd_tc_kernel(const Bw
         master_decay();  // S <- diag(gamma) S in TMEM, and T, under the R products
         t_solve();
         wait_mma();
-        if (tid == 0) {  // the state copy is the chunk's checkpoint
-            tc::bulk_store(a.ckpt + (bh * N + n) * KV, sm8 + OFF_ST, kStateBytes);
-            tc::bulk_commit();
-        }
         __syncthreads();  // T is published
         // R = V - Kg S and Delta = T diag(beta) R, value column v = tid on warps 0..3
         if (warp < 4) {
@@ -1187,14 +1183,14 @@ __global__ void __launch_bounds__(bwdtc::NT, 1) kda_chunk_bwd_tc_kernel(const Bw
                 Dl[t * VM + tid] = acc;
             }
         }
+        tc::fence_proxy_async_smem();
         __syncthreads();
-        tile_rows(Dl, OFF_DLT, 32, 16, 0);
-        {  // R, Delta, A', T and M for phase 2
-            float4* rdn = reinterpret_cast<float4*>(a.rd + (bh * N + n) * (size_t)RD);
-            rdn[tid] = reinterpret_cast<const float4*>(Rv)[tid];
-            rdn[NT + tid] = reinterpret_cast<const float4*>(Dl)[tid];
-            if (tid < 3 * BC * BC / 4) rdn[2 * NT + tid] = reinterpret_cast<const float4*>(Ap)[tid];
+        if (tid == 0) {  // R, Delta, A', T and M (contiguous) for phase 2
+            tc::bulk_store(a.rd + (bh * N + n) * (size_t)RD, Rv, RD * 4);
+            tc::bulk_commit();
         }
+        tile_rows(Dl, OFF_DLT, 32, 16, 0);
+        if (tid == 0) tc::bulk_wait_read_all();  // before the next chunk's v lands in R
         tc::fence_before_sync();
         __syncthreads();
         if (tid == 0) {  // S += Kt^T Delta (K step 0 the hi rows, 1 the lo rows)
@@ -1204,6 +1200,9 @@ __global__ void __launch_bounds__(bwdtc::NT, 1) kda_chunk_bwd_tc_kernel(const Bw
                 tc::mma_bf16(tm + TM_M, tile::desc_mn(sb + OFF_KT, 4096, p >> 1),
                              tile::desc_mn(sb + OFF_DLT, 4096, p & 1), ID_MN_MN128, 1u);
             tc::mma_commit(bar_mma);
+            // the state copy is the chunk's checkpoint
+            tc::bulk_store(a.ckpt + (bh * N + n) * KV, sm8 + OFF_ST, kStateBytes);
+            tc::bulk_commit();
         }
     }
     if (N > 0 && !*s_fail) wait_mma();
