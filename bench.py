@@ -375,16 +375,28 @@ def run_backward(args, kda, inputs, peaks, ws, barrier):
     C = 16
     flops = B * H * T * bwd_flops_per_token_head(C, K, V)
     achieved = flops / per / 1e12
-    peak = fp32_peak_tflops()
+    tensor = K == 128 and V == 128  # the tensor-core form; other shapes run on the CUDA cores
+    if tensor:
+        # the contractions with the state (12KV of the count) are tcgen05 products, each as the
+        # four bf16 products of hi/lo operand halves; the rest runs on the CUDA cores
+        roof = {"bound": "tensor", "peak": peaks["bf16_tflops"],
+                "peak_source": f"bf16 dense, {peaks['source']} (burst)",
+                "kernel": "kda_chunk_bwd_tc_kernel (+ the batch sum of dA_log, ddt_bias)",
+                "tensor_products_per_state_product": 4,
+                "fp32_cuda_core_frac": achieved / fp32_peak_tflops(),
+                "traffic": measured_traffic("kda_chunk_bwd_tc_kernel",
+                                            ("chunk_bwd.cu", "chunk_tiles.cuh", "tc_ptx.cuh",
+                                             "common.cuh")) if T == 4096 else None}
+    else:
+        roof = {"bound": "alu", "peak": fp32_peak_tflops(),
+                "peak_source": "fp32 FMA: 152 SMs x 128 lanes x 2 x 2070 MHz",
+                "kernel": "kda_chunk_bwd_kernel (+ the batch sum of dA_log, ddt_bias)",
+                "traffic": None}
+    roof.update({"achieved": achieved, "unit": "TFLOP/s", "frac": achieved / roof["peak"],
+                 "flops_convention": "12KV+3CK+2CV+C^2/3 per token-head, C=16"})
     res = {"value": ws * B * T / per, "unit": "tokens/s", "ms_per_step": per * 1e3,
            "steps": args.backward_steps,
-           "roofline": {"bound": "alu", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                        "frac": achieved / peak,
-                        "traffic": measured_traffic("kda_chunk_bwd_kernel", ("chunk_bwd.cu", "common.cuh"))
-                        if T == 4096 else None,
-                        "flops_convention": "12KV+3CK+2CV+C^2/3 per token-head, C=16",
-                        "peak_source": "fp32 FMA: 152 SMs x 128 lanes x 2 x 2070 MHz",
-                        "kernel": "kda_chunk_bwd_kernel (+ the batch sum of dA_log, ddt_bias)"},
+           "roofline": roof,
            "gpu_launches": launches,
            "config": {"workload": f"{WORKLOAD} backward B{B} H{H} T{T} K={K} V={V}, "
                                   "bf16 inputs, fp32 gradients, dL/dhT given",
