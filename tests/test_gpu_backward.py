@@ -83,7 +83,10 @@ def run_bwd(kda, inp, seed, with_dhT=True, threads=8):
     (1, 2, 17, 16, 8, "f32", 0.3, None),            # one chunk and one token
     (1, 2, 70, 128, 64, "f32", 0.1, None),          # K > V
     (1, 2, 70, 64, 128, "f32", 0.1, None),          # K < V
-    (1, 4, 300, 128, 128, "bf16", 0.1, None),       # the kernel's largest tile, bf16 I/O
+    (1, 4, 300, 128, 128, "bf16", 0.1, None),       # the tensor-core form, bf16 I/O
+    (2, 2, 77, 128, 128, "f32", 0.2, (-3.0, 2.0)),  # the tensor-core form, fp32 I/O, ragged
+    (1, 2, 1, 128, 128, "f32", 0.3, None),          # the tensor-core form, one token
+    (1, 2, 16, 128, 128, "bf16", 0.0, None),        # the tensor-core form, one chunk, no h0
 ])
 def test_backward_matches_oracle(kda, B, H, T, K, V, dtype, h0_std, A_log):
     inp = inputs.make(B, H, T, K, V, dtype=dtype, seed=100 + T + K, h0_std=h0_std, A_log=A_log)
@@ -106,8 +109,17 @@ def test_backward_strong_decay_and_z_sweep(kda):
     check_all(g, ref, inp)
 
 
-def test_backward_empty_sequence(kda):
-    inp = inputs.make(2, 3, 0, 16, 8, dtype="f32", seed=5, h0_std=0.1)
+def test_backward_tensor_core_form_without_dhT_and_strong_decay(kda):
+    # K = V = 128 takes the tensor-core form; per-token decay down to e^{-96} and no dL/dhT
+    inp = inputs.make(1, 2, 64, 128, 128, dtype="f32", seed=43, h0_std=0.1,
+                      A_log_value=float(np.log(16.0)), z_sweep=(-6.0, 6.0))
+    g, ref = run_bwd(kda, inp, seed=44, with_dhT=False)
+    check_all(g, ref, inp)
+
+
+@pytest.mark.parametrize("K,V", [(16, 8), (128, 128)])
+def test_backward_empty_sequence(kda, K, V):
+    inp = inputs.make(2, 3, 0, K, V, dtype="f32", seed=5, h0_std=0.1)
     adj = inputs.adjoints(inp, seed=6)
     d = inp.to("cuda")
     g = kda.chunk_backward(d.q, d.k, d.v, d.z, d.beta, d.A_log, d.dt_bias, adj.d_o.to("cuda"),
@@ -116,7 +128,7 @@ def test_backward_empty_sequence(kda):
     assert torch.equal(g["dh0"].cpu(), adj.dhT)
     assert torch.count_nonzero(g["dA_log"]).item() == 0
     assert torch.count_nonzero(g["ddt_bias"]).item() == 0
-    assert g["dq"].shape == (2, 3, 0, 16) and g["dv"].shape == (2, 3, 0, 8)
+    assert g["dq"].shape == (2, 3, 0, K) and g["dv"].shape == (2, 3, 0, V)
 
 
 def test_backward_is_deterministic(kda):

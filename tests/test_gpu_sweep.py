@@ -81,6 +81,8 @@ def test_backward_breadth_sweep(kda):
     for n in range(60):
         c = _case(rng)
         c["T"] = min(c["T"], 120)
+        if n % 3 == 2:  # every third case takes the tensor-core form (K = V = 128)
+            c.update(K=128, V=128)
         inp = inputs.make(c["B"], c["H"], c["T"], c["K"], c["V"], dtype=c["dtype"],
                           seed=c["seed"], dt_std=c["dt_std"], h0_std=c["h0_std"],
                           A_log_value=c["A_log_value"])
