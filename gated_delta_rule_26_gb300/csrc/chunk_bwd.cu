@@ -769,12 +769,15 @@ constexpr int F_BET = F_DM + BC * BC, F_GAM = F_BET + BC, F_RED = F_GAM + KM;
 constexpr int F_GT = F_RED + 4 * KM;            // g (the per-token log decay) [KM][GP]
 constexpr int F_END = F_GT + KM * GP;
 constexpr uint32_t OFF_MISC = OFF_F + 4u * F_END;  // four mbarriers, TMEM base, failure flag
-// staging of the next chunk's raw q, k, z and v (phase 1) or dO (phase 2) rows, bulk-copied
+// staging of the next chunk's rows, bulk-copied: three I/O tiles (q, k, then z in phase 1 or
+// dO in phase 2) and an 8 KB slot (v in phase 1, the fp32 g phase 1 kept in phase 2)
 constexpr uint32_t OFF_STG = OFF_MISC + 64;
 template <typename IO>
 constexpr uint32_t stg_tile() { return (uint32_t)(BC * KM * sizeof(IO)); }
 template <typename IO>
-constexpr size_t smem_bytes() { return OFF_STG + 4 * stg_tile<IO>() + 1024; }  // + alignment slack
+constexpr uint32_t off_gslot() { return OFF_STG + 3 * stg_tile<IO>(); }
+template <typename IO>
+constexpr size_t smem_bytes() { return off_gslot<IO>() + BC * KM * 4 + 1024; }  // + alignment slack
 static_assert((OFF_F + 4u * F_R) % 16 == 0 && (OFF_F + 4u * F_DL) % 16 == 0 &&
               (OFF_F + 4u * F_DO) % 16 == 0 && (OFF_F + 4u * F_DY) % 16 == 0, "float4 rows");
 static_assert(OFF_MISC % 16 == 0 && OFF_STG % 16 == 0, "mbarriers and bulk-copy destinations");
@@ -787,10 +790,12 @@ constexpr uint32_t ID_K_K32 = tc::idesc_bf16(128, 32, 0, 0);
 constexpr uint32_t ID_K_K64 = tc::idesc_bf16(128, 64, 0, 0);
 constexpr uint32_t ID_MN_MN128 = tc::idesc_bf16(128, 128, 1, 1);
 constexpr uint32_t kStateBytes = 65536;        // one operand copy of the state (hi + lo)
-// floats phase 1 keeps per chunk for phase 2: R, Delta [BC][V], then A', T, M [BC][BC]
-constexpr int RD = 2 * BC * VM + 3 * BC * BC;
+// floats phase 1 keeps per chunk for phase 2: R, Delta [BC][V], A', T, M [BC][BC] (contiguous in
+// shared memory, RD_SM floats), then g [BC][K]
+constexpr int RD_SM = 2 * BC * VM + 3 * BC * BC;
+constexpr int RD = RD_SM + BC * KM;
 static_assert(F_DL == F_R + BC * VM && F_AP == F_DL + BC * VM && F_TM == F_AP + BC * BC &&
-              F_MM == F_TM + BC * BC && F_MM + BC * BC == F_R + RD, "R, Delta, A', T, M contiguous");
+              F_MM == F_TM + BC * BC && F_MM + BC * BC == F_R + RD_SM, "R, Delta, A', T, M contiguous");
 }  // namespace bwdtc
 
 // x = hi + lo with hi = bf16(x), lo = bf16(x - hi), eight values at a time
@@ -934,32 +939,36 @@ __global__ void __launch_bounds__(bwdtc::NT, 1) kda_chunk_bwd_tc_kernel(const Bw
     auto prefetch_state = [&](int n) {
         if (n >= 0 && n < N) prefetch_l2(reinterpret_cast<const char*>(a.ckpt + (bh * N + n) * KV) + 128 * tid);
     };
-    // Request chunk n's raw q, k, z and v (phase 1) or dO (phase 2) rows into the staging tiles
-    // (bulk copies on bar_in, issued by thread 0) and its beta into bnext (threads < BC).
+    // Request chunk n's raw rows into the staging tiles (bulk copies on bar_in, issued by thread
+    // 0): q, k, and z, v (phase 1) or dO (phase 2); and its beta into bnext (threads < BC).
     float bnext = 0.f;
     auto request = [&](int n, bool full) {
         const int t0 = n * BC, cn = min(BC, T - t0);
         if (tid == 0) {
             const uint32_t bytes = (uint32_t)(cn * K * sizeof(IO));
             const size_t g0 = (bh * T + t0) * (size_t)K;
-            tc::mbar_arrive_expect_tx(bar_in, 4 * bytes);
+            tc::mbar_arrive_expect_tx(bar_in, (full ? 3 : 4) * bytes);
             tc::bulk_load(sm8 + OFF_STG, a.q + g0, bytes, bar_in);
             tc::bulk_load(sm8 + OFF_STG + stg_tile<IO>(), a.k + g0, bytes, bar_in);
-            tc::bulk_load(sm8 + OFF_STG + 2 * stg_tile<IO>(), a.z + g0, bytes, bar_in);
-            tc::bulk_load(sm8 + OFF_STG + 3 * stg_tile<IO>(), (full ? a.d_o : a.v) + g0, bytes, bar_in);
+            tc::bulk_load(sm8 + OFF_STG + 2 * stg_tile<IO>(), (full ? a.d_o : a.z) + g0, bytes, bar_in);
+            if (!full) tc::bulk_load(sm8 + off_gslot<IO>(), a.v + g0, bytes, bar_in);
         }
         if (tid < BC) bnext = tid < cn ? ld_io(a.beta + bh * T + t0 + tid) : 0.f;
     };
-    // Request chunk n's R, Delta, A', T, M (phase 2) into place (one bulk copy on bar_rd).
+    // Request chunk n's record from phase 2: R, Delta, A', T, M into place and g into the
+    // staging slot (two bulk copies on bar_rd).
     auto request_rd = [&](int n) {
         if (tid == 0) {
+            const float* src = a.rd + (bh * N + n) * (size_t)RD;
             tc::mbar_arrive_expect_tx(bar_rd, RD * 4);
-            tc::bulk_load(Rv, a.rd + (bh * N + n) * (size_t)RD, RD * 4, bar_rd);
+            tc::bulk_load(Rv, src, RD_SM * 4, bar_rd);
+            tc::bulk_load(sm8 + off_gslot<IO>(), src + RD_SM, BC * KM * 4, bar_rd);
         }
     };
-    // Chunk n's staged rows into the fp32 tiles: q, k, G and g (from z), beta, and v (phase 1,
-    // into R) or dO (phase 2, whose R, Delta, A', T, M arrive by request_rd); the staging is then
-    // free and the next chunk's rows are requested; then the in-chunk cumulative sum and gamma.
+    // Chunk n's staged rows into the fp32 tiles: q, k, beta, g (phase 1: from z, and kept in XT
+    // for the chunk's record; phase 2: as phase 1 kept it), v (phase 1, into R) or dO (phase 2,
+    // whose R, Delta, A', T, M arrive by request_rd); the staging is then free and the next
+    // chunk's rows are requested; then G, the in-chunk cumulative sum of g, and gamma.
     auto load_inputs = [&](int n, bool full) {
         const int t0 = n * BC, cn = min(BC, T - t0);
         if (!tc::mbar_wait(bar_in, ph_in)) fail();
@@ -970,21 +979,25 @@ __global__ void __launch_bounds__(bwdtc::NT, 1) kda_chunk_bwd_tc_kernel(const Bw
         }
         const IO* sq = reinterpret_cast<const IO*>(sm8 + OFF_STG);
         const IO* sk = sq + BC * K;
-        const IO* sz = sk + BC * K;
-        const IO* sv = sz + BC * K;
+        const IO* s2 = sk + BC * K;  // z (phase 1) or dO (phase 2)
+        const IO* sv = reinterpret_cast<const IO*>(sm8 + off_gslot<IO>());
+        const float* sg = reinterpret_cast<const float*>(sm8 + off_gslot<IO>());
         float run[4];  // this thread's tokens 4 qtr + r: prefix sums of g within the four
 #pragma unroll
         for (int r = 0; r < 4; ++r) {
             const int t = 4 * qtr + r, idx = t * K + col;
             const bool in = t < cn;
-            const float g = in ? kda_log_decay(ld_io(sz + idx), dtc, eA) : 0.f;
+            const float g = full ? sg[idx] : (in ? kda_log_decay(ld_io(s2 + idx), dtc, eA) : 0.f);
             Kr[ci(col, t)] = in ? ld_io(sk + idx) : 0.f;
             Qr[ci(col, t)] = in ? ld_io(sq + idx) : 0.f;
             Gt[ci(col, t)] = g;
             run[r] = r ? run[r - 1] + g : g;
-            const float x = in ? ld_io(sv + idx) : 0.f;
-            if (full) dO[idx] = x;
-            else Rv[idx] = x;
+            if (full) {
+                dO[idx] = in ? ld_io(s2 + idx) : 0.f;
+            } else {
+                Rv[idx] = in ? ld_io(sv + idx) : 0.f;
+                XT[idx] = g;
+            }
         }
         red[qtr * KM + col] = run[3];
         if (tid < BC) bet[tid] = bnext;
@@ -1185,12 +1198,14 @@ __global__ void __launch_bounds__(bwdtc::NT, 1) kda_chunk_bwd_tc_kernel(const Bw
         }
         tc::fence_proxy_async_smem();
         __syncthreads();
-        if (tid == 0) {  // R, Delta, A', T and M (contiguous) for phase 2
-            tc::bulk_store(a.rd + (bh * N + n) * (size_t)RD, Rv, RD * 4);
+        if (tid == 0) {  // R, Delta, A', T and M (contiguous), and g, for phase 2
+            float* dst = a.rd + (bh * N + n) * (size_t)RD;
+            tc::bulk_store(dst, Rv, RD_SM * 4);
+            tc::bulk_store(dst + RD_SM, XT, BC * KM * 4);
             tc::bulk_commit();
         }
         tile_rows(Dl, OFF_DLT, 32, 16, 0);
-        if (tid == 0) tc::bulk_wait_read_all();  // before the next chunk's v lands in R
+        if (tid == 0) tc::bulk_wait_read_all();  // before the next chunk's v and g land in R, XT
         tc::fence_before_sync();
         __syncthreads();
         if (tid == 0) {  // S += Kt^T Delta (K step 0 the hi rows, 1 the lo rows)
@@ -1426,33 +1441,43 @@ __global__ void __launch_bounds__(bwdtc::NT, 1) kda_chunk_bwd_tc_kernel(const Bw
         float* rowP = colP + 4 * BC * KM;                       // [BC][2][KM]
         {
             const int c = col;
-            float colS[BC];
-#pragma unroll
-            for (int t = 0; t < BC; ++t) colS[t] = 0.f;
+            float gs[4], ks[4], qs[4], bs[4], dMd[4], rM[4], rA[4];
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
                 const int s = u == 0 ? qtr : u == 1 ? 7 - qtr : u == 2 ? 8 + qtr : 15 - qtr;
-                const float gs = Gc[ci(c, s)], ks = Kr[ci(c, s)], qs = Qr[ci(c, s)], bs = bet[s];
-                const float dMd = dM[s * BC + s];
-                float rM = dMd * ks, rA = 0.f;  // the diagonal pair (E = 1, dB[s][s] = 0)
-#pragma unroll
-                for (int t = 0; t < BC; ++t) {
-                    if (t < s) {
-                        const float E = __expf(gs - Gc[ci(c, t)]);
-                        const float kt = Kr[ci(c, t)];
-                        const float w = dM[s * BC + t] * E, x = bs * dB[s * BC + t] * E;
-                        rM = fmaf(w, kt, rM);
-                        rA = fmaf(x, kt, rA);
-                        colS[t] = fmaf(w, qs, fmaf(x, ks, colS[t]));
-                    } else if (t == s) {
-                        colS[t] = fmaf(dMd, qs, colS[t]);
-                    }
-                }
-                rowP[(2 * s) * KM + c] = rM;
-                rowP[(2 * s + 1) * KM + c] = rA;
+                gs[u] = Gc[ci(c, s)];
+                ks[u] = Kr[ci(c, s)];
+                qs[u] = Qr[ci(c, s)];
+                bs[u] = bet[s];
+                dMd[u] = dM[s * BC + s];
+                rM[u] = dMd[u] * ks[u];  // the diagonal pair (E = 1, dB[s][s] = 0)
+                rA[u] = 0.f;
             }
 #pragma unroll
-            for (int t = 0; t < BC; ++t) colP[(qtr * BC + t) * KM + c] = colS[t];
+            for (int t = 0; t < BC; ++t) {
+                const float gt = Gc[ci(c, t)], kt = Kr[ci(c, t)];
+                float cs = 0.f;
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int s = u == 0 ? qtr : u == 1 ? 7 - qtr : u == 2 ? 8 + qtr : 15 - qtr;
+                    if (t < s) {
+                        const float E = __expf(gs[u] - gt);
+                        const float w = dM[s * BC + t] * E, x = bs[u] * dB[s * BC + t] * E;
+                        rM[u] = fmaf(w, kt, rM[u]);
+                        rA[u] = fmaf(x, kt, rA[u]);
+                        cs = fmaf(w, qs[u], fmaf(x, ks[u], cs));
+                    } else if (t == s) {
+                        cs = fmaf(dMd[u], qs[u], cs);
+                    }
+                }
+                colP[(qtr * BC + t) * KM + c] = cs;
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int s = u == 0 ? qtr : u == 1 ? 7 - qtr : u == 2 ? 8 + qtr : 15 - qtr;
+                rowP[(2 * s) * KM + c] = rM[u];
+                rowP[(2 * s + 1) * KM + c] = rA[u];
+            }
         }
         if (tid == 0) tc::bulk_wait_read_all();  // dV has left XT
         __syncthreads();

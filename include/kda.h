@@ -230,10 +230,10 @@ int kda_fused_recurrent(const kda_dims* dims, kda_dtype io_dtype, const void* q,
  * cores, each float32 operand split into two bf16 halves and all four half products
  * accumulated in float32 (about 2^-15 relative per product term), the state and its gradient
  * kept in float32; other sizes run in float32 on the CUDA cores.  Scratch: (B*H*ceil(T/16)*
- * (K*V + R) + B*H*(K+1)) float32, R = 2*16*V + 3*16*16 for K = V = 128 and 2*16*V otherwise
- * (the state entering every 16-token chunk and the chunk's R, Delta and, for K = V = 128,
- * A', T, M), from cudaMallocAsync on `stream`, freed on it; KDA_ERR_NO_MEMORY if that
- * fails.  A bounded wait of the tensor-core form that gives up is reported by
+ * (K*V + R) + B*H*(K+1)) float32, R = 2*16*V + 3*16*16 + 16*K for K = V = 128 and 2*16*V
+ * otherwise (the state entering every 16-token chunk and the chunk's R, Delta and, for
+ * K = V = 128, A', T, M and the log decay g), from cudaMallocAsync on `stream`, freed on it;
+ * KDA_ERR_NO_MEMORY if that fails.  A bounded wait of the tensor-core form that gives up is reported by
  * kda_device_status.  Alignment: q, k, v, z, d_o, dq,
  * dk, dv, dz, h0, dhT, dh0 16 bytes; beta, dbeta, dA_log, ddt_bias, A_log, dt_bias their
  * element size.  Two kernels per call (the pass, then the batch sum of dA_log / ddt_bias).
