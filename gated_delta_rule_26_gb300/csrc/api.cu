@@ -249,6 +249,8 @@ int kda_device_status(kda_stream_t stream) {
     return timed_out ? KDA_ERR_TIMEOUT : KDA_OK;
 }
 
+int kda_release_scratch(void) { return from_cuda(kda::scratch_release()); }
+
 int kda_selftest_bounded_wait(unsigned long long limit_ns, kda_stream_t stream) {
     if (limit_ns == 0 || limit_ns > 10000000000ull) return KDA_ERR_INVALID_ARG;
     return from_cuda(kda::launch_bounded_wait_selftest(limit_ns, (cudaStream_t)stream));

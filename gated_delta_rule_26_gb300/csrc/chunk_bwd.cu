@@ -1594,7 +1594,7 @@ cudaError_t launch_chunk_backward(const BwdLaunch& L, cudaStream_t s) {
     const size_t rd_bytes = sizeof(float) * BH * (size_t)N * (fixed ? (size_t)bwdtc::RD : (size_t)(2 * BC * V));
     const size_t part_bytes = sizeof(float) * BH * (size_t)(1 + K);
     char* scratch = nullptr;
-    cudaError_t e = cudaMallocAsync(reinterpret_cast<void**>(&scratch),
+    cudaError_t e = scratch_alloc(reinterpret_cast<void**>(&scratch),
                                     ck_bytes + rd_bytes + part_bytes + 256, s);
     if (e != cudaSuccess) return e;
     float* dA_part = reinterpret_cast<float*>(scratch);
@@ -1649,7 +1649,7 @@ cudaError_t launch_chunk_backward(const BwdLaunch& L, cudaStream_t s) {
         e = cudaGetLastError();
         count_launches(2);
     }
-    const cudaError_t ef = cudaFreeAsync(scratch, s);
+    const cudaError_t ef = scratch_free(scratch, s);
     return e != cudaSuccess ? e : ef;
 }
 

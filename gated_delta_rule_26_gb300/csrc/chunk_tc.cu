@@ -1543,12 +1543,12 @@ cudaError_t launch_chunk_split(const ChunkArgs& a, cudaStream_t s) {
             const size_t bytes = 2 * round_up(items_max * kItemBytes, 256) +
                                  (a.hT ? 0 : (size_t)BH * KD * VD * sizeof(float));
             void* p = nullptr;
-            if (cudaMallocAsync(&p, bytes, s) != cudaSuccess) {
+            if (scratch_alloc(&p, bytes, s) != cudaSuccess) {
                 cudaGetLastError();
                 return cudaErrorMemoryAllocation;
             }
             const cudaError_t err = run_chunk_split_overlap(a, s, p, seg_len);
-            const cudaError_t ferr = cudaFreeAsync(p, s);
+            const cudaError_t ferr = scratch_free(p, s);
             return err != cudaSuccess ? err : ferr;
         }
     }
@@ -1556,12 +1556,12 @@ cudaError_t launch_chunk_split(const ChunkArgs& a, cudaStream_t s) {
     if (seg_len < 1) return cudaErrorMemoryAllocation;
     const size_t bytes = split_scratch_bytes(a, seg_len);
     void* p = nullptr;
-    if (cudaMallocAsync(&p, bytes, s) != cudaSuccess) {
+    if (scratch_alloc(&p, bytes, s) != cudaSuccess) {
         cudaGetLastError();
         return cudaErrorMemoryAllocation;
     }
     const cudaError_t err = run_chunk_split(a, s, p, bytes);
-    const cudaError_t ferr = cudaFreeAsync(p, s);
+    const cudaError_t ferr = scratch_free(p, s);
     return err != cudaSuccess ? err : ferr;
 }
 
@@ -1608,7 +1608,7 @@ cudaError_t launch_chunk_fused(const ChunkArgs& a, cudaStream_t s) {
     const size_t flag_bytes = round_up(sizeof(unsigned) * (1 + (size_t)BH), 256);
     const size_t bytes = flag_bytes + (a.hT ? 0 : (size_t)BH * KD * VD * sizeof(float));
     void* p = nullptr;
-    if (cudaMallocAsync(&p, bytes, s) != cudaSuccess) {
+    if (scratch_alloc(&p, bytes, s) != cudaSuccess) {
         cudaGetLastError();
         return cudaErrorMemoryAllocation;
     }
@@ -1623,7 +1623,7 @@ cudaError_t launch_chunk_fused(const ChunkArgs& a, cudaStream_t s) {
         count_launches(1);
         err = cudaGetLastError();
     }
-    const cudaError_t ferr = cudaFreeAsync(p, s);
+    const cudaError_t ferr = scratch_free(p, s);
     return err != cudaSuccess ? err : ferr;
 }
 
@@ -1734,12 +1734,12 @@ cudaError_t launch_chunk_scan(const ChunkArgs& a, cudaStream_t s) {
     const size_t bytes = scan_scratch_bytes(a, seg_len, &nsub_max);
     if (bytes > kSplitScratchCap) return cudaErrorMemoryAllocation;
     void* p = nullptr;
-    if (cudaMallocAsync(&p, bytes, s) != cudaSuccess) {
+    if (scratch_alloc(&p, bytes, s) != cudaSuccess) {
         cudaGetLastError();
         return cudaErrorMemoryAllocation;
     }
     const cudaError_t err = run_chunk_split_scan(a, s, p, seg_len, nsub_max);
-    const cudaError_t ferr = cudaFreeAsync(p, s);
+    const cudaError_t ferr = scratch_free(p, s);
     return err != cudaSuccess ? err : ferr;
 }
 

@@ -60,6 +60,13 @@ struct BwdLaunch {
 // Count `n` kernel launches (read through kda_launch_count()).
 void count_launches(int n);
 
+// Scratch of the library's calls, stream-ordered on `s`, from the library's own pool of the
+// current device, which keeps freed blocks for the next call (pool.cu); scratch_release hands
+// the pool's unused blocks back to the system.
+cudaError_t scratch_alloc(void** p, size_t bytes, cudaStream_t s);
+cudaError_t scratch_free(void* p, cudaStream_t s);
+cudaError_t scratch_release();
+
 // Internal launchers (one per kernel family); each returns a cudaError_t from the launch.
 cudaError_t launch_gate(int B, int H, int T, int K, kda_dtype zdt, const void* z,
                         const float* A_log, const float* dt_bias, int chunk, float* g,

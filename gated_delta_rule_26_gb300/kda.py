@@ -68,6 +68,8 @@ def load() -> ctypes.CDLL:
         lib.kda_selftest_bounded_wait.restype = i
         lib.kda_launch_count.argtypes = []
         lib.kda_launch_count.restype = ctypes.c_ulonglong
+        lib.kda_release_scratch.argtypes = []
+        lib.kda_release_scratch.restype = i
         for fn in (lib.kda_gate, lib.kda_chunk_forward, lib.kda_recurrent_step,
                    lib.kda_fused_recurrent, lib.kda_chunk_backward):
             fn.restype = i
@@ -85,6 +87,11 @@ def selftest_bounded_wait(limit_ns: int, stream=None) -> None:
     """Launch a kernel whose wait can never be satisfied; it ends after `limit_ns`."""
     _check("kda_selftest_bounded_wait", load().kda_selftest_bounded_wait(int(limit_ns),
                                                                           _stream(stream)))
+
+
+def release_scratch() -> None:
+    """Hand the blocks the library's scratch pool keeps for later calls back to the system."""
+    _check("kda_release_scratch", load().kda_release_scratch())
 
 
 def launch_count() -> int:

@@ -32,9 +32,15 @@
  *   need only their element alignment.
  * - The caller owns every buffer.  The library keeps no state between calls
  *   except the CUDA resources the runtime itself caches, the split form's second
- *   stream and the no-alloc form's fixed array (both below); it is re-entrant.
- *   Scratch memory, where a path needs it, is taken with cudaMallocAsync on the
- *   caller's stream and released on the same stream before the call returns.
+ *   stream, the no-alloc form's fixed array (both below) and its scratch pool; it
+ *   is re-entrant.  Scratch memory, where a path needs it, is taken stream-ordered
+ *   on the caller's stream from a memory pool of the library's own on the current
+ *   device (cudaMallocFromPoolAsync) and returned to it on the same stream before
+ *   the call returns.  The pool keeps the blocks returned to it for later calls
+ *   (the device's default pool hands them back to the system at every
+ *   synchronisation, and mapping them again cost as much as a backward kernel):
+ *   it holds up to the largest scratch in use at once until kda_release_scratch()
+ *   or the end of the process.
  * - Work is enqueued on `stream` (NULL = the legacy default stream); calls
  *   return as soon as it is enqueued.  Argument errors are detected on the host
  *   before anything is launched; a launch error is reported as KDA_ERR_CUDA;
@@ -104,9 +110,8 @@ int kda_chunk_forward(const kda_dims* dims, kda_dtype io_dtype, const void* q, c
  *           sequences than SMs, one CTA per SM takes (segment, sequence) work items of a few
  *           chunks in order and the fp32 state passes between a sequence's segments through
  *           hT (or, when hT is NULL, a B*H*K*V*4-byte scratch buffer); a counter and one flag
- *           per sequence (4*(B*H + 1) bytes) are cleared and freed on `stream` by the call
- *           (cudaMallocAsync / cudaMemsetAsync / cudaFreeAsync; KDA_ERR_NO_MEMORY if the
- *           allocation fails).
+ *           per sequence (4*(B*H + 1) bytes) are taken from the scratch pool, cleared and
+ *           returned on `stream` by the call (KDA_ERR_NO_MEMORY if the allocation fails).
  *   split : the chunk-parallel WY form of kda-adjoint-2026-10-01 section 2 as two kernels.  A
  *           prep kernel spreads every chunk of every sequence over the GPU and writes, per
  *           chunk, the state-independent operands ([W^T | Q'^T], [U^T | U'^T], K~ =
@@ -114,9 +119,9 @@ int kda_chunk_forward(const kda_dims* dims, kda_dtype io_dtype, const void* q, c
  *           walks the chunks of each sequence with the fp32 state on chip (S <- Gamma_last S
  *           + K~^T (U - W S), o = scale (Q' S + U')).  Suited to few, long sequences, where
  *           the fused form leaves most of the GPU idle.  The operands live in scratch that
- *           the call allocates and frees on `stream` (cudaMallocAsync / cudaFreeAsync, at most
- *           1 GiB: longer inputs run as consecutive segments of chunks); KDA_ERR_NO_MEMORY if
- *           that allocation fails.  With B*H at most half the SMs and four or more chunks,
+ *           the call takes from the scratch pool and returns on `stream` (at most 1 GiB:
+ *           longer inputs run as consecutive segments of chunks); KDA_ERR_NO_MEMORY if that
+ *           allocation fails.  With B*H at most half the SMs and four or more chunks,
  *           the call runs each segment's carry on a second stream, beside the next segment's
  *           prep, with two operand buffers, and joins it back into `stream` (events) before
  *           it returns.  That stream and its five events are created on the first such call
@@ -147,8 +152,8 @@ int kda_chunk_forward_fused(const kda_dims* dims, kda_dtype io_dtype, const void
  * in parallel.  About three times the carry work of the split form, but the sequential part
  * is one K x K by K x V product per sub-segment instead of one chunk step per chunk.
  * kda_chunk_forward takes this form by itself where it is the faster one.
- * Shapes, arguments and errors as kda_chunk_forward_split.  Scratch (cudaMallocAsync /
- * cudaFreeAsync on `stream`, at most 1 GiB, longer inputs in segments of chunks): the
+ * Shapes, arguments and errors as kda_chunk_forward_split.  Scratch (from the scratch pool on
+ * `stream`, at most 1 GiB, longer inputs in segments of chunks): the
  * per-chunk operands, 3 x B*H*K*V*4 bytes per sub-segment for the maps and the entering
  * states, and B*H*K*V*4 for the carried state when hT is NULL; KDA_ERR_NO_MEMORY if that
  * allocation fails.  The result equals the split form's to rounding (the state reaches each
@@ -232,8 +237,8 @@ int kda_fused_recurrent(const kda_dims* dims, kda_dtype io_dtype, const void* q,
  * kept in float32; other sizes run in float32 on the CUDA cores.  Scratch: (B*H*ceil(T/16)*
  * (K*V + R) + B*H*(K+1)) float32, R = 2*16*V + 3*16*16 + 16*K for K = V = 128 and 2*16*V
  * otherwise (the state entering every 16-token chunk and the chunk's R, Delta and, for
- * K = V = 128, A', T, M and the log decay g), from cudaMallocAsync on `stream`, freed on it;
- * KDA_ERR_NO_MEMORY if that fails.  A bounded wait of the tensor-core form that gives up is reported by
+ * K = V = 128, A', T, M and the log decay g), from the scratch pool on `stream`, returned on
+ * it; KDA_ERR_NO_MEMORY if that fails.  A bounded wait of the tensor-core form that gives up is reported by
  * kda_device_status.  Alignment: q, k, v, z, d_o, dq,
  * dk, dv, dz, h0, dhT, dh0 16 bytes; beta, dbeta, dA_log, ddt_bias, A_log, dt_bias their
  * element size.  Two kernels per call (the pass, then the batch sum of dA_log / ddt_bias).
@@ -244,6 +249,14 @@ int kda_chunk_backward(const kda_dims* dims, kda_dtype io_dtype, const void* q, 
                        const float* dhT, float* dq, float* dk, float* dv, float* dz,
                        float* dbeta, float* dA_log, float* ddt_bias, float* dh0,
                        kda_stream_t stream);
+
+/*
+ * kda_release_scratch -- wait for the current device to finish its work, then hand the blocks
+ * the library's scratch pool holds for later calls back to the system (the pool is described
+ * at the top of this header; a later call takes its scratch anew).  KDA_ERR_CUDA if a CUDA
+ * call fails.
+ */
+int kda_release_scratch(void);
 
 /* A static, human-readable name for a status code. */
 const char* kda_status_string(int status);

@@ -143,6 +143,22 @@ def test_backward_is_deterministic(kda):
         assert torch.equal(a[n], b[n]), n
 
 
+def test_backward_same_after_scratch_release(kda):
+    # the scratch pool keeps its blocks between calls; releasing them changes nothing but memory
+    inp = inputs.make(1, 2, 50, 128, 128, dtype="bf16", seed=61, h0_std=0.1)
+    adj = inputs.adjoints(inp, seed=62)
+    d = inp.to("cuda")
+    args = (d.q, d.k, d.v, d.z, d.beta, d.A_log, d.dt_bias, adj.d_o.to("cuda"), inp.scale)
+    a = kda.chunk_backward(*args, h0=d.h0, dhT=adj.dhT.to("cuda"))
+    torch.cuda.synchronize()
+    kda.release_scratch()
+    b = kda.chunk_backward(*args, h0=d.h0, dhT=adj.dhT.to("cuda"))
+    torch.cuda.synchronize()
+    assert kda.device_status() == 0
+    for n in NAMES:
+        assert torch.equal(a[n], b[n]), n
+
+
 def test_backward_full_size_sampled_head(kda):
     """The prefill workload (B8 H32 T4096 K=V=128, bf16) whole on the GPU; head 5 of all eight
     sequences recomputed by the oracle (dA_log[5] and ddt_bias[5] sum exactly those)."""
