@@ -26,7 +26,11 @@
 // The state and its adjoint sit in shared memory (rows of odd pitch, so that both row and column
 // walks are free of bank conflicts); every per-(token, channel) gradient term is produced by
 // the same thread, so dq, dk and dG accumulate in registers.
+#include <algorithm>
+#include <functional>
+#include <queue>
 #include <type_traits>
+#include <vector>
 
 #include "chunk_tiles.cuh"
 #include "common.cuh"
@@ -808,8 +812,25 @@ __device__ __forceinline__ void split8(const float (&f)[8], uint4& hi, uint4& lo
     lo = tile::pack8(r);
 }
 
+// Work items of the tensor-core backward, taken from *counter in order by one CTA per SM at
+// most: first the forward walk's segments (every sequence's segment 0, then segment 1, ...),
+// then the reverse walk's (every sequence's last segment first).  A segment is seg_len chunks
+// of one sequence.  The state passes between a sequence's forward segments through s_hand and
+// its adjoint between reverse segments through ds_hand; flags[2 bh] counts the sequence's
+// finished forward segments, flags[2 bh + 1] its finished reverse ones.  An item waits only for
+// items earlier in the order, which CTAs that are already running have taken, so the schedule
+// cannot deadlock; every wait is bounded.
+struct BwdSched {
+    int nseg, seg_len, n_items;
+    int* counter;
+    unsigned* flags;
+    float* s_hand;
+    float* ds_hand;
+};
+
 template <typename IO>
-__global__ void __launch_bounds__(bwdtc::NT, 1) kda_chunk_bwd_tc_kernel(const BwdArgs<IO> a) {
+__global__ void __launch_bounds__(bwdtc::NT, 1) kda_chunk_bwd_tc_kernel(const BwdArgs<IO> a,
+                                                                          const BwdSched sc) {
     using namespace bwdtc;
     extern __shared__ uint8_t smem_bwd_raw[];
     uint8_t* sm8 = reinterpret_cast<uint8_t*>(
@@ -838,17 +859,18 @@ __global__ void __launch_bounds__(bwdtc::NT, 1) kda_chunk_bwd_tc_kernel(const Bw
     uint64_t* bar_rd = bar_mma + 3;   // a chunk's R, Delta, A', T, M (phase 2)
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm8 + OFF_MISC + 32);
     volatile int* s_fail = reinterpret_cast<volatile int*>(sm8 + OFF_MISC + 36);
+    volatile int* s_item = reinterpret_cast<volatile int*>(sm8 + OFF_MISC + 40);
     const uint32_t sb = tc::smem_u32(sm8);
 
     constexpr int K = KM, V = VM;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int T = a.T;
-    const size_t bh = blockIdx.x;
-    const int h = (int)(bh % a.H);
     const int N = (T + BC - 1) / BC;
-    const float eA = expf(a.A_log[h]), ieA = expf(-a.A_log[h]);
-    const float dtc = __ldg(a.dt_bias + (size_t)h * KM + (threadIdx.x & 127));
     const size_t KV = (size_t)K * V;
+    // the current work item: sequence bh (head h), chunks [n_lo, n_hi)
+    size_t bh = 0;
+    int h = 0, n_lo = 0, n_hi = 0;
+    float eA = 1.f, ieA = 1.f, dtc = 0.f;
     // thread roles: channel or value column col (= the TMEM lane this warp reaches), and the
     // quarter qtr (tokens 4 qtr .. + 3, or TMEM columns 32 qtr .. + 31 of a 128-column matrix)
     const int col = tid & 127, qtr = tid >> 7;
@@ -937,7 +959,7 @@ __global__ void __launch_bounds__(bwdtc::NT, 1) kda_chunk_bwd_tc_kernel(const Bw
 
     // Ask L2 for the state copy phase 1 kept for chunk n, one 128-byte line per thread.
     auto prefetch_state = [&](int n) {
-        if (n >= 0 && n < N) prefetch_l2(reinterpret_cast<const char*>(a.ckpt + (bh * N + n) * KV) + 128 * tid);
+        if (n >= n_lo && n < n_hi) prefetch_l2(reinterpret_cast<const char*>(a.ckpt + (bh * N + n) * KV) + 128 * tid);
     };
     // Request chunk n's raw rows into the staging tiles (bulk copies on bar_in, issued by thread
     // 0): q, k, and z, v (phase 1) or dO (phase 2); and its beta into bnext (threads < BC).
@@ -1004,7 +1026,7 @@ __global__ void __launch_bounds__(bwdtc::NT, 1) kda_chunk_bwd_tc_kernel(const Bw
         tc::fence_proxy_async_smem();
         __syncthreads();
         const int nx = full ? n - 1 : n + 1;
-        if (nx >= 0 && nx < N) request(nx, full);
+        if (nx >= n_lo && nx < n_hi) request(nx, full);
         {  // G = the in-chunk cumulative sum: the earlier quarters' totals, then the prefix
             float off = 0.f;
 #pragma unroll
@@ -1147,441 +1169,545 @@ __global__ void __launch_bounds__(bwdtc::NT, 1) kda_chunk_bwd_tc_kernel(const Bw
         }
     };
 
-    // ======================================================= phase 1: chunk states forward
-    master_init(a.h0 ? a.h0 + bh * KV : nullptr);
-    if (N > 0) request(0, false);
-    tc::fence_before_sync();
-    __syncthreads();
-    for (int n = 0; n < N && !*s_fail; ++n) {
-        load_inputs(n, false);
-        if (n > 0) wait_mma();  // the previous chunk's state update has read Kt and Delta
-        if (tid == 0) tc::bulk_wait_read_all();  // the previous state copy has gone out
+    // ======================================================= work items
+    const int BHs = sc.n_items / (2 * sc.nseg);
+    float dA_acc = 0.f, ddt_acc = 0.f;  // reverse walk: this thread's channel col, tokens of qtr
+    for (;;) {
+        if (tid == 0) *s_item = atomicAdd(sc.counter, 1);
         __syncthreads();
-        master_copy();  // S as an operand
-        build_tiles(false, false);
-        arows();
-        tc::fence_before_sync();
+        const int item = *s_item;
+        if (item >= sc.n_items || *s_fail) break;
+        const bool fwd = item < BHs * sc.nseg;
+        const int idx = fwd ? item : item - BHs * sc.nseg;
+        const int seg = fwd ? idx / BHs : sc.nseg - 1 - idx / BHs;
+        bh = (size_t)(idx % BHs);
+        h = (int)(bh % a.H);
+        eA = expf(a.A_log[h]);
+        ieA = expf(-a.A_log[h]);
+        dtc = __ldg(a.dt_bias + (size_t)h * KM + col);
+        n_lo = min(N, seg * sc.seg_len);
+        n_hi = min(N, n_lo + sc.seg_len);
+        if (tid == 0) {  // the item this one continues
+            bool ok = true;
+            if (fwd && seg > 0) ok = tc::flag_wait_geq(sc.flags + 2 * bh, (unsigned)seg);
+            else if (!fwd && seg == sc.nseg - 1) ok = tc::flag_wait_geq(sc.flags + 2 * bh, (unsigned)sc.nseg);
+            else if (!fwd) ok = tc::flag_wait_geq(sc.flags + 2 * bh + 1, (unsigned)(sc.nseg - 1 - seg));
+            if (!ok) fail();
+            // what it wrote by bulk copy is read here by bulk copy
+            asm volatile("fence.proxy.async.global;" ::: "memory");
+        }
         __syncthreads();
-        if (tid == 0) {
-            tc::fence_after_sync();
+        if (fwd) {
+            // ============================================= forward walk: chunk states
+            master_init(seg == 0 ? (a.h0 ? a.h0 + bh * KV : nullptr) : sc.s_hand + bh * KV);
+            if (n_lo < n_hi) request(n_lo, false);
+            tc::fence_before_sync();
+            __syncthreads();
+            for (int n = n_lo; n < n_hi && !*s_fail; ++n) {
+                load_inputs(n, false);
+                if (n > n_lo) wait_mma();  // the previous chunk's state update has read Kt and Delta
+                if (tid == 0) tc::bulk_wait_read_all();  // the previous state copy has gone out
+                __syncthreads();
+                master_copy();  // S as an operand
+                build_tiles(false, false);
+                arows();
+                tc::fence_before_sync();
+                __syncthreads();
+                if (tid == 0) {
+                    tc::fence_after_sync();
 #pragma unroll 1
-            for (int p = 0; p < 2; ++p) {
+                    for (int p = 0; p < 2; ++p) {
 #pragma unroll
-                for (int ks = 0; ks < 8; ++ks)
-                    tc::mma_bf16(tm + TM_A, tile::desc_mn(sb + OFF_ST + p * ST_LO, 16384, ks),
-                                 tile::desc_k(sb + OFF_AQK, 32, ks), ID_MN_K32, (p | ks) != 0);
-            }
-            tc::mma_commit(bar_mma);
-        }
-        master_decay();  // S <- diag(gamma) S in TMEM, and T, under the R products
-        t_solve();
-        wait_mma();
-        __syncthreads();  // T is published
-        // R = V - Kg S and Delta = T diag(beta) R, value column v = tid on warps 0..3
-        if (warp < 4) {
-            uint32_t r[16], r2[16];
-            tc::tmem_ld16(tile::taddr(tm + TM_A, warp, 0), r);
-            tc::tmem_ld16(tile::taddr(tm + TM_A, warp, 16), r2);
-            tc::tmem_ld_wait();
-            float rr[BC];
-#pragma unroll
-            for (int t = 0; t < BC; ++t)
-                rr[t] = Rv[t * VM + tid] - (__uint_as_float(r[t]) + __uint_as_float(r2[t]));
-#pragma unroll
-            for (int t = 0; t < BC; ++t) {
-                float acc = 0.f;
-#pragma unroll
-                for (int i = 0; i <= t; ++i) acc = fmaf(Tm[t * BC + i], bet[i] * rr[i], acc);
-                Rv[t * VM + tid] = rr[t];
-                Dl[t * VM + tid] = acc;
-            }
-        }
-        tc::fence_proxy_async_smem();
-        __syncthreads();
-        if (tid == 0) {  // R, Delta, A', T and M (contiguous), and g, for phase 2
-            float* dst = a.rd + (bh * N + n) * (size_t)RD;
-            tc::bulk_store(dst, Rv, RD_SM * 4);
-            tc::bulk_store(dst + RD_SM, XT, BC * KM * 4);
-            tc::bulk_commit();
-        }
-        tile_rows(Dl, OFF_DLT, 32, 16, 0);
-        if (tid == 0) tc::bulk_wait_read_all();  // before the next chunk's v and g land in R, XT
-        tc::fence_before_sync();
-        __syncthreads();
-        if (tid == 0) {  // S += Kt^T Delta (K step 0 the hi rows, 1 the lo rows)
-            tc::fence_after_sync();
-#pragma unroll
-            for (int p = 0; p < 4; ++p)
-                tc::mma_bf16(tm + TM_M, tile::desc_mn(sb + OFF_KT, 4096, p >> 1),
-                             tile::desc_mn(sb + OFF_DLT, 4096, p & 1), ID_MN_MN128, 1u);
-            tc::mma_commit(bar_mma);
-            // the state copy is the chunk's checkpoint
-            tc::bulk_store(a.ckpt + (bh * N + n) * KV, sm8 + OFF_ST, kStateBytes);
-            tc::bulk_commit();
-        }
-    }
-    if (N > 0 && !*s_fail) wait_mma();
-    if (tid == 0) tc::bulk_wait_all();  // every checkpoint is in global memory
-    // R, Delta, A', T, M (generic stores) are read back by bulk copies, and the tiles phase 2
-    // fills by bulk copy were last written by generic stores
-    asm volatile("fence.proxy.async.global;" ::: "memory");
-    tc::fence_proxy_async_smem();
-    __syncthreads();
-    if (N > 0) {
-        request(N - 1, true);
-        request_rd(N - 1);
-        prefetch_state(N - 1);
-    }
-
-    // ======================================================= phase 2: reverse
-    master_init(a.dhT ? a.dhT + bh * KV : nullptr);
-    tc::fence_before_sync();
-    __syncthreads();
-    float dA_acc = 0.f, ddt_acc = 0.f;  // this thread's channel col, tokens of quarter qtr
-    for (int n = N - 1; n >= 0 && !*s_fail; --n) {
-        const int t0 = n * BC, cn = min(BC, T - t0);
-        load_inputs(n, true);
-        prefetch_state(n - 1);
-        if (n < N - 1) wait_mma();  // the previous chunk's dS update has read its tiles
-        build_tiles(true, false);
-        if (tid == 0) tc::bulk_wait_read_all();  // the previous chunk's dq, dk, dz have left
-        __syncthreads();
-        master_copy();  // dS as an operand
-        tc::fence_before_sync();
-        __syncthreads();
-        if (tid == 128) {  // dDelta^T = dS^T Kt^T + dO^T (scale M), dKt^T = dS Delta^T
-            tc::fence_after_sync();
-#pragma unroll 1
-            for (int p = 0; p < 2; ++p) {
-#pragma unroll
-                for (int ks = 0; ks < 8; ++ks)
-                    tc::mma_bf16(tm + TM_A, tile::desc_mn(sb + OFF_ST + p * ST_LO, 16384, ks),
-                                 tile::desc_k(sb + OFF_KT, 32, ks), ID_MN_K32, (p | ks) != 0);
-#pragma unroll
-                for (int ks = 0; ks < 8; ++ks)
-                    tc::mma_bf16(tm + TM_B, tile::desc_k(sb + OFF_ST + p * ST_LO, 128, ks),
-                                 tile::desc_k(sb + OFF_DLT, 32, ks), ID_K_K32, (p | ks) != 0);
-                // A = dO^T (rows 0..15 hi, 32..47 lo of [dO ; dY] read MN-major), B = scale M^T
-                tc::mma_bf16(tm + TM_A, tile::desc_mn(sb + OFF_DOY, 8192, 2 * p),
-                             tile::desc_k(sb + OFF_AQK, 32, 0), ID_MN_K32, 1u);
-            }
-            tc::mma_commit(bar_mma);
-        }
-        wait_mma();
-        if (tid == 0) {  // the state entering this chunk, as phase 1 kept it
-            tc::mbar_arrive_expect_tx(bar_ld, kStateBytes);
-            tc::bulk_load(sm8 + OFF_ST, a.ckpt + (bh * N + n) * KV, kStateBytes, bar_ld);
-        }
-        if (warp < 4) {  // dDelta, then dY = T^T dDelta
-            uint32_t r[16], r2[16];
-            tc::tmem_ld16(tile::taddr(tm + TM_A, warp, 0), r);
-            tc::tmem_ld16(tile::taddr(tm + TM_A, warp, 16), r2);
-            tc::tmem_ld_wait();
-            float dd[BC];
-#pragma unroll
-            for (int t = 0; t < BC; ++t) dd[t] = __uint_as_float(r[t]) + __uint_as_float(r2[t]);
-#pragma unroll
-            for (int i = 0; i < BC; ++i) {
-                float acc = 0.f;
-#pragma unroll
-                for (int t = i; t < BC; ++t) acc = fmaf(Tm[t * BC + i], dd[t], acc);
-                dY[i * VM + tid] = acc;
-            }
-        }
-        float dq_r[4] = {0.f, 0.f, 0.f, 0.f}, dk_r[4] = {0.f, 0.f, 0.f, 0.f};
-        float dG_r[4] = {0.f, 0.f, 0.f, 0.f};
-        float dgl_part = 0.f;
-        {  // dKt = Delta dS^T: channel col, tokens 4 qtr ..
-            uint32_t r[4], r2[4];
-            tc::tmem_ld4(tile::taddr(tm + TM_B, warp, 4 * qtr), r);
-            tc::tmem_ld4(tile::taddr(tm + TM_B, warp, 16 + 4 * qtr), r2);
-            tc::tmem_ld_wait();
-            const float gl = Gc[ci(col, (BC - 1))];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int t = 4 * qtr + u;
-                const float x = __uint_as_float(r[u]) + __uint_as_float(r2[u]);
-                const float eL = expf(gl - Gc[ci(col, t)]);
-                const float kk = Kr[ci(col, t)];
-                dk_r[u] += x * eL;
-                dG_r[u] -= x * kk * eL;
-                dgl_part += x * kk * eL;
-            }
-        }
-        build_tiles(true, true);  // scale M^T has been read
-        __syncthreads();
-        tile_rows(dY, OFF_DOY, 64, 32, 16);
-        {  // the first part of dbeta_t, sum_v R_tv dY_tv (warp t), into the M slot (M is done)
-            const int t = warp;
-            float sr = 0.f;
-            for (int vv = lane; vv < V; vv += 32) sr = fmaf(Rv[t * VM + vv], dY[t * VM + vv], sr);
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) sr += __shfl_xor_sync(0xffffffffu, sr, off);
-            if (lane == 0) Mm[t] = sr;
-        }
-        tc::fence_before_sync();
-        __syncthreads();
-        wait_ld();
-        if (tid == 0) {  // [dQg^T | P^T] = S [dO ; dY]^T
-            tc::fence_after_sync();
-#pragma unroll 1
-            for (int p = 0; p < 2; ++p) {
-#pragma unroll
-                for (int ks = 0; ks < 8; ++ks)
-                    tc::mma_bf16(tm + TM_C, tile::desc_k(sb + OFF_ST + p * ST_LO, 128, ks),
-                                 tile::desc_k(sb + OFF_DOY, 64, ks), ID_K_K64, (p | ks) != 0);
-            }
-            // [dO ; dY] Delta^T (rows 0..63 of D; the M = 128 read's rows 64..127 are ignored)
-#pragma unroll
-            for (int ks = 0; ks < 8; ++ks)
-                tc::mma_bf16(tm + TM_B, tile::desc_k(sb + OFF_DOY, 64, ks),
-                             tile::desc_k(sb + OFF_DLT, 32, ks), ID_K_K32, ks != 0);
-            tc::mma_commit(bar_mma);
-        }
-        {  // dgamma_c partial over the value quarter qtr (times gamma_c), then dS <- gamma dS
-            uint32_t r0[16], r1[16];
-            master_ld(r0, r1);
-            float sacc = 0.f;
-#pragma unroll
-            for (int g = 0; g < 4; ++g) {
-                const uint32_t off = tile::kmaj_off(col, 32 * qtr + 8 * g, 128);
-                float shi[8], slo[8];
-                tile::unpack8(*reinterpret_cast<const uint4*>(sm8 + OFF_ST + off), shi);
-                tile::unpack8(*reinterpret_cast<const uint4*>(sm8 + OFF_ST + ST_LO + off), slo);
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    const float d = __uint_as_float(g < 2 ? r0[8 * g + j] : r1[8 * (g - 2) + j]);
-                    sacc = fmaf(shi[j] + slo[j], d, sacc);
+                        for (int ks = 0; ks < 8; ++ks)
+                            tc::mma_bf16(tm + TM_A, tile::desc_mn(sb + OFF_ST + p * ST_LO, 16384, ks),
+                                         tile::desc_k(sb + OFF_AQK, 32, ks), ID_MN_K32, (p | ks) != 0);
+                    }
+                    tc::mma_commit(bar_mma);
                 }
-            }
-            const float gm = gam[col];
-            red[qtr * KM + col] = sacc * gm;
+                master_decay();  // S <- diag(gamma) S in TMEM, and T, under the R products
+                t_solve();
+                wait_mma();
+                __syncthreads();  // T is published
+                // R = V - Kg S and Delta = T diag(beta) R, value column v = tid on warps 0..3
+                if (warp < 4) {
+                    uint32_t r[16], r2[16];
+                    tc::tmem_ld16(tile::taddr(tm + TM_A, warp, 0), r);
+                    tc::tmem_ld16(tile::taddr(tm + TM_A, warp, 16), r2);
+                    tc::tmem_ld_wait();
+                    float rr[BC];
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-                r0[j] = __float_as_uint(__uint_as_float(r0[j]) * gm);
-                r1[j] = __float_as_uint(__uint_as_float(r1[j]) * gm);
-            }
-            master_st(r0, r1);
-        }
-        // dV = diag(beta) dY
-        for (int idx = tid; idx < BC * V; idx += NT) XT[idx] = bet[idx >> 7] * dY[idx];  // dV, staged
-        wait_mma();
-        if (warp < 2) {  // dM = scale dO Delta^T (i <= t), dB = -dY Delta^T (i < t): rows of D
-            uint32_t r0[16], r1[16];
-            tc::tmem_ld16(tile::taddr(tm + TM_B, warp, 0), r0);
-            tc::tmem_ld16(tile::taddr(tm + TM_B, warp, 16), r1);
-            tc::tmem_ld_wait();
-            float x[BC];
+                    for (int t = 0; t < BC; ++t)
+                        rr[t] = Rv[t * VM + tid] - (__uint_as_float(r[t]) + __uint_as_float(r2[t]));
 #pragma unroll
-            for (int i = 0; i < BC; ++i) x[i] = __uint_as_float(r0[i]) + __uint_as_float(r1[i]);
-            float* dst = lane < 16 ? dM + lane * BC : dB + (lane - 16) * BC;
-            if (warp == 1) {  // the lo rows' share
+                    for (int t = 0; t < BC; ++t) {
+                        float acc = 0.f;
 #pragma unroll
-                for (int i = 0; i < BC; ++i) dst[i] = x[i];
-            }
-            tc::named_sync(1, 64);
-            if (warp == 0) {
-                const int t = lane & 15;
-#pragma unroll
-                for (int i = 0; i < BC; ++i) {
-                    const float v = x[i] + dst[i];
-                    dst[i] = lane < 16 ? (i <= t ? a.scale * v : 0.f) : (i < t ? -v : 0.f);
-                }
-                __syncwarp();
-                // dbeta_t = sum_v R_tv dY_tv + sum_{i<t} A'_ti dB_ti
-                if (lane < cn) {
-                    float sb2 = Mm[lane];
-                    for (int i = 0; i < lane; ++i) sb2 = fmaf(Ap[lane * BC + i], dB[lane * BC + i], sb2);
-                    a.dbeta[bh * T + t0 + lane] = sb2;
-                }
-            }
-        }
-        {  // dQg = scale dO S^T and P = dY S^T, dKg = -diag(beta) P
-            uint32_t rx[4], ry[4], rx2[4], ry2[4];
-            tc::tmem_ld4(tile::taddr(tm + TM_C, warp, 4 * qtr), rx);
-            tc::tmem_ld4(tile::taddr(tm + TM_C, warp, 16 + 4 * qtr), ry);
-            tc::tmem_ld4(tile::taddr(tm + TM_C, warp, 32 + 4 * qtr), rx2);
-            tc::tmem_ld4(tile::taddr(tm + TM_C, warp, 48 + 4 * qtr), ry2);
-            tc::tmem_ld_wait();
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int t = 4 * qtr + u;
-                const float Ga = expf(Gc[ci(col, t)]);
-                const float dqg = a.scale * (__uint_as_float(rx[u]) + __uint_as_float(rx2[u]));
-                const float dkg = -bet[t] * (__uint_as_float(ry[u]) + __uint_as_float(ry2[u]));
-                dq_r[u] += dqg * Ga;
-                dk_r[u] += dkg * Ga;
-                dG_r[u] += (dqg * Qr[ci(col, t)] + dkg * Kr[ci(col, t)]) * Ga;
-            }
-        }
-        tc::fence_proxy_async_smem();  // R, Delta, A', T, M are done: the next chunk's may land
-        tc::fence_before_sync();
-        __syncthreads();
-        if (n > 0) request_rd(n - 1);
-        if (tid == 0) {
-            tc::bulk_store(a.dv + (bh * T + t0) * (size_t)V, XT, (uint32_t)(cn * V * 4));
-            tc::bulk_commit();
-        }
-        if (tid == 0) {  // dS += [scale Qg ; -beta Kg]^T [dO ; dY] (K steps 0, 1 hi; 2, 3 lo)
-            tc::fence_after_sync();
-#pragma unroll
-            for (int p = 0; p < 4; ++p) {
-#pragma unroll
-                for (int ks = 0; ks < 2; ++ks)
-                    tc::mma_bf16(tm + TM_M, tile::desc_mn(sb + OFF_AQK, 8192, 2 * (p >> 1) + ks),
-                                 tile::desc_mn(sb + OFF_DOY, 8192, 2 * (p & 1) + ks), ID_MN_MN128, 1u);
-            }
-            tc::mma_commit(bar_mma);
-        }
-        // pairwise terms of dA' = diag(beta) dB and dM, each pair's decay E = e^{G_s - G_t} (t < s)
-        // taken once: thread (c = col) takes the rows s in {qtr, 7 - qtr, 8 + qtr, 15 - qtr} (30
-        // pairs below the diagonal each) and sums the row terms of s and the column terms of every
-        // t <= s; the sums meet in the state-copy region (free until the next chunk's copy)
-        float* colP = reinterpret_cast<float*>(sm8 + OFF_ST);  // [4][BC][KM]
-        float* rowP = colP + 4 * BC * KM;                       // [BC][2][KM]
-        {
-            const int c = col;
-            float gs[4], ks[4], qs[4], bs[4], dMd[4], rM[4], rA[4];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int s = u == 0 ? qtr : u == 1 ? 7 - qtr : u == 2 ? 8 + qtr : 15 - qtr;
-                gs[u] = Gc[ci(c, s)];
-                ks[u] = Kr[ci(c, s)];
-                qs[u] = Qr[ci(c, s)];
-                bs[u] = bet[s];
-                dMd[u] = dM[s * BC + s];
-                rM[u] = dMd[u] * ks[u];  // the diagonal pair (E = 1, dB[s][s] = 0)
-                rA[u] = 0.f;
-            }
-#pragma unroll
-            for (int t = 0; t < BC; ++t) {
-                const float gt = Gc[ci(c, t)], kt = Kr[ci(c, t)];
-                float cs = 0.f;
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const int s = u == 0 ? qtr : u == 1 ? 7 - qtr : u == 2 ? 8 + qtr : 15 - qtr;
-                    if (t < s) {
-                        const float E = __expf(gs[u] - gt);
-                        const float w = dM[s * BC + t] * E, x = bs[u] * dB[s * BC + t] * E;
-                        rM[u] = fmaf(w, kt, rM[u]);
-                        rA[u] = fmaf(x, kt, rA[u]);
-                        cs = fmaf(w, qs[u], fmaf(x, ks[u], cs));
-                    } else if (t == s) {
-                        cs = fmaf(dMd[u], qs[u], cs);
+                        for (int i = 0; i <= t; ++i) acc = fmaf(Tm[t * BC + i], bet[i] * rr[i], acc);
+                        Rv[t * VM + tid] = rr[t];
+                        Dl[t * VM + tid] = acc;
                     }
                 }
-                colP[(qtr * BC + t) * KM + c] = cs;
-            }
+                tc::fence_proxy_async_smem();
+                __syncthreads();
+                if (tid == 0) {  // R, Delta, A', T and M (contiguous), and g, for phase 2
+                    float* dst = a.rd + (bh * N + n) * (size_t)RD;
+                    tc::bulk_store(dst, Rv, RD_SM * 4);
+                    tc::bulk_store(dst + RD_SM, XT, BC * KM * 4);
+                    tc::bulk_commit();
+                }
+                tile_rows(Dl, OFF_DLT, 32, 16, 0);
+                if (tid == 0) tc::bulk_wait_read_all();  // before the next chunk's v and g land in R, XT
+                tc::fence_before_sync();
+                __syncthreads();
+                if (tid == 0) {  // S += Kt^T Delta (K step 0 the hi rows, 1 the lo rows)
+                    tc::fence_after_sync();
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int s = u == 0 ? qtr : u == 1 ? 7 - qtr : u == 2 ? 8 + qtr : 15 - qtr;
-                rowP[(2 * s) * KM + c] = rM[u];
-                rowP[(2 * s + 1) * KM + c] = rA[u];
-            }
-        }
-        if (tid == 0) tc::bulk_wait_read_all();  // dV has left XT
-        __syncthreads();
-        // this thread's tokens t = 4 qtr + r: dq += rowM, dk += rowA + col, dG += k rowA + q rowM
-        // - k col (col = the column terms of dM and dA', summed over the four row owners)
-#pragma unroll
-        for (int r = 0; r < 4; ++r) {
-            const int t = 4 * qtr + r;
-            const float kt = Kr[ci(col, t)], qt = Qr[ci(col, t)];
-            const float cs = (colP[t * KM + col] + colP[(BC + t) * KM + col]) +
-                             (colP[(2 * BC + t) * KM + col] + colP[(3 * BC + t) * KM + col]);
-            const float rM = rowP[(2 * t) * KM + col], rA = rowP[(2 * t + 1) * KM + col];
-            dq_r[r] += rM;
-            dk_r[r] += rA + cs;
-            dG_r[r] += kt * rA + qt * rM - kt * cs;
-        }
-        // dG exchange ([BC][KM] in XT), the last token's share of d(G_last), reverse cumsum,
-        // gate derivative; dq and dk out
-#pragma unroll
-        for (int r = 0; r < 4; ++r) XT[(4 * qtr + r) * KM + col] = dG_r[r];
-        red[qtr * KM + col] += dgl_part;
-        __syncthreads();
-        float* ost = reinterpret_cast<float*>(sm8 + OFF_ST);  // dq, dk, dz [BC][KM] each, staged
-        {
-            const int c = col;
-            const float dgl = red[c] + red[KM + c] + red[2 * KM + c] + red[3 * KM + c];
-            float suffix = dgl;
-            for (int t = BC - 1; t > 4 * qtr + 3; --t) suffix += XT[t * KM + c];
-#pragma unroll
-            for (int r = 3; r >= 0; --r) {
-                const int t = 4 * qtr + r;
-                suffix += XT[t * KM + c];
-                if (t < cn) {
-                    // g = -e^{A_log} softplus(x) with x = z + dt_bias, and sigmoid(x) =
-                    // 1 - e^{-softplus(x)} = -expm1(g e^{-A_log})
-                    const float g = Gt[ci(c, t)];
-                    const float dz = suffix * (-eA) * -expm1f(g * ieA);
-                    ost[t * KM + c] = dq_r[r];
-                    ost[(BC + t) * KM + c] = dk_r[r];
-                    ost[(2 * BC + t) * KM + c] = dz;
-                    ddt_acc += dz;
-                    dA_acc = fmaf(suffix, g, dA_acc);
+                    for (int p = 0; p < 4; ++p)
+                        tc::mma_bf16(tm + TM_M, tile::desc_mn(sb + OFF_KT, 4096, p >> 1),
+                                     tile::desc_mn(sb + OFF_DLT, 4096, p & 1), ID_MN_MN128, 1u);
+                    tc::mma_commit(bar_mma);
+                    // the state copy is the chunk's checkpoint
+                    tc::bulk_store(a.ckpt + (bh * N + n) * KV, sm8 + OFF_ST, kStateBytes);
+                    tc::bulk_commit();
                 }
             }
-        }
-        tc::fence_proxy_async_smem();
-        __syncthreads();
-        if (tid == 0) {
-            const size_t g0 = (bh * T + t0) * (size_t)K;
-            const uint32_t bytes = (uint32_t)(cn * K * 4);
-            tc::bulk_store(a.dq + g0, ost, bytes);
-            tc::bulk_store(a.dk + g0, ost + BC * KM, bytes);
-            tc::bulk_store(a.dz + g0, ost + 2 * BC * KM, bytes);
-            tc::bulk_commit();
-        }
-    }
-    if (N > 0 && !*s_fail) wait_mma();  // the last dS update
-    if (tid == 0) tc::bulk_wait_all();  // the gradients are in global memory
-
-    // ---- dh0, and the per-(b, h) partial sums of dA_log and ddt_bias
-    if (a.dh0) {
-        uint32_t r0[16], r1[16];
-        master_ld(r0, r1);
-        float* p = a.dh0 + bh * KV + (size_t)col * V + 32 * qtr;
+            if (n_hi > n_lo && !*s_fail) wait_mma();
+            if (seg < sc.nseg - 1) {  // the state for the sequence's next segment
+                uint32_t r0[16], r1[16];
+                master_ld(r0, r1);
+                float* ps = sc.s_hand + bh * KV + (size_t)col * V + 32 * qtr;
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-            p[j] = __uint_as_float(r0[j]);
-            p[16 + j] = __uint_as_float(r1[j]);
+                for (int j = 0; j < 16; ++j) {
+                    ps[j] = __uint_as_float(r0[j]);
+                    ps[16 + j] = __uint_as_float(r1[j]);
+                }
+            }
+            if (tid == 0) tc::bulk_wait_all();  // every checkpoint and record is in global memory
+            // they are read back by bulk copies, and the tiles the next item fills by bulk copy
+            // were last written by generic stores
+            asm volatile("fence.proxy.async.global;" ::: "memory");
+            tc::fence_proxy_async_smem();
+            __threadfence();
+            tc::fence_before_sync();
+            __syncthreads();
+            if (tid == 0) tc::st_release_gpu(sc.flags + 2 * bh, (unsigned)(seg + 1));
+        } else {
+            // ============================================= reverse walk
+            master_init(seg == sc.nseg - 1 ? (a.dhT ? a.dhT + bh * KV : nullptr) : sc.ds_hand + bh * KV);
+            if (n_lo < n_hi) {
+                request(n_hi - 1, true);
+                request_rd(n_hi - 1);
+                prefetch_state(n_hi - 1);
+            }
+            tc::fence_before_sync();
+            __syncthreads();
+            dA_acc = 0.f;
+            ddt_acc = 0.f;
+    for (int n = n_hi - 1; n >= n_lo && !*s_fail; --n) {
+                const int t0 = n * BC, cn = min(BC, T - t0);
+                load_inputs(n, true);
+                prefetch_state(n - 1);
+                if (n < n_hi - 1) wait_mma();  // the previous chunk's dS update has read its tiles
+                build_tiles(true, false);
+                if (tid == 0) tc::bulk_wait_read_all();  // the previous chunk's dq, dk, dz have left
+                __syncthreads();
+                master_copy();  // dS as an operand
+                tc::fence_before_sync();
+                __syncthreads();
+                if (tid == 128) {  // dDelta^T = dS^T Kt^T + dO^T (scale M), dKt^T = dS Delta^T
+                    tc::fence_after_sync();
+#pragma unroll 1
+                    for (int p = 0; p < 2; ++p) {
+#pragma unroll
+                        for (int ks = 0; ks < 8; ++ks)
+                            tc::mma_bf16(tm + TM_A, tile::desc_mn(sb + OFF_ST + p * ST_LO, 16384, ks),
+                                         tile::desc_k(sb + OFF_KT, 32, ks), ID_MN_K32, (p | ks) != 0);
+#pragma unroll
+                        for (int ks = 0; ks < 8; ++ks)
+                            tc::mma_bf16(tm + TM_B, tile::desc_k(sb + OFF_ST + p * ST_LO, 128, ks),
+                                         tile::desc_k(sb + OFF_DLT, 32, ks), ID_K_K32, (p | ks) != 0);
+                        // A = dO^T (rows 0..15 hi, 32..47 lo of [dO ; dY] read MN-major), B = scale M^T
+                        tc::mma_bf16(tm + TM_A, tile::desc_mn(sb + OFF_DOY, 8192, 2 * p),
+                                     tile::desc_k(sb + OFF_AQK, 32, 0), ID_MN_K32, 1u);
+                    }
+                    tc::mma_commit(bar_mma);
+                }
+                wait_mma();
+                if (tid == 0) {  // the state entering this chunk, as phase 1 kept it
+                    tc::mbar_arrive_expect_tx(bar_ld, kStateBytes);
+                    tc::bulk_load(sm8 + OFF_ST, a.ckpt + (bh * N + n) * KV, kStateBytes, bar_ld);
+                }
+                if (warp < 4) {  // dDelta, then dY = T^T dDelta
+                    uint32_t r[16], r2[16];
+                    tc::tmem_ld16(tile::taddr(tm + TM_A, warp, 0), r);
+                    tc::tmem_ld16(tile::taddr(tm + TM_A, warp, 16), r2);
+                    tc::tmem_ld_wait();
+                    float dd[BC];
+#pragma unroll
+                    for (int t = 0; t < BC; ++t) dd[t] = __uint_as_float(r[t]) + __uint_as_float(r2[t]);
+#pragma unroll
+                    for (int i = 0; i < BC; ++i) {
+                        float acc = 0.f;
+#pragma unroll
+                        for (int t = i; t < BC; ++t) acc = fmaf(Tm[t * BC + i], dd[t], acc);
+                        dY[i * VM + tid] = acc;
+                    }
+                }
+                float dq_r[4] = {0.f, 0.f, 0.f, 0.f}, dk_r[4] = {0.f, 0.f, 0.f, 0.f};
+                float dG_r[4] = {0.f, 0.f, 0.f, 0.f};
+                float dgl_part = 0.f;
+                {  // dKt = Delta dS^T: channel col, tokens 4 qtr ..
+                    uint32_t r[4], r2[4];
+                    tc::tmem_ld4(tile::taddr(tm + TM_B, warp, 4 * qtr), r);
+                    tc::tmem_ld4(tile::taddr(tm + TM_B, warp, 16 + 4 * qtr), r2);
+                    tc::tmem_ld_wait();
+                    const float gl = Gc[ci(col, (BC - 1))];
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const int t = 4 * qtr + u;
+                        const float x = __uint_as_float(r[u]) + __uint_as_float(r2[u]);
+                        const float eL = expf(gl - Gc[ci(col, t)]);
+                        const float kk = Kr[ci(col, t)];
+                        dk_r[u] += x * eL;
+                        dG_r[u] -= x * kk * eL;
+                        dgl_part += x * kk * eL;
+                    }
+                }
+                build_tiles(true, true);  // scale M^T has been read
+                __syncthreads();
+                tile_rows(dY, OFF_DOY, 64, 32, 16);
+                {  // the first part of dbeta_t, sum_v R_tv dY_tv (warp t), into the M slot (M is done)
+                    const int t = warp;
+                    float sr = 0.f;
+                    for (int vv = lane; vv < V; vv += 32) sr = fmaf(Rv[t * VM + vv], dY[t * VM + vv], sr);
+#pragma unroll
+                    for (int off = 16; off > 0; off >>= 1) sr += __shfl_xor_sync(0xffffffffu, sr, off);
+                    if (lane == 0) Mm[t] = sr;
+                }
+                tc::fence_before_sync();
+                __syncthreads();
+                wait_ld();
+                if (tid == 0) {  // [dQg^T | P^T] = S [dO ; dY]^T
+                    tc::fence_after_sync();
+#pragma unroll 1
+                    for (int p = 0; p < 2; ++p) {
+#pragma unroll
+                        for (int ks = 0; ks < 8; ++ks)
+                            tc::mma_bf16(tm + TM_C, tile::desc_k(sb + OFF_ST + p * ST_LO, 128, ks),
+                                         tile::desc_k(sb + OFF_DOY, 64, ks), ID_K_K64, (p | ks) != 0);
+                    }
+                    // [dO ; dY] Delta^T (rows 0..63 of D; the M = 128 read's rows 64..127 are ignored)
+#pragma unroll
+                    for (int ks = 0; ks < 8; ++ks)
+                        tc::mma_bf16(tm + TM_B, tile::desc_k(sb + OFF_DOY, 64, ks),
+                                     tile::desc_k(sb + OFF_DLT, 32, ks), ID_K_K32, ks != 0);
+                    tc::mma_commit(bar_mma);
+                }
+                {  // dgamma_c partial over the value quarter qtr (times gamma_c), then dS <- gamma dS
+                    uint32_t r0[16], r1[16];
+                    master_ld(r0, r1);
+                    float sacc = 0.f;
+#pragma unroll
+                    for (int g = 0; g < 4; ++g) {
+                        const uint32_t off = tile::kmaj_off(col, 32 * qtr + 8 * g, 128);
+                        float shi[8], slo[8];
+                        tile::unpack8(*reinterpret_cast<const uint4*>(sm8 + OFF_ST + off), shi);
+                        tile::unpack8(*reinterpret_cast<const uint4*>(sm8 + OFF_ST + ST_LO + off), slo);
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) {
+                            const float d = __uint_as_float(g < 2 ? r0[8 * g + j] : r1[8 * (g - 2) + j]);
+                            sacc = fmaf(shi[j] + slo[j], d, sacc);
+                        }
+                    }
+                    const float gm = gam[col];
+                    red[qtr * KM + col] = sacc * gm;
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        r0[j] = __float_as_uint(__uint_as_float(r0[j]) * gm);
+                        r1[j] = __float_as_uint(__uint_as_float(r1[j]) * gm);
+                    }
+                    master_st(r0, r1);
+                }
+                // dV = diag(beta) dY
+                for (int idx = tid; idx < BC * V; idx += NT) XT[idx] = bet[idx >> 7] * dY[idx];  // dV, staged
+                wait_mma();
+                if (warp < 2) {  // dM = scale dO Delta^T (i <= t), dB = -dY Delta^T (i < t): rows of D
+                    uint32_t r0[16], r1[16];
+                    tc::tmem_ld16(tile::taddr(tm + TM_B, warp, 0), r0);
+                    tc::tmem_ld16(tile::taddr(tm + TM_B, warp, 16), r1);
+                    tc::tmem_ld_wait();
+                    float x[BC];
+#pragma unroll
+                    for (int i = 0; i < BC; ++i) x[i] = __uint_as_float(r0[i]) + __uint_as_float(r1[i]);
+                    float* dst = lane < 16 ? dM + lane * BC : dB + (lane - 16) * BC;
+                    if (warp == 1) {  // the lo rows' share
+#pragma unroll
+                        for (int i = 0; i < BC; ++i) dst[i] = x[i];
+                    }
+                    tc::named_sync(1, 64);
+                    if (warp == 0) {
+                        const int t = lane & 15;
+#pragma unroll
+                        for (int i = 0; i < BC; ++i) {
+                            const float v = x[i] + dst[i];
+                            dst[i] = lane < 16 ? (i <= t ? a.scale * v : 0.f) : (i < t ? -v : 0.f);
+                        }
+                        __syncwarp();
+                        // dbeta_t = sum_v R_tv dY_tv + sum_{i<t} A'_ti dB_ti
+                        if (lane < cn) {
+                            float sb2 = Mm[lane];
+                            for (int i = 0; i < lane; ++i) sb2 = fmaf(Ap[lane * BC + i], dB[lane * BC + i], sb2);
+                            a.dbeta[bh * T + t0 + lane] = sb2;
+                        }
+                    }
+                }
+                {  // dQg = scale dO S^T and P = dY S^T, dKg = -diag(beta) P
+                    uint32_t rx[4], ry[4], rx2[4], ry2[4];
+                    tc::tmem_ld4(tile::taddr(tm + TM_C, warp, 4 * qtr), rx);
+                    tc::tmem_ld4(tile::taddr(tm + TM_C, warp, 16 + 4 * qtr), ry);
+                    tc::tmem_ld4(tile::taddr(tm + TM_C, warp, 32 + 4 * qtr), rx2);
+                    tc::tmem_ld4(tile::taddr(tm + TM_C, warp, 48 + 4 * qtr), ry2);
+                    tc::tmem_ld_wait();
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const int t = 4 * qtr + u;
+                        const float Ga = expf(Gc[ci(col, t)]);
+                        const float dqg = a.scale * (__uint_as_float(rx[u]) + __uint_as_float(rx2[u]));
+                        const float dkg = -bet[t] * (__uint_as_float(ry[u]) + __uint_as_float(ry2[u]));
+                        dq_r[u] += dqg * Ga;
+                        dk_r[u] += dkg * Ga;
+                        dG_r[u] += (dqg * Qr[ci(col, t)] + dkg * Kr[ci(col, t)]) * Ga;
+                    }
+                }
+                tc::fence_proxy_async_smem();  // R, Delta, A', T, M are done: the next chunk's may land
+                tc::fence_before_sync();
+                __syncthreads();
+                if (n > n_lo) request_rd(n - 1);
+                if (tid == 0) {
+                    tc::bulk_store(a.dv + (bh * T + t0) * (size_t)V, XT, (uint32_t)(cn * V * 4));
+                    tc::bulk_commit();
+                }
+                if (tid == 0) {  // dS += [scale Qg ; -beta Kg]^T [dO ; dY] (K steps 0, 1 hi; 2, 3 lo)
+                    tc::fence_after_sync();
+#pragma unroll
+                    for (int p = 0; p < 4; ++p) {
+#pragma unroll
+                        for (int ks = 0; ks < 2; ++ks)
+                            tc::mma_bf16(tm + TM_M, tile::desc_mn(sb + OFF_AQK, 8192, 2 * (p >> 1) + ks),
+                                         tile::desc_mn(sb + OFF_DOY, 8192, 2 * (p & 1) + ks), ID_MN_MN128, 1u);
+                    }
+                    tc::mma_commit(bar_mma);
+                }
+                // pairwise terms of dA' = diag(beta) dB and dM, each pair's decay E = e^{G_s - G_t} (t < s)
+                // taken once: thread (c = col) takes the rows s in {qtr, 7 - qtr, 8 + qtr, 15 - qtr} (30
+                // pairs below the diagonal each) and sums the row terms of s and the column terms of every
+                // t <= s; the sums meet in the state-copy region (free until the next chunk's copy)
+                float* colP = reinterpret_cast<float*>(sm8 + OFF_ST);  // [4][BC][KM]
+                float* rowP = colP + 4 * BC * KM;                       // [BC][2][KM]
+                {
+                    const int c = col;
+                    float gs[4], ks[4], qs[4], bs[4], dMd[4], rM[4], rA[4];
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const int s = u == 0 ? qtr : u == 1 ? 7 - qtr : u == 2 ? 8 + qtr : 15 - qtr;
+                        gs[u] = Gc[ci(c, s)];
+                        ks[u] = Kr[ci(c, s)];
+                        qs[u] = Qr[ci(c, s)];
+                        bs[u] = bet[s];
+                        dMd[u] = dM[s * BC + s];
+                        rM[u] = dMd[u] * ks[u];  // the diagonal pair (E = 1, dB[s][s] = 0)
+                        rA[u] = 0.f;
+                    }
+#pragma unroll
+                    for (int t = 0; t < BC; ++t) {
+                        const float gt = Gc[ci(c, t)], kt = Kr[ci(c, t)];
+                        float cs = 0.f;
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) {
+                            const int s = u == 0 ? qtr : u == 1 ? 7 - qtr : u == 2 ? 8 + qtr : 15 - qtr;
+                            if (t < s) {
+                                const float E = __expf(gs[u] - gt);
+                                const float w = dM[s * BC + t] * E, x = bs[u] * dB[s * BC + t] * E;
+                                rM[u] = fmaf(w, kt, rM[u]);
+                                rA[u] = fmaf(x, kt, rA[u]);
+                                cs = fmaf(w, qs[u], fmaf(x, ks[u], cs));
+                            } else if (t == s) {
+                                cs = fmaf(dMd[u], qs[u], cs);
+                            }
+                        }
+                        colP[(qtr * BC + t) * KM + c] = cs;
+                    }
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const int s = u == 0 ? qtr : u == 1 ? 7 - qtr : u == 2 ? 8 + qtr : 15 - qtr;
+                        rowP[(2 * s) * KM + c] = rM[u];
+                        rowP[(2 * s + 1) * KM + c] = rA[u];
+                    }
+                }
+                if (tid == 0) tc::bulk_wait_read_all();  // dV has left XT
+                __syncthreads();
+                // this thread's tokens t = 4 qtr + r: dq += rowM, dk += rowA + col, dG += k rowA + q rowM
+                // - k col (col = the column terms of dM and dA', summed over the four row owners)
+#pragma unroll
+                for (int r = 0; r < 4; ++r) {
+                    const int t = 4 * qtr + r;
+                    const float kt = Kr[ci(col, t)], qt = Qr[ci(col, t)];
+                    const float cs = (colP[t * KM + col] + colP[(BC + t) * KM + col]) +
+                                     (colP[(2 * BC + t) * KM + col] + colP[(3 * BC + t) * KM + col]);
+                    const float rM = rowP[(2 * t) * KM + col], rA = rowP[(2 * t + 1) * KM + col];
+                    dq_r[r] += rM;
+                    dk_r[r] += rA + cs;
+                    dG_r[r] += kt * rA + qt * rM - kt * cs;
+                }
+                // dG exchange ([BC][KM] in XT), the last token's share of d(G_last), reverse cumsum,
+                // gate derivative; dq and dk out
+#pragma unroll
+                for (int r = 0; r < 4; ++r) XT[(4 * qtr + r) * KM + col] = dG_r[r];
+                red[qtr * KM + col] += dgl_part;
+                __syncthreads();
+                float* ost = reinterpret_cast<float*>(sm8 + OFF_ST);  // dq, dk, dz [BC][KM] each, staged
+                {
+                    const int c = col;
+                    const float dgl = red[c] + red[KM + c] + red[2 * KM + c] + red[3 * KM + c];
+                    float suffix = dgl;
+                    for (int t = BC - 1; t > 4 * qtr + 3; --t) suffix += XT[t * KM + c];
+#pragma unroll
+                    for (int r = 3; r >= 0; --r) {
+                        const int t = 4 * qtr + r;
+                        suffix += XT[t * KM + c];
+                        if (t < cn) {
+                            // g = -e^{A_log} softplus(x) with x = z + dt_bias, and sigmoid(x) =
+                            // 1 - e^{-softplus(x)} = -expm1(g e^{-A_log})
+                            const float g = Gt[ci(c, t)];
+                            const float dz = suffix * (-eA) * -expm1f(g * ieA);
+                            ost[t * KM + c] = dq_r[r];
+                            ost[(BC + t) * KM + c] = dk_r[r];
+                            ost[(2 * BC + t) * KM + c] = dz;
+                            ddt_acc += dz;
+                            dA_acc = fmaf(suffix, g, dA_acc);
+                        }
+                    }
+                }
+                tc::fence_proxy_async_smem();
+                __syncthreads();
+                if (tid == 0) {
+                    const size_t g0 = (bh * T + t0) * (size_t)K;
+                    const uint32_t bytes = (uint32_t)(cn * K * 4);
+                    tc::bulk_store(a.dq + g0, ost, bytes);
+                    tc::bulk_store(a.dk + g0, ost + BC * KM, bytes);
+                    tc::bulk_store(a.dz + g0, ost + 2 * BC * KM, bytes);
+                    tc::bulk_commit();
+                }
+            }
+            if (n_hi > n_lo && !*s_fail) wait_mma();  // the segment's last dS update
+            if (tid == 0) tc::bulk_wait_all();  // the gradients are in global memory
+            // the adjoint for the sequence's earlier segment, or dh0
+            float* dst = seg > 0 ? sc.ds_hand + bh * KV : (a.dh0 ? a.dh0 + bh * KV : nullptr);
+            if (dst) {
+                uint32_t r0[16], r1[16];
+                master_ld(r0, r1);
+                float* pd = dst + (size_t)col * V + 32 * qtr;
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    pd[j] = __uint_as_float(r0[j]);
+                    pd[16 + j] = __uint_as_float(r1[j]);
+                }
+            }
+            // the segment's partial sums of dA_log and ddt_bias
+            const size_t ps = bh * sc.nseg + seg;
+            red[qtr * KM + col] = ddt_acc;
+            for (int off = 16; off > 0; off >>= 1) dA_acc += __shfl_xor_sync(0xffffffffu, dA_acc, off);
+            __syncthreads();
+            if (lane == 0) XT[warp] = dA_acc;
+            if (tid < K) a.ddt_part[ps * K + tid] = red[tid] + red[KM + tid] + red[2 * KM + tid] + red[3 * KM + tid];
+            __syncthreads();
+            if (tid == 0) {
+                float sacc = 0.f;
+                for (int w = 0; w < NT / 32; ++w) sacc += XT[w];
+                a.dA_part[ps] = sacc;
+            }
+            __threadfence();
+            tc::fence_before_sync();
+            __syncthreads();
+            if (tid == 0 && seg > 0) tc::st_release_gpu(sc.flags + 2 * bh + 1, (unsigned)(sc.nseg - seg));
         }
     }
-    red[qtr * KM + col] = ddt_acc;
-    for (int off = 16; off > 0; off >>= 1) dA_acc += __shfl_xor_sync(0xffffffffu, dA_acc, off);
-    __syncthreads();
-    if (lane == 0) XT[warp] = dA_acc;
-    if (tid < K) a.ddt_part[bh * K + tid] = red[tid] + red[KM + tid] + red[2 * KM + tid] + red[3 * KM + tid];
     tc::fence_before_sync();
     __syncthreads();
-    if (tid == 0) {
-        float s = 0.f;
-        for (int w = 0; w < NT / 32; ++w) s += XT[w];
-        a.dA_part[bh] = s;
-    }
     if (warp == 0) {
         tc::fence_after_sync();
         tc::tmem_dealloc(tm, TM_COLS);
     }
 }
 
-// dA_log[h] = sum_b dA_part[b, h];  ddt_bias[h, c] = sum_b ddt_part[b, h, c]
-__global__ void kda_bwd_reduce_kernel(int B, int H, int K, const float* __restrict__ dA_part,
+// dA_log[h] = sum over b and segments of dA_part[b, h, seg];  ddt_bias[h, c] likewise of
+// ddt_part[b, h, seg, c]
+__global__ void kda_bwd_reduce_kernel(int B, int H, int K, int nseg, const float* __restrict__ dA_part,
                                       const float* __restrict__ ddt_part, float* __restrict__ dA_log,
                                       float* __restrict__ ddt_bias) {
     const int i = blockIdx.x * blockDim.x + threadIdx.x;
     if (i < H) {
         float s = 0.f;
-        for (int b = 0; b < B; ++b) s += dA_part[(size_t)b * H + i];
+        for (int b = 0; b < B; ++b)
+            for (int g = 0; g < nseg; ++g) s += dA_part[((size_t)b * H + i) * nseg + g];
         dA_log[i] = s;
     }
     if (i < H * K) {
+        const int hh = i / K, c = i - hh * K;
         float s = 0.f;
-        for (int b = 0; b < B; ++b) s += ddt_part[(size_t)b * H * K + i];
+        for (int b = 0; b < B; ++b)
+            for (int g = 0; g < nseg; ++g) s += ddt_part[(((size_t)b * H + hh) * nseg + g) * K + c];
         ddt_bias[i] = s;
     }
 }
+
+}  // namespace
+
+namespace {
+
+// Makespan, in units of one sequence's backward, of the tensor-core backward's work items taken
+// in kernel order by `nsm` CTAs: the forward walk 0.37 and the reverse walk 0.63 of a sequence
+// (as measured per chunk), each split evenly over nseg segments, plus 0.002 per segment for its
+// handoff (the state or adjoint through global memory, a flag, the first chunk's rows).
+double bwd_makespan(long long BH, int nseg, int nsm) {
+    std::priority_queue<double, std::vector<double>, std::greater<double>> free_at;
+    const long long items = 2 * BH * nseg;
+    for (long long i = 0; i < std::min<long long>(nsm, items); ++i) free_at.push(0.0);
+    const double f = 0.37 / nseg, r = 0.63 / nseg, hand = nseg > 1 ? 0.002 : 0.0;
+    std::vector<double> fdone((size_t)BH, 0.0), rdone((size_t)BH, 0.0);
+    double end = 0.0;
+    auto take = [&](double ready, double dur) {
+        const double t = std::max(free_at.top(), ready) + dur;
+        free_at.pop();
+        free_at.push(t);
+        end = std::max(end, t);
+        return t;
+    };
+    for (int g = 0; g < nseg; ++g)
+        for (long long b = 0; b < BH; ++b) fdone[b] = take(fdone[b], f + hand);
+    for (int g = nseg - 1; g >= 0; --g)
+        for (long long b = 0; b < BH; ++b) rdone[b] = take(g == nseg - 1 ? fdone[b] : rdone[b], r + hand);
+    return end;
+}
+
+// Segments per walk for the tensor-core backward: of 1, 2, 4 and 8 (segments of at least 8
+// chunks), the count whose schedule finishes first by at least 2 %.
+int bwd_segments(long long BH, int N, int nsm) {
+    if (nsm < 1 || BH > 64LL * nsm) return 1;  // many waves: little to gain
+    int best = 1;
+    double bm = bwd_makespan(BH, 1, nsm);
+    for (int g = 2; g <= 8; g *= 2) {
+        if (N < 8 * g) break;
+        const double m = bwd_makespan(BH, g, nsm);
+        if (m < 0.98 * bm) {
+            bm = m;
+            best = g;
+        }
+    }
+    return best;
+}
+
+size_t round256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 }  // namespace
 
@@ -1589,18 +1715,34 @@ cudaError_t launch_chunk_backward(const BwdLaunch& L, cudaStream_t s) {
     const int B = L.B, H = L.H, T = L.T, K = L.K, V = L.V;
     const int N = (T + BC - 1) / BC;
     const size_t BH = (size_t)B * H;
-    const size_t ck_bytes = sizeof(float) * BH * (size_t)N * K * V;
+    const size_t KV = (size_t)K * V;
     const bool fixed = K == 128 && V == 128;
+    int dev = 0, nsm = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    // the tensor-core form's schedule: nseg segments of seg_len chunks per walk
+    const int nseg = fixed ? bwd_segments((long long)BH, N, nsm) : 1;
+    const int seg_len = std::max(1, (N + nseg - 1) / nseg);
+    const long long n_items = 2LL * (long long)BH * nseg;
+    if (fixed && n_items > 0x7fffffffLL) return cudaErrorInvalidValue;
+    // scratch: partial sums, the schedule's counter and flags, the handoffs, the chunk states and
+    // the chunk records
+    const size_t part_bytes = round256(sizeof(float) * BH * (size_t)nseg * (1 + K));
+    const size_t sched_bytes = fixed ? round256(sizeof(unsigned) * (1 + 2 * BH)) : 0;
+    const size_t hand_bytes = nseg > 1 ? 2 * sizeof(float) * BH * KV : 0;
+    const size_t ck_bytes = sizeof(float) * BH * (size_t)N * KV;
     const size_t rd_bytes = sizeof(float) * BH * (size_t)N * (fixed ? (size_t)bwdtc::RD : (size_t)(2 * BC * V));
-    const size_t part_bytes = sizeof(float) * BH * (size_t)(1 + K);
     char* scratch = nullptr;
-    cudaError_t e = scratch_alloc(reinterpret_cast<void**>(&scratch),
-                                    ck_bytes + rd_bytes + part_bytes + 256, s);
+    e = scratch_alloc(reinterpret_cast<void**>(&scratch),
+                      part_bytes + sched_bytes + hand_bytes + ck_bytes + rd_bytes, s);
     if (e != cudaSuccess) return e;
     float* dA_part = reinterpret_cast<float*>(scratch);
-    float* ddt_part = dA_part + BH;
-    float* ckpt = reinterpret_cast<float*>(scratch + ((part_bytes + 255) & ~(size_t)255));
-    float* rd = ckpt + BH * (size_t)N * K * V;
+    float* ddt_part = dA_part + BH * nseg;
+    unsigned* sched = reinterpret_cast<unsigned*>(scratch + part_bytes);
+    float* hand = reinterpret_cast<float*>(scratch + part_bytes + sched_bytes);
+    float* ckpt = reinterpret_cast<float*>(scratch + part_bytes + sched_bytes + hand_bytes);
+    float* rd = ckpt + BH * (size_t)N * KV;
     auto run = [&](auto io_tag, auto kc_tag) -> cudaError_t {
         using IO = decltype(io_tag);
         constexpr int KC = decltype(kc_tag)::value;
@@ -1619,7 +1761,8 @@ cudaError_t launch_chunk_backward(const BwdLaunch& L, cudaStream_t s) {
         kda_chunk_bwd_kernel<IO, KC><<<(unsigned)BH, BNT, BWD_SMEM_BYTES, s>>>(a);
         return cudaGetLastError();
     };
-    // K = V = 128: the tensor-core form (its state copies are the same 64 KB as an fp32 state)
+    // K = V = 128: the tensor-core form (its state copies are the same 64 KB as an fp32 state),
+    // one CTA per SM at most taking the work items of BwdSched
     auto run_tc = [&](auto io_tag) -> cudaError_t {
         using IO = decltype(io_tag);
         BwdArgs<IO> a;
@@ -1634,7 +1777,11 @@ cudaError_t launch_chunk_backward(const BwdLaunch& L, cudaStream_t s) {
         cudaError_t err = cudaFuncSetAttribute(kda_chunk_bwd_tc_kernel<IO>,
                                                cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (err != cudaSuccess) return err;
-        kda_chunk_bwd_tc_kernel<IO><<<(unsigned)BH, bwdtc::NT, smem, s>>>(a);
+        if ((err = cudaMemsetAsync(sched, 0, sched_bytes, s)) != cudaSuccess) return err;
+        const BwdSched sc{nseg, seg_len, (int)n_items, reinterpret_cast<int*>(sched), sched + 1,
+                          nseg > 1 ? hand : nullptr, nseg > 1 ? hand + BH * KV : nullptr};
+        const unsigned grid = (unsigned)std::min<long long>(n_items, nsm);
+        kda_chunk_bwd_tc_kernel<IO><<<grid, bwdtc::NT, smem, s>>>(a, sc);
         return cudaGetLastError();
     };
     using Any = std::integral_constant<int, 0>;
@@ -1644,8 +1791,8 @@ cudaError_t launch_chunk_backward(const BwdLaunch& L, cudaStream_t s) {
         e = fixed ? run_tc(float{}) : run(float{}, Any{});
     if (e == cudaSuccess) {
         const int n = H * K;
-        kda_bwd_reduce_kernel<<<(n + 255) / 256, 256, 0, s>>>(B, H, K, dA_part, ddt_part, L.dA_log,
-                                                               L.ddt_bias);
+        kda_bwd_reduce_kernel<<<(n + 255) / 256, 256, 0, s>>>(B, H, K, nseg, dA_part, ddt_part,
+                                                               L.dA_log, L.ddt_bias);
         e = cudaGetLastError();
         count_launches(2);
     }
