@@ -234,11 +234,16 @@ int kda_fused_recurrent(const kda_dims* dims, kda_dtype io_dtype, const void* q,
  * to float32 accuracy: for K = V = 128 the contractions with the state run on the tensor
  * cores, each float32 operand split into two bf16 halves and all four half products
  * accumulated in float32 (about 2^-15 relative per product term), the state and its gradient
- * kept in float32; other sizes run in float32 on the CUDA cores.  Scratch: (B*H*ceil(T/16)*
- * (K*V + R) + B*H*(K+1)) float32, R = 2*16*V + 3*16*16 + 16*K for K = V = 128 and 2*16*V
- * otherwise (the state entering every 16-token chunk and the chunk's R, Delta and, for
- * K = V = 128, A', T, M and the log decay g), from the scratch pool on `stream`, returned on
- * it; KDA_ERR_NO_MEMORY if that fails.  A bounded wait of the tensor-core form that gives up is reported by
+ * kept in float32; other sizes run in float32 on the CUDA cores.  For K = V = 128 the pass is
+ * one persistent kernel (at most one CTA per SM) that takes each sequence's forward and
+ * reverse walks as work items, split into up to 8 segments per walk when the sequences
+ * outnumber the SMs, the state handed between segments in scratch.  Scratch:
+ * (B*H*ceil(T/16)*(K*V + R) + B*H*S*(K+1)) float32, R = 2*16*V + 3*16*16 + 16*K for
+ * K = V = 128 and 2*16*V otherwise (the state entering every 16-token chunk and the chunk's
+ * R, Delta and, for K = V = 128, A', T, M and the log decay g), S the segments per walk, plus
+ * for K = V = 128 (1 + 2*B*H) uint32 (the schedule's counter and flags, cleared on `stream`)
+ * and, with more than one segment, 2*B*H*K*V float32 (the handoffs); from the scratch pool on
+ * `stream`, returned on it; KDA_ERR_NO_MEMORY if that fails.  A bounded wait of the tensor-core form that gives up is reported by
  * kda_device_status.  Alignment: q, k, v, z, d_o, dq,
  * dk, dv, dz, h0, dhT, dh0 16 bytes; beta, dbeta, dA_log, ddt_bias, A_log, dt_bias their
  * element size.  Two kernels per call (the pass, then the batch sum of dA_log / ddt_bias).

@@ -159,6 +159,31 @@ def test_backward_same_after_scratch_release(kda):
         assert torch.equal(a[n], b[n]), n
 
 
+def test_backward_segmented_schedule_sampled_heads(kda):
+    """B*H = 160 sequences (just over the SM count) of a ragged length: the tensor-core form
+    splits each walk into segments handed between CTAs; two heads of all five sequences are
+    recomputed by the oracle."""
+    inp = inputs.make(5, 32, 300, 128, 128, dtype="bf16", seed=71, h0_std=0.1)
+    adj = inputs.adjoints(inp, seed=72)
+    d = inp.to("cuda")
+    g = kda.chunk_backward(d.q, d.k, d.v, d.z, d.beta, d.A_log, d.dt_bias, adj.d_o.to("cuda"),
+                           inp.scale, h0=d.h0, dhT=adj.dhT.to("cuda"))
+    torch.cuda.synchronize()
+    assert kda.device_status() == 0
+    for h in (3, 17):
+        sl = lambda t: None if t is None else t[:, h:h + 1].contiguous()
+        ref = oracle.backward(sl(inp.q), sl(inp.k), sl(inp.v), sl(inp.z), sl(inp.beta),
+                              inp.A_log[h:h + 1], inp.dt_bias[h:h + 1], inp.scale, sl(inp.h0),
+                              sl(adj.d_o), sl(adj.dhT), threads=8)
+        for n in ("dq", "dk", "dv", "dz", "dbeta", "dh0"):
+            check(n, g[n][:, h:h + 1], ref[n])
+        gate = oracle.gate(sl(inp.z), inp.A_log[h:h + 1], inp.dt_bias[h:h + 1])
+        check_reduced("dA_log", g["dA_log"][h:h + 1], ref["dA_log"],
+                      np.abs(ref["dg"] * gate).sum(axis=(0, 2, 3)))
+        check_reduced("ddt_bias", g["ddt_bias"][h:h + 1], ref["ddt_bias"],
+                      np.abs(ref["dz"]).sum(axis=(0, 2)))
+
+
 def test_backward_full_size_sampled_head(kda):
     """The prefill workload (B8 H32 T4096 K=V=128, bf16) whole on the GPU; head 5 of all eight
     sequences recomputed by the oracle (dA_log[5] and ddt_bias[5] sum exactly those)."""
