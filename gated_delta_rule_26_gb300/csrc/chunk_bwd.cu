@@ -3,11 +3,13 @@
 // backward and its gradients dq, dk, dv, dg, dbeta and the state gradient; each step below
 // is the chain rule applied to the chunked form of the forward).
 //
-// One CTA (512 threads) per (b, h), fp32 throughout, chunks of 16 tokens.  Phase 1 walks
-// the chunks forward and keeps the state entering each chunk, and the chunk's R and Delta,
-// in a scratch buffer.  Phase 2 walks them in reverse with dS, the adjoint of the state
-// leaving the chunk.  Per chunk, with S the state entering it, G the in-chunk cumulative
-// log decay, Gamma = e^G,
+// Two forms walk the same equations in chunks of 16 tokens.  Phase 1 walks a sequence's chunks
+// forward and keeps the state entering each chunk, and the chunk's R and Delta, in a scratch
+// buffer; phase 2 walks them in reverse with dS, the adjoint of the state leaving the chunk.
+// kda_chunk_bwd_kernel (any K, V): one CTA of 512 threads per (b, h), fp32 on the CUDA cores.
+// kda_chunk_bwd_tc_kernel (K = V = 128): the state products on the tensor cores, one
+// persistent CTA per SM taking the walks as work items (its own comment below).  Per chunk,
+// with S the state entering it, G the in-chunk cumulative log decay, Gamma = e^G,
 // gamma = e^{G_last}, Kg = K Gamma, Qg = Q Gamma, Kt = K e^{G_last - G},
 // A'[t,i] = sum_c k_tc k_ic e^{G_tc - G_ic} (i < t), M[t,i] = sum_c q_tc k_ic e^{G_tc - G_ic}
 // (i <= t), T = (I + diag(beta) A')^{-1}, R = V - Kg S, Delta = T diag(beta) R, the forward is
@@ -23,9 +25,10 @@
 //     dS <- diag(gamma) dS + scale Qg^T dO - Kg^T diag(beta) dY,
 // then dg = the reverse in-chunk cumulative sum of dG and the gate's own derivative:
 //     dz = dg (-e^{A_log}) sigmoid(z + dt_bias), ddt_bias += dz, dA_log += dg g.
-// The state and its adjoint sit in shared memory (rows of odd pitch, so that both row and column
-// walks are free of bank conflicts); every per-(token, channel) gradient term is produced by
-// the same thread, so dq, dk and dG accumulate in registers.
+// In the CUDA-core form the state and its adjoint sit in shared memory (rows of odd pitch, so
+// that both row and column walks are free of bank conflicts); in both forms every
+// per-(token, channel) gradient term is produced by the same thread, so dq, dk and dG
+// accumulate in registers.
 #include <algorithm>
 #include <functional>
 #include <queue>
@@ -733,22 +736,24 @@ __global__ void __launch_bounds__(BNT, 1) kda_chunk_bwd_kernel(const BwdArgs<IO>
 
 // ============================================================== tensor-core form, K = V = 128
 // The same chunk walk and adjoint equations, with the state (phase 1) and its adjoint (phase 2)
-// resident in TMEM as fp32 and every contraction with them on tcgen05:
-//   phase 1   R^T = V^T - S^T Kg^T                      M = v, N = 16 tokens, K = c
-//             S <- diag(gamma) S + Kt^T Delta           M = c, N = v, K = 16 tokens
-//   phase 2   dDelta^T = dS^T Kt^T (+ scale M^T dO on the CUDA cores)   M = v, N = 16
-//             dKt^T = dS Delta^T                        M = c, N = 16, K = v
-//             [dQg^T | P^T] = S [dO ; dY]^T             M = c, N = 32 (dQg = scale x)
+// resident in TMEM as fp32 and every contraction with them on tcgen05 (M = 128 over c or v):
+//   phase 1   R^T = V^T - S^T Kg^T                                  N = 16 tokens, K = c
+//             S <- diag(gamma) S + Kt^T Delta                       N = v, K = 16 tokens
+//   phase 2   dDelta^T = dS^T Kt^T + dO^T (scale M)                 N = 16, K = c, then 16
+//             dKt^T = dS Delta^T                                    N = 16, K = v
+//             [dQg^T | P^T] = S [dO ; dY]^T                         N = 32 (dQg = scale x)
+//             [dM | dB] from [dO ; dY] Delta^T                      N = 16, K = v
 //             dS <- diag(gamma) dS + [scale Qg ; -beta Kg]^T [dO ; dY]   K = 32 tokens
 // Every operand x is split into bf16 x_hi = bf16(x) and x_lo = bf16(x - x_hi), within 2^-16 |x|
 // of x together, and a product A B is accumulated in fp32 as the four products of the halves.
-// The small operand's halves are stacked along N ([B_hi ; B_lo], 32 or 64 rows), so each K
-// step of the state is read by two MMAs (A_hi, A_lo) and the epilogue adds the two column
-// blocks; each product term is within about 2 * 2^-16 of its exact value, and the state and
-// its adjoint stay fp32 in TMEM.  The operand copy of the state (hi and lo, 64 KB) is also what phase 1 keeps per
-// chunk: phase 2 brings it back with one bulk copy, already in the operand layout.  The
-// pairwise terms, the T solve, the gate and the per-token outputs are the CUDA-core code of
-// the kernel above.
+// The small operand's halves are stacked along N ([B_hi ; B_lo], doubling the N above), so
+// each K step of the state is read by two MMAs (A_hi, A_lo) and the epilogue adds the two
+// column blocks; each product term is within about 2 * 2^-16 of its exact value, and the state
+// and its adjoint stay fp32 in TMEM.  The operand copy of the state (hi and lo, 64 KB) is also
+// what phase 1 keeps per chunk, with the chunk's R, Delta, A', T, M and g: phase 2 brings them
+// back by bulk copy, the state already in the operand layout.  The pairwise terms, the T
+// solve, the gate and the per-token outputs run on the CUDA cores as in the kernel above.
+// One persistent CTA per SM takes the walks as work items (BwdSched below).
 namespace bwdtc {
 constexpr int NT = 512;
 // shared memory (bytes from a 1024-byte aligned base): tensor-core operand tiles, each a
