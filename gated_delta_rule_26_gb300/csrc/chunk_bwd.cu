@@ -1050,14 +1050,17 @@ __global__ void __launch_bounds__(bwdtc::NT, 1) kda_chunk_bwd_tc_kernel(const Bw
         if (tid < 256) {
             const int t = tid & 15, c0 = 8 * (tid >> 4);
             float kt[8], kg[8], qg[8];
+            // Kt unless this is the [scale Qg ; -beta Kg] pass; K e^G (and Q e^G) unless this is
+            // phase 2's first pass, which writes Kt and scale M^T only
+            const bool need_kt = !aqk, need_kg = !full || aqk;
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
                 const int c = c0 + j;
-                const float g = Gc[ci(c, t)], gl = Gc[ci(c, BC - 1)], kk = Kr[ci(c, t)];
-                const float eg = __expf(g);
-                kt[j] = kk * __expf(gl - g);
+                const float g = Gc[ci(c, t)], kk = Kr[ci(c, t)];
+                kt[j] = need_kt ? kk * __expf(Gc[ci(c, BC - 1)] - g) : 0.f;
+                const float eg = need_kg ? __expf(g) : 0.f;
                 kg[j] = kk * eg;
-                qg[j] = full ? Qr[ci(c, t)] * eg : 0.f;
+                qg[j] = (full && aqk) ? Qr[ci(c, t)] * eg : 0.f;
             }
             uint4 hi, lo;
             if (!aqk) {
