@@ -222,7 +222,8 @@ def fused_recurrent(q, k, v, z, beta, A_log, dt_bias, state: torch.Tensor,
 def chunk_backward(q, k, v, z, beta, A_log, dt_bias, d_o, scale: Optional[float] = None,
                    h0: Optional[torch.Tensor] = None, dhT: Optional[torch.Tensor] = None,
                    want_dh0: bool = True, stream=None) -> dict:
-    """Gradients of the chunked forward's inputs from d_o = dL/do and dhT = dL/dhT.
+    """Gradients of the chunked forward's inputs from d_o = dL/do and dhT = dL/dhT, to float32
+    accuracy (kda_chunk_backward).
 
     Returns float32 tensors: dq, dk, dz (B, H, T, K), dv (B, H, T, V), dbeta (B, H, T),
     dA_log (H), ddt_bias (H, K) and dh0 (B, H, K, V) (None unless ``want_dh0``)."""

@@ -4,7 +4,7 @@ compared with the f64 oracle at the bars of the fixed-case parity tests:
 
 * forward, fp32 I/O: max|x - y| / max|y| <= 1e-4 per tensor;
 * forward, bf16 I/O: ||x - y||_2 / ||y||_2 <= 2e-2 and max|x - y| <= 5e-2;
-* backward (fp32 arithmetic for either I/O dtype): max|x - y| / max|y| <= 1e-4 per gradient,
+* backward (fp32 accuracy for either I/O dtype): max|x - y| / max|y| <= 1e-4 per gradient,
   and for the batch sums dA_log and ddt_bias max|x - y| <= 1e-4 max sum|terms| (the bar of
   tests/test_gpu_backward.py, which states why).
 
