@@ -572,7 +572,10 @@ __device__ __forceinline__ void chunk_loop(const CUtensorMap* tm_q, const CUtens
     bool o_pend = false, s_pend = false;
     size_t o_bh = 0;
     int o_t0 = 0, o_cn = 0;
-    auto o_emit = [&](int tb0, int ntb) {  // this warp: lanes of its quarter, tokens [tb0, tb0 + ntb)
+    // The previous chunk's output, this warp's lanes (columns v = row) and tokens [tb0, tb0 + ntb):
+    // straight to global memory, or (staged) into the free state-copy slot as a bf16 [t][v] tile
+    // that one bulk copy then writes (o_store).
+    auto o_emit = [&](int tb0, int ntb, bool staged) {
 #pragma unroll 1
         for (int tb = tb0; tb < tb0 + ntb; tb += 16) {
             uint32_t dq[16], dp[16];
@@ -582,8 +585,19 @@ __device__ __forceinline__ void chunk_loop(const CUtensorMap* tm_q, const CUtens
             float o[16];
 #pragma unroll
             for (int j = 0; j < 16; ++j) o[j] = scale * (__uint_as_float(dq[j]) + __uint_as_float(dp[j]));
-            store_o16_pairs(out + (o_bh * T + o_t0 + tb) * VD, row, lane, o_cn - tb, o);
+            if (staged) {
+                __nv_bfloat16* st = reinterpret_cast<__nv_bfloat16*>(sm + OFF_S) + tb * VD + row;
+#pragma unroll
+                for (int j = 0; j < 16; ++j) st[j * VD] = __float2bfloat16_rn(o[j]);
+            } else {
+                store_o16_pairs(out + (o_bh * T + o_t0 + tb) * VD, row, lane, o_cn - tb, o);
+            }
         }
+    };
+    // The staged output tile (rows below o_cn) to global memory, by thread 0 after a barrier.
+    auto o_store = [&]() {
+        tc::bulk_store(out + (o_bh * T + o_t0) * VD, sm + OFF_S, (uint32_t)(o_cn * VD * 2));
+        tc::bulk_commit();
     };
     while (cur_it < n_items && !failed) {
         const int it = cur_it;
@@ -809,15 +823,18 @@ __device__ __forceinline__ void chunk_loop(const CUtensorMap* tm_q, const CUtens
                 }
                 // the previous chunk's output (fused kernel): warps 2..15, each its TMEM lane
                 // quarter; quarters 2 and 3 have four such warps (16 tokens each), quarters 0 and
-                // 1 three (32, 16 and 16 tokens)
+                // 1 three (32, 16 and 16 tokens).  Staged in the state-copy slot unless that holds
+                // this chunk's state already (an item change loaded it: s_pend false).
                 if (!kSplit && o_pend) {
                     const int j = warp >> 2;
-                    if (q4 >= 2) o_emit(16 * j, 16);
-                    else o_emit(j == 1 ? 0 : 16 * j, j == 1 ? 32 : 16);
+                    if (q4 >= 2) o_emit(16 * j, 16, s_pend);
+                    else o_emit(j == 1 ? 0 : 16 * j, j == 1 ? 32 : 16, s_pend);
                 }
             }
+            const bool o_staged = !kSplit && o_pend && s_pend;
             o_pend = false;
             KDA_SYNC_FOR_MMA();
+            if (o_staged && tid == 0) o_store();
             // The four merge products.  Each is M = 128 rows of which the first 64 (or 32) are
             // the blocks' rows: the other rows read whatever follows in shared memory and their
             // results are never read.  T (LV_TB) serves as the K-major A operand [t][i] and, read
@@ -986,6 +1003,8 @@ __device__ __forceinline__ void chunk_loop(const CUtensorMap* tm_q, const CUtens
                 }
             }
         }
+        // the staged output has left the state-copy slot that this chunk's copy refills below
+        if (!kSplit && tid == 0) tc::bulk_wait_read_all();
         KDA_SYNC_FOR_MMA();
         // ---------------------------------------------------------------- P5: Q'^T and U'^T
         // (without a next item this fetches the current one again, unused)
@@ -1213,7 +1232,10 @@ __device__ __forceinline__ void chunk_loop(const CUtensorMap* tm_q, const CUtens
 #undef KDA_PAIR_MMA
     if (!kSplit && !failed && o_pend) {  // the last chunk's output: all warps, 16 tokens each
         tc::fence_after_sync();
-        o_emit(16 * part, 16);
+        o_emit(16 * part, 16, true);
+        tc::fence_proxy_async_smem();
+        __syncthreads();
+        if (tid == 0) o_store();
     }
 
     if (failed && tid == 0) {
@@ -1225,7 +1247,7 @@ __device__ __forceinline__ void chunk_loop(const CUtensorMap* tm_q, const CUtens
         if (!kSplit) tc::mbar_wait(&ms.bar_z, ph_z, 200000000ull);
         tc::mbar_wait(&ms.bar_v, ph_v, 200000000ull);
     }
-    if (kSplit && tid == 0) tc::bulk_wait_all();
+    if (tid == 0) tc::bulk_wait_all();
     tc::fence_before_sync();
     __syncthreads();
     if (warp == 0) tc::tmem_dealloc(tmem, 512);
