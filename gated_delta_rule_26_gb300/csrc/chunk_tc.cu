@@ -77,13 +77,13 @@ constexpr uint32_t OFF_MISC = OFF_S + 32768;
 constexpr uint32_t LV_PA = 0;       // level pair A operand, K-major 128 rows (32 KB)   P3
 constexpr uint32_t LV_PB = 32768;   // level pair B operand, K-major 64 rows (16 KB)    P3
 constexpr uint32_t LV_AF = 0;       // A fp32 [t][i] (16 KB, swizzled; diagonal 16 x 16 blocks)  P3-P4
-constexpr uint32_t LV_MB = 16384;   // M bf16 K-major [t][i] (8 KB)          P3-P5
+constexpr uint32_t LV_MB = 16384;   // M bf16 K-major [t][i] (8 KB)          P3-P5 (fused: -C3)
 constexpr uint32_t LV_TB = 24576;   // T bf16 K-major [t][i] (8 KB)          P4-P5
 constexpr uint32_t LV_UT = 0;       // U^T K-major [v][i] (16 KB)            P5
 constexpr uint32_t LV_Z = 49152;    // z tile of the NEXT chunk (16 KB)      P5-P2
 constexpr uint32_t LV_AB = 49152;   // A bf16 K-major [t][i] (8 KB), in the z slot         P3-P4
 constexpr uint32_t LV_MG = 57344;   // merge products P, P' (8 KB), in the z slot            P4
-constexpr uint32_t LV_DELTA = 16384;// Delta^T K-major [v][t] (16 KB)        C2-C3
+constexpr uint32_t LV_DELTA = 32768;// Delta^T K-major [v][t] (16 KB)        C2-C3 (fused; M stays)
 constexpr uint32_t LV_UPS = 32768;  // prep kernel: U'^T staging, K-major [v][t] (16 KB)
 // K~ (K e^{G_last - G}, MN-major [t][c]) lives in the v-tile slot OFF_V from its build (under
 // the second level pair's GEMM in the fused kernel, under the W/U GEMM in the prep kernel) to C3
@@ -578,13 +578,12 @@ __device__ __forceinline__ void chunk_loop(const CUtensorMap* tm_q, const CUtens
     auto o_emit = [&](int tb0, int ntb, bool staged) {
 #pragma unroll 1
         for (int tb = tb0; tb < tb0 + ntb; tb += 16) {
-            uint32_t dq[16], dp[16];
+            uint32_t dq[16];
             tc::tmem_ld16(taddr(tmem, warp, TM_D1 + 64 + tb), dq);
-            tc::tmem_ld16(taddr(tmem, warp, TM_UP + tb), dp);
             tc::tmem_ld_wait();
             float o[16];
 #pragma unroll
-            for (int j = 0; j < 16; ++j) o[j] = scale * (__uint_as_float(dq[j]) + __uint_as_float(dp[j]));
+            for (int j = 0; j < 16; ++j) o[j] = scale * __uint_as_float(dq[j]);
             if (staged) {
                 __nv_bfloat16* st = reinterpret_cast<__nv_bfloat16*>(sm + OFF_S) + tb * VD + row;
 #pragma unroll
@@ -931,6 +930,8 @@ __device__ __forceinline__ void chunk_loop(const CUtensorMap* tm_q, const CUtens
                 store16_k(TB, 32 + lane, 16 * part, 64, f);
             }
         }
+        // the staged output has left the state-copy slot that this chunk's copy refills next
+        if (!kSplit && tid == 0) tc::bulk_wait_read_all();
         KDA_SYNC_FOR_MMA();
         // ---------------------------------------------------------------- P5: W^T, U^T
         if (tid == 0) {
@@ -942,9 +943,10 @@ __device__ __forceinline__ void chunk_loop(const CUtensorMap* tm_q, const CUtens
             }
             tc::mma_commit(&ms.bar_m0);
         }
-        // while it runs: (Q Gamma)^T straight into TMEM (lane c, column t), the starting value
-        // of Q'^T; thread (quarter, part) takes channels 32 quarter + lane, tokens 16 part ..
-        {
+        // while it runs (prep kernel): (Q Gamma)^T straight into TMEM (lane c, column t), the
+        // starting value of Q'^T; thread (quarter, part) takes channels 32 quarter + lane, tokens
+        // 16 part ..
+        if constexpr (kSplit) {
             const int c = row, tb = 16 * part;
             uint32_t r[16];
 #pragma unroll
@@ -956,6 +958,34 @@ __device__ __forceinline__ void chunk_loop(const CUtensorMap* tm_q, const CUtens
             }
             tc::tmem_st16(taddr(tmem, warp, TM_QP + tb), r);
             tc::tmem_st_wait();
+        } else {
+            // (fused kernel) the state the previous chunk's C3 left in TMEM: this chunk's bf16
+            // operand [c][v] for C1 (unless an item change already loaded it), then
+            // S <- diag(Gamma_last) S in place for C3 (the bf16 copy stays unscaled)
+            const int c = row, v0 = 32 * part;
+            uint32_t d0[16], d1[16];
+            tc::tmem_ld16(taddr(tmem, warp, TM_S + v0), d0);
+            tc::tmem_ld16(taddr(tmem, warp, TM_S + v0 + 16), d1);
+            tc::tmem_ld_wait();
+            if (s_pend) {
+                float f[16];
+#pragma unroll
+                for (int j = 0; j < 16; ++j) f[j] = __uint_as_float(d0[j]);
+                store16_mn(sm + OFF_S, c, v0, 16384, f);
+#pragma unroll
+                for (int j = 0; j < 16; ++j) f[j] = __uint_as_float(d1[j]);
+                store16_mn(sm + OFF_S, c, v0 + 16, 16384, f);
+            }
+            const float gl = ex2(G2[63 * KD + gsw(c)]);
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                d0[j] = __float_as_uint(__uint_as_float(d0[j]) * gl);
+                d1[j] = __float_as_uint(__uint_as_float(d1[j]) * gl);
+            }
+            tc::tmem_st16(taddr(tmem, warp, TM_S + v0), d0);
+            tc::tmem_st16(taddr(tmem, warp, TM_S + v0 + 16), d1);
+            tc::tmem_st_wait();
+            s_pend = false;
         }
         // and, in the prep kernel, K~ = K e^{G_last - G} -> the v-tile slot (MN-major [t][c])
         if constexpr (kSplit) {
@@ -973,15 +1003,30 @@ __device__ __forceinline__ void chunk_loop(const CUtensorMap* tm_q, const CUtens
         }
         KDA_WAIT(bar_m0, ph0);
         if (failed) break;
-        // q and k are free: request the next chunk's q, k (and z, which the prep kernel keeps
-        // on the same barrier; the fused kernel requested it after the inverse)
-        if (tid == 0 && has_next) {
-            tc::mbar_arrive_expect_tx(&ms.bar_qkz, (kSplit ? 3u : 2u) * 16384u);
+        // prep kernel: q and k are free: request the next chunk's q, k and z (on one barrier)
+        if (kSplit && tid == 0 && has_next) {
+            tc::mbar_arrive_expect_tx(&ms.bar_qkz, 3u * 16384u);
             tc::tma_load_3d(sm + OFF_Q, tm_q, 0, nt0, (int)nbh, &ms.bar_qkz);
             tc::tma_load_3d(sm + OFF_K, tm_k, 0, nt0, (int)nbh, &ms.bar_qkz);
-            if (kSplit) tc::tma_load_3d(sm + OFF_LVL + LV_Z, tm_z, 0, nt0, (int)nbh, &ms.bar_qkz);
+            tc::tma_load_3d(sm + OFF_LVL + LV_Z, tm_z, 0, nt0, (int)nbh, &ms.bar_qkz);
         }
-        {
+        if (!kSplit && part >= 2) {
+            // (fused kernel) parts 2-3: (Q Gamma)^T row c, tokens 32 (part - 2) .. -> [. | QG^T]
+            // (U stays in TMEM for the carry)
+            const int c = row, tb = 32 * (part - 2);
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                float f[16];
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const int t = tb + 16 * hh + j;
+                    const float qv = __uint_as_float((uint32_t)*reinterpret_cast<const uint16_t*>(
+                                                         sm + OFF_Q + t * 256 + c * 2) << 16);
+                    f[j] = qv * ex2(G2[t * KD + gsw(c)]);
+                }
+                store16_mn(sm + OFF_A1, c, 64 + tb + 16 * hh, 16384, f);
+            }
+        } else {
             // parts 0-1: W^T row c, columns 32*part.. -> [W^T | .]; parts 2-3: U^T row v -> K-major
             const bool is_u = part >= 2;
             const int cb = 32 * (part & 1);
@@ -1003,9 +1048,13 @@ __device__ __forceinline__ void chunk_loop(const CUtensorMap* tm_q, const CUtens
                 }
             }
         }
-        // the staged output has left the state-copy slot that this chunk's copy refills below
-        if (!kSplit && tid == 0) tc::bulk_wait_read_all();
         KDA_SYNC_FOR_MMA();
+        // q is read: request the next chunk's q, k (fused kernel; the prep kernel did above)
+        if (!kSplit && tid == 0 && has_next) {
+            tc::mbar_arrive_expect_tx(&ms.bar_qkz, 2u * 16384u);
+            tc::tma_load_3d(sm + OFF_Q, tm_q, 0, nt0, (int)nbh, &ms.bar_qkz);
+            tc::tma_load_3d(sm + OFF_K, tm_k, 0, nt0, (int)nbh, &ms.bar_qkz);
+        }
         // ---------------------------------------------------------------- P5: Q'^T and U'^T
         // (without a next item this fetches the current one again, unused)
         const GatePre gp = gate_fetch(nbh, nt0 / C);
@@ -1017,7 +1066,7 @@ __device__ __forceinline__ void chunk_loop(const CUtensorMap* tm_q, const CUtens
             tc::tma_store_3d(tm_kt, sm + OFF_V + 8192, 64, 0, it);
             tc::bulk_commit();
         }
-        if (tid == 0) {
+        if (kSplit && tid == 0) {
             // Q'^T = (Q Gamma)^T - W^T M^T  (onto the values stored above);  U'^T = U^T M^T
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks) {
@@ -1027,25 +1076,10 @@ __device__ __forceinline__ void chunk_loop(const CUtensorMap* tm_q, const CUtens
             }
             tc::mma_commit(&ms.bar_m1);
         }
-        // while it runs (fused kernel): the state that the previous chunk's C3 left in TMEM ->
-        // bf16 operand [c][v] for this chunk's C1, unless an item change already loaded it
-        if (!kSplit && s_pend) {
-            const int c = row, v0 = 32 * part;
-            uint32_t d0[16], d1[16];
-            tc::tmem_ld16(taddr(tmem, warp, TM_S + v0), d0);
-            tc::tmem_ld16(taddr(tmem, warp, TM_S + v0 + 16), d1);
-            tc::tmem_ld_wait();
-            float f[16];
-#pragma unroll
-            for (int j = 0; j < 16; ++j) f[j] = __uint_as_float(d0[j]);
-            store16_mn(sm + OFF_S, c, v0, 16384, f);
-#pragma unroll
-            for (int j = 0; j < 16; ++j) f[j] = __uint_as_float(d1[j]);
-            store16_mn(sm + OFF_S, c, v0 + 16, 16384, f);
+        if constexpr (kSplit) {
+            KDA_WAIT(bar_m1, ph1);
+            if (failed) break;
         }
-        s_pend = false;
-        KDA_WAIT(bar_m1, ph1);
-        if (failed) break;
         // ---------------------------------------------------------------- S: operands out | next gate
         if constexpr (kSplit) {
             // Q'^T -> [. | Q'^T], U'^T -> staging (K-major [v][t]), Gamma_last -> global; then
@@ -1086,40 +1120,9 @@ __device__ __forceinline__ void chunk_loop(const CUtensorMap* tm_q, const CUtens
                 }
             }
         } else {
-            {
-                // Q'^T row c, columns 16*part.. -> [. | Q'^T];  S <- diag(Gamma_last) S in TMEM
-                // (this chunk's bf16 copy of S stays unscaled)
-                const int c = row;
-                {
-                    uint32_t d[16];
-                    tc::tmem_ld16(taddr(tmem, warp, TM_QP + 16 * part), d);
-                    tc::tmem_ld_wait();
-                    float f[16];
-    #pragma unroll
-                    for (int j = 0; j < 16; ++j) f[j] = __uint_as_float(d[j]);
-                    store16_mn(sm + OFF_A1, c, 64 + 16 * part, 16384, f);
-                }
-                const float gl = ex2(G2[63 * KD + gsw(c)]);
-                {
-                    const int v0 = 32 * part;
-                    uint32_t d0[16], d1[16];
-                    tc::tmem_ld16(taddr(tmem, warp, TM_S + v0), d0);
-                    tc::tmem_ld16(taddr(tmem, warp, TM_S + v0 + 16), d1);
-                    tc::tmem_ld_wait();
-    #pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        d0[j] = __float_as_uint(__uint_as_float(d0[j]) * gl);
-                        d1[j] = __float_as_uint(__uint_as_float(d1[j]) * gl);
-                    }
-                    tc::tmem_st16(taddr(tmem, warp, TM_S + v0), d0);
-                    tc::tmem_st16(taddr(tmem, warp, TM_S + v0 + 16), d1);
-                }
-                tc::tmem_st_wait();
-            }
-            KDA_SYNC_FOR_MMA();
         // ---------------------------------------------------------------- C: carry | next gate
             if (group_c) {
-                // C1: D[v][t'] = sum_c S[c][v] A1[c][t']  -> (W S)^T for t' < 64, (Q' S)^T above
+                // C1: D[v][t'] = sum_c S[c][v] A1[c][t']  -> (W S)^T for t' < 64, (QG S)^T above
                 if (tid == 0) {
     #pragma unroll
                     for (int ks = 0; ks < 8; ++ks)
@@ -1152,13 +1155,19 @@ __device__ __forceinline__ void chunk_loop(const CUtensorMap* tm_q, const CUtens
                 tc::fence_before_sync();
                 tc::named_sync(1, 256);
                 tc::fence_after_sync();
-                // C3: S += K~^T Delta (K~ in the v-tile slot).  o = scale ((Q' S)^T + U'^T)^T is
-                //     written during the next chunk's inverse (o_emit): its TMEM columns live on
+                // C3: S += K~^T Delta (K~ in the v-tile slot), and (M Delta)^T onto (QG S)^T:
+                //     o = scale (QG S + M Delta) (= scale (Q' S + U') with Q' = QG - M W,
+                //     U' = M U) is written during the next chunk's inverse (o_emit): its TMEM
+                //     columns live on
                 if (tid == 0 && !failed) {
 #pragma unroll
                     for (int ks = 0; ks < 4; ++ks)
                         tc::mma_bf16(tmem + TM_S, desc_mn(sb + OFF_V, 8192, ks),
                                      desc_k(sb + OFF_LVL + LV_DELTA, 128, ks), IDESC_SK, 1u);
+#pragma unroll
+                    for (int ks = 0; ks < 4; ++ks)
+                        tc::mma_bf16(tmem + TM_D1 + 64, desc_k(sb + OFF_LVL + LV_DELTA, 128, ks),
+                                     desc_k(sb + OFF_LVL + LV_MB, 64, ks), IDESC_QU, 1u);
                     tc::mma_commit(&ms.bar_m1);
                 }
                 {
