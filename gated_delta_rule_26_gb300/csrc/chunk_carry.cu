@@ -6,13 +6,15 @@
 // the chunks of a segment in order; per chunk n (kda-adjoint-2026-10-01, section 2, with
 // the read scale of kdafix-2026-10-02 "Fix 2"):
 //
-//   C1  D = S^T [W^T | Q'^T] = [(W S)^T | (Q' S)^T]       tcgen05, S as a bf16 operand
-//   C2  Delta^T = U^T - (W S)^T   and   o = scale ((Q' S)^T + U'^T)^T   -> bf16 to HBM
-//   C3  S <- diag(Gamma_last) S + K~^T Delta,  K~ = K e^{G_last - G}      tcgen05, fp32 in TMEM
+//   C1  D = S^T [W^T | (Q Gamma)^T] = [(W S)^T | (Q Gamma S)^T]   tcgen05, S as a bf16 operand
+//   C2  Delta^T = U^T - (W S)^T
+//   C3  (M Delta)^T onto (Q Gamma S)^T, then o = scale (Q Gamma S + M Delta) -> bf16 to HBM,
+//       and S <- diag(Gamma_last) S + K~^T Delta,  K~ = K e^{G_last - G}  tcgen05, fp32 in TMEM
 //
 // which is the chunked WY form of the per-token recurrence S <- diag(alpha) S,
-// u = v - S^T k, S <- S + beta k u^T, o = S^T (scale q).  The operands of a chunk arrive by
-// TMA into one of two stages while the previous chunk is processed.
+// u = v - S^T k, S <- S + beta k u^T, o = S^T (scale q): with Q' = Q Gamma - M W and U' = M U
+// the output scale (Q' S + U') of the WY form is scale (Q Gamma S + M Delta).  The operands of
+// a chunk arrive by TMA into one of two stages while the previous chunk is processed.
 //
 // The chunk-parallel state scan.  Per chunk the carry is affine in the state,
 //     S_{n+1} = P_n S_n + Z_n,   P_n = diag(Gamma_last) - K~^T W,   Z_n = K~^T U,
@@ -43,26 +45,30 @@ constexpr int NT2 = 512;
 constexpr uint32_t K2_S = 0;            // 32 KB S bf16, MN-major [c][v] (2 atoms)
 constexpr uint32_t K2_DELTA = 32768;    // 16 KB Delta^T, K-major [v][t]
 constexpr uint32_t K2_STAGE = 49152;    // two operand stages
-// one stage: [W^T | Q'^T] (MN-major, 2 atoms), [U^T | U'^T] (K-major [v][t], 2 atoms),
-// K~ (MN-major [t][c], 2 atoms of 8 KB), Gamma_last.
-constexpr uint32_t ST_WQ = 0, ST_UU = 32768, ST_KT = 65536, ST_GL = 81920;
-constexpr uint32_t ST_BYTES = 82944;  // 81 KB, a multiple of 1024
+// one stage: [W^T | (Q Gamma)^T] (MN-major, 2 atoms), U^T (K-major [v][t]), K~ (MN-major
+// [t][c], 2 atoms of 8 KB), M (K-major [t][s]), Gamma_last.
+constexpr uint32_t ST_WQ = 0, ST_UU = 32768, ST_KT = 49152, ST_MM = 65536, ST_GL = 73728;
+constexpr uint32_t ST_BYTES = 74752;  // 73 KB, a multiple of 1024
 constexpr uint32_t ST_TX = (uint32_t)kItemBytes;
 constexpr uint32_t K2_MISC = K2_STAGE + 2 * ST_BYTES;
 
 struct CarryMisc {
     alignas(8) uint64_t bar_full[2];  // TMA: one stage's operands
     uint64_t bar_mma;                 // tensor-core commits (C1, C3 alternate)
+    uint64_t bar_o;                   // tensor-core commit: M Delta (before C3)
     uint32_t tmem_base;
 };
 constexpr uint32_t K2_SMEM = K2_MISC + sizeof(CarryMisc) + 1024;
 static_assert(K2_SMEM <= 227 * 1024, "carry kernel shared memory");
-static_assert(ST_TX <= ST_BYTES && ST_GL + kItemGL <= ST_BYTES, "stage layout");
+static_assert(ST_TX <= ST_BYTES && ST_GL + kItemGL <= ST_BYTES && ST_MM + kItemMM <= ST_GL &&
+                  ST_KT + kItemKT <= ST_MM && ST_UU + kItemUU <= ST_KT,
+              "stage layout");
 
 constexpr uint32_t TM_S2 = 0;    // fp32 state, lanes = key channel c, cols = v   (128)
-constexpr uint32_t TM_D2 = 128;  // S^T [W^T | Q'^T]                              (128)
+constexpr uint32_t TM_D2 = 128;  // S^T [W^T | (Q Gamma)^T], + (M Delta)^T above   (128)
 constexpr uint32_t IDESC_SQ2 = tc::idesc_bf16(128, 128, 1, 1);
 constexpr uint32_t IDESC_SK2 = tc::idesc_bf16(128, 128, 1, 0);
+constexpr uint32_t IDESC_MD2 = tc::idesc_bf16(128, 64, 0, 0);
 
 }  // namespace
 
@@ -70,7 +76,8 @@ __global__ void __launch_bounds__(NT2, 1)
     kda_chunk_carry_kernel(const __grid_constant__ CUtensorMap tm_wq,
                            const __grid_constant__ CUtensorMap tm_uu,
                            const __grid_constant__ CUtensorMap tm_kt,
-                           const float* __restrict__ gl, int T, int seg_n0, int seg_len,
+                           const uint8_t* __restrict__ mm, const float* __restrict__ gl, int T,
+                           int seg_n0, int seg_len,
                            float scale, const float* h_in, __nv_bfloat16* __restrict__ out,
                            float* h_out, CarryGrid cg) {
     extern __shared__ uint8_t smem_raw[];
@@ -100,6 +107,7 @@ __global__ void __launch_bounds__(NT2, 1)
         tc::mbar_init(&ms.bar_full[0], 1);
         tc::mbar_init(&ms.bar_full[1], 1);
         tc::mbar_init(&ms.bar_mma, 1);
+        tc::mbar_init(&ms.bar_o, 1);
         tc::fence_barrier_init();
         tc::tma_prefetch_desc(&tm_wq);
         tc::tma_prefetch_desc(&tm_uu);
@@ -119,15 +127,15 @@ __global__ void __launch_bounds__(NT2, 1)
         uint8_t* st = sm + K2_STAGE + s * ST_BYTES;
         const int item = (int)bh * seg_len + j;
         uint64_t* bar = &ms.bar_full[s];
-        tc::mbar_arrive_expect_tx(bar, zero_u ? ST_TX - 32768u : ST_TX);
+        // the P role carries U = 0; only the plain role makes o (and reads M)
+        tc::mbar_arrive_expect_tx(bar, ST_TX - (zero_u ? (uint32_t)kItemUU : 0u) -
+                                           (write_o ? 0u : (uint32_t)kItemMM));
         tc::tma_load_3d(st + ST_WQ, &tm_wq, 0, 0, 2 * item, bar);
         tc::tma_load_3d(st + ST_WQ + 16384, &tm_wq, 0, 0, 2 * item + 1, bar);
-        if (!zero_u) {  // the P role carries U = 0
-            tc::tma_load_3d(st + ST_UU, &tm_uu, 0, 0, 2 * item, bar);
-            tc::tma_load_3d(st + ST_UU + 16384, &tm_uu, 0, 0, 2 * item + 1, bar);
-        }
+        if (!zero_u) tc::tma_load_3d(st + ST_UU, &tm_uu, 0, 0, item, bar);
         tc::tma_load_3d(st + ST_KT, &tm_kt, 0, 0, item, bar);
         tc::tma_load_3d(st + ST_KT + 8192, &tm_kt, 64, 0, item, bar);
+        if (write_o) tc::bulk_load(st + ST_MM, mm + (size_t)item * kItemMM, (uint32_t)kItemMM, bar);
         tc::bulk_load(st + ST_GL, gl + (size_t)item * KD, (uint32_t)kItemGL, bar);
     };
     if (tid == 0 && j1 > j0) {
@@ -164,7 +172,7 @@ __global__ void __launch_bounds__(NT2, 1)
     __syncthreads();
     tc::fence_after_sync();
 
-    uint32_t ph_full = 0u, ph_m = 0u;  // ph_full: bit s = parity of stage s
+    uint32_t ph_full = 0u, ph_m = 0u, ph_o = 0u;  // ph_full: bit s = parity of stage s
     bool failed = false;
 #define KDA_CARRY_WAIT(bar, ph)                                          \
     do {                                                                 \
@@ -190,7 +198,7 @@ __global__ void __launch_bounds__(NT2, 1)
         // stage s ^ 1 was consumed by the previous chunk: refill it two chunks ahead of that one
         // (a thread of warp 1, so that thread 0 issues C1 at once)
         if (tid == 32 && j >= j0 + 1 && j + 1 < j1) issue(j + 1, s ^ 1);
-        // C1: D[v][t'] = sum_c S[c][v] [W^T | Q'^T][c][t']
+        // C1: D[v][t'] = sum_c S[c][v] [W^T | (Q Gamma)^T][c][t']
         if (tid == 0) {
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks)
@@ -221,22 +229,17 @@ __global__ void __launch_bounds__(NT2, 1)
         KDA_CARRY_WAIT(ms.bar_mma, ph_m);
         if (failed) break;
         // ---------------------------------------------------------------- K2: C2
-        // C2: lane v, tokens 16 part ..: Delta^T -> K-major [v][t] (C3 waits for it); o is
-        // computed and written to HBM after C3 has been issued
+        // C2: lane v, tokens 16 part ..: Delta^T -> K-major [v][t] (C3 waits for it)
         const int v = row, tb = 16 * part;
-        uint32_t dq[16];
-        float up[16];
         {
             uint32_t dw[16];
             tc::tmem_ld16(taddr(tmem, warp, TM_D2 + tb), dw);
-            tc::tmem_ld16(taddr(tmem, warp, TM_D2 + 64 + tb), dq);
             float u[16];
             if (zero_u) {
 #pragma unroll
-                for (int i = 0; i < 16; ++i) u[i] = up[i] = 0.f;
+                for (int i = 0; i < 16; ++i) u[i] = 0.f;
             } else {
                 load16_k(st + ST_UU, v, tb, 128, u);
-                load16_k(st + ST_UU + 16384, v, tb, 128, up);
             }
             tc::tmem_ld_wait();
             float f[16];
@@ -249,21 +252,46 @@ __global__ void __launch_bounds__(NT2, 1)
         __syncthreads();
         tc::fence_after_sync();
         // ---------------------------------------------------------------- K2: C3 + o out
-        // C3: S += K~^T Delta, while this thread's o values go out
+        // (M Delta)^T onto (Q Gamma S)^T (its own commit), then C3: S += K~^T Delta, while
+        // this thread's o values go out
         if (tid == 0) {
+            if (write_o) {
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks)
+                    tc::mma_bf16(tmem + TM_D2 + 64, desc_k(sb + K2_DELTA, 128, ks),
+                                 desc_k(stb + ST_MM, 64, ks), IDESC_MD2, 1u);
+                tc::mma_commit(&ms.bar_o);
+            }
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks)
                 tc::mma_bf16(tmem + TM_S2, desc_mn(stb + ST_KT, 8192, ks),
                              desc_k(sb + K2_DELTA, 128, ks), IDESC_SK2, 1u);
             tc::mma_commit(&ms.bar_mma);
         }
+        bool ok_o = true;
         if (write_o) {
-            float o[16];
+            // every thread waits for M Delta itself (no CTA barrier in between); a timeout,
+            // made warp-uniform for the lane exchange of the stores, skips them and is
+            // counted at the barrier after C3
+            ok_o = __all_sync(0xffffffffu, tc::mbar_wait(&ms.bar_o, ph_o));
+            ph_o ^= 1u;
+            if (ok_o) {
+                tc::fence_after_sync();
+                uint32_t d[16];
+                tc::tmem_ld16(taddr(tmem, warp, TM_D2 + 64 + tb), d);
+                tc::tmem_ld_wait();
+                float o[16];
 #pragma unroll
-            for (int i = 0; i < 16; ++i) o[i] = scale * (__uint_as_float(dq[i]) + up[i]);
-            store_o16_pairs(out + (bh * T + t0 + tb) * VD, v, lane, cn - tb, o);
+                for (int i = 0; i < 16; ++i) o[i] = scale * __uint_as_float(d[i]);
+                store_o16_pairs(out + (bh * T + t0 + tb) * VD, v, lane, cn - tb, o);
+            }
         }
-        KDA_CARRY_WAIT(ms.bar_mma, ph_m);
+        {
+            const bool ok = tid != 0 || tc::mbar_wait(&ms.bar_mma, ph_m);
+            ph_m ^= 1u;
+            if (__syncthreads_or(!ok || !ok_o)) failed = true;
+            tc::fence_after_sync();
+        }
         if (failed) break;
 
         // ---------------------------------------------------------------- K2: S to bf16
@@ -318,6 +346,7 @@ __global__ void __launch_bounds__(NT2, 1)
         atomicExch(&g_kda_carry_timeout, 1);
         // give the tensor-core and TMA work still in flight a bounded chance to finish
         tc::mbar_wait(&ms.bar_mma, ph_m, 200000000ull);
+        if (write_o) tc::mbar_wait(&ms.bar_o, ph_o, 200000000ull);
         tc::mbar_wait(&ms.bar_full[0], ph_full & 1u, 200000000ull);
         tc::mbar_wait(&ms.bar_full[1], (ph_full >> 1) & 1u, 200000000ull);
     }
@@ -326,27 +355,24 @@ __global__ void __launch_bounds__(NT2, 1)
     if (warp == 0) tc::tmem_dealloc(tmem, 256);
 }
 
-cudaError_t launch_chunk_carry(const CUtensorMap& wq, const CUtensorMap& uu, const CUtensorMap& kt,
-                               const float* gl, int BH, int T, int seg_n0, int seg_len,
+cudaError_t launch_chunk_carry(const SplitOperands& ops, int BH, int T, int seg_n0, int seg_len,
                                float scale, const float* h_in, __nv_bfloat16* out, float* h_out,
                                cudaStream_t s) {
-    return launch_chunk_carry_grid(wq, uu, kt, gl, T, seg_n0, seg_len, scale, h_in, out, h_out,
+    return launch_chunk_carry_grid(ops, T, seg_n0, seg_len, scale, h_in, out, h_out,
                                    CarryGrid{BH, 1, seg_len, 0, nullptr, nullptr}, s);
 }
 
-cudaError_t launch_chunk_carry_grid(const CUtensorMap& wq, const CUtensorMap& uu,
-                                    const CUtensorMap& kt, const float* gl, int T, int seg_n0,
-                                    int seg_len, float scale, const float* h_in,
-                                    __nv_bfloat16* out, float* h_out, const CarryGrid& cg,
-                                    cudaStream_t s) {
+cudaError_t launch_chunk_carry_grid(const SplitOperands& ops, int T, int seg_n0, int seg_len,
+                                    float scale, const float* h_in, __nv_bfloat16* out,
+                                    float* h_out, const CarryGrid& cg, cudaStream_t s) {
     cudaError_t err = cudaFuncSetAttribute(kda_chunk_carry_kernel,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            (int)K2_SMEM);
     if (err != cudaSuccess) return err;
     const int grid = cg.BH * cg.nsub * (cg.scan_roles ? 2 : 1);
     if (grid < 1) return cudaSuccess;
-    kda_chunk_carry_kernel<<<grid, NT2, K2_SMEM, s>>>(wq, uu, kt, gl, T, seg_n0, seg_len, scale,
-                                                       h_in, out, h_out, cg);
+    kda_chunk_carry_kernel<<<grid, NT2, K2_SMEM, s>>>(ops.wq, ops.uu, ops.kt, ops.mm, ops.gl, T,
+                                                       seg_n0, seg_len, scale, h_in, out, h_out, cg);
     count_launches(1);
     return cudaGetLastError();
 }

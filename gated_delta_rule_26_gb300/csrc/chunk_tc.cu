@@ -27,17 +27,18 @@
 //   P4  T = (I + A)^{-1}: 16 x 16 diagonal blocks by forward substitution (fp32, CUDA
 //       cores), then the block merges T_21 = -T_22 A_21 T_11 (16 -> 32 for both halves at
 //       once, then 32 -> 64) as four small tcgen05 products with bf16 operands.
-//   P5  W^T = (diag(beta) K Gamma)^T T^T and U^T = (diag(beta) V)^T T^T  (tcgen05), then
-//       Q'^T = (Q Gamma)^T I - W^T M^T (identity and negated-B MMAs) and U'^T = U^T M^T,
-//       so that o = scale (Q' S + U') and Delta = U - W S come from ONE product with S.
-//   C1  D = S^T [W^T | Q'^T] = [(W S)^T | (Q' S)^T]  (M = 128 value channels, N = 128,
-//       K = 128; S as bf16 operand).  Before it, the fp32 state in TMEM is scaled by
-//       Gamma_last (row c by e^{G_last,c}).
-//   C2  from TMEM, one value channel per thread: Delta^T = U^T - (W S)^T; then, while C3
-//       runs, o = scale ((Q' S)^T + U'^T)^T -> bf16 to HBM.
+//   P5  W^T = (diag(beta) K Gamma)^T T^T and U^T = (diag(beta) V)^T T^T  (tcgen05); A1 then
+//       holds [W^T | (Q Gamma)^T], so that Delta = U - W S and the state's share of the
+//       output come from ONE product with S.
+//   C1  D = S^T [W^T | (Q Gamma)^T] = [(W S)^T | (Q Gamma S)^T]  (M = 128 value channels,
+//       N = 128, K = 128; S as bf16 operand).  Before it, the fp32 state in TMEM is scaled
+//       by Gamma_last (row c by e^{G_last,c}).
+//   C2  from TMEM, one value channel per thread: Delta^T = U^T - (W S)^T.
 //   C3  S += (K * e^{G_last - G})^T Delta   accumulated in TMEM in fp32 (the carry with a
 //       single exponential of the log-space difference, kda-adjoint-2026-10-01 sections 2
-//       and 5b), then S -> bf16 operand.
+//       and 5b), and (M Delta)^T onto (Q Gamma S)^T: o = scale (Q Gamma S + M Delta), which
+//       is scale (Q' S + U') with Q' = Q Gamma - M W and U' = M U, goes out as bf16 during
+//       the next chunk's inverse.  The new S becomes the bf16 operand under the next W/U GEMM.
 //
 // Operand layouts are the tcgen05 canonical 128-byte-swizzled layouts, either K-major
 // (rows of 128 B along the contraction) or MN-major (rows of 128 B along M/N); both are
@@ -70,7 +71,7 @@ constexpr uint32_t OFF_G = 65536;               // 32 KB fp32 G[t][c]
 constexpr uint32_t OFF_Q = OFF_G + 32768;       // 16 KB bf16 q tile, row-major [t][c]
 constexpr uint32_t OFF_K = OFF_Q + 16384;       // 16 KB bf16 k tile
 constexpr uint32_t OFF_V = OFF_K + 16384;       // 16 KB bf16 v tile, later T fp32 [t][i]
-constexpr uint32_t OFF_A1 = OFF_V + 16384;      // 32 KB [W^T | Q'^T], MN-major (2 atoms)
+constexpr uint32_t OFF_A1 = OFF_V + 16384;      // 32 KB [W^T | (Q Gamma)^T], MN-major (2 atoms)
 constexpr uint32_t OFF_S = OFF_A1 + 32768;      // 32 KB S bf16, MN-major [c][v] (2 atoms)
 constexpr uint32_t OFF_MISC = OFF_S + 32768;
 // multi-use region, in order of use within a chunk
@@ -84,12 +85,11 @@ constexpr uint32_t LV_Z = 49152;    // z tile of the NEXT chunk (16 KB)      P5-
 constexpr uint32_t LV_AB = 49152;   // A bf16 K-major [t][i] (8 KB), in the z slot         P3-P4
 constexpr uint32_t LV_MG = 57344;   // merge products P, P' (8 KB), in the z slot            P4
 constexpr uint32_t LV_DELTA = 32768;// Delta^T K-major [v][t] (16 KB)        C2-C3 (fused; M stays)
-constexpr uint32_t LV_UPS = 32768;  // prep kernel: U'^T staging, K-major [v][t] (16 KB)
 // K~ (K e^{G_last - G}, MN-major [t][c]) lives in the v-tile slot OFF_V from its build (under
 // the second level pair's GEMM in the fused kernel, under the W/U GEMM in the prep kernel) to C3
 // or its store.
 // beta K Gamma and beta V (MN-major [t][.], 16 KB each) live in the A1 slot from P3 until
-// the W/U GEMM has read them; then A1 takes [W^T | Q'^T].
+// the W/U GEMM has read them; then A1 takes [W^T | (Q Gamma)^T].
 constexpr uint32_t OFF_BKG = OFF_A1, OFF_BV = OFF_A1 + 16384;
 
 struct Misc {
@@ -111,16 +111,14 @@ constexpr uint32_t SMEM_BYTES = OFF_MISC + sizeof(Misc) + 1024;
 constexpr uint32_t TM_S = 0;      // fp32 state, lanes = key channel c, cols = v   (128)
 constexpr uint32_t TM_LVL = 384;  // two level-pair score tiles                    (2 x 64)
 constexpr uint32_t TM_MG = 384;   // the inverse's merge products                  (2 x 64)
-constexpr uint32_t TM_QP = 128;   // Q'^T = (Q Gamma)^T - W^T M^T                  (64)
-constexpr uint32_t TM_UP = 192;   // U'^T = U^T M^T                                (64)
-constexpr uint32_t TM_D1 = 256;   // S^T [W^T | Q'^T]                              (128)
+constexpr uint32_t TM_QG = 128;   // prep kernel: (Q Gamma)^T                      (64)
+constexpr uint32_t TM_D1 = 256;   // S^T [W^T | (Q Gamma)^T], + (M Delta)^T above   (128)
 constexpr uint32_t TM_W = 384;    // W^T                                           (64)
 constexpr uint32_t TM_U = 448;    // U^T                                           (64)
 
 constexpr uint32_t IDESC_LVL = tc::idesc_bf16(128, 64, 0, 0);
 constexpr uint32_t IDESC_WU = tc::idesc_bf16(128, 64, 1, 0);
 constexpr uint32_t IDESC_QU = tc::idesc_bf16(128, 64, 0, 0);
-constexpr uint32_t IDESC_QNEG = tc::idesc_bf16(128, 64, 0, 0) | (1u << 14);  // negate B
 constexpr uint32_t IDESC_SQ = tc::idesc_bf16(128, 128, 1, 1);
 constexpr uint32_t IDESC_SK = tc::idesc_bf16(128, 128, 1, 0);
 constexpr uint32_t IDESC_MG64 = tc::idesc_bf16(128, 64, 0, 1);  // inverse merges
@@ -302,11 +300,13 @@ __device__ __forceinline__ int swz(int t, int i) {
 }
 
 // What the chunk-parallel prep kernel writes per work item (one chunk of one sequence):
-// [W^T | Q'^T] and [U^T | U'^T] through the tile maps tm_wq / tm_uu (z = 2 item, 2 item + 1),
-// K~ through tm_kt (z = item) and Gamma_last (fp32) at gl + 128 item.  Items are the chunks
-// [seg_n0, seg_n0 + seg_len) of every sequence, item = bh * seg_len + (n - seg_n0).
+// [W^T | (Q Gamma)^T] through the tile map tm_wq (z = 2 item, 2 item + 1), U^T through tm_uu
+// and K~ through tm_kt (z = item), the M tile (its shared-memory bytes) at mm + kItemMM item
+// and Gamma_last (fp32) at gl + 128 item.  Items are the chunks [seg_n0, seg_n0 + seg_len) of
+// every sequence, item = bh * seg_len + (n - seg_n0).
 struct PrepSeg {
     int seg_n0, seg_len, items;
+    uint8_t* mm;
     float* gl;
 };
 
@@ -566,7 +566,7 @@ __device__ __forceinline__ void chunk_loop(const CUtensorMap* tm_q, const CUtens
         }                                                                \
     } while (0)
 
-    // The output of a chunk, o = scale ((Q' S)^T + U'^T)^T from TMEM (lanes = v), is written
+    // The output of a chunk, o = scale (Q Gamma S + M Delta) from TMEM (lanes = v), is written
     // during the next chunk's inverse, by warps that the forward substitution leaves idle, or
     // after the loop for the last chunk: (o_bh, o_t0, o_cn) name the chunk whose o is pending.
     bool o_pend = false, s_pend = false;
@@ -915,7 +915,7 @@ __device__ __forceinline__ void chunk_loop(const CUtensorMap* tm_q, const CUtens
             KDA_WAIT(bar_m1, ph1);
             if (failed) break;
             // fused kernel: the z slot is free (A_bf and the merge tiles are read): the next
-            // chunk's z tile, for its gate under this chunk's Q'/U' GEMM
+            // chunk's z tile, for its gate beside this chunk's carry
             if (!kSplit && tid == 0 && has_next) {
                 tc::mbar_arrive_expect_tx(&ms.bar_z, 16384u);
                 tc::tma_load_3d(sm + OFF_LVL + LV_Z, tm_z, 0, nt0, (int)nbh, &ms.bar_z);
@@ -943,9 +943,9 @@ __device__ __forceinline__ void chunk_loop(const CUtensorMap* tm_q, const CUtens
             }
             tc::mma_commit(&ms.bar_m0);
         }
-        // while it runs (prep kernel): (Q Gamma)^T straight into TMEM (lane c, column t), the
-        // starting value of Q'^T; thread (quarter, part) takes channels 32 quarter + lane, tokens
-        // 16 part ..
+        // while it runs (prep kernel): (Q Gamma)^T into TMEM (lane c, column t), for the upper
+        // half of A1 once the GEMM has read it; thread (quarter, part) takes channels
+        // 32 quarter + lane, tokens 16 part ..
         if constexpr (kSplit) {
             const int c = row, tb = 16 * part;
             uint32_t r[16];
@@ -956,7 +956,7 @@ __device__ __forceinline__ void chunk_loop(const CUtensorMap* tm_q, const CUtens
                                                      sm + OFF_Q + t * 256 + c * 2) << 16);
                 r[j] = __float_as_uint(qv * ex2(G2[t * KD + gsw(c)]));
             }
-            tc::tmem_st16(taddr(tmem, warp, TM_QP + tb), r);
+            tc::tmem_st16(taddr(tmem, warp, TM_QG + tb), r);
             tc::tmem_st_wait();
         } else {
             // (fused kernel) the state the previous chunk's C3 left in TMEM: this chunk's bf16
@@ -1047,6 +1047,18 @@ __device__ __forceinline__ void chunk_loop(const CUtensorMap* tm_q, const CUtens
                     store16_k(sm + OFF_LVL + LV_UT, row, cb + 16, 128, f1);
                 }
             }
+            if constexpr (kSplit) {
+                // (prep kernel) (Q Gamma)^T from TMEM, tokens 16 part .. -> [. | QG^T] (the
+                // GEMM is done reading the beta V tile there); Gamma_last -> global
+                uint32_t d[16];
+                tc::tmem_ld16(taddr(tmem, warp, TM_QG + 16 * part), d);
+                tc::tmem_ld_wait();
+                float f[16];
+#pragma unroll
+                for (int j = 0; j < 16; ++j) f[j] = __uint_as_float(d[j]);
+                store16_mn(sm + OFF_A1, row, 64 + 16 * part, 16384, f);
+                if (part == 0) seg.gl[(size_t)it * KD + row] = ex2(G2[63 * KD + gsw(row)]);
+            }
         }
         KDA_SYNC_FOR_MMA();
         // q is read: request the next chunk's q, k (fused kernel; the prep kernel did above)
@@ -1055,64 +1067,26 @@ __device__ __forceinline__ void chunk_loop(const CUtensorMap* tm_q, const CUtens
             tc::tma_load_3d(sm + OFF_Q, tm_q, 0, nt0, (int)nbh, &ms.bar_qkz);
             tc::tma_load_3d(sm + OFF_K, tm_k, 0, nt0, (int)nbh, &ms.bar_qkz);
         }
-        // ---------------------------------------------------------------- P5: Q'^T and U'^T
         // (without a next item this fetches the current one again, unused)
         const GatePre gp = gate_fetch(nbh, nt0 / C);
+        // ---------------------------------------------------------------- S: operands out | next gate
         if (kSplit && tid == 0) {
-            // W^T, U^T and K~ are final: out while the next GEMM reads them too
+            // [W^T | (Q Gamma)^T], U^T, K~ and M are final: out while every warp computes the
+            // next item's gate
             tc::tma_store_3d(tm_wq, sm + OFF_A1, 0, 0, 2 * it);
-            tc::tma_store_3d(tm_uu, sm + OFF_LVL + LV_UT, 0, 0, 2 * it);
+            tc::tma_store_3d(tm_wq, sm + OFF_A1 + 16384, 0, 0, 2 * it + 1);
+            tc::tma_store_3d(tm_uu, sm + OFF_LVL + LV_UT, 0, 0, it);
             tc::tma_store_3d(tm_kt, sm + OFF_V, 0, 0, it);
             tc::tma_store_3d(tm_kt, sm + OFF_V + 8192, 64, 0, it);
+            tc::bulk_store(seg.mm + (size_t)it * kItemMM, sm + OFF_LVL + LV_MB, (uint32_t)kItemMM);
             tc::bulk_commit();
         }
-        if (kSplit && tid == 0) {
-            // Q'^T = (Q Gamma)^T - W^T M^T  (onto the values stored above);  U'^T = U^T M^T
-#pragma unroll
-            for (int ks = 0; ks < 4; ++ks) {
-                const uint64_t b = desc_k(sb + OFF_LVL + LV_MB, 64, ks);
-                tc::mma_bf16(tmem + TM_QP, desc_k(sb + OFF_A1, 128, ks), b, IDESC_QNEG, 1u);
-                tc::mma_bf16(tmem + TM_UP, desc_k(sb + OFF_LVL + LV_UT, 128, ks), b, IDESC_QU, ks > 0);
-            }
-            tc::mma_commit(&ms.bar_m1);
-        }
         if constexpr (kSplit) {
-            KDA_WAIT(bar_m1, ph1);
-            if (failed) break;
-        }
-        // ---------------------------------------------------------------- S: operands out | next gate
-        if constexpr (kSplit) {
-            // Q'^T -> [. | Q'^T], U'^T -> staging (K-major [v][t]), Gamma_last -> global; then
-            // these two tiles go out by TMA (W^T, U^T and K~ left before the last GEMM) while
-            // every warp computes the next item's gate.
-            {
-                uint32_t d[16], e[16];
-                tc::tmem_ld16(taddr(tmem, warp, TM_QP + 16 * part), d);
-                tc::tmem_ld16(taddr(tmem, warp, TM_UP + 16 * part), e);
-                tc::tmem_ld_wait();
-                float f[16];
-#pragma unroll
-                for (int j = 0; j < 16; ++j) f[j] = __uint_as_float(d[j]);
-                store16_mn(sm + OFF_A1, row, 64 + 16 * part, 16384, f);
-#pragma unroll
-                for (int j = 0; j < 16; ++j) f[j] = __uint_as_float(e[j]);
-                store16_k(sm + OFF_LVL + LV_UPS, row, 16 * part, 128, f);
-                if (part == 0) seg.gl[(size_t)it * KD + row] = ex2(G2[63 * KD + gsw(row)]);
-            }
-            tc::fence_proxy_async_smem();
-            tc::fence_before_sync();
-            __syncthreads();
-            tc::fence_after_sync();
-            if (tid == 0) {
-                tc::tma_store_3d(tm_wq, sm + OFF_A1 + 16384, 0, 0, 2 * it + 1);
-                tc::tma_store_3d(tm_uu, sm + OFF_LVL + LV_UPS, 0, 0, 2 * it + 1);
-                tc::bulk_commit();
-            }
         // ---------------------------------------------------------------- S2: next gate
             if (has_next && !gate_scan(nbh, nt0 / C, gp)) failed = true;
         // ---------------------------------------------------------------- S3: drain stores
             if (tid == 0) {
-                // the stores have read the v-tile slot, A1 and the staging: refill / reuse them
+                // the stores have read the v-tile slot, A1, U^T and M: refill / reuse them
                 tc::bulk_wait_read_all();
                 if (has_next) {
                     tc::mbar_arrive_expect_tx(&ms.bar_v, 16384u);
@@ -1176,7 +1150,7 @@ __device__ __forceinline__ void chunk_loop(const CUtensorMap* tm_q, const CUtens
                     tc::fence_after_sync();
                 }
                 // K~ is consumed: request the next chunk's v tile into its slot.  The new state's
-                // bf16 copy for the next C1 is made under the next chunk's Q'/U' GEMM (s_pend).
+                // bf16 copy for the next C1 is made under the next chunk's W/U GEMM (s_pend).
                 if (tid == 0 && has_next && !failed) {
                     tc::mbar_arrive_expect_tx(&ms.bar_v, 16384u);
                     tc::tma_load_3d(sm + OFF_V, tm_v, 0, nt0, (int)nbh, &ms.bar_v);
@@ -1274,7 +1248,7 @@ __global__ void __launch_bounds__(NT, 1)
                         const float* __restrict__ h0, __nv_bfloat16* __restrict__ out,
                         float* __restrict__ hT, FusedSched fs) {
     chunk_loop<false>(&tm_q, &tm_k, &tm_v, &tm_z, nullptr, nullptr, nullptr, H, T, beta, A_log,
-                      dt_bias, scale, h0, out, hT, PrepSeg{0, 1, 0, nullptr}, fs);
+                      dt_bias, scale, h0, out, hT, PrepSeg{0, 1, 0, nullptr, nullptr}, fs);
 }
 
 // The chunk-parallel half of the split forward: every chunk of the segment is one work
@@ -1429,6 +1403,19 @@ int split_segment_len(const ChunkArgs& a, size_t bytes) {
     return (int)len;
 }
 
+// The per-chunk operands of up to items_max items, carved from p (kItemBytes items_max bytes):
+// the [W^T | (Q Gamma)^T], U^T, K~ and M tiles, then Gamma_last, each array item after item.
+bool split_operands(uint8_t* p, size_t items_max, SplitOperands* o) {
+    uint8_t* wq = p;
+    uint8_t* uu = wq + items_max * kItemWQ;
+    uint8_t* kt = uu + items_max * kItemUU;
+    o->mm = kt + items_max * kItemKT;
+    o->gl = reinterpret_cast<float*>(o->mm + items_max * kItemMM);
+    return make_map3(&o->wq, wq, 64, 128, 2 * items_max, 128, 16384, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) &&
+           make_map3(&o->uu, uu, 64, 128, items_max, 128, 16384, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) &&
+           make_map3(&o->kt, kt, 128, 64, items_max, 256, 16384, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
 // The split forward with caller-provided scratch: per segment of chunks, the prep kernel
 // (all chunks of all sequences in parallel) then the carry kernel (one CTA per sequence).
 cudaError_t run_chunk_split(const ChunkArgs& a, cudaStream_t s, void* scratch, size_t bytes) {
@@ -1437,17 +1424,10 @@ cudaError_t run_chunk_split(const ChunkArgs& a, cudaStream_t s, void* scratch, s
     if (seg_len < 1) return cudaErrorMemoryAllocation;
     const size_t items_max = (size_t)BH * seg_len;
     uint8_t* p = static_cast<uint8_t*>(scratch);
-    uint8_t* wq = p;
-    uint8_t* uu = wq + items_max * kItemWQ;
-    uint8_t* kt = uu + items_max * kItemUU;
-    float* gl = reinterpret_cast<float*>(kt + items_max * kItemKT);
     float* state = reinterpret_cast<float*>(p + round_up(items_max * kItemBytes, 256));
-    CUtensorMap m[4], mwq, muu, mkt;
-    if (!make_input_maps(a, m) ||
-        !make_map3(&mwq, wq, 64, 128, 2 * items_max, 128, 16384, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_map3(&muu, uu, 64, 128, 2 * items_max, 128, 16384, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_map3(&mkt, kt, 128, 64, items_max, 256, 16384, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B))
-        return cudaErrorInvalidValue;
+    CUtensorMap m[4];
+    SplitOperands ops;
+    if (!make_input_maps(a, m) || !split_operands(p, items_max, &ops)) return cudaErrorInvalidValue;
     cudaError_t err = cudaFuncSetAttribute(kda_chunk_prep_kernel,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            (int)SMEM_BYTES);
@@ -1457,12 +1437,12 @@ cudaError_t run_chunk_split(const ChunkArgs& a, cudaStream_t s, void* scratch, s
     for (int n0 = 0; n0 < N; n0 += seg_len) {
         const int len = min(seg_len, N - n0), items = BH * len;
         kda_chunk_prep_kernel<<<min(items, nsm), NT, SMEM_BYTES, s>>>(
-            m[0], m[1], m[2], m[3], mwq, muu, mkt, a.H, a.T, (const __nv_bfloat16*)a.beta, a.A_log,
-            a.dt_bias, PrepSeg{n0, len, items, gl});
+            m[0], m[1], m[2], m[3], ops.wq, ops.uu, ops.kt, a.H, a.T, (const __nv_bfloat16*)a.beta,
+            a.A_log, a.dt_bias, PrepSeg{n0, len, items, ops.mm, ops.gl});
         count_launches(1);
         if ((err = cudaGetLastError()) != cudaSuccess) return err;
-        err = launch_chunk_carry(mwq, muu, mkt, gl, BH, a.T, n0, len, a.scale,
-                                 n0 == 0 ? a.h0 : h_state, (__nv_bfloat16*)a.out, h_state, s);
+        err = launch_chunk_carry(ops, BH, a.T, n0, len, a.scale, n0 == 0 ? a.h0 : h_state,
+                                 (__nv_bfloat16*)a.out, h_state, s);
         if (err != cudaSuccess) return err;
     }
     return cudaSuccess;
@@ -1506,19 +1486,12 @@ cudaError_t overlap_res_ready(OverlapRes& r) {
 cudaError_t run_chunk_split_overlap(const ChunkArgs& a, cudaStream_t s, void* scratch, int seg_len) {
     const int N = (a.T + C - 1) / C, BH = a.B * a.H, nsm = sm_count();
     const size_t items_max = (size_t)BH * seg_len, buf_bytes = round_up(items_max * kItemBytes, 256);
-    CUtensorMap m[4], mwq[2], muu[2], mkt[2];
-    float* gl[2];
+    CUtensorMap m[4];
+    SplitOperands ops[2];
     if (!make_input_maps(a, m)) return cudaErrorInvalidValue;
-    for (int b = 0; b < 2; ++b) {
-        uint8_t* wq = static_cast<uint8_t*>(scratch) + b * buf_bytes;
-        uint8_t* uu = wq + items_max * kItemWQ;
-        uint8_t* kt = uu + items_max * kItemUU;
-        gl[b] = reinterpret_cast<float*>(kt + items_max * kItemKT);
-        if (!make_map3(&mwq[b], wq, 64, 128, 2 * items_max, 128, 16384, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
-            !make_map3(&muu[b], uu, 64, 128, 2 * items_max, 128, 16384, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
-            !make_map3(&mkt[b], kt, 128, 64, items_max, 256, 16384, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B))
+    for (int b = 0; b < 2; ++b)
+        if (!split_operands(static_cast<uint8_t*>(scratch) + b * buf_bytes, items_max, &ops[b]))
             return cudaErrorInvalidValue;
-    }
     float* h_state = a.hT ? a.hT
                           : reinterpret_cast<float*>(static_cast<uint8_t*>(scratch) + 2 * buf_bytes);
     cudaError_t err = cudaFuncSetAttribute(kda_chunk_prep_kernel,
@@ -1541,14 +1514,15 @@ cudaError_t run_chunk_split_overlap(const ChunkArgs& a, cudaStream_t s, void* sc
         if (i >= 2) err = cudaStreamWaitEvent(s, ev[3 + b], 0);  // carry of segment i - 2 read buffer b
         if (err != cudaSuccess) break;
         kda_chunk_prep_kernel<<<min(items, prep_grid), NT, SMEM_BYTES, s>>>(
-            m[0], m[1], m[2], m[3], mwq[b], muu[b], mkt[b], a.H, a.T, (const __nv_bfloat16*)a.beta,
-            a.A_log, a.dt_bias, PrepSeg{n0, len, items, gl[b]});
+            m[0], m[1], m[2], m[3], ops[b].wq, ops[b].uu, ops[b].kt, a.H, a.T,
+            (const __nv_bfloat16*)a.beta, a.A_log, a.dt_bias,
+            PrepSeg{n0, len, items, ops[b].mm, ops[b].gl});
         count_launches(1);
         if ((err = cudaGetLastError()) != cudaSuccess) break;
         if ((err = cudaEventRecord(ev[1 + b], s)) != cudaSuccess) break;
         if ((err = cudaStreamWaitEvent(s2, ev[1 + b], 0)) != cudaSuccess) break;
-        err = launch_chunk_carry(mwq[b], muu[b], mkt[b], gl[b], BH, a.T, n0, len, a.scale,
-                                 n0 == 0 ? a.h0 : h_state, (__nv_bfloat16*)a.out, h_state, s2);
+        err = launch_chunk_carry(ops[b], BH, a.T, n0, len, a.scale, n0 == 0 ? a.h0 : h_state,
+                                 (__nv_bfloat16*)a.out, h_state, s2);
         if (err == cudaSuccess) err = cudaEventRecord(ev[3 + b], s2);
     }
     // join: `s` continues only after the last carry (also on failure, so nothing is left behind)
@@ -1558,17 +1532,61 @@ cudaError_t run_chunk_split_overlap(const ChunkArgs& a, cudaStream_t s, void* sc
     return err != cudaSuccess ? err : jerr;
 }
 
+// Makespan of the overlapped split form (run_chunk_split_overlap) with segments of L chunks,
+// the last one shorter, in units of one prep item (one chunk of one sequence on one CTA):
+// the prep of a segment of l chunks takes ceil(BH l / G) items on its G CTAs, the carry
+// about a fifth of an item per chunk, and each launch about half an item more (measured on
+// the B1 H32 and B1 H4 T65536 workloads, about 12 us per item); the prep of segment i starts
+// after the prep of i - 1 and the carry of i - 2 (whose operand buffer it overwrites), the
+// carry of i after the prep of i and the carry of i - 1.
+double overlap_makespan(long long BH, long long N, long long G, long long L) {
+    double p_end = 0.0, c_prev = 0.0, c_prev2 = 0.0;
+    for (long long n0 = 0; n0 < N; n0 += L) {
+        const long long l = std::min(L, N - n0);
+        p_end = std::max(p_end, c_prev2) + (double)((BH * l + G - 1) / G) + 0.5;
+        const double c = std::max(p_end, c_prev) + 0.2 * (double)l + 0.5;
+        c_prev2 = c_prev;
+        c_prev = c;
+    }
+    return c_prev;
+}
+
+// Chunks per segment of the overlapped split form: the length of at most `cap` (what the
+// scratch allows) with the smallest makespan above, among lengths that make at most 64
+// segments of at least 16 chunks where possible.  Lengths whose BH L items fill the prep's
+// waves, and a short last segment (a short last carry), come out ahead.  The last answer is
+// kept, for calls that repeat a shape.
+int overlap_segment_len(long long BH, long long N, long long G, int cap) {
+    static thread_local long long last[5] = {-1, -1, -1, -1, -1};
+    if (last[0] == BH && last[1] == N && last[2] == G && last[3] == cap) return (int)last[4];
+    const long long lo = std::max(16LL, (N + 63) / 64), hi = std::min((long long)cap, N);
+    long long best_len = hi;
+    if (hi > lo) {
+        const long long step = std::max(1LL, (hi - lo) / 256);
+        double best = overlap_makespan(BH, N, G, hi);
+        for (long long L = lo; L < hi; L += step) {
+            const double m = overlap_makespan(BH, N, G, L);
+            if (m < best - 1e-9) {
+                best = m;
+                best_len = L;
+            }
+        }
+    }
+    last[0] = BH; last[1] = N; last[2] = G; last[3] = cap; last[4] = best_len;
+    return (int)best_len;
+}
+
 // Scratch of the allocating split forward: at most this much per call (longer inputs are
 // processed in segments of chunks).
 constexpr size_t kSplitScratchCap = size_t(1) << 30;
 
 cudaError_t launch_chunk_split(const ChunkArgs& a, cudaStream_t s) {
     const int N = (a.T + C - 1) / C, BH = a.B * a.H, nsm = sm_count();
-    // few sequences: two operand buffers and the carry beside the next segment's prep, in up to
-    // sixteen segments of at least 16 chunks (a short last carry)
+    // few sequences: two operand buffers and the carry beside the next segment's prep, in
+    // segments of the length that the makespan model above picks
     if (2 * BH <= nsm && N >= 4) {
-        int seg_len = split_segment_len(a, kSplitScratchCap / 2);  // per buffer (and the state)
-        seg_len = min(seg_len, max(16, (N + 15) / 16));
+        const int cap = split_segment_len(a, kSplitScratchCap / 2);  // per buffer (and the state)
+        const int seg_len = cap >= 1 ? overlap_segment_len(BH, N, nsm - BH, cap) : 0;
         if (seg_len >= 1) {
             const size_t items_max = (size_t)BH * seg_len;
             const size_t bytes = 2 * round_up(items_max * kItemBytes, 256) +
@@ -1703,10 +1721,6 @@ cudaError_t run_chunk_split_scan(const ChunkArgs& a, cudaStream_t s, void* scrat
     const int N = (a.T + C - 1) / C, BH = a.B * a.H, nsm = sm_count();
     const size_t KVB = (size_t)KD * VD * sizeof(float), items_max = (size_t)BH * seg_len;
     uint8_t* p = static_cast<uint8_t*>(scratch);
-    uint8_t* wq = p;
-    uint8_t* uu = wq + items_max * kItemWQ;
-    uint8_t* kt = uu + items_max * kItemUU;
-    float* gl = reinterpret_cast<float*>(kt + items_max * kItemKT);
     size_t off = round_up(items_max * kItemBytes, 256);
     float* state = a.hT;
     if (!state) {
@@ -1717,12 +1731,9 @@ cudaError_t run_chunk_split_scan(const ChunkArgs& a, cudaStream_t s, void* scrat
     float* zbuf = reinterpret_cast<float*>(p + off);
     float* pbuf = reinterpret_cast<float*>(p + off + map_bytes);
     float* sbuf = reinterpret_cast<float*>(p + off + 2 * map_bytes);
-    CUtensorMap m[4], mwq, muu, mkt;
-    if (!make_input_maps(a, m) ||
-        !make_map3(&mwq, wq, 64, 128, 2 * items_max, 128, 16384, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_map3(&muu, uu, 64, 128, 2 * items_max, 128, 16384, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_map3(&mkt, kt, 128, 64, items_max, 256, 16384, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B))
-        return cudaErrorInvalidValue;
+    CUtensorMap m[4];
+    SplitOperands ops;
+    if (!make_input_maps(a, m) || !split_operands(p, items_max, &ops)) return cudaErrorInvalidValue;
     cudaError_t err = cudaFuncSetAttribute(kda_chunk_prep_kernel,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            (int)SMEM_BYTES);
@@ -1730,8 +1741,8 @@ cudaError_t run_chunk_split_scan(const ChunkArgs& a, cudaStream_t s, void* scrat
     for (int n0 = 0; n0 < N; n0 += seg_len) {
         const int len = std::min(seg_len, N - n0), items = BH * len;
         kda_chunk_prep_kernel<<<std::min(items, nsm), NT, SMEM_BYTES, s>>>(
-            m[0], m[1], m[2], m[3], mwq, muu, mkt, a.H, a.T, (const __nv_bfloat16*)a.beta, a.A_log,
-            a.dt_bias, PrepSeg{n0, len, items, gl});
+            m[0], m[1], m[2], m[3], ops.wq, ops.uu, ops.kt, a.H, a.T, (const __nv_bfloat16*)a.beta,
+            a.A_log, a.dt_bias, PrepSeg{n0, len, items, ops.mm, ops.gl});
         count_launches(1);
         if ((err = cudaGetLastError()) != cudaSuccess) return err;
         const float* h_seg = n0 == 0 ? a.h0 : state;  // entering state of the segment (may be null)
@@ -1739,18 +1750,17 @@ cudaError_t run_chunk_split_scan(const ChunkArgs& a, cudaStream_t s, void* scrat
         const int sub_len = (len + nsub - 1) / nsub;
         nsub = (len + sub_len - 1) / sub_len;
         if (nsub < 2) {
-            err = launch_chunk_carry(mwq, muu, mkt, gl, BH, a.T, n0, len, a.scale, h_seg,
-                                     (__nv_bfloat16*)a.out, state, s);
+            err = launch_chunk_carry(ops, BH, a.T, n0, len, a.scale, h_seg, (__nv_bfloat16*)a.out,
+                                     state, s);
         } else {
             // the maps (P, Z) of sub-segments 0 .. nsub - 2, their entering states in order,
             // then the plain carry of every sub-segment from its entering state
-            err = launch_chunk_carry_grid(mwq, muu, mkt, gl, a.T, n0, len, a.scale, nullptr, nullptr,
-                                          nullptr, CarryGrid{BH, nsub - 1, sub_len, 1, zbuf, pbuf}, s);
+            err = launch_chunk_carry_grid(ops, a.T, n0, len, a.scale, nullptr, nullptr, nullptr,
+                                          CarryGrid{BH, nsub - 1, sub_len, 1, zbuf, pbuf}, s);
             if (err == cudaSuccess) err = launch_carry_combine(BH, nsub, h_seg, pbuf, zbuf, sbuf, s);
             if (err == cudaSuccess)
-                err = launch_chunk_carry_grid(mwq, muu, mkt, gl, a.T, n0, len, a.scale, sbuf,
-                                              (__nv_bfloat16*)a.out, state,
-                                              CarryGrid{BH, nsub, sub_len, 0, nullptr, nullptr}, s);
+                err = launch_chunk_carry_grid(ops, a.T, n0, len, a.scale, sbuf, (__nv_bfloat16*)a.out,
+                                              state, CarryGrid{BH, nsub, sub_len, 0, nullptr, nullptr}, s);
         }
         if (err != cudaSuccess) return err;
     }

@@ -15,13 +15,14 @@ namespace tile {
 constexpr int C = 64, KD = 128, VD = 128;
 
 // Bytes of the per-chunk operands the chunk-parallel prep kernel hands to the carry kernel:
-// [W^T | Q'^T] and [U^T | U'^T] (2 x 128 x 64 bf16 each), K~ (64 x 128 bf16), Gamma_last
-// (128 fp32).
+// [W^T | (Q Gamma)^T] (2 x 128 x 64 bf16), U^T (128 x 64 bf16), K~ (64 x 128 bf16), M (64 x 64
+// bf16, the masked Q K products of the output) and Gamma_last (128 fp32).
 constexpr size_t kItemWQ = 2u * 128u * 64u * 2u;
-constexpr size_t kItemUU = 2u * 128u * 64u * 2u;
+constexpr size_t kItemUU = 128u * 64u * 2u;
 constexpr size_t kItemKT = 64u * 128u * 2u;
+constexpr size_t kItemMM = 64u * 64u * 2u;
 constexpr size_t kItemGL = 128u * 4u;
-constexpr size_t kItemBytes = kItemWQ + kItemUU + kItemKT + kItemGL;
+constexpr size_t kItemBytes = kItemWQ + kItemUU + kItemKT + kItemMM + kItemGL;
 
 __device__ __forceinline__ float ex2(float x) {
     float y;
@@ -120,24 +121,30 @@ __device__ __forceinline__ uint32_t taddr(uint32_t base, int warp, uint32_t col)
 
 }  // namespace tile
 
-// Host side of the split forward's carry kernel (chunk_carry.cu).  CarryGrid: BH sequences x
-// nsub sub-segments of sub_len chunks per launch; with scan_roles the grid doubles into the
-// scan's Z role (from S = 0, into zbuf) and P role (from the identity with U = 0, into pbuf),
-// both laid out [sub][bh][K][V] and neither writing o.
+// Host side of the split forward's carry kernel (chunk_carry.cu).  SplitOperands: where the
+// prep kernel left a segment's per-chunk operands (item = bh * seg_len + chunk of the
+// segment): tile maps of [W^T | (Q Gamma)^T] (z = 2 item, 2 item + 1), U^T (z = item) and K~
+// (z = item), and the M tiles (mm + kItemMM item, the bytes of the shared-memory tile) and
+// Gamma_last (gl + 128 item) as plain arrays.
+struct SplitOperands {
+    CUtensorMap wq, uu, kt;
+    uint8_t* mm;
+    float* gl;
+};
+// CarryGrid: BH sequences x nsub sub-segments of sub_len chunks per launch; with scan_roles
+// the grid doubles into the scan's Z role (from S = 0, into zbuf) and P role (from the
+// identity with U = 0, into pbuf), both laid out [sub][bh][K][V] and neither writing o.
 struct CarryGrid {
     int BH, nsub, sub_len, scan_roles;
     float* zbuf;
     float* pbuf;
 };
-cudaError_t launch_chunk_carry_grid(const CUtensorMap& wq, const CUtensorMap& uu,
-                                    const CUtensorMap& kt, const float* gl, int T, int seg_n0,
-                                    int seg_len, float scale, const float* h_in,
-                                    __nv_bfloat16* out, float* h_out, const CarryGrid& cg,
-                                    cudaStream_t s);
+cudaError_t launch_chunk_carry_grid(const SplitOperands& ops, int T, int seg_n0, int seg_len,
+                                    float scale, const float* h_in, __nv_bfloat16* out,
+                                    float* h_out, const CarryGrid& cg, cudaStream_t s);
 cudaError_t launch_carry_combine(int BH, int nsub, const float* h_in, const float* pbuf,
                                  const float* zbuf, float* s_out, cudaStream_t s);
-cudaError_t launch_chunk_carry(const CUtensorMap& wq, const CUtensorMap& uu, const CUtensorMap& kt,
-                               const float* gl, int BH, int T, int seg_n0, int seg_len,
+cudaError_t launch_chunk_carry(const SplitOperands& ops, int BH, int T, int seg_n0, int seg_len,
                                float scale, const float* h_in, __nv_bfloat16* out, float* h_out,
                                cudaStream_t s);
 cudaError_t read_and_clear_carry_timeout(int* timed_out);

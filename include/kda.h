@@ -114,10 +114,11 @@ int kda_chunk_forward(const kda_dims* dims, kda_dtype io_dtype, const void* q, c
  *           returned on `stream` by the call (KDA_ERR_NO_MEMORY if the allocation fails).
  *   split : the chunk-parallel WY form of kda-adjoint-2026-10-01 section 2 as two kernels.  A
  *           prep kernel spreads every chunk of every sequence over the GPU and writes, per
- *           chunk, the state-independent operands ([W^T | Q'^T], [U^T | U'^T], K~ =
- *           K e^{G_last - G} in bf16, Gamma_last in fp32: 82,432 bytes); a carry kernel then
- *           walks the chunks of each sequence with the fp32 state on chip (S <- Gamma_last S
- *           + K~^T (U - W S), o = scale (Q' S + U')).  Suited to few, long sequences, where
+ *           chunk, the state-independent operands ([W^T | (Q Gamma)^T], U^T, K~ =
+ *           K e^{G_last - G} and the masked score matrix M in bf16, Gamma_last in fp32:
+ *           74,240 bytes); a carry kernel then walks the chunks of each sequence with the
+ *           fp32 state on chip (Delta = U - W S, S <- Gamma_last S + K~^T Delta,
+ *           o = scale (Q Gamma S + M Delta)).  Suited to few, long sequences, where
  *           the fused form leaves most of the GPU idle.  The operands live in scratch that
  *           the call takes from the scratch pool and returns on `stream` (at most 1 GiB:
  *           longer inputs run as consecutive segments of chunks); KDA_ERR_NO_MEMORY if that
@@ -173,9 +174,9 @@ int kda_chunk_forward_scan(const kda_dims* dims, kda_dtype io_dtype, const void*
  * array of 64 MiB, reserved on each GPU where this entry point is called (the library loads
  * its module lazily), until the process exits.  The call makes no cudaMalloc /
  * cudaMallocAsync / cudaFree call of its own.
- *   Limit: one chunk of every sequence must fit, i.e. B*H*82,432 bytes, plus B*H*65,536 when
- *   hT is NULL (the carried state then lives in the array too), at most 64 MiB: B*H <= 814
- *   with hT, B*H <= 453 without.  Larger B*H returns KDA_ERR_UNSUPPORTED and launches
+ *   Limit: one chunk of every sequence must fit, i.e. B*H*74,240 bytes, plus B*H*65,536 when
+ *   hT is NULL (the carried state then lives in the array too), at most 64 MiB: B*H <= 903
+ *   with hT, B*H <= 480 without.  Larger B*H returns KDA_ERR_UNSUPPORTED and launches
  *   nothing.  Any T: longer inputs run as consecutive segments of chunks.
  *   Shapes as kda_chunk_forward_split (bf16, K = V = 128, chunk 64, T >= 1).
  *   The first call on each device looks up the array's device address (cudaGetSymbolAddress

@@ -163,7 +163,7 @@ def test_scale_enters_only_the_read_on_gpu(kda):
     (1, 2, 200, 22, None),              # ragged last chunk
     (2, 3, 700, 23, math.log(16.0)),    # the strongest decay of the workloads' range
     (1, 4, 1024, 24, None),             # sixteen chunks of carry
-    (1, 4, 4096, 30, None),             # split form: four segments on two operand buffers
+    (1, 4, 4096, 30, None),             # split form: two segments on two operand buffers
 ])
 def test_tensor_core_forms_match_oracle(kda, form, B, H, T, seed, A_log_value):
     inp = inputs.make(B, H, T, 128, 128, chunk=64, dtype="bf16", seed=seed, dt_std=0.1,
@@ -249,9 +249,10 @@ def test_split_form_run_twice_is_bitwise_identical(kda):
 
 @pytest.mark.parametrize("T", [260, 2100])
 def test_split_form_without_final_state(kda, T):
-    # no hT: the carry keeps its state in the call's own scratch (T = 2100: three segments
-    # of the overlapped form, the state passing between them through that scratch)
-    inp = inputs.make(1, 3, T, 128, 128, chunk=64, dtype="bf16", seed=27, h0_std=0.1)
+    # no hT: the carry keeps its state in the call's own scratch (T = 2100: two segments of
+    # the overlapped form, 17 + 16 chunks, the state passing between them through that
+    # scratch)
+    inp = inputs.make(1, 6, T, 128, 128, chunk=64, dtype="bf16", seed=27, h0_std=0.1)
     run_and_compare(kda, inp, want_hT=False, form="split")
 
 

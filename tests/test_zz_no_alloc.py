@@ -31,9 +31,9 @@ def _close_to_oracle(got, ref):
 @pytest.mark.gpu
 def test_noalloc_split_matches_allocating_split_twice(kda):
     # B*H = 32, T = 4000: 63 chunks (the last one ragged), h0 given.  One chunk of all 32
-    # sequences takes 2.6 MB of the 64 MiB array, so the no-alloc call runs segments of 25,
-    # 25 and 13 chunks; the allocating call cuts elsewhere (segments of 16 chunks, the carry
-    # on a second stream).  Both run the same per-chunk arithmetic and hand the fp32 state
+    # sequences takes 2.4 MB of the 64 MiB array, so the no-alloc call runs segments of 28,
+    # 28 and 7 chunks (27, 27 and 9 without hT); the allocating call cuts elsewhere (segments
+    # of 18, 18, 18 and 9 chunks on two operand buffers, the carry on a second stream).  Both run the same per-chunk arithmetic and hand the fp32 state
     # across every cut unrounded, so their outputs are identical bit for bit.
     inp = inputs.make(2, 16, 4000, 128, 128, chunk=64, dtype="bf16", seed=31, h0_std=0.1,
                       dt_std=0.1)
@@ -79,6 +79,6 @@ def test_noalloc_rejects_too_many_sequences_on_the_host():
     p = vp(1 << 20)
     call = lambda B, H, hT: f(ctypes.byref(_Dims(B, H, 64, 128, 128)), 1, p, p, p, p, p, p, p,
                               0.1, None, 64, p, hT, None)
-    assert call(1, 815, p) == -2       # 815 * 82,432 bytes > 64 MiB
-    assert call(5, 163, p) == -2       # the same count as B * H
-    assert call(1, 454, None) == -2    # without hT: 454 * (82,432 + 65,536) > 64 MiB
+    assert call(1, 904, p) == -2       # 904 * 74,240 bytes > 64 MiB
+    assert call(8, 113, p) == -2       # the same count as B * H
+    assert call(1, 481, None) == -2    # without hT: 481 * (74,240 + 65,536) > 64 MiB
