@@ -1010,24 +1010,29 @@ __device__ __forceinline__ void chunk_loop(const CUtensorMap* tm_q, const CUtens
             tc::tma_load_3d(sm + OFF_K, tm_k, 0, nt0, (int)nbh, &ms.bar_qkz);
             tc::tma_load_3d(sm + OFF_LVL + LV_Z, tm_z, 0, nt0, (int)nbh, &ms.bar_qkz);
         }
-        if (!kSplit && part >= 2) {
-            // (fused kernel) parts 2-3: (Q Gamma)^T row c, tokens 32 (part - 2) .. -> [. | QG^T]
-            // (U stays in TMEM for the carry)
-            const int c = row, tb = 32 * (part - 2);
+        if constexpr (!kSplit) {
+            // (fused kernel) every part: W^T row c, columns 16 part .. -> [W^T | .] and
+            // (Q Gamma)^T row c, tokens 16 part .. -> [. | QG^T], the latter while the TMEM load
+            // of the former is in flight (U stays in TMEM for the carry)
+            const int c = row, tb = 16 * part;
+            uint32_t d[16];
+            tc::tmem_ld16(taddr(tmem, warp, TM_W + tb), d);
+            float f[16];
 #pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-                float f[16];
-#pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    const int t = tb + 16 * hh + j;
-                    const float qv = __uint_as_float((uint32_t)*reinterpret_cast<const uint16_t*>(
-                                                         sm + OFF_Q + t * 256 + c * 2) << 16);
-                    f[j] = qv * ex2(G2[t * KD + gsw(c)]);
-                }
-                store16_mn(sm + OFF_A1, c, 64 + tb + 16 * hh, 16384, f);
+            for (int j = 0; j < 16; ++j) {
+                const int t = tb + j;
+                const float qv = __uint_as_float((uint32_t)*reinterpret_cast<const uint16_t*>(
+                                                     sm + OFF_Q + t * 256 + c * 2) << 16);
+                f[j] = qv * ex2(G2[t * KD + gsw(c)]);
             }
+            store16_mn(sm + OFF_A1, c, 64 + tb, 16384, f);
+            tc::tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < 16; ++j) f[j] = __uint_as_float(d[j]);
+            store16_mn(sm + OFF_A1, c, tb, 16384, f);
         } else {
-            // parts 0-1: W^T row c, columns 32*part.. -> [W^T | .]; parts 2-3: U^T row v -> K-major
+            // (prep kernel) parts 0-1: W^T row c, columns 32*part.. -> [W^T | .]; parts 2-3:
+            // U^T row v -> K-major
             const bool is_u = part >= 2;
             const int cb = 32 * (part & 1);
             const uint32_t col = is_u ? TM_U : TM_W;
