@@ -82,6 +82,8 @@ constexpr uint32_t LV_MB = 16384;   // M bf16 K-major [t][i] (8 KB)          P3-
 constexpr uint32_t LV_TB = 24576;   // T bf16 K-major [t][i] (8 KB)          P4-P5
 constexpr uint32_t LV_UT = 0;       // U^T K-major [v][i] (16 KB)            P5
 constexpr uint32_t LV_Z = 49152;    // z tile of the NEXT chunk (16 KB)      P5-P2
+constexpr uint32_t LV_GTF = 0;      // fused kernel: the gate's warp totals (8 KB)   carry window
+constexpr uint32_t LV_GTP = 32768;  // prep kernel: the gate's warp totals (8 KB)    S2
 constexpr uint32_t LV_AB = 49152;   // A bf16 K-major [t][i] (8 KB), in the z slot         P3-P4
 constexpr uint32_t LV_MG = 57344;   // merge products P, P' (8 KB), in the z slot            P4
 constexpr uint32_t LV_DELTA = 32768;// Delta^T K-major [v][t] (16 KB)        C2-C3 (fused; M stays)
@@ -222,14 +224,22 @@ __device__ __forceinline__ void diag_block(const uint8_t* sm, Misc& ms, int b4, 
         for (int j = 0; j < 4; ++j) s = fmaf(qq[a][j], kk[a][j], s);
         v[6 + a] = s;
     }
+    // e^{G_a - G_b} = the product of e^{G_s - G_{s-1}} over b < s <= a: three ex2 per channel
+    float ee[4][4];
 #pragma unroll
     for (int a = 1; a < 4; ++a)
 #pragma unroll
-        for (int b = 0; b < a; ++b) {
+        for (int j = 0; j < 4; ++j) ee[a][j] = ex2(gg[a][j] - gg[a - 1][j]);
+#pragma unroll
+    for (int a = 1; a < 4; ++a) {
+        float dec[4] = {1.f, 1.f, 1.f, 1.f};
+#pragma unroll
+        for (int b = a - 1; b >= 0; --b) {
             float sa = 0.f, sq = 0.f;
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-                const float kd = kk[b][j] * ex2(gg[a][j] - gg[b][j]);
+                dec[j] *= ee[b + 1][j];
+                const float kd = kk[b][j] * dec[j];
                 sa = fmaf(kk[a][j], kd, sa);
                 sq = fmaf(qq[a][j], kd, sq);
             }
@@ -237,6 +247,7 @@ __device__ __forceinline__ void diag_block(const uint8_t* sm, Misc& ms, int b4, 
             v[idx] = sa;
             v[10 + idx] = sq;
         }
+    }
     // reduce-scatter over the 32 lanes: lane l ends with value (l >> 1) & 15
 #pragma unroll
     for (int off = 16, w = 8; off >= 2; off >>= 1, w >>= 1) {
@@ -509,15 +520,16 @@ __device__ __forceinline__ void chunk_loop(const CUtensorMap* tm_q, const CUtens
             a3 = fmaf(m, softplus_fast(x3), a3);
             acc[a] = make_float4(a0, a1, a2, a3);
         }
-        // the warp total goes to its last row for the later warps to read
-        *reinterpret_cast<float4*>(G2 + (TPW * wg + TPW - 1) * KD + g4off(lane)) = acc[TPW - 1];
+        // the warp total goes to the totals slot for the later warps to read (a slot of its
+        // own, so the rows below need no second barrier)
+        float4* gtot = reinterpret_cast<float4*>(sm + OFF_LVL + (kSplit ? LV_GTP : LV_GTF));
+        gtot[wg * 32 + lane] = acc[TPW - 1];
         tc::named_sync(2, 32 * GW);
         float4 pre = make_float4(0.f, 0.f, 0.f, 0.f);
         for (int g = 0; g < wg; ++g) {
-            const float4 x = *reinterpret_cast<const float4*>(G2 + (TPW * g + TPW - 1) * KD + g4off(lane));
+            const float4 x = gtot[g * 32 + lane];
             pre.x += x.x; pre.y += x.y; pre.z += x.z; pre.w += x.w;
         }
-        tc::named_sync(2, 32 * GW);
 #pragma unroll
         for (int a = 0; a < TPW; ++a)
             *reinterpret_cast<float4*>(G2 + (TPW * wg + a) * KD + g4off(lane)) =
@@ -757,6 +769,7 @@ __device__ __forceinline__ void chunk_loop(const CUtensorMap* tm_q, const CUtens
         }
         tc::fence_before_sync();
         __syncthreads();
+        bool mok = true;  // this thread's waits for the inverse's merge products
         // ---------------------------------------------------------------- P4: T = (I + A)^{-1}
         // T (bf16, K-major [t][i] in LV_TB) blockwise: the four 16 x 16 diagonal blocks by
         // forward substitution on CUDA cores in fp32 (from the diagonal blocks of Af), then the
@@ -772,22 +785,26 @@ __device__ __forceinline__ void chunk_loop(const CUtensorMap* tm_q, const CUtens
                 const int R = tid >> 4, j = tid & 15;
                 const float* Ab = Af + 16 * R * 64;  // rows 16R.. ; (row & 15) == t
                 float x[16];
-                // the strictly lower part of this block row by row, in 16-byte groups, all
-                // issued before the substitution starts (36 groups)
-                float4 ar[16][4];
-#pragma unroll
-                for (int t = 1; t < 16; ++t)
+                // the strictly lower part of this block row by row, in 16-byte groups, each
+                // row's loads issued two rows ahead of its use (three rows in registers)
+                float4 ar[3][4];
+                auto load_row = [&](int t) {
 #pragma unroll
                     for (int q = 0; q < 4; ++q)
                         if (4 * q < t)
-                            ar[t][q] = *reinterpret_cast<const float4*>(Ab + t * 64 + (((4 * R + q) ^ t) << 2));
+                            ar[t % 3][q] = *reinterpret_cast<const float4*>(Ab + t * 64 + (((4 * R + q) ^ t) << 2));
+                };
+                load_row(1);
+                load_row(2);
 #pragma unroll
                 for (int t = 0; t < 16; ++t) {
+                    if (t >= 1 && t + 2 < 16) load_row(t + 2);
                     float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
                         if (4 * q < t) {
-                            const float av[4] = {ar[t][q].x, ar[t][q].y, ar[t][q].z, ar[t][q].w};
+                            const float4 aq = ar[t % 3][q];
+                            const float av[4] = {aq.x, aq.y, aq.z, aq.w};
 #pragma unroll
                             for (int u = 0; u < 4; ++u)
                                 if (4 * q + u < t) acc[u] = fmaf(av[u], x[4 * q + u], acc[u]);
@@ -799,6 +816,8 @@ __device__ __forceinline__ void chunk_loop(const CUtensorMap* tm_q, const CUtens
                 for (int t = 0; t < 16; ++t)
                     *reinterpret_cast<__nv_bfloat16*>(TB + kmaj_off(16 * R + t, 16 * R + j, 64)) =
                         __float2bfloat16_rn(x[t]);
+                // then the previous chunk's output, tokens 0..15 of this warp's lane quarter
+                if (!kSplit && o_pend) o_emit(0, 16, s_pend);
             } else {
                 // 16-byte groups of zeros: the 12 off-diagonal 16 x 16 blocks of T, and the 10
                 // blocks of A_bf on or above the diagonal (the merges read them against zeros
@@ -820,14 +839,13 @@ __device__ __forceinline__ void chunk_loop(const CUtensorMap* tm_q, const CUtens
                     *reinterpret_cast<uint4*>(base + kmaj_off(16 * R + (q >> 1), 16 * Cb + 8 * (q & 1), 64)) =
                         make_uint4(0u, 0u, 0u, 0u);
                 }
-                // the previous chunk's output (fused kernel): warps 2..15, each its TMEM lane
-                // quarter; quarters 2 and 3 have four such warps (16 tokens each), quarters 0 and
-                // 1 three (32, 16 and 16 tokens).  Staged in the state-copy slot unless that holds
-                // this chunk's state already (an item change loaded it: s_pend false).
+                // the previous chunk's output (fused kernel): 16 tokens per warp, 16 (warp / 4)
+                // .. of its TMEM lane quarter (warps 0 and 1 take tokens 0..15 of theirs after
+                // the substitution).  Staged in the state-copy slot unless that holds this
+                // chunk's state already (an item change loaded it: s_pend false).
                 if (!kSplit && o_pend) {
                     const int j = warp >> 2;
-                    if (q4 >= 2) o_emit(16 * j, 16, s_pend);
-                    else o_emit(j == 1 ? 0 : 16 * j, j == 1 ? 32 : 16, s_pend);
+                    o_emit(16 * j, 16, s_pend);
                 }
             }
             const bool o_staged = !kSplit && o_pend && s_pend;
@@ -841,6 +859,16 @@ __device__ __forceinline__ void chunk_loop(const CUtensorMap* tm_q, const CUtens
             // K-major layout (row = TMEM lane) and are read MN-major by the next product.
             // (b) 16 -> 32, first product: P = A_bf T_d  (T_d = the diagonal blocks; blocks (1,0)
             //     and (3,2) of P are A_10 T_00 and A_32 T_22)
+            // Only the warps that read a product back wait for it (each thread on the mbarrier
+            // itself), and they hand the tiles they write to the issuing thread 0 (warp 0)
+            // through named barriers among themselves; the other warps go on to the barrier
+            // before P5.  A timed-out wait skips its tile and is counted at that barrier.  A
+            // warp that waits on an mbarrier waits for every phase of it in turn (a parity
+            // wait cannot tell a phase from the one two before it).
+            const bool w_b = q4 < 2;                                        // warps 0,1,4,5,8,9,12,13
+            const bool w_c = (q4 == 0 && part == 0) || (q4 == 1 && part == 2);  // warps 0, 9
+            const bool w_d = q4 == 1 && part < 2;                           // warps 1, 5
+            const bool w_e = q4 == 0 && part < 2;                           // warps 0, 4
             if (tid == 0) {
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks)
@@ -848,91 +876,120 @@ __device__ __forceinline__ void chunk_loop(const CUtensorMap* tm_q, const CUtens
                                  desc_mn(sb + OFF_LVL + LV_TB, 8192, ks), IDESC_MG64, ks > 0);
                 tc::mma_commit(&ms.bar_m0);
             }
-            KDA_WAIT(bar_m0, ph0);
-            if (failed) break;
-            if (q4 < 2) {  // rows 0..63 of P -> bf16 tile LV_MG
-                uint32_t d[16];
-                tc::tmem_ld16(taddr(tmem, warp, TM_MG + 16 * part), d);
-                tc::tmem_ld_wait();
-                float f[16];
+            if (w_b) {  // rows 0..63 of P -> bf16 tile LV_MG
+                mok = tc::mbar_wait(&ms.bar_m0, ph0);
+                tc::fence_after_sync();
+                if (mok) {
+                    uint32_t d[16];
+                    tc::tmem_ld16(taddr(tmem, warp, TM_MG + 16 * part), d);
+                    tc::tmem_ld_wait();
+                    float f[16];
 #pragma unroll
-                for (int j = 0; j < 16; ++j) f[j] = __uint_as_float(d[j]);
-                store16_k(sm + OFF_LVL + LV_MG, row, 16 * part, 64, f);
+                    for (int j = 0; j < 16; ++j) f[j] = __uint_as_float(d[j]);
+                    store16_k(sm + OFF_LVL + LV_MG, row, 16 * part, 64, f);
+                }
+                tc::fence_proxy_async_smem();
+                tc::fence_before_sync();
+                tc::named_sync(3, 256);
             }
-            KDA_SYNC_FOR_MMA();
+            ph0 ^= 1u;
             // (c) second product: Q = T_d P;  T_10 = -Q[16:32, 0:16], T_32 = -Q[48:64, 32:48]
-            if (tid == 0) {
+            if (tid == 0 && mok) {
+                tc::fence_after_sync();
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks)
                     tc::mma_bf16(tmem + TM_MG + 64, desc_k(sb + OFF_LVL + LV_TB, 64, ks),
                                  desc_mn(sb + OFF_LVL + LV_MG, 8192, ks), IDESC_MG64, ks > 0);
                 tc::mma_commit(&ms.bar_m1);
             }
-            KDA_WAIT(bar_m1, ph1);
-            if (failed) break;
-            if ((q4 == 0 && part == 0) || (q4 == 1 && part == 2)) {
-                uint32_t d[16];
-                tc::tmem_ld16(taddr(tmem, warp, TM_MG + 64 + 16 * part), d);
-                tc::tmem_ld_wait();
-                if (lane >= 16) {
-                    float f[16];
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) f[j] = -__uint_as_float(d[j]);
-                    store16_k(TB, row, 16 * part, 64, f);
-                }
+            if (w_c || w_e) {
+                // (warp 4 waits here too although it reads nothing of this product: a parity
+                // wait must not skip a phase, and warp 4 waits for the next one in (e))
+                mok = tc::mbar_wait(&ms.bar_m1, ph1) && mok;
+                tc::fence_after_sync();
             }
-            KDA_SYNC_FOR_MMA();
+            if (w_c) {
+                if (mok) {
+                    uint32_t d[16];
+                    tc::tmem_ld16(taddr(tmem, warp, TM_MG + 64 + 16 * part), d);
+                    tc::tmem_ld_wait();
+                    if (lane >= 16) {
+                        float f[16];
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) f[j] = -__uint_as_float(d[j]);
+                        store16_k(TB, row, 16 * part, 64, f);
+                    }
+                }
+                tc::fence_proxy_async_smem();
+                tc::fence_before_sync();
+                tc::named_sync(4, 64);
+            }
+            ph1 ^= 1u;
             // (d) 32 -> 64, first product: P' = A_bf[:, 0:32] T[0:32, 0:32]; rows 32..63 are
             //     A_21 T_11 (the rest of T's first 32 columns below row 31 is still zero)
-            if (tid == 0) {
+            if (tid == 0 && mok) {
+                tc::fence_after_sync();
 #pragma unroll
                 for (int ks = 0; ks < 2; ++ks)
                     tc::mma_bf16(tmem + TM_MG, desc_k(sb + OFF_LVL + LV_AB, 64, ks),
                                  desc_mn(sb + OFF_LVL + LV_TB, 8192, ks), IDESC_MG32, ks > 0);
                 tc::mma_commit(&ms.bar_m0);
             }
-            KDA_WAIT(bar_m0, ph0);
-            if (failed) break;
-            if (q4 == 1 && part < 2) {  // rows 32..63 of P' -> tile rows 0..31
-                uint32_t d[16];
-                tc::tmem_ld16(taddr(tmem, warp, TM_MG + 16 * part), d);
-                tc::tmem_ld_wait();
-                float f[16];
+            if (w_d) {  // rows 32..63 of P' -> tile rows 0..31
+                mok = tc::mbar_wait(&ms.bar_m0, ph0) && mok;
+                tc::fence_after_sync();
+                if (mok) {
+                    uint32_t d[16];
+                    tc::tmem_ld16(taddr(tmem, warp, TM_MG + 16 * part), d);
+                    tc::tmem_ld_wait();
+                    float f[16];
 #pragma unroll
-                for (int j = 0; j < 16; ++j) f[j] = __uint_as_float(d[j]);
-                store16_k(sm + OFF_LVL + LV_MG, lane, 16 * part, 64, f);
+                    for (int j = 0; j < 16; ++j) f[j] = __uint_as_float(d[j]);
+                    store16_k(sm + OFF_LVL + LV_MG, lane, 16 * part, 64, f);
+                }
+                tc::fence_proxy_async_smem();
+                tc::fence_before_sync();
             }
-            KDA_SYNC_FOR_MMA();
+            if (w_d || warp == 0) tc::named_sync(5, 96);  // warps 1 and 5 to warp 0
+            ph0 ^= 1u;
             // (e) second product: Y = T_22 P'[32:64, :] (A from row 32 of T, K = columns 32..63);
             //     T_21 = -Y
-            if (tid == 0) {
+            if (tid == 0 && mok) {
+                tc::fence_after_sync();
 #pragma unroll
                 for (int ks = 0; ks < 2; ++ks)
                     tc::mma_bf16(tmem + TM_MG + 64, desc_k(sb + OFF_LVL + LV_TB + 4096, 64, 2 + ks),
                                  desc_mn(sb + OFF_LVL + LV_MG, 8192, ks), IDESC_MG32, ks > 0);
                 tc::mma_commit(&ms.bar_m1);
             }
-            KDA_WAIT(bar_m1, ph1);
-            if (failed) break;
-            // fused kernel: the z slot is free (A_bf and the merge tiles are read): the next
-            // chunk's z tile, for its gate beside this chunk's carry
-            if (!kSplit && tid == 0 && has_next) {
-                tc::mbar_arrive_expect_tx(&ms.bar_z, 16384u);
-                tc::tma_load_3d(sm + OFF_LVL + LV_Z, tm_z, 0, nt0, (int)nbh, &ms.bar_z);
-            }
-            if (q4 == 0 && part < 2) {
-                uint32_t d[16];
-                tc::tmem_ld16(taddr(tmem, warp, TM_MG + 64 + 16 * part), d);
-                tc::tmem_ld_wait();
-                float f[16];
+            if (w_e) {
+                mok = tc::mbar_wait(&ms.bar_m1, ph1) && mok;
+                tc::fence_after_sync();
+                // fused kernel: the z slot is free (A_bf and the merge tiles are read): the next
+                // chunk's z tile, for its gate beside this chunk's carry
+                if (!kSplit && tid == 0 && has_next && mok) {
+                    tc::mbar_arrive_expect_tx(&ms.bar_z, 16384u);
+                    tc::tma_load_3d(sm + OFF_LVL + LV_Z, tm_z, 0, nt0, (int)nbh, &ms.bar_z);
+                }
+                if (mok) {
+                    uint32_t d[16];
+                    tc::tmem_ld16(taddr(tmem, warp, TM_MG + 64 + 16 * part), d);
+                    tc::tmem_ld_wait();
+                    float f[16];
 #pragma unroll
-                for (int j = 0; j < 16; ++j) f[j] = -__uint_as_float(d[j]);
-                store16_k(TB, 32 + lane, 16 * part, 64, f);
+                    for (int j = 0; j < 16; ++j) f[j] = -__uint_as_float(d[j]);
+                    store16_k(TB, 32 + lane, 16 * part, 64, f);
+                }
             }
+            ph1 ^= 1u;
         }
         // the staged output has left the state-copy slot that this chunk's copy refills next
         if (!kSplit && tid == 0) tc::bulk_wait_read_all();
-        KDA_SYNC_FOR_MMA();
+        tc::fence_proxy_async_smem();
+        tc::fence_before_sync();
+        if (__syncthreads_or(!mok)) failed = true;
+        tc::fence_after_sync();
+        if (failed) break;
         // ---------------------------------------------------------------- P5: W^T, U^T
         if (tid == 0) {
 #pragma unroll
