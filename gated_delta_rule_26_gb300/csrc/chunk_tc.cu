@@ -70,7 +70,7 @@ constexpr uint32_t OFF_LVL = 0;                 // 64 KB multi-use region (see L
 constexpr uint32_t OFF_G = 65536;               // 32 KB fp32 G[t][c]
 constexpr uint32_t OFF_Q = OFF_G + 32768;       // 16 KB bf16 q tile, row-major [t][c]
 constexpr uint32_t OFF_K = OFF_Q + 16384;       // 16 KB bf16 k tile
-constexpr uint32_t OFF_V = OFF_K + 16384;       // 16 KB bf16 v tile, later T fp32 [t][i]
+constexpr uint32_t OFF_V = OFF_K + 16384;       // 16 KB bf16 v tile, then K~
 constexpr uint32_t OFF_A1 = OFF_V + 16384;      // 32 KB [W^T | (Q Gamma)^T], MN-major (2 atoms)
 constexpr uint32_t OFF_S = OFF_A1 + 32768;      // 32 KB S bf16, MN-major [c][v] (2 atoms)
 constexpr uint32_t OFF_MISC = OFF_S + 32768;
@@ -1261,7 +1261,8 @@ __device__ __forceinline__ void chunk_loop(const CUtensorMap* tm_q, const CUtens
             ph_qkz ^= 1u;
             ph_z ^= 1u;
         }
-        tc::fence_proxy_async_smem();
+        // (no proxy fence here: what the async proxy reads next, the threads that write it
+        // fence before the barrier that precedes that read)
         tc::fence_before_sync();
         if (__syncthreads_or(failed)) failed = true;
         tc::fence_after_sync();
