@@ -377,56 +377,105 @@ cudaError_t launch_chunk_carry_grid(const SplitOperands& ops, int T, int seg_n0,
     return cudaGetLastError();
 }
 
-// The sequential half of the scan: per sequence (blockIdx.x / 4) and 32-column tile of the
-// state (blockIdx.x % 4), S_0 = the segment's entering state (h_in, or zero when it is null),
+// The sequential half of the scan: per sequence (blockIdx.x / 8) and 16-column slice of the
+// state (blockIdx.x % 8), S_0 = the segment's entering state (h_in, or zero when it is null),
 // then S_{j+1} = P_j S_j + Z_j for j = 0 .. nsub - 2, every S_j written to s_out [j][bh] for
 // the plain carry of sub-segment j.  fp32 throughout: P_j and Z_j come from the carry's TMEM
-// state, and S is kept in shared memory between steps.
-__global__ void __launch_bounds__(256)
+// state, and S is kept in shared memory between steps.  Thread (rb, cb) = (tid / 8, tid % 8)
+// owns the 4 x 2 block of rows 4 rb .. and slice columns 2 cb ..; P_j sits transposed in
+// shared memory (Pt[k][c]), so a step reads one float4 of P and one float2 of S per 8 FMAs,
+// and P_{j+1} and Z_{j+1} are loaded into registers while step j computes.  Each output is Z
+// plus the products over k in ascending order.
+constexpr int kCmbThreads = 256, kCmbSlices = 8, kCmbW = VD / kCmbSlices;
+constexpr size_t kCmbSmem = (size_t)KD * KD * sizeof(float) + (size_t)KD * kCmbW * sizeof(float);
+static_assert(kCmbW == 16 && (KD / 4) * (kCmbW / 2) == kCmbThreads, "combine blocking");
+__global__ void __launch_bounds__(kCmbThreads)
     kda_carry_combine_kernel(int BH, int nsub, const float* __restrict__ h_in,
                              const float* __restrict__ pbuf, const float* __restrict__ zbuf,
                              float* __restrict__ s_out) {
-    __shared__ float Ss[KD][33];  // odd pitch: the stores of a warp (16 rows) hit distinct banks
+    extern __shared__ float4 cmb_smem[];
+    float* Pt = reinterpret_cast<float*>(cmb_smem);  // [k][c], 128 x 128
+    float* Ss = Pt + KD * KD;                         // [k][slice column], 128 x 16
     const int tid = threadIdx.x;
-    const size_t bh = blockIdx.x / 4;
-    const int v0 = 32 * (blockIdx.x % 4);
+    const size_t bh = blockIdx.x / kCmbSlices;
+    const int v0 = kCmbW * (blockIdx.x % kCmbSlices);
     const size_t KV = (size_t)KD * VD;
-    // thread: row c = tid / 2, columns v0 + 16 (tid % 2) .. + 15
-    const int c = tid >> 1, vh = 16 * (tid & 1);
-    float acc[16];
+    const int r0 = 4 * (tid >> 3), c0 = 2 * (tid & 7);
+    // P_j into registers: float4 f = tid + 256 m holds row r = f % 128, columns 4 (f / 128) ..
+    float4 pr[16];
+    float2 zr[4];
+    auto load_pz = [&](int j) {
+        const float* P = pbuf + ((size_t)j * BH + bh) * KV;
 #pragma unroll
-    for (int i = 0; i < 16; ++i)
-        acc[i] = h_in ? h_in[bh * KV + (size_t)c * VD + v0 + vh + i] : 0.f;
-    for (int j = 0;; ++j) {
-        float* dst = s_out + ((size_t)j * BH + bh) * KV + (size_t)c * VD + v0 + vh;
+        for (int m = 0; m < 16; ++m) {
+            const int f = tid + kCmbThreads * m, r = f & (KD - 1), k4 = 4 * (f >> 7);
+            pr[m] = __ldcg(reinterpret_cast<const float4*>(P + (size_t)r * KD + k4));
+        }
+        const float* Z = zbuf + ((size_t)j * BH + bh) * KV + v0 + c0;
 #pragma unroll
-        for (int i = 0; i < 16; i += 4)
-            *reinterpret_cast<float4*>(dst + i) = make_float4(acc[i], acc[i + 1], acc[i + 2], acc[i + 3]);
-        if (j + 1 >= nsub) break;
-        __syncthreads();  // the previous step's readers of Ss are done
+        for (int a = 0; a < 4; ++a) zr[a] = __ldcg(reinterpret_cast<const float2*>(Z + (size_t)(r0 + a) * VD));
+    };
+    auto store_pt = [&]() {
 #pragma unroll
-        for (int i = 0; i < 16; ++i) Ss[c][vh + i] = acc[i];
-        __syncthreads();
-        const float* P = pbuf + ((size_t)j * BH + bh) * KV + (size_t)c * KD;
-        const float* Z = zbuf + ((size_t)j * BH + bh) * KV + (size_t)c * VD + v0 + vh;
+        for (int m = 0; m < 16; ++m) {
+            const int f = tid + kCmbThreads * m, r = f & (KD - 1), k4 = 4 * (f >> 7);
+            Pt[(k4 + 0) * KD + r] = pr[m].x;
+            Pt[(k4 + 1) * KD + r] = pr[m].y;
+            Pt[(k4 + 2) * KD + r] = pr[m].z;
+            Pt[(k4 + 3) * KD + r] = pr[m].w;
+        }
+    };
+    auto out_block = [&](int j, const float2 (&x)[4]) {
+        float* dst = s_out + ((size_t)j * BH + bh) * KV + v0 + c0;
 #pragma unroll
-        for (int i = 0; i < 16; ++i) acc[i] = Z[i];
+        for (int a = 0; a < 4; ++a) {
+            *reinterpret_cast<float2*>(dst + (size_t)(r0 + a) * VD) = x[a];
+            *reinterpret_cast<float2*>(Ss + (r0 + a) * kCmbW + c0) = x[a];
+        }
+    };
+    {
+        float2 x[4];
+#pragma unroll
+        for (int a = 0; a < 4; ++a)
+            x[a] = h_in ? *reinterpret_cast<const float2*>(h_in + bh * KV + (size_t)(r0 + a) * VD + v0 + c0)
+                        : make_float2(0.f, 0.f);
+        out_block(0, x);
+    }
+    if (nsub > 1) {
+        load_pz(0);
+        store_pt();
+    }
+    for (int j = 0; j + 1 < nsub; ++j) {
+        __syncthreads();  // P_j and S_j are in shared memory
+        float2 acc[4];
+#pragma unroll
+        for (int a = 0; a < 4; ++a) acc[a] = zr[a];
+        if (j + 2 < nsub) load_pz(j + 1);
 #pragma unroll 4
-        for (int k = 0; k < KD; k += 4) {
-            const float4 p = *reinterpret_cast<const float4*>(P + k);
-            const float pk[4] = {p.x, p.y, p.z, p.w};
+        for (int k = 0; k < KD; ++k) {
+            const float4 p = *reinterpret_cast<const float4*>(Pt + k * KD + r0);
+            const float2 x = *reinterpret_cast<const float2*>(Ss + k * kCmbW + c0);
+            const float pa[4] = {p.x, p.y, p.z, p.w};
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-#pragma unroll
-                for (int i = 0; i < 16; ++i) acc[i] = fmaf(pk[u], Ss[k + u][vh + i], acc[i]);
+            for (int a = 0; a < 4; ++a) {
+                acc[a].x = fmaf(pa[a], x.x, acc[a].x);
+                acc[a].y = fmaf(pa[a], x.y, acc[a].y);
             }
         }
+        __syncthreads();  // every read of P_j and S_j is done
+        out_block(j + 1, acc);
+        if (j + 2 < nsub) store_pt();
     }
 }
 
 cudaError_t launch_carry_combine(int BH, int nsub, const float* h_in, const float* pbuf,
                                  const float* zbuf, float* s_out, cudaStream_t s) {
-    kda_carry_combine_kernel<<<BH * 4, 256, 0, s>>>(BH, nsub, h_in, pbuf, zbuf, s_out);
+    cudaError_t err = cudaFuncSetAttribute(kda_carry_combine_kernel,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           (int)kCmbSmem);
+    if (err != cudaSuccess) return err;
+    kda_carry_combine_kernel<<<BH * kCmbSlices, kCmbThreads, kCmbSmem, s>>>(BH, nsub, h_in, pbuf,
+                                                                          zbuf, s_out);
     count_launches(1);
     return cudaGetLastError();
 }
