@@ -303,6 +303,34 @@ def test_few_sequences_take_the_scan_and_match_the_oracle(kda):
     check("hT", hT[bs, hs].unsqueeze(0), h_ref, "bf16")
 
 
+@pytest.mark.parametrize("B,H,T", [
+    (1, 24, 5000),   # 79 chunks: five overlapped segments of 16 (the last ragged)
+    (2, 19, 3000),   # B*H = 38, 47 chunks: segments of 18, 18 and 11
+    (3, 11, 6000),   # B*H = 33, 94 chunks: six segments of 18 (the last of 4)
+])
+def test_split_segment_plans_match_noalloc_and_oracle(kda, B, H, T):
+    """The overlapped split form cuts each call into segments of the length its makespan model
+    picks for B*H and T, on two operand buffers; the no-alloc form cuts the same chunks
+    elsewhere (as many chunks as its fixed array holds).  Both hand the fp32 state on at
+    chunk boundaries, so their outputs agree bit for bit; sampled sequences against the
+    oracle, token by token."""
+    inp = inputs.make(B, H, T, 128, 128, chunk=64, dtype="bf16", seed=90 + H, h0_std=0.1,
+                      dt_std=0.1)
+    d = inp.to("cuda")
+    args = (d.q, d.k, d.v, d.z, d.beta, d.A_log, d.dt_bias, inp.scale, d.h0, 64)
+    o, h = kda.chunk_forward(*args, form="split")
+    o2, h2 = kda.chunk_forward(*args, form="split_noalloc")
+    torch.cuda.synchronize()
+    assert kda.device_status() == 0
+    assert torch.equal(o, o2) and torch.equal(h, h2)
+    pairs = [(0, 0), (B - 1, H - 1)]
+    q, k, v, z, beta, A, dt, h0 = _sample_pairs(inp, pairs)
+    o_ref, h_ref = oracle.forward(q, k, v, z, beta, A, dt, inp.scale, h0, threads=len(pairs))
+    bs, hs = [p[0] for p in pairs], [p[1] for p in pairs]
+    check("o", o[bs, hs].unsqueeze(0), o_ref, "bf16")
+    check("hT", h[bs, hs].unsqueeze(0), h_ref, "bf16")
+
+
 # ---------------------------------------------------------------- full-size workloads, sampled
 def _sample_pairs(inp, pairs):
     """Gather (b, h) sequences into a (1, n, T, *) problem the oracle can run."""
