@@ -6,7 +6,8 @@
 // the chunks of a segment in order; per chunk n (kda-adjoint-2026-10-01, section 2, with
 // the read scale of kdafix-2026-10-02 "Fix 2"):
 //
-//   C1  D = S^T [W^T | (Q Gamma)^T] = [(W S)^T | (Q Gamma S)^T]   tcgen05, S as a bf16 operand
+//   C1  D = [(W S)^T | (Q Gamma S)^T]: S^T W^T and S^T (Q Gamma)^T, the latter with Q Gamma
+//       as a K-major operand [t][c]                                 tcgen05, S as a bf16 operand
 //   C2  Delta^T = U^T - (W S)^T
 //   C3  (M Delta)^T onto (Q Gamma S)^T, then o = scale (Q Gamma S + M Delta) -> bf16 to HBM,
 //       and S <- diag(Gamma_last) S + K~^T Delta,  K~ = K e^{G_last - G}  tcgen05, fp32 in TMEM
@@ -45,8 +46,8 @@ constexpr int NT2 = 512;
 constexpr uint32_t K2_S = 0;            // 32 KB S bf16, MN-major [c][v] (2 atoms)
 constexpr uint32_t K2_DELTA = 32768;    // 16 KB Delta^T, K-major [v][t]
 constexpr uint32_t K2_STAGE = 49152;    // two operand stages
-// one stage: [W^T | (Q Gamma)^T] (MN-major, 2 atoms), U^T (K-major [v][t]), K~ (MN-major
-// [t][c], 2 atoms of 8 KB), M (K-major [t][s]), Gamma_last.
+// one stage: W^T (MN-major [c][t]), Q Gamma (K-major [t][c], 2 atoms of 8 KB), U^T (K-major
+// [v][t]), K~ (MN-major [t][c], 2 atoms of 8 KB), M (K-major [t][s]), Gamma_last.
 constexpr uint32_t ST_WQ = 0, ST_UU = 32768, ST_KT = 49152, ST_MM = 65536, ST_GL = 73728;
 constexpr uint32_t ST_BYTES = 74752;  // 73 KB, a multiple of 1024
 constexpr uint32_t ST_TX = (uint32_t)kItemBytes;
@@ -65,8 +66,9 @@ static_assert(ST_TX <= ST_BYTES && ST_GL + kItemGL <= ST_BYTES && ST_MM + kItemM
               "stage layout");
 
 constexpr uint32_t TM_S2 = 0;    // fp32 state, lanes = key channel c, cols = v   (128)
-constexpr uint32_t TM_D2 = 128;  // S^T [W^T | (Q Gamma)^T], + (M Delta)^T above   (128)
-constexpr uint32_t IDESC_SQ2 = tc::idesc_bf16(128, 128, 1, 1);
+constexpr uint32_t TM_D2 = 128;  // [(W S)^T | (Q Gamma S)^T], + (M Delta)^T above (128)
+constexpr uint32_t IDESC_SW2 = tc::idesc_bf16(128, 64, 1, 1);  // C1, W half (B MN-major)
+constexpr uint32_t IDESC_SG2 = tc::idesc_bf16(128, 64, 1, 0);  // C1, Q Gamma half (B K-major)
 constexpr uint32_t IDESC_SK2 = tc::idesc_bf16(128, 128, 1, 0);
 constexpr uint32_t IDESC_MD2 = tc::idesc_bf16(128, 64, 0, 0);
 
@@ -74,6 +76,7 @@ constexpr uint32_t IDESC_MD2 = tc::idesc_bf16(128, 64, 0, 0);
 
 __global__ void __launch_bounds__(NT2, 1)
     kda_chunk_carry_kernel(const __grid_constant__ CUtensorMap tm_wq,
+                           const __grid_constant__ CUtensorMap tm_qg,
                            const __grid_constant__ CUtensorMap tm_uu,
                            const __grid_constant__ CUtensorMap tm_kt,
                            const uint8_t* __restrict__ mm, const float* __restrict__ gl, int T,
@@ -110,6 +113,7 @@ __global__ void __launch_bounds__(NT2, 1)
         tc::mbar_init(&ms.bar_o, 1);
         tc::fence_barrier_init();
         tc::tma_prefetch_desc(&tm_wq);
+        tc::tma_prefetch_desc(&tm_qg);
         tc::tma_prefetch_desc(&tm_uu);
         tc::tma_prefetch_desc(&tm_kt);
     }
@@ -131,7 +135,8 @@ __global__ void __launch_bounds__(NT2, 1)
         tc::mbar_arrive_expect_tx(bar, ST_TX - (zero_u ? (uint32_t)kItemUU : 0u) -
                                            (write_o ? 0u : (uint32_t)kItemMM));
         tc::tma_load_3d(st + ST_WQ, &tm_wq, 0, 0, 2 * item, bar);
-        tc::tma_load_3d(st + ST_WQ + 16384, &tm_wq, 0, 0, 2 * item + 1, bar);
+        tc::tma_load_3d(st + ST_WQ + 16384, &tm_qg, 0, 0, 4 * item + 2, bar);
+        tc::tma_load_3d(st + ST_WQ + 24576, &tm_qg, 0, 0, 4 * item + 3, bar);
         if (!zero_u) tc::tma_load_3d(st + ST_UU, &tm_uu, 0, 0, item, bar);
         tc::tma_load_3d(st + ST_KT, &tm_kt, 0, 0, item, bar);
         tc::tma_load_3d(st + ST_KT + 8192, &tm_kt, 64, 0, item, bar);
@@ -198,12 +203,15 @@ __global__ void __launch_bounds__(NT2, 1)
         // stage s ^ 1 was consumed by the previous chunk: refill it two chunks ahead of that one
         // (a thread of warp 1, so that thread 0 issues C1 at once)
         if (tid == 32 && j >= j0 + 1 && j + 1 < j1) issue(j + 1, s ^ 1);
-        // C1: D[v][t'] = sum_c S[c][v] [W^T | (Q Gamma)^T][c][t']
+        // C1: D[v][t'] = sum_c S[c][v] W^T[c][t'] (t' < 64), sum_c S[c][v] QG[t'][c] above
         if (tid == 0) {
 #pragma unroll
-            for (int ks = 0; ks < 8; ++ks)
-                tc::mma_bf16(tmem + TM_D2, desc_mn(sb + K2_S, 16384, ks),
-                             desc_mn(stb + ST_WQ, 16384, ks), IDESC_SQ2, ks > 0);
+            for (int ks = 0; ks < 8; ++ks) {
+                const uint64_t a = desc_mn(sb + K2_S, 16384, ks);
+                tc::mma_bf16(tmem + TM_D2, a, desc_mn(stb + ST_WQ, 16384, ks), IDESC_SW2, ks > 0);
+                tc::mma_bf16(tmem + TM_D2 + 64, a, desc_k(stb + ST_WQ + 16384, 64, ks), IDESC_SG2,
+                             ks > 0);
+            }
             tc::mma_commit(&ms.bar_mma);
         }
         // meanwhile: S <- diag(Gamma_last) S in TMEM (row c, this warp's 32 columns)
@@ -371,7 +379,7 @@ cudaError_t launch_chunk_carry_grid(const SplitOperands& ops, int T, int seg_n0,
     if (err != cudaSuccess) return err;
     const int grid = cg.BH * cg.nsub * (cg.scan_roles ? 2 : 1);
     if (grid < 1) return cudaSuccess;
-    kda_chunk_carry_kernel<<<grid, NT2, K2_SMEM, s>>>(ops.wq, ops.uu, ops.kt, ops.mm, ops.gl, T,
+    kda_chunk_carry_kernel<<<grid, NT2, K2_SMEM, s>>>(ops.wq, ops.qg, ops.uu, ops.kt, ops.mm, ops.gl, T,
                                                        seg_n0, seg_len, scale, h_in, out, h_out, cg);
     count_launches(1);
     return cudaGetLastError();

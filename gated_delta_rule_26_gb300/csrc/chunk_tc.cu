@@ -27,12 +27,14 @@
 //   P4  T = (I + A)^{-1}: 16 x 16 diagonal blocks by forward substitution (fp32, CUDA
 //       cores), then the block merges T_21 = -T_22 A_21 T_11 (16 -> 32 for both halves at
 //       once, then 32 -> 64) as four small tcgen05 products with bf16 operands.
-//   P5  W^T = (diag(beta) K Gamma)^T T^T and U^T = (diag(beta) V)^T T^T  (tcgen05); A1 then
-//       holds [W^T | (Q Gamma)^T], so that Delta = U - W S and the state's share of the
-//       output come from ONE product with S.
+//   P5  W^T = (diag(beta) K Gamma)^T T^T and U^T = (diag(beta) V)^T T^T  (tcgen05).  The
+//       fused kernel forms Q Gamma row-major (a K-major operand [t][c]) during the inverse's
+//       merges, on the warps that read no merge product; the prep kernel puts (Q Gamma)^T
+//       next to W^T in A1.
 //   C1  D = S^T [W^T | (Q Gamma)^T] = [(W S)^T | (Q Gamma S)^T]  (M = 128 value channels,
-//       N = 128, K = 128; S as bf16 operand).  Before it, the fp32 state in TMEM is scaled
-//       by Gamma_last (row c by e^{G_last,c}).
+//       N = 64 + 64, K = 128; S as bf16 operand), so that Delta = U - W S and the state's
+//       share of the output come from one pass over S.  Before it, the fp32 state in TMEM is
+//       scaled by Gamma_last (row c by e^{G_last,c}).
 //   C2  from TMEM, one value channel per thread: Delta^T = U^T - (W S)^T.
 //   C3  S += (K * e^{G_last - G})^T Delta   accumulated in TMEM in fp32 (the carry with a
 //       single exponential of the log-space difference, kda-adjoint-2026-10-01 sections 2
@@ -71,7 +73,7 @@ constexpr uint32_t OFF_G = 65536;               // 32 KB fp32 G[t][c]
 constexpr uint32_t OFF_Q = OFF_G + 32768;       // 16 KB bf16 q tile, row-major [t][c]
 constexpr uint32_t OFF_K = OFF_Q + 16384;       // 16 KB bf16 k tile
 constexpr uint32_t OFF_V = OFF_K + 16384;       // 16 KB bf16 v tile, then K~
-constexpr uint32_t OFF_A1 = OFF_V + 16384;      // 32 KB [W^T | (Q Gamma)^T], MN-major (2 atoms)
+constexpr uint32_t OFF_A1 = OFF_V + 16384;      // 32 KB W^T | (prep kernel) (Q Gamma)^T, MN-major
 constexpr uint32_t OFF_S = OFF_A1 + 32768;      // 32 KB S bf16, MN-major [c][v] (2 atoms)
 constexpr uint32_t OFF_MISC = OFF_S + 32768;
 // multi-use region, in order of use within a chunk
@@ -80,9 +82,9 @@ constexpr uint32_t LV_PB = 32768;   // level pair B operand, K-major 64 rows (16
 constexpr uint32_t LV_AF = 0;       // A fp32 [t][i] (16 KB, swizzled; diagonal 16 x 16 blocks)  P3-P4
 constexpr uint32_t LV_MB = 16384;   // M bf16 K-major [t][i] (8 KB)          P3-P5 (fused: -C3)
 constexpr uint32_t LV_TB = 24576;   // T bf16 K-major [t][i] (8 KB)          P4-P5
-constexpr uint32_t LV_UT = 0;       // U^T K-major [v][i] (16 KB)            P5
 constexpr uint32_t LV_Z = 49152;    // z tile of the NEXT chunk (16 KB)      P5-P2
-constexpr uint32_t LV_GTF = 0;      // fused kernel: the gate's warp totals (8 KB)   carry window
+constexpr uint32_t LV_GTF = 24576;  // fused kernel: the gate's warp totals (8 KB), in the T slot  window
+constexpr uint32_t LV_QG = 0;       // fused kernel: Q Gamma bf16 K-major [t][c] (16 KB)  merges - C1
 constexpr uint32_t LV_GTP = 32768;  // prep kernel: the gate's warp totals (8 KB)    S2
 constexpr uint32_t LV_AB = 49152;   // A bf16 K-major [t][i] (8 KB), in the z slot         P3-P4
 constexpr uint32_t LV_MG = 57344;   // merge products P, P' (8 KB), in the z slot            P4
@@ -91,7 +93,7 @@ constexpr uint32_t LV_DELTA = 32768;// Delta^T K-major [v][t] (16 KB)        C2-
 // the second level pair's GEMM in the fused kernel, under the W/U GEMM in the prep kernel) to C3
 // or its store.
 // beta K Gamma and beta V (MN-major [t][.], 16 KB each) live in the A1 slot from P3 until
-// the W/U GEMM has read them; then A1 takes [W^T | (Q Gamma)^T].
+// the W/U GEMM has read them; then A1 takes W^T (and, in the prep kernel, (Q Gamma)^T).
 constexpr uint32_t OFF_BKG = OFF_A1, OFF_BV = OFF_A1 + 16384;
 
 struct Misc {
@@ -113,15 +115,15 @@ constexpr uint32_t SMEM_BYTES = OFF_MISC + sizeof(Misc) + 1024;
 constexpr uint32_t TM_S = 0;      // fp32 state, lanes = key channel c, cols = v   (128)
 constexpr uint32_t TM_LVL = 384;  // two level-pair score tiles                    (2 x 64)
 constexpr uint32_t TM_MG = 384;   // the inverse's merge products                  (2 x 64)
-constexpr uint32_t TM_QG = 128;   // prep kernel: (Q Gamma)^T                      (64)
-constexpr uint32_t TM_D1 = 256;   // S^T [W^T | (Q Gamma)^T], + (M Delta)^T above   (128)
+constexpr uint32_t TM_D1 = 256;   // [(W S)^T | (Q Gamma S)^T], + (M Delta)^T above (128)
 constexpr uint32_t TM_W = 384;    // W^T                                           (64)
 constexpr uint32_t TM_U = 448;    // U^T                                           (64)
 
 constexpr uint32_t IDESC_LVL = tc::idesc_bf16(128, 64, 0, 0);
 constexpr uint32_t IDESC_WU = tc::idesc_bf16(128, 64, 1, 0);
 constexpr uint32_t IDESC_QU = tc::idesc_bf16(128, 64, 0, 0);
-constexpr uint32_t IDESC_SQ = tc::idesc_bf16(128, 128, 1, 1);
+constexpr uint32_t IDESC_SW = tc::idesc_bf16(128, 64, 1, 1);   // C1, W half (B MN-major)
+constexpr uint32_t IDESC_SG = tc::idesc_bf16(128, 64, 1, 0);   // C1, Q Gamma half (B K-major)
 constexpr uint32_t IDESC_SK = tc::idesc_bf16(128, 128, 1, 0);
 constexpr uint32_t IDESC_MG64 = tc::idesc_bf16(128, 64, 0, 1);  // inverse merges
 constexpr uint32_t IDESC_MG32 = tc::idesc_bf16(128, 32, 0, 1);
@@ -311,10 +313,11 @@ __device__ __forceinline__ int swz(int t, int i) {
 }
 
 // What the chunk-parallel prep kernel writes per work item (one chunk of one sequence):
-// [W^T | (Q Gamma)^T] through the tile map tm_wq (z = 2 item, 2 item + 1), U^T through tm_uu
-// and K~ through tm_kt (z = item), the M tile (its shared-memory bytes) at mm + kItemMM item
-// and Gamma_last (fp32) at gl + 128 item.  Items are the chunks [seg_n0, seg_n0 + seg_len) of
-// every sequence, item = bh * seg_len + (n - seg_n0).
+// W^T (MN-major [c][t]) through the tile map tm_wq (z = 2 item), Q Gamma (K-major [t][c], two
+// 64-channel atoms) through tm_qg over the same array (z = 4 item + 2, 4 item + 3), U^T through
+// tm_uu and K~ through tm_kt (z = item), the M tile (its shared-memory bytes) at
+// mm + kItemMM item and Gamma_last (fp32) at gl + 128 item.  Items are the chunks
+// [seg_n0, seg_n0 + seg_len) of every sequence, item = bh * seg_len + (n - seg_n0).
 struct PrepSeg {
     int seg_n0, seg_len, items;
     uint8_t* mm;
@@ -342,8 +345,9 @@ struct FusedSched {
 template <bool kSplit>
 __device__ __forceinline__ void chunk_loop(const CUtensorMap* tm_q, const CUtensorMap* tm_k,
                                            const CUtensorMap* tm_v, const CUtensorMap* tm_z,
-                                           const CUtensorMap* tm_wq, const CUtensorMap* tm_uu,
-                                           const CUtensorMap* tm_kt, int H, int T,
+                                           const CUtensorMap* tm_wq, const CUtensorMap* tm_qg,
+                                           const CUtensorMap* tm_uu, const CUtensorMap* tm_kt,
+                                           int H, int T,
                                            const __nv_bfloat16* __restrict__ beta,
                                            const float* __restrict__ A_log,
                                            const float* __restrict__ dt_bias, float scale,
@@ -982,6 +986,22 @@ __device__ __forceinline__ void chunk_loop(const CUtensorMap* tm_q, const CUtens
                 }
             }
             ph1 ^= 1u;
+            // the warps that read no merge product back: Q Gamma (bf16, K-major [t][c] in the
+            // A slot, which the substitution is done with) for the C1 operand (fused kernel) or
+            // the carry kernel's (prep kernel), four (token, 8 channels) items per thread
+            if (q4 >= 2) {
+                const int i0 = ((warp >> 2) * 2 + (q4 - 2)) * 32 + lane;  // 0..255 over these 8 warps
+#pragma unroll
+                for (int m = 0; m < 4; ++m) {
+                    const int item = i0 + 256 * m, t = item >> 4, c8 = item & 15;
+                    float g8[8], qf[8], f[8];
+                    load8g(G2, t, c8, g8);
+                    unpack8(*reinterpret_cast<const uint4*>(sm + OFF_Q + t * 256 + c8 * 16), qf);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) f[j] = qf[j] * ex2(g8[j]);
+                    *reinterpret_cast<uint4*>(sm + OFF_LVL + LV_QG + kmaj_off(t, c8 * 8, 64)) = pack8(f);
+                }
+            }
         }
         // the staged output has left the state-copy slot that this chunk's copy refills next
         if (!kSplit && tid == 0) tc::bulk_wait_read_all();
@@ -990,6 +1010,12 @@ __device__ __forceinline__ void chunk_loop(const CUtensorMap* tm_q, const CUtens
         if (__syncthreads_or(!mok)) failed = true;
         tc::fence_after_sync();
         if (failed) break;
+        // (fused kernel) q and k are read: request the next chunk's q and k tiles
+        if (!kSplit && tid == 0 && has_next) {
+            tc::mbar_arrive_expect_tx(&ms.bar_qkz, 2u * 16384u);
+            tc::tma_load_3d(sm + OFF_Q, tm_q, 0, nt0, (int)nbh, &ms.bar_qkz);
+            tc::tma_load_3d(sm + OFF_K, tm_k, 0, nt0, (int)nbh, &ms.bar_qkz);
+        }
         // ---------------------------------------------------------------- P5: W^T, U^T
         if (tid == 0) {
 #pragma unroll
@@ -1000,22 +1026,7 @@ __device__ __forceinline__ void chunk_loop(const CUtensorMap* tm_q, const CUtens
             }
             tc::mma_commit(&ms.bar_m0);
         }
-        // while it runs (prep kernel): (Q Gamma)^T into TMEM (lane c, column t), for the upper
-        // half of A1 once the GEMM has read it; thread (quarter, part) takes channels
-        // 32 quarter + lane, tokens 16 part ..
-        if constexpr (kSplit) {
-            const int c = row, tb = 16 * part;
-            uint32_t r[16];
-#pragma unroll
-            for (int j = 0; j < 16; ++j) {
-                const int t = tb + j;
-                const float qv = __uint_as_float((uint32_t)*reinterpret_cast<const uint16_t*>(
-                                                     sm + OFF_Q + t * 256 + c * 2) << 16);
-                r[j] = __float_as_uint(qv * ex2(G2[t * KD + gsw(c)]));
-            }
-            tc::tmem_st16(taddr(tmem, warp, TM_QG + tb), r);
-            tc::tmem_st_wait();
-        } else {
+        if constexpr (!kSplit) {
             // (fused kernel) the state the previous chunk's C3 left in TMEM: this chunk's bf16
             // operand [c][v] for C1 (unless an item change already loaded it), then
             // S <- diag(Gamma_last) S in place for C3 (the bf16 copy stays unscaled)
@@ -1068,28 +1079,20 @@ __device__ __forceinline__ void chunk_loop(const CUtensorMap* tm_q, const CUtens
             tc::tma_load_3d(sm + OFF_LVL + LV_Z, tm_z, 0, nt0, (int)nbh, &ms.bar_qkz);
         }
         if constexpr (!kSplit) {
-            // (fused kernel) every part: W^T row c, columns 16 part .. -> [W^T | .] and
-            // (Q Gamma)^T row c, tokens 16 part .. -> [. | QG^T], the latter while the TMEM load
-            // of the former is in flight (U stays in TMEM for the carry)
+            // (fused kernel) every part: W^T row c, columns 16 part .. -> A1 (U stays in TMEM
+            // for the carry, Q Gamma is in the A slot already)
             const int c = row, tb = 16 * part;
             uint32_t d[16];
             tc::tmem_ld16(taddr(tmem, warp, TM_W + tb), d);
-            float f[16];
-#pragma unroll
-            for (int j = 0; j < 16; ++j) {
-                const int t = tb + j;
-                const float qv = __uint_as_float((uint32_t)*reinterpret_cast<const uint16_t*>(
-                                                     sm + OFF_Q + t * 256 + c * 2) << 16);
-                f[j] = qv * ex2(G2[t * KD + gsw(c)]);
-            }
-            store16_mn(sm + OFF_A1, c, 64 + tb, 16384, f);
             tc::tmem_ld_wait();
+            float f[16];
 #pragma unroll
             for (int j = 0; j < 16; ++j) f[j] = __uint_as_float(d[j]);
             store16_mn(sm + OFF_A1, c, tb, 16384, f);
         } else {
-            // (prep kernel) parts 0-1: W^T row c, columns 32*part.. -> [W^T | .]; parts 2-3:
-            // U^T row v -> K-major
+            // (prep kernel) parts 0-1: W^T row c, columns 32*part.. -> A1; parts 2-3: U^T row v
+            // -> K-major, in the state-copy slot (which this kernel has free: Q Gamma is in the
+            // A slot, where U^T used to go)
             const bool is_u = part >= 2;
             const int cb = 32 * (part & 1);
             const uint32_t col = is_u ? TM_U : TM_W;
@@ -1105,39 +1108,23 @@ __device__ __forceinline__ void chunk_loop(const CUtensorMap* tm_q, const CUtens
                     store16_mn(sm + OFF_A1, row, cb, 16384, f0);
                     store16_mn(sm + OFF_A1, row, cb + 16, 16384, f1);
                 } else {
-                    store16_k(sm + OFF_LVL + LV_UT, row, cb, 128, f0);
-                    store16_k(sm + OFF_LVL + LV_UT, row, cb + 16, 128, f1);
+                    store16_k(sm + OFF_S, row, cb, 128, f0);
+                    store16_k(sm + OFF_S, row, cb + 16, 128, f1);
                 }
             }
-            if constexpr (kSplit) {
-                // (prep kernel) (Q Gamma)^T from TMEM, tokens 16 part .. -> [. | QG^T] (the
-                // GEMM is done reading the beta V tile there); Gamma_last -> global
-                uint32_t d[16];
-                tc::tmem_ld16(taddr(tmem, warp, TM_QG + 16 * part), d);
-                tc::tmem_ld_wait();
-                float f[16];
-#pragma unroll
-                for (int j = 0; j < 16; ++j) f[j] = __uint_as_float(d[j]);
-                store16_mn(sm + OFF_A1, row, 64 + 16 * part, 16384, f);
-                if (part == 0) seg.gl[(size_t)it * KD + row] = ex2(G2[63 * KD + gsw(row)]);
-            }
+            if (kSplit && part == 0) seg.gl[(size_t)it * KD + row] = ex2(G2[63 * KD + gsw(row)]);
         }
         KDA_SYNC_FOR_MMA();
-        // q is read: request the next chunk's q, k (fused kernel; the prep kernel did above)
-        if (!kSplit && tid == 0 && has_next) {
-            tc::mbar_arrive_expect_tx(&ms.bar_qkz, 2u * 16384u);
-            tc::tma_load_3d(sm + OFF_Q, tm_q, 0, nt0, (int)nbh, &ms.bar_qkz);
-            tc::tma_load_3d(sm + OFF_K, tm_k, 0, nt0, (int)nbh, &ms.bar_qkz);
-        }
         // (without a next item this fetches the current one again, unused)
         const GatePre gp = gate_fetch(nbh, nt0 / C);
         // ---------------------------------------------------------------- S: operands out | next gate
         if (kSplit && tid == 0) {
-            // [W^T | (Q Gamma)^T], U^T, K~ and M are final: out while every warp computes the
-            // next item's gate
+            // W^T, Q Gamma, U^T, K~ and M are final: out while every warp computes the next
+            // item's gate
             tc::tma_store_3d(tm_wq, sm + OFF_A1, 0, 0, 2 * it);
-            tc::tma_store_3d(tm_wq, sm + OFF_A1 + 16384, 0, 0, 2 * it + 1);
-            tc::tma_store_3d(tm_uu, sm + OFF_LVL + LV_UT, 0, 0, it);
+            tc::tma_store_3d(tm_qg, sm + OFF_LVL + LV_QG, 0, 0, 4 * it + 2);
+            tc::tma_store_3d(tm_qg, sm + OFF_LVL + LV_QG + 8192, 0, 0, 4 * it + 3);
+            tc::tma_store_3d(tm_uu, sm + OFF_S, 0, 0, it);
             tc::tma_store_3d(tm_kt, sm + OFF_V, 0, 0, it);
             tc::tma_store_3d(tm_kt, sm + OFF_V + 8192, 64, 0, it);
             tc::bulk_store(seg.mm + (size_t)it * kItemMM, sm + OFF_LVL + LV_MB, (uint32_t)kItemMM);
@@ -1148,7 +1135,7 @@ __device__ __forceinline__ void chunk_loop(const CUtensorMap* tm_q, const CUtens
             if (has_next && !gate_scan(nbh, nt0 / C, gp)) failed = true;
         // ---------------------------------------------------------------- S3: drain stores
             if (tid == 0) {
-                // the stores have read the v-tile slot, A1, U^T and M: refill / reuse them
+                // the stores have read the v-tile slot, A1, Q Gamma, U^T and M: refill / reuse them
                 tc::bulk_wait_read_all();
                 if (has_next) {
                     tc::mbar_arrive_expect_tx(&ms.bar_v, 16384u);
@@ -1158,12 +1145,16 @@ __device__ __forceinline__ void chunk_loop(const CUtensorMap* tm_q, const CUtens
         } else {
         // ---------------------------------------------------------------- C: carry | next gate
             if (group_c) {
-                // C1: D[v][t'] = sum_c S[c][v] A1[c][t']  -> (W S)^T for t' < 64, (QG S)^T above
+                // C1: D[v][t'] = sum_c S[c][v] W^T[c][t'] (t' < 64), sum_c S[c][v] QG[t'][c]
+                //     above; two MMAs of N = 64 per K step, the second with a K-major B
                 if (tid == 0) {
     #pragma unroll
-                    for (int ks = 0; ks < 8; ++ks)
-                        tc::mma_bf16(tmem + TM_D1, desc_mn(sb + OFF_S, 16384, ks),
-                                     desc_mn(sb + OFF_A1, 16384, ks), IDESC_SQ, ks > 0);
+                    for (int ks = 0; ks < 8; ++ks) {
+                        const uint64_t a = desc_mn(sb + OFF_S, 16384, ks);
+                        tc::mma_bf16(tmem + TM_D1, a, desc_mn(sb + OFF_A1, 16384, ks), IDESC_SW, ks > 0);
+                        tc::mma_bf16(tmem + TM_D1 + 64, a, desc_k(sb + OFF_LVL + LV_QG, 64, ks),
+                                     IDESC_SG, ks > 0);
+                    }
                     tc::mma_commit(&ms.bar_m0);
                 }
                 {
@@ -1310,7 +1301,7 @@ __global__ void __launch_bounds__(NT, 1)
                         const float* __restrict__ dt_bias, float scale,
                         const float* __restrict__ h0, __nv_bfloat16* __restrict__ out,
                         float* __restrict__ hT, FusedSched fs) {
-    chunk_loop<false>(&tm_q, &tm_k, &tm_v, &tm_z, nullptr, nullptr, nullptr, H, T, beta, A_log,
+    chunk_loop<false>(&tm_q, &tm_k, &tm_v, &tm_z, nullptr, nullptr, nullptr, nullptr, H, T, beta, A_log,
                       dt_bias, scale, h0, out, hT, PrepSeg{0, 1, 0, nullptr, nullptr}, fs);
 }
 
@@ -1322,11 +1313,12 @@ __global__ void __launch_bounds__(NT, 1)
                           const __grid_constant__ CUtensorMap tm_v,
                           const __grid_constant__ CUtensorMap tm_z,
                           const __grid_constant__ CUtensorMap tm_wq,
+                          const __grid_constant__ CUtensorMap tm_qg,
                           const __grid_constant__ CUtensorMap tm_uu,
                           const __grid_constant__ CUtensorMap tm_kt, int H, int T,
                           const __nv_bfloat16* __restrict__ beta, const float* __restrict__ A_log,
                           const float* __restrict__ dt_bias, PrepSeg seg) {
-    chunk_loop<true>(&tm_q, &tm_k, &tm_v, &tm_z, &tm_wq, &tm_uu, &tm_kt, H, T, beta, A_log,
+    chunk_loop<true>(&tm_q, &tm_k, &tm_v, &tm_z, &tm_wq, &tm_qg, &tm_uu, &tm_kt, H, T, beta, A_log,
                      dt_bias, 0.f, nullptr, nullptr, nullptr, seg,
                      FusedSched{0, 1, 0, nullptr, nullptr, nullptr});
 }
@@ -1475,6 +1467,7 @@ bool split_operands(uint8_t* p, size_t items_max, SplitOperands* o) {
     o->mm = kt + items_max * kItemKT;
     o->gl = reinterpret_cast<float*>(o->mm + items_max * kItemMM);
     return make_map3(&o->wq, wq, 64, 128, 2 * items_max, 128, 16384, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) &&
+           make_map3(&o->qg, wq, 64, 64, 4 * items_max, 128, 8192, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B) &&
            make_map3(&o->uu, uu, 64, 128, items_max, 128, 16384, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) &&
            make_map3(&o->kt, kt, 128, 64, items_max, 256, 16384, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B);
 }
@@ -1500,7 +1493,7 @@ cudaError_t run_chunk_split(const ChunkArgs& a, cudaStream_t s, void* scratch, s
     for (int n0 = 0; n0 < N; n0 += seg_len) {
         const int len = min(seg_len, N - n0), items = BH * len;
         kda_chunk_prep_kernel<<<min(items, nsm), NT, SMEM_BYTES, s>>>(
-            m[0], m[1], m[2], m[3], ops.wq, ops.uu, ops.kt, a.H, a.T, (const __nv_bfloat16*)a.beta,
+            m[0], m[1], m[2], m[3], ops.wq, ops.qg, ops.uu, ops.kt, a.H, a.T, (const __nv_bfloat16*)a.beta,
             a.A_log, a.dt_bias, PrepSeg{n0, len, items, ops.mm, ops.gl});
         count_launches(1);
         if ((err = cudaGetLastError()) != cudaSuccess) return err;
@@ -1577,7 +1570,7 @@ cudaError_t run_chunk_split_overlap(const ChunkArgs& a, cudaStream_t s, void* sc
         if (i >= 2) err = cudaStreamWaitEvent(s, ev[3 + b], 0);  // carry of segment i - 2 read buffer b
         if (err != cudaSuccess) break;
         kda_chunk_prep_kernel<<<min(items, prep_grid), NT, SMEM_BYTES, s>>>(
-            m[0], m[1], m[2], m[3], ops[b].wq, ops[b].uu, ops[b].kt, a.H, a.T,
+            m[0], m[1], m[2], m[3], ops[b].wq, ops[b].qg, ops[b].uu, ops[b].kt, a.H, a.T,
             (const __nv_bfloat16*)a.beta, a.A_log, a.dt_bias,
             PrepSeg{n0, len, items, ops[b].mm, ops[b].gl});
         count_launches(1);
@@ -1804,7 +1797,7 @@ cudaError_t run_chunk_split_scan(const ChunkArgs& a, cudaStream_t s, void* scrat
     for (int n0 = 0; n0 < N; n0 += seg_len) {
         const int len = std::min(seg_len, N - n0), items = BH * len;
         kda_chunk_prep_kernel<<<std::min(items, nsm), NT, SMEM_BYTES, s>>>(
-            m[0], m[1], m[2], m[3], ops.wq, ops.uu, ops.kt, a.H, a.T, (const __nv_bfloat16*)a.beta,
+            m[0], m[1], m[2], m[3], ops.wq, ops.qg, ops.uu, ops.kt, a.H, a.T, (const __nv_bfloat16*)a.beta,
             a.A_log, a.dt_bias, PrepSeg{n0, len, items, ops.mm, ops.gl});
         count_launches(1);
         if ((err = cudaGetLastError()) != cudaSuccess) return err;

@@ -15,8 +15,9 @@ namespace tile {
 constexpr int C = 64, KD = 128, VD = 128;
 
 // Bytes of the per-chunk operands the chunk-parallel prep kernel hands to the carry kernel:
-// [W^T | (Q Gamma)^T] (2 x 128 x 64 bf16), U^T (128 x 64 bf16), K~ (64 x 128 bf16), M (64 x 64
-// bf16, the masked Q K products of the output) and Gamma_last (128 fp32).
+// W^T (128 x 64 bf16, MN-major) and Q Gamma (64 x 128 bf16, K-major), U^T (128 x 64 bf16),
+// K~ (64 x 128 bf16), M (64 x 64 bf16, the masked Q K products of the output) and Gamma_last
+// (128 fp32).
 constexpr size_t kItemWQ = 2u * 128u * 64u * 2u;
 constexpr size_t kItemUU = 128u * 64u * 2u;
 constexpr size_t kItemKT = 64u * 128u * 2u;
@@ -123,11 +124,12 @@ __device__ __forceinline__ uint32_t taddr(uint32_t base, int warp, uint32_t col)
 
 // Host side of the split forward's carry kernel (chunk_carry.cu).  SplitOperands: where the
 // prep kernel left a segment's per-chunk operands (item = bh * seg_len + chunk of the
-// segment): tile maps of [W^T | (Q Gamma)^T] (z = 2 item, 2 item + 1), U^T (z = item) and K~
-// (z = item), and the M tiles (mm + kItemMM item, the bytes of the shared-memory tile) and
-// Gamma_last (gl + 128 item) as plain arrays.
+// segment): tile maps of W^T (z = 2 item) and, over the same array, of Q Gamma's two 64-channel
+// atoms (z = 4 item + 2, 4 item + 3), of U^T (z = item) and K~ (z = item), and the M tiles
+// (mm + kItemMM item, the bytes of the shared-memory tile) and Gamma_last (gl + 128 item) as
+// plain arrays.
 struct SplitOperands {
-    CUtensorMap wq, uu, kt;
+    CUtensorMap wq, qg, uu, kt;
     uint8_t* mm;
     float* gl;
 };
