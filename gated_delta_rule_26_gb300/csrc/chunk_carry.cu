@@ -203,16 +203,21 @@ __global__ void __launch_bounds__(NT2, 1)
         // stage s ^ 1 was consumed by the previous chunk: refill it two chunks ahead of that one
         // (a thread of warp 1, so that thread 0 issues C1 at once)
         if (tid == 32 && j >= j0 + 1 && j + 1 < j1) issue(j + 1, s ^ 1);
-        // C1: D[v][t'] = sum_c S[c][v] W^T[c][t'] (t' < 64), sum_c S[c][v] QG[t'][c] above
+        // C1: D[v][t'] = sum_c S[c][v] W^T[c][t'] (t' < 64) under its own commit (Delta waits
+        // for it), then sum_c S[c][v] QG[t'][c] above, which runs beside Delta (only the plain
+        // role writes o; M Delta's commit covers it)
         if (tid == 0) {
 #pragma unroll
-            for (int ks = 0; ks < 8; ++ks) {
-                const uint64_t a = desc_mn(sb + K2_S, 16384, ks);
-                tc::mma_bf16(tmem + TM_D2, a, desc_mn(stb + ST_WQ, 16384, ks), IDESC_SW2, ks > 0);
-                tc::mma_bf16(tmem + TM_D2 + 64, a, desc_k(stb + ST_WQ + 16384, 64, ks), IDESC_SG2,
-                             ks > 0);
-            }
+            for (int ks = 0; ks < 8; ++ks)
+                tc::mma_bf16(tmem + TM_D2, desc_mn(sb + K2_S, 16384, ks),
+                             desc_mn(stb + ST_WQ, 16384, ks), IDESC_SW2, ks > 0);
             tc::mma_commit(&ms.bar_mma);
+            if (write_o) {
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks)
+                    tc::mma_bf16(tmem + TM_D2 + 64, desc_mn(sb + K2_S, 16384, ks),
+                                 desc_k(stb + ST_WQ + 16384, 64, ks), IDESC_SG2, ks > 0);
+            }
         }
         // meanwhile: S <- diag(Gamma_last) S in TMEM (row c, this warp's 32 columns)
         {

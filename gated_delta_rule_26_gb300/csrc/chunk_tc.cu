@@ -1053,6 +1053,7 @@ __device__ __forceinline__ void chunk_loop(const CUtensorMap* tm_q, const CUtens
             tc::tmem_st16(taddr(tmem, warp, TM_S + v0), d0);
             tc::tmem_st16(taddr(tmem, warp, TM_S + v0 + 16), d1);
             tc::tmem_st_wait();
+            tc::fence_proxy_async_smem();  // the copy is read by C1's first half after the wait
             s_pend = false;
         }
         // and, in the prep kernel, K~ = K e^{G_last - G} -> the v-tile slot (MN-major [t][c])
@@ -1071,6 +1072,15 @@ __device__ __forceinline__ void chunk_loop(const CUtensorMap* tm_q, const CUtens
         }
         KDA_WAIT(bar_m0, ph0);
         if (failed) break;
+        // (fused kernel) the state's bf16 copy and Q Gamma are in place: the Q Gamma half of C1
+        // now, under the W^T extraction (the carry window's C1 commit covers it; the previous
+        // chunk's output has left those TMEM columns during the substitution)
+        if (!kSplit && tid == 0) {
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks)
+                tc::mma_bf16(tmem + TM_D1 + 64, desc_mn(sb + OFF_S, 16384, ks),
+                             desc_k(sb + OFF_LVL + LV_QG, 64, ks), IDESC_SG, ks > 0);
+        }
         // prep kernel: q and k are free: request the next chunk's q, k and z (on one barrier)
         if (kSplit && tid == 0 && has_next) {
             tc::mbar_arrive_expect_tx(&ms.bar_qkz, 3u * 16384u);
@@ -1149,13 +1159,10 @@ __device__ __forceinline__ void chunk_loop(const CUtensorMap* tm_q, const CUtens
                 //     above; two MMAs of N = 64 per K step, the second with a K-major B
                 if (tid == 0) {
     #pragma unroll
-                    for (int ks = 0; ks < 8; ++ks) {
-                        const uint64_t a = desc_mn(sb + OFF_S, 16384, ks);
-                        tc::mma_bf16(tmem + TM_D1, a, desc_mn(sb + OFF_A1, 16384, ks), IDESC_SW, ks > 0);
-                        tc::mma_bf16(tmem + TM_D1 + 64, a, desc_k(sb + OFF_LVL + LV_QG, 64, ks),
-                                     IDESC_SG, ks > 0);
-                    }
-                    tc::mma_commit(&ms.bar_m0);
+                    for (int ks = 0; ks < 8; ++ks)
+                        tc::mma_bf16(tmem + TM_D1, desc_mn(sb + OFF_S, 16384, ks),
+                                     desc_mn(sb + OFF_A1, 16384, ks), IDESC_SW, ks > 0);
+                    tc::mma_commit(&ms.bar_m0);  // (the Q Gamma half went out after the W/U GEMM)
                 }
                 {
                     const bool ok = tid != 0 || tc::mbar_wait(&ms.bar_m0, ph0);
